@@ -1,0 +1,58 @@
+"""The fp64 oracle against results fixed by mathematics (CPU only)."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import oracle_pins as pins
+
+
+@pytest.mark.parametrize("pin", pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(oracle.ssd_recurrence)
+
+
+@pytest.mark.parametrize("Q", [1, 4, 16, 32])
+def test_stage_definitions_match_chunked_algorithm(Q):
+    """The per-stage oracle intermediates (cumulative decay, chunk-local
+    states, states entering each chunk) equal the stage values of the chunked
+    algorithm written out independently in oracle_pins.chunked_form."""
+    x, dt, A, B, C, D, s0 = pins.small_problem(21, b=2, L=64, H=4, P=3, N=5, G=2)
+    _, fin, cums, locs, ins = pins.chunked_form(x, dt, A, B, C, D, s0, Q)
+    nc = 64 // Q
+    cum = oracle.chunk_cumsum(dt, A, Q)
+    st = oracle.chunk_states(x, dt, A, B, Q)
+    sin, f2 = oracle.states_entering(x, dt, A, B, C, Q, s0)
+    assert cum.shape == (2, 4, nc, Q) and st.shape == (2, nc, 4, 3, 5) and sin.shape == st.shape
+    for b in range(2):
+        for h in range(4):
+            for c in range(nc):
+                pins._close(cum[b, h, c], cums[b, h, c], what="cumsum")
+                pins._close(st[b, c, h], locs[b, h, c], what="chunk state")
+                pins._close(sin[b, c, h], ins[b, h, c], what="state entering chunk")
+    pins._close(f2, fin, what="final")
+
+
+def test_snapshots_of_zero_input_are_pure_decay():
+    """With x = 0 the state entering chunk c is exp(sum of all earlier dt*A)
+    times the initial state: ties the cumulative decay to the recurrence."""
+    x, dt, A, B, C, D, s0 = pins.small_problem(22, b=1, L=48, H=2, P=2, N=3, G=1)
+    sin, _ = oracle.states_entering(np.zeros_like(x), dt, A, B, C, 16, s0)
+    cum = oracle.chunk_cumsum(dt, A, 16)                 # [1, H, 3, 16]
+    total = np.concatenate([np.zeros((1, 2, 1)), np.cumsum(cum[:, :, :, -1], axis=2)[:, :, :-1]], axis=2)
+    for c in range(3):
+        want = np.exp(total[0, :, c])[:, None, None] * s0[0]
+        pins._close(sin[0, c], want, what=f"pure decay chunk {c}")
+
+
+def test_empty_sequence():
+    x = np.zeros((1, 0, 2, 3))
+    y, f = oracle.ssd_recurrence(x, np.zeros((1, 0, 2)), -np.ones(2), np.zeros((1, 0, 1, 4)),
+                                 np.zeros((1, 0, 1, 4)), np.ones(2), np.ones((1, 2, 3, 4)))
+    assert y.shape == (1, 0, 2, 3)
+    assert np.array_equal(f, np.ones((1, 2, 3, 4)))
+
+
+def test_rejects_bad_groups():
+    with pytest.raises(ValueError):
+        oracle.ssd_recurrence(np.zeros((1, 4, 3, 2)), np.zeros((1, 4, 3)), -np.ones(3),
+                              np.zeros((1, 4, 2, 2)), np.zeros((1, 4, 2, 2)))
