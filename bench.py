@@ -1,0 +1,491 @@
+"""Benchmark of the fused SSD forward (ssd_fwd) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one ssd_fwd call (the whole chunked forward: cumulative decay,
+chunk states, state passing, chunk outputs) over one batch of the Mamba-2
+130M-shaped layer workload: batch 4, L 2048, H 24, P 64, N 128, G 1, Q 64,
+bf16 inputs, fp32 state / accumulation / y.  Inputs are seeded synthetic
+tensors (ssd_inputs.py), resident in HBM before timing starts; L2 (129 MB,
+larger than this workload's 58 MB) is flushed by a 512 MB write between
+timed steps, outside the timed events.
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun) give every rank
+its own independent batch: weak scaling, no data-path collective.
+--impl reference times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import ssd_inputs as si  # noqa: E402
+
+WORKLOAD = "mamba2_130m"
+FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------------------
+# byte / flop models (algorithmic, per call)
+# ---------------------------------------------------------------------------
+def elem_bytes(dtype):
+    return 4 if dtype == "f32" else 2
+
+
+def compulsory_bytes(cfg, y_bytes=4):
+    """Reads of x, dt, B, C, A, D (+ init) and writes of y and final state."""
+    b, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
+    e = elem_bytes(cfg.dtype)
+    rd = b * L * H * P * e + b * L * H * e + 2 * b * L * G * N * e + 2 * H * 4
+    if cfg.has_init:
+        rd += b * H * P * N * 4
+    wr = b * L * H * P * y_bytes + b * H * P * N * 4
+    return rd + wr
+
+
+def chunked_flops(cfg):
+    """Tensor-core flops of the chunked algorithm with full Q x Q tiles:
+    per token H (4PN + 2QP) + G 2QN, plus the state pass 2PN H / Q."""
+    H, P, N, G, Q = cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups, cfg.chunk_size
+    per_tok = H * (4 * P * N + 2 * Q * P) + G * 2 * Q * N + H * 2 * P * N / Q
+    return per_tok * cfg.tokens
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+
+        def find(keys):
+            for k in keys:
+                for kk, v in pk.items():
+                    if kk.lower() == k and isinstance(v, (int, float)):
+                        return float(v)
+            return None
+        hbm = find(["hbm_gbs", "hbm_gb_s", "hbm_bandwidth_gbs"])
+        tf = find(["bf16_tflops", "bf16_dense_tflops"])
+        tfs = find(["bf16_tflops_sustained"])
+        if hbm:
+            return {"hbm_gbs": hbm, "bf16_tflops": tf or FALLBACK_BF16_TFLOPS,
+                    "bf16_tflops_sustained": tfs, "source": "measured"}
+    except (OSError, ValueError):
+        pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampler (nvidia-smi during the timed region)
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# ncu traffic recorded under profiles/ (null when the kernel source changed)
+# ---------------------------------------------------------------------------
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "state_space_model_fwd_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    path = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_sha():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def run_reference(args):
+    """The fp64 CPU oracle timed on this host's cores: each step runs the
+    recurrence over a bounded sample of heads of the workload, scaled to
+    tokens/s of the whole workload by the fraction of heads sampled."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    cfg = si.CONFIGS[args.workload]
+    inp = si.make_inputs(cfg)
+    f = inp.as_f64()
+    nh = max(1, min(cfg.nheads, args.ref_heads))
+    g_of = [h * cfg.ngroups // cfg.nheads for h in range(nh)]
+    sl = dict(x=f["x"][:, :, :nh], dt=f["dt"][:, :, :nh], A=f["A"][:nh], D=f["D"][:nh],
+              init=None if f["init_state"] is None else f["init_state"][:, :nh])
+    Bs = f["B"][:, :, g_of]
+    Cs = f["C"][:, :, g_of]
+
+    def step():
+        oracle.ssd_recurrence(sl["x"], sl["dt"], sl["A"], Bs, Cs, sl["D"], sl["init"])
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times) * cfg.nheads / nh
+    value = cfg.tokens / t
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": "ssd_fwd_tokens_per_s", "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": cfg.name, "batch": cfg.batch, "seqlen": cfg.seqlen,
+                                        "nheads": cfg.nheads, "headdim": cfg.headdim, "dstate": cfg.dstate,
+                                        "ngroups": cfg.ngroups, "chunk_size": cfg.chunk_size},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"fp64 recurrence over {nh} of {cfg.nheads} heads, all batches and steps, "
+                                   f"scaled by {cfg.nheads}/{nh}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(cfg, inp, budget_s=20.0):
+    """Oracle time on this host for a bounded sample of heads, scaled."""
+    import oracle
+    oracle.build()
+    f = inp.as_f64()
+    nh = 1
+    t_one = None
+    while True:
+        g_of = [h * cfg.ngroups // cfg.nheads for h in range(nh)]
+        t0 = time.perf_counter()
+        oracle.ssd_recurrence(f["x"][:, :, :nh], f["dt"][:, :, :nh], f["A"][:nh], f["B"][:, :, g_of],
+                              f["C"][:, :, g_of], f["D"][:nh],
+                              None if f["init_state"] is None else f["init_state"][:, :nh])
+        t_one = time.perf_counter() - t0
+        if t_one * 4 > budget_s or nh == cfg.nheads:
+            break
+        nh = min(cfg.nheads, nh * 4)
+    t_full = t_one * cfg.nheads / nh
+    return {"value": cfg.tokens / t_full, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fp64 recurrence over {nh} of {cfg.nheads} heads (all batches, all {cfg.seqlen} steps), "
+                      f"{t_one:.2f} s, scaled by {cfg.nheads}/{nh}"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(si.CONFIGS))
+    ap.add_argument("--ref-heads", type=int, default=4)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import state_space_model_fwd_gb300 as ssd
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+
+    cfg = si.CONFIGS[args.workload]
+    cfg_rank = cfg.replace(seed=cfg.seed + 7919 * rank)
+    inp = si.make_inputs(cfg_rank)
+    t = inp.to_torch(dev)
+    y = torch.empty(t["x"].shape, device=dev, dtype=torch.float32)
+    fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), device=dev, dtype=torch.float32)
+    ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], cfg.chunk_size))),
+                     device=dev, dtype=torch.uint8)
+    flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"], cfg.chunk_size,
+                    y=y, final_state=fin, workspace=ws)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        wall0 = time.perf_counter()
+        for s, e in evs:
+            flush.zero_()
+            s.record(stream)
+            step()
+            e.record(stream)
+        barrier()
+        wall = time.perf_counter() - wall0
+    step_ms = [s.elapsed_time(e) for s, e in evs]
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        tm = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tm.item())
+    launches_per_step = None
+
+    # per-launch device times (separate pass, events between the launches)
+    ssd.launch_timing(True)
+    per_launch = []
+    for _ in range(max(5, args.steps // 2)):
+        flush.zero_()
+        step()
+        per_launch.append(ssd.launch_times_ms())
+    ssd.launch_timing(False)
+    launches_per_step = len(per_launch[-1])
+    kernel_names = [name for name, _ in per_launch[-1]]
+    launch_ms = [statistics.mean(p[i][1] for p in per_launch) for i in range(launches_per_step)]
+    dom = int(np.argmax(launch_ms))
+
+    peaks = load_peaks()
+    cbytes = compulsory_bytes(cfg, 4)
+    dom_name = kernel_names[dom] if dom < len(kernel_names) else f"launch{dom}"
+    dom_bytes = KERNEL_BYTES(cfg, dom_name)
+    achieved = dom_bytes / (launch_ms[dom] * 1e-3) / 1e9
+    tokens = cfg.tokens
+    value = world * tokens / (ms * 1e-3)
+
+    # end-to-end through the C ABI with host buffers: H2D inputs, call, D2H outputs
+    h = inp.to_torch("cpu", pin_memory=True)
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    dbufs = {k: torch.empty_like(v, device=dev) for k, v in h.items() if v is not None}
+    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
+    d2h = y_h.numel() * y_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def e2e_step():
+        for k, v in dbufs.items():
+            v.copy_(h[k], non_blocking=True)
+        ssd.ssd_fwd(dbufs["x"], dbufs["dt"], dbufs["A"], dbufs["B"], dbufs["C"], dbufs["D"],
+                    dbufs.get("init_state"), cfg.chunk_size, y=y, final_state=fin, workspace=ws)
+        y_h.copy_(y, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        tm = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tm.item())
+
+    sweep = {}
+    if not args.no_sweep and rank == 0:
+        sweep = run_sweep(ssd, dev, flush, peaks)
+
+    if rank == 0:
+        clocks = clk.summary()
+        traffic = recorded_traffic(dom_name, cfg.name)
+        line = {
+            "metric": "ssd_fwd_tokens_per_s", "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": cfg.batch, "seqlen": cfg.seqlen, "nheads": cfg.nheads,
+                       "headdim": cfg.headdim, "dstate": cfg.dstate, "ngroups": cfg.ngroups,
+                       "chunk_size": cfg.chunk_size, "state_dtype": "f32", "y_dtype": "f32",
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": "flushed between timed steps (512 MB write, outside the step events)"},
+            "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps,
+            "launches_per_step": launches_per_step,
+            "launch_ms": {kernel_names[i] if i < len(kernel_names) else f"launch{i}": round(v, 5)
+                          for i, v in enumerate(launch_ms)},
+            "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes": dom_bytes, "peak_source": peaks["source"]},
+            "op_roofline": {"compulsory_bytes": cbytes, "flops": chunked_flops(cfg),
+                            "achieved_gbs": cbytes / (ms * 1e-3) / 1e9,
+                            "frac_hbm": cbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                            "achieved_tflops": chunked_flops(cfg) / (ms * 1e-3) / 1e12},
+            "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "wall_s_timed_region": wall,
+            "sm_count": nsm,
+            "sweep": sweep,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(cfg, inp)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def KERNEL_BYTES(cfg, name):
+    """Algorithmic bytes one launch of the named kernel must move."""
+    b, L, H, P, N, G, Q = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups, cfg.chunk_size
+    e = elem_bytes(cfg.dtype)
+    nc = L // Q
+    x = b * L * H * P * e
+    dt = b * L * H * e
+    bc = b * L * G * N * e
+    st = b * nc * H * P * N * 4
+    cum = b * H * L * 4
+    y = b * L * H * P * 4
+    init = b * H * P * N * 4 if cfg.has_init else 0
+    fin = b * H * P * N * 4
+    return {
+        "chunk_cumsum": dt + cum,
+        "chunk_state_simt": x + dt + bc + cum + st,
+        "state_passing": st + cum + init + st + fin,
+        "chunk_scan_simt": x + dt + 2 * bc + cum + st + y,
+    }.get(name, compulsory_bytes(cfg))
+
+
+def run_sweep(ssd, dev, flush, peaks, steps=10):
+    """Device-timed ssd_fwd on the other workloads, plus the sequential scan on
+    the 16K-token one (the chunked-versus-sequential comparison)."""
+    import torch
+    out = {}
+    for name in ("mamba2_2p7b", "long_16k", "wide_head", "wide_head_q128"):
+        cfg = si.CONFIGS[name]
+        inp = si.make_inputs(cfg)
+        t = inp.to_torch(dev)
+        y = torch.empty(t["x"].shape, device=dev, dtype=torch.float32)
+        fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), device=dev, dtype=torch.float32)
+        ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], cfg.chunk_size))),
+                         device=dev, dtype=torch.uint8)
+
+        def run():
+            ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"], cfg.chunk_size,
+                        y=y, final_state=fin, workspace=ws)
+
+        ms = time_device(run, flush, steps)
+        cb = compulsory_bytes(cfg, 4)
+        rec = {"tokens_per_s": cfg.tokens / (ms * 1e-3), "ms": ms,
+               "frac_hbm": cb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+               "tflops": chunked_flops(cfg) / (ms * 1e-3) / 1e12}
+        if name == "long_16k":
+            def scan():
+                ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
+                                       y=y, final_state=fin)
+            sms = time_device(scan, flush, 3)
+            rec["selective_scan_ms"] = sms
+            rec["chunked_vs_sequential_speedup"] = sms / ms
+        out[name] = rec
+        del t, y, fin, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def time_device(fn, flush, steps):
+    import torch
+    for _ in range(3):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        ts.append(s.elapsed_time(e))
+    return statistics.mean(ts)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * ssd.h -- C ABI of libssd: the Mamba-2 state-space-duality (SSD) chunked
+ * forward pass on NVIDIA GB300 (sm_103a).
+ *
+ * The operation (one scalar decay per head, "Why SSM and linear-RNN FLOPs do
+ * not convert into GPU FLOPs", paragraph 1):
+ *
+ *     h_t = exp(dt_t * A_h) * h_{t-1} + dt_t * x_t B_t^T      h_t in R^{P x N}
+ *     y_t = h_t C_t + D_h * x_t
+ *
+ * computed chunk-wise ("Mamba-2 in NVIDIA cuTile: Faster Forward Kernels",
+ * section "Why Mamba-2 is a useful kernel example": one kernel prepares the
+ * cumulative decay values, another the state entering each chunk, a third
+ * the outputs, with the intra-chunk interactions kept on-chip).  The
+ * quadratic-inside / linear-across split with chunk size Q follows the
+ * da_be19 thread, post 5/6.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Shapes use the names of the pages' notation:
+ *   b = batch, L = seqlen, H = nheads, P = headdim, N = dstate,
+ *   G = ngroups (heads h = g*H/G .. (g+1)*H/G - 1 share B and C),
+ *   Q = chunk_size, nc = L / Q.
+ * Tensor layouts (row-major, contiguous, element type in brackets; "T" is
+ * fp32 or bf16 as given by ssd_shape_t.dtype):
+ *   x          [b, L, H, P]       T
+ *   dt         [b, L, H]          T   (already positive: no softplus/bias here)
+ *   A          [H]                fp32 (negative)
+ *   B, C       [b, L, G, N]       T
+ *   D          [H]                fp32 (skip term; NULL = no skip)
+ *   init_state [b, H, P, N]       fp32 (NULL = zero initial state)
+ *   y          [b, L, H, P]       ydtype (fp32, or the input dtype)
+ *   final_state[b, H, P, N]       fp32 (NULL = not written)
+ *   dA_cumsum  [b, H, nc, Q]      fp32 inclusive cumsum of dt*A inside a chunk
+ *   states     [b, nc, H, P, N]   fp32 state each chunk produces from zero
+ *   states_in  [b, nc, H, P, N]   fp32 state entering each chunk
+ * Ownership: every pointer is caller-owned device memory (x, y, ... may come
+ * from any allocator); the library allocates nothing and keeps no pointer
+ * after a call returns.  Every pointer must be 16-byte aligned.
+ * Execution: calls are asynchronous on `stream` (0 = legacy default stream).
+ * Errors: argument errors are detected on the host and returned before
+ * anything is enqueued (SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED);
+ * a failed launch returns SSD_ERR_CUDA.  No entry point synchronises.
+ * Supported on the GPU: chunk_size 64 or 128, L % chunk_size == 0,
+ * H % G == 0, P in {16, 32, 64, 128}, N in {16, 32, 64, 128, 256}.
+ * Outputs are bitwise reproducible run to run: no floating-point atomics.
+ */
+#ifndef SSD_H_
+#define SSD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define SSD_API __attribute__((visibility("default")))
+#else
+#define SSD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misaligned pointer */
+    SSD_ERR_UNSUPPORTED = 2,   /* valid shape this build does not run */
+    SSD_ERR_CUDA = 3,          /* a CUDA launch or query failed */
+    SSD_ERR_WORKSPACE = 4      /* workspace missing or smaller than required */
+} ssd_status_t;
+
+typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype_t;
+
+/*
+ * Problem description.  `dtype` is the element type of x, dt, B, C.
+ * `ydtype` is the element type of y: SSD_DTYPE_F32 (the default of a
+ * zero-initialised struct; y keeps the fp32 accumulator's precision) or the
+ * input dtype (bf16 y: half the output bytes, plus bf16 output rounding of at
+ * most 2^-9 relative).
+ */
+typedef struct {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk_size;
+    ssd_dtype_t dtype;
+    ssd_dtype_t ydtype;
+} ssd_shape_t;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+SSD_API const char *ssd_status_string(ssd_status_t status);
+
+/* Version of this ABI: (major << 16) | minor. */
+SSD_API int ssd_abi_version(void);
+
+/*
+ * Bytes of device workspace ssd_fwd needs for `shape` (0 for an invalid
+ * shape).  The workspace holds the per-segment states of the two-pass
+ * chunk scan; it needs no initialisation and may be reused by later calls
+ * on the same stream.
+ */
+SSD_API size_t ssd_fwd_workspace_size(const ssd_shape_t *shape);
+
+/*
+ * Fused SSD forward: y and final_state from x, dt, A, B, C, D, init_state.
+ * The whole chunked algorithm -- cumulative decay, chunk states, the pass of
+ * states between chunks, chunk outputs -- runs on the GPU with the state and
+ * the intra-chunk score matrix kept on-chip; only per-segment states touch
+ * the workspace.  `workspace` must hold ssd_fwd_workspace_size(shape) bytes
+ * (SSD_ERR_WORKSPACE otherwise).  D, init_state, final_state may be NULL.
+ */
+SSD_API ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void *dt,
+                     const float *A, const void *B, const void *C,
+                     const float *D, const float *init_state, void *y,
+                     float *final_state, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/*
+ * Stage 1: dA_cumsum[b,h,c,q] = sum_{k<=q} dt[b, c*Q+k, h] * A[h].
+ * ("Mamba-2 in NVIDIA cuTile", section "Why Mamba-2 is a useful kernel
+ * example": the kernel that prepares the cumulative decay values.)
+ */
+SSD_API ssd_status_t ssd_chunk_cumsum(const ssd_shape_t *shape, const void *dt,
+                              const float *A, float *dA_cumsum,
+                              cudaStream_t stream);
+
+/*
+ * Stage 2: states[b,c,h,p,n] = sum_q exp(cum[Q-1] - cum[q]) * dt_q *
+ *          x[b, cQ+q, h, p] * B[b, cQ+q, g(h), n]   (cum = dA_cumsum[b,h,c,:]),
+ * the state chunk c produces from a zero start: a decay-weighted x^T B
+ * contraction per chunk (the BMMs for state accumulation of the da_be19
+ * thread, post 5/6).
+ */
+SSD_API ssd_status_t ssd_chunk_state(const ssd_shape_t *shape, const void *x,
+                             const void *dt, const void *B,
+                             const float *dA_cumsum, float *states,
+                             cudaStream_t stream);
+
+/*
+ * Stage 3: states_in[b,0] = init_state (zeros when NULL);
+ *          states_in[b,c+1] = exp(dA_cumsum[b,h,c,Q-1]) * states_in[b,c] + states[b,c];
+ *          final_state = the value after the last chunk (if non-NULL).
+ * ("Mamba-2 in NVIDIA cuTile", the kernel that calculates the state
+ * entering each chunk.)
+ */
+SSD_API ssd_status_t ssd_state_passing(const ssd_shape_t *shape, const float *states,
+                               const float *dA_cumsum, const float *init_state,
+                               float *states_in, float *final_state,
+                               cudaStream_t stream);
+
+/*
+ * Stage 4: for t in chunk c (cum = dA_cumsum[b,h,c,:], i = t - cQ):
+ *   y[b,t,h,:] = sum_{j<=i} (C_t . B_j) exp(cum_i - cum_j) dt_j x_j
+ *              + exp(cum_i) * states_in[b,c,h] C_t + D[h] x_t
+ * The masked intra-chunk score matrix stays on-chip ("Mamba-2 in NVIDIA
+ * cuTile", the output kernel whose intermediate interactions stay in
+ * registers).  D may be NULL.
+ */
+SSD_API ssd_status_t ssd_chunk_scan(const ssd_shape_t *shape, const void *x,
+                            const void *dt, const void *B, const void *C,
+                            const float *dA_cumsum, const float *states_in,
+                            const float *D, void *y, cudaStream_t stream);
+
+/*
+ * The same recurrence as ssd_fwd, evaluated as a plain sequential scan over
+ * t on the fp32 ALUs (no tensor cores): the schedule the scan-versus-matmul
+ * comparison of "Why SSM and linear-RNN FLOPs do not convert into GPU
+ * FLOPs", paragraph 1, measures.  Same arguments and layouts as ssd_fwd,
+ * no workspace.  Requires only H % G == 0 (any L, any chunk_size field).
+ */
+SSD_API ssd_status_t selective_scan_fwd(const ssd_shape_t *shape, const void *x,
+                                const void *dt, const float *A, const void *B,
+                                const void *C, const float *D,
+                                const float *init_state, void *y,
+                                float *final_state, cudaStream_t stream);
+
+/*
+ * Launch timing (instrumentation; the pages have no counterpart).  While
+ * enabled, every entry point records a CUDA event on its stream before each
+ * kernel it launches and one after the last, so a caller can read the device
+ * time of each launch of the most recent call.  Disabled by default; the
+ * events cost a few microseconds of host time per launch.
+ *   ssd_launch_timing_enable(1) creates the events (SSD_ERR_CUDA on failure),
+ *   ssd_launch_timing_enable(0) destroys them.
+ *   ssd_launch_timing_read(ms, cap) waits for the last call's events, writes
+ *   up to `cap` per-launch durations in milliseconds and returns the number
+ *   of launches of that call (-1 if timing is off or no call was recorded).
+ *   ssd_launch_timing_name(i) names the kernel of launch i of that call
+ *   (static storage; NULL when out of range).
+ * Not thread-safe: one host thread should drive a timed sequence of calls.
+ */
+SSD_API ssd_status_t ssd_launch_timing_enable(int enable);
+SSD_API int ssd_launch_timing_read(float *ms, int cap);
+SSD_API const char *ssd_launch_timing_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSD_H_ */

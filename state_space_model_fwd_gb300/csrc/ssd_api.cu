@@ -1,0 +1,299 @@
+// ssd_api.cu -- the extern "C" entry points of libssd: argument validation
+// on the host, then kernel launches on the caller's stream.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ssd.h"
+#include "ssd_common.cuh"
+#include "ssd_tc.cuh"
+
+namespace {
+
+using ssd::bf16;
+using ssd::Dims;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2_in(int64_t v, int64_t lo, int64_t hi) {
+    return v >= lo && v <= hi && (v & (v - 1)) == 0;
+}
+
+// Shape checks shared by every entry point.  `need_chunks` adds the chunked
+// algorithm's restrictions (Q in {64, 128}, L % Q == 0).
+ssd_status_t check_shape(const ssd_shape_t *s, bool need_chunks, Dims *d) {
+    if (!s) return SSD_ERR_INVALID_ARG;
+    if (s->batch < 0 || s->seqlen < 0 || s->nheads <= 0 || s->headdim <= 0 || s->dstate <= 0 ||
+        s->ngroups <= 0)
+        return SSD_ERR_INVALID_ARG;
+    if (s->dtype != SSD_DTYPE_F32 && s->dtype != SSD_DTYPE_BF16) return SSD_ERR_INVALID_ARG;
+    if (s->ydtype != SSD_DTYPE_F32 && s->ydtype != s->dtype) return SSD_ERR_INVALID_ARG;
+    if (s->nheads % s->ngroups != 0) return SSD_ERR_INVALID_ARG;
+    if (!pow2_in(s->headdim, 16, 128) || !pow2_in(s->dstate, 16, 256)) return SSD_ERR_UNSUPPORTED;
+    if (need_chunks) {
+        if (s->chunk_size <= 0) return SSD_ERR_INVALID_ARG;
+        if (s->chunk_size != 64 && s->chunk_size != 128) return SSD_ERR_UNSUPPORTED;
+        if (s->seqlen % s->chunk_size != 0) return SSD_ERR_UNSUPPORTED;
+    }
+    // every index is formed in int64; keep each grid dimension in range
+    if (s->batch > 65535 || s->nheads > 65535) return SSD_ERR_UNSUPPORTED;
+    d->b = s->batch;
+    d->L = s->seqlen;
+    d->H = s->nheads;
+    d->P = s->headdim;
+    d->N = s->dstate;
+    d->G = s->ngroups;
+    d->Q = need_chunks ? s->chunk_size : 64;
+    d->nc = need_chunks ? s->seqlen / s->chunk_size : 0;
+    d->hpg = (int)(s->nheads / s->ngroups);
+    return SSD_OK;
+}
+
+bool ptrs_ok(std::initializer_list<const void *> required, std::initializer_list<const void *> optional) {
+    for (const void *p : required)
+        if (!p || !aligned16(p)) return false;
+    for (const void *p : optional)
+        if (p && !aligned16(p)) return false;
+    return true;
+}
+
+ssd_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Workspace of the unfused (four-launch) path: cumsum, chunk states,
+// states entering chunks.
+size_t staged_workspace(const Dims &d) {
+    return align256(sizeof(float) * d.b * d.H * d.L) + 2 * align256(sizeof(float) * d.b * d.nc * d.H * d.P * d.N);
+}
+
+template <typename T, typename TY>
+ssd_status_t fwd_staged(const Dims &d, const void *x, const void *dt, const float *A, const void *B,
+                        const void *C, const float *D, const float *init, void *y, float *fin, void *ws,
+                        cudaStream_t s) {
+    char *w = static_cast<char *>(ws);
+    float *cum = reinterpret_cast<float *>(w);
+    float *states = reinterpret_cast<float *>(w + align256(sizeof(float) * d.b * d.H * d.L));
+    float *states_in =
+        reinterpret_cast<float *>(w + align256(sizeof(float) * d.b * d.H * d.L) +
+                                  align256(sizeof(float) * d.b * d.nc * d.H * d.P * d.N));
+    const T *xt = static_cast<const T *>(x), *dtt = static_cast<const T *>(dt);
+    const T *Bt = static_cast<const T *>(B), *Ct = static_cast<const T *>(C);
+    ssd::timing_begin(s);
+    cudaError_t e = ssd::launch_chunk_cumsum<T>(d, dtt, A, cum, s);
+    ssd::timing_mark(s, "chunk_cumsum");
+    if (e == cudaSuccess) e = ssd::launch_chunk_state_simt<T>(d, xt, dtt, Bt, cum, states, s);
+    ssd::timing_mark(s, "chunk_state_simt");
+    if (e == cudaSuccess) e = ssd::launch_state_passing(d, states, cum, init, states_in, fin, s);
+    ssd::timing_mark(s, "state_passing");
+    if (e == cudaSuccess)
+        e = ssd::launch_chunk_scan_simt<T, TY>(d, xt, dtt, Bt, Ct, cum, states_in, D, static_cast<TY *>(y), s);
+    ssd::timing_mark(s, "chunk_scan_simt");
+    return from_cuda(e);
+}
+
+// L == 0: nothing to compute; the final state is the initial state.
+ssd_status_t empty_sequence(const Dims &d, const float *init, float *fin, cudaStream_t s) {
+    if (!fin || d.b == 0) return SSD_OK;
+    const size_t bytes = sizeof(float) * d.b * d.H * d.P * d.N;
+    cudaError_t e = init ? cudaMemcpyAsync(fin, init, bytes, cudaMemcpyDeviceToDevice, s)
+                         : cudaMemsetAsync(fin, 0, bytes, s);
+    return from_cuda(e);
+}
+
+// --- launch timing ---------------------------------------------------------
+constexpr int kMaxTimed = 16;
+struct LaunchTimer {
+    bool on = false;
+    int used = 0;
+    cudaEvent_t ev[kMaxTimed + 1] = {};
+    const char *name[kMaxTimed] = {};
+};
+LaunchTimer g_timer;
+
+}  // namespace
+
+namespace ssd {
+void timing_begin(cudaStream_t s) {
+    if (!g_timer.on) return;
+    g_timer.used = 0;
+    if (cudaEventRecord(g_timer.ev[0], s) == cudaSuccess) g_timer.used = 1;
+}
+void timing_mark(cudaStream_t s, const char *kernel_name) {
+    if (!g_timer.on || g_timer.used == 0 || g_timer.used > kMaxTimed) return;
+    if (cudaEventRecord(g_timer.ev[g_timer.used], s) == cudaSuccess) {
+        g_timer.name[g_timer.used - 1] = kernel_name;
+        ++g_timer.used;
+    }
+}
+}  // namespace ssd
+
+extern "C" {
+
+ssd_status_t ssd_launch_timing_enable(int enable) {
+    if (enable && !g_timer.on) {
+        for (int i = 0; i <= kMaxTimed; ++i)
+            if (cudaEventCreate(&g_timer.ev[i]) != cudaSuccess) return SSD_ERR_CUDA;
+        g_timer.on = true;
+        g_timer.used = 0;
+    } else if (!enable && g_timer.on) {
+        for (int i = 0; i <= kMaxTimed; ++i) cudaEventDestroy(g_timer.ev[i]);
+        g_timer.on = false;
+        g_timer.used = 0;
+    }
+    return SSD_OK;
+}
+
+const char *ssd_launch_timing_name(int i) {
+    if (!g_timer.on || i < 0 || i >= g_timer.used - 1) return nullptr;
+    return g_timer.name[i];
+}
+
+int ssd_launch_timing_read(float *ms, int cap) {
+    if (!g_timer.on || g_timer.used < 2) return -1;
+    const int n = g_timer.used - 1;
+    if (cudaEventSynchronize(g_timer.ev[n]) != cudaSuccess) return -1;
+    for (int i = 0; i < n && i < cap; ++i)
+        if (cudaEventElapsedTime(&ms[i], g_timer.ev[i], g_timer.ev[i + 1]) != cudaSuccess) return -1;
+    return n;
+}
+
+const char *ssd_status_string(ssd_status_t st) {
+    switch (st) {
+        case SSD_OK: return "SSD_OK";
+        case SSD_ERR_INVALID_ARG: return "SSD_ERR_INVALID_ARG: null or misaligned pointer, or invalid shape";
+        case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: shape outside what the GPU kernels run";
+        case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA launch failed";
+        case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "SSD_ERR_UNKNOWN";
+}
+
+int ssd_abi_version(void) { return (1 << 16) | 0; }
+
+size_t ssd_fwd_workspace_size(const ssd_shape_t *shape) {
+    Dims d;
+    if (check_shape(shape, true, &d) != SSD_OK) return 0;
+    if (ssd::tc_fwd_supported(d, shape->dtype)) return ssd::tc_fwd_workspace(d);
+    return staged_workspace(d);
+}
+
+ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void *dt, const float *A, const void *B,
+                     const void *C, const float *D, const float *init_state, void *y, float *final_state,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, true, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0) return SSD_OK;
+    if (d.L == 0) {
+        if (!ptrs_ok({A}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+        return empty_sequence(d, init_state, final_state, stream);
+    }
+    if (!ptrs_ok({x, dt, A, B, C, y}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+    const bool tc = ssd::tc_fwd_supported(d, shape->dtype);
+    const size_t need = tc ? ssd::tc_fwd_workspace(d) : staged_workspace(d);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return SSD_ERR_WORKSPACE;
+    if (tc)
+        return from_cuda(
+            ssd::tc_fwd(d, shape->ydtype, x, dt, A, B, C, D, init_state, y, final_state, workspace, stream));
+    if (shape->dtype == SSD_DTYPE_F32)
+        return fwd_staged<float, float>(d, x, dt, A, B, C, D, init_state, y, final_state, workspace, stream);
+    if (shape->ydtype == SSD_DTYPE_F32)
+        return fwd_staged<bf16, float>(d, x, dt, A, B, C, D, init_state, y, final_state, workspace, stream);
+    return fwd_staged<bf16, bf16>(d, x, dt, A, B, C, D, init_state, y, final_state, workspace, stream);
+}
+
+ssd_status_t ssd_chunk_cumsum(const ssd_shape_t *shape, const void *dt, const float *A, float *dA_cumsum,
+                              cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, true, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0 || d.L == 0) return SSD_OK;
+    if (!ptrs_ok({dt, A, dA_cumsum}, {})) return SSD_ERR_INVALID_ARG;
+    if (shape->dtype == SSD_DTYPE_F32)
+        return from_cuda(ssd::launch_chunk_cumsum<float>(d, static_cast<const float *>(dt), A, dA_cumsum, stream));
+    return from_cuda(ssd::launch_chunk_cumsum<bf16>(d, static_cast<const bf16 *>(dt), A, dA_cumsum, stream));
+}
+
+ssd_status_t ssd_chunk_state(const ssd_shape_t *shape, const void *x, const void *dt, const void *B,
+                             const float *dA_cumsum, float *states, cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, true, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0 || d.L == 0) return SSD_OK;
+    if (!ptrs_ok({x, dt, B, dA_cumsum, states}, {})) return SSD_ERR_INVALID_ARG;
+    if (ssd::tc_stage_supported(d, shape->dtype))
+        return from_cuda(ssd::tc_chunk_state(d, x, dt, B, dA_cumsum, states, stream));
+    if (shape->dtype == SSD_DTYPE_F32)
+        return from_cuda(ssd::launch_chunk_state_simt<float>(d, static_cast<const float *>(x),
+                                                             static_cast<const float *>(dt),
+                                                             static_cast<const float *>(B), dA_cumsum, states,
+                                                             stream));
+    return from_cuda(ssd::launch_chunk_state_simt<bf16>(d, static_cast<const bf16 *>(x),
+                                                        static_cast<const bf16 *>(dt),
+                                                        static_cast<const bf16 *>(B), dA_cumsum, states, stream));
+}
+
+ssd_status_t ssd_state_passing(const ssd_shape_t *shape, const float *states, const float *dA_cumsum,
+                               const float *init_state, float *states_in, float *final_state,
+                               cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, true, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0) return SSD_OK;
+    if (d.L == 0) {
+        if (!ptrs_ok({}, {init_state, final_state})) return SSD_ERR_INVALID_ARG;
+        return empty_sequence(d, init_state, final_state, stream);
+    }
+    if (!ptrs_ok({states, dA_cumsum}, {init_state, states_in, final_state})) return SSD_ERR_INVALID_ARG;
+    return from_cuda(ssd::launch_state_passing(d, states, dA_cumsum, init_state, states_in, final_state, stream));
+}
+
+ssd_status_t ssd_chunk_scan(const ssd_shape_t *shape, const void *x, const void *dt, const void *B, const void *C,
+                            const float *dA_cumsum, const float *states_in, const float *D, void *y,
+                            cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, true, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0 || d.L == 0) return SSD_OK;
+    if (!ptrs_ok({x, dt, B, C, dA_cumsum, states_in, y}, {D})) return SSD_ERR_INVALID_ARG;
+    if (ssd::tc_stage_supported(d, shape->dtype))
+        return from_cuda(ssd::tc_chunk_scan(d, shape->ydtype, x, dt, B, C, dA_cumsum, states_in, D, y, stream));
+    if (shape->dtype == SSD_DTYPE_F32)
+        return from_cuda(ssd::launch_chunk_scan_simt<float, float>(
+            d, static_cast<const float *>(x), static_cast<const float *>(dt), static_cast<const float *>(B),
+            static_cast<const float *>(C), dA_cumsum, states_in, D, static_cast<float *>(y), stream));
+    const bf16 *xb = static_cast<const bf16 *>(x), *dtb = static_cast<const bf16 *>(dt);
+    const bf16 *Bb = static_cast<const bf16 *>(B), *Cb = static_cast<const bf16 *>(C);
+    if (shape->ydtype == SSD_DTYPE_F32)
+        return from_cuda(ssd::launch_chunk_scan_simt<bf16, float>(d, xb, dtb, Bb, Cb, dA_cumsum, states_in, D,
+                                                                  static_cast<float *>(y), stream));
+    return from_cuda(ssd::launch_chunk_scan_simt<bf16, bf16>(d, xb, dtb, Bb, Cb, dA_cumsum, states_in, D,
+                                                             static_cast<bf16 *>(y), stream));
+}
+
+ssd_status_t selective_scan_fwd(const ssd_shape_t *shape, const void *x, const void *dt, const float *A,
+                                const void *B, const void *C, const float *D, const float *init_state, void *y,
+                                float *final_state, cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, false, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0) return SSD_OK;
+    if (d.L == 0) {
+        if (!ptrs_ok({A}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+        return empty_sequence(d, init_state, final_state, stream);
+    }
+    if (!ptrs_ok({x, dt, A, B, C, y}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+    if (shape->dtype == SSD_DTYPE_F32)
+        return from_cuda(ssd::launch_selective_scan<float, float>(
+            d, static_cast<const float *>(x), static_cast<const float *>(dt), A, static_cast<const float *>(B),
+            static_cast<const float *>(C), D, init_state, static_cast<float *>(y), final_state, stream));
+    const bf16 *xb = static_cast<const bf16 *>(x), *dtb = static_cast<const bf16 *>(dt);
+    const bf16 *Bb = static_cast<const bf16 *>(B), *Cb = static_cast<const bf16 *>(C);
+    if (shape->ydtype == SSD_DTYPE_F32)
+        return from_cuda(ssd::launch_selective_scan<bf16, float>(d, xb, dtb, A, Bb, Cb, D, init_state,
+                                                                 static_cast<float *>(y), final_state, stream));
+    return from_cuda(ssd::launch_selective_scan<bf16, bf16>(d, xb, dtb, A, Bb, Cb, D, init_state,
+                                                            static_cast<bf16 *>(y), final_state, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,425 @@
+// ssd_simt.cu -- CUDA-core (FFMA) kernels of libssd.
+//
+//  * chunk cumsum (stage 1) and state passing (stage 3): bandwidth-bound
+//    elementwise work, one pass over their inputs.
+//  * chunk state (stage 2) and chunk scan (stage 4) on fp32 FFMA: the path
+//    for fp32 inputs, whose 1e-4 x RMS tolerance rules out bf16/tf32 tensor
+//    cores.
+//  * selective_scan_fwd: the recurrence as a sequential scan over t, the
+//    schedule "Why SSM and linear-RNN FLOPs do not convert into GPU FLOPs"
+//    (paragraph 1) contrasts with the matmul reformulation.
+#include "ssd_common.cuh"
+
+namespace ssd {
+namespace {
+
+constexpr int kTile = 64;         // SIMT GEMM tile edge
+constexpr int kLd = kTile + 4;    // padded smem row
+
+// ---------------------------------------------------------------------------
+// Stage 1: cum[b,h,c,q] = sum_{k<=q} dt[b,cQ+k,h] * A[h].  One warp per
+// (b, h, c); lane l owns QPL consecutive positions, a warp shuffle scan
+// joins the lane totals.
+// ---------------------------------------------------------------------------
+template <typename T, int QPL>
+__global__ void __launch_bounds__(256) chunk_cumsum_kernel(Dims d, const T *__restrict__ dt,
+                                                           const float *__restrict__ A,
+                                                           float *__restrict__ cum) {
+    const int lane = threadIdx.x & 31;
+    const int64_t h = (int64_t)blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t c = blockIdx.x, b = blockIdx.z;
+    if (h >= d.H) return;  // warp-uniform
+    const float a = A[h];
+    float v[QPL];
+    float run = 0.f;
+#pragma unroll
+    for (int i = 0; i < QPL; ++i) {
+        const int64_t t = c * d.Q + lane * QPL + i;
+        run += to_f32(dt[(b * d.L + t) * d.H + h]) * a;
+        v[i] = run;
+    }
+    float tot = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, tot, off);
+        if (lane >= off) tot += o;
+    }
+    const float excl = tot - run;
+    float *out = cum + ((b * d.H + h) * d.nc + c) * d.Q + lane * QPL;
+#pragma unroll
+    for (int i = 0; i < QPL; ++i) out[i] = v[i] + excl;
+}
+
+// ---------------------------------------------------------------------------
+// Stage 3: sequential pass of states across chunks.  One thread per four
+// consecutive (p, n) entries of one (b, h); 128-bit loads and stores.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) state_passing_kernel(Dims d, const float4 *__restrict__ states,
+                                                            const float *__restrict__ cum,
+                                                            const float4 *__restrict__ init,
+                                                            float4 *__restrict__ states_in,
+                                                            float4 *__restrict__ fin) {
+    const int64_t PN4 = d.P * d.N / 4;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t h = blockIdx.y, b = blockIdx.z;
+    if (e >= PN4) return;
+    float4 s = init ? init[(b * d.H + h) * PN4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float *last = cum + (b * d.H + h) * d.nc * d.Q + (d.Q - 1);
+    for (int64_t c = 0; c < d.nc; ++c) {
+        const int64_t off = ((b * d.nc + c) * d.H + h) * PN4 + e;
+        if (states_in) states_in[off] = s;
+        const float g = expf(last[c * d.Q]);
+        const float4 v = states[off];
+        s.x = fmaf(g, s.x, v.x);
+        s.y = fmaf(g, s.y, v.y);
+        s.z = fmaf(g, s.z, v.z);
+        s.w = fmaf(g, s.w, v.w);
+    }
+    if (fin) fin[(b * d.H + h) * PN4 + e] = s;
+}
+
+// Rank-1-update micro kernel: acc[i][j] += sum_k As[k][r0+i] * Bs[k][c0+j].
+__device__ __forceinline__ void mma_tile(const float *As, int lda, const float *Bs, int ldb, int K, int r0,
+                                         int c0, float (&acc)[4][4]) {
+#pragma unroll 8
+    for (int k = 0; k < K; ++k) {
+        const float4 a = *reinterpret_cast<const float4 *>(As + k * lda + r0);
+        const float4 bb = *reinterpret_cast<const float4 *>(Bs + k * ldb + c0);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+        const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 2 on FFMA: states[b,c,h] = (w o x_c)^T B_c, w_q = exp(cum_last - cum_q) dt_q.
+// One CTA per (c, h, b); 64x64 output tiles, 4x4 per thread.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) chunk_state_simt_kernel(Dims d, const T *__restrict__ x,
+                                                               const T *__restrict__ dt,
+                                                               const T *__restrict__ B,
+                                                               const float *__restrict__ cum,
+                                                               float *__restrict__ states) {
+    __shared__ float w_s[128];
+    __shared__ __align__(16) float As[kTile * kLd];
+    __shared__ __align__(16) float Bs[kTile * kLd];
+    const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int64_t g = h / d.hpg;
+    const int tid = threadIdx.x;
+    const float *cc = cum + ((b * d.H + h) * d.nc + c) * d.Q;
+    for (int q = tid; q < d.Q; q += blockDim.x)
+        w_s[q] = expf(cc[d.Q - 1] - cc[q]) * to_f32(dt[(b * d.L + c * d.Q + q) * d.H + h]);
+    __syncthreads();
+    const int tr = tid >> 4, tcol = tid & 15;
+    for (int64_t p0 = 0; p0 < d.P; p0 += kTile)
+        for (int64_t n0 = 0; n0 < d.N; n0 += kTile) {
+            float acc[4][4] = {};
+            for (int64_t q0 = 0; q0 < d.Q; q0 += kTile) {
+                for (int i = tid; i < kTile * kTile; i += blockDim.x) {
+                    const int q = i / kTile, k = i % kTile;
+                    const int64_t t = c * d.Q + q0 + q;
+                    As[q * kLd + k] = (p0 + k < d.P)
+                                          ? w_s[q0 + q] * to_f32(x[((b * d.L + t) * d.H + h) * d.P + p0 + k])
+                                          : 0.f;
+                    Bs[q * kLd + k] = (n0 + k < d.N) ? to_f32(B[((b * d.L + t) * d.G + g) * d.N + n0 + k]) : 0.f;
+                }
+                __syncthreads();
+                mma_tile(As, kLd, Bs, kLd, kTile, tr * 4, tcol * 4, acc);
+                __syncthreads();
+            }
+            float *out = states + ((b * d.nc + c) * d.H + h) * d.P * d.N;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t p = p0 + tr * 4 + i;
+                if (p >= d.P) continue;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t n = n0 + tcol * 4 + j;
+                    if (n < d.N) out[p * d.N + n] = acc[i][j];
+                }
+            }
+        }
+}
+
+// ---------------------------------------------------------------------------
+// Stage 4 on FFMA.  One CTA per (c, h, b).
+//   M[t,s] = (C_t . B_s) exp(cum_t - cum_s) dt_s  for s <= t (kept in smem)
+//   y_t    = sum_s M[t,s] x_s + exp(cum_t) states_in C_t + D x_t
+// ---------------------------------------------------------------------------
+template <typename T, typename TY>
+__global__ void __launch_bounds__(256) chunk_scan_simt_kernel(Dims d, const T *__restrict__ x,
+                                                              const T *__restrict__ dt,
+                                                              const T *__restrict__ B,
+                                                              const T *__restrict__ C,
+                                                              const float *__restrict__ cum,
+                                                              const float *__restrict__ states_in,
+                                                              const float *__restrict__ D,
+                                                              TY *__restrict__ y) {
+    extern __shared__ __align__(16) float smem[];
+    const int Q = (int)d.Q;
+    float *cum_s = smem;                // [128]
+    float *dt_s = cum_s + 128;          // [128]
+    float *Ms = dt_s + 128;             // [Q][Q], Ms[s*Q + t]
+    float *As = Ms + Q * Q;             // [64][kLd]
+    float *Bs = As + kTile * kLd;       // [64][kLd]
+    const int64_t c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int64_t g = h / d.hpg;
+    const int tid = threadIdx.x;
+    const int tr = tid >> 4, tcol = tid & 15;
+    const int64_t t_base = c * d.Q;
+    const float *cc = cum + ((b * d.H + h) * d.nc + c) * d.Q;
+    for (int q = tid; q < Q; q += blockDim.x) {
+        cum_s[q] = cc[q];
+        dt_s[q] = to_f32(dt[(b * d.L + t_base + q) * d.H + h]);
+    }
+    const int nt = Q / kTile;
+    // masked score matrix, tile by tile
+    for (int ti = 0; ti < nt; ++ti)
+        for (int si = 0; si < nt; ++si) {
+            if (si > ti) {
+                for (int i = tid; i < kTile * kTile; i += blockDim.x) {
+                    const int s = si * kTile + i / kTile, t = ti * kTile + i % kTile;
+                    Ms[s * Q + t] = 0.f;
+                }
+                continue;
+            }
+            float acc[4][4] = {};
+            for (int64_t n0 = 0; n0 < d.N; n0 += kTile) {
+                __syncthreads();
+                for (int i = tid; i < kTile * kTile; i += blockDim.x) {
+                    const int r = i / kTile, k = i % kTile;
+                    const bool ok = n0 + k < d.N;
+                    As[k * kLd + r] = ok ? to_f32(C[((b * d.L + t_base + ti * kTile + r) * d.G + g) * d.N + n0 + k]) : 0.f;
+                    Bs[k * kLd + r] = ok ? to_f32(B[((b * d.L + t_base + si * kTile + r) * d.G + g) * d.N + n0 + k]) : 0.f;
+                }
+                __syncthreads();
+                mma_tile(As, kLd, Bs, kLd, kTile, tr * 4, tcol * 4, acc);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int t = ti * kTile + tr * 4 + i, s = si * kTile + tcol * 4 + j;
+                    Ms[s * Q + t] = (s <= t) ? acc[i][j] * __expf(cum_s[t] - cum_s[s]) * dt_s[s] : 0.f;
+                }
+        }
+    const float dh = D ? D[h] : 0.f;
+    const float *hin = states_in + ((b * d.nc + c) * d.H + h) * d.P * d.N;
+    for (int ti = 0; ti < nt; ++ti)
+        for (int64_t p0 = 0; p0 < d.P; p0 += kTile) {
+            float acc[4][4] = {};
+            for (int si = 0; si <= ti; ++si) {
+                __syncthreads();
+                for (int i = tid; i < kTile * kTile; i += blockDim.x) {
+                    const int s = i / kTile, k = i % kTile;
+                    Bs[s * kLd + k] = (p0 + k < d.P)
+                                          ? to_f32(x[((b * d.L + t_base + si * kTile + s) * d.H + h) * d.P + p0 + k])
+                                          : 0.f;
+                }
+                __syncthreads();
+                mma_tile(Ms + si * kTile * Q + ti * kTile, Q, Bs, kLd, kTile, tr * 4, tcol * 4, acc);
+            }
+            for (int64_t n0 = 0; n0 < d.N; n0 += kTile) {
+                __syncthreads();
+                for (int i = tid; i < kTile * kTile; i += blockDim.x) {
+                    const int r = i / kTile, k = i % kTile;
+                    const bool ok = n0 + k < d.N;
+                    const int t = ti * kTile + r;
+                    As[k * kLd + r] =
+                        ok ? to_f32(C[((b * d.L + t_base + t) * d.G + g) * d.N + n0 + k]) * __expf(cum_s[t]) : 0.f;
+                    Bs[k * kLd + r] = (ok && p0 + r < d.P) ? hin[(p0 + r) * d.N + n0 + k] : 0.f;
+                }
+                __syncthreads();
+                mma_tile(As, kLd, Bs, kLd, kTile, tr * 4, tcol * 4, acc);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int64_t t = t_base + ti * kTile + tr * 4 + i;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t p = p0 + tcol * 4 + j;
+                    if (p >= d.P) continue;
+                    const int64_t off = ((b * d.L + t) * d.H + h) * d.P + p;
+                    y[off] = from_f32<TY>(acc[i][j] + dh * to_f32(x[off]));
+                }
+            }
+        }
+}
+
+// ---------------------------------------------------------------------------
+// Sequential selective scan on FFMA.  CTA = 4 warps = 16 head channels of
+// one (b, h); inside a warp lane = (p_sub in 0..3, n_part in 0..7), each lane
+// carries NPL = N/8 state entries of one channel across all t.  Inputs are
+// staged TT steps at a time in shared memory.
+// ---------------------------------------------------------------------------
+template <typename T, typename TY, int NPL>
+__global__ void __launch_bounds__(128) selective_scan_kernel(Dims d, const T *__restrict__ x,
+                                                             const T *__restrict__ dt,
+                                                             const float *__restrict__ A,
+                                                             const T *__restrict__ B,
+                                                             const T *__restrict__ C,
+                                                             const float *__restrict__ D,
+                                                             const float *__restrict__ init,
+                                                             TY *__restrict__ y,
+                                                             float *__restrict__ fin) {
+    constexpr int TT = 16;
+    constexpr int NMAX = NPL * 8;
+    __shared__ __align__(16) float Bs[TT][NMAX];
+    __shared__ __align__(16) float Cs[TT][NMAX];
+    __shared__ float xs[TT][16];
+    __shared__ float us[TT][16];
+    __shared__ float as[TT];
+    __shared__ float ys[TT][16];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ps = lane >> 3, nq = lane & 7;
+    const int pl = warp * 4 + ps;  // channel within the CTA
+    const int64_t h = blockIdx.y, b = blockIdx.z;
+    const int64_t g = h / d.hpg;
+    const int64_t p = (int64_t)blockIdx.x * 16 + pl;
+    const float ah = A[h];
+    const float dh = D ? D[h] : 0.f;
+    float st[NPL];
+#pragma unroll
+    for (int k = 0; k < NPL; ++k)
+        st[k] = (init && p < d.P) ? init[((b * d.H + h) * d.P + p) * d.N + nq * NPL + k] : 0.f;
+
+    for (int64_t t0 = 0; t0 < d.L; t0 += TT) {
+        __syncthreads();
+        for (int i = tid; i < TT * NMAX; i += blockDim.x) {
+            const int tt = i / NMAX, n = i % NMAX;
+            const int64_t t = t0 + tt;
+            const bool ok = t < d.L;
+            Bs[tt][n] = ok ? to_f32(B[((b * d.L + t) * d.G + g) * d.N + n]) : 0.f;
+            Cs[tt][n] = ok ? to_f32(C[((b * d.L + t) * d.G + g) * d.N + n]) : 0.f;
+        }
+        for (int i = tid; i < TT * 16; i += blockDim.x) {
+            const int tt = i / 16, pp = i % 16;
+            const int64_t t = t0 + tt, pg = (int64_t)blockIdx.x * 16 + pp;
+            const bool ok = t < d.L && pg < d.P;
+            const float dtv = t < d.L ? to_f32(dt[(b * d.L + t) * d.H + h]) : 0.f;
+            const float xv = ok ? to_f32(x[((b * d.L + t) * d.H + h) * d.P + pg]) : 0.f;
+            xs[tt][pp] = xv;
+            us[tt][pp] = dtv * xv;
+            if (pp == 0) as[tt] = expf(dtv * ah);
+        }
+        __syncthreads();
+#pragma unroll 2
+        for (int tt = 0; tt < TT; ++tt) {
+            const float a = as[tt], u = us[tt][pl];
+            const float *Bt = &Bs[tt][nq * NPL];
+            const float *Ct = &Cs[tt][nq * NPL];
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < NPL; ++k) {
+                st[k] = fmaf(a, st[k], u * Bt[k]);
+                acc = fmaf(Ct[k], st[k], acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            if (nq == 0) ys[tt][pl] = acc + dh * xs[tt][pl];
+        }
+        __syncthreads();
+        for (int i = tid; i < TT * 16; i += blockDim.x) {
+            const int tt = i / 16, pp = i % 16;
+            const int64_t t = t0 + tt, pg = (int64_t)blockIdx.x * 16 + pp;
+            if (t < d.L && pg < d.P) y[((b * d.L + t) * d.H + h) * d.P + pg] = from_f32<TY>(ys[tt][pp]);
+        }
+    }
+    if (fin && p < d.P) {
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) fin[((b * d.H + h) * d.P + p) * d.N + nq * NPL + k] = st[k];
+    }
+}
+
+}  // namespace
+
+template <typename T>
+cudaError_t launch_chunk_cumsum(const Dims &d, const T *dt, const float *A, float *cum, cudaStream_t s) {
+    dim3 grid((unsigned)d.nc, (unsigned)((d.H + 7) / 8), (unsigned)d.b);
+    if (d.Q == 64)
+        chunk_cumsum_kernel<T, 2><<<grid, 256, 0, s>>>(d, dt, A, cum);
+    else
+        chunk_cumsum_kernel<T, 4><<<grid, 256, 0, s>>>(d, dt, A, cum);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_state_passing(const Dims &d, const float *states, const float *cum, const float *init,
+                                 float *states_in, float *final_state, cudaStream_t s) {
+    const int64_t PN4 = d.P * d.N / 4;
+    dim3 grid((unsigned)((PN4 + 255) / 256), (unsigned)d.H, (unsigned)d.b);
+    state_passing_kernel<<<grid, 256, 0, s>>>(d, reinterpret_cast<const float4 *>(states), cum,
+                                              reinterpret_cast<const float4 *>(init),
+                                              reinterpret_cast<float4 *>(states_in),
+                                              reinterpret_cast<float4 *>(final_state));
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_chunk_state_simt(const Dims &d, const T *x, const T *dt, const T *B, const float *cum,
+                                    float *states, cudaStream_t s) {
+    dim3 grid((unsigned)d.nc, (unsigned)d.H, (unsigned)d.b);
+    chunk_state_simt_kernel<T><<<grid, 256, 0, s>>>(d, x, dt, B, cum, states);
+    return cudaGetLastError();
+}
+
+template <typename T, typename TY>
+cudaError_t launch_chunk_scan_simt(const Dims &d, const T *x, const T *dt, const T *B, const T *C,
+                                   const float *cum, const float *states_in, const float *D, TY *y,
+                                   cudaStream_t s) {
+    const size_t smem = sizeof(float) * (256 + d.Q * d.Q + 2 * kTile * kLd);
+    // opt in to the largest size once per process (idempotent, so a race
+    // between threads only repeats the same call)
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_scan_simt_kernel<T, TY>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(sizeof(float) * (256 + 128 * 128 + 2 * kTile * kLd)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    dim3 grid((unsigned)d.nc, (unsigned)d.H, (unsigned)d.b);
+    chunk_scan_simt_kernel<T, TY><<<grid, 256, smem, s>>>(d, x, dt, B, C, cum, states_in, D, y);
+    return cudaGetLastError();
+}
+
+template <typename T, typename TY>
+cudaError_t launch_selective_scan(const Dims &d, const T *x, const T *dt, const float *A, const T *B, const T *C,
+                                  const float *D, const float *init, TY *y, float *final_state, cudaStream_t s) {
+    dim3 grid((unsigned)((d.P + 15) / 16), (unsigned)d.H, (unsigned)d.b);
+    switch (d.N) {
+        case 16: selective_scan_kernel<T, TY, 2><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
+        case 32: selective_scan_kernel<T, TY, 4><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
+        case 64: selective_scan_kernel<T, TY, 8><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
+        case 128: selective_scan_kernel<T, TY, 16><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
+        case 256: selective_scan_kernel<T, TY, 32><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_chunk_cumsum<float>(const Dims &, const float *, const float *, float *, cudaStream_t);
+template cudaError_t launch_chunk_cumsum<__nv_bfloat16>(const Dims &, const __nv_bfloat16 *, const float *, float *,
+                                                        cudaStream_t);
+template cudaError_t launch_chunk_state_simt<float>(const Dims &, const float *, const float *, const float *,
+                                                    const float *, float *, cudaStream_t);
+template cudaError_t launch_chunk_state_simt<__nv_bfloat16>(const Dims &, const __nv_bfloat16 *,
+                                                            const __nv_bfloat16 *, const __nv_bfloat16 *,
+                                                            const float *, float *, cudaStream_t);
+
+#define SSD_INSTANTIATE_Y(T, TY)                                                                                  \
+    template cudaError_t launch_chunk_scan_simt<T, TY>(const Dims &, const T *, const T *, const T *, const T *,  \
+                                                       const float *, const float *, const float *, TY *,         \
+                                                       cudaStream_t);                                             \
+    template cudaError_t launch_selective_scan<T, TY>(const Dims &, const T *, const T *, const float *,          \
+                                                      const T *, const T *, const float *, const float *, TY *,   \
+                                                      float *, cudaStream_t);
+SSD_INSTANTIATE_Y(float, float)
+SSD_INSTANTIATE_Y(__nv_bfloat16, float)
+SSD_INSTANTIATE_Y(__nv_bfloat16, __nv_bfloat16)
+
+}  // namespace ssd

@@ -1,0 +1,130 @@
+"""The C ABI on the host: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU
+(CPU only: no call here reaches a kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import state_space_model_fwd_gb300 as ssd
+from state_space_model_fwd_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssd.h")
+
+OK, INVALID, UNSUPPORTED, CUDA_ERR, WORKSPACE = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ssd.load_library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SSD_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    assert set(ssd.EXPORTED) <= set(names), names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"libssd.so does not export {name}"
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = ssd.status_string(code)
+        assert s.startswith("SSD_"), s
+    assert ssd.status_string(99) == "SSD_ERR_UNKNOWN"
+    assert lib.ssd_abi_version() >> 16 == 1
+
+
+def shape(**kw):
+    d = dict(batch=2, seqlen=256, nheads=4, headdim=64, dstate=128, ngroups=1, chunk_size=64,
+             dtype=1, ydtype=0)
+    d.update(kw)
+    return ssd.ssd_shape_t(**d)
+
+
+FAKE = ctypes.c_void_p(1 << 20)          # 16-byte aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+
+
+def fwd(lib, s, ptrs=None, ws=FAKE, ws_bytes=1 << 40):
+    p = ptrs or [FAKE] * 9
+    return lib.ssd_fwd(ctypes.byref(s), *p, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nheads=6, ngroups=4), INVALID),        # H % G != 0
+    (dict(seqlen=250), UNSUPPORTED),              # ragged last chunk
+    (dict(chunk_size=32), UNSUPPORTED),
+    (dict(chunk_size=0), INVALID),
+    (dict(headdim=48), UNSUPPORTED),
+    (dict(dstate=512), UNSUPPORTED),
+    (dict(dtype=7), INVALID),
+    (dict(dtype=0, ydtype=1), INVALID),          # bf16 y from fp32 input
+    (dict(batch=-1), INVALID),
+    (dict(nheads=0), INVALID),
+])
+def test_shape_validation(lib, kw, code):
+    assert fwd(lib, shape(**kw)) == code
+
+
+def test_null_and_misaligned_pointers(lib):
+    s = shape()
+    for i in (0, 1, 2, 3, 4, 7):                   # x, dt, A, B, C, y are required
+        p = [FAKE] * 9
+        p[i] = None
+        assert fwd(lib, s, p) == INVALID, i
+        p[i] = MISALIGNED
+        assert fwd(lib, s, p) == INVALID, i
+    p = [FAKE] * 9
+    p[6] = MISALIGNED                               # optional init_state, misaligned
+    assert fwd(lib, s, p) == INVALID
+
+
+def test_workspace_checks(lib):
+    s = shape()
+    need = lib.ssd_fwd_workspace_size(ctypes.byref(s))
+    assert need > 0
+    assert fwd(lib, s, ws=None) == WORKSPACE
+    assert fwd(lib, s, ws_bytes=need - 1) == WORKSPACE
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(shape(seqlen=250))) == 0
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert fwd(lib, shape(batch=0), [None] * 9, ws=None, ws_bytes=0) == OK
+
+
+def test_stage_entry_points_validate(lib):
+    s = shape(seqlen=100)
+    assert lib.ssd_chunk_cumsum(ctypes.byref(s), FAKE, FAKE, FAKE, None) == UNSUPPORTED
+    s = shape()
+    assert lib.ssd_chunk_cumsum(ctypes.byref(s), None, FAKE, FAKE, None) == INVALID
+    assert lib.ssd_chunk_state(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None, None) == INVALID
+    assert lib.ssd_state_passing(ctypes.byref(s), None, FAKE, None, FAKE, None, None) == INVALID
+    assert lib.ssd_chunk_scan(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None) == INVALID
+    assert lib.selective_scan_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, None, FAKE, None, None, FAKE, None,
+                                  None) == INVALID
+    # the sequential scan has no chunk restriction, but still checks groups
+    assert lib.selective_scan_fwd(ctypes.byref(shape(nheads=5, ngroups=2)), *([FAKE] * 9), None) == INVALID
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 64, 2, 16)
+    with pytest.raises(TypeError):
+        ssd.ssd_fwd(x, torch.zeros(1, 64, 2), torch.zeros(2), torch.zeros(1, 64, 1, 16),
+                    torch.zeros(1, 64, 1, 16))
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(ImportError):
+        ssd.load_library(str(tmp_path / "libssd.so"))

@@ -1,0 +1,258 @@
+"""CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+Tolerances (max |err| over the compared outputs, divided by the oracle
+output's RMS, separately for y and final_state):
+  fp32 inputs:  1e-4
+  bf16 inputs (fp32 state and accumulation, fp32 y): 1e-2
+  bf16 y: 1e-2 plus the bf16 output rounding of the oracle value (half an
+  ulp, 2^-9 |y| relative), which a bf16 store adds on top of the arithmetic.
+Full-size workloads compare every output of sampled (batch, head) pairs with
+the oracle run on those heads alone (heads are independent), and the whole
+output against the four-stage decomposed path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ssd_inputs as si
+import state_space_model_fwd_gb300 as ssd
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 1e-2}
+
+
+def rel_err(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape
+    assert np.all(np.isfinite(got)), "non-finite output"
+    rms = np.sqrt(np.mean(want ** 2))
+    return float(np.max(np.abs(got - want)) / max(rms, 1e-30)) if want.size else 0.0
+
+
+def check(got, want, tol, what):
+    e = rel_err(got, want)
+    assert e <= tol, f"{what}: max|err| = {e:.3e} x RMS > {tol:.1e}"
+    return e
+
+
+def bf16_half_ulp_rel(want):
+    """bf16 output rounding bound relative to the RMS: half an ulp of each
+    oracle value (|v| * 2^-8 is an upper bound of half an ulp)."""
+    rms = np.sqrt(np.mean(np.asarray(want, np.float64) ** 2))
+    return float(np.max(np.abs(want)) * 2.0 ** -8 / max(rms, 1e-30))
+
+
+def to_np(t):
+    return t.detach().double().cpu().numpy()
+
+
+def gpu_inputs(inp):
+    return inp.to_torch("cuda")
+
+
+def oracle_full(inp):
+    f = inp.as_f64()
+    return oracle.ssd_recurrence(f["x"], f["dt"], f["A"], f["B"], f["C"], f["D"], f["init_state"])
+
+
+def oracle_heads(inp, pairs):
+    """Oracle on single (batch, head) pairs: returns {(b, h): (y [L, P], final [P, N])}."""
+    cfg = inp.cfg
+    f = inp.as_f64()
+    out = {}
+    for b, h in pairs:
+        g = h * cfg.ngroups // cfg.nheads
+        init = None if f["init_state"] is None else f["init_state"][b:b + 1, h:h + 1]
+        y, fin = oracle.ssd_recurrence(f["x"][b:b + 1, :, h:h + 1], f["dt"][b:b + 1, :, h:h + 1],
+                                       f["A"][h:h + 1], f["B"][b:b + 1, :, g:g + 1], f["C"][b:b + 1, :, g:g + 1],
+                                       f["D"][h:h + 1], init)
+        out[(b, h)] = (y[0, :, 0], fin[0, 0])
+    return out
+
+
+SMALL = {
+    "tiny_f32": si.CONFIGS["tiny_f32"],
+    "f32_p32_n64_init": si.SSDConfig("f32_p32_n64_init", 2, 512, 3, 32, 64, 1, 64, "f32", True, 77),
+    "bf16_p64_n128": si.SSDConfig("bf16_p64_n128", 2, 640, 6, 64, 128, 2, 64, "bf16", True, 78),
+    "bf16_p64_n128_h5": si.SSDConfig("bf16_p64_n128_h5", 1, 1152, 5, 64, 128, 1, 64, "bf16", False, 79),
+    "bf16_p128_n256_q64": si.SSDConfig("bf16_p128_n256_q64", 1, 448, 4, 128, 256, 2, 64, "bf16", True, 80),
+    "bf16_p128_n256_q128": si.SSDConfig("bf16_p128_n256_q128", 1, 640, 4, 128, 256, 2, 128, "bf16", True, 81),
+    "bf16_p16_n16": si.SSDConfig("bf16_p16_n16", 3, 320, 8, 16, 16, 4, 64, "bf16", True, 82),
+    "bf16_p32_n64_q128": si.SSDConfig("bf16_p32_n64_q128", 2, 384, 6, 32, 64, 3, 128, "bf16", False, 83),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_ssd_fwd_small(name):
+    cfg = SMALL[name]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    y, fin = ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
+                         chunk_size=cfg.chunk_size)
+    y_ref, fin_ref = oracle_full(inp)
+    check(to_np(y), y_ref, TOL[cfg.dtype], f"{name} y")
+    check(to_np(fin), fin_ref, TOL[cfg.dtype], f"{name} final")
+
+
+@pytest.mark.parametrize("name", ["bf16_p64_n128", "bf16_p128_n256_q128"])
+def test_ssd_fwd_bf16_output(name):
+    cfg = SMALL[name]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    y, fin = ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
+                         chunk_size=cfg.chunk_size, y_dtype=torch.bfloat16)
+    assert y.dtype == torch.bfloat16
+    y_ref, fin_ref = oracle_full(inp)
+    check(to_np(y), y_ref, TOL["bf16"] + bf16_half_ulp_rel(y_ref), f"{name} bf16 y")
+    check(to_np(fin), fin_ref, TOL["bf16"], f"{name} final")
+
+
+def test_ssd_fwd_no_optional_inputs():
+    cfg = SMALL["bf16_p64_n128"]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    y, fin = ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], None, None, chunk_size=64,
+                         return_final_state=False)
+    assert fin is None
+    f = inp.as_f64()
+    y_ref, _ = oracle.ssd_recurrence(f["x"], f["dt"], f["A"], f["B"], f["C"], None, None)
+    check(to_np(y), y_ref, TOL["bf16"], "no D / init / final y")
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "bf16_p64_n128", "bf16_p128_n256_q128", "bf16_p16_n16"])
+def test_stages_against_definitions(name):
+    """Each stage entry point against the oracle's definition of its output,
+    fed the oracle's own (rounded to fp32) inputs for the stage."""
+    cfg = SMALL[name]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    f = inp.as_f64()
+    Q = cfg.chunk_size
+    tol = TOL[cfg.dtype]
+    cum = ssd.ssd_chunk_cumsum(t["dt"], t["A"], Q)
+    cum_ref = oracle.chunk_cumsum(f["dt"], f["A"], Q)
+    e = np.max(np.abs(to_np(cum) - cum_ref)) / np.max(np.abs(cum_ref))
+    assert e <= 1e-5, f"cumsum rel err {e:.2e}"
+    cum_in = torch.from_numpy(cum_ref.astype(np.float32)).cuda()
+    st = ssd.ssd_chunk_state(t["x"], t["dt"], t["B"], cum_in)
+    st_ref = oracle.chunk_states(f["x"], f["dt"], f["A"], f["B"], Q)
+    check(to_np(st), st_ref, tol, "chunk states")
+    sin_ref, fin_ref = oracle.states_entering(f["x"], f["dt"], f["A"], f["B"], f["C"], Q, f["init_state"])
+    sin, fin = ssd.ssd_state_passing(torch.from_numpy(st_ref.astype(np.float32)).cuda(), cum_in,
+                                     t["init_state"])
+    check(to_np(sin), sin_ref, 1e-5, "states entering chunks")
+    check(to_np(fin), fin_ref, 1e-5, "final state from state passing")
+    y = ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum_in,
+                           torch.from_numpy(sin_ref.astype(np.float32)).cuda(), t["D"])
+    y_ref, _ = oracle_full(inp)
+    check(to_np(y), y_ref, tol, "chunk scan y")
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "f32_p32_n64_init", "bf16_p64_n128", "bf16_p128_n256_q64",
+                                  "bf16_p16_n16"])
+def test_selective_scan_small(name):
+    cfg = SMALL[name]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    y, fin = ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"])
+    y_ref, fin_ref = oracle_full(inp)
+    check(to_np(y), y_ref, TOL[cfg.dtype], f"{name} scan y")
+    check(to_np(fin), fin_ref, TOL[cfg.dtype], f"{name} scan final")
+
+
+def test_selective_scan_ragged_length():
+    cfg = si.SSDConfig("ragged", 1, 333, 2, 16, 32, 1, 64, "f32", True, 90)
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    y, fin = ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"])
+    y_ref, fin_ref = oracle_full(inp)
+    check(to_np(y), y_ref, 1e-4, "ragged scan y")
+    check(to_np(fin), fin_ref, 1e-4, "ragged scan final")
+
+
+def test_empty_sequence_passes_state_through():
+    x = torch.zeros(2, 0, 4, 64, device="cuda", dtype=torch.bfloat16)
+    dt = torch.zeros(2, 0, 4, device="cuda", dtype=torch.bfloat16)
+    B = torch.zeros(2, 0, 1, 128, device="cuda", dtype=torch.bfloat16)
+    A = -torch.ones(4, device="cuda")
+    init = torch.randn(2, 4, 64, 128, device="cuda")
+    y, fin = ssd.ssd_fwd(x, dt, A, B, B, None, init)
+    torch.cuda.synchronize()
+    assert y.shape == x.shape and torch.equal(fin, init)
+    _, fin2 = ssd.ssd_fwd(x, dt, A, B, B, None, None)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(fin2) == 0
+
+
+def test_unsupported_shape_raises():
+    x = torch.zeros(1, 100, 2, 64, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(ssd.SSDError):
+        ssd.ssd_fwd(x, torch.zeros(1, 100, 2, device="cuda", dtype=torch.bfloat16), -torch.ones(2, device="cuda"),
+                    torch.zeros(1, 100, 1, 128, device="cuda", dtype=torch.bfloat16),
+                    torch.zeros(1, 100, 1, 128, device="cuda", dtype=torch.bfloat16))
+
+
+def test_bitwise_deterministic():
+    cfg = SMALL["bf16_p64_n128"]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    outs = [ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"]) for _ in range(3)]
+    for y, fin in outs[1:]:
+        assert torch.equal(y, outs[0][0]) and torch.equal(fin, outs[0][1])
+
+
+FULL = ["mamba2_130m", "mamba2_2p7b", "long_16k", "wide_head", "wide_head_q128"]
+
+
+def sample_pairs(cfg):
+    b, H = cfg.batch, cfg.nheads
+    return sorted({(0, 0), (b - 1, H - 1), (0, H // 2), (b - 1, 1), (b // 2, H // 3)})
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_ssd_fwd_full_size(name):
+    """Full-size workload, same launch configuration the benchmark times:
+    sampled heads against the oracle, every output against the four-stage
+    decomposed path."""
+    cfg = si.CONFIGS[name]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    y, fin = ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
+                         chunk_size=cfg.chunk_size)
+    torch.cuda.synchronize()
+    refs = oracle_heads(inp, sample_pairs(cfg))
+    ys = np.concatenate([refs[k][0] for k in sorted(refs)])
+    fs = np.concatenate([refs[k][1] for k in sorted(refs)])
+    yg = np.concatenate([to_np(y[b, :, h]) for b, h in sorted(refs)])
+    fg = np.concatenate([to_np(fin[b, h]) for b, h in sorted(refs)])
+    check(yg, ys, TOL["bf16"], f"{name} y (sampled heads)")
+    check(fg, fs, TOL["bf16"], f"{name} final (sampled heads)")
+    # whole output against the decomposed stages
+    Q = cfg.chunk_size
+    cum = ssd.ssd_chunk_cumsum(t["dt"], t["A"], Q)
+    st = ssd.ssd_chunk_state(t["x"], t["dt"], t["B"], cum)
+    sin, fin2 = ssd.ssd_state_passing(st, cum, t["init_state"])
+    del st
+    y2 = ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum, sin, t["D"])
+    del sin
+    torch.cuda.synchronize()
+    ry = float((y - y2).abs().max() / y2.float().pow(2).mean().sqrt())
+    rf = float((fin - fin2).abs().max() / fin2.pow(2).mean().sqrt())
+    assert torch.isfinite(y).all()
+    assert ry <= 2 * TOL["bf16"] and rf <= 2 * TOL["bf16"], (ry, rf)
+
+
+def test_selective_scan_long_sequence():
+    cfg = si.CONFIGS["long_16k"]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    y, fin = ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"])
+    torch.cuda.synchronize()
+    pairs = [(0, 0), (0, 47), (0, 20)]
+    refs = oracle_heads(inp, pairs)
+    ys = np.concatenate([refs[k][0] for k in pairs])
+    yg = np.concatenate([to_np(y[b, :, h]) for b, h in pairs])
+    check(yg, ys, TOL["bf16"], "long_16k sequential scan y (sampled heads)")
