@@ -82,6 +82,12 @@ SMALL = {
     "bf16_p128_n256_q128": si.SSDConfig("bf16_p128_n256_q128", 1, 640, 4, 128, 256, 2, 128, "bf16", True, 81),
     "bf16_p16_n16": si.SSDConfig("bf16_p16_n16", 3, 320, 8, 16, 16, 4, 64, "bf16", True, 82),
     "bf16_p32_n64_q128": si.SSDConfig("bf16_p32_n64_q128", 2, 384, 6, 32, 64, 3, 128, "bf16", False, 83),
+    # tensor-core path: many one-chunk segments, grouped heads, Q = 128, N = 64
+    "tc_p64_n128_seg": si.SSDConfig("tc_p64_n128_seg", 2, 640, 4, 64, 128, 1, 64, "bf16", True, 84),
+    "tc_p64_n128_g2": si.SSDConfig("tc_p64_n128_g2", 1, 1024, 8, 64, 128, 2, 64, "bf16", True, 85),
+    "tc_p64_n128_q128": si.SSDConfig("tc_p64_n128_q128", 2, 768, 4, 64, 128, 1, 128, "bf16", True, 86),
+    "tc_p64_n64": si.SSDConfig("tc_p64_n64", 1, 512, 6, 64, 64, 3, 64, "bf16", False, 87),
+    "tc_p64_n128_1seg": si.SSDConfig("tc_p64_n128_1seg", 2, 256, 160, 64, 128, 1, 64, "bf16", True, 88),
 }
 
 
@@ -97,7 +103,7 @@ def test_ssd_fwd_small(name):
     check(to_np(fin), fin_ref, TOL[cfg.dtype], f"{name} final")
 
 
-@pytest.mark.parametrize("name", ["bf16_p64_n128", "bf16_p128_n256_q128"])
+@pytest.mark.parametrize("name", ["bf16_p64_n128", "bf16_p128_n256_q128", "tc_p64_n128_seg", "bf16_p128_n256_q64"])
 def test_ssd_fwd_bf16_output(name):
     cfg = SMALL[name]
     inp = si.make_inputs(cfg)
@@ -195,8 +201,9 @@ def test_unsupported_shape_raises():
                     torch.zeros(1, 100, 1, 128, device="cuda", dtype=torch.bfloat16))
 
 
-def test_bitwise_deterministic():
-    cfg = SMALL["bf16_p64_n128"]
+@pytest.mark.parametrize("name", ["bf16_p64_n128", "tc_p64_n128_seg"])
+def test_bitwise_deterministic(name):
+    cfg = SMALL[name]
     inp = si.make_inputs(cfg)
     t = gpu_inputs(inp)
     outs = [ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"]) for _ in range(3)]
