@@ -56,7 +56,13 @@ bool ptrs_ok(std::initializer_list<const void *> required, std::initializer_list
     return true;
 }
 
-ssd_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA; }
+// A failed runtime call also records itself as the thread's "last error";
+// clear that record so a later, unrelated call does not report it again.
+ssd_status_t from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return SSD_OK;
+    (void)cudaGetLastError();
+    return SSD_ERR_CUDA;
+}
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 

@@ -42,7 +42,7 @@ using namespace tc;
 
 constexpr int kThreads = 256;
 constexpr int kTargetCtas = 148;        // about one CTA per SM of a GB300 (152 SMs)
-constexpr int kSmemLimit = 227 * 1024;
+constexpr int kSmemLimit = 226 * 1024;  // dynamic bytes; leaves room for the static mbarriers
 
 struct TcParams {
     const bf16 *dt;
@@ -758,15 +758,20 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     prm.cps = p.cps;
     prm.y_f32 = ydtype == SSD_DTYPE_F32 ? 1 : 0;
 
-    static bool attr = false;
+    // raise each kernel's dynamic shared memory limit to what this call needs
+    static int scan_attr = 0, seg_attr = 0;
     const int seg_smem = C::SMEM_SEG_BASE + (int)(C::HB * p.cps * sizeof(float));
-    if (!attr) {
+    if (scan_attr < C::SMEM_SCAN) {
         cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::SMEM_SCAN);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(seg_state_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        scan_attr = C::SMEM_SCAN;
+    }
+    if (p.nseg > 1 && seg_attr < seg_smem) {
+        cudaError_t e = cudaFuncSetAttribute(seg_state_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             seg_smem);
         if (e != cudaSuccess) return e;
-        attr = true;
+        seg_attr = seg_smem;
     }
     if (seg_smem > kSmemLimit) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(prm.status, 0, sizeof(unsigned), s);
