@@ -69,7 +69,9 @@ struct Cfg {
     static constexpr int XW_BYTES = M * Q * 2;
     static constexpr int SBF_BYTES = M * N * 2;       // [N/64 blocks][M rows][64]
     static constexpr int MM_BYTES = HB * Q * Q * 2;   // per head [Q/64 blocks][Q rows][64]
-    static constexpr int SCR_BYTES = SBF_BYTES > MM_BYTES ? SBF_BYTES : MM_BYTES;
+    // scratch: the bf16 state copy and the low half of the scaled x during the
+    // state/inter MMAs, then the masked score matrices
+    static constexpr int SCR_BYTES = SBF_BYTES + XW_BYTES > MM_BYTES ? SBF_BYTES + XW_BYTES : MM_BYTES;
     static constexpr int SMALL_FLOATS = 4 * HB * Q + 4 * HB;
     static constexpr int SMALL_BYTES = SMALL_FLOATS * 4 + 128;
     static constexpr int smem_scan(int stages) {
@@ -81,7 +83,7 @@ struct Cfg {
     static constexpr bool SCAN_FITS = smem_scan(STAGES) <= kSmemLimit;
     // segment-state kernel: two stages of (x, B) plus the scaled x
     static constexpr int SEG_STAGE_BYTES = X_BYTES + BC_BYTES;
-    static constexpr int SMEM_SEG_BASE = 2 * SEG_STAGE_BYTES + XW_BYTES + SMALL_BYTES + 1024;
+    static constexpr int SMEM_SEG_BASE = 2 * SEG_STAGE_BYTES + 2 * XW_BYTES + SMALL_BYTES + 1024;
     // TMEM columns of the scan kernel
     static constexpr int COL_S = 0;
     static constexpr int COL_R3 = N;                 // inter-chunk term, [M][Q]
@@ -142,11 +144,13 @@ __device__ __forceinline__ float warp_chunk_cumsum(const float *dtv, float a, fl
     return __shfl_sync(0xffffffffu, tot, 31);
 }
 
-// x tile scaled row-wise by w: xw[s, (h, p)] = w[h][s] * x[s, (h, p)].
-// Works on whole 16-byte chunks of the swizzled layout (a row's chunks stay
-// in that row, so the scale of a chunk is its row's).
+// x tile scaled row-wise by w, split into two bf16 tiles whose sum carries
+// the product to about 2^-17 relative: hi = bf16(w x), lo = bf16(w x - hi).
+// (One bf16 rounding of w x, 2^-9 relative, is visible in the state entries
+// that a single recent token dominates.)  Works on whole 16-byte chunks of
+// the swizzled layout: a chunk stays in its row, so its scale is its row's.
 template <class C>
-__device__ __forceinline__ void build_xw(const uint8_t *xs, uint8_t *xw, const float *w) {
+__device__ __forceinline__ void build_xw(const uint8_t *xs, uint8_t *xw_hi, uint8_t *xw_lo, const float *w) {
     constexpr int CHUNKS = (C::M / 64) * C::Q * 8;
     for (int i = threadIdx.x; i < CHUNKS; i += kThreads) {
         const int blk = i / (C::Q * 8);
@@ -154,14 +158,21 @@ __device__ __forceinline__ void build_xw(const uint8_t *xs, uint8_t *xw, const f
         const int h = blk / C::PB;
         const float ws = w[h * C::Q + s];
         uint4 v = *reinterpret_cast<const uint4 *>(xs + (size_t)i * 16);
+        uint4 lo;
         uint32_t *u = reinterpret_cast<uint32_t *>(&v);
+        uint32_t *l = reinterpret_cast<uint32_t *>(&lo);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             __nv_bfloat162 p2 = *reinterpret_cast<__nv_bfloat162 *>(&u[j]);
-            float2 f = __bfloat1622float2(p2);
-            u[j] = pack_bf16x2(f.x * ws, f.y * ws);
+            const float2 f = __bfloat1622float2(p2);
+            const float a = f.x * ws, b2 = f.y * ws;
+            const __nv_bfloat162 hi2 = __floats2bfloat162_rn(a, b2);
+            const float2 hf = __bfloat1622float2(hi2);
+            u[j] = *reinterpret_cast<const uint32_t *>(&hi2);
+            l[j] = pack_bf16x2(a - hf.x, b2 - hf.y);
         }
-        *reinterpret_cast<uint4 *>(xw + (size_t)i * 16) = v;
+        *reinterpret_cast<uint4 *>(xw_hi + (size_t)i * 16) = v;
+        *reinterpret_cast<uint4 *>(xw_lo + (size_t)i * 16) = lo;
     }
 }
 
@@ -198,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
     uint8_t *xw = stages + 2 * C::SEG_STAGE_BYTES;
-    float *small = reinterpret_cast<float *>(xw + C::XW_BYTES);
+    uint8_t *xw_lo = xw + C::XW_BYTES;
+    float *small = reinterpret_cast<float *>(xw_lo + C::XW_BYTES);
     float *dtv = small;               // [HB][Q]
     float *cum = dtv + C::HB * C::Q;  // [HB][Q]
     float *w = cum + C::HB * C::Q;    // [HB][Q]
@@ -295,17 +307,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (tid == 0) fl.waited = it + 1;
         __syncthreads();
         if (abort_sh) break;
-        build_xw<C>(stage, xw, w);
+        build_xw<C>(stage, xw, xw_lo, w);
         fence_async_smem();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(C::M, C::N, true, true);
-            const uint32_t a0 = smem_u32(xw), b0 = smem_u32(stage + C::X_BYTES);
+            const uint32_t a0 = smem_u32(xw), a1 = smem_u32(xw_lo), b0 = smem_u32(stage + C::X_BYTES);
 #pragma unroll
             for (int ks = 0; ks < C::Q / 16; ++ks)
                 mma_bf16(tmem, sdesc(a0 + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
                          idesc, (it | ks) != 0);
+#pragma unroll
+            for (int ks = 0; ks < C::Q / 16; ++ks)
+                mma_bf16(tmem, sdesc(a1 + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
+                         idesc, true);
             mma_commit(&mma_bar);
             fl.mma = true;
         }
@@ -358,7 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *stages = smem;
     uint8_t *xw = stages + C::STAGES * C::STAGE_BYTES;
-    uint8_t *scr = xw + C::XW_BYTES;  // bf16 state copy, then the masked score matrices
+    uint8_t *scr = xw + C::XW_BYTES;  // bf16 state copy + low half of w x, then the masked score matrices
+    uint8_t *xw_lo = scr + C::SBF_BYTES;
     float *small = reinterpret_cast<float *>(scr + C::SCR_BYTES);
     float *dtv = small;                 // [HB][Q]
     float *cum = dtv + C::HB * C::Q;    // [HB][Q]
@@ -473,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (abort_sh) break;
         // (2) scaled x for the state update; bf16 copy of the entering state
         //     (operand of S C^T), then S *= exp(chunk total) in place
-        build_xw<C>(xs, xw, w);
+        build_xw<C>(xs, xw, xw_lo, w);
         if (warp < 4) {
             const float dec = decay[rh];
 #pragma unroll 1
@@ -520,9 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16(tmem + C::COL_R3, sdesc(ss + aoff, 16, 1024), sdesc(sc + boff, 16, 1024), id_inter, ks > 0);
             }
             const uint32_t id_state = idesc_bf16(C::M, C::N, true, true);
+            const uint32_t swl = smem_u32(xw_lo);
 #pragma unroll
             for (int ks = 0; ks < C::Q / 16; ++ks)
                 mma_bf16(tmem + C::COL_S, sdesc(sw + ks * 2048, C::Q * 128, 1024),
+                         sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
+#pragma unroll
+            for (int ks = 0; ks < C::Q / 16; ++ks)
+                mma_bf16(tmem + C::COL_S, sdesc(swl + ks * 2048, C::Q * 128, 1024),
                          sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
             (void)sx;
             mma_commit(&mma_bar);
