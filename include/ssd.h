@@ -67,7 +67,8 @@ typedef enum {
     SSD_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misaligned pointer */
     SSD_ERR_UNSUPPORTED = 2,   /* valid shape this build does not run */
     SSD_ERR_CUDA = 3,          /* a CUDA launch or query failed */
-    SSD_ERR_WORKSPACE = 4      /* workspace missing or smaller than required */
+    SSD_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+    SSD_ERR_SCRATCH_LIMIT = 5  /* ssd_fwd_noalloc: shape needs more than its static scratch */
 } ssd_status_t;
 
 typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype_t;
@@ -112,6 +113,31 @@ SSD_API ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void
                      const float *D, const float *init_state, void *y,
                      float *final_state, void *workspace, size_t workspace_bytes,
                      cudaStream_t stream);
+
+/*
+ * ssd_fwd without a workspace argument, for callers that cannot allocate
+ * device memory: code running inside a host application or inference
+ * server that owns the whole device memory pool and forbids allocations
+ * outside it, or latency-critical paths that must not call cudaMalloc after
+ * start-up (it can block on the device and can fail under memory pressure).
+ * The pages have no counterpart; it is the same computation as ssd_fwd.
+ *
+ * Scratch comes from one static device buffer of SSD_NOALLOC_SCRATCH_BYTES
+ * that lives in this library (every GPU that loads the library holds it
+ * until the process exits).  Shapes whose ssd_fwd_workspace_size() exceeds
+ * it return SSD_ERR_SCRATCH_LIMIT before anything is enqueued.  The call
+ * itself allocates nothing: no cudaMalloc, no cudaFree.
+ * The first call on each device looks up the buffer's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one buffer: calls whose
+ * GPU work overlaps (different streams, or several host threads) race on
+ * it, so serialise them.  Inputs, outputs and errors as for ssd_fwd.
+ */
+#define SSD_NOALLOC_SCRATCH_BYTES (16u << 20)
+SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, const void *dt,
+                                     const float *A, const void *B, const void *C,
+                                     const float *D, const float *init_state, void *y,
+                                     float *final_state, cudaStream_t stream);
 
 /*
  * Stage 1: dA_cumsum[b,h,c,q] = sum_{k<=q} dt[b, c*Q+k, h] * A[h].

@@ -29,7 +29,7 @@ SSD_DTYPE_BF16 = 1
 EXPORTED = ("ssd_status_string", "ssd_abi_version", "ssd_fwd_workspace_size", "ssd_fwd",
             "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
             "selective_scan_fwd", "ssd_launch_timing_enable", "ssd_launch_timing_read",
-            "ssd_launch_timing_name")
+            "ssd_launch_timing_name", "ssd_fwd_noalloc")
 
 
 class ssd_shape_t(ctypes.Structure):
@@ -75,7 +75,9 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_launch_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i32]
         lib.ssd_launch_timing_name.argtypes = [i32]
         lib.ssd_launch_timing_name.restype = ctypes.c_char_p
-        for name in EXPORTED[3:-1]:
+        lib.ssd_fwd_noalloc.argtypes = [shp] + [vp] * 10
+        lib.ssd_fwd_noalloc.restype = i32
+        for name in EXPORTED[3:-2]:
             getattr(lib, name).restype = i32
         if path == LIB_PATH:
             _lib = lib
@@ -170,6 +172,24 @@ def ssd_fwd(x, dt, A, B, C, D=None, init_state=None, chunk_size=64, *, y=None, f
                      _ptr(init_state), _ptr(y), _ptr(final_state), _ptr(workspace),
                      workspace.numel(), _stream(stream))
     _check("ssd_fwd", st)
+    return y, final_state
+
+
+def ssd_fwd_noalloc(x, dt, A, B, C, D=None, init_state=None, chunk_size=64, *, y, final_state=None,
+                    stream=None):
+    """ssd_fwd for callers that cannot allocate device memory: the library
+    takes its scratch from a static device buffer (SSD_NOALLOC_SCRATCH_BYTES)
+    and this wrapper allocates nothing either -- the caller passes y (and
+    final_state, if wanted).  Calls whose GPU work overlaps share that buffer
+    and race; serialise them.  Returns ``(y, final_state)``."""
+    lib = load_library()
+    b, L, H, P, G, N = _check_inputs(x, dt, A, B, C, D, init_state)
+    _need(y, "y", None, x.shape)
+    _need(final_state, "final_state", torch.float32, (b, H, P, N))
+    shape = make_shape(x, B, chunk_size, y.dtype)
+    st = lib.ssd_fwd_noalloc(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                             _ptr(init_state), _ptr(y), _ptr(final_state), _stream(stream))
+    _check("ssd_fwd_noalloc", st)
     return y, final_state
 
 
@@ -291,6 +311,6 @@ def launch_times_ms() -> list:
     return [((lib.ssd_launch_timing_name(i) or b"?").decode(), float(buf[i])) for i in range(min(n, 16))]
 
 
-__all__ = ["launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
+__all__ = ["ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
            "ssd_state_passing", "ssd_chunk_scan", "selective_scan_fwd", "ssd_shape_t", "SSDError",
            "load_library", "status_string", "EXPORTED", "LIB_PATH"]

@@ -3,6 +3,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "ssd.h"
 #include "ssd_common.cuh"
 #include "ssd_tc.cuh"
@@ -170,6 +172,8 @@ const char *ssd_status_string(ssd_status_t st) {
         case SSD_ERR_UNSUPPORTED: return "SSD_ERR_UNSUPPORTED: shape outside what the GPU kernels run";
         case SSD_ERR_CUDA: return "SSD_ERR_CUDA: a CUDA launch failed";
         case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
+        case SSD_ERR_SCRATCH_LIMIT:
+            return "SSD_ERR_SCRATCH_LIMIT: shape needs more scratch than ssd_fwd_noalloc's static buffer holds";
     }
     return "SSD_ERR_UNKNOWN";
 }
@@ -302,4 +306,66 @@ ssd_status_t selective_scan_fwd(const ssd_shape_t *shape, const void *x, const v
                                                             static_cast<bf16 *>(y), final_state, stream));
 }
 
+// ---------------------------------------------------------------------------
+// ssd_fwd_noalloc: ssd_fwd with scratch from a static device buffer.
+// ---------------------------------------------------------------------------
 }  // extern "C"
+
+namespace {
+
+// The scratch every ssd_fwd_noalloc call uses; one copy per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch on the current device, looked up
+// once per device (host code only sees a host-side stand-in for the symbol).
+cudaError_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, const void *dt, const float *A,
+                                        const void *B, const void *C, const float *D, const float *init_state,
+                                        void *y, float *final_state, cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, true, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0) return SSD_OK;
+    if (d.L == 0) {
+        if (!ptrs_ok({A}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+        return empty_sequence(d, init_state, final_state, stream);
+    }
+    if (!ptrs_ok({x, dt, A, B, C, y}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+    const bool tc = ssd::tc_fwd_supported(d, shape->dtype);
+    const size_t need = tc ? ssd::tc_fwd_workspace(d) : staged_workspace(d);
+    if (need > SSD_NOALLOC_SCRATCH_BYTES) return SSD_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return from_cuda(e);
+    // the kernels write every scratch word they later read, except the
+    // status word, which the fused path clears on the stream before use
+    if (tc)
+        return from_cuda(
+            ssd::tc_fwd(d, shape->ydtype, x, dt, A, B, C, D, init_state, y, final_state, scratch, stream));
+    if (shape->dtype == SSD_DTYPE_F32)
+        return fwd_staged<float, float>(d, x, dt, A, B, C, D, init_state, y, final_state, scratch, stream);
+    if (shape->ydtype == SSD_DTYPE_F32)
+        return fwd_staged<bf16, float>(d, x, dt, A, B, C, D, init_state, y, final_state, scratch, stream);
+    return fwd_staged<bf16, bf16>(d, x, dt, A, B, C, D, init_state, y, final_state, scratch, stream);
+}
