@@ -9,6 +9,9 @@
 //               exp(sum_{k>t, k in segment} dt_k A) dt_t x_t^T B_t
 //       one long-K tcgen05 contraction per segment, accumulated in TMEM;
 //       writes S_seg and the segment's total log-decay to the workspace.
+//       The last CTA of each (batch, head block) to finish then passes the
+//       states across segments in order, leaving the state entering each
+//       segment in the workspace.
 //
 //   chunk_scan_kernel (every segment)
 //       folds the earlier segments' states into the state entering the
@@ -40,20 +43,23 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
 constexpr int kTargetCtas = 148;        // about one CTA per SM of a GB300 (152 SMs)
 constexpr int kSmemLimit = 226 * 1024;  // dynamic bytes; leaves room for the static mbarriers
+constexpr uint64_t kWaitNs = 100000000ull;    // a wait gives up after 0.1 s
+constexpr uint64_t kDrainNs = 20000000ull;    // the exit drain gives up after 0.02 s
 
 struct TcParams {
     const bf16 *dt;
     const float *A, *D, *init;
     void *y;
     float *fin;
-    float *seg_state;  // [b, nseg, H, P, N]
-    float *seg_tot;    // [b, nseg, H]  total dt*A of each segment
-    unsigned *status;  // bit 0: an mbarrier wait gave up
+    float *seg_state;   // [b, nseg, H, P, N]: segment-local states, then (in place) states entering segments
+    float *seg_tot;     // [b, nseg, H]  total dt*A of each segment
+    unsigned *counter;  // [b, nhb] segment-state CTAs finished (zeroed before the launch)
+    unsigned *status;   // bit 0: a wait gave up
     long long b, L, H, G;
     int hpg, nc, nseg, cps;  // cps: chunks per segment
+    int nhb;
     int y_f32;
 };
 
@@ -65,25 +71,29 @@ struct Cfg {
     static constexpr int PB = P / 64;           // 64-wide column blocks of one head's x tile
     static constexpr int X_BYTES = M * Q * 2;   // [M/64 blocks][Q rows][64]
     static constexpr int BC_BYTES = N * Q * 2;  // [N/64 blocks][Q rows][64]
-    static constexpr int STAGE_BYTES = X_BYTES + 2 * BC_BYTES;
-    static constexpr int XW_BYTES = M * Q * 2;
-    static constexpr int SBF_BYTES = M * N * 2;       // [N/64 blocks][M rows][64]
-    static constexpr int MM_BYTES = HB * Q * Q * 2;   // per head [Q/64 blocks][Q rows][64]
-    // scratch: the bf16 state copy and the low half of the scaled x during the
-    // state/inter MMAs, then the masked score matrices
-    static constexpr int SCR_BYTES = SBF_BYTES + XW_BYTES > MM_BYTES ? SBF_BYTES + XW_BYTES : MM_BYTES;
-    static constexpr int SMALL_FLOATS = 4 * HB * Q + 4 * HB;
-    static constexpr int SMALL_BYTES = SMALL_FLOATS * 4 + 128;
-    static constexpr int smem_scan(int stages) {
-        return stages * STAGE_BYTES + XW_BYTES + SCR_BYTES + SMALL_BYTES + 1024;
+    static constexpr int XW_BYTES = M * Q * 2;  // one of the hi / lo halves of w x
+    static constexpr int SBF_BYTES = M * N * 2; // [N/64 blocks][M rows][64]
+    static constexpr int MM_BYTES = HB * Q * Q * 2;  // per head [Q/64 blocks][Q rows][64]
+    // per-stage vectors: dt, cum, w, exp(cum) for each head, then exp(total)
+    static constexpr int VEC_FLOATS = 4 * HB * Q + 32;
+    static constexpr int VEC_BYTES = ((VEC_FLOATS * 4 + 1023) / 1024) * 1024;
+
+    // scan kernel: stages of (x, B, C, vectors), 1 or 2 buffers of w x, the
+    // bf16 state copy and the score matrices
+    static constexpr int SCAN_STAGE = X_BYTES + 2 * BC_BYTES + VEC_BYTES;
+    static constexpr int scan_smem(int st, int xwb) {
+        return st * SCAN_STAGE + xwb * 2 * XW_BYTES + SBF_BYTES + MM_BYTES + 1024;
     }
-    static constexpr int STAGES = smem_scan(2) <= kSmemLimit ? 2 : 1;
-    // at least 116 KB so that a single CTA (and its 512 TMEM columns) sits on an SM
-    static constexpr int SMEM_SCAN = smem_scan(STAGES) > 116 * 1024 ? smem_scan(STAGES) : 116 * 1024;
-    static constexpr bool SCAN_FITS = smem_scan(STAGES) <= kSmemLimit;
-    // segment-state kernel: two stages of (x, B) plus the scaled x
-    static constexpr int SEG_STAGE_BYTES = X_BYTES + BC_BYTES;
-    static constexpr int SMEM_SEG_BASE = 2 * SEG_STAGE_BYTES + 2 * XW_BYTES + SMALL_BYTES + 1024;
+    static constexpr int SCAN_ST = scan_smem(2, 2) <= kSmemLimit || scan_smem(2, 1) <= kSmemLimit ? 2 : 1;
+    static constexpr int SCAN_XWB = scan_smem(SCAN_ST, 2) <= kSmemLimit ? 2 : 1;
+    static constexpr int SMEM_SCAN = scan_smem(SCAN_ST, SCAN_XWB);
+    static constexpr bool SCAN_FITS = SMEM_SCAN <= kSmemLimit;
+
+    // segment-state kernel: stages of (x, B, vectors, w x hi / lo)
+    static constexpr int SEG_STAGE = X_BYTES + BC_BYTES + VEC_BYTES + 2 * XW_BYTES;
+    static constexpr int SEG_ST = 2 * SEG_STAGE + 1024 + 4096 <= kSmemLimit ? 2 : 1;
+    static constexpr int SMEM_SEG_BASE = SEG_ST * SEG_STAGE + 1024;  // + chunk totals [HB][cps]
+
     // TMEM columns of the scan kernel
     static constexpr int COL_S = 0;
     static constexpr int COL_R3 = N;                 // inter-chunk term, [M][Q]
@@ -92,35 +102,45 @@ struct Cfg {
     static constexpr bool CB_ALIAS = COL_END + Q > 512;
     static constexpr int COL_CB = CB_ALIAS ? COL_R : COL_END;  // C B^T, [Q][Q]
     static constexpr int TMEM_USED = CB_ALIAS ? COL_END : COL_END + Q;
-    static constexpr bool TMEM_FITS = TMEM_USED <= 512;
+    static constexpr bool TMEM_FITS = TMEM_USED <= 512 && !CB_ALIAS;
     static constexpr uint32_t SEG_TMEM = N < 32 ? 32 : N;
 };
 
-constexpr uint32_t kWaitPolls = 1u << 20;  // about 0.1 s of polling per wait
-
+// ---------------------------------------------------------------------------
+// waiting with a bound
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ void flag_timeout(unsigned *status) {
     if (status) atomicOr(status, 1u);
 }
 
-// Bookkeeping of asynchronous work in flight, so that a CTA that gives up
-// on a wait can still let its own copies and MMAs land (bounded) before it
-// frees TMEM and exits.
-struct Inflight {
-    int issued = 0;   // chunks whose TMA loads were issued
-    int waited = 0;   // chunks whose loads were waited for
-    bool mma = false; // a commit not yet waited for
-    uint32_t mma_phase = 0;
-};
-
-template <int STAGES>
-__device__ __forceinline__ void drain(Inflight &f, uint64_t *full_bar, uint64_t *mma_bar) {
-    for (int k = f.waited; k < f.issued; ++k)
-        mbar_wait(&full_bar[k % STAGES], (uint32_t)((k / STAGES) & 1), kWaitPolls);
-    if (f.mma) mbar_wait(mma_bar, f.mma_phase, kWaitPolls);
+// Poll `bar` for the phase of `parity`; give up after kWaitNs of wall time
+// or as soon as another role has given up (abort flag), so nothing spins
+// forever.
+__device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15) == 15) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitNs) break;
+            __nanosleep(64);
+        }
+    }
+    *abort_flag = 1;
+    return false;
 }
 
-// Inclusive scan of dt*A over one chunk for head h, by one warp.  Writes
-// cum (log-decay from the chunk start) and returns the chunk total.
+// Warp-group wait: one elected thread polls, the named barrier hands the
+// outcome (and the memory ordering of the completed phase) to the group.
+__device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                           volatile int *slot, int bar_id, int gtid, int nthreads) {
+    if (gtid == 0) *slot = wait_bounded(bar, parity, abort_flag) ? 1 : 0;
+    named_bar_sync(bar_id, nthreads);
+    return *slot != 0;
+}
+
+// Inclusive scan of dt*A over one chunk for one head, by one warp; returns
+// the chunk total.
 template <int Q>
 __device__ __forceinline__ float warp_chunk_cumsum(const float *dtv, float a, float *cum) {
     constexpr int QPL = Q / 32;
@@ -144,15 +164,36 @@ __device__ __forceinline__ float warp_chunk_cumsum(const float *dtv, float a, fl
     return __shfl_sync(0xffffffffu, tot, 31);
 }
 
+// dt of chunk c for the CTA's heads into dtv[HB][Q] (one warp; zeros for
+// heads past H).
+template <class C>
+__device__ __forceinline__ void warp_load_dt(const TcParams &prm, int b, int h0, int c, float *dtv) {
+    const int lane = threadIdx.x & 31;
+    constexpr int PER = C::HB * C::Q / 32;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int idx = lane + 32 * i;
+        const int hh = idx / C::Q, q = idx % C::Q;
+        const long long h = h0 + hh;
+        v[i] = h < prm.H ? __bfloat162float(prm.dt[((long long)b * prm.L + (long long)c * C::Q + q) * prm.H + h]) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) dtv[lane + 32 * i] = v[i];
+    __syncwarp();
+}
+
 // x tile scaled row-wise by w, split into two bf16 tiles whose sum carries
 // the product to about 2^-17 relative: hi = bf16(w x), lo = bf16(w x - hi).
 // (One bf16 rounding of w x, 2^-9 relative, is visible in the state entries
 // that a single recent token dominates.)  Works on whole 16-byte chunks of
 // the swizzled layout: a chunk stays in its row, so its scale is its row's.
-template <class C>
-__device__ __forceinline__ void build_xw(const uint8_t *xs, uint8_t *xw_hi, uint8_t *xw_lo, const float *w) {
+template <class C, int NT>
+__device__ __forceinline__ void build_xw(const uint8_t *xs, uint8_t *xw_hi, uint8_t *xw_lo, const float *w,
+                                         int gtid) {
     constexpr int CHUNKS = (C::M / 64) * C::Q * 8;
-    for (int i = threadIdx.x; i < CHUNKS; i += kThreads) {
+#pragma unroll 2
+    for (int i = gtid; i < CHUNKS; i += NT) {
         const int blk = i / (C::Q * 8);
         const int s = (i / 8) % C::Q;
         const int h = blk / C::PB;
@@ -176,238 +217,320 @@ __device__ __forceinline__ void build_xw(const uint8_t *xs, uint8_t *xw_hi, uint
     }
 }
 
-// Issue the TMA loads of chunk c: x tiles of the CTA's heads, then B (and C).
+// TMA loads of chunk c: x tiles of the CTA's heads, B, and (optionally) C.
+// Returns the bytes the loads deliver.
 template <class C>
-__device__ __forceinline__ void issue_chunk_loads(uint8_t *stage, uint64_t *bar, const CUtensorMap *mx,
-                                                  const CUtensorMap *mb, const CUtensorMap *mc, int h0, int g,
-                                                  int c, int b, bool with_c) {
-    const uint32_t bytes = C::X_BYTES + C::BC_BYTES * (with_c ? 2 : 1);
-    mbar_arrive_expect_tx(bar, bytes);
+__device__ __forceinline__ uint32_t chunk_load_bytes(bool with_c) {
+    return C::X_BYTES + C::BC_BYTES * (with_c ? 2 : 1);
+}
+
+template <class C>
+__device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint8_t *cs, uint64_t *bar,
+                                                  const CUtensorMap *mx, const CUtensorMap *mb,
+                                                  const CUtensorMap *mc, int h0, int g, int c, int b) {
 #pragma unroll
     for (int hh = 0; hh < C::HB; ++hh)
 #pragma unroll
         for (int pb = 0; pb < C::PB; ++pb)
-            tma_load_4d(stage + (hh * C::PB + pb) * (C::Q * 128), mx, bar, pb * 64, h0 + hh, c * C::Q, b);
-    uint8_t *sb = stage + C::X_BYTES;
+            tma_load_4d(xs + (hh * C::PB + pb) * (C::Q * 128), mx, bar, pb * 64, h0 + hh, c * C::Q, b);
 #pragma unroll
-    for (int nb = 0; nb < C::N / 64; ++nb) tma_load_4d(sb + nb * (C::Q * 128), mb, bar, nb * 64, g, c * C::Q, b);
-    if (with_c) {
-        uint8_t *sc = sb + C::BC_BYTES;
+    for (int nb = 0; nb < C::N / 64; ++nb) tma_load_4d(bs + nb * (C::Q * 128), mb, bar, nb * 64, g, c * C::Q, b);
+    if (cs)
 #pragma unroll
         for (int nb = 0; nb < C::N / 64; ++nb)
-            tma_load_4d(sc + nb * (C::Q * 128), mc, bar, nb * 64, g, c * C::Q, b);
-    }
+            tma_load_4d(cs + nb * (C::Q * 128), mc, bar, nb * 64, g, c * C::Q, b);
 }
 
 // ===========================================================================
-// Segment local states: S_seg for segments 0 .. nseg-2.
+// Segment-local states (segments 0 .. nseg-2), then -- in the last CTA of
+// each (batch, head block) to finish -- the pass of states across segments.
+//   warp 0     : TMA loads of x, B; dt and the segment weights
+//                w_t = exp(sum_{k>t in segment} dt_k A) dt_t
+//   warp 1     : tcgen05.mma S += (w o x)^T B into TMEM
+//   warps 4-7  : w o x as bf16 hi + lo operand tiles; TMEM -> HBM at the end
 // ===========================================================================
+constexpr int kSegThreads = 256;
+
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kSegThreads, 1)
     seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb, TcParams prm) {
+    constexpr int ST = C::SEG_ST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *stages = smem;
-    uint8_t *xw = stages + 2 * C::SEG_STAGE_BYTES;
-    uint8_t *xw_lo = xw + C::XW_BYTES;
-    float *small = reinterpret_cast<float *>(xw_lo + C::XW_BYTES);
-    float *dtv = small;               // [HB][Q]
-    float *cum = dtv + C::HB * C::Q;  // [HB][Q]
-    float *w = cum + C::HB * C::Q;    // [HB][Q]
-    float *tail = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(small) + C::SMALL_BYTES);  // [HB][cps]
-    __shared__ uint64_t full_bar[2], mma_bar;
+    float *tot_s = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE);  // [HB][cps]
+    __shared__ uint64_t full_bar[2], empty_bar[2], xw_bar[2], done_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_sh;
+    __shared__ volatile int slot[4];
+    __shared__ int last_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, hblk = blockIdx.y, b = blockIdx.z;
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
     const int c0 = seg * prm.cps;
-    const int c1 = min(prm.nc, c0 + prm.cps);
-    const int nch = c1 - c0;
-    const long long L = prm.L, H = prm.H;
+    const int nch = min(prm.nc, c0 + prm.cps) - c0;
+    const long long H = prm.H;
+    auto stage_x = [&](int s) { return smem + s * C::SEG_STAGE; };
+    auto stage_b = [&](int s) { return smem + s * C::SEG_STAGE + C::X_BYTES; };
+    auto stage_v = [&](int s) { return reinterpret_cast<float *>(smem + s * C::SEG_STAGE + C::X_BYTES + C::BC_BYTES); };
+    auto stage_xh = [&](int s) { return smem + s * C::SEG_STAGE + C::X_BYTES + C::BC_BYTES + C::VEC_BYTES; };
+    auto stage_xl = [&](int s) { return stage_xh(s) + C::XW_BYTES; };
 
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(&tmem_base_sh, C::SEG_TMEM);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&full_bar[0], 1);
-        mbar_init(&full_bar[1], 1);
-        mbar_init(&mma_bar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+            mbar_init(&xw_bar[i], 1);
+        }
+        mbar_init(&done_bar, 1);
+        mbar_init(&drain_bar, 1);
         fence_mbar_init();
+        abort_sh = 0;
         prefetch_tmap(&mx);
         prefetch_tmap(&mb);
     }
-    // per-chunk totals of dt*A for every chunk of the segment, then the
-    // suffix sums: tail[h][k] = sum of the totals of chunks after k.
-    for (int item = warp; item < C::HB * nch; item += kThreads / 32) {
-        const int hh = item / nch, k = item % nch;
-        const long long h = h0 + hh;
-        float s = 0.f;
-        if (h < H)
-            for (int q = lane; q < C::Q; q += 32)
-                s += __bfloat162float(prm.dt[((long long)b * L + (long long)(c0 + k) * C::Q + q) * H + h]);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) tail[hh * prm.cps + k] = h < H ? s * prm.A[h] : 0.f;
+    int nload[2] = {0, 0};  // TMA loads issued per stage (producer lane 0)
+    // chunk totals of dt*A over the segment: groups of 8 threads reduce one
+    // (head, chunk) pair each, in a fixed order (bitwise reproducible)
+    {
+        // the loop bound is the same for every lane of a warp (j0 steps over
+        // whole warps' worth of groups), so the shuffles see a full warp
+        const int grp = tid >> 3, gl = tid & 7;
+        const int npair = C::HB * nch;
+        for (int j0 = (tid >> 5) * 4; j0 < npair; j0 += kSegThreads / 8) {
+            const int j = j0 + (grp & 3);
+            const bool valid = j < npair;
+            const int hh = valid ? j / nch : 0, k = valid ? j % nch : 0;
+            const long long h = h0 + hh;
+            float sum = 0.f;
+            if (valid && h < H)
+#pragma unroll 4
+                for (int q = gl; q < C::Q; q += 8)
+                    sum += __bfloat162float(prm.dt[((long long)b * prm.L + (long long)(c0 + k) * C::Q + q) * H + h]);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if (valid && gl == 0) tot_s[hh * prm.cps + k] = h < H ? sum * prm.A[h] : 0.f;
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // suffix sums: tot_s[h][k] <- sum of the totals of the chunks after k
     if (tid < C::HB) {
         float run = 0.f;
         for (int k = nch - 1; k >= 0; --k) {
-            const float t = tail[tid * prm.cps + k];
-            tail[tid * prm.cps + k] = run;
+            const float t = tot_s[tid * prm.cps + k];
+            tot_s[tid * prm.cps + k] = run;
             run += t;
         }
         const long long h = h0 + tid;
         if (h < H) prm.seg_tot[((long long)b * prm.nseg + seg) * H + h] = run;
     }
-    const uint32_t tmem = tmem_base_sh;
-    __shared__ int abort_sh;
-    if (tid == 0) abort_sh = 0;
-    Inflight fl;  // meaningful in thread 0, which issues all async work
-    if (tid == 0) {
-        issue_chunk_loads<C>(stages, &full_bar[0], &mx, &mb, nullptr, h0, g, c0, b, false);
-        fl.issued = 1;
-    }
-
-    for (int it = 0; it < nch; ++it) {
-        const int c = c0 + it;
-        const int st = it & 1;
-        uint8_t *stage = stages + st * C::SEG_STAGE_BYTES;
-        // dt of this chunk
-        for (int i = tid; i < C::HB * C::Q; i += kThreads) {
-            const int hh = i / C::Q, q = i % C::Q;
-            const long long h = h0 + hh;
-            dtv[i] = h < H ? __bfloat162float(prm.dt[((long long)b * L + (long long)c * C::Q + q) * H + h]) : 0.f;
-        }
-        __syncthreads();
-        if (abort_sh) break;
-        if (warp < C::HB) {
-            const long long h = h0 + warp;
-            const float a = h < H ? prm.A[h] : 0.f;
-            float *cw = cum + warp * C::Q;
-            const float total = warp_chunk_cumsum<C::Q>(dtv + warp * C::Q, a, cw);
-            __syncwarp();
-            const float after = tail[warp * prm.cps + it];
-            for (int q = lane; q < C::Q; q += 32)
-                w[warp * C::Q + q] = expf(after + total - cw[q]) * dtv[warp * C::Q + q];
-        }
-        // the previous MMA has finished reading xw and the other stage
-        // (waited at the end of the last iteration): prefetch the next chunk
-        if (tid == 0 && it + 1 < nch) {
-            issue_chunk_loads<C>(stages + (st ^ 1) * C::SEG_STAGE_BYTES, &full_bar[st ^ 1], &mx, &mb, nullptr,
-                                 h0, g, c + 1, b, false);
-            fl.issued = it + 2;
-        }
-        if (!mbar_wait(&full_bar[st], (it >> 1) & 1, kWaitPolls)) abort_sh = 1;
-        else if (tid == 0) fl.waited = it + 1;
-        __syncthreads();
-        if (abort_sh) break;
-        build_xw<C>(stage, xw, xw_lo, w);
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t idesc = idesc_bf16(C::M, C::N, true, true);
-            const uint32_t a0 = smem_u32(xw), a1 = smem_u32(xw_lo), b0 = smem_u32(stage + C::X_BYTES);
-#pragma unroll
-            for (int ks = 0; ks < C::Q / 16; ++ks)
-                mma_bf16(tmem, sdesc(a0 + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
-                         idesc, (it | ks) != 0);
-#pragma unroll
-            for (int ks = 0; ks < C::Q / 16; ++ks)
-                mma_bf16(tmem, sdesc(a1 + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
-                         idesc, true);
-            mma_commit(&mma_bar);
-            fl.mma = true;
-        }
-        if (!mbar_wait(&mma_bar, fl.mma_phase, kWaitPolls)) abort_sh = 1;
-        else if (tid == 0) fl.mma = false;
-        fl.mma_phase ^= 1;
-        tc_fence_after();
-    }
     __syncthreads();
-    if (abort_sh) {
-        if (tid == 0) {
-            flag_timeout(prm.status);
-            drain<2>(fl, full_bar, &mma_bar);
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, C::SEG_TMEM);
-        return;
-    }
-    // write the segment state: row r = (head, p) of TMEM lane r
-    if (warp < 4) {
-        const int r = warp * 32 + lane;
-        const int hh = r / C::P, p = r % C::P;
-        const long long h = h0 + hh;
-        float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + h) * C::P + p) * C::N;
-#pragma unroll 1
-        for (int n0 = 0; n0 < C::N; n0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + n0, v);
-            tmem_ld_wait();
-            if (h < H)
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0) {
+        // ---------------- producer: TMA + segment weights ----------------
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % ST;
+            const int c = c0 + it;
+            if (it >= ST) {
+                int ok = lane == 0 ? (wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            }
+            if (lane == 0) {
+                mbar_expect_tx(&full_bar[s], chunk_load_bytes<C>(false));
+                issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c, b);
+                ++nload[s];
+            }
+            float *vec = stage_v(s);
+            float *dtv = vec, *cum = vec + C::HB * C::Q, *w = vec + 2 * C::HB * C::Q;
+            warp_load_dt<C>(prm, b, h0, c, dtv);
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            for (int hh = 0; hh < C::HB; ++hh) {
+                const long long h = h0 + hh;
+                const float a = h < H ? prm.A[h] : 0.f;
+                const float total = warp_chunk_cumsum<C::Q>(dtv + hh * C::Q, a, cum + hh * C::Q);
+                __syncwarp();
+                const float after = tot_s[hh * prm.cps + it];
+                for (int q = lane; q < C::Q; q += 32)
+                    w[hh * C::Q + q] = expf(after + total - cum[hh * C::Q + q]) * dtv[hh * C::Q + q];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_bar[s]);
         }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(C::M, C::N, true, true);
+            for (int it = 0; it < nch; ++it) {
+                const int s = it % ST;
+                if (!wait_bounded(&xw_bar[s], (it / ST) & 1, &abort_sh)) break;
+                tc_fence_after();
+                const uint32_t ah = smem_u32(stage_xh(s)), al = smem_u32(stage_xl(s)), b0 = smem_u32(stage_b(s));
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16(tmem, sdesc(ah + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
+                             idesc, (it | ks) != 0);
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16(tmem, sdesc(al + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
+                             idesc, true);
+                mma_commit(&empty_bar[s]);
+            }
+            mma_commit(&done_bar);  // completes once every MMA above has
+        }
+    } else if (warp >= 4) {
+        // ---------------- w o x operand builders ----------------
+        const int gtid = tid - 128;
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % ST;
+            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[0], 1, gtid, 128)) break;
+            const float *w = stage_v(s) + 2 * C::HB * C::Q;
+            build_xw<C, 128>(stage_x(s), stage_xh(s), stage_xl(s), w, gtid);
+            fence_async_smem();
+            named_bar_sync(1, 128);
+            if (gtid == 0) mbar_arrive(&xw_bar[s]);
+        }
+        // segment state: TMEM lane r = row (head, p)
+        if (group_wait(&done_bar, 0, &abort_sh, &slot[1], 1, gtid, 128)) {
+            tc_fence_after();
+            const int q4 = warp & 3;
+            const int r = q4 * 32 + lane;
+            const int hh = r / C::P, p = r % C::P;
+            const long long h = h0 + hh;
+            float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + h) * C::P + p) * C::N;
+#pragma unroll 1
+            for (int n0 = 0; n0 < C::N; n0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + n0, v);
+                tmem_ld_wait();
+                if (h < H)
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+        }
+    }
+    // let this CTA's own copies and MMAs land (they normally have) before
+    // TMEM is freed and the CTA exits
+    if (warp == 0 && lane == 0)
+        for (int s = 0; s < ST; ++s)
+            if (nload[s] > 0) mbar_wait(&full_bar[s], (uint32_t)((nload[s] - 1) & 1), kDrainNs);
+    if (warp == 1 && lane == 0) {
+        mma_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, kDrainNs);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, C::SEG_TMEM);
+    if (warp == 1) tmem_dealloc(tmem, C::SEG_TMEM);
+    if (abort_sh) {
+        if (tid == 0) flag_timeout(prm.status);
+        return;
+    }
+
+    // ---------------- pass of states across segments ----------------
+    // The last of the unit's nseg-1 CTAs to finish folds the segment states
+    // in order, in place: slot s becomes the state entering segment s + 1.
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(prm.counter + (long long)b * prm.nhb + hblk, 1u);
+        last_sh = prev == (unsigned)(prm.nseg - 2);
+    }
+    __syncthreads();
+    if (!last_sh) return;
+    __threadfence();
+    constexpr int E4 = C::M * C::N / 4;  // float4s of the CTA's (head, p, n) block
+    for (int e = tid; e < E4; e += kSegThreads) {
+        const int r = (e * 4) / C::N, n = (e * 4) % C::N;
+        const int hh = r / C::P, p = r % C::P;
+        const long long h = h0 + hh;
+        if (h >= H) continue;
+        float4 acc = prm.init ? *reinterpret_cast<const float4 *>(prm.init + ((b * H + h) * C::P + p) * C::N + n)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < prm.nseg - 1; ++sp) {
+            const float e_sp = expf(__ldcg(prm.seg_tot + ((long long)b * prm.nseg + sp) * H + h));
+            float4 *slot_p = reinterpret_cast<float4 *>(
+                prm.seg_state + ((((long long)b * prm.nseg + sp) * H + h) * C::P + p) * C::N + n);
+            const float4 v = __ldcg(slot_p);
+            acc.x = fmaf(e_sp, acc.x, v.x);
+            acc.y = fmaf(e_sp, acc.y, v.y);
+            acc.z = fmaf(e_sp, acc.z, v.z);
+            acc.w = fmaf(e_sp, acc.w, v.w);
+            __stcg(slot_p, acc);
+        }
+    }
 }
 
 // ===========================================================================
-// Chunk scan with the state carried in TMEM.
+// Chunk scan with the state carried in TMEM (every segment).
+//   warp 0     : TMA loads of x, B, C; dt, cumulative decay, w, exp(cum)
+//   warp 1     : tcgen05.mma issue (C B^T; S C^T; S += (w x)^T B; X^T M^T)
+//   warps 4-7  : w o x operand tiles; bf16 state copy and S *= exp(total)
+//   warps 8-11 : masked, decayed score matrices M_h (bf16) from C B^T
+//   warps 12-15: y = intra + exp(cum) inter + D x, straight to HBM
 // ===========================================================================
+constexpr int kScanThreads = 512;
+
 template <class C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
                       const __grid_constant__ CUtensorMap mc, TcParams prm) {
+    constexpr int ST = C::SCAN_ST;
+    constexpr int XWB = C::SCAN_XWB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *stages = smem;
-    uint8_t *xw = stages + C::STAGES * C::STAGE_BYTES;
-    uint8_t *scr = xw + C::XW_BYTES;  // bf16 state copy + low half of w x, then the masked score matrices
-    uint8_t *xw_lo = scr + C::SBF_BYTES;
-    float *small = reinterpret_cast<float *>(scr + C::SCR_BYTES);
-    float *dtv = small;                 // [HB][Q]
-    float *cum = dtv + C::HB * C::Q;    // [HB][Q]
-    float *w = cum + C::HB * C::Q;      // [HB][Q]
-    float *ecum = w + C::HB * C::Q;     // [HB][Q]
-    float *decay = ecum + C::HB * C::Q; // [HB]
-    __shared__ uint64_t full_bar[2], mma_bar;
+    uint8_t *xw_base = smem + ST * C::SCAN_STAGE;
+    uint8_t *sbf = xw_base + XWB * 2 * C::XW_BYTES;
+    uint8_t *mm = sbf + C::SBF_BYTES;
+    __shared__ uint64_t full_bar[2], empty_bar[2];
+    __shared__ uint64_t cb_bar, mask_bar, wg1_bar, state_bar, y_bar, free_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_sh;
+    __shared__ volatile int slot[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, hblk = blockIdx.y, b = blockIdx.z;
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
     const int c0 = seg * prm.cps;
-    const int c1 = min(prm.nc, c0 + prm.cps);
-    const int nch = c1 - c0;
+    const int nch = min(prm.nc, c0 + prm.cps) - c0;
     const long long L = prm.L, H = prm.H;
-    const int quarter = warp & 3;            // TMEM lane quarter this warp may access
-    const int row = quarter * 32 + lane;     // (head, p) row for warps 0-3 / 4-7
-    const int rh = row / C::P, rp = row % C::P;
-    const long long hrow = h0 + rh;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
+    auto stage_b = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES; };
+    auto stage_c = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + C::BC_BYTES; };
+    auto stage_v = [&](int s) {
+        return reinterpret_cast<float *>(smem + s * C::SCAN_STAGE + C::X_BYTES + 2 * C::BC_BYTES);
+    };
+    // per-stage vectors: dtv [HB][Q], cum [HB][Q], w [HB][Q], ecum [HB][Q], decay [HB]
+    auto xw_hi = [&](int i) { return xw_base + i * 2 * C::XW_BYTES; };
+    auto xw_lo = [&](int i) { return xw_base + i * 2 * C::XW_BYTES + C::XW_BYTES; };
 
-    if (warp == 0) {
+    if (warp == 1) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&full_bar[0], 1);
-        mbar_init(&full_bar[1], 1);
-        mbar_init(&mma_bar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], 1);
+        }
+        mbar_init(&cb_bar, 1);
+        mbar_init(&mask_bar, 1);
+        mbar_init(&wg1_bar, 1);
+        mbar_init(&state_bar, 1);
+        mbar_init(&y_bar, 1);
+        mbar_init(&free_bar, 1);
+        mbar_init(&drain_bar, 1);
         fence_mbar_init();
+        abort_sh = 0;
         prefetch_tmap(&mx);
         prefetch_tmap(&mb);
         prefetch_tmap(&mc);
@@ -416,160 +539,214 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
-    __shared__ int abort_sh;
-    if (tid == 0) abort_sh = 0;
-    Inflight fl;  // meaningful in thread 0, which issues all async work
-    if (tid == 0) {
-        issue_chunk_loads<C>(stages, &full_bar[0], &mx, &mb, &mc, h0, g, c0, b, true);
-        fl.issued = 1;
-    }
+    int nload[2] = {0, 0};  // TMA loads issued per stage (producer lane 0)
+    const int q4 = warp & 3;                  // TMEM lane quarter of this warp
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
 
-    // state entering the segment: fold the earlier segments' states
-    if (warp < 4) {
-        const float *init_row = (prm.init && hrow < H) ? prm.init + (((long long)b * H + hrow) * C::P + rp) * C::N : nullptr;
-#pragma unroll 1
-        for (int n0 = 0; n0 < C::N; n0 += 16) {
-            float v[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = init_row ? init_row[n0 + j] : 0.f;
-            if (hrow < H)
-                for (int sp = 0; sp < seg; ++sp) {
-                    const float e = expf(prm.seg_tot[((long long)b * prm.nseg + sp) * H + hrow]);
-                    const float *src =
-                        prm.seg_state + ((((long long)b * prm.nseg + sp) * H + hrow) * C::P + rp) * C::N + n0;
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const float4 s4 = *reinterpret_cast<const float4 *>(src + j);
-                        v[j] = fmaf(e, v[j], s4.x);
-                        v[j + 1] = fmaf(e, v[j + 1], s4.y);
-                        v[j + 2] = fmaf(e, v[j + 2], s4.z);
-                        v[j + 3] = fmaf(e, v[j + 3], s4.w);
-                    }
-                }
-            tmem_st16(tmem + lane_off + C::COL_S + n0, v);
-        }
-        tmem_st_wait();
-    }
-    const float dh_row = (prm.D && hrow < H) ? prm.D[hrow] : 0.f;
-
-    for (int it = 0; it < nch; ++it) {
-        const int c = c0 + it;
-        const int st = C::STAGES == 2 ? (it & 1) : 0;
-        const uint32_t full_parity = C::STAGES == 2 ? ((it >> 1) & 1) : (it & 1);
-        uint8_t *stage = stages + st * C::STAGE_BYTES;
-        uint8_t *xs = stage;
-        uint8_t *bs = stage + C::X_BYTES;
-        uint8_t *cs = bs + C::BC_BYTES;
-        if (C::STAGES == 2 && tid == 0 && it + 1 < nch) {
-            issue_chunk_loads<C>(stages + (st ^ 1) * C::STAGE_BYTES, &full_bar[st ^ 1], &mx, &mb, &mc, h0, g, c + 1,
-                                 b, true);
-            fl.issued = it + 2;
-        }
-        for (int i = tid; i < C::HB * C::Q; i += kThreads) {
-            const int hh = i / C::Q, q = i % C::Q;
-            const long long h = h0 + hh;
-            dtv[i] = h < H ? __bfloat162float(prm.dt[((long long)b * L + (long long)c * C::Q + q) * H + h]) : 0.f;
-        }
-        __syncthreads();
-        // (1) cumulative decay of each head
-        if (warp < C::HB) {
-            const long long h = h0 + warp;
-            const float a = h < H ? prm.A[h] : 0.f;
-            float *cw = cum + warp * C::Q;
-            const float total = warp_chunk_cumsum<C::Q>(dtv + warp * C::Q, a, cw);
-            __syncwarp();
-            for (int q = lane; q < C::Q; q += 32) {
-                w[warp * C::Q + q] = expf(total - cw[q]) * dtv[warp * C::Q + q];
-                ecum[warp * C::Q + q] = expf(cw[q]);
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % ST;
+            const int c = c0 + it;
+            if (it >= ST) {
+                int ok = lane == 0 ? (wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
-            if (lane == 0) decay[warp] = expf(total);
-        }
-        if (!mbar_wait(&full_bar[st], full_parity, kWaitPolls)) abort_sh = 1;
-        else if (tid == 0) fl.waited = it + 1;
-        __syncthreads();
-        if (abort_sh) break;
-        // (2) scaled x for the state update; bf16 copy of the entering state
-        //     (operand of S C^T), then S *= exp(chunk total) in place
-        build_xw<C>(xs, xw, xw_lo, w);
-        if (warp < 4) {
-            const float dec = decay[rh];
-#pragma unroll 1
-            for (int n0 = 0; n0 < C::N; n0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
-                tmem_ld_wait();
-                uint8_t *dst = scr + (n0 / 64) * (C::M * 128);
+            if (lane == 0) {
+                mbar_expect_tx(&full_bar[s], chunk_load_bytes<C>(true));
+                issue_chunk_loads<C>(stage_x(s), stage_b(s), stage_c(s), &full_bar[s], &mx, &mb, &mc, h0, g, c, b);
+                ++nload[s];
+            }
+            float *vec = stage_v(s);
+            float *dtv = vec, *cum = vec + C::HB * C::Q, *w = vec + 2 * C::HB * C::Q, *ecum = vec + 3 * C::HB * C::Q;
+            float *decay = vec + 4 * C::HB * C::Q;
+            warp_load_dt<C>(prm, b, h0, c, dtv);
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int col = (n0 % 64) + jj * 8;
-                    uint4 pk;
-                    pk.x = pack_bf16x2(v[jj * 8 + 0], v[jj * 8 + 1]);
-                    pk.y = pack_bf16x2(v[jj * 8 + 2], v[jj * 8 + 3]);
-                    pk.z = pack_bf16x2(v[jj * 8 + 4], v[jj * 8 + 5]);
-                    pk.w = pack_bf16x2(v[jj * 8 + 6], v[jj * 8 + 7]);
-                    *reinterpret_cast<uint4 *>(dst + swz128(row, col)) = pk;
+            for (int hh = 0; hh < C::HB; ++hh) {
+                const long long h = h0 + hh;
+                const float a = h < H ? prm.A[h] : 0.f;
+                const float total = warp_chunk_cumsum<C::Q>(dtv + hh * C::Q, a, cum + hh * C::Q);
+                __syncwarp();
+                for (int q = lane; q < C::Q; q += 32) {
+                    const float cq = cum[hh * C::Q + q];
+                    w[hh * C::Q + q] = expf(total - cq) * dtv[hh * C::Q + q];
+                    ecum[hh * C::Q + q] = expf(cq);
                 }
+                if (lane == 0) decay[hh] = expf(total);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full_bar[s]);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t id_cb = idesc_bf16(C::Q, C::Q, false, false);
+            const uint32_t id_inter = idesc_bf16(C::M, C::Q, false, false);
+            const uint32_t id_state = idesc_bf16(C::M, C::N, true, true);
+            const uint32_t id_intra = idesc_bf16(C::M, C::Q, true, false);
+            for (int it = 0; it < nch; ++it) {
+                const int s = it % ST;
+                const int xb = XWB == 2 ? (it & 1) : 0;
+                const uint32_t sx = smem_u32(stage_x(s)), sb = smem_u32(stage_b(s)), sc = smem_u32(stage_c(s));
+                // C B^T: needs the chunk's tiles and the previous scores consumed
+                if (!wait_bounded(&full_bar[s], (it / ST) & 1, &abort_sh)) break;
+                if (it > 0 && !wait_bounded(&mask_bar, (it - 1) & 1, &abort_sh)) break;
+                tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] *= dec;
-                tmem_st16(tmem + lane_off + C::COL_S + n0, v);
+                for (int ks = 0; ks < C::N / 16; ++ks) {
+                    const uint32_t koff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
+                    mma_bf16(tmem + C::COL_CB, sdesc(sc + koff, 16, 1024), sdesc(sb + koff, 16, 1024), id_cb, ks > 0);
+                }
+                mma_commit(&cb_bar);
+                // S C^T and S += (w x)^T B: need the bf16 state copy, the scaled
+                // state and w x (warps 4-7), and the last epilogue done with TMEM
+                if (!wait_bounded(&wg1_bar, it & 1, &abort_sh)) break;
+                if (it > 0 && !wait_bounded(&free_bar, (it - 1) & 1, &abort_sh)) break;
+                tc_fence_after();
+                const uint32_t ss = smem_u32(sbf);
+#pragma unroll
+                for (int ks = 0; ks < C::N / 16; ++ks) {
+                    const uint32_t aoff = (ks / 4) * (C::M * 128) + (ks % 4) * 32;
+                    const uint32_t boff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
+                    mma_bf16(tmem + C::COL_R3, sdesc(ss + aoff, 16, 1024), sdesc(sc + boff, 16, 1024), id_inter,
+                             ks > 0);
+                }
+                const uint32_t swh = smem_u32(xw_hi(xb)), swl = smem_u32(xw_lo(xb));
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16(tmem + C::COL_S, sdesc(swh + ks * 2048, C::Q * 128, 1024),
+                             sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16(tmem + C::COL_S, sdesc(swl + ks * 2048, C::Q * 128, 1024),
+                             sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
+                mma_commit(&state_bar);
+                // X^T M_h^T per head: needs the score matrices (warps 8-11)
+                if (!wait_bounded(&mask_bar, it & 1, &abort_sh)) break;
+                tc_fence_after();
+                const uint32_t sm = smem_u32(mm);
+#pragma unroll
+                for (int hh = 0; hh < C::HB; ++hh)
+#pragma unroll
+                    for (int ks = 0; ks < C::Q / 16; ++ks) {
+                        const uint32_t boff = hh * (C::Q * C::Q * 2) + (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
+                        mma_bf16(tmem + C::COL_R + hh * C::Q, sdesc(sx + ks * 2048, C::Q * 128, 1024),
+                                 sdesc(sm + boff, 16, 1024), id_intra, ks > 0);
+                    }
+                mma_commit(&y_bar);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------- w x operands; state copy and decay ----------------
+        const int gtid = tid - 128;
+        const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
+        const long long hrow = h0 + rh;
+        // state entering the segment
+        {
+            const float *src = nullptr;
+            if (seg > 0)
+                src = prm.seg_state + ((((long long)b * prm.nseg + (seg - 1)) * H + hrow) * C::P + rp) * C::N;
+            else if (prm.init)
+                src = prm.init + (((long long)b * H + hrow) * C::P + rp) * C::N;
+            if (hrow >= H) src = nullptr;
+#pragma unroll 1
+            for (int n0 = 0; n0 < C::N; n0 += 32) {
+                float v0[16], v1[16];
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const float4 a = src ? __ldcg(reinterpret_cast<const float4 *>(src + n0 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 c2 = src ? __ldcg(reinterpret_cast<const float4 *>(src + n0 + 16 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v0[j] = a.x; v0[j + 1] = a.y; v0[j + 2] = a.z; v0[j + 3] = a.w;
+                    v1[j] = c2.x; v1[j + 1] = c2.y; v1[j + 2] = c2.z; v1[j + 3] = c2.w;
+                }
+                tmem_st16(tmem + lane_off + C::COL_S + n0, v0);
+                tmem_st16(tmem + lane_off + C::COL_S + n0 + 16, v1);
             }
             tmem_st_wait();
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // (3) C B^T, the inter-chunk term S C^T, and S += (w o x)^T B
-        if (tid == 0) {
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % ST;
+            const int xb = XWB == 2 ? (it & 1) : 0;
+            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[0], 1, gtid, 128)) break;
+            const float *vec = stage_v(s);
+            if (XWB == 1 && it > 0) {
+                if (!group_wait(&state_bar, (it - 1) & 1, &abort_sh, &slot[1], 1, gtid, 128)) break;
+            }
+            build_xw<C, 128>(stage_x(s), xw_hi(xb), xw_lo(xb), vec + 2 * C::HB * C::Q, gtid);
+            if (XWB == 2 && it > 0) {
+                if (!group_wait(&state_bar, (it - 1) & 1, &abort_sh, &slot[1], 1, gtid, 128)) break;
+            }
             tc_fence_after();
-            const uint32_t sx = smem_u32(xs), sb = smem_u32(bs), sc = smem_u32(cs), ss = smem_u32(scr);
-            const uint32_t sw = smem_u32(xw);
-            const uint32_t id_cb = idesc_bf16(C::Q, C::Q, false, false);
-#pragma unroll
-            for (int ks = 0; ks < C::N / 16; ++ks) {
-                const uint32_t koff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                mma_bf16(tmem + C::COL_CB, sdesc(sc + koff, 16, 1024), sdesc(sb + koff, 16, 1024), id_cb, ks > 0);
-            }
-            const uint32_t id_inter = idesc_bf16(C::M, C::Q, false, false);
-#pragma unroll
-            for (int ks = 0; ks < C::N / 16; ++ks) {
-                const uint32_t aoff = (ks / 4) * (C::M * 128) + (ks % 4) * 32;
-                const uint32_t boff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                mma_bf16(tmem + C::COL_R3, sdesc(ss + aoff, 16, 1024), sdesc(sc + boff, 16, 1024), id_inter, ks > 0);
-            }
-            const uint32_t id_state = idesc_bf16(C::M, C::N, true, true);
-            const uint32_t swl = smem_u32(xw_lo);
-#pragma unroll
-            for (int ks = 0; ks < C::Q / 16; ++ks)
-                mma_bf16(tmem + C::COL_S, sdesc(sw + ks * 2048, C::Q * 128, 1024),
-                         sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
-#pragma unroll
-            for (int ks = 0; ks < C::Q / 16; ++ks)
-                mma_bf16(tmem + C::COL_S, sdesc(swl + ks * 2048, C::Q * 128, 1024),
-                         sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
-            (void)sx;
-            mma_commit(&mma_bar);
-            fl.mma = true;
-        }
-        if (!mbar_wait(&mma_bar, fl.mma_phase, kWaitPolls)) abort_sh = 1;
-        else if (tid == 0) fl.mma = false;
-        fl.mma_phase ^= 1;
-        tc_fence_after();
-        __syncthreads();
-        if (abort_sh) break;
-        // (4) masked, decayed score matrix of each head, bf16, into scr
-        {
-            const int half = warp >> 2;  // warps 0-3: first half of the s columns, 4-7: second half
-            int t;
-            bool active;
-            if (C::Q == 64) {
-                t = quarter * 16 + lane;  // M = 64 accumulator: 16 rows per lane quarter
-                active = lane < 16;
-            } else {
-                t = quarter * 32 + lane;
-                active = true;
-            }
+            const float dec = vec[4 * C::HB * C::Q + rh];
 #pragma unroll 1
-            for (int s0 = half * (C::Q / 2); s0 < (half + 1) * (C::Q / 2); s0 += 16) {
+            for (int n0 = 0; n0 < C::N; n0 += 32) {
+                float v0[16], v1[16];
+                tmem_ld16(tmem + lane_off + C::COL_S + n0, v0);
+                tmem_ld16(tmem + lane_off + C::COL_S + n0 + 16, v1);
+                tmem_ld_wait();
+                uint8_t *dst = sbf + (n0 / 64) * (C::M * 128);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float *v = jj < 2 ? v0 + jj * 8 : v1 + (jj - 2) * 8;
+                    uint4 pk;
+                    pk.x = pack_bf16x2(v[0], v[1]);
+                    pk.y = pack_bf16x2(v[2], v[3]);
+                    pk.z = pack_bf16x2(v[4], v[5]);
+                    pk.w = pack_bf16x2(v[6], v[7]);
+                    *reinterpret_cast<uint4 *>(dst + swz128(row, (n0 % 64) + jj * 8)) = pk;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    v0[j] *= dec;
+                    v1[j] *= dec;
+                }
+                tmem_st16(tmem + lane_off + C::COL_S + n0, v0);
+                tmem_st16(tmem + lane_off + C::COL_S + n0 + 16, v1);
+            }
+            fence_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
+            named_bar_sync(1, 128);
+            if (gtid == 0) mbar_arrive(&wg1_bar);
+        }
+        // final state after the segment's last chunk
+        if (seg == prm.nseg - 1 && prm.fin) {  // (a uniform test: group_wait handles an abort)
+            if (group_wait(&state_bar, (nch - 1) & 1, &abort_sh, &slot[2], 1, gtid, 128)) {
+                tc_fence_after();
+                float *dst = prm.fin + (((long long)b * H + hrow) * C::P + rp) * C::N;
+#pragma unroll 1
+                for (int n0 = 0; n0 < C::N; n0 += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
+                    tmem_ld_wait();
+                    if (hrow < H)
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
+            }
+        }
+    } else if (warp >= 8 && warp < 12) {
+        // ---------------- masked, decayed score matrices ----------------
+        const int gtid = tid - 256;
+        int t;
+        bool active;
+        if (C::Q == 64) {  // M = 64 accumulator: rows 16 q4 .. 16 q4 + 15 in lanes 0-15
+            t = q4 * 16 + lane;
+            active = lane < 16;
+        } else {
+            t = q4 * 32 + lane;
+            active = true;
+        }
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % ST;
+            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[3], 2, gtid, 128)) break;
+            if (!group_wait(&cb_bar, it & 1, &abort_sh, &slot[4], 2, gtid, 128)) break;
+            tc_fence_after();
+            const float *vec = stage_v(s);
+            const float *dtv = vec, *cum = vec + C::HB * C::Q;
+#pragma unroll 1
+            for (int s0 = 0; s0 < C::Q; s0 += 16) {
                 float cb[16];
                 tmem_ld16(tmem + lane_off + C::COL_CB + s0, cb);
                 tmem_ld_wait();
@@ -577,15 +754,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int hh = 0; hh < C::HB; ++hh) {
                         const float ct = cum[hh * C::Q + t];
-                        uint8_t *dst = scr + hh * (C::Q * C::Q * 2) + (s0 / 64) * (C::Q * 128);
+                        uint8_t *dst = mm + hh * (C::Q * C::Q * 2) + (s0 / 64) * (C::Q * 128);
 #pragma unroll
                         for (int jj = 0; jj < 2; ++jj) {
                             float m[8];
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
-                                const int s = s0 + jj * 8 + j;
-                                m[j] = (s <= t) ? cb[jj * 8 + j] * __expf(ct - cum[hh * C::Q + s]) * dtv[hh * C::Q + s]
-                                                : 0.f;
+                                const int sc = s0 + jj * 8 + j;
+                                m[j] = (sc <= t) ? cb[jj * 8 + j] * __expf(ct - cum[hh * C::Q + sc]) * dtv[hh * C::Q + sc]
+                                                 : 0.f;
                             }
                             uint4 pk;
                             pk.x = pack_bf16x2(m[0], m[1]);
@@ -597,40 +774,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(2, 128);
+            if (gtid == 0) mbar_arrive(&mask_bar);
         }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // (5) intra-chunk term per head: Y_h^T = X^T M_h^T
-        if (tid == 0) {
+    } else if (warp >= 12) {
+        // ---------------- epilogue ----------------
+        const int gtid = tid - 384;
+        const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
+        const long long hrow = h0 + rh;
+        const float dh = (prm.D && hrow < H) ? prm.D[hrow] : 0.f;
+        const int pc = rp % 64;
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % ST;
+            const int c = c0 + it;
+            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[5], 3, gtid, 128)) break;
+            if (!group_wait(&y_bar, it & 1, &abort_sh, &slot[6], 3, gtid, 128)) break;
             tc_fence_after();
-            const uint32_t sx = smem_u32(xs), ss = smem_u32(scr);
-            const uint32_t id_intra = idesc_bf16(C::M, C::Q, true, false);
-#pragma unroll
-            for (int hh = 0; hh < C::HB; ++hh)
-#pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks) {
-                    const uint32_t boff = hh * (C::Q * C::Q * 2) + (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                    mma_bf16(tmem + C::COL_R + hh * C::Q, sdesc(sx + ks * 2048, C::Q * 128, 1024),
-                             sdesc(ss + boff, 16, 1024), id_intra, ks > 0);
-                }
-            mma_commit(&mma_bar);
-            fl.mma = true;
-        }
-        if (!mbar_wait(&mma_bar, fl.mma_phase, kWaitPolls)) abort_sh = 1;
-        else if (tid == 0) fl.mma = false;
-        fl.mma_phase ^= 1;
-        tc_fence_after();
-        __syncthreads();
-        if (abort_sh) break;
-        // (6) epilogue: y = intra + exp(cum) * inter + D x, rows (head, p)
-        {
-            const int half = warp >> 2;
-            const uint8_t *xrow = xs + (rh * C::PB + rp / 64) * (C::Q * 128);
-            const int pc = rp % 64;
+            const float *ecum = stage_v(s) + 3 * C::HB * C::Q + rh * C::Q;
+            const uint8_t *xrow = stage_x(s) + (rh * C::PB + rp / 64) * (C::Q * 128);
             const long long ybase = (((long long)b * L + (long long)c * C::Q) * H + hrow) * C::P + rp;
 #pragma unroll 1
-            for (int t0 = half * (C::Q / 2); t0 < (half + 1) * (C::Q / 2); t0 += 16) {
+            for (int t0 = 0; t0 < C::Q; t0 += 16) {
                 float ri[16], re[16];
                 tmem_ld16(tmem + lane_off + C::COL_R + rh * C::Q + t0, ri);
                 tmem_ld16(tmem + lane_off + C::COL_R3 + t0, re);
@@ -640,52 +806,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 16; ++j) {
                         const int t = t0 + j;
                         const float xv = __bfloat162float(*reinterpret_cast<const bf16 *>(xrow + swz128(t, pc)));
-                        const float yv = ri[j] + ecum[rh * C::Q + t] * re[j] + dh_row * xv;
+                        const float yv = fmaf(ecum[t], re[j], ri[j]) + dh * xv;
                         const long long off = ybase + (long long)t * H * C::P;
                         if (prm.y_f32)
-                            reinterpret_cast<float *>(prm.y)[off] = yv;
+                            __stcs(reinterpret_cast<float *>(prm.y) + off, yv);
                         else
                             reinterpret_cast<bf16 *>(prm.y)[off] = __float2bfloat16_rn(yv);
                     }
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (C::STAGES == 1 && tid == 0 && it + 1 < nch) {
-            issue_chunk_loads<C>(stages, &full_bar[0], &mx, &mb, &mc, h0, g, c + 1, b, true);
-            fl.issued = it + 2;
+            fence_async_smem();
+            tc_fence_before();
+            named_bar_sync(3, 128);
+            if (gtid == 0) {
+                mbar_arrive(&free_bar);
+                mbar_arrive(&empty_bar[s]);
+            }
         }
     }
-    __syncthreads();
-    if (abort_sh) {
-        if (tid == 0) {
-            flag_timeout(prm.status);
-            drain<C::STAGES>(fl, full_bar, &mma_bar);
-        }
-        tc_fence_before();
-        __syncthreads();
-        if (warp == 0) tmem_dealloc(tmem, 512);
-        return;
-    }
-    // final state: the last segment's TMEM state after its last chunk
-    if (seg == prm.nseg - 1 && prm.fin && warp < 4) {
-        tc_fence_after();
-        float *dst = prm.fin + (((long long)b * H + hrow) * C::P + rp) * C::N;
-#pragma unroll 1
-        for (int n0 = 0; n0 < C::N; n0 += 16) {
-            float v[16];
-            tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
-            tmem_ld_wait();
-            if (hrow < H)
-#pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        }
+    // let this CTA's own copies and MMAs land (they normally have) before
+    // TMEM is freed and the CTA exits
+    if (warp == 0 && lane == 0)
+        for (int s = 0; s < ST; ++s)
+            if (nload[s] > 0) mbar_wait(&full_bar[s], (uint32_t)((nload[s] - 1) & 1), kDrainNs);
+    if (warp == 1 && lane == 0) {
+        mma_commit(&drain_bar);
+        mbar_wait(&drain_bar, 0, kDrainNs);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (abort_sh && tid == 0) flag_timeout(prm.status);
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------
@@ -737,10 +888,17 @@ Plan plan_for(const Dims &d) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Workspace: status word | per-unit counters | segment states | segment totals.
+// The first two are cleared on the stream by every call.
+template <class C>
+size_t header_bytes(const Dims &d) {
+    return 256 + align256(sizeof(unsigned) * d.b * plan_for<C>(d).nhb);
+}
+
 template <class C>
 size_t workspace_for(const Dims &d) {
     const Plan p = plan_for<C>(d);
-    size_t bytes = 256;  // status word
+    size_t bytes = header_bytes<C>(d);
     if (p.nseg > 1)
         bytes += align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N) + align256(sizeof(float) * d.b * p.nseg * d.H);
     return bytes;
@@ -763,13 +921,16 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     prm.y = y;
     prm.fin = fin;
     char *w = static_cast<char *>(ws);
+    const size_t hdr = header_bytes<C>(d);
     prm.status = reinterpret_cast<unsigned *>(w);
+    prm.counter = reinterpret_cast<unsigned *>(w + 256);
     prm.seg_state = nullptr;
     prm.seg_tot = nullptr;
     if (p.nseg > 1) {
-        prm.seg_state = reinterpret_cast<float *>(w + 256);
-        prm.seg_tot = reinterpret_cast<float *>(w + 256 + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
+        prm.seg_state = reinterpret_cast<float *>(w + hdr);
+        prm.seg_tot = reinterpret_cast<float *>(w + hdr + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
     }
+    prm.nhb = p.nhb;
     prm.b = d.b;
     prm.L = d.L;
     prm.H = d.H;
@@ -796,18 +957,18 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
         seg_attr = seg_smem;
     }
     if (seg_smem > kSmemLimit) return cudaErrorInvalidValue;
-    cudaError_t e = cudaMemsetAsync(prm.status, 0, sizeof(unsigned), s);
+    cudaError_t e = cudaMemsetAsync(w, 0, hdr, s);
     if (e != cudaSuccess) return e;
     timing_begin(s);
     if (p.nseg > 1) {
         dim3 grid(p.nseg - 1, p.nhb, (unsigned)d.b);
-        seg_state_kernel<C><<<grid, kThreads, seg_smem, s>>>(mx, mb, prm);
+        seg_state_kernel<C><<<grid, kSegThreads, seg_smem, s>>>(mx, mb, prm);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         timing_mark(s, "seg_state_tc");
     }
     dim3 grid(p.nseg, p.nhb, (unsigned)d.b);
-    chunk_scan_kernel<C><<<grid, kThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
+    chunk_scan_kernel<C><<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
     e = cudaGetLastError();
     timing_mark(s, "chunk_scan_tc");
     return e;
@@ -832,7 +993,7 @@ bool tc_fwd_supported(const Dims &d, ssd_dtype_t dtype) {
     dispatch(d, [&](auto c) {
         using C = decltype(c);
         ok = C::SCAN_FITS && C::TMEM_FITS && (d.G == 1 || d.hpg % C::HB == 0) && d.L < (1ll << 31) &&
-             d.H < (1 << 30) && d.b < (1 << 30);
+             d.H < (1 << 30) && d.b < 65536;
         if (ok) {
             const Plan p = plan_for<C>(d);
             ok = C::SMEM_SEG_BASE + (int)(C::HB * p.cps * sizeof(float)) <= kSmemLimit;

@@ -50,6 +50,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
         : "memory");
 }
 
+// Raise the phase's expected transaction bytes without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -62,14 +68,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: gives up after `limit` polls and returns false, so a lost
-// arrival can never hang the GPU; the caller records the failure.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t limit = (1u << 26)) {
-    for (uint32_t i = 0; i < limit; ++i) {
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: gives up after `limit_ns` nanoseconds of wall time and
+// returns false, so a lost arrival can never hang the GPU; the caller
+// records the failure.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns = 100000000ull) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (i > 64) __nanosleep(32);
+        if ((i & 15) == 15) {
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+            __nanosleep(64);
+        }
     }
-    return false;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -195,6 +211,12 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 }
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
+
+// Barrier among `nthreads` threads (whole warps) on hardware barrier `id`
+// (id 0 is the one __syncthreads uses).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 }  // namespace tc
 }  // namespace ssd
