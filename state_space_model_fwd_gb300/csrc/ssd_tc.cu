@@ -49,13 +49,14 @@ constexpr uint64_t kWaitNs = 100000000ull;    // a wait gives up after 0.1 s
 constexpr uint64_t kDrainNs = 20000000ull;    // the exit drain gives up after 0.02 s
 
 struct TcParams {
+    long long *trace;  // optional event trace of CTA (0, 0, 0) (trace builds only)
+    const bf16 *x;     // [b, L, H, P] (the epilogue's D x term)
     const bf16 *dt;
     const float *A, *D, *init;
     void *y;
     float *fin;
     float *seg_state;   // [b, nseg, H, P, N]: segment-local states, then (in place) states entering segments
-    float *seg_tot;     // [b, nseg, H]  total dt*A of each segment
-    unsigned *counter;  // [b, nhb] segment-state CTAs finished (zeroed before the launch)
+    float *seg_tot;     // [b, H, nseg]  total dt*A of each segment
     unsigned *status;   // bit 0: a wait gave up
     long long b, L, H, G;
     int hpg, nc, nseg, cps;  // cps: chunks per segment
@@ -74,37 +75,60 @@ struct Cfg {
     static constexpr int XW_BYTES = M * Q * 2;  // one of the hi / lo halves of w x
     static constexpr int SBF_BYTES = M * N * 2; // [N/64 blocks][M rows][64]
     static constexpr int MM_BYTES = HB * Q * Q * 2;  // per head [Q/64 blocks][Q rows][64]
-    // per-stage vectors: dt, cum, w, exp(cum) for each head, then exp(total)
-    static constexpr int VEC_FLOATS = 4 * HB * Q + 32;
-    static constexpr int VEC_BYTES = ((VEC_FLOATS * 4 + 1023) / 1024) * 1024;
+    // per-stage vectors, [HB][Q] each: dt, cum, w, exp(cum), u = exp(cum - r),
+    // v = exp(r - cum) dt (r: the cumulative decay at mid-chunk); then per
+    // head exp(chunk total) and a flag for chunks whose decay range is too
+    // wide to factor in fp32
+    static constexpr int V_DT = 0, V_CUM = HB * Q, V_W = 2 * HB * Q, V_ECUM = 3 * HB * Q, V_U = 4 * HB * Q,
+                         V_V = 5 * HB * Q, V_DECAY = 6 * HB * Q, V_WIDE = 6 * HB * Q + HB;
+    static constexpr int VEC_FLOATS = 6 * HB * Q + 32;
+    // exp(cum) of two chunks, handed from the score-matrix warps to the epilogue
+    static constexpr int EPI_BYTES = ((2 * HB * Q * 4 + 1023) / 1024) * 1024;
 
-    // scan kernel: stages of (x, B, C, vectors), 1 or 2 buffers of w x, the
-    // bf16 state copy and the score matrices
-    static constexpr int SCAN_STAGE = X_BYTES + 2 * BC_BYTES + VEC_BYTES;
+    // scan kernel: TMA stages of (x, B, C), a ring of kVecSlots vector sets,
+    // 1 or 2 buffers of w x (hi + lo), the bf16 state copy, the score
+    // matrices and the epilogue's exp(cum)
+    static constexpr int SCAN_STAGE = X_BYTES + 2 * BC_BYTES;
+    // (rounded to 1 KB: the swizzled operand tiles after it need 1024-byte alignment)
+    static constexpr int VEC_RING = ((4 * VEC_FLOATS * 4 + 1023) / 1024) * 1024;
     static constexpr int scan_smem(int st, int xwb) {
-        return st * SCAN_STAGE + xwb * 2 * XW_BYTES + SBF_BYTES + MM_BYTES + 1024;
+        return st * SCAN_STAGE + VEC_RING + xwb * 2 * XW_BYTES + SBF_BYTES + MM_BYTES + EPI_BYTES + 1024;
     }
     static constexpr int SCAN_ST = scan_smem(2, 2) <= kSmemLimit || scan_smem(2, 1) <= kSmemLimit ? 2 : 1;
     static constexpr int SCAN_XWB = scan_smem(SCAN_ST, 2) <= kSmemLimit ? 2 : 1;
     static constexpr int SMEM_SCAN = scan_smem(SCAN_ST, SCAN_XWB);
     static constexpr bool SCAN_FITS = SMEM_SCAN <= kSmemLimit;
 
-    // segment-state kernel: stages of (x, B, vectors, w x hi / lo)
-    static constexpr int SEG_STAGE = X_BYTES + BC_BYTES + VEC_BYTES + 2 * XW_BYTES;
-    static constexpr int SEG_ST = 2 * SEG_STAGE + 1024 + 4096 <= kSmemLimit ? 2 : 1;
-    static constexpr int SMEM_SEG_BASE = SEG_ST * SEG_STAGE + 1024;  // + chunk totals [HB][cps]
+    // segment-state kernel: TMA stages of (x, B), two buffers of w x (hi +
+    // lo), a ring of vector sets, then the chunk totals [HB][cps]
+    static constexpr int SEG_STAGE = X_BYTES + BC_BYTES;
+    static constexpr int seg_smem(int st) { return st * SEG_STAGE + 4 * XW_BYTES + VEC_RING + 1024 + 4096; }
+    static constexpr int SEG_ST = seg_smem(4) <= kSmemLimit ? 4 : (seg_smem(3) <= kSmemLimit ? 3 : 2);
+    static constexpr int SMEM_SEG_BASE = SEG_ST * SEG_STAGE + 4 * XW_BYTES + VEC_RING + 1024;  // + [HB][cps]
 
     // TMEM columns of the scan kernel
     static constexpr int COL_S = 0;
-    static constexpr int COL_R3 = N;                 // inter-chunk term, [M][Q]
-    static constexpr int COL_R = N + Q;              // intra-chunk term per head, [M][Q] each
-    static constexpr int COL_END = N + Q + HB * Q;
-    static constexpr bool CB_ALIAS = COL_END + Q > 512;
-    static constexpr int COL_CB = CB_ALIAS ? COL_R : COL_END;  // C B^T, [Q][Q]
-    static constexpr int TMEM_USED = CB_ALIAS ? COL_END : COL_END + Q;
-    static constexpr bool TMEM_FITS = TMEM_USED <= 512 && !CB_ALIAS;
+    static constexpr int COL_R3 = N;                 // inter-chunk term, two buffers of [M][Q]
+    static constexpr int COL_R = N + 2 * Q;          // intra-chunk term per head, [M][Q] each
+    static constexpr int COL_CB = N + 2 * Q + HB * Q;  // C B^T, [Q][Q]
+    static constexpr int TMEM_USED = COL_CB + Q;
+    static constexpr bool TMEM_FITS = TMEM_USED <= 512;
     static constexpr uint32_t SEG_TMEM = N < 32 ? 32 : N;
 };
+
+// Event trace (SSD_TRACE builds): clock64() of role events of CTA (0, 0, 0),
+// trace[event * 256 + chunk].  Compiled out otherwise.
+#ifdef SSD_TRACE
+#define TRACE(ev, it)                                                                                  \
+    do {                                                                                               \
+        if (prm.trace && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (it) < 256)          \
+            prm.trace[(ev) * 256 + (it)] = clock64();                                                  \
+    } while (0)
+#else
+#define TRACE(ev, it) \
+    do {              \
+    } while (0)
+#endif
 
 // ---------------------------------------------------------------------------
 // waiting with a bound
@@ -117,14 +141,13 @@ __device__ __forceinline__ void flag_timeout(unsigned *status) {
 // or as soon as another role has given up (abort flag), so nothing spins
 // forever.
 __device__ __forceinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15) == 15) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitNs) break;
-            __nanosleep(64);
-        }
+    for (;;) {
+        // sleeps in hardware (up to 20 us) until the phase completes
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitNs) break;
     }
     *abort_flag = 1;
     return false;
@@ -162,25 +185,6 @@ __device__ __forceinline__ float warp_chunk_cumsum(const float *dtv, float a, fl
 #pragma unroll
     for (int i = 0; i < QPL; ++i) cum[lane * QPL + i] = v[i] + excl;
     return __shfl_sync(0xffffffffu, tot, 31);
-}
-
-// dt of chunk c for the CTA's heads into dtv[HB][Q] (one warp; zeros for
-// heads past H).
-template <class C>
-__device__ __forceinline__ void warp_load_dt(const TcParams &prm, int b, int h0, int c, float *dtv) {
-    const int lane = threadIdx.x & 31;
-    constexpr int PER = C::HB * C::Q / 32;
-    float v[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int idx = lane + 32 * i;
-        const int hh = idx / C::Q, q = idx % C::Q;
-        const long long h = h0 + hh;
-        v[i] = h < prm.H ? __bfloat162float(prm.dt[((long long)b * prm.L + (long long)c * C::Q + q) * prm.H + h]) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < PER; ++i) dtv[lane + 32 * i] = v[i];
-    __syncwarp();
 }
 
 // x tile scaled row-wise by w, split into two bf16 tiles whose sum carries
@@ -242,27 +246,32 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 }
 
 // ===========================================================================
-// Segment-local states (segments 0 .. nseg-2), then -- in the last CTA of
-// each (batch, head block) to finish -- the pass of states across segments.
-//   warp 0     : TMA loads of x, B; dt and the segment weights
-//                w_t = exp(sum_{k>t in segment} dt_k A) dt_t
-//   warp 1     : tcgen05.mma S += (w o x)^T B into TMEM
-//   warps 4-7  : w o x as bf16 hi + lo operand tiles; TMEM -> HBM at the end
+// Segment-local states (segments 0 .. nseg-2):
+//   S_seg = sum_t exp(sum_{k>t in segment} dt_k A) dt_t x_t^T B_t
+//   warp 0      : TMA loads of the x and B tiles (kSegStages-deep ring)
+//   warp 1      : tcgen05.mma S += (w o x)^T B into TMEM
+//   warp 2      : dt and the segment weights w (kVecSlots-deep ring)
+//   warps 4-11  : w o x as bf16 hi + lo operand tiles (two buffers);
+//                 warps 4-7 move the TMEM state to HBM at the end
 // ===========================================================================
-constexpr int kSegThreads = 256;
+constexpr int kSegThreads = 384;
+constexpr int kVecSlots = 4;
 
 template <class C>
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb, TcParams prm) {
-    constexpr int ST = C::SEG_ST;
+    constexpr int ST = C::SEG_ST, NV = kVecSlots;
+    constexpr int HQ = C::HB * C::Q;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *tot_s = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE);  // [HB][cps]
-    __shared__ uint64_t full_bar[2], empty_bar[2], xw_bar[2], done_bar, drain_bar;
+    uint8_t *xw_base = smem + ST * C::SEG_STAGE;
+    float *vec_base = reinterpret_cast<float *>(xw_base + 2 * 2 * C::XW_BYTES);
+    float *tot_s = vec_base + NV * C::VEC_FLOATS;  // [HB][cps]
+    __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], xfull_bar[2], xempty_bar[2];
+    __shared__ uint64_t done_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
-    __shared__ volatile int slot[4];
-    __shared__ int last_sh;
+    __shared__ volatile int slot[8];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, hblk = blockIdx.y, b = blockIdx.z;
@@ -273,19 +282,26 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     const long long H = prm.H;
     auto stage_x = [&](int s) { return smem + s * C::SEG_STAGE; };
     auto stage_b = [&](int s) { return smem + s * C::SEG_STAGE + C::X_BYTES; };
-    auto stage_v = [&](int s) { return reinterpret_cast<float *>(smem + s * C::SEG_STAGE + C::X_BYTES + C::BC_BYTES); };
-    auto stage_xh = [&](int s) { return smem + s * C::SEG_STAGE + C::X_BYTES + C::BC_BYTES + C::VEC_BYTES; };
-    auto stage_xl = [&](int s) { return stage_xh(s) + C::XW_BYTES; };
+    auto xw_hi = [&](int i) { return xw_base + i * 2 * C::XW_BYTES; };
+    auto xw_lo = [&](int i) { return xw_base + i * 2 * C::XW_BYTES + C::XW_BYTES; };
+    auto vec = [&](int v) { return vec_base + v * C::VEC_FLOATS; };
 
     if (warp == 1) {
         tmem_alloc(&tmem_base_sh, C::SEG_TMEM);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < ST; ++i) {
             mbar_init(&full_bar[i], 1);
             mbar_init(&empty_bar[i], 1);
-            mbar_init(&xw_bar[i], 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&vfull_bar[i], 1);
+            mbar_init(&vempty_bar[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&xfull_bar[i], 1);
+            mbar_init(&xempty_bar[i], 1);
         }
         mbar_init(&done_bar, 1);
         mbar_init(&drain_bar, 1);
@@ -294,12 +310,12 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         prefetch_tmap(&mx);
         prefetch_tmap(&mb);
     }
-    int nload[2] = {0, 0};  // TMA loads issued per stage (producer lane 0)
+    int nload[4] = {};  // TMA loads issued per stage (producer lane 0)
     // chunk totals of dt*A over the segment: groups of 8 threads reduce one
-    // (head, chunk) pair each, in a fixed order (bitwise reproducible)
+    // (head, chunk) pair each, in a fixed order (bitwise reproducible); the
+    // loop bound is the same for every lane of a warp, so the shuffles see
+    // a full warp
     {
-        // the loop bound is the same for every lane of a warp (j0 steps over
-        // whole warps' worth of groups), so the shuffles see a full warp
         const int grp = tid >> 3, gl = tid & 7;
         const int npair = C::HB * nch;
         for (int j0 = (tid >> 5) * 4; j0 < npair; j0 += kSegThreads / 8) {
@@ -330,50 +346,75 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             run += t;
         }
         const long long h = h0 + tid;
-        if (h < H) prm.seg_tot[((long long)b * prm.nseg + seg) * H + h] = run;
+        if (h < H) prm.seg_tot[((long long)b * H + h) * prm.nseg + seg] = run;
     }
     __syncthreads();
     const uint32_t tmem = tmem_base_sh;
 
     if (warp == 0) {
-        // ---------------- producer: TMA + segment weights ----------------
-        for (int it = 0; it < nch; ++it) {
-            const int s = it % ST;
-            const int c = c0 + it;
-            if (it >= ST) {
-                int ok = lane == 0 ? (wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            }
-            if (lane == 0) {
-                mbar_expect_tx(&full_bar[s], chunk_load_bytes<C>(false));
-                issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c, b);
+        // ---------------- TMA producer ----------------
+        if (lane == 0)
+            for (int it = 0; it < nch; ++it) {
+                const int s = it % ST;
+                if (it >= ST && !wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh)) break;
+                mbar_arrive_expect_tx(&full_bar[s], chunk_load_bytes<C>(false));
+                issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c0 + it,
+                                     b);
                 ++nload[s];
             }
-            float *vec = stage_v(s);
-            float *dtv = vec, *cum = vec + C::HB * C::Q, *w = vec + 2 * C::HB * C::Q;
-            warp_load_dt<C>(prm, b, h0, c, dtv);
+    } else if (warp == 2) {
+        // ---------------- segment weights ----------------
+        constexpr int PER = HQ / 32;
+        float dnext[PER];
+        auto fetch_dt = [&](int c) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int idx = lane + 32 * i;
+                const int hh = idx / C::Q, q = idx % C::Q;
+                const long long h = h0 + hh;
+                dnext[i] = h < H ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + (long long)c * C::Q + q) * H + h))
+                                 : 0.f;
+            }
+        };
+        fetch_dt(c0);
+        for (int it = 0; it < nch; ++it) {
+            const int v = it % NV;
+            if (it >= NV) {
+                int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], ((it / NV) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            }
+            float *vv = vec(v);
+#pragma unroll
+            for (int i = 0; i < PER; ++i) vv[C::V_DT + lane + 32 * i] = dnext[i];
+            __syncwarp();
+            if (it + 1 < nch) fetch_dt(c0 + it + 1);
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
                 const long long h = h0 + hh;
                 const float a = h < H ? prm.A[h] : 0.f;
-                const float total = warp_chunk_cumsum<C::Q>(dtv + hh * C::Q, a, cum + hh * C::Q);
+                float *cum = vv + C::V_CUM + hh * C::Q;
+                const float *dtv = vv + C::V_DT + hh * C::Q;
+                const float total = warp_chunk_cumsum<C::Q>(dtv, a, cum);
                 __syncwarp();
                 const float after = tot_s[hh * prm.cps + it];
                 for (int q = lane; q < C::Q; q += 32)
-                    w[hh * C::Q + q] = expf(after + total - cum[hh * C::Q + q]) * dtv[hh * C::Q + q];
+                    vv[C::V_W + hh * C::Q + q] = __expf(after + total - cum[q]) * dtv[q];
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_bar[s]);
+            if (lane == 0) {
+                TRACE(14, it);
+                mbar_arrive(&vfull_bar[v]);
+            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(C::M, C::N, true, true);
             for (int it = 0; it < nch; ++it) {
-                const int s = it % ST;
-                if (!wait_bounded(&xw_bar[s], (it / ST) & 1, &abort_sh)) break;
+                const int s = it % ST, xb = it & 1;
+                if (!wait_bounded(&xfull_bar[xb], (it >> 1) & 1, &abort_sh)) break;
                 tc_fence_after();
-                const uint32_t ah = smem_u32(stage_xh(s)), al = smem_u32(stage_xl(s)), b0 = smem_u32(stage_b(s));
+                const uint32_t ah = smem_u32(xw_hi(xb)), al = smem_u32(xw_lo(xb)), b0 = smem_u32(stage_b(s));
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
                     mma_bf16(tmem, sdesc(ah + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
@@ -383,6 +424,8 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                     mma_bf16(tmem, sdesc(al + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
                              idesc, true);
                 mma_commit(&empty_bar[s]);
+                mma_commit(&xempty_bar[xb]);
+                TRACE(16, it);
             }
             mma_commit(&done_bar);  // completes once every MMA above has
         }
@@ -390,31 +433,43 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         // ---------------- w o x operand builders ----------------
         const int gtid = tid - 128;
         for (int it = 0; it < nch; ++it) {
-            const int s = it % ST;
-            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[0], 1, gtid, 128)) break;
-            const float *w = stage_v(s) + 2 * C::HB * C::Q;
-            build_xw<C, 128>(stage_x(s), stage_xh(s), stage_xl(s), w, gtid);
+            const int s = it % ST, v = it % NV, xb = it & 1;
+            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[0], 1, gtid, 256)) break;
+            if (!group_wait(&vfull_bar[v], (it / NV) & 1, &abort_sh, &slot[1], 1, gtid, 256)) break;
+            if (it >= 2 && !group_wait(&xempty_bar[xb], ((it >> 1) & 1) ^ 1, &abort_sh, &slot[2], 1, gtid, 256)) break;
+            build_xw<C, 256>(stage_x(s), xw_hi(xb), xw_lo(xb), vec(v) + C::V_W, gtid);
             fence_async_smem();
-            named_bar_sync(1, 128);
-            if (gtid == 0) mbar_arrive(&xw_bar[s]);
+            named_bar_sync(1, 256);
+            if (gtid == 0) {
+                TRACE(15, it);
+                mbar_arrive(&xfull_bar[xb]);
+                mbar_arrive(&vempty_bar[v]);
+            }
         }
         // segment state: TMEM lane r = row (head, p)
-        if (group_wait(&done_bar, 0, &abort_sh, &slot[1], 1, gtid, 128)) {
-            tc_fence_after();
-            const int q4 = warp & 3;
-            const int r = q4 * 32 + lane;
-            const int hh = r / C::P, p = r % C::P;
-            const long long h = h0 + hh;
-            float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + h) * C::P + p) * C::N;
+        if (warp < 8) {
+            if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 2, gtid, 128)) {
+                tc_fence_after();
+                const int q4 = warp & 3;
+                const int r = q4 * 32 + lane;
+                const int hh = r / C::P, p = r % C::P;
+                const long long h = h0 + hh;
+                float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + h) * C::P + p) * C::N;
 #pragma unroll 1
-            for (int n0 = 0; n0 < C::N; n0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + n0, v);
-                tmem_ld_wait();
-                if (h < H)
+                for (int n0 = 0; n0 < C::N; n0 += 32) {
+                    float v0[16], v1[16];
+                    tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + n0, v0);
+                    tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + n0 + 16, v1);
+                    tmem_ld_wait();
+                    if (h < H) {
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                        for (int j = 0; j < 16; j += 4) {
+                            *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v0[j], v0[j + 1], v0[j + 2], v0[j + 3]);
+                            *reinterpret_cast<float4 *>(dst + n0 + 16 + j) =
+                                make_float4(v1[j], v1[j + 1], v1[j + 2], v1[j + 3]);
+                        }
+                    }
+                }
             }
         }
     }
@@ -430,48 +485,102 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, C::SEG_TMEM);
-    if (abort_sh) {
-        if (tid == 0) flag_timeout(prm.status);
-        return;
-    }
+    if (abort_sh && tid == 0) flag_timeout(prm.status);
+}
 
-    // ---------------- pass of states across segments ----------------
-    // The last of the unit's nseg-1 CTAs to finish folds the segment states
-    // in order, in place: slot s becomes the state entering segment s + 1.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(prm.counter + (long long)b * prm.nhb + hblk, 1u);
-        last_sh = prev == (unsigned)(prm.nseg - 2);
+// ---------------------------------------------------------------------------
+// Pass of states across segments, in place: slot s of the segment-state
+// array (the local state of segment s) becomes the state entering segment
+// s + 1 = exp(T_s) (state entering s) + local_s, T_s the segment's total
+// dt*A.  One thread per four consecutive (p, n) of one (b, h); the loads
+// of a batch of segments are issued before any of their results is stored.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) segment_pass_kernel(const float *__restrict__ init, float *seg_state,
+                                                           const float *__restrict__ seg_tot, long long H, int PN,
+                                                           int nseg) {
+    const int PN4 = PN / 4;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const long long h = blockIdx.y, b = blockIdx.z;
+    if (e >= PN4) return;
+    float4 acc = init ? __ldg(reinterpret_cast<const float4 *>(init + (b * H + h) * PN) + e)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nsp = nseg - 1;
+    const float *tot = seg_tot + (b * H + h) * nseg;
+    constexpr int KB = 8;
+    for (int s0 = 0; s0 < nsp; s0 += KB) {
+        float4 v[KB];
+        float ex[KB];
+#pragma unroll
+        for (int k = 0; k < KB; ++k)
+            if (s0 + k < nsp) {
+                v[k] = __ldcg(reinterpret_cast<const float4 *>(seg_state + (((b * nseg + s0 + k) * H + h) * PN)) + e);
+                ex[k] = expf(__ldcg(tot + s0 + k));
+            }
+#pragma unroll
+        for (int k = 0; k < KB; ++k)
+            if (s0 + k < nsp) {
+                acc.x = fmaf(ex[k], acc.x, v[k].x);
+                acc.y = fmaf(ex[k], acc.y, v[k].y);
+                acc.z = fmaf(ex[k], acc.z, v[k].z);
+                acc.w = fmaf(ex[k], acc.w, v[k].w);
+                __stcg(reinterpret_cast<float4 *>(seg_state + (((b * nseg + s0 + k) * H + h) * PN)) + e, acc);
+            }
     }
-    __syncthreads();
-    if (!last_sh) return;
-    __threadfence();
-    constexpr int E4 = C::M * C::N / 4;  // float4s of the CTA's (head, p, n) block
-    for (int e = tid; e < E4; e += kSegThreads) {
-        const int r = (e * 4) / C::N, n = (e * 4) % C::N;
-        const int hh = r / C::P, p = r % C::P;
-        const long long h = h0 + hh;
-        if (h >= H) continue;
-        float4 acc = prm.init ? *reinterpret_cast<const float4 *>(prm.init + ((b * H + h) * C::P + p) * C::N + n)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int sp = 0; sp < prm.nseg - 1; ++sp) {
-            const float e_sp = expf(__ldcg(prm.seg_tot + ((long long)b * prm.nseg + sp) * H + h));
-            float4 *slot_p = reinterpret_cast<float4 *>(
-                prm.seg_state + ((((long long)b * prm.nseg + sp) * H + h) * C::P + p) * C::N + n);
-            const float4 v = __ldcg(slot_p);
-            acc.x = fmaf(e_sp, acc.x, v.x);
-            acc.y = fmaf(e_sp, acc.y, v.y);
-            acc.z = fmaf(e_sp, acc.z, v.z);
-            acc.w = fmaf(e_sp, acc.w, v.w);
-            __stcg(slot_p, acc);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_y(T *p, float v);
+template <>
+__device__ __forceinline__ void store_y<float>(float *p, float v) { __stcs(p, v); }
+template <>
+__device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+// x[t][p] of this thread's (head, p) column for the Q steps of a chunk,
+// two bf16 per register (fetched one chunk ahead, while the epilogue waits).
+template <class C>
+__device__ __forceinline__ void fetch_x_column(const bf16 *xg, long long stride, bool live, uint32_t (&xp)[C::Q / 2]) {
+    const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xg);
+#pragma unroll
+    for (int j = 0; j < C::Q / 2; ++j) {
+        const uint32_t lo = live ? __ldg(x16 + (long long)(2 * j) * stride) : 0u;
+        const uint32_t hi = live ? __ldg(x16 + (long long)(2 * j + 1) * stride) : 0u;
+        xp[j] = lo | (hi << 16);
+    }
+}
+
+// Epilogue of one chunk for this thread's row: TMEM row of the intra term
+// (its head's buffer) and of the inter term, exp(cum) of its head, and the
+// x column fetched ahead.
+template <class C, typename T>
+__device__ __forceinline__ void epilogue_rows(uint32_t tmem_lane, int it, int rh, const float *ecum,
+                                              const uint32_t (&xp)[C::Q / 2], T *yp, long long stride, float dh,
+                                              bool live) {
+#pragma unroll
+    for (int t0 = 0; t0 < C::Q; t0 += 16) {
+        float ri[16], re[16];
+        tmem_ld16(tmem_lane + C::COL_R + rh * C::Q + t0, ri);
+        tmem_ld16(tmem_lane + C::COL_R3 + (it & 1) * C::Q + t0, re);
+        tmem_ld_wait();
+        if (live) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 e4 = *reinterpret_cast<const float4 *>(ecum + t0 + j);
+                const uint32_t w0 = xp[(t0 + j) / 2], w1 = xp[(t0 + j) / 2 + 1];
+                const float x0 = __uint_as_float(w0 << 16), x1 = __uint_as_float(w0 & 0xFFFF0000u);
+                const float x2 = __uint_as_float(w1 << 16), x3 = __uint_as_float(w1 & 0xFFFF0000u);
+                store_y<T>(yp + (long long)(t0 + j) * stride, fmaf(dh, x0, fmaf(e4.x, re[j], ri[j])));
+                store_y<T>(yp + (long long)(t0 + j + 1) * stride, fmaf(dh, x1, fmaf(e4.y, re[j + 1], ri[j + 1])));
+                store_y<T>(yp + (long long)(t0 + j + 2) * stride, fmaf(dh, x2, fmaf(e4.z, re[j + 2], ri[j + 2])));
+                store_y<T>(yp + (long long)(t0 + j + 3) * stride, fmaf(dh, x3, fmaf(e4.w, re[j + 3], ri[j + 3])));
+            }
         }
     }
 }
 
 // ===========================================================================
 // Chunk scan with the state carried in TMEM (every segment).
-//   warp 0     : TMA loads of x, B, C; dt, cumulative decay, w, exp(cum)
+//   warp 0     : TMA loads of x, B, C; dt (fetched a chunk ahead), cumulative
+//                decay, w, exp(cum) and the factors u, v of exp(cum_t - cum_s)
 //   warp 1     : tcgen05.mma issue (C B^T; S C^T; S += (w x)^T B; X^T M^T)
 //   warps 4-7  : w o x operand tiles; bf16 state copy and S *= exp(total)
 //   warps 8-11 : masked, decayed score matrices M_h (bf16) from C B^T
@@ -485,13 +594,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                       const __grid_constant__ CUtensorMap mc, TcParams prm) {
     constexpr int ST = C::SCAN_ST;
     constexpr int XWB = C::SCAN_XWB;
+    constexpr int HQ = C::HB * C::Q;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xw_base = smem + ST * C::SCAN_STAGE;
+    constexpr int NV = kVecSlots;
+    float *vec_base = reinterpret_cast<float *>(smem + ST * C::SCAN_STAGE);
+    uint8_t *xw_base = smem + ST * C::SCAN_STAGE + C::VEC_RING;
     uint8_t *sbf = xw_base + XWB * 2 * C::XW_BYTES;
     uint8_t *mm = sbf + C::SBF_BYTES;
-    __shared__ uint64_t full_bar[2], empty_bar[2];
-    __shared__ uint64_t cb_bar, mask_bar, wg1_bar, state_bar, y_bar, free_bar, drain_bar;
+    float *epi_vec = reinterpret_cast<float *>(mm + C::MM_BYTES);  // [2][HB][Q]
+    __shared__ uint64_t full_bar[2], empty_bar[2], free_r3_bar[2], epi_bar[2], vfull_bar[NV], vempty_bar[NV];
+    __shared__ uint64_t cb_bar, mask_bar, wg1_bar, state_bar, y_bar, free_r_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
     __shared__ volatile int slot[8];
@@ -506,10 +619,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
     auto stage_b = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES; };
     auto stage_c = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + C::BC_BYTES; };
-    auto stage_v = [&](int s) {
-        return reinterpret_cast<float *>(smem + s * C::SCAN_STAGE + C::X_BYTES + 2 * C::BC_BYTES);
-    };
-    // per-stage vectors: dtv [HB][Q], cum [HB][Q], w [HB][Q], ecum [HB][Q], decay [HB]
+    auto vec = [&](int v) { return vec_base + v * C::VEC_FLOATS; };
     auto xw_hi = [&](int i) { return xw_base + i * 2 * C::XW_BYTES; };
     auto xw_lo = [&](int i) { return xw_base + i * 2 * C::XW_BYTES + C::XW_BYTES; };
 
@@ -521,13 +631,19 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&full_bar[i], 1);
             mbar_init(&empty_bar[i], 1);
+            mbar_init(&free_r3_bar[i], 1);
+            mbar_init(&epi_bar[i], 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&vfull_bar[i], 1);
+            mbar_init(&vempty_bar[i], 1);
         }
         mbar_init(&cb_bar, 1);
         mbar_init(&mask_bar, 1);
         mbar_init(&wg1_bar, 1);
         mbar_init(&state_bar, 1);
         mbar_init(&y_bar, 1);
-        mbar_init(&free_bar, 1);
+        mbar_init(&free_r_bar, 1);
         mbar_init(&drain_bar, 1);
         fence_mbar_init();
         abort_sh = 0;
@@ -538,44 +654,79 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) TRACE(13, 0);
     const uint32_t tmem = tmem_base_sh;
     int nload[2] = {0, 0};  // TMA loads issued per stage (producer lane 0)
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
 
     if (warp == 0) {
-        // ---------------- producer ----------------
+        // ---------------- TMA producer ----------------
+        if (lane == 0)
+            for (int it = 0; it < nch; ++it) {
+                const int s = it % ST;
+                if (it >= ST && !wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh)) break;
+                mbar_arrive_expect_tx(&full_bar[s], chunk_load_bytes<C>(true));
+                issue_chunk_loads<C>(stage_x(s), stage_b(s), stage_c(s), &full_bar[s], &mx, &mb, &mc, h0, g, c0 + it,
+                                     b);
+                ++nload[s];
+                TRACE(0, it);
+            }
+    } else if (warp == 2) {
+        // ---------------- per-chunk vectors (run up to NV chunks ahead) ----------------
+        constexpr int PER = HQ / 32;
+        float dnext[PER];
+        auto fetch_dt = [&](int c) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int idx = lane + 32 * i;
+                const int hh = idx / C::Q, q = idx % C::Q;
+                const long long h = h0 + hh;
+                dnext[i] = h < H ? __bfloat162float(__ldg(prm.dt + ((long long)b * L + (long long)c * C::Q + q) * H + h))
+                                 : 0.f;
+            }
+        };
+        fetch_dt(c0);
         for (int it = 0; it < nch; ++it) {
-            const int s = it % ST;
-            const int c = c0 + it;
-            if (it >= ST) {
-                int ok = lane == 0 ? (wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
+            const int v = it % NV;
+            if (it >= NV) {
+                int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], ((it / NV) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
-            if (lane == 0) {
-                mbar_expect_tx(&full_bar[s], chunk_load_bytes<C>(true));
-                issue_chunk_loads<C>(stage_x(s), stage_b(s), stage_c(s), &full_bar[s], &mx, &mb, &mc, h0, g, c, b);
-                ++nload[s];
-            }
-            float *vec = stage_v(s);
-            float *dtv = vec, *cum = vec + C::HB * C::Q, *w = vec + 2 * C::HB * C::Q, *ecum = vec + 3 * C::HB * C::Q;
-            float *decay = vec + 4 * C::HB * C::Q;
-            warp_load_dt<C>(prm, b, h0, c, dtv);
+            float *vv = vec(v);
+#pragma unroll
+            for (int i = 0; i < PER; ++i) vv[C::V_DT + lane + 32 * i] = dnext[i];
+            __syncwarp();
+            if (it + 1 < nch) fetch_dt(c0 + it + 1);  // in flight while this chunk's vectors are computed
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
                 const long long h = h0 + hh;
                 const float a = h < H ? prm.A[h] : 0.f;
-                const float total = warp_chunk_cumsum<C::Q>(dtv + hh * C::Q, a, cum + hh * C::Q);
+                float *cum = vv + C::V_CUM + hh * C::Q;
+                const float *dtv = vv + C::V_DT + hh * C::Q;
+                const float total = warp_chunk_cumsum<C::Q>(dtv, a, cum);
                 __syncwarp();
+                const float r = cum[C::Q / 2 - 1];
+                // exp(cum_t - cum_s) = u_t v_s / dt_s factors in fp32 only while
+                // each half-chunk's decay stays within e^80
+                const bool wide = (cum[0] - r) > 80.f || (r - total) > 80.f;
                 for (int q = lane; q < C::Q; q += 32) {
-                    const float cq = cum[hh * C::Q + q];
-                    w[hh * C::Q + q] = expf(total - cq) * dtv[hh * C::Q + q];
-                    ecum[hh * C::Q + q] = expf(cq);
+                    const float cq = cum[q];
+                    vv[C::V_W + hh * C::Q + q] = __expf(total - cq) * dtv[q];
+                    vv[C::V_ECUM + hh * C::Q + q] = __expf(cq);
+                    vv[C::V_U + hh * C::Q + q] = wide ? 0.f : __expf(cq - r);
+                    vv[C::V_V + hh * C::Q + q] = wide ? 0.f : __expf(r - cq) * dtv[q];
                 }
-                if (lane == 0) decay[hh] = expf(total);
+                if (lane == 0) {
+                    vv[C::V_DECAY + hh] = __expf(total);
+                    vv[C::V_WIDE + hh] = wide ? 1.f : 0.f;
+                }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&full_bar[s]);
+            if (lane == 0) {
+                TRACE(1, it);
+                mbar_arrive(&vfull_bar[v]);
+            }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -598,18 +749,20 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     mma_bf16(tmem + C::COL_CB, sdesc(sc + koff, 16, 1024), sdesc(sb + koff, 16, 1024), id_cb, ks > 0);
                 }
                 mma_commit(&cb_bar);
-                // S C^T and S += (w x)^T B: need the bf16 state copy, the scaled
-                // state and w x (warps 4-7), and the last epilogue done with TMEM
+                TRACE(2, it);
+                // S C^T into inter buffer it & 1, and S += (w x)^T B: need the bf16
+                // state copy, the scaled state and w x (warps 4-7), and the
+                // epilogue two chunks back done with that inter buffer
                 if (!wait_bounded(&wg1_bar, it & 1, &abort_sh)) break;
-                if (it > 0 && !wait_bounded(&free_bar, (it - 1) & 1, &abort_sh)) break;
+                if (it >= 2 && !wait_bounded(&free_r3_bar[it & 1], ((it >> 1) & 1) ^ 1, &abort_sh)) break;
                 tc_fence_after();
                 const uint32_t ss = smem_u32(sbf);
 #pragma unroll
                 for (int ks = 0; ks < C::N / 16; ++ks) {
                     const uint32_t aoff = (ks / 4) * (C::M * 128) + (ks % 4) * 32;
                     const uint32_t boff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                    mma_bf16(tmem + C::COL_R3, sdesc(ss + aoff, 16, 1024), sdesc(sc + boff, 16, 1024), id_inter,
-                             ks > 0);
+                    mma_bf16(tmem + C::COL_R3 + (it & 1) * C::Q, sdesc(ss + aoff, 16, 1024),
+                             sdesc(sc + boff, 16, 1024), id_inter, ks > 0);
                 }
                 const uint32_t swh = smem_u32(xw_hi(xb)), swl = smem_u32(xw_lo(xb));
 #pragma unroll
@@ -621,8 +774,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     mma_bf16(tmem + C::COL_S, sdesc(swl + ks * 2048, C::Q * 128, 1024),
                              sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
                 mma_commit(&state_bar);
-                // X^T M_h^T per head: needs the score matrices (warps 8-11)
+                TRACE(3, it);
+                // X^T M_h^T per head: needs the score matrices (warps 8-11) and
+                // the last epilogue done with the intra buffers
                 if (!wait_bounded(&mask_bar, it & 1, &abort_sh)) break;
+                if (it > 0 && !wait_bounded(&free_r_bar, (it - 1) & 1, &abort_sh)) break;
                 tc_fence_after();
                 const uint32_t sm = smem_u32(mm);
 #pragma unroll
@@ -634,6 +790,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                                  sdesc(sm + boff, 16, 1024), id_intra, ks > 0);
                     }
                 mma_commit(&y_bar);
+                // every read of the stage and of the vector set is done once these MMAs are
+                mma_commit(&empty_bar[s]);
+                mma_commit(&vempty_bar[it % NV]);
+                TRACE(4, it);
             }
         }
     } else if (warp >= 4 && warp < 8) {
@@ -664,20 +824,25 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             }
             tmem_st_wait();
         }
+        if (gtid == 0) TRACE(13, 1);
         for (int it = 0; it < nch; ++it) {
             const int s = it % ST;
             const int xb = XWB == 2 ? (it & 1) : 0;
             if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[0], 1, gtid, 128)) break;
-            const float *vec = stage_v(s);
+            if (!group_wait(&vfull_bar[it % NV], (it / NV) & 1, &abort_sh, &slot[7], 1, gtid, 128)) break;
+            if (gtid == 0) TRACE(5, it);
+            const float *vv = vec(it % NV);
             if (XWB == 1 && it > 0) {
                 if (!group_wait(&state_bar, (it - 1) & 1, &abort_sh, &slot[1], 1, gtid, 128)) break;
             }
-            build_xw<C, 128>(stage_x(s), xw_hi(xb), xw_lo(xb), vec + 2 * C::HB * C::Q, gtid);
+            build_xw<C, 128>(stage_x(s), xw_hi(xb), xw_lo(xb), vv + C::V_W, gtid);
+            if (gtid == 0) TRACE(6, it);
             if (XWB == 2 && it > 0) {
                 if (!group_wait(&state_bar, (it - 1) & 1, &abort_sh, &slot[1], 1, gtid, 128)) break;
             }
+            if (gtid == 0) TRACE(7, it);
             tc_fence_after();
-            const float dec = vec[4 * C::HB * C::Q + rh];
+            const float dec = vv[C::V_DECAY + rh];
 #pragma unroll 1
             for (int n0 = 0; n0 < C::N; n0 += 32) {
                 float v0[16], v1[16];
@@ -707,7 +872,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             named_bar_sync(1, 128);
-            if (gtid == 0) mbar_arrive(&wg1_bar);
+            if (gtid == 0) {
+                TRACE(8, it);
+                mbar_arrive(&wg1_bar);
+            }
         }
         // final state after the segment's last chunk
         if (seg == prm.nseg - 1 && prm.fin) {  // (a uniform test: group_wait handles an abort)
@@ -728,100 +896,126 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
     } else if (warp >= 8 && warp < 12) {
         // ---------------- masked, decayed score matrices ----------------
+        //   M_h[t, s] = CB[t, s] exp(cum_t - cum_s) dt_s = CB[t, s] u_t v_s   (s <= t)
+        // Q = 64: C B^T is an M = 64 accumulator (rows 16 q4 .. 16 q4 + 15 in
+        // lanes 0-15); lanes 16-31 take the row of lane - 16 and either the
+        // second head (two heads) or the second half of the columns.
+        // Q = 128: lane = row, every thread covers all heads and columns.
         const int gtid = tid - 256;
-        int t;
-        bool active;
-        if (C::Q == 64) {  // M = 64 accumulator: rows 16 q4 .. 16 q4 + 15 in lanes 0-15
-            t = q4 * 16 + lane;
-            active = lane < 16;
-        } else {
-            t = q4 * 32 + lane;
-            active = true;
-        }
+        constexpr bool HALVES = C::Q == 64;
+        const int t = HALVES ? q4 * 16 + (lane & 15) : q4 * 32 + lane;
+        const int half = HALVES ? (lane >> 4) : 0;
+        constexpr int NH = (HALVES && C::HB == 2) ? 1 : C::HB;              // heads per thread
+        constexpr int NCOL = (HALVES && C::HB == 1) ? C::Q / 2 : C::Q;       // columns per thread
         for (int it = 0; it < nch; ++it) {
-            const int s = it % ST;
-            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[3], 2, gtid, 128)) break;
+            if (!group_wait(&vfull_bar[it % NV], (it / NV) & 1, &abort_sh, &slot[3], 2, gtid, 128)) break;
             if (!group_wait(&cb_bar, it & 1, &abort_sh, &slot[4], 2, gtid, 128)) break;
+            if (gtid == 0) TRACE(9, it);
             tc_fence_after();
-            const float *vec = stage_v(s);
-            const float *dtv = vec, *cum = vec + C::HB * C::Q;
+            const float *vv = vec(it % NV);
 #pragma unroll 1
-            for (int s0 = 0; s0 < C::Q; s0 += 16) {
-                float cb[16];
-                tmem_ld16(tmem + lane_off + C::COL_CB + s0, cb);
+            for (int cb0 = 0; cb0 < C::Q; cb0 += 32) {
+                float cb[32];
+                tmem_ld16(tmem + lane_off + C::COL_CB + cb0, *reinterpret_cast<float(*)[16]>(cb));
+                tmem_ld16(tmem + lane_off + C::COL_CB + cb0 + 16, *reinterpret_cast<float(*)[16]>(cb + 16));
                 tmem_ld_wait();
-                if (active) {
+                if (HALVES) {
 #pragma unroll
-                    for (int hh = 0; hh < C::HB; ++hh) {
-                        const float ct = cum[hh * C::Q + t];
-                        uint8_t *dst = mm + hh * (C::Q * C::Q * 2) + (s0 / 64) * (C::Q * 128);
+                    for (int j = 0; j < 32; ++j) cb[j] = __shfl_sync(0xffffffffu, cb[j], lane & 15);
+                }
+                // (two heads: each half-warp its head; one head: each half-warp
+                // its half of the columns)
+                const bool mine = !(HALVES && C::HB == 1) || (cb0 / 32) == half;
 #pragma unroll
-                        for (int jj = 0; jj < 2; ++jj) {
-                            float m[8];
+                for (int hi = 0; hi < (mine ? NH : 0); ++hi) {
+                    const int hh = (HALVES && C::HB == 2) ? half : hi;
+                    const float *vvv = vv + C::V_V + hh * C::Q;
+                    const bool wide = vv[C::V_WIDE + hh] != 0.f;
+                    const float ut = vv[C::V_U + hh * C::Q + t];
+                    uint8_t *dst = mm + hh * (C::Q * C::Q * 2) + (cb0 / 64) * (C::Q * 128);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        float m[8];
+                        if (!wide) {
+                            const float4 va = *reinterpret_cast<const float4 *>(vvv + cb0 + jj * 8);
+                            const float4 vb = *reinterpret_cast<const float4 *>(vvv + cb0 + jj * 8 + 4);
+                            const float vs[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
                             for (int j = 0; j < 8; ++j) {
-                                const int sc = s0 + jj * 8 + j;
-                                m[j] = (sc <= t) ? cb[jj * 8 + j] * __expf(ct - cum[hh * C::Q + sc]) * dtv[hh * C::Q + sc]
-                                                 : 0.f;
+                                const int sc = cb0 + jj * 8 + j;
+                                const float prod = cb[jj * 8 + j] * ut * vs[j];
+                                m[j] = sc <= t ? prod : 0.f;
                             }
-                            uint4 pk;
-                            pk.x = pack_bf16x2(m[0], m[1]);
-                            pk.y = pack_bf16x2(m[2], m[3]);
-                            pk.z = pack_bf16x2(m[4], m[5]);
-                            pk.w = pack_bf16x2(m[6], m[7]);
-                            *reinterpret_cast<uint4 *>(dst + swz128(t, (s0 % 64) + jj * 8)) = pk;
+                        } else {
+                            const float ct = vv[C::V_CUM + hh * C::Q + t];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int sc = cb0 + jj * 8 + j;
+                                m[j] = sc <= t ? cb[jj * 8 + j] * __expf(ct - vv[C::V_CUM + hh * C::Q + sc]) *
+                                                     vv[C::V_DT + hh * C::Q + sc]
+                                               : 0.f;
+                            }
                         }
+                        uint4 pk;
+                        pk.x = pack_bf16x2(m[0], m[1]);
+                        pk.y = pack_bf16x2(m[2], m[3]);
+                        pk.z = pack_bf16x2(m[4], m[5]);
+                        pk.w = pack_bf16x2(m[6], m[7]);
+                        *reinterpret_cast<uint4 *>(dst + swz128(t, (cb0 % 64) + jj * 8)) = pk;
                     }
                 }
+                __syncwarp();
             }
+            (void)NCOL;
+            // exp(cum) for the epilogue (the stage may be refilled before it runs)
+            for (int i = gtid; i < HQ; i += 128) epi_vec[(it & 1) * HQ + i] = vv[C::V_ECUM + i];
             fence_async_smem();
             tc_fence_before();
             named_bar_sync(2, 128);
-            if (gtid == 0) mbar_arrive(&mask_bar);
+            if (gtid == 0) {
+                TRACE(10, it);
+                mbar_arrive(&mask_bar);
+                mbar_arrive(&epi_bar[it & 1]);
+            }
         }
     } else if (warp >= 12) {
         // ---------------- epilogue ----------------
+        // y = intra + exp(cum) inter + D x for row (head, p), 16 steps t at a
+        // time: TMEM loads, x from L2 (the tile was just loaded), stores.
         const int gtid = tid - 384;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const long long hrow = h0 + rh;
-        const float dh = (prm.D && hrow < H) ? prm.D[hrow] : 0.f;
-        const int pc = rp % 64;
+        const bool live = hrow < H;
+        const float dh = (prm.D && live) ? prm.D[hrow] : 0.f;
+        const long long ystride = H * C::P;
+        auto row_base = [&](int c) {
+            return (((long long)b * L + (long long)c * C::Q) * H + (live ? hrow : 0)) * C::P + rp;
+        };
+        uint32_t xp[C::Q / 2];
+        fetch_x_column<C>(prm.x + row_base(c0), ystride, live, xp);
         for (int it = 0; it < nch; ++it) {
-            const int s = it % ST;
             const int c = c0 + it;
-            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[5], 3, gtid, 128)) break;
             if (!group_wait(&y_bar, it & 1, &abort_sh, &slot[6], 3, gtid, 128)) break;
+            if (!group_wait(&epi_bar[it & 1], (it >> 1) & 1, &abort_sh, &slot[5], 3, gtid, 128)) break;
+            if (gtid == 0) TRACE(11, it);
             tc_fence_after();
-            const float *ecum = stage_v(s) + 3 * C::HB * C::Q + rh * C::Q;
-            const uint8_t *xrow = stage_x(s) + (rh * C::PB + rp / 64) * (C::Q * 128);
-            const long long ybase = (((long long)b * L + (long long)c * C::Q) * H + hrow) * C::P + rp;
-#pragma unroll 1
-            for (int t0 = 0; t0 < C::Q; t0 += 16) {
-                float ri[16], re[16];
-                tmem_ld16(tmem + lane_off + C::COL_R + rh * C::Q + t0, ri);
-                tmem_ld16(tmem + lane_off + C::COL_R3 + t0, re);
-                tmem_ld_wait();
-                if (hrow < H) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int t = t0 + j;
-                        const float xv = __bfloat162float(*reinterpret_cast<const bf16 *>(xrow + swz128(t, pc)));
-                        const float yv = fmaf(ecum[t], re[j], ri[j]) + dh * xv;
-                        const long long off = ybase + (long long)t * H * C::P;
-                        if (prm.y_f32)
-                            __stcs(reinterpret_cast<float *>(prm.y) + off, yv);
-                        else
-                            reinterpret_cast<bf16 *>(prm.y)[off] = __float2bfloat16_rn(yv);
-                    }
-                }
-            }
-            fence_async_smem();
+            const float *ecum = epi_vec + (it & 1) * HQ + rh * C::Q;
+            const long long base = row_base(c);
+            if (prm.y_f32)
+                epilogue_rows<C, float>(tmem + lane_off, it, rh, ecum, xp, reinterpret_cast<float *>(prm.y) + base,
+                                        ystride, dh, live);
+            else
+                epilogue_rows<C, bf16>(tmem + lane_off, it, rh, ecum, xp, reinterpret_cast<bf16 *>(prm.y) + base,
+                                       ystride, dh, live);
+            // TMEM reads are done: let the next chunk's MMAs in, then fetch its x
             tc_fence_before();
             named_bar_sync(3, 128);
             if (gtid == 0) {
-                mbar_arrive(&free_bar);
-                mbar_arrive(&empty_bar[s]);
+                TRACE(12, it);
+                mbar_arrive(&free_r_bar);
+                mbar_arrive(&free_r3_bar[it & 1]);
             }
+            if (it + 1 < nch) fetch_x_column<C>(prm.x + row_base(c + 1), ystride, live, xp);
         }
     }
     // let this CTA's own copies and MMAs land (they normally have) before
@@ -888,12 +1082,16 @@ Plan plan_for(const Dims &d) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Workspace: status word | per-unit counters | segment states | segment totals.
-// The first two are cleared on the stream by every call.
+// Workspace: status word | segment states | segment totals.  The status
+// word is cleared on the stream by every call.
 template <class C>
-size_t header_bytes(const Dims &d) {
-    return 256 + align256(sizeof(unsigned) * d.b * plan_for<C>(d).nhb);
+size_t header_bytes(const Dims &) {
+    return 256;
 }
+
+#ifdef SSD_TRACE
+constexpr size_t kTraceBytes = 32 * 256 * sizeof(long long);
+#endif
 
 template <class C>
 size_t workspace_for(const Dims &d) {
@@ -901,6 +1099,9 @@ size_t workspace_for(const Dims &d) {
     size_t bytes = header_bytes<C>(d);
     if (p.nseg > 1)
         bytes += align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N) + align256(sizeof(float) * d.b * p.nseg * d.H);
+#ifdef SSD_TRACE
+    bytes += kTraceBytes;
+#endif
     return bytes;
 }
 
@@ -914,6 +1115,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
         !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
     TcParams prm;
+    prm.x = static_cast<const bf16 *>(x);
     prm.dt = static_cast<const bf16 *>(dt);
     prm.A = A;
     prm.D = D;
@@ -923,7 +1125,6 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     char *w = static_cast<char *>(ws);
     const size_t hdr = header_bytes<C>(d);
     prm.status = reinterpret_cast<unsigned *>(w);
-    prm.counter = reinterpret_cast<unsigned *>(w + 256);
     prm.seg_state = nullptr;
     prm.seg_tot = nullptr;
     if (p.nseg > 1) {
@@ -931,6 +1132,10 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
         prm.seg_tot = reinterpret_cast<float *>(w + hdr + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
     }
     prm.nhb = p.nhb;
+    prm.trace = nullptr;
+#ifdef SSD_TRACE
+    prm.trace = reinterpret_cast<long long *>(w + workspace_for<C>(d) - kTraceBytes);
+#endif
     prm.b = d.b;
     prm.L = d.L;
     prm.H = d.H;
@@ -966,6 +1171,12 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         timing_mark(s, "seg_state_tc");
+        const int pn = (int)(C::P * C::N);
+        dim3 pgrid((unsigned)((pn / 4 + 255) / 256), (unsigned)d.H, (unsigned)d.b);
+        segment_pass_kernel<<<pgrid, 256, 0, s>>>(init, prm.seg_state, prm.seg_tot, d.H, pn, p.nseg);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        timing_mark(s, "segment_pass");
     }
     dim3 grid(p.nseg, p.nhb, (unsigned)d.b);
     chunk_scan_kernel<C><<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
@@ -978,7 +1189,6 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
 template <class F>
 bool dispatch(const Dims &d, F &&f) {
     if (d.P == 64 && d.N == 128 && d.Q == 64) return f(Cfg<64, 128, 64>{}), true;
-    if (d.P == 64 && d.N == 128 && d.Q == 128) return f(Cfg<64, 128, 128>{}), true;
     if (d.P == 128 && d.N == 256 && d.Q == 64) return f(Cfg<128, 256, 64>{}), true;
     if (d.P == 64 && d.N == 64 && d.Q == 64) return f(Cfg<64, 64, 64>{}), true;
     return false;
