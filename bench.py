@@ -412,6 +412,19 @@ def main():
         torch.distributed.destroy_process_group()
 
 
+def tc_plan(cfg, target_ctas=148):
+    """Segment plan of the fused tensor-core path (mirrors the library):
+    CTAs own 128/P heads; segments of consecutive chunks fill ~148 CTAs."""
+    hb = 128 // cfg.headdim
+    nhb = -(-cfg.nheads // hb)
+    units = cfg.batch * nhb
+    nc = cfg.seqlen // cfg.chunk_size
+    nseg = max(1, min(nc, target_ctas // units))
+    cps = -(-nc // nseg)
+    nseg = -(-nc // cps)
+    return nseg, cps, nc
+
+
 def KERNEL_BYTES(cfg, name):
     """Algorithmic bytes one launch of the named kernel must move."""
     b, L, H, P, N, G, Q = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups, cfg.chunk_size
@@ -425,11 +438,18 @@ def KERNEL_BYTES(cfg, name):
     y = b * L * H * P * 4
     init = b * H * P * N * 4 if cfg.has_init else 0
     fin = b * H * P * N * 4
+    nseg, cps, _ = tc_plan(cfg)
+    seg_states = b * (nseg - 1) * H * P * N * 4
+    covered = min(nc, (nseg - 1) * cps) / nc  # share of the sequence the segment-state kernel reads
     return {
         "chunk_cumsum": dt + cum,
         "chunk_state_simt": x + dt + bc + cum + st,
         "state_passing": st + cum + init + st + fin,
         "chunk_scan_simt": x + dt + 2 * bc + cum + st + y,
+        # fused tensor-core path
+        "seg_state_tc": covered * (x + dt + bc) + seg_states,
+        "segment_pass": 2 * seg_states + init,
+        "chunk_scan_tc": x + dt + 2 * bc + seg_states + init + y + fin,
     }.get(name, compulsory_bytes(cfg))
 
 
