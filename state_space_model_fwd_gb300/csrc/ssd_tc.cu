@@ -124,7 +124,17 @@ struct Cfg {
         if (prm.trace && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (it) < 256)          \
             prm.trace[(ev) * 256 + (it)] = clock64();                                                  \
     } while (0)
+#define TRACE_CTA(slot)                                                                                 \
+    do {                                                                                                 \
+        if (prm.trace) {                                                                                 \
+            const int cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);             \
+            if (cta_ < 1024) prm.trace[32 * 256 + 2 * cta_ + (slot)] = (long long)globaltimer_ns();       \
+        }                                                                                                \
+    } while (0)
 #else
+#define TRACE_CTA(slot) \
+    do {                \
+    } while (0)
 #define TRACE(ev, it) \
     do {              \
     } while (0)
@@ -528,6 +538,23 @@ __global__ void __launch_bounds__(256) segment_pass_kernel(const float *__restri
     }
 }
 
+// Scores of a chunk whose decay range is too wide to factor in fp32: direct
+// exponent per entry (rare; kept out of line so the hot loop stays small).
+struct F8 {
+    float v[8];
+};
+
+__device__ __noinline__ F8 wide_scores(F8 cb, const float *cum, const float *dtv, int t, int s0) {
+    const float ct = cum[t];
+    F8 m;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int sc = s0 + j;
+        m.v[j] = sc <= t ? cb.v[j] * __expf(ct - cum[sc]) * dtv[sc] : 0.f;
+    }
+    return m;
+}
+
 template <typename T>
 __device__ __forceinline__ void store_y(T *p, float v);
 template <>
@@ -588,7 +615,7 @@ __device__ __forceinline__ void epilogue_rows(uint32_t tmem_lane, int it, int rh
 // ===========================================================================
 constexpr int kScanThreads = 512;
 
-template <class C>
+template <class C, typename YT>
 __global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
                       const __grid_constant__ CUtensorMap mc, TcParams prm) {
@@ -654,7 +681,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) TRACE(13, 0);
+    if (tid == 0) {
+        TRACE(13, 0);
+        TRACE_CTA(0);
+    }
     const uint32_t tmem = tmem_base_sh;
     int nload[2] = {0, 0};  // TMA loads issued per stage (producer lane 0)
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
@@ -947,14 +977,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                                 m[j] = sc <= t ? prod : 0.f;
                             }
                         } else {
-                            const float ct = vv[C::V_CUM + hh * C::Q + t];
+                            F8 c8;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int sc = cb0 + jj * 8 + j;
-                                m[j] = sc <= t ? cb[jj * 8 + j] * __expf(ct - vv[C::V_CUM + hh * C::Q + sc]) *
-                                                     vv[C::V_DT + hh * C::Q + sc]
-                                               : 0.f;
-                            }
+                            for (int j = 0; j < 8; ++j) c8.v[j] = cb[jj * 8 + j];
+                            const F8 r8 = wide_scores(c8, vv + C::V_CUM + hh * C::Q, vv + C::V_DT + hh * C::Q, t,
+                                                      cb0 + jj * 8);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) m[j] = r8.v[j];
                         }
                         uint4 pk;
                         pk.x = pack_bf16x2(m[0], m[1]);
@@ -1001,12 +1030,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             tc_fence_after();
             const float *ecum = epi_vec + (it & 1) * HQ + rh * C::Q;
             const long long base = row_base(c);
-            if (prm.y_f32)
-                epilogue_rows<C, float>(tmem + lane_off, it, rh, ecum, xp, reinterpret_cast<float *>(prm.y) + base,
-                                        ystride, dh, live);
-            else
-                epilogue_rows<C, bf16>(tmem + lane_off, it, rh, ecum, xp, reinterpret_cast<bf16 *>(prm.y) + base,
-                                       ystride, dh, live);
+            epilogue_rows<C, YT>(tmem + lane_off, it, rh, ecum, xp, reinterpret_cast<YT *>(prm.y) + base, ystride,
+                                 dh, live);
             // TMEM reads are done: let the next chunk's MMAs in, then fetch its x
             tc_fence_before();
             named_bar_sync(3, 128);
@@ -1030,6 +1055,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) flag_timeout(prm.status);
+    if (tid == 0) TRACE_CTA(1);
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
@@ -1090,7 +1116,7 @@ size_t header_bytes(const Dims &) {
 }
 
 #ifdef SSD_TRACE
-constexpr size_t kTraceBytes = 32 * 256 * sizeof(long long);
+constexpr size_t kTraceBytes = (32 * 256 + 2048) * sizeof(long long);
 #endif
 
 template <class C>
@@ -1148,10 +1174,14 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
 
     // raise each kernel's dynamic shared memory limit to what this call needs
     static int scan_attr = 0, seg_attr = 0;
+    auto scan_kernel = prm.y_f32 ? chunk_scan_kernel<C, float> : chunk_scan_kernel<C, bf16>;
     const int seg_smem = C::SMEM_SEG_BASE + (int)(C::HB * p.cps * sizeof(float));
     if (scan_attr < C::SMEM_SCAN) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_SCAN);
+        cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<C, float>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_SCAN);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chunk_scan_kernel<C, bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM_SCAN);
         if (e != cudaSuccess) return e;
         scan_attr = C::SMEM_SCAN;
     }
@@ -1179,7 +1209,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
         timing_mark(s, "segment_pass");
     }
     dim3 grid(p.nseg, p.nhb, (unsigned)d.b);
-    chunk_scan_kernel<C><<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
+    scan_kernel<<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
     e = cudaGetLastError();
     timing_mark(s, "chunk_scan_tc");
     return e;
