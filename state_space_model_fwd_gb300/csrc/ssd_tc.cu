@@ -56,7 +56,9 @@ struct TcParams {
     void *y;
     float *fin;
     float *seg_state;   // [b, nseg, H, P, N]: segment-local states, then (in place) states entering segments
-    float *seg_tot;     // [b, H, nseg]  total dt*A of each segment
+    float *seg_tot;     // [b, H, nseg]  total dt*A of each segment (may be null)
+    const float *cum_in;    // [b, H, nc, Q] given in-chunk cumulative decay (null: computed from dt, A)
+    const float *entering;  // [b, nseg, H, P, N] state entering each segment (null: init / segment pass)
     unsigned *status;   // bit 0: a wait gave up
     long long b, L, H, G;
     int hpg, nc, nseg, cps;  // cps: chunks per segment
@@ -197,6 +199,24 @@ __device__ __forceinline__ float warp_chunk_cumsum(const float *dtv, float a, fl
     return __shfl_sync(0xffffffffu, tot, 31);
 }
 
+// In-chunk cumulative decay of chunk c for head h into cum[Q] (one warp):
+// read from the caller's dA_cumsum when given, else the scan of dt*A.
+// Returns the chunk total.
+template <class C>
+__device__ __forceinline__ float chunk_cum(const TcParams &prm, int b, long long h, int c, const float *dtv, float a,
+                                           float *cum) {
+    if (prm.cum_in) {
+        const int lane = threadIdx.x & 31;
+        const float *src = prm.cum_in + (((long long)b * prm.H + (h < prm.H ? h : 0)) * prm.nc + c) * C::Q;
+        for (int q = lane; q < C::Q; q += 32) cum[q] = h < prm.H ? __ldg(src + q) : 0.f;
+        __syncwarp();
+        return cum[C::Q - 1];
+    }
+    const float total = warp_chunk_cumsum<C::Q>(dtv, a, cum);
+    __syncwarp();
+    return total;
+}
+
 // x tile scaled row-wise by w, split into two bf16 tiles whose sum carries
 // the product to about 2^-17 relative: hi = bf16(w x), lo = bf16(w x - hi).
 // (One bf16 rounding of w x, 2^-9 relative, is visible in the state entries
@@ -334,14 +354,20 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             const int hh = valid ? j / nch : 0, k = valid ? j % nch : 0;
             const long long h = h0 + hh;
             float sum = 0.f;
-            if (valid && h < H)
+            if (valid && h < H && !prm.cum_in)
 #pragma unroll 4
                 for (int q = gl; q < C::Q; q += 8)
                     sum += __bfloat162float(prm.dt[((long long)b * prm.L + (long long)(c0 + k) * C::Q + q) * H + h]);
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if (valid && gl == 0) tot_s[hh * prm.cps + k] = h < H ? sum * prm.A[h] : 0.f;
+            if (valid && gl == 0) {
+                float tot = 0.f;
+                if (h < H)  // (with a given cumulative decay, A is not an input)
+                    tot = prm.cum_in ? prm.cum_in[(((long long)b * H + h) * prm.nc + c0 + k) * C::Q + C::Q - 1]
+                                     : sum * prm.A[h];
+                tot_s[hh * prm.cps + k] = tot;
+            }
         }
     }
     tc_fence_before();
@@ -356,7 +382,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             run += t;
         }
         const long long h = h0 + tid;
-        if (h < H) prm.seg_tot[((long long)b * H + h) * prm.nseg + seg] = run;
+        if (h < H && prm.seg_tot) prm.seg_tot[((long long)b * H + h) * prm.nseg + seg] = run;
     }
     __syncthreads();
     const uint32_t tmem = tmem_base_sh;
@@ -401,11 +427,10 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
                 const long long h = h0 + hh;
-                const float a = h < H ? prm.A[h] : 0.f;
+                const float a = (h < H && prm.A) ? prm.A[h] : 0.f;
                 float *cum = vv + C::V_CUM + hh * C::Q;
                 const float *dtv = vv + C::V_DT + hh * C::Q;
-                const float total = warp_chunk_cumsum<C::Q>(dtv, a, cum);
-                __syncwarp();
+                const float total = chunk_cum<C>(prm, b, h, c0 + it, dtv, a, cum);
                 const float after = tot_s[hh * prm.cps + it];
                 for (int q = lane; q < C::Q; q += 32)
                     vv[C::V_W + hh * C::Q + q] = __expf(after + total - cum[q]) * dtv[q];
@@ -731,11 +756,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
                 const long long h = h0 + hh;
-                const float a = h < H ? prm.A[h] : 0.f;
+                const float a = (h < H && prm.A) ? prm.A[h] : 0.f;
                 float *cum = vv + C::V_CUM + hh * C::Q;
                 const float *dtv = vv + C::V_DT + hh * C::Q;
-                const float total = warp_chunk_cumsum<C::Q>(dtv, a, cum);
-                __syncwarp();
+                const float total = chunk_cum<C>(prm, b, h, c0 + it, dtv, a, cum);
                 const float r = cum[C::Q / 2 - 1];
                 // exp(cum_t - cum_s) = u_t v_s / dt_s factors in fp32 only while
                 // each half-chunk's decay stays within e^80
@@ -834,7 +858,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         // state entering the segment
         {
             const float *src = nullptr;
-            if (seg > 0)
+            if (prm.entering)
+                src = prm.entering + ((((long long)b * prm.nseg + seg) * H + hrow) * C::P + rp) * C::N;
+            else if (seg > 0)
                 src = prm.seg_state + ((((long long)b * prm.nseg + (seg - 1)) * H + hrow) * C::P + rp) * C::N;
             else if (prm.init)
                 src = prm.init + (((long long)b * H + hrow) * C::P + rp) * C::N;
@@ -1158,6 +1184,8 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
         prm.seg_tot = reinterpret_cast<float *>(w + hdr + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
     }
     prm.nhb = p.nhb;
+    prm.cum_in = nullptr;
+    prm.entering = nullptr;
     prm.trace = nullptr;
 #ifdef SSD_TRACE
     prm.trace = reinterpret_cast<long long *>(w + workspace_for<C>(d) - kTraceBytes);
@@ -1256,14 +1284,111 @@ cudaError_t tc_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void 
     return e;
 }
 
-bool tc_stage_supported(const Dims &, ssd_dtype_t) { return false; }
-cudaError_t tc_chunk_state(const Dims &, const void *, const void *, const void *, const float *, float *,
-                           cudaStream_t) {
-    return cudaErrorNotSupported;
+bool tc_stage_supported(const Dims &d, ssd_dtype_t dtype) {
+    if (dtype != SSD_DTYPE_BF16 || d.L == 0 || d.b == 0) return false;
+    bool ok = false;
+    dispatch(d, [&](auto c) {
+        using C = decltype(c);
+        ok = C::SCAN_FITS && C::TMEM_FITS && (d.G == 1 || d.hpg % C::HB == 0) && d.L < (1ll << 31) &&
+             d.H < (1 << 30) && d.b < 65536 && d.nc < 65536 &&
+             C::SMEM_SEG_BASE + (int)(C::HB * sizeof(float)) <= kSmemLimit;
+    });
+    return ok;
 }
-cudaError_t tc_chunk_scan(const Dims &, ssd_dtype_t, const void *, const void *, const void *, const void *,
-                          const float *, const float *, const float *, void *, cudaStream_t) {
-    return cudaErrorNotSupported;
+
+namespace {
+
+// Parameters of a one-chunk-per-segment launch of the fused kernels, as the
+// stage entry points use them.
+TcParams stage_params(const Dims &d, const void *dt, const float *cum) {
+    TcParams prm{};
+    prm.dt = static_cast<const bf16 *>(dt);
+    prm.cum_in = cum;
+    prm.b = d.b;
+    prm.L = d.L;
+    prm.H = d.H;
+    prm.G = d.G;
+    prm.hpg = d.hpg;
+    prm.nc = (int)d.nc;
+    prm.nseg = (int)d.nc;
+    prm.cps = 1;
+    prm.y_f32 = 1;
+    return prm;
+}
+
+template <class C>
+cudaError_t run_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
+                            float *states, cudaStream_t s) {
+    CUtensorMap mx, mb;
+    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q))
+        return cudaErrorInvalidValue;
+    TcParams prm = stage_params(d, dt, cum);
+    prm.seg_state = states;  // [b, nc, H, P, N]: one segment per chunk
+    prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
+    const int smem = C::SMEM_SEG_BASE + (int)(C::HB * sizeof(float));
+    static int attr = 0;
+    if (attr < smem) {
+        cudaError_t e = cudaFuncSetAttribute(seg_state_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = smem;
+    }
+    timing_begin(s);
+    dim3 grid((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b);
+    seg_state_kernel<C><<<grid, kSegThreads, smem, s>>>(mx, mb, prm);
+    const cudaError_t e = cudaGetLastError();
+    timing_mark(s, "chunk_state_tc");
+    return e;
+}
+
+template <class C>
+cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
+                           const void *Cm, const float *cum, const float *states_in, const float *D, void *y,
+                           cudaStream_t s) {
+    CUtensorMap mx, mb, mc;
+    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) ||
+        !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
+        return cudaErrorInvalidValue;
+    TcParams prm = stage_params(d, dt, cum);
+    prm.x = static_cast<const bf16 *>(x);
+    prm.entering = states_in;  // [b, nc, H, P, N]: the state entering each chunk
+    prm.D = D;
+    prm.y = y;
+    prm.y_f32 = ydtype == SSD_DTYPE_F32 ? 1 : 0;
+    prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
+    static int attr = 0;
+    if (attr < C::SMEM_SCAN) {
+        cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<C, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_SCAN);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chunk_scan_kernel<C, bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM_SCAN);
+        if (e != cudaSuccess) return e;
+        attr = C::SMEM_SCAN;
+    }
+    auto kern = prm.y_f32 ? chunk_scan_kernel<C, float> : chunk_scan_kernel<C, bf16>;
+    timing_begin(s);
+    dim3 grid((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b);
+    kern<<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
+    const cudaError_t e = cudaGetLastError();
+    timing_mark(s, "chunk_scan_stage_tc");
+    return e;
+}
+
+}  // namespace
+
+cudaError_t tc_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
+                           float *states, cudaStream_t s) {
+    cudaError_t e = cudaErrorNotSupported;
+    dispatch(d, [&](auto c) { e = run_chunk_state<decltype(c)>(d, x, dt, B, cum, states, s); });
+    return e;
+}
+
+cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
+                          const void *C, const float *cum, const float *states_in, const float *D, void *y,
+                          cudaStream_t s) {
+    cudaError_t e = cudaErrorNotSupported;
+    dispatch(d, [&](auto c) { e = run_chunk_scan<decltype(c)>(d, ydtype, x, dt, B, C, cum, states_in, D, y, s); });
+    return e;
 }
 
 }  // namespace ssd

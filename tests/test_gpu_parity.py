@@ -128,7 +128,8 @@ def test_ssd_fwd_no_optional_inputs():
     check(to_np(y), y_ref, TOL["bf16"], "no D / init / final y")
 
 
-@pytest.mark.parametrize("name", ["tiny_f32", "bf16_p64_n128", "bf16_p128_n256_q128", "bf16_p16_n16"])
+@pytest.mark.parametrize("name", ["tiny_f32", "bf16_p64_n128", "bf16_p128_n256_q128", "bf16_p16_n16",
+                                  "tc_p64_n128_seg", "tc_p64_n128_g2", "bf16_p128_n256_q64", "bf16_p64_n128_h5"])
 def test_stages_against_definitions(name):
     """Each stage entry point against the oracle's definition of its output,
     fed the oracle's own (rounded to fp32) inputs for the stage."""
@@ -155,6 +156,24 @@ def test_stages_against_definitions(name):
                            torch.from_numpy(sin_ref.astype(np.float32)).cuda(), t["D"])
     y_ref, _ = oracle_full(inp)
     check(to_np(y), y_ref, tol, "chunk scan y")
+
+
+@pytest.mark.parametrize("name", ["tc_p64_n128_seg", "bf16_p128_n256_q64"])
+def test_stage_chain_matches_fused(name):
+    """cumsum -> chunk_state -> state_passing -> chunk_scan (each on its own
+    kernel) against ssd_fwd and the oracle, y in fp32 and in bf16."""
+    cfg = SMALL[name]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    Q = cfg.chunk_size
+    cum = ssd.ssd_chunk_cumsum(t["dt"], t["A"], Q)
+    st = ssd.ssd_chunk_state(t["x"], t["dt"], t["B"], cum)
+    sin, fin = ssd.ssd_state_passing(st, cum, t["init_state"])
+    y_ref, fin_ref = oracle_full(inp)
+    for y_dtype, tol in ((torch.float32, TOL["bf16"]), (torch.bfloat16, TOL["bf16"] + bf16_half_ulp_rel(y_ref))):
+        y = ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum, sin, t["D"], y_dtype=y_dtype)
+        check(to_np(y), y_ref, tol, f"{name} staged y ({y_dtype})")
+    check(to_np(fin), fin_ref, TOL["bf16"], f"{name} staged final")
 
 
 @pytest.mark.parametrize("name", ["tiny_f32", "f32_p32_n64_init", "bf16_p64_n128", "bf16_p128_n256_q64",
