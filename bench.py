@@ -441,15 +441,17 @@ def KERNEL_BYTES(cfg, name):
     nseg, cps, _ = tc_plan(cfg)
     seg_states = b * (nseg - 1) * H * P * N * 4
     covered = min(nc, (nseg - 1) * cps) / nc  # share of the sequence the segment-state kernel reads
+    cbm = b * nc * G * Q * Q * 2  # masked C B^T of every (chunk, group), bf16
     return {
         "chunk_cumsum": dt + cum,
         "chunk_state_simt": x + dt + bc + cum + st,
         "state_passing": st + cum + init + st + fin,
         "chunk_scan_simt": x + dt + 2 * bc + cum + st + y,
-        # fused tensor-core path
-        "seg_state_tc": covered * (x + dt + bc) + seg_states,
-        "segment_pass": 2 * seg_states + init,
-        "chunk_scan_tc": x + dt + 2 * bc + seg_states + init + y + fin,
+        # fused tensor-core path: C B^T, segment states (with the pass across
+        # segments: one read and one write of every segment state), chunk scan
+        "cb_mask_tc": 2 * bc + cbm,
+        "seg_state_tc": covered * (x + dt + bc) + 3 * seg_states + (init if nseg > 1 else 0),
+        "chunk_scan_tc": x + dt + 2 * bc + cbm + seg_states + init + y + fin,
     }.get(name, compulsory_bytes(cfg))
 
 

@@ -1,38 +1,42 @@
 // ssd_tc.cu -- tcgen05 / TMEM / TMA kernels of libssd (bf16 inputs, fp32
 // state and accumulation).
 //
-// The fused forward runs in two launches over "segments" (runs of
-// consecutive chunks of one batch entry and one head block):
+// Per head, with cum_t the in-chunk cumulative decay (the sum of dt*A over
+// the chunk's steps up to t) and T the cum of the chunk's last step, one
+// chunk of the forward pass is
+//   y_t   = exp(cum_t) C_t S_in + sum_{s<=t} (C_t . B_s) exp(cum_t - cum_s) dt_s x_s + D x_t
+//   S_out = exp(T) S_in + sum_s exp(T - cum_s) dt_s x_s B_s^T
+// (cumulative decay, the state entering each chunk and the outputs, with
+// the intra-chunk interactions kept on-chip: "Mamba-2 in NVIDIA cuTile:
+// Faster Forward Kernels", section "Why Mamba-2 is a useful kernel example";
+// quadratic inside a chunk and linear across chunks: the da_be19 thread,
+// post 5/6).
 //
-//   seg_state_kernel  (segments 0 .. nseg-2)
-//       S_seg = sum over the segment's tokens t of
-//               exp(sum_{k>t, k in segment} dt_k A) dt_t x_t^T B_t
-//       one long-K tcgen05 contraction per segment, accumulated in TMEM;
-//       writes S_seg and the segment's total log-decay to the workspace.
-//       The last CTA of each (batch, head block) to finish then passes the
-//       states across segments in order, leaving the state entering each
-//       segment in the workspace.
+// Every per-head decay is kept out of the score matrix.  With a per-head
+// exponent rho the state is held scaled, Ss = exp(rho) S_in, and
+//   a_s  = exp(rho - cum_s) dt_s x_s                  A operand (TMEM)
+//   R_t  = C_t . Ss + sum_{s<=t} CB[t, s] a_s          one tcgen05 accumulator
+//   y_t  = exp(cum_t - rho) R_t + D x_t
+//   Ss  <- Ss + sum_s a_s B_s^T  = exp(rho - T) S_out  (rho <- rho - T)
+// CB = C B^T masked to s <= t does not depend on the head: it is computed
+// once per chunk and group (cb_mask_kernel) and read by every head block
+// that shares the group, as the B operand of the intra-chunk contraction.
+// rho moves only when an exponent would leave [-kLambda, kLambda] (Ss is
+// then rescaled in TMEM); a chunk whose own decay range exceeds 2 kLambda
+// takes a direct per-entry path for its intra-chunk term.
 //
-//   chunk_scan_kernel (every segment)
-//       folds the earlier segments' states into the state entering the
-//       segment, then walks its chunks: per chunk
-//         CB   = C B^T                              (tcgen05, shared by heads)
-//         M_h  = CB o exp(cum_t - cum_s) dt_s, s<=t (CUDA cores, bf16, smem)
-//         Y^T  = X^T M_h^T (intra) + S C^T (inter)  (tcgen05, TMEM)
-//         y    = intra + exp(cum_t) inter + D x     (epilogue, straight to HBM)
-//         S    = exp(cum_last) S + (w o X)^T B      (TMEM, w_s = exp(cum_last - cum_s) dt_s)
-//       so the running state and the Q x Q score matrix never leave the SM.
-//
-// ("Mamba-2 in NVIDIA cuTile: Faster Forward Kernels", section "Why Mamba-2
-// is a useful kernel example": cumulative decay, state entering each chunk,
-// outputs, with the intra-chunk interactions kept on-chip; the da_be19
-// thread, post 5/6: quadratic inside a chunk, linear across chunks, the
-// work dominated by batched matrix multiplications.)
+// The fused forward is three launches:
+//   cb_mask_kernel     CB of every (chunk, group), bf16
+//   seg_state_kernel   the local state of each segment (a run of consecutive
+//                      chunks) but the last, one long-K contraction per
+//                      segment; the last CTA of each (batch, head block)
+//                      passes the states across the segments
+//   chunk_scan_kernel  every segment: the scaled state chain and the outputs
 //
 // Tiles: a CTA owns HB heads of one group with HB * P = 128, so every
 // state-shaped contraction has M = 128 rows (head, p) and TMEM lane r holds
-// row r.  Operand tiles are 128-byte swizzled rows of 64 bf16; TMA loads x,
-// B and C tiles of Q rows straight into that layout.
+// row r.  x, B, C and CB tiles arrive by TMA in 128-byte swizzled rows of 64
+// bf16.
 #include <cudaTypedefs.h>
 
 #include "ssd_tc.cuh"
@@ -47,75 +51,69 @@ constexpr int kTargetCtas = 148;        // about one CTA per SM of a GB300 (152 
 constexpr int kSmemLimit = 226 * 1024;  // dynamic bytes; leaves room for the static mbarriers
 constexpr uint64_t kWaitNs = 100000000ull;    // a wait gives up after 0.1 s
 constexpr uint64_t kDrainNs = 20000000ull;    // the exit drain gives up after 0.02 s
+constexpr float kLambda = 64.f;               // |exponent| bound of the scaled operands
 
 struct TcParams {
     long long *trace;  // optional event trace of CTA (0, 0, 0) (trace builds only)
-    const bf16 *x;     // [b, L, H, P] (the epilogue's D x term)
     const bf16 *dt;
     const float *A, *D, *init;
     void *y;
     float *fin;
-    float *seg_state;   // [b, nseg, H, P, N]: segment-local states, then (in place) states entering segments
+    float *seg_state;   // [b, nseg, H, P, N]: segment-local states, then (in place) states entering segments 1..
     float *seg_tot;     // [b, H, nseg]  total dt*A of each segment (may be null)
     const float *cum_in;    // [b, H, nc, Q] given in-chunk cumulative decay (null: computed from dt, A)
-    const float *entering;  // [b, nseg, H, P, N] state entering each segment (null: init / segment pass)
-    unsigned *status;   // bit 0: a wait gave up
+    const float *entering;  // [b, nseg, H, P, N] state entering each segment (null: init / seg_state)
+    unsigned *status;   // bit 0: a wait gave up (may be null)
+    unsigned *counters; // [b, nhb] finished segment CTAs (seg_state_kernel, with seg_pass)
     long long b, L, H, G;
     int hpg, nc, nseg, cps;  // cps: chunks per segment
     int nhb;
-    int y_f32;
+    int seg_pass;
 };
 
 template <int P_, int N_, int Q_>
 struct Cfg {
     static constexpr int P = P_, N = N_, Q = Q_;
-    static constexpr int HB = 128 / P;          // heads per CTA
-    static constexpr int M = 128;               // rows (head, p)
-    static constexpr int PB = P / 64;           // 64-wide column blocks of one head's x tile
-    static constexpr int X_BYTES = M * Q * 2;   // [M/64 blocks][Q rows][64]
-    static constexpr int BC_BYTES = N * Q * 2;  // [N/64 blocks][Q rows][64]
-    static constexpr int XW_BYTES = M * Q * 2;  // one of the hi / lo halves of w x
-    static constexpr int SBF_BYTES = M * N * 2; // [N/64 blocks][M rows][64]
-    static constexpr int MM_BYTES = HB * Q * Q * 2;  // per head [Q/64 blocks][Q rows][64]
-    // per-stage vectors, [HB][Q] each: dt, cum, w, exp(cum), u = exp(cum - r),
-    // v = exp(r - cum) dt (r: the cumulative decay at mid-chunk); then per
-    // head exp(chunk total) and a flag for chunks whose decay range is too
-    // wide to factor in fp32
-    static constexpr int V_DT = 0, V_CUM = HB * Q, V_W = 2 * HB * Q, V_ECUM = 3 * HB * Q, V_U = 4 * HB * Q,
-                         V_V = 5 * HB * Q, V_DECAY = 6 * HB * Q, V_WIDE = 6 * HB * Q + HB;
-    static constexpr int VEC_FLOATS = 6 * HB * Q + 32;
-    // exp(cum) of two chunks, handed from the score-matrix warps to the epilogue
-    static constexpr int EPI_BYTES = ((2 * HB * Q * 4 + 1023) / 1024) * 1024;
+    static constexpr int HB = 128 / P;           // heads per CTA
+    static constexpr int M = 128;                // rows (head, p)
+    static constexpr int PB = P / 64;            // 64-wide column blocks of one head's x tile
+    static constexpr int X_BYTES = M * Q * 2;    // [M/64 blocks][Q rows][64]
+    static constexpr int BC_BYTES = N * Q * 2;   // [N/64 blocks][Q rows][64]
+    static constexpr int CBM_BYTES = Q * Q * 2;  // [Q rows t][Q s]
+    // vector set of one chunk (floats): per head [Q] arrays dt, cum, a-factor,
+    // epilogue factor; then per head the state rescale factor, the factor of
+    // the bf16 state copy, rho after the chunk; then two block flags
+    // (some head rescales, some head takes the wide path)
+    static constexpr int V_DT = 0, V_CUM = HB * Q, V_AL = 2 * HB * Q, V_EF = 3 * HB * Q;
+    static constexpr int V_F = 4 * HB * Q, V_SBF = V_F + HB, V_RHON = V_SBF + HB, V_FLAG = V_RHON + HB;
+    static constexpr int VEC_FLOATS = 4 * HB * Q + 32;
+    static constexpr int NV = 4;  // vector sets in flight
+    static constexpr int VEC_RING = ((NV * VEC_FLOATS * 4 + 1023) / 1024) * 1024;
 
-    // scan kernel: TMA stages of (x, B, C), a ring of kVecSlots vector sets,
-    // 1 or 2 buffers of w x (hi + lo), the bf16 state copy, the score
-    // matrices and the epilogue's exp(cum)
-    static constexpr int SCAN_STAGE = X_BYTES + 2 * BC_BYTES;
-    // (rounded to 1 KB: the swizzled operand tiles after it need 1024-byte alignment)
-    static constexpr int VEC_RING = ((4 * VEC_FLOATS * 4 + 1023) / 1024) * 1024;
-    static constexpr int scan_smem(int st, int xwb) {
-        return st * SCAN_STAGE + VEC_RING + xwb * 2 * XW_BYTES + SBF_BYTES + MM_BYTES + EPI_BYTES + 1024;
-    }
-    static constexpr int SCAN_ST = scan_smem(2, 2) <= kSmemLimit || scan_smem(2, 1) <= kSmemLimit ? 2 : 1;
-    static constexpr int SCAN_XWB = scan_smem(SCAN_ST, 2) <= kSmemLimit ? 2 : 1;
-    static constexpr int SMEM_SCAN = scan_smem(SCAN_ST, SCAN_XWB);
+    // scan kernel: TMA stages of (x, B, C, CB) and the vector ring
+    static constexpr int SCAN_STAGE = X_BYTES + 2 * BC_BYTES + CBM_BYTES;
+    static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + 1024; }
+    static constexpr int SCAN_ST = scan_smem(4) <= kSmemLimit ? 4 : (scan_smem(3) <= kSmemLimit ? 3 : 2);
+    static constexpr int SMEM_SCAN = scan_smem(SCAN_ST);
     static constexpr bool SCAN_FITS = SMEM_SCAN <= kSmemLimit;
+    // scan TMEM: Ss [N] | bf16 copy of Ss [N/2] x NB | A hi+lo [Q] x NB | R [Q] x NB
+    static constexpr int tmem_cols(int nb) { return N + nb * (N / 2 + 2 * Q); }
+    static constexpr int NB = tmem_cols(2) <= 512 ? 2 : 1;
+    static constexpr int COL_S = 0, COL_SB = N, COL_A = N + NB * N / 2, COL_R = COL_A + NB * Q;
+    static constexpr bool TMEM_FITS = tmem_cols(NB) <= 512;
 
-    // segment-state kernel: TMA stages of (x, B), two buffers of w x (hi +
-    // lo), a ring of vector sets, then the chunk totals [HB][cps]
+    // segment-state kernel: TMA stages of (x, B), the vector ring, then the
+    // chunk totals [HB][cps]
     static constexpr int SEG_STAGE = X_BYTES + BC_BYTES;
-    static constexpr int seg_smem(int st) { return st * SEG_STAGE + 4 * XW_BYTES + VEC_RING + 1024 + 4096; }
-    static constexpr int SEG_ST = seg_smem(4) <= kSmemLimit ? 4 : (seg_smem(3) <= kSmemLimit ? 3 : 2);
-    static constexpr int SMEM_SEG_BASE = SEG_ST * SEG_STAGE + 4 * XW_BYTES + VEC_RING + 1024;  // + [HB][cps]
+    static constexpr int seg_smem(int st) { return st * SEG_STAGE + VEC_RING + 1024; }
+    static constexpr int SEG_ST = seg_smem(4) + 4096 <= kSmemLimit ? 4 : (seg_smem(3) + 4096 <= kSmemLimit ? 3 : 2);
+    static constexpr int SMEM_SEG_BASE = seg_smem(SEG_ST);
+    static constexpr int SEG_COLS = N + 2 * Q;  // S [N] | A hi+lo [Q] x 2
+    static constexpr uint32_t SEG_TMEM =
+        SEG_COLS <= 64 ? 64 : SEG_COLS <= 128 ? 128 : SEG_COLS <= 256 ? 256 : 512;
 
-    // TMEM columns of the scan kernel
-    static constexpr int COL_S = 0;
-    static constexpr int COL_R3 = N;                 // inter-chunk term, two buffers of [M][Q]
-    static constexpr int COL_R = N + 2 * Q;          // intra-chunk term per head, [M][Q] each
-    static constexpr int COL_CB = N + 2 * Q + HB * Q;  // C B^T, [Q][Q]
-    static constexpr int TMEM_USED = COL_CB + Q;
-    static constexpr bool TMEM_FITS = TMEM_USED <= 512;
-    static constexpr uint32_t SEG_TMEM = N < 32 ? 32 : N;
+    // C B^T kernel: C and B tiles of one chunk
+    static constexpr int SMEM_CB = 2 * BC_BYTES + 1024;
 };
 
 // Event trace (SSD_TRACE builds): clock64() of role events of CTA (0, 0, 0),
@@ -174,6 +172,12 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, volat
     return *slot != 0;
 }
 
+// Phase parity to wait for at the it-th use of one of n ring slots: the
+// fill of round it / n ("full" side) or the release of the previous round
+// ("free" side, only for it >= n).
+__device__ __forceinline__ uint32_t fill_parity(int it, int n) { return (uint32_t)((it / n) & 1); }
+__device__ __forceinline__ uint32_t free_parity(int it, int n) { return (uint32_t)(((it / n) & 1) ^ 1); }
+
 // Inclusive scan of dt*A over one chunk for one head, by one warp; returns
 // the chunk total.
 template <int Q>
@@ -217,47 +221,50 @@ __device__ __forceinline__ float chunk_cum(const TcParams &prm, int b, long long
     return total;
 }
 
-// x tile scaled row-wise by w, split into two bf16 tiles whose sum carries
-// the product to about 2^-17 relative: hi = bf16(w x), lo = bf16(w x - hi).
-// (One bf16 rounding of w x, 2^-9 relative, is visible in the state entries
-// that a single recent token dominates.)  Works on whole 16-byte chunks of
-// the swizzled layout: a chunk stays in its row, so its scale is its row's.
-template <class C, int NT>
-__device__ __forceinline__ void build_xw(const uint8_t *xs, uint8_t *xw_hi, uint8_t *xw_lo, const float *w,
-                                         int gtid) {
-    constexpr int CHUNKS = (C::M / 64) * C::Q * 8;
-#pragma unroll 2
-    for (int i = gtid; i < CHUNKS; i += NT) {
-        const int blk = i / (C::Q * 8);
-        const int s = (i / 8) % C::Q;
-        const int h = blk / C::PB;
-        const float ws = w[h * C::Q + s];
-        uint4 v = *reinterpret_cast<const uint4 *>(xs + (size_t)i * 16);
-        uint4 lo;
-        uint32_t *u = reinterpret_cast<uint32_t *>(&v);
-        uint32_t *l = reinterpret_cast<uint32_t *>(&lo);
+// dt of the CTA's heads for chunk c, lane-strided: element lane + 32 i of
+// the [HB][Q] block.
+template <class C>
+__device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int c, float (&d)[C::HB * C::Q / 32]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 p2 = *reinterpret_cast<__nv_bfloat162 *>(&u[j]);
-            const float2 f = __bfloat1622float2(p2);
-            const float a = f.x * ws, b2 = f.y * ws;
-            const __nv_bfloat162 hi2 = __floats2bfloat162_rn(a, b2);
-            const float2 hf = __bfloat1622float2(hi2);
-            u[j] = *reinterpret_cast<const uint32_t *>(&hi2);
-            l[j] = pack_bf16x2(a - hf.x, b2 - hf.y);
-        }
-        *reinterpret_cast<uint4 *>(xw_hi + (size_t)i * 16) = v;
-        *reinterpret_cast<uint4 *>(xw_lo + (size_t)i * 16) = lo;
+    for (int i = 0; i < C::HB * C::Q / 32; ++i) {
+        const int idx = lane + 32 * i;
+        const int hh = idx / C::Q, q = idx % C::Q;
+        const long long h = h0 + hh;
+        d[i] = h < prm.H ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + (long long)c * C::Q + q) * prm.H + h))
+                         : 0.f;
     }
 }
 
-// TMA loads of chunk c: x tiles of the CTA's heads, B, and (optionally) C.
-// Returns the bytes the loads deliver.
+// Build this thread's half of the A operand of one chunk in TMEM:
+//   a_s = f_s x_s (s in [32 half, 32 half + 32)), split into bf16 hi and lo
+//   (hi = bf16(a), lo = bf16(a - hi): together about 2^-17 relative; a
+//   single bf16 rounding of a, 2^-9, shows in state entries that one recent
+//   token dominates).  Column j of the hi block holds s = 2j, 2j + 1; the lo
+//   block follows Q / 2 columns later.  The x values are returned packed
+//   (two bf16 per word) for the epilogue's D x term.
 template <class C>
-__device__ __forceinline__ uint32_t chunk_load_bytes(bool with_c) {
-    return C::X_BYTES + C::BC_BYTES * (with_c ? 2 : 1);
+__device__ __forceinline__ void build_a(const uint8_t *xs_blk, uint32_t pcol, const float *f, int half,
+                                       uint32_t tmem_a, uint32_t (&xw)[16]) {
+    uint32_t hi[16], lo[16];
+    const unsigned short *xs16 = reinterpret_cast<const unsigned short *>(xs_blk);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t s0 = (uint32_t)(half * 32 + 2 * j);
+        const uint32_t x0 = xs16[swz128(s0, pcol) >> 1];
+        const uint32_t x1 = xs16[swz128(s0 + 1, pcol) >> 1];
+        xw[j] = x0 | (x1 << 16);
+        const float a0 = __uint_as_float(x0 << 16) * f[2 * j];
+        const float a1 = __uint_as_float(x1 << 16) * f[2 * j + 1];
+        const uint32_t h = pack_bf16x2(a0, a1);
+        hi[j] = h;
+        lo[j] = pack_bf16x2(a0 - __uint_as_float(h << 16), a1 - __uint_as_float(h & 0xFFFF0000u));
+    }
+    tmem_st16u(tmem_a + half * 16, hi);
+    tmem_st16u(tmem_a + C::Q / 2 + half * 16, lo);
 }
 
+// TMA loads of chunk c: x tiles of the CTA's heads, B, and (optionally) C.
 template <class C>
 __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint8_t *cs, uint64_t *bar,
                                                   const CUtensorMap *mx, const CUtensorMap *mb,
@@ -276,32 +283,113 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 }
 
 // ===========================================================================
+// CB[t, s] = C_t . B_s for s <= t (0 above the diagonal), bf16, one CTA per
+// (chunk, group, batch):  [b, nc, G, Q, Q].  M = Q = 64 tcgen05 contraction
+// over N; rows 16w .. 16w + 15 of the M = 64 accumulator sit in TMEM lanes
+// 32w .. 32w + 15.
+// ===========================================================================
+template <class C>
+__global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CUtensorMap mb,
+                                                      const __grid_constant__ CUtensorMap mc, bf16 *cbm, int nc,
+                                                      int G, unsigned *status) {
+    static_assert(C::Q == 64, "the M = 64 accumulator layout is assumed");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *cs = smem, *bs = smem + C::BC_BYTES;
+    __shared__ uint64_t full_bar, done_bar;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int ok_sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    if (warp == 0) {
+        tmem_alloc(&tmem_base_sh, 64);
+        tmem_relinquish();
+    }
+    if (tid == 32) {
+        mbar_init(&full_bar, 1);
+        mbar_init(&done_bar, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    if (tid == 32) {
+        int ok = 0;
+        mbar_arrive_expect_tx(&full_bar, 2 * C::BC_BYTES);
+#pragma unroll
+        for (int nb = 0; nb < C::N / 64; ++nb) {
+            tma_load_4d(cs + nb * (C::Q * 128), &mc, &full_bar, nb * 64, g, c * C::Q, b);
+            tma_load_4d(bs + nb * (C::Q * 128), &mb, &full_bar, nb * 64, g, c * C::Q, b);
+        }
+        if (mbar_wait(&full_bar, 0, kWaitNs)) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(C::Q, C::Q, false, false);
+#pragma unroll
+            for (int ks = 0; ks < C::N / 16; ++ks) {
+                const uint32_t koff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
+                mma_bf16(tmem, sdesc(smem_u32(cs) + koff, 16, 1024), sdesc(smem_u32(bs) + koff, 16, 1024), id, ks > 0);
+            }
+            mma_commit(&done_bar);
+            ok = mbar_wait(&done_bar, 0, kWaitNs) ? 1 : 0;
+        } else {
+            mbar_wait(&full_bar, 0, kDrainNs);
+        }
+        ok_sh = ok;
+        if (!ok) flag_timeout(status);
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (ok_sh) {
+        const int t = warp * 16 + (lane & 15);
+        float v[64];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + k * 16, *reinterpret_cast<float(*)[16]>(v + 16 * k));
+        tmem_ld_wait();
+        if (lane < 16) {
+            uint4 *dst = reinterpret_cast<uint4 *>(cbm + ((((long long)b * nc + c) * G + g) * C::Q + t) * C::Q);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                uint4 w;
+                w.x = pack_bf16x2(8 * k + 0 <= t ? v[8 * k + 0] : 0.f, 8 * k + 1 <= t ? v[8 * k + 1] : 0.f);
+                w.y = pack_bf16x2(8 * k + 2 <= t ? v[8 * k + 2] : 0.f, 8 * k + 3 <= t ? v[8 * k + 3] : 0.f);
+                w.z = pack_bf16x2(8 * k + 4 <= t ? v[8 * k + 4] : 0.f, 8 * k + 5 <= t ? v[8 * k + 5] : 0.f);
+                w.w = pack_bf16x2(8 * k + 6 <= t ? v[8 * k + 6] : 0.f, 8 * k + 7 <= t ? v[8 * k + 7] : 0.f);
+                dst[k] = w;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// ===========================================================================
 // Segment-local states (segments 0 .. nseg-2):
-//   S_seg = sum_t exp(sum_{k>t in segment} dt_k A) dt_t x_t^T B_t
-//   warp 0      : TMA loads of the x and B tiles (kSegStages-deep ring)
-//   warp 1      : tcgen05.mma S += (w o x)^T B into TMEM
-//   warp 2      : dt and the segment weights w (kVecSlots-deep ring)
-//   warps 4-11  : w o x as bf16 hi + lo operand tiles (two buffers);
-//                 warps 4-7 move the TMEM state to HBM at the end
+//   S_seg = sum_t exp(sum_{k>t, k in segment} dt_k A) dt_t x_t^T B_t
+//   warp 0      : TMA loads of the x and B tiles
+//   warp 1      : tcgen05.mma S += A^T B, A read from TMEM
+//   warp 2      : dt and the segment weights (a ring of vector sets)
+//   warps 4-11  : the A operand (weights x x, bf16 hi + lo) into TMEM, two
+//                 buffers; then the state to HBM and, in the last CTA of a
+//                 (batch, head block), the pass across segments
 // ===========================================================================
 constexpr int kSegThreads = 384;
-constexpr int kVecSlots = 4;
 
 template <class C>
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb, TcParams prm) {
-    constexpr int ST = C::SEG_ST, NV = kVecSlots;
-    constexpr int HQ = C::HB * C::Q;
+    constexpr int ST = C::SEG_ST, NV = C::NV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *xw_base = smem + ST * C::SEG_STAGE;
-    float *vec_base = reinterpret_cast<float *>(xw_base + 2 * 2 * C::XW_BYTES);
-    float *tot_s = vec_base + NV * C::VEC_FLOATS;  // [HB][cps]
-    __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], xfull_bar[2], xempty_bar[2];
+    float *vec_base = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE);
+    float *tot_s = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE + C::VEC_RING);  // [HB][cps]
+    __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], afull_bar[2], afree_bar[2];
     __shared__ uint64_t done_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
     __shared__ volatile int slot[8];
+    __shared__ int last_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, hblk = blockIdx.y, b = blockIdx.z;
@@ -312,8 +400,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     const long long H = prm.H;
     auto stage_x = [&](int s) { return smem + s * C::SEG_STAGE; };
     auto stage_b = [&](int s) { return smem + s * C::SEG_STAGE + C::X_BYTES; };
-    auto xw_hi = [&](int i) { return xw_base + i * 2 * C::XW_BYTES; };
-    auto xw_lo = [&](int i) { return xw_base + i * 2 * C::XW_BYTES + C::XW_BYTES; };
     auto vec = [&](int v) { return vec_base + v * C::VEC_FLOATS; };
 
     if (warp == 1) {
@@ -323,15 +409,15 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], 1);
+            mbar_init(&empty_bar[i], 2);  // the MMAs' commit and the operand builders
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(&vfull_bar[i], 1);
             mbar_init(&vempty_bar[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&xfull_bar[i], 1);
-            mbar_init(&xempty_bar[i], 1);
+            mbar_init(&afull_bar[i], 1);
+            mbar_init(&afree_bar[i], 1);
         }
         mbar_init(&done_bar, 1);
         mbar_init(&drain_bar, 1);
@@ -386,44 +472,35 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     }
     __syncthreads();
     const uint32_t tmem = tmem_base_sh;
+    constexpr uint32_t COL_A = C::N;
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0)
             for (int it = 0; it < nch; ++it) {
                 const int s = it % ST;
-                if (it >= ST && !wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh)) break;
-                mbar_arrive_expect_tx(&full_bar[s], chunk_load_bytes<C>(false));
+                if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
+                mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES + C::BC_BYTES);
                 issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c0 + it,
                                      b);
                 ++nload[s];
             }
     } else if (warp == 2) {
         // ---------------- segment weights ----------------
-        constexpr int PER = HQ / 32;
+        constexpr int PER = C::HB * C::Q / 32;
         float dnext[PER];
-        auto fetch_dt = [&](int c) {
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int idx = lane + 32 * i;
-                const int hh = idx / C::Q, q = idx % C::Q;
-                const long long h = h0 + hh;
-                dnext[i] = h < H ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + (long long)c * C::Q + q) * H + h))
-                                 : 0.f;
-            }
-        };
-        fetch_dt(c0);
+        fetch_dt<C>(prm, b, h0, c0, dnext);
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV;
             if (it >= NV) {
-                int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], ((it / NV) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
+                int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], free_parity(it, NV), &abort_sh) ? 1 : 0) : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
             float *vv = vec(v);
 #pragma unroll
             for (int i = 0; i < PER; ++i) vv[C::V_DT + lane + 32 * i] = dnext[i];
             __syncwarp();
-            if (it + 1 < nch) fetch_dt(c0 + it + 1);
+            if (it + 1 < nch) fetch_dt<C>(prm, b, h0, c0 + it + 1, dnext);
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
                 const long long h = h0 + hh;
@@ -433,7 +510,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 const float total = chunk_cum<C>(prm, b, h, c0 + it, dtv, a, cum);
                 const float after = tot_s[hh * prm.cps + it];
                 for (int q = lane; q < C::Q; q += 32)
-                    vv[C::V_W + hh * C::Q + q] = __expf(after + total - cum[q]) * dtv[q];
+                    vv[C::V_AL + hh * C::Q + q] = __expf(after + total - cum[q]) * dtv[q];
             }
             __syncwarp();
             if (lane == 0) {
@@ -444,65 +521,103 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(C::M, C::N, true, true);
+            const uint32_t idesc = idesc_bf16(C::M, C::N, false, true);
             for (int it = 0; it < nch; ++it) {
-                const int s = it % ST, xb = it & 1;
-                if (!wait_bounded(&xfull_bar[xb], (it >> 1) & 1, &abort_sh)) break;
+                const int s = it % ST, a = it & 1;
+                if (!wait_bounded(&afull_bar[a], fill_parity(it, 2), &abort_sh)) break;
+                if (!wait_bounded(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
                 tc_fence_after();
-                const uint32_t ah = smem_u32(xw_hi(xb)), al = smem_u32(xw_lo(xb)), b0 = smem_u32(stage_b(s));
+                const uint32_t ta = tmem + COL_A + a * C::Q, b0 = smem_u32(stage_b(s));
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16(tmem, sdesc(ah + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
-                             idesc, (it | ks) != 0);
+                    mma_bf16_ta(tmem, ta + ks * 8, sdesc(b0 + ks * 2048, C::Q * 128, 1024), idesc, (it | ks) != 0);
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16(tmem, sdesc(al + ks * 2048, C::Q * 128, 1024), sdesc(b0 + ks * 2048, C::Q * 128, 1024),
-                             idesc, true);
+                    mma_bf16_ta(tmem, ta + C::Q / 2 + ks * 8, sdesc(b0 + ks * 2048, C::Q * 128, 1024), idesc, true);
                 mma_commit(&empty_bar[s]);
-                mma_commit(&xempty_bar[xb]);
+                mma_commit(&afree_bar[a]);
                 TRACE(16, it);
             }
             mma_commit(&done_bar);  // completes once every MMA above has
         }
     } else if (warp >= 4) {
-        // ---------------- w o x operand builders ----------------
+        // ---------------- A operand builders ----------------
         const int gtid = tid - 128;
+        const int q4 = warp & 3, half = (warp - 4) >> 2;
+        const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
+        const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+        const uint32_t pcol = (uint32_t)(rp % 64);
+        const int blk = rh * C::PB + rp / 64;
+        uint32_t xw[16];
         for (int it = 0; it < nch; ++it) {
-            const int s = it % ST, v = it % NV, xb = it & 1;
-            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[0], 1, gtid, 256)) break;
-            if (!group_wait(&vfull_bar[v], (it / NV) & 1, &abort_sh, &slot[1], 1, gtid, 256)) break;
-            if (it >= 2 && !group_wait(&xempty_bar[xb], ((it >> 1) & 1) ^ 1, &abort_sh, &slot[2], 1, gtid, 256)) break;
-            build_xw<C, 256>(stage_x(s), xw_hi(xb), xw_lo(xb), vec(v) + C::V_W, gtid);
-            fence_async_smem();
+            const int s = it % ST, v = it % NV, a = it & 1;
+            if (!group_wait(&full_bar[s], fill_parity(it, ST), &abort_sh, &slot[0], 1, gtid, 256)) break;
+            if (!group_wait(&vfull_bar[v], fill_parity(it, NV), &abort_sh, &slot[1], 1, gtid, 256)) break;
+            if (it >= 2 && !group_wait(&afree_bar[a], free_parity(it, 2), &abort_sh, &slot[2], 1, gtid, 256)) break;
+            tc_fence_after();
+            build_a<C>(stage_x(s) + blk * (C::Q * 128), pcol, vec(v) + C::V_AL + rh * C::Q + half * 32, half,
+                       tmem + lane_off + COL_A + a * C::Q, xw);
+            tmem_st_wait();
+            tc_fence_before();
             named_bar_sync(1, 256);
             if (gtid == 0) {
                 TRACE(15, it);
-                mbar_arrive(&xfull_bar[xb]);
+                mbar_arrive(&afull_bar[a]);
+                mbar_arrive(&empty_bar[s]);
                 mbar_arrive(&vempty_bar[v]);
             }
         }
-        // segment state: TMEM lane r = row (head, p)
-        if (warp < 8) {
-            if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 2, gtid, 128)) {
-                tc_fence_after();
-                const int q4 = warp & 3;
-                const int r = q4 * 32 + lane;
-                const int hh = r / C::P, p = r % C::P;
-                const long long h = h0 + hh;
-                float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + h) * C::P + p) * C::N;
+        (void)xw;
+        // segment state: TMEM lane r = row (head, p); warps 4-7 columns
+        // [0, N/2), warps 8-11 [N/2, N)
+        const long long hrow = h0 + rh;
+        bool stored = false;
+        if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 1, gtid, 256)) {
+            tc_fence_after();
+            float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + hrow) * C::P + rp) * C::N;
 #pragma unroll 1
-                for (int n0 = 0; n0 < C::N; n0 += 32) {
-                    float v0[16], v1[16];
-                    tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + n0, v0);
-                    tmem_ld16(tmem + ((uint32_t)(q4 * 32) << 16) + n0 + 16, v1);
-                    tmem_ld_wait();
-                    if (h < H) {
+            for (int n0 = half * (C::N / 2); n0 < (half + 1) * (C::N / 2); n0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + lane_off + n0, v);
+                tmem_ld_wait();
+                if (hrow < H) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v0[j], v0[j + 1], v0[j + 2], v0[j + 3]);
-                            *reinterpret_cast<float4 *>(dst + n0 + 16 + j) =
-                                make_float4(v1[j], v1[j + 1], v1[j + 2], v1[j + 3]);
-                        }
+                    for (int j = 0; j < 16; j += 4)
+                        __stcg(reinterpret_cast<float4 *>(dst + n0 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+                }
+            }
+            stored = true;
+        }
+        // pass across segments, in place, by the last of the (nseg - 1) CTAs
+        // of this (batch, head block): slot k becomes the state entering
+        // segment k + 1 = exp(T_k) (state entering k) + local_k
+        if (prm.seg_pass && stored) {
+            __threadfence();
+            named_bar_sync(1, 256);
+            if (gtid == 0) {
+                const unsigned done = atomicAdd(&prm.counters[(long long)b * prm.nhb + hblk], 1u);
+                last_sh = done == (unsigned)(prm.nseg - 2) ? 1 : 0;
+            }
+            named_bar_sync(1, 256);
+            if (last_sh) {
+                __threadfence();
+                constexpr int ROW4 = C::N / 4;
+                for (int e = gtid; e < C::M * ROW4; e += 256) {
+                    const int r = e / ROW4, n4 = e % ROW4;
+                    const long long h = h0 + r / C::P;
+                    if (h >= H) continue;
+                    const long long off = (h * C::P + r % C::P) * C::N + 4 * n4;
+                    float4 acc = prm.init ? __ldg(reinterpret_cast<const float4 *>(prm.init + b * H * C::P * C::N + off))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < prm.nseg - 1; ++k) {
+                        float4 *p = reinterpret_cast<float4 *>(prm.seg_state + ((long long)b * prm.nseg + k) * H * C::P * C::N + off);
+                        const float4 loc = __ldcg(p);
+                        const float ex = expf(__ldcg(prm.seg_tot + ((long long)b * H + h) * prm.nseg + k));
+                        acc.x = fmaf(ex, acc.x, loc.x);
+                        acc.y = fmaf(ex, acc.y, loc.y);
+                        acc.z = fmaf(ex, acc.z, loc.z);
+                        acc.w = fmaf(ex, acc.w, loc.w);
+                        __stcg(p, acc);
                     }
                 }
             }
@@ -523,61 +638,38 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     if (abort_sh && tid == 0) flag_timeout(prm.status);
 }
 
-// ---------------------------------------------------------------------------
-// Pass of states across segments, in place: slot s of the segment-state
-// array (the local state of segment s) becomes the state entering segment
-// s + 1 = exp(T_s) (state entering s) + local_s, T_s the segment's total
-// dt*A.  One thread per four consecutive (p, n) of one (b, h); the loads
-// of a batch of segments are issued before any of their results is stored.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) segment_pass_kernel(const float *__restrict__ init, float *seg_state,
-                                                           const float *__restrict__ seg_tot, long long H, int PN,
-                                                           int nseg) {
-    const int PN4 = PN / 4;
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
-    const long long h = blockIdx.y, b = blockIdx.z;
-    if (e >= PN4) return;
-    float4 acc = init ? __ldg(reinterpret_cast<const float4 *>(init + (b * H + h) * PN) + e)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    const int nsp = nseg - 1;
-    const float *tot = seg_tot + (b * H + h) * nseg;
-    constexpr int KB = 8;
-    for (int s0 = 0; s0 < nsp; s0 += KB) {
-        float4 v[KB];
-        float ex[KB];
+// Epilogue fix-up of a chunk whose decay range is too wide to scale (rare;
+// kept out of line so the hot path stays small): R holds the inter-chunk
+// term only; replace this thread's 32 accumulator columns by
+//   ef_t R_t + sum_{s<=t} CB[t, s] exp(cum_t - cum_s) dt_s x_s
+// computed with direct per-entry decay factors, so the caller stores them
+// with a unit factor.
+template <class C>
+__device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const uint8_t *xs_blk, const uint8_t *cbm,
+                                        const float *cum, const float *dtv, uint32_t pcol, int t0) {
+    const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xs_blk);
+    const unsigned short *c16 = reinterpret_cast<const unsigned short *>(cbm);
+#pragma unroll 1
+    for (int j0 = 0; j0 < 32; j0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + j0, v);
+        tmem_ld_wait();
 #pragma unroll
-        for (int k = 0; k < KB; ++k)
-            if (s0 + k < nsp) {
-                v[k] = __ldcg(reinterpret_cast<const float4 *>(seg_state + (((b * nseg + s0 + k) * H + h) * PN)) + e);
-                ex[k] = expf(__ldcg(tot + s0 + k));
+        for (int j = 0; j < 16; ++j) {
+            const int t = t0 + j0 + j;
+            const float ct = cum[t];
+            float acc = 0.f;
+#pragma unroll 1
+            for (int s = 0; s <= t; ++s) {
+                const float xv = __uint_as_float((uint32_t)x16[swz128((uint32_t)s, pcol) >> 1] << 16);
+                const float cb = __uint_as_float((uint32_t)c16[swz128((uint32_t)t, (uint32_t)s) >> 1] << 16);
+                acc = fmaf(cb * __expf(ct - cum[s]) * dtv[s], xv, acc);
             }
-#pragma unroll
-        for (int k = 0; k < KB; ++k)
-            if (s0 + k < nsp) {
-                acc.x = fmaf(ex[k], acc.x, v[k].x);
-                acc.y = fmaf(ex[k], acc.y, v[k].y);
-                acc.z = fmaf(ex[k], acc.z, v[k].z);
-                acc.w = fmaf(ex[k], acc.w, v[k].w);
-                __stcg(reinterpret_cast<float4 *>(seg_state + (((b * nseg + s0 + k) * H + h) * PN)) + e, acc);
-            }
+            v[j] = fmaf(ef[j0 + j], v[j], acc);
+        }
+        tmem_st16(taddr + j0, v);
     }
-}
-
-// Scores of a chunk whose decay range is too wide to factor in fp32: direct
-// exponent per entry (rare; kept out of line so the hot loop stays small).
-struct F8 {
-    float v[8];
-};
-
-__device__ __noinline__ F8 wide_scores(F8 cb, const float *cum, const float *dtv, int t, int s0) {
-    const float ct = cum[t];
-    F8 m;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int sc = s0 + j;
-        m.v[j] = sc <= t ? cb.v[j] * __expf(ct - cum[sc]) * dtv[sc] : 0.f;
-    }
-    return m;
+    tmem_st_wait();
 }
 
 template <typename T>
@@ -587,79 +679,36 @@ __device__ __forceinline__ void store_y<float>(float *p, float v) { __stcs(p, v)
 template <>
 __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
-// x[t][p] of this thread's (head, p) column for the Q steps of a chunk,
-// two bf16 per register (fetched one chunk ahead, while the epilogue waits).
-template <class C>
-__device__ __forceinline__ void fetch_x_column(const bf16 *xg, long long stride, bool live, uint32_t (&xp)[C::Q / 2]) {
-    const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xg);
-#pragma unroll
-    for (int j = 0; j < C::Q / 2; ++j) {
-        const uint32_t lo = live ? __ldg(x16 + (long long)(2 * j) * stride) : 0u;
-        const uint32_t hi = live ? __ldg(x16 + (long long)(2 * j + 1) * stride) : 0u;
-        xp[j] = lo | (hi << 16);
-    }
-}
-
-// Epilogue of one chunk for this thread's row: TMEM row of the intra term
-// (its head's buffer) and of the inter term, exp(cum) of its head, and the
-// x column fetched ahead.
-template <class C, typename T>
-__device__ __forceinline__ void epilogue_rows(uint32_t tmem_lane, int it, int rh, const float *ecum,
-                                              const uint32_t (&xp)[C::Q / 2], T *yp, long long stride, float dh,
-                                              bool live) {
-#pragma unroll
-    for (int t0 = 0; t0 < C::Q; t0 += 16) {
-        float ri[16], re[16];
-        tmem_ld16(tmem_lane + C::COL_R + rh * C::Q + t0, ri);
-        tmem_ld16(tmem_lane + C::COL_R3 + (it & 1) * C::Q + t0, re);
-        tmem_ld_wait();
-        if (live) {
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                const float4 e4 = *reinterpret_cast<const float4 *>(ecum + t0 + j);
-                const uint32_t w0 = xp[(t0 + j) / 2], w1 = xp[(t0 + j) / 2 + 1];
-                const float x0 = __uint_as_float(w0 << 16), x1 = __uint_as_float(w0 & 0xFFFF0000u);
-                const float x2 = __uint_as_float(w1 << 16), x3 = __uint_as_float(w1 & 0xFFFF0000u);
-                store_y<T>(yp + (long long)(t0 + j) * stride, fmaf(dh, x0, fmaf(e4.x, re[j], ri[j])));
-                store_y<T>(yp + (long long)(t0 + j + 1) * stride, fmaf(dh, x1, fmaf(e4.y, re[j + 1], ri[j + 1])));
-                store_y<T>(yp + (long long)(t0 + j + 2) * stride, fmaf(dh, x2, fmaf(e4.z, re[j + 2], ri[j + 2])));
-                store_y<T>(yp + (long long)(t0 + j + 3) * stride, fmaf(dh, x3, fmaf(e4.w, re[j + 3], ri[j + 3])));
-            }
-        }
-    }
-}
-
 // ===========================================================================
-// Chunk scan with the state carried in TMEM (every segment).
-//   warp 0     : TMA loads of x, B, C; dt (fetched a chunk ahead), cumulative
-//                decay, w, exp(cum) and the factors u, v of exp(cum_t - cum_s)
-//   warp 1     : tcgen05.mma issue (C B^T; S C^T; S += (w x)^T B; X^T M^T)
-//   warps 4-7  : w o x operand tiles; bf16 state copy and S *= exp(total)
-//   warps 8-11 : masked, decayed score matrices M_h (bf16) from C B^T
-//   warps 12-15: y = intra + exp(cum) inter + D x, straight to HBM
+// Chunk scan with the scaled state carried in TMEM (every segment).
+//   warp 0     : TMA loads of x, B, C, CB
+//   warp 1     : tcgen05.mma issue, per chunk  R = A CB^T;  Ss += A B (once
+//                the state warps are done with Ss);  R += SB C^T
+//   warp 2     : dt, cumulative decay, rho, the A factors and epilogue
+//                factors (a ring of vector sets)
+//   warps 4-7  : state: Ss rescale when rho moves, and its bf16 copy SB
+//                (the A operand of the inter-chunk term)
+//   warps 8-15 : A operand of the next chunk into TMEM; epilogue
+//                y = factor R + D x straight to HBM
 // ===========================================================================
 constexpr int kScanThreads = 512;
 
 template <class C, typename YT>
 __global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
-                      const __grid_constant__ CUtensorMap mc, TcParams prm) {
-    constexpr int ST = C::SCAN_ST;
-    constexpr int XWB = C::SCAN_XWB;
-    constexpr int HQ = C::HB * C::Q;
+                      const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap mcb, TcParams prm) {
+    constexpr int ST = C::SCAN_ST, NV = C::NV, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int NV = kVecSlots;
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SCAN_STAGE);
-    uint8_t *xw_base = smem + ST * C::SCAN_STAGE + C::VEC_RING;
-    uint8_t *sbf = xw_base + XWB * 2 * C::XW_BYTES;
-    uint8_t *mm = sbf + C::SBF_BYTES;
-    float *epi_vec = reinterpret_cast<float *>(mm + C::MM_BYTES);  // [2][HB][Q]
-    __shared__ uint64_t full_bar[2], empty_bar[2], free_r3_bar[2], epi_bar[2], vfull_bar[NV], vempty_bar[NV];
-    __shared__ uint64_t cb_bar, mask_bar, wg1_bar, state_bar, y_bar, free_r_bar, drain_bar;
+    __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV];
+    __shared__ uint64_t afull_bar[NB], afree_bar[NB], rfull_bar[NB], rfree_bar[NB], sbfree_bar[NB];
+    __shared__ uint64_t rt_bar, sdone_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
     __shared__ volatile int slot[8];
+    __shared__ volatile int wide_a[NB];
+    __shared__ __align__(16) float ones_sh[32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.x, hblk = blockIdx.y, b = blockIdx.z;
@@ -671,38 +720,40 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
     auto stage_b = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES; };
     auto stage_c = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + C::BC_BYTES; };
+    auto stage_cb = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + 2 * C::BC_BYTES; };
     auto vec = [&](int v) { return vec_base + v * C::VEC_FLOATS; };
-    auto xw_hi = [&](int i) { return xw_base + i * 2 * C::XW_BYTES; };
-    auto xw_lo = [&](int i) { return xw_base + i * 2 * C::XW_BYTES + C::XW_BYTES; };
 
     if (warp == 1) {
         tmem_alloc(&tmem_base_sh, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < ST; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], 1);
-            mbar_init(&free_r3_bar[i], 1);
-            mbar_init(&epi_bar[i], 1);
+            mbar_init(&empty_bar[i], 2);  // the MMAs' commit, and the A builders (the epilogue on a wide chunk)
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(&vfull_bar[i], 1);
-            mbar_init(&vempty_bar[i], 1);
+            mbar_init(&vempty_bar[i], 2);  // state warps and epilogue
         }
-        mbar_init(&cb_bar, 1);
-        mbar_init(&mask_bar, 1);
-        mbar_init(&wg1_bar, 1);
-        mbar_init(&state_bar, 1);
-        mbar_init(&y_bar, 1);
-        mbar_init(&free_r_bar, 1);
+        for (int i = 0; i < NB; ++i) {
+            mbar_init(&afull_bar[i], 1);
+            mbar_init(&afree_bar[i], 1);
+            mbar_init(&rfull_bar[i], 1);
+            mbar_init(&rfree_bar[i], 1);
+            mbar_init(&sbfree_bar[i], 1);
+        }
+        mbar_init(&rt_bar, 1);
+        mbar_init(&sdone_bar, 1);
         mbar_init(&drain_bar, 1);
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
         prefetch_tmap(&mb);
         prefetch_tmap(&mc);
+        prefetch_tmap(&mcb);
     }
+    if (tid < 32) ones_sh[tid] = 1.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -711,7 +762,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         TRACE_CTA(0);
     }
     const uint32_t tmem = tmem_base_sh;
-    int nload[2] = {0, 0};  // TMA loads issued per stage (producer lane 0)
+    int nload[4] = {0, 0, 0, 0};  // TMA loads issued per stage (producer lane 0)
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
 
@@ -720,61 +771,87 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (lane == 0)
             for (int it = 0; it < nch; ++it) {
                 const int s = it % ST;
-                if (it >= ST && !wait_bounded(&empty_bar[s], ((it / ST) & 1) ^ 1, &abort_sh)) break;
-                mbar_arrive_expect_tx(&full_bar[s], chunk_load_bytes<C>(true));
+                if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
+                mbar_arrive_expect_tx(&full_bar[s], C::SCAN_STAGE);
                 issue_chunk_loads<C>(stage_x(s), stage_b(s), stage_c(s), &full_bar[s], &mx, &mb, &mc, h0, g, c0 + it,
                                      b);
+                tma_load_3d(stage_cb(s), &mcb, &full_bar[s], 0, 0, (int)((((long long)b * prm.nc) + c0 + it) * prm.G + g));
                 ++nload[s];
                 TRACE(0, it);
             }
     } else if (warp == 2) {
         // ---------------- per-chunk vectors (run up to NV chunks ahead) ----------------
-        constexpr int PER = HQ / 32;
+        constexpr int PER = C::HB * C::Q / 32;
         float dnext[PER];
-        auto fetch_dt = [&](int c) {
+        float rho[C::HB];
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int idx = lane + 32 * i;
-                const int hh = idx / C::Q, q = idx % C::Q;
-                const long long h = h0 + hh;
-                dnext[i] = h < H ? __bfloat162float(__ldg(prm.dt + ((long long)b * L + (long long)c * C::Q + q) * H + h))
-                                 : 0.f;
-            }
-        };
-        fetch_dt(c0);
+        for (int hh = 0; hh < C::HB; ++hh) rho[hh] = 0.f;
+        fetch_dt<C>(prm, b, h0, c0, dnext);
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV;
             if (it >= NV) {
-                int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], ((it / NV) & 1) ^ 1, &abort_sh) ? 1 : 0) : 0;
+                int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], free_parity(it, NV), &abort_sh) ? 1 : 0) : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
             float *vv = vec(v);
 #pragma unroll
             for (int i = 0; i < PER; ++i) vv[C::V_DT + lane + 32 * i] = dnext[i];
             __syncwarp();
-            if (it + 1 < nch) fetch_dt(c0 + it + 1);  // in flight while this chunk's vectors are computed
+            if (it + 1 < nch) fetch_dt<C>(prm, b, h0, c0 + it + 1, dnext);  // in flight while this chunk's vectors are computed
+            bool rescale = false, wide = false;
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
                 const long long h = h0 + hh;
                 const float a = (h < H && prm.A) ? prm.A[h] : 0.f;
                 float *cum = vv + C::V_CUM + hh * C::Q;
                 const float *dtv = vv + C::V_DT + hh * C::Q;
-                const float total = chunk_cum<C>(prm, b, h, c0 + it, dtv, a, cum);
-                const float r = cum[C::Q / 2 - 1];
-                // exp(cum_t - cum_s) = u_t v_s / dt_s factors in fp32 only while
-                // each half-chunk's decay stays within e^80
-                const bool wide = (cum[0] - r) > 80.f || (r - total) > 80.f;
+                const float T = chunk_cum<C>(prm, b, h, c0 + it, dtv, a, cum);
+                // range [lo, hi] of the cumulative decay over the chunk and its start (0)
+                float lo = 0.f, hi = 0.f;
+                for (int q = lane; q < C::Q; q += 32) {
+                    lo = fminf(lo, cum[q]);
+                    hi = fmaxf(hi, cum[q]);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+                    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+                }
+                // rho stays while every exponent rho - cum_s stays within kLambda;
+                // else it moves to the middle of the chunk's range; a range wider
+                // than 2 kLambda centres the state at the chunk's end and leaves
+                // the intra-chunk term to the direct path
+                float rc = rho[hh], f = 1.f, sbf = 1.f;
+                bool hw = false;
+                if (rho[hh] - lo > kLambda || hi - rho[hh] > kLambda) {
+                    rescale = true;
+                    if (hi - lo <= 2.f * kLambda) {
+                        rc = 0.5f * (lo + hi);
+                        f = __expf(rc - rho[hh]);
+                        sbf = f;
+                    } else {
+                        hw = true;
+                        rc = T;
+                        f = __expf(T - rho[hh]);
+                        sbf = __expf(-rho[hh]);
+                    }
+                }
+                wide |= hw;
                 for (int q = lane; q < C::Q; q += 32) {
                     const float cq = cum[q];
-                    vv[C::V_W + hh * C::Q + q] = __expf(total - cq) * dtv[q];
-                    vv[C::V_ECUM + hh * C::Q + q] = __expf(cq);
-                    vv[C::V_U + hh * C::Q + q] = wide ? 0.f : __expf(cq - r);
-                    vv[C::V_V + hh * C::Q + q] = wide ? 0.f : __expf(r - cq) * dtv[q];
+                    vv[C::V_AL + hh * C::Q + q] = __expf(rc - cq) * dtv[q];
+                    vv[C::V_EF + hh * C::Q + q] = __expf(hw ? cq : cq - rc);
                 }
                 if (lane == 0) {
-                    vv[C::V_DECAY + hh] = __expf(total);
-                    vv[C::V_WIDE + hh] = wide ? 1.f : 0.f;
+                    vv[C::V_F + hh] = f;
+                    vv[C::V_SBF + hh] = sbf;
+                    vv[C::V_RHON + hh] = rc - T;
                 }
+                rho[hh] = rc - T;
+            }
+            if (lane == 0) {
+                vv[C::V_FLAG] = rescale ? 1.f : 0.f;
+                vv[C::V_FLAG + 1] = wide ? 1.f : 0.f;
             }
             __syncwarp();
             if (lane == 0) {
@@ -785,77 +862,61 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t id_cb = idesc_bf16(C::Q, C::Q, false, false);
+            const uint32_t id_intra = idesc_bf16(C::M, C::Q, false, false);
+            const uint32_t id_state = idesc_bf16(C::M, C::N, false, true);
             const uint32_t id_inter = idesc_bf16(C::M, C::Q, false, false);
-            const uint32_t id_state = idesc_bf16(C::M, C::N, true, true);
-            const uint32_t id_intra = idesc_bf16(C::M, C::Q, true, false);
             for (int it = 0; it < nch; ++it) {
-                const int s = it % ST;
-                const int xb = XWB == 2 ? (it & 1) : 0;
-                const uint32_t sx = smem_u32(stage_x(s)), sb = smem_u32(stage_b(s)), sc = smem_u32(stage_c(s));
-                // C B^T: needs the chunk's tiles and the previous scores consumed
-                if (!wait_bounded(&full_bar[s], (it / ST) & 1, &abort_sh)) break;
-                if (it > 0 && !wait_bounded(&mask_bar, (it - 1) & 1, &abort_sh)) break;
+                const int s = it % ST, a = it % NB;
+                const uint32_t sb_ = smem_u32(stage_b(s)), sc = smem_u32(stage_c(s)), scb = smem_u32(stage_cb(s));
+                const uint32_t ta = tmem + C::COL_A + a * C::Q, tr = tmem + C::COL_R + a * C::Q;
+                const uint32_t tsb = tmem + C::COL_SB + a * (C::N / 2);
+                if (!wait_bounded(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
+                if (!wait_bounded(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
+                if (it >= NB && !wait_bounded(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
                 tc_fence_after();
+                const bool wide = wide_a[a] != 0;
+                // R = A CB^T (hi, then lo)
+                if (!wide) {
 #pragma unroll
-                for (int ks = 0; ks < C::N / 16; ++ks) {
-                    const uint32_t koff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                    mma_bf16(tmem + C::COL_CB, sdesc(sc + koff, 16, 1024), sdesc(sb + koff, 16, 1024), id_cb, ks > 0);
+                    for (int ks = 0; ks < C::Q / 16; ++ks)
+                        mma_bf16_ta(tr, ta + ks * 8, sdesc(scb + ks * 32, 16, 1024), id_intra, ks > 0);
+#pragma unroll
+                    for (int ks = 0; ks < C::Q / 16; ++ks)
+                        mma_bf16_ta(tr, ta + C::Q / 2 + ks * 8, sdesc(scb + ks * 32, 16, 1024), id_intra, true);
                 }
-                mma_commit(&cb_bar);
                 TRACE(2, it);
-                // S C^T into inter buffer it & 1, and S += (w x)^T B: need the bf16
-                // state copy, the scaled state and w x (warps 4-7), and the
-                // epilogue two chunks back done with that inter buffer
-                if (!wait_bounded(&wg1_bar, it & 1, &abort_sh)) break;
-                if (it >= 2 && !wait_bounded(&free_r3_bar[it & 1], ((it >> 1) & 1) ^ 1, &abort_sh)) break;
+                // Ss += A^T B: once the state warps have read (and rescaled) Ss
+                // and written SB
+                if (!wait_bounded(&rt_bar, (uint32_t)(it & 1), &abort_sh)) break;
                 tc_fence_after();
-                const uint32_t ss = smem_u32(sbf);
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 8, sdesc(sb_ + ks * 2048, C::Q * 128, 1024), id_state, true);
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16_ta(tmem + C::COL_S, ta + C::Q / 2 + ks * 8, sdesc(sb_ + ks * 2048, C::Q * 128, 1024),
+                                id_state, true);
+                mma_commit(&sdone_bar);
+                mma_commit(&afree_bar[a]);
+                TRACE(3, it);
+                // R += SB C^T
 #pragma unroll
                 for (int ks = 0; ks < C::N / 16; ++ks) {
-                    const uint32_t aoff = (ks / 4) * (C::M * 128) + (ks % 4) * 32;
                     const uint32_t boff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                    mma_bf16(tmem + C::COL_R3 + (it & 1) * C::Q, sdesc(ss + aoff, 16, 1024),
-                             sdesc(sc + boff, 16, 1024), id_inter, ks > 0);
+                    mma_bf16_ta(tr, tsb + ks * 8, sdesc(sc + boff, 16, 1024), id_inter, !wide || ks > 0);
                 }
-                const uint32_t swh = smem_u32(xw_hi(xb)), swl = smem_u32(xw_lo(xb));
-#pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16(tmem + C::COL_S, sdesc(swh + ks * 2048, C::Q * 128, 1024),
-                             sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
-#pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16(tmem + C::COL_S, sdesc(swl + ks * 2048, C::Q * 128, 1024),
-                             sdesc(sb + ks * 2048, C::Q * 128, 1024), id_state, true);
-                mma_commit(&state_bar);
-                TRACE(3, it);
-                // X^T M_h^T per head: needs the score matrices (warps 8-11) and
-                // the last epilogue done with the intra buffers
-                if (!wait_bounded(&mask_bar, it & 1, &abort_sh)) break;
-                if (it > 0 && !wait_bounded(&free_r_bar, (it - 1) & 1, &abort_sh)) break;
-                tc_fence_after();
-                const uint32_t sm = smem_u32(mm);
-#pragma unroll
-                for (int hh = 0; hh < C::HB; ++hh)
-#pragma unroll
-                    for (int ks = 0; ks < C::Q / 16; ++ks) {
-                        const uint32_t boff = hh * (C::Q * C::Q * 2) + (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                        mma_bf16(tmem + C::COL_R + hh * C::Q, sdesc(sx + ks * 2048, C::Q * 128, 1024),
-                                 sdesc(sm + boff, 16, 1024), id_intra, ks > 0);
-                    }
-                mma_commit(&y_bar);
-                // every read of the stage and of the vector set is done once these MMAs are
+                mma_commit(&rfull_bar[a]);
+                mma_commit(&sbfree_bar[a]);
                 mma_commit(&empty_bar[s]);
-                mma_commit(&vempty_bar[it % NV]);
                 TRACE(4, it);
             }
         }
     } else if (warp >= 4 && warp < 8) {
-        // ---------------- w x operands; state copy and decay ----------------
+        // ---------------- state: rescale and bf16 copy ----------------
         const int gtid = tid - 128;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const long long hrow = h0 + rh;
-        // state entering the segment
+        // state entering the segment (rho = 0: Ss = S_in)
         {
             const float *src = nullptr;
             if (prm.entering)
@@ -866,77 +927,70 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 src = prm.init + (((long long)b * H + hrow) * C::P + rp) * C::N;
             if (hrow >= H) src = nullptr;
 #pragma unroll 1
-            for (int n0 = 0; n0 < C::N; n0 += 32) {
-                float v0[16], v1[16];
+            for (int n0 = 0; n0 < C::N; n0 += 16) {
+                float v[16];
 #pragma unroll
                 for (int j = 0; j < 16; j += 4) {
                     const float4 a = src ? __ldcg(reinterpret_cast<const float4 *>(src + n0 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float4 c2 = src ? __ldcg(reinterpret_cast<const float4 *>(src + n0 + 16 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v0[j] = a.x; v0[j + 1] = a.y; v0[j + 2] = a.z; v0[j + 3] = a.w;
-                    v1[j] = c2.x; v1[j + 1] = c2.y; v1[j + 2] = c2.z; v1[j + 3] = c2.w;
+                    v[j] = a.x;
+                    v[j + 1] = a.y;
+                    v[j + 2] = a.z;
+                    v[j + 3] = a.w;
                 }
-                tmem_st16(tmem + lane_off + C::COL_S + n0, v0);
-                tmem_st16(tmem + lane_off + C::COL_S + n0 + 16, v1);
+                tmem_st16(tmem + lane_off + C::COL_S + n0, v);
             }
             tmem_st_wait();
         }
         if (gtid == 0) TRACE(13, 1);
+        float rho_end = 0.f;
         for (int it = 0; it < nch; ++it) {
-            const int s = it % ST;
-            const int xb = XWB == 2 ? (it & 1) : 0;
-            if (!group_wait(&full_bar[s], (it / ST) & 1, &abort_sh, &slot[0], 1, gtid, 128)) break;
-            if (!group_wait(&vfull_bar[it % NV], (it / NV) & 1, &abort_sh, &slot[7], 1, gtid, 128)) break;
-            if (gtid == 0) TRACE(5, it);
-            const float *vv = vec(it % NV);
-            if (XWB == 1 && it > 0) {
-                if (!group_wait(&state_bar, (it - 1) & 1, &abort_sh, &slot[1], 1, gtid, 128)) break;
-            }
-            build_xw<C, 128>(stage_x(s), xw_hi(xb), xw_lo(xb), vv + C::V_W, gtid);
-            if (gtid == 0) TRACE(6, it);
-            if (XWB == 2 && it > 0) {
-                if (!group_wait(&state_bar, (it - 1) & 1, &abort_sh, &slot[1], 1, gtid, 128)) break;
-            }
+            const int v = it % NV, sb = it % NB;
+            if (!group_wait(&vfull_bar[v], fill_parity(it, NV), &abort_sh, &slot[0], 1, gtid, 128)) break;
+            if (it > 0 && !group_wait(&sdone_bar, (uint32_t)((it - 1) & 1), &abort_sh, &slot[1], 1, gtid, 128)) break;
+            if (it >= NB && !group_wait(&sbfree_bar[sb], free_parity(it, NB), &abort_sh, &slot[2], 1, gtid, 128)) break;
             if (gtid == 0) TRACE(7, it);
             tc_fence_after();
-            const float dec = vv[C::V_DECAY + rh];
+            const float *vv = vec(v);
+            const float f = vv[C::V_F + rh], sbf = vv[C::V_SBF + rh];
+            const bool rescale = vv[C::V_FLAG] != 0.f;
+            rho_end = vv[C::V_RHON + rh];
 #pragma unroll 1
             for (int n0 = 0; n0 < C::N; n0 += 32) {
                 float v0[16], v1[16];
                 tmem_ld16(tmem + lane_off + C::COL_S + n0, v0);
                 tmem_ld16(tmem + lane_off + C::COL_S + n0 + 16, v1);
                 tmem_ld_wait();
-                uint8_t *dst = sbf + (n0 / 64) * (C::M * 128);
+                uint32_t w[16];
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const float *v = jj < 2 ? v0 + jj * 8 : v1 + (jj - 2) * 8;
-                    uint4 pk;
-                    pk.x = pack_bf16x2(v[0], v[1]);
-                    pk.y = pack_bf16x2(v[2], v[3]);
-                    pk.z = pack_bf16x2(v[4], v[5]);
-                    pk.w = pack_bf16x2(v[6], v[7]);
-                    *reinterpret_cast<uint4 *>(dst + swz128(row, (n0 % 64) + jj * 8)) = pk;
+                for (int j = 0; j < 8; ++j) {
+                    w[j] = pack_bf16x2(v0[2 * j] * sbf, v0[2 * j + 1] * sbf);
+                    w[8 + j] = pack_bf16x2(v1[2 * j] * sbf, v1[2 * j + 1] * sbf);
                 }
+                tmem_st16u(tmem + lane_off + C::COL_SB + sb * (C::N / 2) + n0 / 2, w);
+                if (rescale) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    v0[j] *= dec;
-                    v1[j] *= dec;
+                    for (int j = 0; j < 16; ++j) {
+                        v0[j] *= f;
+                        v1[j] *= f;
+                    }
+                    tmem_st16(tmem + lane_off + C::COL_S + n0, v0);
+                    tmem_st16(tmem + lane_off + C::COL_S + n0 + 16, v1);
                 }
-                tmem_st16(tmem + lane_off + C::COL_S + n0, v0);
-                tmem_st16(tmem + lane_off + C::COL_S + n0 + 16, v1);
             }
-            fence_async_smem();
             tmem_st_wait();
             tc_fence_before();
             named_bar_sync(1, 128);
             if (gtid == 0) {
                 TRACE(8, it);
-                mbar_arrive(&wg1_bar);
+                mbar_arrive(&rt_bar);
+                mbar_arrive(&vempty_bar[v]);
             }
         }
-        // final state after the segment's last chunk
+        // final state after the segment's last chunk: S = exp(-rho) Ss
         if (seg == prm.nseg - 1 && prm.fin) {  // (a uniform test: group_wait handles an abort)
-            if (group_wait(&state_bar, (nch - 1) & 1, &abort_sh, &slot[2], 1, gtid, 128)) {
+            if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[3], 1, gtid, 128)) {
                 tc_fence_after();
+                const float sc = __expf(-rho_end);
                 float *dst = prm.fin + (((long long)b * H + hrow) * C::P + rp) * C::N;
 #pragma unroll 1
                 for (int n0 = 0; n0 < C::N; n0 += 16) {
@@ -946,127 +1000,96 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     if (hrow < H)
 #pragma unroll
                         for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(dst + n0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                            *reinterpret_cast<float4 *>(dst + n0 + j) =
+                                make_float4(v[j] * sc, v[j + 1] * sc, v[j + 2] * sc, v[j + 3] * sc);
                 }
             }
         }
-    } else if (warp >= 8 && warp < 12) {
-        // ---------------- masked, decayed score matrices ----------------
-        //   M_h[t, s] = CB[t, s] exp(cum_t - cum_s) dt_s = CB[t, s] u_t v_s   (s <= t)
-        // Q = 64: C B^T is an M = 64 accumulator (rows 16 q4 .. 16 q4 + 15 in
-        // lanes 0-15); lanes 16-31 take the row of lane - 16 and either the
-        // second head (two heads) or the second half of the columns.
-        // Q = 128: lane = row, every thread covers all heads and columns.
+    } else if (warp >= 8) {
+        // ---------------- A operand of the next chunk; epilogue of this one ----------------
+        // thread = row (head, p), half = which 32 of the Q steps
         const int gtid = tid - 256;
-        constexpr bool HALVES = C::Q == 64;
-        const int t = HALVES ? q4 * 16 + (lane & 15) : q4 * 32 + lane;
-        const int half = HALVES ? (lane >> 4) : 0;
-        constexpr int NH = (HALVES && C::HB == 2) ? 1 : C::HB;              // heads per thread
-        constexpr int NCOL = (HALVES && C::HB == 1) ? C::Q / 2 : C::Q;       // columns per thread
-        for (int it = 0; it < nch; ++it) {
-            if (!group_wait(&vfull_bar[it % NV], (it / NV) & 1, &abort_sh, &slot[3], 2, gtid, 128)) break;
-            if (!group_wait(&cb_bar, it & 1, &abort_sh, &slot[4], 2, gtid, 128)) break;
-            if (gtid == 0) TRACE(9, it);
-            tc_fence_after();
-            const float *vv = vec(it % NV);
-#pragma unroll 1
-            for (int cb0 = 0; cb0 < C::Q; cb0 += 32) {
-                float cb[32];
-                tmem_ld16(tmem + lane_off + C::COL_CB + cb0, *reinterpret_cast<float(*)[16]>(cb));
-                tmem_ld16(tmem + lane_off + C::COL_CB + cb0 + 16, *reinterpret_cast<float(*)[16]>(cb + 16));
-                tmem_ld_wait();
-                if (HALVES) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) cb[j] = __shfl_sync(0xffffffffu, cb[j], lane & 15);
-                }
-                // (two heads: each half-warp its head; one head: each half-warp
-                // its half of the columns)
-                const bool mine = !(HALVES && C::HB == 1) || (cb0 / 32) == half;
-#pragma unroll
-                for (int hi = 0; hi < (mine ? NH : 0); ++hi) {
-                    const int hh = (HALVES && C::HB == 2) ? half : hi;
-                    const float *vvv = vv + C::V_V + hh * C::Q;
-                    const bool wide = vv[C::V_WIDE + hh] != 0.f;
-                    const float ut = vv[C::V_U + hh * C::Q + t];
-                    uint8_t *dst = mm + hh * (C::Q * C::Q * 2) + (cb0 / 64) * (C::Q * 128);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        float m[8];
-                        if (!wide) {
-                            const float4 va = *reinterpret_cast<const float4 *>(vvv + cb0 + jj * 8);
-                            const float4 vb = *reinterpret_cast<const float4 *>(vvv + cb0 + jj * 8 + 4);
-                            const float vs[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int sc = cb0 + jj * 8 + j;
-                                const float prod = cb[jj * 8 + j] * ut * vs[j];
-                                m[j] = sc <= t ? prod : 0.f;
-                            }
-                        } else {
-                            F8 c8;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) c8.v[j] = cb[jj * 8 + j];
-                            const F8 r8 = wide_scores(c8, vv + C::V_CUM + hh * C::Q, vv + C::V_DT + hh * C::Q, t,
-                                                      cb0 + jj * 8);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) m[j] = r8.v[j];
-                        }
-                        uint4 pk;
-                        pk.x = pack_bf16x2(m[0], m[1]);
-                        pk.y = pack_bf16x2(m[2], m[3]);
-                        pk.z = pack_bf16x2(m[4], m[5]);
-                        pk.w = pack_bf16x2(m[6], m[7]);
-                        *reinterpret_cast<uint4 *>(dst + swz128(t, (cb0 % 64) + jj * 8)) = pk;
-                    }
-                }
-                __syncwarp();
-            }
-            (void)NCOL;
-            // exp(cum) for the epilogue (the stage may be refilled before it runs)
-            for (int i = gtid; i < HQ; i += 128) epi_vec[(it & 1) * HQ + i] = vv[C::V_ECUM + i];
-            fence_async_smem();
-            tc_fence_before();
-            named_bar_sync(2, 128);
-            if (gtid == 0) {
-                TRACE(10, it);
-                mbar_arrive(&mask_bar);
-                mbar_arrive(&epi_bar[it & 1]);
-            }
-        }
-    } else if (warp >= 12) {
-        // ---------------- epilogue ----------------
-        // y = intra + exp(cum) inter + D x for row (head, p), 16 steps t at a
-        // time: TMEM loads, x from L2 (the tile was just loaded), stores.
-        const int gtid = tid - 384;
+        const int half = (warp - 8) >> 2;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const long long hrow = h0 + rh;
         const bool live = hrow < H;
         const float dh = (prm.D && live) ? prm.D[hrow] : 0.f;
+        const uint32_t pcol = (uint32_t)(rp % 64);
+        const int blk = rh * C::PB + rp / 64;
         const long long ystride = H * C::P;
-        auto row_base = [&](int c) {
-            return (((long long)b * L + (long long)c * C::Q) * H + (live ? hrow : 0)) * C::P + rp;
-        };
-        uint32_t xp[C::Q / 2];
-        fetch_x_column<C>(prm.x + row_base(c0), ystride, live, xp);
-        for (int it = 0; it < nch; ++it) {
-            const int c = c0 + it;
-            if (!group_wait(&y_bar, it & 1, &abort_sh, &slot[6], 3, gtid, 128)) break;
-            if (!group_wait(&epi_bar[it & 1], (it >> 1) & 1, &abort_sh, &slot[5], 3, gtid, 128)) break;
-            if (gtid == 0) TRACE(11, it);
+        uint32_t xcur[16], xnext[16];
+        auto build = [&](int c, uint32_t(&xw)[16]) -> bool {
+            const int s = c % ST, v = c % NV, a = c % NB;
+            if (!group_wait(&full_bar[s], fill_parity(c, ST), &abort_sh, &slot[4], 2, gtid, 256)) return false;
+            if (!group_wait(&vfull_bar[v], fill_parity(c, NV), &abort_sh, &slot[5], 2, gtid, 256)) return false;
+            if (c >= NB && !group_wait(&afree_bar[a], free_parity(c, NB), &abort_sh, &slot[6], 2, gtid, 256))
+                return false;
+            if (gtid == 0) TRACE(5, c);
             tc_fence_after();
-            const float *ecum = epi_vec + (it & 1) * HQ + rh * C::Q;
-            const long long base = row_base(c);
-            epilogue_rows<C, YT>(tmem + lane_off, it, rh, ecum, xp, reinterpret_cast<YT *>(prm.y) + base, ystride,
-                                 dh, live);
-            // TMEM reads are done: let the next chunk's MMAs in, then fetch its x
+            const float *vv = vec(v);
+            build_a<C>(stage_x(s) + blk * (C::Q * 128), pcol, vv + C::V_AL + rh * C::Q + half * 32, half,
+                       tmem + lane_off + C::COL_A + a * C::Q, xw);
+            const bool wide = vv[C::V_FLAG + 1] != 0.f;
+            tmem_st_wait();
             tc_fence_before();
-            named_bar_sync(3, 128);
+            named_bar_sync(2, 256);
             if (gtid == 0) {
-                TRACE(12, it);
-                mbar_arrive(&free_r_bar);
-                mbar_arrive(&free_r3_bar[it & 1]);
+                TRACE(6, c);
+                wide_a[a] = wide ? 1 : 0;
+                mbar_arrive(&afull_bar[a]);
+                if (!wide) mbar_arrive(&empty_bar[s]);  // (a wide chunk's epilogue still reads the stage)
             }
-            if (it + 1 < nch) fetch_x_column<C>(prm.x + row_base(c + 1), ystride, live, xp);
+            return true;
+        };
+        auto epilogue = [&](int c, const uint32_t(&xw)[16]) -> bool {
+            const int s = c % ST, v = c % NV, r = c % NB;
+            if (!group_wait(&rfull_bar[r], fill_parity(c, NB), &abort_sh, &slot[7], 2, gtid, 256)) return false;
+            if (gtid == 0) TRACE(9, c);
+            tc_fence_after();
+            const float *vv = vec(v);
+            const float *ef = vv + C::V_EF + rh * C::Q + half * 32;
+            const bool wide = vv[C::V_FLAG + 1] != 0.f;
+            const uint32_t tr = tmem + lane_off + C::COL_R + r * C::Q + half * 32;
+            if (wide) {
+                wide_fixup<C>(tr, ef, stage_x(s) + blk * (C::Q * 128), stage_cb(s), vv + C::V_CUM + rh * C::Q,
+                              vv + C::V_DT + rh * C::Q, pcol, half * 32);
+                ef = ones_sh;
+            }
+            float acc[32];
+            tmem_ld16(tr, *reinterpret_cast<float(*)[16]>(acc));
+            tmem_ld16(tr + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
+            tmem_ld_wait();
+            if (live) {
+                YT *yp = reinterpret_cast<YT *>(prm.y) +
+                         (((long long)b * L + (long long)(c0 + c) * C::Q + half * 32) * H + hrow) * C::P + rp;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
+                    const uint32_t w0 = xw[j / 2], w1 = xw[j / 2 + 1];
+                    store_y<YT>(yp + (long long)j * ystride, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
+                    store_y<YT>(yp + (long long)(j + 1) * ystride,
+                                fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
+                    store_y<YT>(yp + (long long)(j + 2) * ystride, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
+                    store_y<YT>(yp + (long long)(j + 3) * ystride,
+                                fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
+                }
+            }
+            tc_fence_before();
+            named_bar_sync(2, 256);
+            if (gtid == 0) {
+                TRACE(10, c);
+                mbar_arrive(&rfree_bar[r]);
+                mbar_arrive(&vempty_bar[v]);
+                if (wide) mbar_arrive(&empty_bar[s]);
+            }
+            return true;
+        };
+        bool ok = nch > 0 ? build(0, xcur) : true;
+        for (int it = 0; ok && it < nch; ++it) {
+            if (it + 1 < nch && !build(it + 1, xnext)) break;
+            if (!epilogue(it, xcur)) break;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xcur[j] = xnext[j];
         }
     }
     // let this CTA's own copies and MMAs land (they normally have) before
@@ -1115,6 +1138,20 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over the CB matrices [planes][Q][Q], box (64, Q, 1), 128-byte
+// swizzle.
+bool make_cb_map(CUtensorMap *m, const void *base, uint64_t Q, uint64_t planes) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {Q, Q, planes};
+    cuuint64_t strides[2] = {Q * 2, Q * Q * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)Q, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Plan {
     int nseg, cps, nhb;
 };
@@ -1134,11 +1171,14 @@ Plan plan_for(const Dims &d) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Workspace: status word | segment states | segment totals.  The status
-// word is cleared on the stream by every call.
+size_t cb_bytes(const Dims &d) { return align256(sizeof(bf16) * d.b * d.nc * d.G * d.Q * d.Q); }
+
+// Workspace: status word and segment counters | CB matrices | segment
+// states | segment totals.  The header is cleared on the stream by every
+// call.
 template <class C>
-size_t header_bytes(const Dims &) {
-    return 256;
+size_t header_bytes(const Dims &d) {
+    return 256 + align256(sizeof(unsigned) * d.b * ((d.H + C::HB - 1) / C::HB));
 }
 
 #ifdef SSD_TRACE
@@ -1148,7 +1188,7 @@ constexpr size_t kTraceBytes = (32 * 256 + 2048) * sizeof(long long);
 template <class C>
 size_t workspace_for(const Dims &d) {
     const Plan p = plan_for<C>(d);
-    size_t bytes = header_bytes<C>(d);
+    size_t bytes = header_bytes<C>(d) + cb_bytes(d);
     if (p.nseg > 1)
         bytes += align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N) + align256(sizeof(float) * d.b * p.nseg * d.H);
 #ifdef SSD_TRACE
@@ -1158,17 +1198,86 @@ size_t workspace_for(const Dims &d) {
 }
 
 template <class C>
+cudaError_t raise_smem(const void *fn, int bytes, int &done) {
+    if (done >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done = bytes;
+    return e;
+}
+
+template <class C>
+cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, bf16 *cbm, unsigned *status, cudaStream_t s) {
+    CUtensorMap mb, mc;
+    if (!make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
+        return cudaErrorInvalidValue;
+    static int attr = 0;
+    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::SMEM_CB, attr);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)d.nc, (unsigned)d.G, (unsigned)d.b);
+    cb_mask_kernel<C><<<grid, 128, C::SMEM_CB, s>>>(mb, mc, cbm, (int)d.nc, (int)d.G, status);
+    e = cudaGetLastError();
+    timing_mark(s, "cb_mask_tc");
+    return e;
+}
+
+template <class C>
+cudaError_t launch_scan(const Dims &d, const TcParams &prm, ssd_dtype_t ydtype, const void *x, const void *B,
+                        const void *Cm, const bf16 *cbm, dim3 grid, const char *name, cudaStream_t s) {
+    CUtensorMap mx, mb, mc, mcb;
+    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) ||
+        !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q) || !make_cb_map(&mcb, cbm, C::Q, d.b * d.nc * d.G))
+        return cudaErrorInvalidValue;
+    static int attr_f = 0, attr_b = 0;
+    cudaError_t e;
+    if (ydtype == SSD_DTYPE_F32) {
+        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
+        if (e != cudaSuccess) return e;
+        chunk_scan_kernel<C, float><<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, mcb, prm);
+    } else {
+        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
+        if (e != cudaSuccess) return e;
+        chunk_scan_kernel<C, bf16><<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, mcb, prm);
+    }
+    e = cudaGetLastError();
+    timing_mark(s, name);
+    return e;
+}
+
+template <class C>
+cudaError_t launch_seg_state(const Dims &d, const TcParams &prm, const void *x, const void *B, dim3 grid,
+                             const char *name, cudaStream_t s) {
+    CUtensorMap mx, mb;
+    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q))
+        return cudaErrorInvalidValue;
+    const int smem = C::SMEM_SEG_BASE + (int)(C::HB * prm.cps * sizeof(float));
+    if (smem > kSmemLimit) return cudaErrorInvalidValue;
+    static int attr = 0;
+    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(seg_state_kernel<C>), smem, attr);
+    if (e != cudaSuccess) return e;
+    seg_state_kernel<C><<<grid, kSegThreads, smem, s>>>(mx, mb, prm);
+    e = cudaGetLastError();
+    timing_mark(s, name);
+    return e;
+}
+
+TcParams base_params(const Dims &d, const void *dt) {
+    TcParams prm{};
+    prm.dt = static_cast<const bf16 *>(dt);
+    prm.b = d.b;
+    prm.L = d.L;
+    prm.H = d.H;
+    prm.G = d.G;
+    prm.hpg = d.hpg;
+    prm.nc = (int)d.nc;
+    return prm;
+}
+
+template <class C>
 cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B,
                     const void *Cm, const float *D, const float *init, void *y, float *fin, void *ws,
                     cudaStream_t s) {
     const Plan p = plan_for<C>(d);
-    CUtensorMap mx, mb, mc;
-    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) ||
-        !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
-        return cudaErrorInvalidValue;
-    TcParams prm;
-    prm.x = static_cast<const bf16 *>(x);
-    prm.dt = static_cast<const bf16 *>(dt);
+    TcParams prm = base_params(d, dt);
     prm.A = A;
     prm.D = D;
     prm.init = init;
@@ -1177,70 +1286,30 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     char *w = static_cast<char *>(ws);
     const size_t hdr = header_bytes<C>(d);
     prm.status = reinterpret_cast<unsigned *>(w);
-    prm.seg_state = nullptr;
-    prm.seg_tot = nullptr;
+    prm.counters = reinterpret_cast<unsigned *>(w + 256);
+    bf16 *cbm = reinterpret_cast<bf16 *>(w + hdr);
+    const size_t seg_off = hdr + cb_bytes(d);
     if (p.nseg > 1) {
-        prm.seg_state = reinterpret_cast<float *>(w + hdr);
-        prm.seg_tot = reinterpret_cast<float *>(w + hdr + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
+        prm.seg_state = reinterpret_cast<float *>(w + seg_off);
+        prm.seg_tot = reinterpret_cast<float *>(w + seg_off + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
     }
     prm.nhb = p.nhb;
-    prm.cum_in = nullptr;
-    prm.entering = nullptr;
-    prm.trace = nullptr;
+    prm.nseg = p.nseg;
+    prm.cps = p.cps;
+    prm.seg_pass = 1;
 #ifdef SSD_TRACE
     prm.trace = reinterpret_cast<long long *>(w + workspace_for<C>(d) - kTraceBytes);
 #endif
-    prm.b = d.b;
-    prm.L = d.L;
-    prm.H = d.H;
-    prm.G = d.G;
-    prm.hpg = d.hpg;
-    prm.nc = (int)d.nc;
-    prm.nseg = p.nseg;
-    prm.cps = p.cps;
-    prm.y_f32 = ydtype == SSD_DTYPE_F32 ? 1 : 0;
-
-    // raise each kernel's dynamic shared memory limit to what this call needs
-    static int scan_attr = 0, seg_attr = 0;
-    auto scan_kernel = prm.y_f32 ? chunk_scan_kernel<C, float> : chunk_scan_kernel<C, bf16>;
-    const int seg_smem = C::SMEM_SEG_BASE + (int)(C::HB * p.cps * sizeof(float));
-    if (scan_attr < C::SMEM_SCAN) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<C, float>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_SCAN);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunk_scan_kernel<C, bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     C::SMEM_SCAN);
-        if (e != cudaSuccess) return e;
-        scan_attr = C::SMEM_SCAN;
-    }
-    if (p.nseg > 1 && seg_attr < seg_smem) {
-        cudaError_t e = cudaFuncSetAttribute(seg_state_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             seg_smem);
-        if (e != cudaSuccess) return e;
-        seg_attr = seg_smem;
-    }
-    if (seg_smem > kSmemLimit) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(w, 0, hdr, s);
     if (e != cudaSuccess) return e;
     timing_begin(s);
+    e = launch_cb<C>(d, B, Cm, cbm, prm.status, s);
+    if (e != cudaSuccess) return e;
     if (p.nseg > 1) {
-        dim3 grid(p.nseg - 1, p.nhb, (unsigned)d.b);
-        seg_state_kernel<C><<<grid, kSegThreads, seg_smem, s>>>(mx, mb, prm);
-        e = cudaGetLastError();
+        e = launch_seg_state<C>(d, prm, x, B, dim3(p.nseg - 1, p.nhb, (unsigned)d.b), "seg_state_tc", s);
         if (e != cudaSuccess) return e;
-        timing_mark(s, "seg_state_tc");
-        const int pn = (int)(C::P * C::N);
-        dim3 pgrid((unsigned)((pn / 4 + 255) / 256), (unsigned)d.H, (unsigned)d.b);
-        segment_pass_kernel<<<pgrid, 256, 0, s>>>(init, prm.seg_state, prm.seg_tot, d.H, pn, p.nseg);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        timing_mark(s, "segment_pass");
     }
-    dim3 grid(p.nseg, p.nhb, (unsigned)d.b);
-    scan_kernel<<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
-    e = cudaGetLastError();
-    timing_mark(s, "chunk_scan_tc");
-    return e;
+    return launch_scan<C>(d, prm, ydtype, x, B, Cm, cbm, dim3(p.nseg, p.nhb, (unsigned)d.b), "chunk_scan_tc", s);
 }
 
 // Dispatch over the compiled tile configurations.
@@ -1252,6 +1321,12 @@ bool dispatch(const Dims &d, F &&f) {
     return false;
 }
 
+template <class C>
+bool shape_ok(const Dims &d) {
+    return C::SCAN_FITS && C::TMEM_FITS && (d.G == 1 || d.hpg % C::HB == 0) && d.L < (1ll << 31) &&
+           d.H < (1 << 30) && d.b < 65536 && d.nc < 65536 && d.G < 65536 && d.b * d.nc * d.G < (1ll << 31);
+}
+
 }  // namespace
 
 bool tc_fwd_supported(const Dims &d, ssd_dtype_t dtype) {
@@ -1260,12 +1335,7 @@ bool tc_fwd_supported(const Dims &d, ssd_dtype_t dtype) {
     bool ok = false;
     dispatch(d, [&](auto c) {
         using C = decltype(c);
-        ok = C::SCAN_FITS && C::TMEM_FITS && (d.G == 1 || d.hpg % C::HB == 0) && d.L < (1ll << 31) &&
-             d.H < (1 << 30) && d.b < 65536;
-        if (ok) {
-            const Plan p = plan_for<C>(d);
-            ok = C::SMEM_SEG_BASE + (int)(C::HB * p.cps * sizeof(float)) <= kSmemLimit;
-        }
+        ok = shape_ok<C>(d) && C::SMEM_SEG_BASE + (int)(C::HB * plan_for<C>(d).cps * sizeof(float)) <= kSmemLimit;
     });
     return ok;
 }
@@ -1289,89 +1359,51 @@ bool tc_stage_supported(const Dims &d, ssd_dtype_t dtype) {
     bool ok = false;
     dispatch(d, [&](auto c) {
         using C = decltype(c);
-        ok = C::SCAN_FITS && C::TMEM_FITS && (d.G == 1 || d.hpg % C::HB == 0) && d.L < (1ll << 31) &&
-             d.H < (1 << 30) && d.b < 65536 && d.nc < 65536 &&
-             C::SMEM_SEG_BASE + (int)(C::HB * sizeof(float)) <= kSmemLimit;
+        ok = shape_ok<C>(d) && C::SMEM_SEG_BASE + (int)(C::HB * sizeof(float)) <= kSmemLimit;
     });
     return ok;
 }
 
 namespace {
 
-// Parameters of a one-chunk-per-segment launch of the fused kernels, as the
-// stage entry points use them.
-TcParams stage_params(const Dims &d, const void *dt, const float *cum) {
-    TcParams prm{};
-    prm.dt = static_cast<const bf16 *>(dt);
-    prm.cum_in = cum;
-    prm.b = d.b;
-    prm.L = d.L;
-    prm.H = d.H;
-    prm.G = d.G;
-    prm.hpg = d.hpg;
-    prm.nc = (int)d.nc;
-    prm.nseg = (int)d.nc;
-    prm.cps = 1;
-    prm.y_f32 = 1;
-    return prm;
-}
-
 template <class C>
 cudaError_t run_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
                             float *states, cudaStream_t s) {
-    CUtensorMap mx, mb;
-    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q))
-        return cudaErrorInvalidValue;
-    TcParams prm = stage_params(d, dt, cum);
+    TcParams prm = base_params(d, dt);
+    prm.cum_in = cum;
     prm.seg_state = states;  // [b, nc, H, P, N]: one segment per chunk
+    prm.nseg = (int)d.nc;
+    prm.cps = 1;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
-    const int smem = C::SMEM_SEG_BASE + (int)(C::HB * sizeof(float));
-    static int attr = 0;
-    if (attr < smem) {
-        cudaError_t e = cudaFuncSetAttribute(seg_state_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr = smem;
-    }
     timing_begin(s);
-    dim3 grid((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b);
-    seg_state_kernel<C><<<grid, kSegThreads, smem, s>>>(mx, mb, prm);
-    const cudaError_t e = cudaGetLastError();
-    timing_mark(s, "chunk_state_tc");
-    return e;
+    return launch_seg_state<C>(d, prm, x, B, dim3((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b), "chunk_state_tc",
+                               s);
 }
 
+// The CB matrices of a stage call live in stream-ordered scratch
+// (cudaMallocAsync / cudaFreeAsync on the caller's stream).
 template <class C>
 cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
                            const void *Cm, const float *cum, const float *states_in, const float *D, void *y,
                            cudaStream_t s) {
-    CUtensorMap mx, mb, mc;
-    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) ||
-        !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
-        return cudaErrorInvalidValue;
-    TcParams prm = stage_params(d, dt, cum);
-    prm.x = static_cast<const bf16 *>(x);
+    TcParams prm = base_params(d, dt);
+    prm.cum_in = cum;
     prm.entering = states_in;  // [b, nc, H, P, N]: the state entering each chunk
     prm.D = D;
     prm.y = y;
-    prm.y_f32 = ydtype == SSD_DTYPE_F32 ? 1 : 0;
+    prm.nseg = (int)d.nc;
+    prm.cps = 1;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
-    static int attr = 0;
-    if (attr < C::SMEM_SCAN) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_scan_kernel<C, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_SCAN);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunk_scan_kernel<C, bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     C::SMEM_SCAN);
-        if (e != cudaSuccess) return e;
-        attr = C::SMEM_SCAN;
-    }
-    auto kern = prm.y_f32 ? chunk_scan_kernel<C, float> : chunk_scan_kernel<C, bf16>;
+    void *cbm = nullptr;
+    cudaError_t e = cudaMallocAsync(&cbm, cb_bytes(d), s);
+    if (e != cudaSuccess) return e;
     timing_begin(s);
-    dim3 grid((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b);
-    kern<<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, prm);
-    const cudaError_t e = cudaGetLastError();
-    timing_mark(s, "chunk_scan_stage_tc");
-    return e;
+    e = launch_cb<C>(d, B, Cm, static_cast<bf16 *>(cbm), nullptr, s);
+    if (e == cudaSuccess)
+        e = launch_scan<C>(d, prm, ydtype, x, B, Cm, static_cast<const bf16 *>(cbm),
+                           dim3((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b), "chunk_scan_stage_tc", s);
+    const cudaError_t e2 = cudaFreeAsync(cbm, s);
+    return e != cudaSuccess ? e : e2;
 }
 
 }  // namespace

@@ -103,6 +103,46 @@ def test_ssd_fwd_small(name):
     check(to_np(fin), fin_ref, TOL[cfg.dtype], f"{name} final")
 
 
+def decay_regime_inputs(cfg, ranges):
+    """Inputs of `cfg` with dt of head h scaled (then rounded to bf16) so that
+    the median decay range of its chunks, -sum(dt A) over a chunk, is about
+    ranges[h]: chunks that keep the state scale, chunks that rescale it and
+    chunks too wide to scale at all, in chosen heads."""
+    inp = si.make_inputs(cfg)
+    Q = cfg.chunk_size
+    dt = si.bf16_bits_to_f32(inp.dt).astype(np.float64)
+    A = inp.A.astype(np.float64)
+    per_chunk = -(dt * A[None, None, :]).reshape(cfg.batch, cfg.seqlen // Q, Q, cfg.nheads).sum(2)
+    med = np.median(per_chunk.reshape(-1, cfg.nheads), axis=0)
+    inp.dt = si.to_bf16_bits(dt * (np.asarray(ranges, np.float64) / med)[None, None, :])
+    return inp
+
+
+@pytest.mark.parametrize("ranges", [
+    # head blocks: both heads too wide to scale | one wide, one quiet |
+    # rescaling every chunk and every other chunk | quiet
+    (400.0, 300.0, 200.0, 10.0, 100.0, 60.0, 30.0, 3.0),
+    # every head near the limit: rescales, with some chunks past it
+    (115.0,) * 8,
+])
+def test_ssd_fwd_decay_regimes(ranges):
+    """Tensor-core path with strong decay: the scaled-state bookkeeping (rescale
+    when an exponent would leave its range; the direct path for chunks whose own
+    range is too wide to scale) against the oracle, fused and staged."""
+    cfg = si.SSDConfig("tc_decay", 1, 1280, 8, 64, 128, 1, 64, "bf16", True, 91)
+    inp = decay_regime_inputs(cfg, ranges)
+    t = gpu_inputs(inp)
+    y, fin = ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"], chunk_size=64)
+    y_ref, fin_ref = oracle_full(inp)
+    check(to_np(y), y_ref, TOL["bf16"], "decay regimes y")
+    check(to_np(fin), fin_ref, TOL["bf16"], "decay regimes final")
+    cum = ssd.ssd_chunk_cumsum(t["dt"], t["A"], 64)
+    st = ssd.ssd_chunk_state(t["x"], t["dt"], t["B"], cum)
+    sin, _ = ssd.ssd_state_passing(st, cum, t["init_state"])
+    y2 = ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum, sin, t["D"])
+    check(to_np(y2), y_ref, TOL["bf16"], "decay regimes staged y")
+
+
 @pytest.mark.parametrize("name", ["bf16_p64_n128", "bf16_p128_n256_q128", "tc_p64_n128_seg", "bf16_p128_n256_q64"])
 def test_ssd_fwd_bf16_output(name):
     cfg = SMALL[name]
