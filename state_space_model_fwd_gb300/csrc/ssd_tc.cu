@@ -55,6 +55,7 @@ constexpr float kLambda = 64.f;               // |exponent| bound of the scaled 
 
 struct TcParams {
     long long *trace;  // optional event trace of CTA (0, 0, 0) (trace builds only)
+    const bf16 *x;     // [b, L, H, P] (the epilogue's D x term)
     const bf16 *dt;
     const float *A, *D, *init;
     void *y;
@@ -69,6 +70,15 @@ struct TcParams {
     int hpg, nc, nseg, cps;  // cps: chunks per segment
     int nhb;
     int seg_pass;
+    int dt_tma;  // dt has a TMA map (H % 8 == 0): the vector warps take it from a TMA ring
+    // [b, nc, G] set to 1 by the C B^T kernel once a matrix is in memory;
+    // the chunk scan's TMA producer polls the flag of a chunk before loading
+    // its matrix (the C B^T grid is wholly resident or done by then)
+    unsigned *cb_ready;
+    // launched with a programmatic dependency on the segment-state kernel:
+    // the state warps of segments > 0 wait for it before reading the states
+    // entering them
+    int dep_seg;
 };
 
 template <int P_, int N_, int Q_>
@@ -88,11 +98,16 @@ struct Cfg {
     static constexpr int V_F = 4 * HB * Q, V_SBF = V_F + HB, V_RHON = V_SBF + HB, V_FLAG = V_RHON + HB;
     static constexpr int VEC_FLOATS = 4 * HB * Q + 32;
     static constexpr int NV = 4;  // vector sets in flight
+    static constexpr int DT_BYTES = 8 * Q * 2;  // dt of 8 heads (one 16-byte box row) x Q steps, one TMA box
+    static constexpr int DT_RING = 4 * DT_BYTES;  // kDtAhead boxes
     static constexpr int VEC_RING = ((NV * VEC_FLOATS * 4 + 1023) / 1024) * 1024;
 
-    // scan kernel: TMA stages of (x, B, C, CB) and the vector ring
+    // scan kernel: TMA stages of (x, B, C, CB), the vector ring, and the y
+    // tile of one chunk ([half][M/64 blocks][Q/2 steps][64], fp32 or bf16)
+    // that the TMA stores to HBM
     static constexpr int SCAN_STAGE = X_BYTES + 2 * BC_BYTES + CBM_BYTES;
-    static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + 1024; }
+    static constexpr int Y_BYTES = M * Q * 4;
+    static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + Y_BYTES + DT_RING + 1024; }
     static constexpr int SCAN_ST = scan_smem(4) <= kSmemLimit ? 4 : (scan_smem(3) <= kSmemLimit ? 3 : 2);
     static constexpr int SMEM_SCAN = scan_smem(SCAN_ST);
     static constexpr bool SCAN_FITS = SMEM_SCAN <= kSmemLimit;
@@ -102,12 +117,11 @@ struct Cfg {
     static constexpr int COL_S = 0, COL_SB = N, COL_A = N + NB * N / 2, COL_R = COL_A + NB * Q;
     static constexpr bool TMEM_FITS = tmem_cols(NB) <= 512;
 
-    // segment-state kernel: TMA stages of (x, B), the vector ring, then the
-    // chunk totals [HB][cps]
+    // segment-state kernel: TMA stages of (x, B) and the vector ring
     static constexpr int SEG_STAGE = X_BYTES + BC_BYTES;
-    static constexpr int seg_smem(int st) { return st * SEG_STAGE + VEC_RING + 1024; }
-    static constexpr int SEG_ST = seg_smem(4) + 4096 <= kSmemLimit ? 4 : (seg_smem(3) + 4096 <= kSmemLimit ? 3 : 2);
-    static constexpr int SMEM_SEG_BASE = seg_smem(SEG_ST);
+    static constexpr int seg_smem(int st) { return st * SEG_STAGE + VEC_RING + DT_RING + 1024; }
+    static constexpr int SEG_ST = seg_smem(4) <= kSmemLimit ? 4 : (seg_smem(3) <= kSmemLimit ? 3 : 2);
+    static constexpr int SMEM_SEG = seg_smem(SEG_ST);
     static constexpr int SEG_COLS = N + 2 * Q;  // S [N] | A hi+lo [Q] x 2
     static constexpr uint32_t SEG_TMEM =
         SEG_COLS <= 64 ? 64 : SEG_COLS <= 128 ? 128 : SEG_COLS <= 256 ? 256 : 512;
@@ -119,10 +133,23 @@ struct Cfg {
 // Event trace (SSD_TRACE builds): clock64() of role events of CTA (0, 0, 0),
 // trace[event * 256 + chunk].  Compiled out otherwise.
 #ifdef SSD_TRACE
+// (kept in shared memory while the kernel runs: a global store before an
+// mbarrier arrive would delay the arrive until the store is performed)
+#define TRACE_DECL __shared__ long long trace_sh[32 * 16]
 #define TRACE(ev, it)                                                                                  \
     do {                                                                                               \
-        if (prm.trace && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (it) < 256)          \
-            prm.trace[(ev) * 256 + (it)] = clock64();                                                  \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && (it) < 16)                         \
+            trace_sh[(ev) * 16 + (it)] = clock64();                                                    \
+    } while (0)
+#define TRACE_INIT()                                                                                   \
+    do {                                                                                               \
+        for (int i_ = threadIdx.x; i_ < 32 * 16; i_ += blockDim.x) trace_sh[i_] = 0;                   \
+    } while (0)
+#define TRACE_FLUSH()                                                                                  \
+    do {                                                                                               \
+        if (prm.trace && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)                         \
+            for (int i_ = threadIdx.x; i_ < 32 * 16; i_ += blockDim.x)                                 \
+                if (trace_sh[i_]) prm.trace[(i_ / 16) * 256 + i_ % 16] = trace_sh[i_];                 \
     } while (0)
 #define TRACE_CTA(slot)                                                                                 \
     do {                                                                                                 \
@@ -131,7 +158,24 @@ struct Cfg {
             if (cta_ < 1024) prm.trace[32 * 256 + 2 * cta_ + (slot)] = (long long)globaltimer_ns();       \
         }                                                                                                \
     } while (0)
+#define TRACE_CTA2(slot)                                                                                \
+    do {                                                                                                 \
+        if (prm.trace) {                                                                                 \
+            const int cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);             \
+            if (cta_ < 1024) prm.trace[32 * 256 + 2048 + 2 * cta_ + (slot)] = (long long)globaltimer_ns(); \
+        }                                                                                                \
+    } while (0)
 #else
+#define TRACE_DECL
+#define TRACE_INIT() \
+    do {             \
+    } while (0)
+#define TRACE_FLUSH() \
+    do {              \
+    } while (0)
+#define TRACE_CTA2(slot) \
+    do {                 \
+    } while (0)
 #define TRACE_CTA(slot) \
     do {                \
     } while (0)
@@ -172,69 +216,171 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, volat
     return *slot != 0;
 }
 
+// Poll a flag in global memory (set by another grid) until it is non-zero,
+// with the same bound as wait_bounded; then order the acquire before this
+// thread's TMA reads.
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, volatile int *abort_flag) {
+    if (ld_acquire_gpu(flag) == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(flag) == 0) {
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                return false;
+            }
+            __nanosleep(200);
+        }
+    }
+    fence_async_global();
+    return true;
+}
+
 // Phase parity to wait for at the it-th use of one of n ring slots: the
 // fill of round it / n ("full" side) or the release of the previous round
 // ("free" side, only for it >= n).
 __device__ __forceinline__ uint32_t fill_parity(int it, int n) { return (uint32_t)((it / n) & 1); }
 __device__ __forceinline__ uint32_t free_parity(int it, int n) { return (uint32_t)(((it / n) & 1) ^ 1); }
 
-// Inclusive scan of dt*A over one chunk for one head, by one warp; returns
-// the chunk total.
-template <int Q>
-__device__ __forceinline__ float warp_chunk_cumsum(const float *dtv, float a, float *cum) {
-    constexpr int QPL = Q / 32;
+// Per-chunk vectors are computed by one warp with everything in registers:
+// lane l holds steps q = QPL l .. QPL l + QPL - 1 of every head of the CTA.
+constexpr int kDtAhead = 4;  // chunks of dt loads in flight ahead of use
+
+template <class C>
+struct ChunkDt {
+    static constexpr int QPL = C::Q / 32;
+    float d[C::HB][QPL];
+};
+
+// dt of chunk c (plain loads; the caller keeps kDtAhead chunks in flight).
+template <class C>
+__device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int c, ChunkDt<C> &o) {
     const int lane = threadIdx.x & 31;
-    float v[QPL];
-    float run = 0.f;
 #pragma unroll
-    for (int i = 0; i < QPL; ++i) {
-        run += dtv[lane * QPL + i] * a;
-        v[i] = run;
-    }
-    float tot = run;
+    for (int hh = 0; hh < C::HB; ++hh)
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, tot, off);
-        if (lane >= off) tot += o;
-    }
-    const float excl = tot - run;
-#pragma unroll
-    for (int i = 0; i < QPL; ++i) cum[lane * QPL + i] = v[i] + excl;
-    return __shfl_sync(0xffffffffu, tot, 31);
+        for (int j = 0; j < ChunkDt<C>::QPL; ++j) {
+            const long long h = h0 + hh;
+            const long long t = (long long)c * C::Q + ChunkDt<C>::QPL * lane + j;
+            o.d[hh][j] = h < prm.H ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + t) * prm.H + h)) : 0.f;
+        }
 }
 
-// In-chunk cumulative decay of chunk c for head h into cum[Q] (one warp):
-// read from the caller's dA_cumsum when given, else the scan of dt*A.
-// Returns the chunk total.
+// dt of the chunks ahead for a vector warp.  With a TMA map, lane 0 keeps
+// kDtAhead boxes ([Q steps][8 heads] bf16) in flight in a private ring, so
+// no global load of the warp is outstanding when it arrives on a barrier
+// (an arrive waits for the arriving thread's earlier loads); without one
+// (H not a multiple of 8) each chunk's dt is loaded when needed.
 template <class C>
-__device__ __forceinline__ float chunk_cum(const TcParams &prm, int b, long long h, int c, const float *dtv, float a,
-                                           float *cum) {
-    if (prm.cum_in) {
+struct DtFeed {
+    uint8_t *ring;
+    uint64_t *bar;  // [kDtAhead], count 1
+    const CUtensorMap *map;
+    int b, h0, n;
+    int issued;  // boxes issued so far (step i's box went to slot i % kDtAhead)
+    __device__ __forceinline__ void issue(int k, int c) {
+        mbar_arrive_expect_tx(&bar[k], C::DT_BYTES);
+        tma_load_3d(ring + k * C::DT_BYTES, map, &bar[k], h0 & ~7, c * C::Q, b);
+        ++issued;
+    }
+    template <class F>
+    __device__ __forceinline__ void start(const TcParams &prm, F chunk_of) {
+        issued = 0;
+        if (prm.dt_tma && (threadIdx.x & 31) == 0)
+#pragma unroll
+            for (int k = 0; k < kDtAhead; ++k)
+                if (k < n) issue(k, chunk_of(k));
+    }
+    // dt of step `it` (chunk chunk_of(it)); false when the wait gave up
+    template <class F>
+    __device__ __forceinline__ bool take(const TcParams &prm, int it, F chunk_of, volatile int *abort_flag,
+                                         ChunkDt<C> &o) {
         const int lane = threadIdx.x & 31;
-        const float *src = prm.cum_in + (((long long)b * prm.H + (h < prm.H ? h : 0)) * prm.nc + c) * C::Q;
-        for (int q = lane; q < C::Q; q += 32) cum[q] = h < prm.H ? __ldg(src + q) : 0.f;
+        if (!prm.dt_tma) {
+            fetch_dt<C>(prm, b, h0, chunk_of(it), o);
+            return true;
+        }
+        const int k = it % kDtAhead;
+        int ok = lane == 0 ? (wait_bounded(&bar[k], (uint32_t)((it / kDtAhead) & 1), abort_flag) ? 1 : 0) : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+        const unsigned short *d16 = reinterpret_cast<const unsigned short *>(ring + k * C::DT_BYTES);
+#pragma unroll
+        for (int hh = 0; hh < C::HB; ++hh)
+#pragma unroll
+            for (int j = 0; j < ChunkDt<C>::QPL; ++j)
+                o.d[hh][j] = h0 + hh < prm.H
+                                 ? __uint_as_float((uint32_t)d16[(ChunkDt<C>::QPL * lane + j) * 8 + (h0 & 7) + hh] << 16)
+                                 : 0.f;
         __syncwarp();
-        return cum[C::Q - 1];
+        if (lane == 0 && it + kDtAhead < n) {
+            fence_async_smem();
+            issue(k, chunk_of(it + kDtAhead));
+        }
+        return true;
     }
-    const float total = warp_chunk_cumsum<C::Q>(dtv, a, cum);
-    __syncwarp();
-    return total;
+    // let outstanding boxes land before the CTA exits (lane 0)
+    __device__ __forceinline__ void drain() {
+        if ((threadIdx.x & 31) == 0)
+#pragma unroll
+            for (int k = 0; k < kDtAhead; ++k) {
+                const int nk = issued > k ? (issued - k + kDtAhead - 1) / kDtAhead : 0;  // boxes slot k received
+                if (nk > 0) mbar_wait(&bar[k], (uint32_t)((nk - 1) & 1), kDrainNs);
+            }
+    }
+};
+
+// In-chunk cumulative decay of every head for this lane's steps: the scan of
+// dt*A (all heads' shuffle chains interleaved), or the caller's dA_cumsum.
+// T[hh] = the chunk total (cum of the last step).
+template <class C>
+__device__ __forceinline__ void chunk_cums(const TcParams &prm, int b, int h0, int c, const ChunkDt<C> &dt,
+                                           float (&cum)[C::HB][C::Q / 32], float (&T)[C::HB]) {
+    constexpr int QPL = C::Q / 32;
+    const int lane = threadIdx.x & 31;
+    if (prm.cum_in) {
+#pragma unroll
+        for (int hh = 0; hh < C::HB; ++hh) {
+            const long long h = h0 + hh;
+            const float *src = prm.cum_in + (((long long)b * prm.H + (h < prm.H ? h : 0)) * prm.nc + c) * C::Q;
+#pragma unroll
+            for (int j = 0; j < QPL; ++j) cum[hh][j] = h < prm.H ? __ldg(src + QPL * lane + j) : 0.f;
+            T[hh] = h < prm.H ? __ldg(src + C::Q - 1) : 0.f;
+        }
+        return;
+    }
+    float run[C::HB], tot[C::HB];
+#pragma unroll
+    for (int hh = 0; hh < C::HB; ++hh) {
+        const long long h = h0 + hh;
+        const float a = (h < prm.H && prm.A) ? prm.A[h] : 0.f;
+        run[hh] = 0.f;
+#pragma unroll
+        for (int j = 0; j < QPL; ++j) {
+            run[hh] += dt.d[hh][j] * a;
+            cum[hh][j] = run[hh];
+        }
+        tot[hh] = run[hh];
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+        for (int hh = 0; hh < C::HB; ++hh) {
+            const float o = __shfl_up_sync(0xffffffffu, tot[hh], off);
+            if (lane >= off) tot[hh] += o;
+        }
+#pragma unroll
+    for (int hh = 0; hh < C::HB; ++hh) {
+        const float excl = tot[hh] - run[hh];
+#pragma unroll
+        for (int j = 0; j < QPL; ++j) cum[hh][j] += excl;
+        T[hh] = __shfl_sync(0xffffffffu, tot[hh], 31);
+    }
 }
 
-// dt of the CTA's heads for chunk c, lane-strided: element lane + 32 i of
-// the [HB][Q] block.
-template <class C>
-__device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int c, float (&d)[C::HB * C::Q / 32]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int i = 0; i < C::HB * C::Q / 32; ++i) {
-        const int idx = lane + 32 * i;
-        const int hh = idx / C::Q, q = idx % C::Q;
-        const long long h = h0 + hh;
-        d[i] = h < prm.H ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + (long long)c * C::Q + q) * prm.H + h))
-                         : 0.f;
-    }
+// Order-preserving integer key of a float (for warp min / max reductions).
+__device__ __forceinline__ int fkey(float f) {
+    const int i = __float_as_int(f);
+    return i >= 0 ? i : i ^ 0x7FFFFFFF;
 }
+__device__ __forceinline__ float unkey(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
 
 // Build this thread's half of the A operand of one chunk in TMEM:
 //   a_s = f_s x_s (s in [32 half, 32 half + 32)), split into bf16 hi and lo
@@ -245,15 +391,18 @@ __device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int
 //   (two bf16 per word) for the epilogue's D x term.
 template <class C>
 __device__ __forceinline__ void build_a(const uint8_t *xs_blk, uint32_t pcol, const float *f, int half,
-                                       uint32_t tmem_a, uint32_t (&xw)[16]) {
+                                       uint32_t tmem_a) {
     uint32_t hi[16], lo[16];
-    const unsigned short *xs16 = reinterpret_cast<const unsigned short *>(xs_blk);
+    // byte offset of (row s, column pcol) is 128 s + sw[s % 8]: the 16-byte
+    // chunk of the column moves with the row's position in its 8-row atom
+    const uint8_t *sw[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) sw[k] = xs_blk + (((((pcol >> 3) ^ (uint32_t)k) & 7u) << 4) | ((pcol & 7u) << 1));
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        const uint32_t s0 = (uint32_t)(half * 32 + 2 * j);
-        const uint32_t x0 = xs16[swz128(s0, pcol) >> 1];
-        const uint32_t x1 = xs16[swz128(s0 + 1, pcol) >> 1];
-        xw[j] = x0 | (x1 << 16);
+        const int s0 = half * 32 + 2 * j;
+        const uint32_t x0 = *reinterpret_cast<const unsigned short *>(sw[s0 & 7] + s0 * 128);
+        const uint32_t x1 = *reinterpret_cast<const unsigned short *>(sw[(s0 + 1) & 7] + (s0 + 1) * 128);
         const float a0 = __uint_as_float(x0 << 16) * f[2 * j];
         const float a1 = __uint_as_float(x1 << 16) * f[2 * j + 1];
         const uint32_t h = pack_bf16x2(a0, a1);
@@ -262,6 +411,18 @@ __device__ __forceinline__ void build_a(const uint8_t *xs_blk, uint32_t pcol, co
     }
     tmem_st16u(tmem_a + half * 16, hi);
     tmem_st16u(tmem_a + C::Q / 2 + half * 16, lo);
+}
+
+// x[t][p] of one (head, p) row for 32 consecutive steps, two bf16 per word,
+// from global memory (L2): fetched a chunk ahead by the epilogue.
+__device__ __forceinline__ void fetch_x_half(const bf16 *xg, long long stride, bool live, uint32_t (&xp)[16]) {
+    const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xg);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const uint32_t lo = live ? __ldg(x16 + (long long)(2 * j) * stride) : 0u;
+        const uint32_t hi = live ? __ldg(x16 + (long long)(2 * j + 1) * stride) : 0u;
+        xp[j] = lo | (hi << 16);
+    }
 }
 
 // TMA loads of chunk c: x tiles of the CTA's heads, B, and (optionally) C.
@@ -291,7 +452,7 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 template <class C>
 __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CUtensorMap mb,
                                                       const __grid_constant__ CUtensorMap mc, bf16 *cbm, int nc,
-                                                      int G, unsigned *status) {
+                                                      int G, unsigned *ready, unsigned *status) {
     static_assert(C::Q == 64, "the M = 64 accumulator layout is assumed");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -301,6 +462,7 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
     __shared__ int ok_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    griddep_launch();
     if (warp == 0) {
         tmem_alloc(&tmem_base_sh, 64);
         tmem_relinquish();
@@ -325,10 +487,11 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
         if (mbar_wait(&full_bar, 0, kWaitNs)) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(C::Q, C::Q, false, false);
+            const uint64_t dc = sdesc(smem_u32(cs), 16, 1024), db = sdesc(smem_u32(bs), 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < C::N / 16; ++ks) {
                 const uint32_t koff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                mma_bf16(tmem, sdesc(smem_u32(cs) + koff, 16, 1024), sdesc(smem_u32(bs) + koff, 16, 1024), id, ks > 0);
+                mma_bf16(tmem, desc_add(dc, koff), desc_add(db, koff), id, ks > 0);
             }
             mma_commit(&done_bar);
             ok = mbar_wait(&done_bar, 0, kWaitNs) ? 1 : 0;
@@ -358,9 +521,11 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
                 dst[k] = w;
             }
         }
+        __threadfence();
     }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && ok_sh && ready) st_release_gpu(ready + ((long long)b * nc + c) * G + g, 1u);
     if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
@@ -378,12 +543,15 @@ constexpr int kSegThreads = 384;
 
 template <class C>
 __global__ void __launch_bounds__(kSegThreads, 1)
-    seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb, TcParams prm) {
+    seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
+                     const __grid_constant__ CUtensorMap mdt, TcParams prm) {
     constexpr int ST = C::SEG_ST, NV = C::NV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE);
-    float *tot_s = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE + C::VEC_RING);  // [HB][cps]
+    uint8_t *dt_ring = smem + ST * C::SEG_STAGE + C::VEC_RING;
+    __shared__ uint64_t dt_bar[kDtAhead];
+    TRACE_DECL;
     __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], afull_bar[2], afree_bar[2];
     __shared__ uint64_t done_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
@@ -392,14 +560,21 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     __shared__ int last_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seg = blockIdx.x, hblk = blockIdx.y, b = blockIdx.z;
+    const int seg = blockIdx.z, hblk = blockIdx.x, b = blockIdx.y;
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
     const int c0 = seg * prm.cps;
     const int nch = min(prm.nc, c0 + prm.cps) - c0;
     const long long H = prm.H;
+    // the segment's chunks are taken last to first, so the decay of the
+    // chunks after each one (its weights' offset) accumulates as they come
+    auto chunk_of = [&](int it) { return c0 + nch - 1 - it; };
     auto stage_x = [&](int s) { return smem + s * C::SEG_STAGE; };
     auto stage_b = [&](int s) { return smem + s * C::SEG_STAGE + C::X_BYTES; };
+    // the chunk scan after this kernel may be scheduled at once: its first
+    // segment needs nothing from here
+    griddep_launch();
+    if (tid == 0) TRACE_CTA2(0);
     auto vec = [&](int v) { return vec_base + v * C::VEC_FLOATS; };
 
     if (warp == 1) {
@@ -421,56 +596,18 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         }
         mbar_init(&done_bar, 1);
         mbar_init(&drain_bar, 1);
+        for (int i = 0; i < kDtAhead; ++i) mbar_init(&dt_bar[i], 1);
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
         prefetch_tmap(&mb);
+        if (prm.dt_tma) prefetch_tmap(&mdt);
     }
+    TRACE_INIT();
     int nload[4] = {};  // TMA loads issued per stage (producer lane 0)
-    // chunk totals of dt*A over the segment: groups of 8 threads reduce one
-    // (head, chunk) pair each, in a fixed order (bitwise reproducible); the
-    // loop bound is the same for every lane of a warp, so the shuffles see
-    // a full warp
-    {
-        const int grp = tid >> 3, gl = tid & 7;
-        const int npair = C::HB * nch;
-        for (int j0 = (tid >> 5) * 4; j0 < npair; j0 += kSegThreads / 8) {
-            const int j = j0 + (grp & 3);
-            const bool valid = j < npair;
-            const int hh = valid ? j / nch : 0, k = valid ? j % nch : 0;
-            const long long h = h0 + hh;
-            float sum = 0.f;
-            if (valid && h < H && !prm.cum_in)
-#pragma unroll 4
-                for (int q = gl; q < C::Q; q += 8)
-                    sum += __bfloat162float(prm.dt[((long long)b * prm.L + (long long)(c0 + k) * C::Q + q) * H + h]);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if (valid && gl == 0) {
-                float tot = 0.f;
-                if (h < H)  // (with a given cumulative decay, A is not an input)
-                    tot = prm.cum_in ? prm.cum_in[(((long long)b * H + h) * prm.nc + c0 + k) * C::Q + C::Q - 1]
-                                     : sum * prm.A[h];
-                tot_s[hh * prm.cps + k] = tot;
-            }
-        }
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // suffix sums: tot_s[h][k] <- sum of the totals of the chunks after k
-    if (tid < C::HB) {
-        float run = 0.f;
-        for (int k = nch - 1; k >= 0; --k) {
-            const float t = tot_s[tid * prm.cps + k];
-            tot_s[tid * prm.cps + k] = run;
-            run += t;
-        }
-        const long long h = h0 + tid;
-        if (h < H && prm.seg_tot) prm.seg_tot[((long long)b * H + h) * prm.nseg + seg] = run;
-    }
-    __syncthreads();
     const uint32_t tmem = tmem_base_sh;
     constexpr uint32_t COL_A = C::N;
 
@@ -478,45 +615,57 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         // ---------------- TMA producer ----------------
         if (lane == 0)
             for (int it = 0; it < nch; ++it) {
-                const int s = it % ST;
+                const int s = it % ST, c = chunk_of(it);
                 if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
                 mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES + C::BC_BYTES);
-                issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c0 + it,
-                                     b);
+                issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c, b);
                 ++nload[s];
             }
     } else if (warp == 2) {
         // ---------------- segment weights ----------------
-        constexpr int PER = C::HB * C::Q / 32;
-        float dnext[PER];
-        fetch_dt<C>(prm, b, h0, c0, dnext);
+        //   w_s = exp(after + T - cum_s) dt_s, after = decay of the later chunks
+        constexpr int QPL = C::Q / 32;
+        float after[C::HB];
+#pragma unroll
+        for (int hh = 0; hh < C::HB; ++hh) after[hh] = 0.f;
+        DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
+        feed.start(prm, chunk_of);
         for (int it = 0; it < nch; ++it) {
-            const int v = it % NV;
+            const int v = it % NV, c = chunk_of(it);
+            ChunkDt<C> dt;
+            if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
+            float cum[C::HB][QPL], T[C::HB];
+            chunk_cums<C>(prm, b, h0, c, dt, cum, T);
+            float w[C::HB][QPL];
+#pragma unroll
+            for (int hh = 0; hh < C::HB; ++hh) {
+#pragma unroll
+                for (int j = 0; j < QPL; ++j) w[hh][j] = __expf(after[hh] + T[hh] - cum[hh][j]) * dt.d[hh][j];
+                after[hh] += T[hh];
+            }
             if (it >= NV) {
                 int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], free_parity(it, NV), &abort_sh) ? 1 : 0) : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
             float *vv = vec(v);
 #pragma unroll
-            for (int i = 0; i < PER; ++i) vv[C::V_DT + lane + 32 * i] = dnext[i];
-            __syncwarp();
-            if (it + 1 < nch) fetch_dt<C>(prm, b, h0, c0 + it + 1, dnext);
+            for (int hh = 0; hh < C::HB; ++hh)
 #pragma unroll
-            for (int hh = 0; hh < C::HB; ++hh) {
-                const long long h = h0 + hh;
-                const float a = (h < H && prm.A) ? prm.A[h] : 0.f;
-                float *cum = vv + C::V_CUM + hh * C::Q;
-                const float *dtv = vv + C::V_DT + hh * C::Q;
-                const float total = chunk_cum<C>(prm, b, h, c0 + it, dtv, a, cum);
-                const float after = tot_s[hh * prm.cps + it];
-                for (int q = lane; q < C::Q; q += 32)
-                    vv[C::V_AL + hh * C::Q + q] = __expf(after + total - cum[q]) * dtv[q];
-            }
+                for (int j = 0; j < QPL; ++j) vv[C::V_AL + hh * C::Q + QPL * lane + j] = w[hh][j];
             __syncwarp();
             if (lane == 0) {
                 TRACE(14, it);
                 mbar_arrive(&vfull_bar[v]);
             }
+        }
+        feed.drain();
+        // total dt*A of the segment, for the pass across segments
+        if (lane < C::HB && h0 + lane < H && prm.seg_tot) {
+            float t = after[0];
+#pragma unroll
+            for (int hh = 1; hh < C::HB; ++hh)
+                if (lane == hh) t = after[hh];
+            prm.seg_tot[((long long)b * H + h0 + lane) * prm.nseg + seg] = t;
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -527,13 +676,16 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 if (!wait_bounded(&afull_bar[a], fill_parity(it, 2), &abort_sh)) break;
                 if (!wait_bounded(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
                 tc_fence_after();
-                const uint32_t ta = tmem + COL_A + a * C::Q, b0 = smem_u32(stage_b(s));
+                // one descriptor per operand tile, advanced by constants (the
+                // single issuing thread must not spend cycles per MMA)
+                const uint32_t ta = tmem + COL_A + a * C::Q;
+                const uint64_t db = sdesc(smem_u32(stage_b(s)), C::Q * 128, 1024);
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem, ta + ks * 8, sdesc(b0 + ks * 2048, C::Q * 128, 1024), idesc, (it | ks) != 0);
+                    mma_bf16_ta(tmem, ta + ks * 8, desc_add(db, ks * 2048), idesc, (it | ks) != 0);
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem, ta + C::Q / 2 + ks * 8, sdesc(b0 + ks * 2048, C::Q * 128, 1024), idesc, true);
+                    mma_bf16_ta(tmem, ta + C::Q / 2 + ks * 8, desc_add(db, ks * 2048), idesc, true);
                 mma_commit(&empty_bar[s]);
                 mma_commit(&afree_bar[a]);
                 TRACE(16, it);
@@ -548,7 +700,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t pcol = (uint32_t)(rp % 64);
         const int blk = rh * C::PB + rp / 64;
-        uint32_t xw[16];
         for (int it = 0; it < nch; ++it) {
             const int s = it % ST, v = it % NV, a = it & 1;
             if (!group_wait(&full_bar[s], fill_parity(it, ST), &abort_sh, &slot[0], 1, gtid, 256)) break;
@@ -556,7 +707,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             if (it >= 2 && !group_wait(&afree_bar[a], free_parity(it, 2), &abort_sh, &slot[2], 1, gtid, 256)) break;
             tc_fence_after();
             build_a<C>(stage_x(s) + blk * (C::Q * 128), pcol, vec(v) + C::V_AL + rh * C::Q + half * 32, half,
-                       tmem + lane_off + COL_A + a * C::Q, xw);
+                       tmem + lane_off + COL_A + a * C::Q);
             tmem_st_wait();
             tc_fence_before();
             named_bar_sync(1, 256);
@@ -567,7 +718,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 mbar_arrive(&vempty_bar[v]);
             }
         }
-        (void)xw;
         // segment state: TMEM lane r = row (head, p); warps 4-7 columns
         // [0, N/2), warps 8-11 [N/2, N)
         const long long hrow = h0 + rh;
@@ -601,23 +751,49 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             named_bar_sync(1, 256);
             if (last_sh) {
                 __threadfence();
-                constexpr int ROW4 = C::N / 4;
-                for (int e = gtid; e < C::M * ROW4; e += 256) {
-                    const int r = e / ROW4, n4 = e % ROW4;
-                    const long long h = h0 + r / C::P;
-                    if (h >= H) continue;
-                    const long long off = (h * C::P + r % C::P) * C::N + 4 * n4;
-                    float4 acc = prm.init ? __ldg(reinterpret_cast<const float4 *>(prm.init + b * H * C::P * C::N + off))
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int k = 0; k < prm.nseg - 1; ++k) {
-                        float4 *p = reinterpret_cast<float4 *>(prm.seg_state + ((long long)b * prm.nseg + k) * H * C::P * C::N + off);
-                        const float4 loc = __ldcg(p);
-                        const float ex = expf(__ldcg(prm.seg_tot + ((long long)b * H + h) * prm.nseg + k));
-                        acc.x = fmaf(ex, acc.x, loc.x);
-                        acc.y = fmaf(ex, acc.y, loc.y);
-                        acc.z = fmaf(ex, acc.z, loc.z);
-                        acc.w = fmaf(ex, acc.w, loc.w);
-                        __stcg(p, acc);
+                // 4 elements (float4) per thread at a time, up to 4 segments'
+                // loads issued before any of their results is used
+                constexpr int ROW4 = C::N / 4, E = C::M * ROW4;
+                const long long sstride = H * C::P * C::N;
+                float *base = prm.seg_state + (long long)b * prm.nseg * sstride;
+                for (int e0 = 0; e0 < E; e0 += 4 * 256) {
+                    long long off[4];
+                    long long hh4[4];
+                    float4 acc[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int e = e0 + i * 256 + gtid;
+                        const int r = e / ROW4, n4 = e % ROW4;
+                        hh4[i] = e < E ? h0 + r / C::P : H;
+                        off[i] = (hh4[i] * C::P + r % C::P) * C::N + 4 * n4;
+                        acc[i] = (prm.init && hh4[i] < H)
+                                     ? __ldg(reinterpret_cast<const float4 *>(prm.init + b * sstride + off[i]))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    for (int k0 = 0; k0 < prm.nseg - 1; k0 += 4) {
+                        float4 loc[4][4];
+                        float ex[4][4];
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const bool ok = k0 + kk < prm.nseg - 1 && hh4[i] < H;
+                                loc[kk][i] = ok ? __ldcg(reinterpret_cast<const float4 *>(base + (k0 + kk) * sstride + off[i]))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                                ex[kk][i] = ok ? __ldcg(prm.seg_tot + ((long long)b * H + hh4[i]) * prm.nseg + k0 + kk) : 0.f;
+                            }
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                if (!(k0 + kk < prm.nseg - 1 && hh4[i] < H)) continue;
+                                const float x = expf(ex[kk][i]);
+                                acc[i].x = fmaf(x, acc[i].x, loc[kk][i].x);
+                                acc[i].y = fmaf(x, acc[i].y, loc[kk][i].y);
+                                acc[i].z = fmaf(x, acc[i].z, loc[kk][i].z);
+                                acc[i].w = fmaf(x, acc[i].w, loc[kk][i].w);
+                                __stcg(reinterpret_cast<float4 *>(base + (k0 + kk) * sstride + off[i]), acc[i]);
+                            }
                     }
                 }
             }
@@ -634,8 +810,13 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    TRACE_FLUSH();
     if (warp == 1) tmem_dealloc(tmem, C::SEG_TMEM);
     if (abort_sh && tid == 0) flag_timeout(prm.status);
+    // complete only after the C B^T grid before this one: a grid that waits
+    // for this one then sees those matrices too
+    griddep_wait();
+    if (tid == 0) TRACE_CTA2(1);
 }
 
 // Epilogue fix-up of a chunk whose decay range is too wide to scale (rare;
@@ -675,7 +856,7 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
 template <typename T>
 __device__ __forceinline__ void store_y(T *p, float v);
 template <>
-__device__ __forceinline__ void store_y<float>(float *p, float v) { __stcs(p, v); }
+__device__ __forceinline__ void store_y<float>(float *p, float v) { *p = v; }
 template <>
 __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
@@ -691,32 +872,37 @@ __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) { *p = __float2b
 //   warps 8-15 : A operand of the next chunk into TMEM; epilogue
 //                y = factor R + D x straight to HBM
 // ===========================================================================
-constexpr int kScanThreads = 512;
+constexpr int kScanThreads = 768;
 
 template <class C, typename YT>
 __global__ void __launch_bounds__(kScanThreads, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
-                      const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap mcb, TcParams prm) {
+                      const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap mcb,
+                      const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mdt, TcParams prm) {
     constexpr int ST = C::SCAN_ST, NV = C::NV, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SCAN_STAGE);
+    YT *ybuf = reinterpret_cast<YT *>(smem + ST * C::SCAN_STAGE + C::VEC_RING);
+    uint8_t *dt_ring = smem + ST * C::SCAN_STAGE + C::VEC_RING + C::Y_BYTES;
+    __shared__ uint64_t dt_bar[kDtAhead];
+    TRACE_DECL;
     __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV];
     __shared__ uint64_t afull_bar[NB], afree_bar[NB], rfull_bar[NB], rfree_bar[NB], sbfree_bar[NB];
-    __shared__ uint64_t rt_bar, sdone_bar, drain_bar;
+    __shared__ uint64_t rt_bar, sdone_bar, drain_bar, yfull_bar, yfree_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
-    __shared__ volatile int slot[8];
+    __shared__ volatile int slot[12];
     __shared__ volatile int wide_a[NB];
     __shared__ __align__(16) float ones_sh[32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seg = blockIdx.x, hblk = blockIdx.y, b = blockIdx.z;
+    const int seg = blockIdx.z, hblk = blockIdx.x, b = blockIdx.y;
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
     const int c0 = seg * prm.cps;
     const int nch = min(prm.nc, c0 + prm.cps) - c0;
-    const long long L = prm.L, H = prm.H;
+    const long long H = prm.H;
     auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
     auto stage_b = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES; };
     auto stage_c = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + C::BC_BYTES; };
@@ -746,14 +932,20 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mbar_init(&rt_bar, 1);
         mbar_init(&sdone_bar, 1);
         mbar_init(&drain_bar, 1);
+        mbar_init(&yfull_bar, 1);
+        mbar_init(&yfree_bar, 1);
+        for (int i = 0; i < kDtAhead; ++i) mbar_init(&dt_bar[i], 1);
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
         prefetch_tmap(&mb);
         prefetch_tmap(&mc);
         prefetch_tmap(&mcb);
+        prefetch_tmap(&my);
+        if (prm.dt_tma) prefetch_tmap(&mdt);
     }
     if (tid < 32) ones_sh[tid] = 1.f;
+    TRACE_INIT();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -772,82 +964,98 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             for (int it = 0; it < nch; ++it) {
                 const int s = it % ST;
                 if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
+                const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
+                if (!wait_flag(prm.cb_ready + plane, &abort_sh)) break;
                 mbar_arrive_expect_tx(&full_bar[s], C::SCAN_STAGE);
                 issue_chunk_loads<C>(stage_x(s), stage_b(s), stage_c(s), &full_bar[s], &mx, &mb, &mc, h0, g, c0 + it,
                                      b);
-                tma_load_3d(stage_cb(s), &mcb, &full_bar[s], 0, 0, (int)((((long long)b * prm.nc) + c0 + it) * prm.G + g));
+                tma_load_3d(stage_cb(s), &mcb, &full_bar[s], 0, 0, (int)plane);
                 ++nload[s];
                 TRACE(0, it);
             }
     } else if (warp == 2) {
         // ---------------- per-chunk vectors (run up to NV chunks ahead) ----------------
-        constexpr int PER = C::HB * C::Q / 32;
-        float dnext[PER];
+        constexpr int QPL = C::Q / 32;
         float rho[C::HB];
 #pragma unroll
         for (int hh = 0; hh < C::HB; ++hh) rho[hh] = 0.f;
-        fetch_dt<C>(prm, b, h0, c0, dnext);
+        auto chunk_of = [&](int it) { return c0 + it; };
+        DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
+        feed.start(prm, chunk_of);
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV;
+            ChunkDt<C> dt;
+            if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
+            float cum[C::HB][QPL], T[C::HB];
+            chunk_cums<C>(prm, b, h0, c0 + it, dt, cum, T);
+            // range [lo, hi] of the cumulative decay over the chunk and its start (0)
+            int klo[C::HB], khi[C::HB];
+#pragma unroll
+            for (int hh = 0; hh < C::HB; ++hh) {
+                float lo = 0.f, hi = 0.f;
+#pragma unroll
+                for (int j = 0; j < QPL; ++j) {
+                    lo = fminf(lo, cum[hh][j]);
+                    hi = fmaxf(hi, cum[hh][j]);
+                }
+                klo[hh] = __reduce_min_sync(0xffffffffu, fkey(lo));
+                khi[hh] = __reduce_max_sync(0xffffffffu, fkey(hi));
+            }
+            bool rescale = false, wide = false;
+            float al[C::HB][QPL], ef[C::HB][QPL], f[C::HB], sbf[C::HB], rn[C::HB];
+#pragma unroll
+            for (int hh = 0; hh < C::HB; ++hh) {
+                const float lo = unkey(klo[hh]), hi = unkey(khi[hh]);
+                // rho stays while every exponent rho - cum_s stays within kLambda;
+                // else it moves to the middle of the chunk's range; a range wider
+                // than 2 kLambda centres the state at the chunk's end and leaves
+                // the intra-chunk term to the direct path
+                float rc = rho[hh];
+                f[hh] = 1.f;
+                sbf[hh] = 1.f;
+                bool hw = false;
+                if (rho[hh] - lo > kLambda || hi - rho[hh] > kLambda) {
+                    rescale = true;
+                    if (hi - lo <= 2.f * kLambda) {
+                        rc = 0.5f * (lo + hi);
+                        f[hh] = __expf(rc - rho[hh]);
+                        sbf[hh] = f[hh];
+                    } else {
+                        hw = true;
+                        rc = T[hh];
+                        f[hh] = __expf(T[hh] - rho[hh]);
+                        sbf[hh] = __expf(-rho[hh]);
+                    }
+                }
+                wide |= hw;
+#pragma unroll
+                for (int j = 0; j < QPL; ++j) {
+                    al[hh][j] = __expf(rc - cum[hh][j]) * dt.d[hh][j];
+                    ef[hh][j] = __expf(hw ? cum[hh][j] : cum[hh][j] - rc);
+                }
+                rn[hh] = rc - T[hh];
+                rho[hh] = rn[hh];
+            }
             if (it >= NV) {
                 int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], free_parity(it, NV), &abort_sh) ? 1 : 0) : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
             float *vv = vec(v);
 #pragma unroll
-            for (int i = 0; i < PER; ++i) vv[C::V_DT + lane + 32 * i] = dnext[i];
-            __syncwarp();
-            if (it + 1 < nch) fetch_dt<C>(prm, b, h0, c0 + it + 1, dnext);  // in flight while this chunk's vectors are computed
-            bool rescale = false, wide = false;
-#pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
-                const long long h = h0 + hh;
-                const float a = (h < H && prm.A) ? prm.A[h] : 0.f;
-                float *cum = vv + C::V_CUM + hh * C::Q;
-                const float *dtv = vv + C::V_DT + hh * C::Q;
-                const float T = chunk_cum<C>(prm, b, h, c0 + it, dtv, a, cum);
-                // range [lo, hi] of the cumulative decay over the chunk and its start (0)
-                float lo = 0.f, hi = 0.f;
-                for (int q = lane; q < C::Q; q += 32) {
-                    lo = fminf(lo, cum[q]);
-                    hi = fmaxf(hi, cum[q]);
-                }
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-                    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, off));
-                }
-                // rho stays while every exponent rho - cum_s stays within kLambda;
-                // else it moves to the middle of the chunk's range; a range wider
-                // than 2 kLambda centres the state at the chunk's end and leaves
-                // the intra-chunk term to the direct path
-                float rc = rho[hh], f = 1.f, sbf = 1.f;
-                bool hw = false;
-                if (rho[hh] - lo > kLambda || hi - rho[hh] > kLambda) {
-                    rescale = true;
-                    if (hi - lo <= 2.f * kLambda) {
-                        rc = 0.5f * (lo + hi);
-                        f = __expf(rc - rho[hh]);
-                        sbf = f;
-                    } else {
-                        hw = true;
-                        rc = T;
-                        f = __expf(T - rho[hh]);
-                        sbf = __expf(-rho[hh]);
-                    }
-                }
-                wide |= hw;
-                for (int q = lane; q < C::Q; q += 32) {
-                    const float cq = cum[q];
-                    vv[C::V_AL + hh * C::Q + q] = __expf(rc - cq) * dtv[q];
-                    vv[C::V_EF + hh * C::Q + q] = __expf(hw ? cq : cq - rc);
+                for (int j = 0; j < QPL; ++j) {
+                    const int q = hh * C::Q + QPL * lane + j;
+                    vv[C::V_DT + q] = dt.d[hh][j];
+                    vv[C::V_CUM + q] = cum[hh][j];
+                    vv[C::V_AL + q] = al[hh][j];
+                    vv[C::V_EF + q] = ef[hh][j];
                 }
                 if (lane == 0) {
-                    vv[C::V_F + hh] = f;
-                    vv[C::V_SBF + hh] = sbf;
-                    vv[C::V_RHON + hh] = rc - T;
+                    vv[C::V_F + hh] = f[hh];
+                    vv[C::V_SBF + hh] = sbf[hh];
+                    vv[C::V_RHON + hh] = rn[hh];
                 }
-                rho[hh] = rc - T;
             }
             if (lane == 0) {
                 vv[C::V_FLAG] = rescale ? 1.f : 0.f;
@@ -859,6 +1067,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 mbar_arrive(&vfull_bar[v]);
             }
         }
+        feed.drain();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
@@ -867,7 +1076,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             const uint32_t id_inter = idesc_bf16(C::M, C::Q, false, false);
             for (int it = 0; it < nch; ++it) {
                 const int s = it % ST, a = it % NB;
-                const uint32_t sb_ = smem_u32(stage_b(s)), sc = smem_u32(stage_c(s)), scb = smem_u32(stage_cb(s));
+                // one descriptor per operand tile, advanced by constants (the
+                // single issuing thread must not spend cycles per MMA)
+                const uint64_t dcb = sdesc(smem_u32(stage_cb(s)), 16, 1024);
+                const uint64_t db = sdesc(smem_u32(stage_b(s)), C::Q * 128, 1024);
+                const uint64_t dc = sdesc(smem_u32(stage_c(s)), 16, 1024);
                 const uint32_t ta = tmem + C::COL_A + a * C::Q, tr = tmem + C::COL_R + a * C::Q;
                 const uint32_t tsb = tmem + C::COL_SB + a * (C::N / 2);
                 if (!wait_bounded(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
@@ -879,10 +1092,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 if (!wide) {
 #pragma unroll
                     for (int ks = 0; ks < C::Q / 16; ++ks)
-                        mma_bf16_ta(tr, ta + ks * 8, sdesc(scb + ks * 32, 16, 1024), id_intra, ks > 0);
+                        mma_bf16_ta(tr, ta + ks * 8, desc_add(dcb, ks * 32), id_intra, ks > 0);
 #pragma unroll
                     for (int ks = 0; ks < C::Q / 16; ++ks)
-                        mma_bf16_ta(tr, ta + C::Q / 2 + ks * 8, sdesc(scb + ks * 32, 16, 1024), id_intra, true);
+                        mma_bf16_ta(tr, ta + C::Q / 2 + ks * 8, desc_add(dcb, ks * 32), id_intra, true);
                 }
                 TRACE(2, it);
                 // Ss += A^T B: once the state warps have read (and rescaled) Ss
@@ -891,25 +1104,42 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 8, sdesc(sb_ + ks * 2048, C::Q * 128, 1024), id_state, true);
+                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 8, desc_add(db, ks * 2048), id_state, true);
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + C::Q / 2 + ks * 8, sdesc(sb_ + ks * 2048, C::Q * 128, 1024),
-                                id_state, true);
+                    mma_bf16_ta(tmem + C::COL_S, ta + C::Q / 2 + ks * 8, desc_add(db, ks * 2048), id_state, true);
                 mma_commit(&sdone_bar);
                 mma_commit(&afree_bar[a]);
                 TRACE(3, it);
                 // R += SB C^T
 #pragma unroll
-                for (int ks = 0; ks < C::N / 16; ++ks) {
-                    const uint32_t boff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                    mma_bf16_ta(tr, tsb + ks * 8, sdesc(sc + boff, 16, 1024), id_inter, !wide || ks > 0);
-                }
+                for (int ks = 0; ks < C::N / 16; ++ks)
+                    mma_bf16_ta(tr, tsb + ks * 8, desc_add(dc, (ks / 4) * (C::Q * 128) + (ks % 4) * 32), id_inter,
+                                !wide || ks > 0);
                 mma_commit(&rfull_bar[a]);
                 mma_commit(&sbfree_bar[a]);
                 mma_commit(&empty_bar[s]);
                 TRACE(4, it);
             }
+        }
+    } else if (warp == 3) {
+        // ---------------- y tiles to HBM (TMA stores) ----------------
+        if (lane == 0) {
+            for (int it = 0; it < nch; ++it) {
+                if (!wait_bounded(&yfull_bar, (uint32_t)(it & 1), &abort_sh)) break;
+                // rows of heads past H are clipped by the map
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int bk = 0; bk < C::M / 64; ++bk)
+                        tma_store_4d(&my, ybuf + ((hf * (C::M / 64) + bk) * (C::Q / 2)) * 64, (bk % C::PB) * 64,
+                                     h0 + bk / C::PB, (c0 + it) * C::Q + hf * (C::Q / 2), b);
+                bulk_commit_group();
+                bulk_wait_read_all();  // the tile has left shared memory
+                TRACE(11, it);
+                mbar_arrive(&yfree_bar);
+            }
+            bulk_wait_all();
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- state: rescale and bf16 copy ----------------
@@ -917,6 +1147,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const long long hrow = h0 + rh;
         // state entering the segment (rho = 0: Ss = S_in)
+        if (prm.dep_seg && seg > 0) griddep_wait();
         {
             const float *src = nullptr;
             if (prm.entering)
@@ -961,10 +1192,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 tmem_ld16(tmem + lane_off + C::COL_S + n0 + 16, v1);
                 tmem_ld_wait();
                 uint32_t w[16];
+                if (sbf == 1.f) {  // (uniform per warp: one head per warp)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    w[j] = pack_bf16x2(v0[2 * j] * sbf, v0[2 * j + 1] * sbf);
-                    w[8 + j] = pack_bf16x2(v1[2 * j] * sbf, v1[2 * j + 1] * sbf);
+                    for (int j = 0; j < 8; ++j) {
+                        w[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
+                        w[8 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        w[j] = pack_bf16x2(v0[2 * j] * sbf, v0[2 * j + 1] * sbf);
+                        w[8 + j] = pack_bf16x2(v1[2 * j] * sbf, v1[2 * j + 1] * sbf);
+                    }
                 }
                 tmem_st16u(tmem + lane_off + C::COL_SB + sb * (C::N / 2) + n0 / 2, w);
                 if (rescale) {
@@ -1005,30 +1244,23 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 }
             }
         }
-    } else if (warp >= 8) {
-        // ---------------- A operand of the next chunk; epilogue of this one ----------------
-        // thread = row (head, p), half = which 32 of the Q steps
+    } else if (warp >= 8 && warp < 16) {
+        // ---------------- A operand: thread = row (head, p), half of the Q steps ----------------
         const int gtid = tid - 256;
         const int half = (warp - 8) >> 2;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
-        const long long hrow = h0 + rh;
-        const bool live = hrow < H;
-        const float dh = (prm.D && live) ? prm.D[hrow] : 0.f;
         const uint32_t pcol = (uint32_t)(rp % 64);
         const int blk = rh * C::PB + rp / 64;
-        const long long ystride = H * C::P;
-        uint32_t xcur[16], xnext[16];
-        auto build = [&](int c, uint32_t(&xw)[16]) -> bool {
+        for (int c = 0; c < nch; ++c) {
             const int s = c % ST, v = c % NV, a = c % NB;
-            if (!group_wait(&full_bar[s], fill_parity(c, ST), &abort_sh, &slot[4], 2, gtid, 256)) return false;
-            if (!group_wait(&vfull_bar[v], fill_parity(c, NV), &abort_sh, &slot[5], 2, gtid, 256)) return false;
-            if (c >= NB && !group_wait(&afree_bar[a], free_parity(c, NB), &abort_sh, &slot[6], 2, gtid, 256))
-                return false;
+            if (!group_wait(&full_bar[s], fill_parity(c, ST), &abort_sh, &slot[4], 2, gtid, 256)) break;
+            if (!group_wait(&vfull_bar[v], fill_parity(c, NV), &abort_sh, &slot[5], 2, gtid, 256)) break;
+            if (c >= NB && !group_wait(&afree_bar[a], free_parity(c, NB), &abort_sh, &slot[6], 2, gtid, 256)) break;
             if (gtid == 0) TRACE(5, c);
             tc_fence_after();
             const float *vv = vec(v);
             build_a<C>(stage_x(s) + blk * (C::Q * 128), pcol, vv + C::V_AL + rh * C::Q + half * 32, half,
-                       tmem + lane_off + C::COL_A + a * C::Q, xw);
+                       tmem + lane_off + C::COL_A + a * C::Q);
             const bool wide = vv[C::V_FLAG + 1] != 0.f;
             tmem_st_wait();
             tc_fence_before();
@@ -1039,11 +1271,29 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 mbar_arrive(&afull_bar[a]);
                 if (!wide) mbar_arrive(&empty_bar[s]);  // (a wide chunk's epilogue still reads the stage)
             }
-            return true;
+        }
+    } else if (warp >= 16) {
+        // ---------------- epilogue: y = factor R + D x, thread = row (head, p), half of the steps ----------------
+        const int gtid = tid - 512;
+        const int half = (warp - 16) >> 2;
+        const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
+        const long long hrow = h0 + rh;
+        const bool live = hrow < H;
+        const float dh = (prm.D && live) ? prm.D[hrow] : 0.f;
+        const uint32_t pcol = (uint32_t)(rp % 64);
+        const int blk = rh * C::PB + rp / 64;
+        const long long xstride = H * C::P;
+        auto xrow = [&](int c) {
+            return prm.x + (((long long)b * prm.L + (long long)(c0 + c) * C::Q + half * 32) * H + (live ? hrow : 0)) *
+                               C::P + rp;
         };
-        auto epilogue = [&](int c, const uint32_t(&xw)[16]) -> bool {
+        uint32_t xp[16];
+        if (nch > 0) fetch_x_half(xrow(0), xstride, live, xp);
+        // this thread's column of the y tile [half][blk][Q/2][64]
+        YT *yrow = ybuf + ((half * (C::M / 64) + blk) * (C::Q / 2)) * 64 + pcol;
+        for (int c = 0; c < nch; ++c) {
             const int s = c % ST, v = c % NV, r = c % NB;
-            if (!group_wait(&rfull_bar[r], fill_parity(c, NB), &abort_sh, &slot[7], 2, gtid, 256)) return false;
+            if (!group_wait(&rfull_bar[r], fill_parity(c, NB), &abort_sh, &slot[7], 3, gtid, 256)) break;
             if (gtid == 0) TRACE(9, c);
             tc_fence_after();
             const float *vv = vec(v);
@@ -1059,37 +1309,28 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             tmem_ld16(tr, *reinterpret_cast<float(*)[16]>(acc));
             tmem_ld16(tr + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
             tmem_ld_wait();
-            if (live) {
-                YT *yp = reinterpret_cast<YT *>(prm.y) +
-                         (((long long)b * L + (long long)(c0 + c) * C::Q + half * 32) * H + hrow) * C::P + rp;
+            // the previous chunk's y tile has left shared memory
+            if (c > 0 && !group_wait(&yfree_bar, (uint32_t)((c - 1) & 1), &abort_sh, &slot[8], 3, gtid, 256)) break;
 #pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
-                    const uint32_t w0 = xw[j / 2], w1 = xw[j / 2 + 1];
-                    store_y<YT>(yp + (long long)j * ystride, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
-                    store_y<YT>(yp + (long long)(j + 1) * ystride,
-                                fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
-                    store_y<YT>(yp + (long long)(j + 2) * ystride, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
-                    store_y<YT>(yp + (long long)(j + 3) * ystride,
-                                fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
-                }
+            for (int j = 0; j < 32; j += 4) {
+                const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
+                const uint32_t w0 = xp[j / 2], w1 = xp[j / 2 + 1];
+                store_y<YT>(yrow + j * 64, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
+                store_y<YT>(yrow + (j + 1) * 64, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
+                store_y<YT>(yrow + (j + 2) * 64, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
+                store_y<YT>(yrow + (j + 3) * 64, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
             }
+            fence_async_smem();
             tc_fence_before();
-            named_bar_sync(2, 256);
+            named_bar_sync(3, 256);
             if (gtid == 0) {
                 TRACE(10, c);
                 mbar_arrive(&rfree_bar[r]);
                 mbar_arrive(&vempty_bar[v]);
                 if (wide) mbar_arrive(&empty_bar[s]);
+                mbar_arrive(&yfull_bar);
             }
-            return true;
-        };
-        bool ok = nch > 0 ? build(0, xcur) : true;
-        for (int it = 0; ok && it < nch; ++it) {
-            if (it + 1 < nch && !build(it + 1, xnext)) break;
-            if (!epilogue(it, xcur)) break;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xcur[j] = xnext[j];
+            if (c + 1 < nch) fetch_x_half(xrow(c + 1), xstride, live, xp);  // in flight until the next chunk
         }
     }
     // let this CTA's own copies and MMAs land (they normally have) before
@@ -1103,6 +1344,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    TRACE_FLUSH();
     if (abort_sh && tid == 0) flag_timeout(prm.status);
     if (tid == 0) TRACE_CTA(1);
     if (warp == 1) tmem_dealloc(tmem, 512);
@@ -1152,6 +1394,36 @@ bool make_cb_map(CUtensorMap *m, const void *base, uint64_t Q, uint64_t planes) 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map of y [b][L][H][P] (fp32 or bf16) for TMA stores, box (64, 1, T,
+// 1), no swizzle (the staged tile is plain row-major).
+bool make_y_map(CUtensorMap *m, const void *base, bool f32, uint64_t P, uint64_t H, uint64_t L, uint64_t b,
+                uint32_t T) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const uint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[4] = {P, H, L, b};
+    cuuint64_t strides[3] = {P * es, P * H * es, P * H * L * es};
+    cuuint32_t box[4] = {64, 1, T, 1};
+    cuuint32_t el[4] = {1, 1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base),
+               dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map of dt [b][L][H] (bf16), box (8 heads, Q steps, 1); needs the row
+// stride H * 2 bytes to be a multiple of 16 (H % 8 == 0).
+bool make_dt_map(CUtensorMap *m, const void *base, uint64_t H, uint64_t L, uint64_t b, uint32_t Q) {
+    auto enc = get_encode();
+    if (!enc || H % 8 != 0) return false;
+    cuuint64_t dims[3] = {H, L, b};
+    cuuint64_t strides[2] = {H * 2, H * L * 2};
+    cuuint32_t box[3] = {8, Q, 1};
+    cuuint32_t el[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, el,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Plan {
     int nseg, cps, nhb;
 };
@@ -1176,13 +1448,21 @@ size_t cb_bytes(const Dims &d) { return align256(sizeof(bf16) * d.b * d.nc * d.G
 // Workspace: status word and segment counters | CB matrices | segment
 // states | segment totals.  The header is cleared on the stream by every
 // call.
+size_t flag_bytes(const Dims &d) { return align256(sizeof(unsigned) * d.b * d.nc * d.G); }
+
+// header: status word | segment counters [b, nhb] | C B^T ready flags [b, nc, G]
+template <class C>
+size_t counter_bytes(const Dims &d) {
+    return align256(sizeof(unsigned) * d.b * ((d.H + C::HB - 1) / C::HB));
+}
+
 template <class C>
 size_t header_bytes(const Dims &d) {
-    return 256 + align256(sizeof(unsigned) * d.b * ((d.H + C::HB - 1) / C::HB));
+    return 256 + counter_bytes<C>(d) + flag_bytes(d);
 }
 
 #ifdef SSD_TRACE
-constexpr size_t kTraceBytes = (32 * 256 + 2048) * sizeof(long long);
+constexpr size_t kTraceBytes = (32 * 256 + 4096) * sizeof(long long);
 #endif
 
 template <class C>
@@ -1197,6 +1477,25 @@ size_t workspace_for(const Dims &d) {
     return bytes;
 }
 
+// Launch with (pdl) or without a programmatic dependency on the previous
+// work of the stream.  The first launch of an entry point never has one, so
+// it waits for everything before it on the stream as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, int threads, int smem, cudaStream_t s, bool pdl,
+                     Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <class C>
 cudaError_t raise_smem(const void *fn, int bytes, int &done) {
     if (done >= bytes) return cudaSuccess;
@@ -1206,7 +1505,8 @@ cudaError_t raise_smem(const void *fn, int bytes, int &done) {
 }
 
 template <class C>
-cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, bf16 *cbm, unsigned *status, cudaStream_t s) {
+cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, bf16 *cbm, unsigned *ready, unsigned *status,
+                      cudaStream_t s) {
     CUtensorMap mb, mc;
     if (!make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
@@ -1214,48 +1514,48 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, bf16 *cbm, u
     cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::SMEM_CB, attr);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)d.nc, (unsigned)d.G, (unsigned)d.b);
-    cb_mask_kernel<C><<<grid, 128, C::SMEM_CB, s>>>(mb, mc, cbm, (int)d.nc, (int)d.G, status);
-    e = cudaGetLastError();
+    e = launch_k(cb_mask_kernel<C>, grid, 128, C::SMEM_CB, s, false, mb, mc, cbm, (int)d.nc, (int)d.G, ready, status);
     timing_mark(s, "cb_mask_tc");
     return e;
 }
 
 template <class C>
-cudaError_t launch_scan(const Dims &d, const TcParams &prm, ssd_dtype_t ydtype, const void *x, const void *B,
+cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, const void *B,
                         const void *Cm, const bf16 *cbm, dim3 grid, const char *name, cudaStream_t s) {
-    CUtensorMap mx, mb, mc, mcb;
+    CUtensorMap mx, mb, mc, mcb, my, mdt = {};
+    prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
+    const bool f32 = ydtype == SSD_DTYPE_F32;
     if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) ||
-        !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q) || !make_cb_map(&mcb, cbm, C::Q, d.b * d.nc * d.G))
+        !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q) || !make_cb_map(&mcb, cbm, C::Q, d.b * d.nc * d.G) ||
+        !make_y_map(&my, prm.y, f32, d.P, d.H, d.L, d.b, C::Q / 2))
         return cudaErrorInvalidValue;
     static int attr_f = 0, attr_b = 0;
     cudaError_t e;
-    if (ydtype == SSD_DTYPE_F32) {
+    if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        chunk_scan_kernel<C, float><<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, mcb, prm);
+        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mb, mc, mcb, my, mdt, prm);
     } else {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        chunk_scan_kernel<C, bf16><<<grid, kScanThreads, C::SMEM_SCAN, s>>>(mx, mb, mc, mcb, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mb, mc, mcb, my, mdt, prm);
     }
-    e = cudaGetLastError();
     timing_mark(s, name);
     return e;
 }
 
 template <class C>
-cudaError_t launch_seg_state(const Dims &d, const TcParams &prm, const void *x, const void *B, dim3 grid,
-                             const char *name, cudaStream_t s) {
-    CUtensorMap mx, mb;
+cudaError_t launch_seg_state(const Dims &d, TcParams prm, const void *x, const void *B, dim3 grid,
+                             const char *name, bool pdl, cudaStream_t s) {
+    CUtensorMap mx, mb, mdt = {};
     if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
-    const int smem = C::SMEM_SEG_BASE + (int)(C::HB * prm.cps * sizeof(float));
-    if (smem > kSmemLimit) return cudaErrorInvalidValue;
+    prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
+    const int smem = C::SMEM_SEG;
     static int attr = 0;
     cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(seg_state_kernel<C>), smem, attr);
     if (e != cudaSuccess) return e;
-    seg_state_kernel<C><<<grid, kSegThreads, smem, s>>>(mx, mb, prm);
-    e = cudaGetLastError();
+    e = launch_k(seg_state_kernel<C>, grid, kSegThreads, smem, s, pdl, mx, mb, mdt, prm);
     timing_mark(s, name);
     return e;
 }
@@ -1278,6 +1578,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
                     cudaStream_t s) {
     const Plan p = plan_for<C>(d);
     TcParams prm = base_params(d, dt);
+    prm.x = static_cast<const bf16 *>(x);
     prm.A = A;
     prm.D = D;
     prm.init = init;
@@ -1287,6 +1588,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     const size_t hdr = header_bytes<C>(d);
     prm.status = reinterpret_cast<unsigned *>(w);
     prm.counters = reinterpret_cast<unsigned *>(w + 256);
+    prm.cb_ready = reinterpret_cast<unsigned *>(w + 256 + counter_bytes<C>(d));
     bf16 *cbm = reinterpret_cast<bf16 *>(w + hdr);
     const size_t seg_off = hdr + cb_bytes(d);
     if (p.nseg > 1) {
@@ -1303,13 +1605,16 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     cudaError_t e = cudaMemsetAsync(w, 0, hdr, s);
     if (e != cudaSuccess) return e;
     timing_begin(s);
-    e = launch_cb<C>(d, B, Cm, cbm, prm.status, s);
+    e = launch_cb<C>(d, B, Cm, cbm, prm.cb_ready, prm.status, s);
     if (e != cudaSuccess) return e;
     if (p.nseg > 1) {
-        e = launch_seg_state<C>(d, prm, x, B, dim3(p.nseg - 1, p.nhb, (unsigned)d.b), "seg_state_tc", s);
+        e = launch_seg_state<C>(d, prm, x, B, dim3(p.nhb, (unsigned)d.b, p.nseg - 1), "seg_state_tc", true, s);
         if (e != cudaSuccess) return e;
+        prm.dep_seg = 1;
     }
-    return launch_scan<C>(d, prm, ydtype, x, B, Cm, cbm, dim3(p.nseg, p.nhb, (unsigned)d.b), "chunk_scan_tc", s);
+    // segments in the slowest grid dimension: the first segment's CTAs, which
+    // need nothing from the segment-state kernel, are scheduled first
+    return launch_scan<C>(d, prm, ydtype, x, B, Cm, cbm, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", s);
 }
 
 // Dispatch over the compiled tile configurations.
@@ -1335,7 +1640,7 @@ bool tc_fwd_supported(const Dims &d, ssd_dtype_t dtype) {
     bool ok = false;
     dispatch(d, [&](auto c) {
         using C = decltype(c);
-        ok = shape_ok<C>(d) && C::SMEM_SEG_BASE + (int)(C::HB * plan_for<C>(d).cps * sizeof(float)) <= kSmemLimit;
+        ok = shape_ok<C>(d) && C::SMEM_SEG <= kSmemLimit;
     });
     return ok;
 }
@@ -1359,7 +1664,7 @@ bool tc_stage_supported(const Dims &d, ssd_dtype_t dtype) {
     bool ok = false;
     dispatch(d, [&](auto c) {
         using C = decltype(c);
-        ok = shape_ok<C>(d) && C::SMEM_SEG_BASE + (int)(C::HB * sizeof(float)) <= kSmemLimit;
+        ok = shape_ok<C>(d) && C::SMEM_SEG <= kSmemLimit;
     });
     return ok;
 }
@@ -1376,8 +1681,8 @@ cudaError_t run_chunk_state(const Dims &d, const void *x, const void *dt, const 
     prm.cps = 1;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
     timing_begin(s);
-    return launch_seg_state<C>(d, prm, x, B, dim3((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b), "chunk_state_tc",
-                               s);
+    return launch_seg_state<C>(d, prm, x, B, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc), "chunk_state_tc",
+                               false, s);
 }
 
 // The CB matrices of a stage call live in stream-ordered scratch
@@ -1389,20 +1694,24 @@ cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, con
     TcParams prm = base_params(d, dt);
     prm.cum_in = cum;
     prm.entering = states_in;  // [b, nc, H, P, N]: the state entering each chunk
+    prm.x = static_cast<const bf16 *>(x);
     prm.D = D;
     prm.y = y;
     prm.nseg = (int)d.nc;
     prm.cps = 1;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
-    void *cbm = nullptr;
-    cudaError_t e = cudaMallocAsync(&cbm, cb_bytes(d), s);
+    char *scratch = nullptr;  // ready flags | C B^T matrices
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), flag_bytes(d) + cb_bytes(d), s);
     if (e != cudaSuccess) return e;
+    prm.cb_ready = reinterpret_cast<unsigned *>(scratch);
+    bf16 *cbm = reinterpret_cast<bf16 *>(scratch + flag_bytes(d));
+    e = cudaMemsetAsync(scratch, 0, flag_bytes(d), s);
     timing_begin(s);
-    e = launch_cb<C>(d, B, Cm, static_cast<bf16 *>(cbm), nullptr, s);
+    if (e == cudaSuccess) e = launch_cb<C>(d, B, Cm, cbm, prm.cb_ready, nullptr, s);
     if (e == cudaSuccess)
-        e = launch_scan<C>(d, prm, ydtype, x, B, Cm, static_cast<const bf16 *>(cbm),
-                           dim3((unsigned)d.nc, (unsigned)prm.nhb, (unsigned)d.b), "chunk_scan_stage_tc", s);
-    const cudaError_t e2 = cudaFreeAsync(cbm, s);
+        e = launch_scan<C>(d, prm, ydtype, x, B, Cm, cbm, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc),
+                           "chunk_scan_stage_tc", s);
+    const cudaError_t e2 = cudaFreeAsync(scratch, s);
     return e != cudaSuccess ? e : e2;
 }
 
