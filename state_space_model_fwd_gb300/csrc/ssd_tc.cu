@@ -75,6 +75,7 @@ struct TcParams {
     // the chunk scan's TMA producer polls the flag of a chunk before loading
     // its matrix (the C B^T grid is wholly resident or done by then)
     unsigned *cb_ready;
+    const uint8_t *pack;  // [b, nc, G] chunk packs (PACK_BYTES each)
     // launched with a programmatic dependency on the segment-state kernel:
     // the state warps of segments > 0 wait for it before reading the states
     // entering them
@@ -87,9 +88,13 @@ struct Cfg {
     static constexpr int HB = 128 / P;           // heads per CTA
     static constexpr int M = 128;                // rows (head, p)
     static constexpr int PB = P / 64;            // 64-wide column blocks of one head's x tile
-    static constexpr int X_BYTES = M * Q * 2;    // [M/64 blocks][Q rows][64]
+    static constexpr int X_BYTES = M * Q * 2;    // [Q steps][M/64 = 2 blocks (head, 64 p)][64], one TMA box
     static constexpr int BC_BYTES = N * Q * 2;   // [N/64 blocks][Q rows][64]
     static constexpr int CBM_BYTES = Q * Q * 2;  // [Q rows t][Q s]
+    // chunk pack, written by the C B^T kernel and read with one bulk copy:
+    // [CB (K-major, swizzled) | B tile | C tile], each in the shared-memory
+    // image the MMAs read
+    static constexpr int PACK_BYTES = CBM_BYTES + 2 * BC_BYTES;
     // vector set of one chunk (floats): per head [Q] arrays dt, cum, a-factor,
     // epilogue factor; then per head the state rescale factor, the factor of
     // the bf16 state copy, rho after the chunk; then two block flags
@@ -98,14 +103,14 @@ struct Cfg {
     static constexpr int V_F = 4 * HB * Q, V_SBF = V_F + HB, V_RHON = V_SBF + HB, V_FLAG = V_RHON + HB;
     static constexpr int VEC_FLOATS = 4 * HB * Q + 32;
     static constexpr int NV = 4;  // vector sets in flight
-    static constexpr int DT_BYTES = 8 * Q * 2;  // dt of 8 heads (one 16-byte box row) x Q steps, one TMA box
-    static constexpr int DT_RING = 4 * DT_BYTES;  // kDtAhead boxes
+    static constexpr int DT_BOX = 8 * 4 * Q * 2;  // dt of 8 heads (one 16-byte box row) x 4 chunks, one TMA box
+    static constexpr int DT_RING = 2 * DT_BOX;
     static constexpr int VEC_RING = ((NV * VEC_FLOATS * 4 + 1023) / 1024) * 1024;
 
     // scan kernel: TMA stages of (x, B, C, CB), the vector ring, and the y
     // tile of one chunk ([half][M/64 blocks][Q/2 steps][64], fp32 or bf16)
     // that the TMA stores to HBM
-    static constexpr int SCAN_STAGE = X_BYTES + 2 * BC_BYTES + CBM_BYTES;
+    static constexpr int SCAN_STAGE = X_BYTES + PACK_BYTES;
     static constexpr int Y_BYTES = M * Q * 4;
     static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + Y_BYTES + DT_RING + 1024; }
     static constexpr int SCAN_ST = scan_smem(4) <= kSmemLimit ? 4 : (scan_smem(3) <= kSmemLimit ? 3 : 2);
@@ -122,12 +127,13 @@ struct Cfg {
     static constexpr int seg_smem(int st) { return st * SEG_STAGE + VEC_RING + DT_RING + 1024; }
     static constexpr int SEG_ST = seg_smem(4) <= kSmemLimit ? 4 : (seg_smem(3) <= kSmemLimit ? 3 : 2);
     static constexpr int SMEM_SEG = seg_smem(SEG_ST);
-    static constexpr int SEG_COLS = N + 2 * Q;  // S [N] | A hi+lo [Q] x 2
+    static constexpr int SEG_NA = N + 3 * Q <= 512 ? 3 : 2;  // A buffers of the segment-state kernel
+    static constexpr int SEG_COLS = N + SEG_NA * Q;           // S [N] | A hi+lo [Q] x SEG_NA
     static constexpr uint32_t SEG_TMEM =
         SEG_COLS <= 64 ? 64 : SEG_COLS <= 128 ? 128 : SEG_COLS <= 256 ? 256 : 512;
 
-    // C B^T kernel: C and B tiles of one chunk
-    static constexpr int SMEM_CB = 2 * BC_BYTES + 1024;
+    // C B^T kernel: the chunk pack
+    static constexpr int SMEM_CB = PACK_BYTES + 1024;
 };
 
 // Event trace (SSD_TRACE builds): clock64() of role events of CTA (0, 0, 0),
@@ -242,7 +248,6 @@ __device__ __forceinline__ uint32_t free_parity(int it, int n) { return (uint32_
 
 // Per-chunk vectors are computed by one warp with everything in registers:
 // lane l holds steps q = QPL l .. QPL l + QPL - 1 of every head of the CTA.
-constexpr int kDtAhead = 4;  // chunks of dt loads in flight ahead of use
 
 template <class C>
 struct ChunkDt {
@@ -265,29 +270,38 @@ __device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int
 }
 
 // dt of the chunks ahead for a vector warp.  With a TMA map, lane 0 keeps
-// kDtAhead boxes ([Q steps][8 heads] bf16) in flight in a private ring, so
-// no global load of the warp is outstanding when it arrives on a barrier
-// (an arrive waits for the arriving thread's earlier loads); without one
-// (H not a multiple of 8) each chunk's dt is loaded when needed.
+// two boxes of four chunks each ([4 Q steps][8 heads] bf16) in flight in a
+// private ring, so no global load of the warp is outstanding when it arrives
+// on a barrier (an arrive waits for the arriving thread's earlier loads), and
+// one TMA operation serves four chunks; without a map (H not a multiple of 8)
+// each chunk's dt is loaded when needed.
+constexpr int kDtGroup = 4;
+
 template <class C>
 struct DtFeed {
     uint8_t *ring;
-    uint64_t *bar;  // [kDtAhead], count 1
+    uint64_t *bar;  // [2], count 1
     const CUtensorMap *map;
     int b, h0, n;
-    int issued;  // boxes issued so far (step i's box went to slot i % kDtAhead)
-    __device__ __forceinline__ void issue(int k, int c) {
-        mbar_arrive_expect_tx(&bar[k], C::DT_BYTES);
-        tma_load_3d(ring + k * C::DT_BYTES, map, &bar[k], h0 & ~7, c * C::Q, b);
+    int issued;  // boxes issued so far (box i went to slot i % 2)
+    // first chunk of the box of steps 4 gi .. 4 gi + 3 (chunk_of is linear,
+    // increasing or decreasing; chunks past the segment are only read along)
+    template <class F>
+    __device__ __forceinline__ int box_start(int gi, F chunk_of) const {
+        return min(chunk_of(kDtGroup * gi), chunk_of(kDtGroup * gi + kDtGroup - 1));
+    }
+    template <class F>
+    __device__ __forceinline__ void issue(int gi, F chunk_of) {
+        const int k = gi & 1;
+        mbar_arrive_expect_tx(&bar[k], C::DT_BOX);
+        tma_load_3d(ring + k * C::DT_BOX, map, &bar[k], h0 & ~7, box_start(gi, chunk_of) * C::Q, b);
         ++issued;
     }
     template <class F>
     __device__ __forceinline__ void start(const TcParams &prm, F chunk_of) {
         issued = 0;
         if (prm.dt_tma && (threadIdx.x & 31) == 0)
-#pragma unroll
-            for (int k = 0; k < kDtAhead; ++k)
-                if (k < n) issue(k, chunk_of(k));
+            for (int gi = 0; gi < 2 && kDtGroup * gi < n; ++gi) issue(gi, chunk_of);
     }
     // dt of step `it` (chunk chunk_of(it)); false when the wait gave up
     template <class F>
@@ -298,21 +312,26 @@ struct DtFeed {
             fetch_dt<C>(prm, b, h0, chunk_of(it), o);
             return true;
         }
-        const int k = it % kDtAhead;
-        int ok = lane == 0 ? (wait_bounded(&bar[k], (uint32_t)((it / kDtAhead) & 1), abort_flag) ? 1 : 0) : 0;
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
-        const unsigned short *d16 = reinterpret_cast<const unsigned short *>(ring + k * C::DT_BYTES);
+        const int gi = it / kDtGroup, k = gi & 1;
+        if (it % kDtGroup == 0) {
+            int ok = lane == 0 ? (wait_bounded(&bar[k], (uint32_t)((gi >> 1) & 1), abort_flag) ? 1 : 0) : 0;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+        }
+        const int row0 = (chunk_of(it) - box_start(gi, chunk_of)) * C::Q;
+        const unsigned short *d16 = reinterpret_cast<const unsigned short *>(ring + k * C::DT_BOX);
 #pragma unroll
         for (int hh = 0; hh < C::HB; ++hh)
 #pragma unroll
             for (int j = 0; j < ChunkDt<C>::QPL; ++j)
                 o.d[hh][j] = h0 + hh < prm.H
-                                 ? __uint_as_float((uint32_t)d16[(ChunkDt<C>::QPL * lane + j) * 8 + (h0 & 7) + hh] << 16)
+                                 ? __uint_as_float(
+                                       (uint32_t)d16[(row0 + ChunkDt<C>::QPL * lane + j) * 8 + (h0 & 7) + hh] << 16)
                                  : 0.f;
         __syncwarp();
-        if (lane == 0 && it + kDtAhead < n) {
+        // the box is used up after its last step: refill its slot two boxes on
+        if ((it % kDtGroup == kDtGroup - 1 || it == n - 1) && lane == 0 && kDtGroup * (gi + 2) < n) {
             fence_async_smem();
-            issue(k, chunk_of(it + kDtAhead));
+            issue(gi + 2, chunk_of);
         }
         return true;
     }
@@ -320,8 +339,8 @@ struct DtFeed {
     __device__ __forceinline__ void drain() {
         if ((threadIdx.x & 31) == 0)
 #pragma unroll
-            for (int k = 0; k < kDtAhead; ++k) {
-                const int nk = issued > k ? (issued - k + kDtAhead - 1) / kDtAhead : 0;  // boxes slot k received
+            for (int k = 0; k < 2; ++k) {
+                const int nk = issued > k ? (issued - k + 1) / 2 : 0;  // boxes slot k received
                 if (nk > 0) mbar_wait(&bar[k], (uint32_t)((nk - 1) & 1), kDrainNs);
             }
     }
@@ -382,35 +401,44 @@ __device__ __forceinline__ int fkey(float f) {
 }
 __device__ __forceinline__ float unkey(int k) { return __int_as_float(k >= 0 ? k : k ^ 0x7FFFFFFF); }
 
-// Build this thread's half of the A operand of one chunk in TMEM:
-//   a_s = f_s x_s (s in [32 half, 32 half + 32)), split into bf16 hi and lo
-//   (hi = bf16(a), lo = bf16(a - hi): together about 2^-17 relative; a
-//   single bf16 rounding of a, 2^-9, shows in state entries that one recent
-//   token dominates).  Column j of the hi block holds s = 2j, 2j + 1; the lo
-//   block follows Q / 2 columns later.  The x values are returned packed
-//   (two bf16 per word) for the epilogue's D x term.
-template <class C>
-__device__ __forceinline__ void build_a(const uint8_t *xs_blk, uint32_t pcol, const float *f, int half,
+// Build this thread's part of the A operand of one chunk in TMEM:
+//   a_s = f_s x_s for the NS steps s in [NS part, NS part + NS), split into
+//   bf16 hi and lo (hi = bf16(a), lo = bf16(a - hi): together about 2^-17
+//   relative; a single bf16 rounding of a, 2^-9, shows in state entries that
+//   one recent token dominates).  Column j of the hi block holds s = 2j,
+//   2j + 1; the lo block follows Q / 2 columns later.
+template <class C, int NS>
+__device__ __forceinline__ void build_a(const uint8_t *xs, int blk, uint32_t pcol, const float *f, int part,
                                        uint32_t tmem_a) {
-    uint32_t hi[16], lo[16];
-    // byte offset of (row s, column pcol) is 128 s + sw[s % 8]: the 16-byte
-    // chunk of the column moves with the row's position in its 8-row atom
-    const uint8_t *sw[8];
+    static_assert(NS == 16 || NS == 32, "parts of 16 or 32 steps");
+    static_assert(C::M / 64 == 2, "two 64-wide column blocks per step");
+    uint32_t hi[NS / 2], lo[NS / 2];
+    // the x tile is [step s][block][64] in 128-byte lines (line 2 s + blk),
+    // 128-byte swizzled: the 16-byte chunk of column pcol sits at position
+    // chunk ^ (line % 8); with line % 8 = 2 (s % 4) + blk, the byte offset of
+    // (s, blk, pcol) is 256 s + sw[s % 4]
+    const uint8_t *sw[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) sw[k] = xs_blk + (((((pcol >> 3) ^ (uint32_t)k) & 7u) << 4) | ((pcol & 7u) << 1));
+    for (int k = 0; k < 4; ++k)
+        sw[k] = xs + blk * 128 + (((((pcol >> 3) ^ (uint32_t)(2 * k + blk)) & 7u) << 4) | ((pcol & 7u) << 1));
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int s0 = half * 32 + 2 * j;
-        const uint32_t x0 = *reinterpret_cast<const unsigned short *>(sw[s0 & 7] + s0 * 128);
-        const uint32_t x1 = *reinterpret_cast<const unsigned short *>(sw[(s0 + 1) & 7] + (s0 + 1) * 128);
+    for (int j = 0; j < NS / 2; ++j) {
+        const int s0 = part * NS + 2 * j;
+        const uint32_t x0 = *reinterpret_cast<const unsigned short *>(sw[s0 & 3] + s0 * 256);
+        const uint32_t x1 = *reinterpret_cast<const unsigned short *>(sw[(s0 + 1) & 3] + (s0 + 1) * 256);
         const float a0 = __uint_as_float(x0 << 16) * f[2 * j];
         const float a1 = __uint_as_float(x1 << 16) * f[2 * j + 1];
         const uint32_t h = pack_bf16x2(a0, a1);
         hi[j] = h;
         lo[j] = pack_bf16x2(a0 - __uint_as_float(h << 16), a1 - __uint_as_float(h & 0xFFFF0000u));
     }
-    tmem_st16u(tmem_a + half * 16, hi);
-    tmem_st16u(tmem_a + C::Q / 2 + half * 16, lo);
+    if constexpr (NS == 32) {
+        tmem_st16u(tmem_a + part * 16, hi);
+        tmem_st16u(tmem_a + C::Q / 2 + part * 16, lo);
+    } else {
+        tmem_st8u(tmem_a + part * 8, hi);
+        tmem_st8u(tmem_a + C::Q / 2 + part * 8, lo);
+    }
 }
 
 // x[t][p] of one (head, p) row for 32 consecutive steps, two bf16 per word,
@@ -430,11 +458,7 @@ template <class C>
 __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint8_t *cs, uint64_t *bar,
                                                   const CUtensorMap *mx, const CUtensorMap *mb,
                                                   const CUtensorMap *mc, int h0, int g, int c, int b) {
-#pragma unroll
-    for (int hh = 0; hh < C::HB; ++hh)
-#pragma unroll
-        for (int pb = 0; pb < C::PB; ++pb)
-            tma_load_4d(xs + (hh * C::PB + pb) * (C::Q * 128), mx, bar, pb * 64, h0 + hh, c * C::Q, b);
+    tma_load_5d(xs, mx, bar, 0, 0, h0, c * C::Q, b);  // x: [Q][HB][PB][64], 256 contiguous bytes per step
 #pragma unroll
     for (int nb = 0; nb < C::N / 64; ++nb) tma_load_4d(bs + nb * (C::Q * 128), mb, bar, nb * 64, g, c * C::Q, b);
     if (cs)
@@ -444,24 +468,28 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 }
 
 // ===========================================================================
-// CB[t, s] = C_t . B_s for s <= t (0 above the diagonal), bf16, one CTA per
-// (chunk, group, batch):  [b, nc, G, Q, Q].  M = Q = 64 tcgen05 contraction
-// over N; rows 16w .. 16w + 15 of the M = 64 accumulator sit in TMEM lanes
-// 32w .. 32w + 15.
+// Chunk packs, one CTA per (chunk, group, batch):
+//   CB[t, s] = C_t . B_s for s <= t (0 above the diagonal), bf16, by an
+//   M = Q = 64 tcgen05 contraction over N (rows 16w .. 16w + 15 of the M = 64
+//   accumulator sit in TMEM lanes 32w .. 32w + 15), stored K-major and
+//   swizzled, followed by the chunk's B and C tiles as the TMA delivered
+//   them: pack[(b, c, g)] = [CB | B | C], the shared-memory image the chunk
+//   scan's MMAs read, so that it arrives there with one bulk copy.
 // ===========================================================================
 template <class C>
 __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CUtensorMap mb,
-                                                      const __grid_constant__ CUtensorMap mc, bf16 *cbm, int nc,
+                                                      const __grid_constant__ CUtensorMap mc, uint8_t *pack, int nc,
                                                       int G, unsigned *ready, unsigned *status) {
     static_assert(C::Q == 64, "the M = 64 accumulator layout is assumed");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *cs = smem, *bs = smem + C::BC_BYTES;
+    uint8_t *cbs = smem, *bs = smem + C::CBM_BYTES, *cs = smem + C::CBM_BYTES + C::BC_BYTES;
     __shared__ uint64_t full_bar, done_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int ok_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const long long plane = ((long long)b * nc + c) * G + g;
     griddep_launch();
     if (warp == 0) {
         tmem_alloc(&tmem_base_sh, 64);
@@ -504,13 +532,14 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
     __syncthreads();
     tc_fence_after();
     if (ok_sh) {
+        // masked CB rows into the pack image: row t, 16-byte chunk k of the
+        // 128-byte row at position k ^ (t % 8)
         const int t = warp * 16 + (lane & 15);
         float v[64];
 #pragma unroll
         for (int k = 0; k < 4; ++k) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + k * 16, *reinterpret_cast<float(*)[16]>(v + 16 * k));
         tmem_ld_wait();
         if (lane < 16) {
-            uint4 *dst = reinterpret_cast<uint4 *>(cbm + ((((long long)b * nc + c) * G + g) * C::Q + t) * C::Q);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 uint4 w;
@@ -518,14 +547,20 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
                 w.y = pack_bf16x2(8 * k + 2 <= t ? v[8 * k + 2] : 0.f, 8 * k + 3 <= t ? v[8 * k + 3] : 0.f);
                 w.z = pack_bf16x2(8 * k + 4 <= t ? v[8 * k + 4] : 0.f, 8 * k + 5 <= t ? v[8 * k + 5] : 0.f);
                 w.w = pack_bf16x2(8 * k + 6 <= t ? v[8 * k + 6] : 0.f, 8 * k + 7 <= t ? v[8 * k + 7] : 0.f);
-                dst[k] = w;
+                *reinterpret_cast<uint4 *>(cbs + t * 128 + ((k ^ (t & 7)) << 4)) = w;
             }
         }
-        __threadfence();
+        fence_async_smem();
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == 0 && ok_sh && ready) st_release_gpu(ready + ((long long)b * nc + c) * G + g, 1u);
+    if (tid == 0 && ok_sh) {
+        bulk_store(pack + plane * C::PACK_BYTES, smem, C::PACK_BYTES);
+        bulk_commit_group();
+        bulk_wait_all();
+        __threadfence();
+        if (ready) st_release_gpu(ready + plane, 1u);
+    }
     if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
@@ -539,7 +574,7 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
 //                 buffers; then the state to HBM and, in the last CTA of a
 //                 (batch, head block), the pass across segments
 // ===========================================================================
-constexpr int kSegThreads = 384;
+constexpr int kSegThreads = 640;
 
 template <class C>
 __global__ void __launch_bounds__(kSegThreads, 1)
@@ -550,9 +585,10 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE);
     uint8_t *dt_ring = smem + ST * C::SEG_STAGE + C::VEC_RING;
-    __shared__ uint64_t dt_bar[kDtAhead];
+    __shared__ uint64_t dt_bar[2];
     TRACE_DECL;
-    __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], afull_bar[2], afree_bar[2];
+    constexpr int NA = C::SEG_NA;
+    __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], afull_bar[NA], afree_bar[NA];
     __shared__ uint64_t done_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
@@ -590,13 +626,13 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             mbar_init(&vfull_bar[i], 1);
             mbar_init(&vempty_bar[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NA; ++i) {
             mbar_init(&afull_bar[i], 1);
             mbar_init(&afree_bar[i], 1);
         }
         mbar_init(&done_bar, 1);
         mbar_init(&drain_bar, 1);
-        for (int i = 0; i < kDtAhead; ++i) mbar_init(&dt_bar[i], 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&dt_bar[i], 1);
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
@@ -620,6 +656,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES + C::BC_BYTES);
                 issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c, b);
                 ++nload[s];
+                TRACE(18, it);
             }
     } else if (warp == 2) {
         // ---------------- segment weights ----------------
@@ -672,8 +709,8 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(C::M, C::N, false, true);
             for (int it = 0; it < nch; ++it) {
-                const int s = it % ST, a = it & 1;
-                if (!wait_bounded(&afull_bar[a], fill_parity(it, 2), &abort_sh)) break;
+                const int s = it % ST, a = it % NA;
+                if (!wait_bounded(&afull_bar[a], fill_parity(it, NA), &abort_sh)) break;
                 if (!wait_bounded(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
                 tc_fence_after();
                 // one descriptor per operand tile, advanced by constants (the
@@ -693,24 +730,27 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             mma_commit(&done_bar);  // completes once every MMA above has
         }
     } else if (warp >= 4) {
-        // ---------------- A operand builders ----------------
+        // ---------------- A operand builders: thread = row (head, p), a quarter of the steps ----------------
+        constexpr int NAB = kSegThreads - 128;
         const int gtid = tid - 128;
-        const int q4 = warp & 3, half = (warp - 4) >> 2;
+        const int q4 = warp & 3, part = (warp - 4) >> 2;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t pcol = (uint32_t)(rp % 64);
         const int blk = rh * C::PB + rp / 64;
         for (int it = 0; it < nch; ++it) {
-            const int s = it % ST, v = it % NV, a = it & 1;
-            if (!group_wait(&full_bar[s], fill_parity(it, ST), &abort_sh, &slot[0], 1, gtid, 256)) break;
-            if (!group_wait(&vfull_bar[v], fill_parity(it, NV), &abort_sh, &slot[1], 1, gtid, 256)) break;
-            if (it >= 2 && !group_wait(&afree_bar[a], free_parity(it, 2), &abort_sh, &slot[2], 1, gtid, 256)) break;
+            const int s = it % ST, v = it % NV, a = it % NA;
+            if (!group_wait(&full_bar[s], fill_parity(it, ST), &abort_sh, &slot[0], 1, gtid, NAB)) break;
+            if (gtid == 0) TRACE(19, it);
+            if (!group_wait(&vfull_bar[v], fill_parity(it, NV), &abort_sh, &slot[1], 1, gtid, NAB)) break;
+            if (it >= NA && !group_wait(&afree_bar[a], free_parity(it, NA), &abort_sh, &slot[2], 1, gtid, NAB)) break;
+            if (gtid == 0) TRACE(17, it);
             tc_fence_after();
-            build_a<C>(stage_x(s) + blk * (C::Q * 128), pcol, vec(v) + C::V_AL + rh * C::Q + half * 32, half,
-                       tmem + lane_off + COL_A + a * C::Q);
+            build_a<C, C::Q / 4>(stage_x(s), blk, pcol, vec(v) + C::V_AL + rh * C::Q + part * (C::Q / 4), part,
+                                 tmem + lane_off + COL_A + a * C::Q);
             tmem_st_wait();
             tc_fence_before();
-            named_bar_sync(1, 256);
+            named_bar_sync(1, NAB);
             if (gtid == 0) {
                 TRACE(15, it);
                 mbar_arrive(&afull_bar[a]);
@@ -718,15 +758,15 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 mbar_arrive(&vempty_bar[v]);
             }
         }
-        // segment state: TMEM lane r = row (head, p); warps 4-7 columns
-        // [0, N/2), warps 8-11 [N/2, N)
+        // segment state: TMEM lane r = row (head, p); each group of four
+        // warps a quarter of the columns
         const long long hrow = h0 + rh;
         bool stored = false;
-        if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 1, gtid, 256)) {
+        if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 1, gtid, NAB)) {
             tc_fence_after();
             float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + hrow) * C::P + rp) * C::N;
 #pragma unroll 1
-            for (int n0 = half * (C::N / 2); n0 < (half + 1) * (C::N / 2); n0 += 16) {
+            for (int n0 = part * (C::N / 4); n0 < (part + 1) * (C::N / 4); n0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + lane_off + n0, v);
                 tmem_ld_wait();
@@ -743,26 +783,26 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         // segment k + 1 = exp(T_k) (state entering k) + local_k
         if (prm.seg_pass && stored) {
             __threadfence();
-            named_bar_sync(1, 256);
+            named_bar_sync(1, NAB);
             if (gtid == 0) {
                 const unsigned done = atomicAdd(&prm.counters[(long long)b * prm.nhb + hblk], 1u);
                 last_sh = done == (unsigned)(prm.nseg - 2) ? 1 : 0;
             }
-            named_bar_sync(1, 256);
+            named_bar_sync(1, NAB);
             if (last_sh) {
                 __threadfence();
-                // 4 elements (float4) per thread at a time, up to 4 segments'
+                // 4 elements (float4) per thread at a time, two segments'
                 // loads issued before any of their results is used
                 constexpr int ROW4 = C::N / 4, E = C::M * ROW4;
                 const long long sstride = H * C::P * C::N;
                 float *base = prm.seg_state + (long long)b * prm.nseg * sstride;
-                for (int e0 = 0; e0 < E; e0 += 4 * 256) {
+                for (int e0 = 0; e0 < E; e0 += 4 * NAB) {
                     long long off[4];
                     long long hh4[4];
                     float4 acc[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int e = e0 + i * 256 + gtid;
+                        const int e = e0 + i * NAB + gtid;
                         const int r = e / ROW4, n4 = e % ROW4;
                         hh4[i] = e < E ? h0 + r / C::P : H;
                         off[i] = (hh4[i] * C::P + r % C::P) * C::N + 4 * n4;
@@ -770,11 +810,11 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                                      ? __ldg(reinterpret_cast<const float4 *>(prm.init + b * sstride + off[i]))
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    for (int k0 = 0; k0 < prm.nseg - 1; k0 += 4) {
-                        float4 loc[4][4];
-                        float ex[4][4];
+                    for (int k0 = 0; k0 < prm.nseg - 1; k0 += 2) {
+                        float4 loc[2][4];
+                        float ex[2][4];
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
+                        for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 const bool ok = k0 + kk < prm.nseg - 1 && hh4[i] < H;
@@ -783,7 +823,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                                 ex[kk][i] = ok ? __ldcg(prm.seg_tot + ((long long)b * H + hh4[i]) * prm.nseg + k0 + kk) : 0.f;
                             }
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
+                        for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
                                 if (!(k0 + kk < prm.nseg - 1 && hh4[i] < H)) continue;
@@ -826,9 +866,9 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 // computed with direct per-entry decay factors, so the caller stores them
 // with a unit factor.
 template <class C>
-__device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const uint8_t *xs_blk, const uint8_t *cbm,
+__device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const uint8_t *xs, int blk, const uint8_t *cbm,
                                         const float *cum, const float *dtv, uint32_t pcol, int t0) {
-    const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xs_blk);
+    const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xs);
     const unsigned short *c16 = reinterpret_cast<const unsigned short *>(cbm);
 #pragma unroll 1
     for (int j0 = 0; j0 < 32; j0 += 16) {
@@ -842,7 +882,7 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
             float acc = 0.f;
 #pragma unroll 1
             for (int s = 0; s <= t; ++s) {
-                const float xv = __uint_as_float((uint32_t)x16[swz128((uint32_t)s, pcol) >> 1] << 16);
+                const float xv = __uint_as_float((uint32_t)x16[swz128((uint32_t)(2 * s + blk), pcol) >> 1] << 16);
                 const float cb = __uint_as_float((uint32_t)c16[swz128((uint32_t)t, (uint32_t)s) >> 1] << 16);
                 acc = fmaf(cb * __expf(ct - cum[s]) * dtv[s], xv, acc);
             }
@@ -876,16 +916,15 @@ constexpr int kScanThreads = 768;
 
 template <class C, typename YT>
 __global__ void __launch_bounds__(kScanThreads, 1)
-    chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
-                      const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap mcb,
-                      const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mdt, TcParams prm) {
+    chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap my,
+                      const __grid_constant__ CUtensorMap mdt, TcParams prm) {
     constexpr int ST = C::SCAN_ST, NV = C::NV, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SCAN_STAGE);
     YT *ybuf = reinterpret_cast<YT *>(smem + ST * C::SCAN_STAGE + C::VEC_RING);
     uint8_t *dt_ring = smem + ST * C::SCAN_STAGE + C::VEC_RING + C::Y_BYTES;
-    __shared__ uint64_t dt_bar[kDtAhead];
+    __shared__ uint64_t dt_bar[2];
     TRACE_DECL;
     __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV];
     __shared__ uint64_t afull_bar[NB], afree_bar[NB], rfull_bar[NB], rfree_bar[NB], sbfree_bar[NB];
@@ -904,9 +943,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const int nch = min(prm.nc, c0 + prm.cps) - c0;
     const long long H = prm.H;
     auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
-    auto stage_b = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES; };
-    auto stage_c = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + C::BC_BYTES; };
-    auto stage_cb = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + 2 * C::BC_BYTES; };
+    auto stage_cb = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES; };
+    auto stage_b = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + C::CBM_BYTES; };
+    auto stage_c = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES + C::CBM_BYTES + C::BC_BYTES; };
     auto vec = [&](int v) { return vec_base + v * C::VEC_FLOATS; };
 
     if (warp == 1) {
@@ -934,13 +973,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mbar_init(&drain_bar, 1);
         mbar_init(&yfull_bar, 1);
         mbar_init(&yfree_bar, 1);
-        for (int i = 0; i < kDtAhead; ++i) mbar_init(&dt_bar[i], 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&dt_bar[i], 1);
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
-        prefetch_tmap(&mb);
-        prefetch_tmap(&mc);
-        prefetch_tmap(&mcb);
         prefetch_tmap(&my);
         if (prm.dt_tma) prefetch_tmap(&mdt);
     }
@@ -966,10 +1002,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
                 const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
                 if (!wait_flag(prm.cb_ready + plane, &abort_sh)) break;
+                // two operations per chunk: the x box and the chunk pack
                 mbar_arrive_expect_tx(&full_bar[s], C::SCAN_STAGE);
-                issue_chunk_loads<C>(stage_x(s), stage_b(s), stage_c(s), &full_bar[s], &mx, &mb, &mc, h0, g, c0 + it,
-                                     b);
-                tma_load_3d(stage_cb(s), &mcb, &full_bar[s], 0, 0, (int)plane);
+                tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, (c0 + it) * C::Q, b);
+                bulk_load(stage_cb(s), prm.pack + plane * C::PACK_BYTES, C::PACK_BYTES, &full_bar[s]);
                 ++nload[s];
                 TRACE(0, it);
             }
@@ -1127,13 +1163,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         if (lane == 0) {
             for (int it = 0; it < nch; ++it) {
                 if (!wait_bounded(&yfull_bar, (uint32_t)(it & 1), &abort_sh)) break;
-                // rows of heads past H are clipped by the map
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                    for (int bk = 0; bk < C::M / 64; ++bk)
-                        tma_store_4d(&my, ybuf + ((hf * (C::M / 64) + bk) * (C::Q / 2)) * 64, (bk % C::PB) * 64,
-                                     h0 + bk / C::PB, (c0 + it) * C::Q + hf * (C::Q / 2), b);
+                // one box per chunk; rows of heads past H are clipped by the map
+                tma_store_5d(&my, ybuf, 0, 0, h0, (c0 + it) * C::Q, b);
                 bulk_commit_group();
                 bulk_wait_read_all();  // the tile has left shared memory
                 TRACE(11, it);
@@ -1254,13 +1285,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         for (int c = 0; c < nch; ++c) {
             const int s = c % ST, v = c % NV, a = c % NB;
             if (!group_wait(&full_bar[s], fill_parity(c, ST), &abort_sh, &slot[4], 2, gtid, 256)) break;
+            if (gtid == 0) TRACE(12, c);
             if (!group_wait(&vfull_bar[v], fill_parity(c, NV), &abort_sh, &slot[5], 2, gtid, 256)) break;
             if (c >= NB && !group_wait(&afree_bar[a], free_parity(c, NB), &abort_sh, &slot[6], 2, gtid, 256)) break;
             if (gtid == 0) TRACE(5, c);
             tc_fence_after();
             const float *vv = vec(v);
-            build_a<C>(stage_x(s) + blk * (C::Q * 128), pcol, vv + C::V_AL + rh * C::Q + half * 32, half,
-                       tmem + lane_off + C::COL_A + a * C::Q);
+            build_a<C, 32>(stage_x(s), blk, pcol, vv + C::V_AL + rh * C::Q + half * 32, half,
+                           tmem + lane_off + C::COL_A + a * C::Q);
             const bool wide = vv[C::V_FLAG + 1] != 0.f;
             tmem_st_wait();
             tc_fence_before();
@@ -1289,8 +1321,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         };
         uint32_t xp[16];
         if (nch > 0) fetch_x_half(xrow(0), xstride, live, xp);
-        // this thread's column of the y tile [half][blk][Q/2][64]
-        YT *yrow = ybuf + ((half * (C::M / 64) + blk) * (C::Q / 2)) * 64 + pcol;
+        // this thread's column of the y tile [Q][blk][64], its 32 steps from half * 32
+        YT *yrow = ybuf + ((half * 32) * (C::M / 64) + blk) * 64 + pcol;
         for (int c = 0; c < nch; ++c) {
             const int s = c % ST, v = c % NV, r = c % NB;
             if (!group_wait(&rfull_bar[r], fill_parity(c, NB), &abort_sh, &slot[7], 3, gtid, 256)) break;
@@ -1301,7 +1333,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             const bool wide = vv[C::V_FLAG + 1] != 0.f;
             const uint32_t tr = tmem + lane_off + C::COL_R + r * C::Q + half * 32;
             if (wide) {
-                wide_fixup<C>(tr, ef, stage_x(s) + blk * (C::Q * 128), stage_cb(s), vv + C::V_CUM + rh * C::Q,
+                wide_fixup<C>(tr, ef, stage_x(s), blk, stage_cb(s), vv + C::V_CUM + rh * C::Q,
                               vv + C::V_DT + rh * C::Q, pcol, half * 32);
                 ef = ones_sh;
             }
@@ -1315,10 +1347,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             for (int j = 0; j < 32; j += 4) {
                 const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
                 const uint32_t w0 = xp[j / 2], w1 = xp[j / 2 + 1];
-                store_y<YT>(yrow + j * 64, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
-                store_y<YT>(yrow + (j + 1) * 64, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
-                store_y<YT>(yrow + (j + 2) * 64, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
-                store_y<YT>(yrow + (j + 3) * 64, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
+                constexpr int YS = (C::M / 64) * 64;  // y tile row (one step)
+                store_y<YT>(yrow + j * YS, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
+                store_y<YT>(yrow + (j + 1) * YS, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
+                store_y<YT>(yrow + (j + 2) * YS, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
+                store_y<YT>(yrow + (j + 3) * YS, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
             }
             fence_async_smem();
             tc_fence_before();
@@ -1380,44 +1413,47 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D bf16 map over the CB matrices [planes][Q][Q], box (64, Q, 1), 128-byte
-// swizzle.
-bool make_cb_map(CUtensorMap *m, const void *base, uint64_t Q, uint64_t planes) {
+// 5-D map of x [b][L][H][P] viewed as (64, P/64, H, L, b), box (64, P/64, HB,
+// Q, 1): one box per chunk holds the CTA's heads with 256 contiguous bytes
+// per step ([Q][HB][P/64][64] in shared memory, 128-byte swizzle).
+bool make_x_map(CUtensorMap *m, const void *base, uint64_t P, uint64_t H, uint64_t L, uint64_t b, uint32_t HB,
+                uint32_t Q) {
     auto enc = get_encode();
     if (!enc) return false;
-    cuuint64_t dims[3] = {Q, Q, planes};
-    cuuint64_t strides[2] = {Q * 2, Q * Q * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)Q, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+    cuuint64_t dims[5] = {64, P / 64, H, L, b};
+    cuuint64_t strides[4] = {128, P * 2, P * H * 2, P * H * L * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)(P / 64), HB, Q, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D map of y [b][L][H][P] (fp32 or bf16) for TMA stores, box (64, 1, T,
-// 1), no swizzle (the staged tile is plain row-major).
+// 5-D map of y [b][L][H][P] (fp32 or bf16) viewed as (64, P/64, H, L, b) for
+// TMA stores, box (64, P/64, HB, Q, 1): one chunk of the CTA's heads per
+// store, [Q][HB][P/64][64] in shared memory without swizzle.
 bool make_y_map(CUtensorMap *m, const void *base, bool f32, uint64_t P, uint64_t H, uint64_t L, uint64_t b,
-                uint32_t T) {
+                uint32_t HB, uint32_t Q) {
     auto enc = get_encode();
     if (!enc) return false;
     const uint64_t es = f32 ? 4 : 2;
-    cuuint64_t dims[4] = {P, H, L, b};
-    cuuint64_t strides[3] = {P * es, P * H * es, P * H * L * es};
-    cuuint32_t box[4] = {64, 1, T, 1};
-    cuuint32_t el[4] = {1, 1, 1, 1};
-    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base),
+    cuuint64_t dims[5] = {64, P / 64, H, L, b};
+    cuuint64_t strides[4] = {64 * es, P * es, P * H * es, P * H * L * es};
+    cuuint32_t box[5] = {64, (cuuint32_t)(P / 64), HB, Q, 1};
+    cuuint32_t el[5] = {1, 1, 1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base),
                dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map of dt [b][L][H] (bf16), box (8 heads, Q steps, 1); needs the row
+// 3-D map of dt [b][L][H] (bf16), box (8 heads, 4 Q steps, 1); needs the row
 // stride H * 2 bytes to be a multiple of 16 (H % 8 == 0).
 bool make_dt_map(CUtensorMap *m, const void *base, uint64_t H, uint64_t L, uint64_t b, uint32_t Q) {
     auto enc = get_encode();
     if (!enc || H % 8 != 0) return false;
     cuuint64_t dims[3] = {H, L, b};
     cuuint64_t strides[2] = {H * 2, H * L * 2};
-    cuuint32_t box[3] = {8, Q, 1};
+    cuuint32_t box[3] = {8, (cuuint32_t)(kDtGroup * Q), 1};
     cuuint32_t el[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, el,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -1443,11 +1479,15 @@ Plan plan_for(const Dims &d) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-size_t cb_bytes(const Dims &d) { return align256(sizeof(bf16) * d.b * d.nc * d.G * d.Q * d.Q); }
+// chunk packs [b, nc, G] of PACK_BYTES
+template <class C>
+size_t pack_bytes(const Dims &d) {
+    return align256((size_t)C::PACK_BYTES * d.b * d.nc * d.G);
+}
 
-// Workspace: status word and segment counters | CB matrices | segment
-// states | segment totals.  The header is cleared on the stream by every
-// call.
+// Workspace: header (status word, segment counters, chunk-pack ready flags)
+// | chunk packs | segment states | segment totals.  The header is cleared on
+// the stream by every call.
 size_t flag_bytes(const Dims &d) { return align256(sizeof(unsigned) * d.b * d.nc * d.G); }
 
 // header: status word | segment counters [b, nhb] | C B^T ready flags [b, nc, G]
@@ -1468,7 +1508,7 @@ constexpr size_t kTraceBytes = (32 * 256 + 4096) * sizeof(long long);
 template <class C>
 size_t workspace_for(const Dims &d) {
     const Plan p = plan_for<C>(d);
-    size_t bytes = header_bytes<C>(d) + cb_bytes(d);
+    size_t bytes = header_bytes<C>(d) + pack_bytes<C>(d);
     if (p.nseg > 1)
         bytes += align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N) + align256(sizeof(float) * d.b * p.nseg * d.H);
 #ifdef SSD_TRACE
@@ -1505,7 +1545,7 @@ cudaError_t raise_smem(const void *fn, int bytes, int &done) {
 }
 
 template <class C>
-cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, bf16 *cbm, unsigned *ready, unsigned *status,
+cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pack, unsigned *ready, unsigned *status,
                       cudaStream_t s) {
     CUtensorMap mb, mc;
     if (!make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
@@ -1514,31 +1554,30 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, bf16 *cbm, u
     cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::SMEM_CB, attr);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)d.nc, (unsigned)d.G, (unsigned)d.b);
-    e = launch_k(cb_mask_kernel<C>, grid, 128, C::SMEM_CB, s, false, mb, mc, cbm, (int)d.nc, (int)d.G, ready, status);
+    e = launch_k(cb_mask_kernel<C>, grid, 128, C::SMEM_CB, s, false, mb, mc, pack, (int)d.nc, (int)d.G, ready, status);
     timing_mark(s, "cb_mask_tc");
     return e;
 }
 
 template <class C>
-cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, const void *B,
-                        const void *Cm, const bf16 *cbm, dim3 grid, const char *name, cudaStream_t s) {
-    CUtensorMap mx, mb, mc, mcb, my, mdt = {};
+cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, dim3 grid, const char *name,
+                        cudaStream_t s) {
+    CUtensorMap mx, my, mdt = {};
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
     const bool f32 = ydtype == SSD_DTYPE_F32;
-    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) ||
-        !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q) || !make_cb_map(&mcb, cbm, C::Q, d.b * d.nc * d.G) ||
-        !make_y_map(&my, prm.y, f32, d.P, d.H, d.L, d.b, C::Q / 2))
+    if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q) ||
+        !make_y_map(&my, prm.y, f32, d.P, d.H, d.L, d.b, C::HB, C::Q))
         return cudaErrorInvalidValue;
     static int attr_f = 0, attr_b = 0;
     cudaError_t e;
     if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mb, mc, mcb, my, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, my, mdt, prm);
     } else {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mb, mc, mcb, my, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, my, mdt, prm);
     }
     timing_mark(s, name);
     return e;
@@ -1548,7 +1587,7 @@ template <class C>
 cudaError_t launch_seg_state(const Dims &d, TcParams prm, const void *x, const void *B, dim3 grid,
                              const char *name, bool pdl, cudaStream_t s) {
     CUtensorMap mx, mb, mdt = {};
-    if (!make_map(&mx, x, d.P, d.H, d.L, d.b, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q))
+    if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
     const int smem = C::SMEM_SEG;
@@ -1589,8 +1628,9 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     prm.status = reinterpret_cast<unsigned *>(w);
     prm.counters = reinterpret_cast<unsigned *>(w + 256);
     prm.cb_ready = reinterpret_cast<unsigned *>(w + 256 + counter_bytes<C>(d));
-    bf16 *cbm = reinterpret_cast<bf16 *>(w + hdr);
-    const size_t seg_off = hdr + cb_bytes(d);
+    uint8_t *pack = reinterpret_cast<uint8_t *>(w + hdr);
+    prm.pack = pack;
+    const size_t seg_off = hdr + pack_bytes<C>(d);
     if (p.nseg > 1) {
         prm.seg_state = reinterpret_cast<float *>(w + seg_off);
         prm.seg_tot = reinterpret_cast<float *>(w + seg_off + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
@@ -1605,7 +1645,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     cudaError_t e = cudaMemsetAsync(w, 0, hdr, s);
     if (e != cudaSuccess) return e;
     timing_begin(s);
-    e = launch_cb<C>(d, B, Cm, cbm, prm.cb_ready, prm.status, s);
+    e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s);
     if (e != cudaSuccess) return e;
     if (p.nseg > 1) {
         e = launch_seg_state<C>(d, prm, x, B, dim3(p.nhb, (unsigned)d.b, p.nseg - 1), "seg_state_tc", true, s);
@@ -1614,7 +1654,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     }
     // segments in the slowest grid dimension: the first segment's CTAs, which
     // need nothing from the segment-state kernel, are scheduled first
-    return launch_scan<C>(d, prm, ydtype, x, B, Cm, cbm, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", s);
+    return launch_scan<C>(d, prm, ydtype, x, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", s);
 }
 
 // Dispatch over the compiled tile configurations.
@@ -1701,15 +1741,16 @@ cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, con
     prm.cps = 1;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
     char *scratch = nullptr;  // ready flags | C B^T matrices
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), flag_bytes(d) + cb_bytes(d), s);
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), flag_bytes(d) + pack_bytes<C>(d), s);
     if (e != cudaSuccess) return e;
     prm.cb_ready = reinterpret_cast<unsigned *>(scratch);
-    bf16 *cbm = reinterpret_cast<bf16 *>(scratch + flag_bytes(d));
+    uint8_t *pack = reinterpret_cast<uint8_t *>(scratch + flag_bytes(d));
+    prm.pack = pack;
     e = cudaMemsetAsync(scratch, 0, flag_bytes(d), s);
     timing_begin(s);
-    if (e == cudaSuccess) e = launch_cb<C>(d, B, Cm, cbm, prm.cb_ready, nullptr, s);
+    if (e == cudaSuccess) e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, nullptr, s);
     if (e == cudaSuccess)
-        e = launch_scan<C>(d, prm, ydtype, x, B, Cm, cbm, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc),
+        e = launch_scan<C>(d, prm, ydtype, x, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc),
                            "chunk_scan_stage_tc", s);
     const cudaError_t e2 = cudaFreeAsync(scratch, s);
     return e != cudaSuccess ? e : e2;
