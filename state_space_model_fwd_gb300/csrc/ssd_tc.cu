@@ -55,7 +55,7 @@ constexpr float kLambda = 64.f;               // |exponent| bound of the scaled 
 
 struct TcParams {
     long long *trace;  // optional event trace of CTA (0, 0, 0) (trace builds only)
-    const bf16 *x;     // [b, L, H, P] (the epilogue's D x term)
+    const bf16 *x;     // [b, L, H, P]
     const bf16 *dt;
     const float *A, *D, *init;
     void *y;
@@ -351,7 +351,8 @@ struct DtFeed {
 // T[hh] = the chunk total (cum of the last step).
 template <class C>
 __device__ __forceinline__ void chunk_cums(const TcParams &prm, int b, int h0, int c, const ChunkDt<C> &dt,
-                                           float (&cum)[C::HB][C::Q / 32], float (&T)[C::HB]) {
+                                           const float (&Ah)[C::HB], float (&cum)[C::HB][C::Q / 32],
+                                           float (&T)[C::HB]) {
     constexpr int QPL = C::Q / 32;
     const int lane = threadIdx.x & 31;
     if (prm.cum_in) {
@@ -368,8 +369,7 @@ __device__ __forceinline__ void chunk_cums(const TcParams &prm, int b, int h0, i
     float run[C::HB], tot[C::HB];
 #pragma unroll
     for (int hh = 0; hh < C::HB; ++hh) {
-        const long long h = h0 + hh;
-        const float a = (h < prm.H && prm.A) ? prm.A[h] : 0.f;
+        const float a = Ah[hh];
         run[hh] = 0.f;
 #pragma unroll
         for (int j = 0; j < QPL; ++j) {
@@ -392,6 +392,13 @@ __device__ __forceinline__ void chunk_cums(const TcParams &prm, int b, int h0, i
         for (int j = 0; j < QPL; ++j) cum[hh][j] += excl;
         T[hh] = __shfl_sync(0xffffffffu, tot[hh], 31);
     }
+}
+
+// Decay rate A of each head of the block (0 past H), loaded once per CTA.
+template <class C>
+__device__ __forceinline__ void load_decay(const TcParams &prm, int h0, float (&Ah)[C::HB]) {
+#pragma unroll
+    for (int hh = 0; hh < C::HB; ++hh) Ah[hh] = (h0 + hh < prm.H && prm.A) ? prm.A[h0 + hh] : 0.f;
 }
 
 // Order-preserving integer key of a float (for warp min / max reductions).
@@ -441,16 +448,57 @@ __device__ __forceinline__ void build_a(const uint8_t *xs, int blk, uint32_t pco
     }
 }
 
-// x[t][p] of one (head, p) row for 32 consecutive steps, two bf16 per word,
-// from global memory (L2): fetched a chunk ahead by the epilogue.
-__device__ __forceinline__ void fetch_x_half(const bf16 *xg, long long stride, bool live, uint32_t (&xp)[16]) {
-    const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xg);
+// This thread's x values of the NS steps from NS part on, read from the
+// swizzled x tile (layout as for build_a), two bf16 per word (step 2j in the
+// low half).  They serve both the A operand and the D x term of the output.
+template <class C, int NS>
+__device__ __forceinline__ void load_x_part(const uint8_t *xs, int blk, uint32_t pcol, int part,
+                                            uint32_t (&xk)[NS / 2]) {
+    static_assert(C::M / 64 == 2, "two 64-wide column blocks per step");
+    const uint8_t *sw[4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const uint32_t lo = live ? __ldg(x16 + (long long)(2 * j) * stride) : 0u;
-        const uint32_t hi = live ? __ldg(x16 + (long long)(2 * j + 1) * stride) : 0u;
-        xp[j] = lo | (hi << 16);
+    for (int k = 0; k < 4; ++k)
+        sw[k] = xs + blk * 128 + (((((pcol >> 3) ^ (uint32_t)(2 * k + blk)) & 7u) << 4) | ((pcol & 7u) << 1));
+#pragma unroll
+    for (int j = 0; j < NS / 2; ++j) {
+        const int s0 = part * NS + 2 * j;
+        const uint32_t x0 = *reinterpret_cast<const unsigned short *>(sw[s0 & 3] + s0 * 256);
+        const uint32_t x1 = *reinterpret_cast<const unsigned short *>(sw[(s0 + 1) & 3] + (s0 + 1) * 256);
+        xk[j] = x0 | (x1 << 16);
     }
+}
+
+// The A operand part of build_a from x values already in registers.
+template <class C, int NS>
+__device__ __forceinline__ void build_a_regs(const uint32_t (&xk)[NS / 2], const float *f, int part,
+                                             uint32_t tmem_a) {
+    uint32_t hi[NS / 2], lo[NS / 2];
+#pragma unroll
+    for (int j = 0; j < NS / 2; j += 2) {
+        const float4 f4 = *reinterpret_cast<const float4 *>(f + 2 * j);
+        const float a0 = __uint_as_float(xk[j] << 16) * f4.x;
+        const float a1 = __uint_as_float(xk[j] & 0xFFFF0000u) * f4.y;
+        const float a2 = __uint_as_float(xk[j + 1] << 16) * f4.z;
+        const float a3 = __uint_as_float(xk[j + 1] & 0xFFFF0000u) * f4.w;
+        const uint32_t h0 = pack_bf16x2(a0, a1), h1 = pack_bf16x2(a2, a3);
+        hi[j] = h0;
+        hi[j + 1] = h1;
+        lo[j] = pack_bf16x2(a0 - __uint_as_float(h0 << 16), a1 - __uint_as_float(h0 & 0xFFFF0000u));
+        lo[j + 1] = pack_bf16x2(a2 - __uint_as_float(h1 << 16), a3 - __uint_as_float(h1 & 0xFFFF0000u));
+    }
+    if constexpr (NS == 32) {
+        tmem_st16u(tmem_a + part * 16, hi);
+        tmem_st16u(tmem_a + C::Q / 2 + part * 16, lo);
+    } else {
+        tmem_st8u(tmem_a + part * 8, hi);
+        tmem_st8u(tmem_a + C::Q / 2 + part * 8, lo);
+    }
+}
+
+// Every lane of the warp waits for the phase (bounded); uniform result.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    const bool ok = wait_bounded(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // TMA loads of chunk c: x tiles of the CTA's heads, B, and (optionally) C.
@@ -667,12 +715,14 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         for (int hh = 0; hh < C::HB; ++hh) after[hh] = 0.f;
         DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
         feed.start(prm, chunk_of);
+        float Ah[C::HB];
+        load_decay<C>(prm, h0, Ah);
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV, c = chunk_of(it);
             ChunkDt<C> dt;
             if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
             float cum[C::HB][QPL], T[C::HB];
-            chunk_cums<C>(prm, b, h0, c, dt, cum, T);
+            chunk_cums<C>(prm, b, h0, c, dt, Ah, cum, T);
             float w[C::HB][QPL];
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) {
@@ -861,17 +911,17 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 
 // Epilogue fix-up of a chunk whose decay range is too wide to scale (rare;
 // kept out of line so the hot path stays small): R holds the inter-chunk
-// term only; replace this thread's 32 accumulator columns by
+// term only; replace this thread's NS accumulator columns by
 //   ef_t R_t + sum_{s<=t} CB[t, s] exp(cum_t - cum_s) dt_s x_s
 // computed with direct per-entry decay factors, so the caller stores them
 // with a unit factor.
-template <class C>
+template <class C, int NS>
 __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const uint8_t *xs, int blk, const uint8_t *cbm,
                                         const float *cum, const float *dtv, uint32_t pcol, int t0) {
     const unsigned short *x16 = reinterpret_cast<const unsigned short *>(xs);
     const unsigned short *c16 = reinterpret_cast<const unsigned short *>(cbm);
 #pragma unroll 1
-    for (int j0 = 0; j0 < 32; j0 += 16) {
+    for (int j0 = 0; j0 < NS; j0 += 16) {
         float v[16];
         tmem_ld16(taddr + j0, v);
         tmem_ld_wait();
@@ -902,17 +952,20 @@ __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) { *p = __float2b
 
 // ===========================================================================
 // Chunk scan with the scaled state carried in TMEM (every segment).
-//   warp 0     : TMA loads of x, B, C, CB
+//   warp 0     : TMA loads of x and the chunk pack (C B^T, B, C)
 //   warp 1     : tcgen05.mma issue, per chunk  R = A CB^T;  Ss += A B (once
 //                the state warps are done with Ss);  R += SB C^T
-//   warp 2     : dt, cumulative decay, rho, the A factors and epilogue
+//   warp 2     : dt, cumulative decay, rho, the A factors and output
 //                factors (a ring of vector sets)
+//   warp 3     : TMA stores of the y tiles
 //   warps 4-7  : state: Ss rescale when rho moves, and its bf16 copy SB
 //                (the A operand of the inter-chunk term)
-//   warps 8-15 : A operand of the next chunk into TMEM; epilogue
-//                y = factor R + D x straight to HBM
+//   warps 8-23 : compute, a quarter of the steps each: chunk c's A operand
+//                into TMEM from the staged x (kept in registers), then
+//                chunk c - 1's output y = factor R + D x into the y tile
 // ===========================================================================
 constexpr int kScanThreads = 768;
+constexpr int kComputeWarps = 16;  // warps 8..23
 
 template <class C, typename YT>
 __global__ void __launch_bounds__(kScanThreads, 1)
@@ -932,7 +985,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
     __shared__ volatile int slot[12];
-    __shared__ volatile int wide_a[NB];
     __shared__ __align__(16) float ones_sh[32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -955,23 +1007,24 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], 2);  // the MMAs' commit, and the A builders (the epilogue on a wide chunk)
+            mbar_init(&empty_bar[i], 1 + kComputeWarps);  // the MMAs' commit; each compute warp once x is in registers
+                                                            // (after its output step on a wide chunk)
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(&vfull_bar[i], 1);
-            mbar_init(&vempty_bar[i], 2);  // state warps and epilogue
+            mbar_init(&vempty_bar[i], 1 + kComputeWarps);  // state warps; each compute warp
         }
         for (int i = 0; i < NB; ++i) {
-            mbar_init(&afull_bar[i], 1);
+            mbar_init(&afull_bar[i], kComputeWarps);
             mbar_init(&afree_bar[i], 1);
             mbar_init(&rfull_bar[i], 1);
-            mbar_init(&rfree_bar[i], 1);
+            mbar_init(&rfree_bar[i], kComputeWarps);
             mbar_init(&sbfree_bar[i], 1);
         }
         mbar_init(&rt_bar, 1);
         mbar_init(&sdone_bar, 1);
         mbar_init(&drain_bar, 1);
-        mbar_init(&yfull_bar, 1);
+        mbar_init(&yfull_bar, kComputeWarps);
         mbar_init(&yfree_bar, 1);
         for (int i = 0; i < 2; ++i) mbar_init(&dt_bar[i], 1);
         fence_mbar_init();
@@ -1018,12 +1071,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         auto chunk_of = [&](int it) { return c0 + it; };
         DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
         feed.start(prm, chunk_of);
+        float Ah[C::HB];
+        load_decay<C>(prm, h0, Ah);
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV;
             ChunkDt<C> dt;
             if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
             float cum[C::HB][QPL], T[C::HB];
-            chunk_cums<C>(prm, b, h0, c0 + it, dt, cum, T);
+            chunk_cums<C>(prm, b, h0, c0 + it, dt, Ah, cum, T);
             // range [lo, hi] of the cumulative decay over the chunk and its start (0)
             int klo[C::HB], khi[C::HB];
 #pragma unroll
@@ -1123,7 +1178,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 if (!wait_bounded(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
                 if (it >= NB && !wait_bounded(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
                 tc_fence_after();
-                const bool wide = wide_a[a] != 0;
+                const bool wide = vec(it % NV)[C::V_FLAG + 1] != 0.f;  // (the A builders saw this slot filled)
                 // R = A CB^T (hi, then lo)
                 if (!wide) {
 #pragma unroll
@@ -1275,95 +1330,87 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 }
             }
         }
-    } else if (warp >= 8 && warp < 16) {
-        // ---------------- A operand: thread = row (head, p), half of the Q steps ----------------
-        const int gtid = tid - 256;
-        const int half = (warp - 8) >> 2;
+    } else if (warp >= 8) {
+        // ---------------- compute warps: thread = row (head, p), a quarter of the Q steps ----------------
+        // Chunk c: the A operand from the staged x (kept in registers), then
+        // the output of chunk c - 1:  y = factor R + D x.
+        const int part = (warp - 8) >> 2;
+        constexpr int NS = C::Q / 4;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const uint32_t pcol = (uint32_t)(rp % 64);
         const int blk = rh * C::PB + rp / 64;
-        for (int c = 0; c < nch; ++c) {
-            const int s = c % ST, v = c % NV, a = c % NB;
-            if (!group_wait(&full_bar[s], fill_parity(c, ST), &abort_sh, &slot[4], 2, gtid, 256)) break;
-            if (gtid == 0) TRACE(12, c);
-            if (!group_wait(&vfull_bar[v], fill_parity(c, NV), &abort_sh, &slot[5], 2, gtid, 256)) break;
-            if (c >= NB && !group_wait(&afree_bar[a], free_parity(c, NB), &abort_sh, &slot[6], 2, gtid, 256)) break;
-            if (gtid == 0) TRACE(5, c);
-            tc_fence_after();
-            const float *vv = vec(v);
-            build_a<C, 32>(stage_x(s), blk, pcol, vv + C::V_AL + rh * C::Q + half * 32, half,
-                           tmem + lane_off + C::COL_A + a * C::Q);
-            const bool wide = vv[C::V_FLAG + 1] != 0.f;
-            tmem_st_wait();
-            tc_fence_before();
-            named_bar_sync(2, 256);
-            if (gtid == 0) {
-                TRACE(6, c);
-                wide_a[a] = wide ? 1 : 0;
-                mbar_arrive(&afull_bar[a]);
-                if (!wide) mbar_arrive(&empty_bar[s]);  // (a wide chunk's epilogue still reads the stage)
-            }
-        }
-    } else if (warp >= 16) {
-        // ---------------- epilogue: y = factor R + D x, thread = row (head, p), half of the steps ----------------
-        const int gtid = tid - 512;
-        const int half = (warp - 16) >> 2;
-        const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const long long hrow = h0 + rh;
-        const bool live = hrow < H;
-        const float dh = (prm.D && live) ? prm.D[hrow] : 0.f;
-        const uint32_t pcol = (uint32_t)(rp % 64);
-        const int blk = rh * C::PB + rp / 64;
-        const long long xstride = H * C::P;
-        auto xrow = [&](int c) {
-            return prm.x + (((long long)b * prm.L + (long long)(c0 + c) * C::Q + half * 32) * H + (live ? hrow : 0)) *
-                               C::P + rp;
-        };
-        uint32_t xp[16];
-        if (nch > 0) fetch_x_half(xrow(0), xstride, live, xp);
-        // this thread's column of the y tile [Q][blk][64], its 32 steps from half * 32
-        YT *yrow = ybuf + ((half * 32) * (C::M / 64) + blk) * 64 + pcol;
-        for (int c = 0; c < nch; ++c) {
-            const int s = c % ST, v = c % NV, r = c % NB;
-            if (!group_wait(&rfull_bar[r], fill_parity(c, NB), &abort_sh, &slot[7], 3, gtid, 256)) break;
-            if (gtid == 0) TRACE(9, c);
-            tc_fence_after();
-            const float *vv = vec(v);
-            const float *ef = vv + C::V_EF + rh * C::Q + half * 32;
-            const bool wide = vv[C::V_FLAG + 1] != 0.f;
-            const uint32_t tr = tmem + lane_off + C::COL_R + r * C::Q + half * 32;
-            if (wide) {
-                wide_fixup<C>(tr, ef, stage_x(s), blk, stage_cb(s), vv + C::V_CUM + rh * C::Q,
-                              vv + C::V_DT + rh * C::Q, pcol, half * 32);
-                ef = ones_sh;
+        const float dh = (prm.D && hrow < H) ? prm.D[hrow] : 0.f;
+        constexpr int YS = (C::M / 64) * 64;  // y tile row (one step)
+        YT *yrow = ybuf + ((part * NS) * (C::M / 64) + blk) * 64 + pcol;
+        uint32_t xprev[NS / 2];
+        bool wide_prev = false;
+        for (int c = 0; c <= nch; ++c) {
+            uint32_t xcur[NS / 2];
+            bool wide = false;
+            if (c < nch) {
+                const int s = c % ST, v = c % NV, a = c % NB;
+                if (!warp_wait(&full_bar[s], fill_parity(c, ST), &abort_sh)) break;
+                if (warp == 8 && lane == 0) TRACE(12, c);
+                if (!warp_wait(&vfull_bar[v], fill_parity(c, NV), &abort_sh)) break;
+                if (c >= NB && !warp_wait(&afree_bar[a], free_parity(c, NB), &abort_sh)) break;
+                if (warp == 8 && lane == 0) TRACE(5, c);
+                tc_fence_after();
+                const float *vv = vec(v);
+                load_x_part<C, NS>(stage_x(s), blk, pcol, part, xcur);
+                build_a_regs<C, NS>(xcur, vv + C::V_AL + rh * C::Q + part * NS, part,
+                                    tmem + lane_off + C::COL_A + a * C::Q);
+                wide = vv[C::V_FLAG + 1] != 0.f;
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp == 8) TRACE(6, c);
+                    mbar_arrive(&afull_bar[a]);
+                    if (!wide) mbar_arrive(&empty_bar[s]);  // (a wide chunk's output step still reads the stage)
+                }
             }
-            float acc[32];
-            tmem_ld16(tr, *reinterpret_cast<float(*)[16]>(acc));
-            tmem_ld16(tr + 16, *reinterpret_cast<float(*)[16]>(acc + 16));
-            tmem_ld_wait();
-            // the previous chunk's y tile has left shared memory
-            if (c > 0 && !group_wait(&yfree_bar, (uint32_t)((c - 1) & 1), &abort_sh, &slot[8], 3, gtid, 256)) break;
+            if (c > 0) {
+                const int cp = c - 1, s = cp % ST, v = cp % NV, r = cp % NB;
+                if (!warp_wait(&rfull_bar[r], fill_parity(cp, NB), &abort_sh)) break;
+                if (warp == 8 && lane == 0) TRACE(9, cp);
+                tc_fence_after();
+                const float *vv = vec(v);
+                const float *ef = vv + C::V_EF + rh * C::Q + part * NS;
+                const uint32_t tr = tmem + lane_off + C::COL_R + r * C::Q + part * NS;
+                if (wide_prev) {
+                    wide_fixup<C, NS>(tr, ef, stage_x(s), blk, stage_cb(s), vv + C::V_CUM + rh * C::Q,
+                                      vv + C::V_DT + rh * C::Q, pcol, part * NS);
+                    ef = ones_sh;
+                }
+                float acc[NS];
+                tmem_ld16(tr, *reinterpret_cast<float(*)[16]>(acc));
+                tmem_ld_wait();
+                // the previous chunk's y tile has left shared memory
+                if (cp > 0 && !warp_wait(&yfree_bar, (uint32_t)((cp - 1) & 1), &abort_sh)) break;
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
-                const uint32_t w0 = xp[j / 2], w1 = xp[j / 2 + 1];
-                constexpr int YS = (C::M / 64) * 64;  // y tile row (one step)
-                store_y<YT>(yrow + j * YS, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
-                store_y<YT>(yrow + (j + 1) * YS, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
-                store_y<YT>(yrow + (j + 2) * YS, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
-                store_y<YT>(yrow + (j + 3) * YS, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
+                for (int j = 0; j < NS; j += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
+                    const uint32_t w0 = xprev[j / 2], w1 = xprev[j / 2 + 1];
+                    store_y<YT>(yrow + j * YS, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
+                    store_y<YT>(yrow + (j + 1) * YS, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
+                    store_y<YT>(yrow + (j + 2) * YS, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
+                    store_y<YT>(yrow + (j + 3) * YS, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp == 8) TRACE(10, cp);
+                    mbar_arrive(&rfree_bar[r]);
+                    mbar_arrive(&vempty_bar[v]);
+                    if (wide_prev) mbar_arrive(&empty_bar[s]);
+                    mbar_arrive(&yfull_bar);
+                }
             }
-            fence_async_smem();
-            tc_fence_before();
-            named_bar_sync(3, 256);
-            if (gtid == 0) {
-                TRACE(10, c);
-                mbar_arrive(&rfree_bar[r]);
-                mbar_arrive(&vempty_bar[v]);
-                if (wide) mbar_arrive(&empty_bar[s]);
-                mbar_arrive(&yfull_bar);
-            }
-            if (c + 1 < nch) fetch_x_half(xrow(c + 1), xstride, live, xp);  // in flight until the next chunk
+#pragma unroll
+            for (int j = 0; j < NS / 2; ++j) xprev[j] = xcur[j];
+            wide_prev = wide;
         }
     }
     // let this CTA's own copies and MMAs land (they normally have) before
