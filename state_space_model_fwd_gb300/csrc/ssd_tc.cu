@@ -111,8 +111,7 @@ struct Cfg {
     // tile of one chunk ([half][M/64 blocks][Q/2 steps][64], fp32 or bf16)
     // that the TMA stores to HBM
     static constexpr int SCAN_STAGE = X_BYTES + PACK_BYTES;
-    static constexpr int Y_BYTES = M * Q * 4;
-    static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + Y_BYTES + DT_RING + 1024; }
+    static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + DT_RING + 1024; }
     static constexpr int SCAN_ST = scan_smem(4) <= kSmemLimit ? 4 : (scan_smem(3) <= kSmemLimit ? 3 : 2);
     static constexpr int SMEM_SCAN = scan_smem(SCAN_ST);
     static constexpr bool SCAN_FITS = SMEM_SCAN <= kSmemLimit;
@@ -945,10 +944,16 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
 
 template <typename T>
 __device__ __forceinline__ void store_y(T *p, float v);
+// streaming (evict-first) stores: y is written once and not read back
 template <>
-__device__ __forceinline__ void store_y<float>(float *p, float v) { *p = v; }
+__device__ __forceinline__ void store_y<float>(float *p, float v) {
+    asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
 template <>
-__device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) { *p = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) {
+    const unsigned short u = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(u) : "memory");
+}
 
 // ===========================================================================
 // Chunk scan with the scaled state carried in TMEM (every segment).
@@ -957,31 +962,30 @@ __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) { *p = __float2b
 //                the state warps are done with Ss);  R += SB C^T
 //   warp 2     : dt, cumulative decay, rho, the A factors and output
 //                factors (a ring of vector sets)
-//   warp 3     : TMA stores of the y tiles
 //   warps 4-7  : state: Ss rescale when rho moves, and its bf16 copy SB
 //                (the A operand of the inter-chunk term)
 //   warps 8-23 : compute, a quarter of the steps each: chunk c's A operand
 //                into TMEM from the staged x (kept in registers), then
-//                chunk c - 1's output y = factor R + D x into the y tile
+//                chunk c - 1's output y = factor R + D x to global memory
 // ===========================================================================
 constexpr int kScanThreads = 768;
 constexpr int kComputeWarps = 16;  // warps 8..23
 
 template <class C, typename YT>
 __global__ void __launch_bounds__(kScanThreads, 1)
-    chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap my,
-                      const __grid_constant__ CUtensorMap mdt, TcParams prm) {
+    chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mdt, TcParams prm) {
     constexpr int ST = C::SCAN_ST, NV = C::NV, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SCAN_STAGE);
-    YT *ybuf = reinterpret_cast<YT *>(smem + ST * C::SCAN_STAGE + C::VEC_RING);
-    uint8_t *dt_ring = smem + ST * C::SCAN_STAGE + C::VEC_RING + C::Y_BYTES;
+    uint8_t *dt_ring = smem + ST * C::SCAN_STAGE + C::VEC_RING;
     __shared__ uint64_t dt_bar[2];
     TRACE_DECL;
-    __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV];
+    // a stage's x tile and chunk pack land on separate barriers: the A
+    // builders need only x, the MMAs only the pack
+    __shared__ uint64_t full_bar[4], pfull_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV];
     __shared__ uint64_t afull_bar[NB], afree_bar[NB], rfull_bar[NB], rfree_bar[NB], sbfree_bar[NB];
-    __shared__ uint64_t rt_bar, sdone_bar, drain_bar, yfull_bar, yfree_bar;
+    __shared__ uint64_t rt_bar, sdone_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
     __shared__ volatile int slot[12];
@@ -1007,6 +1011,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) {
             mbar_init(&full_bar[i], 1);
+            mbar_init(&pfull_bar[i], 1);
             mbar_init(&empty_bar[i], 1 + kComputeWarps);  // the MMAs' commit; each compute warp once x is in registers
                                                             // (after its output step on a wide chunk)
         }
@@ -1024,13 +1029,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mbar_init(&rt_bar, 1);
         mbar_init(&sdone_bar, 1);
         mbar_init(&drain_bar, 1);
-        mbar_init(&yfull_bar, kComputeWarps);
-        mbar_init(&yfree_bar, 1);
         for (int i = 0; i < 2; ++i) mbar_init(&dt_bar[i], 1);
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
-        prefetch_tmap(&my);
         if (prm.dt_tma) prefetch_tmap(&mdt);
     }
     if (tid < 32) ones_sh[tid] = 1.f;
@@ -1043,7 +1045,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         TRACE_CTA(0);
     }
     const uint32_t tmem = tmem_base_sh;
-    int nload[4] = {0, 0, 0, 0};  // TMA loads issued per stage (producer lane 0)
+    int nload[4] = {0, 0, 0, 0}, npack[4] = {0, 0, 0, 0};  // x boxes and packs issued per stage (producer lane 0)
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
 
@@ -1054,12 +1056,15 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 const int s = it % ST;
                 if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
                 const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
-                if (!wait_flag(prm.cb_ready + plane, &abort_sh)) break;
-                // two operations per chunk: the x box and the chunk pack
-                mbar_arrive_expect_tx(&full_bar[s], C::SCAN_STAGE);
+                // two operations per chunk: the x box, then the chunk pack
+                // once the C B^T kernel has published it
+                mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES);
                 tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, (c0 + it) * C::Q, b);
-                bulk_load(stage_cb(s), prm.pack + plane * C::PACK_BYTES, C::PACK_BYTES, &full_bar[s]);
                 ++nload[s];
+                if (!wait_flag(prm.cb_ready + plane, &abort_sh)) break;
+                mbar_arrive_expect_tx(&pfull_bar[s], C::PACK_BYTES);
+                bulk_load(stage_cb(s), prm.pack + plane * C::PACK_BYTES, C::PACK_BYTES, &pfull_bar[s]);
+                ++npack[s];
                 TRACE(0, it);
             }
     } else if (warp == 2) {
@@ -1174,7 +1179,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 const uint64_t dc = sdesc(smem_u32(stage_c(s)), 16, 1024);
                 const uint32_t ta = tmem + C::COL_A + a * C::Q, tr = tmem + C::COL_R + a * C::Q;
                 const uint32_t tsb = tmem + C::COL_SB + a * (C::N / 2);
-                if (!wait_bounded(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
+                if (!wait_bounded(&pfull_bar[s], fill_parity(it, ST), &abort_sh)) break;
                 if (!wait_bounded(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
                 if (it >= NB && !wait_bounded(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
                 tc_fence_after();
@@ -1212,20 +1217,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 mma_commit(&empty_bar[s]);
                 TRACE(4, it);
             }
-        }
-    } else if (warp == 3) {
-        // ---------------- y tiles to HBM (TMA stores) ----------------
-        if (lane == 0) {
-            for (int it = 0; it < nch; ++it) {
-                if (!wait_bounded(&yfull_bar, (uint32_t)(it & 1), &abort_sh)) break;
-                // one box per chunk; rows of heads past H are clipped by the map
-                tma_store_5d(&my, ybuf, 0, 0, h0, (c0 + it) * C::Q, b);
-                bulk_commit_group();
-                bulk_wait_read_all();  // the tile has left shared memory
-                TRACE(11, it);
-                mbar_arrive(&yfree_bar);
-            }
-            bulk_wait_all();
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- state: rescale and bf16 copy ----------------
@@ -1341,8 +1332,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const int blk = rh * C::PB + rp / 64;
         const long long hrow = h0 + rh;
         const float dh = (prm.D && hrow < H) ? prm.D[hrow] : 0.f;
-        constexpr int YS = (C::M / 64) * 64;  // y tile row (one step)
-        YT *yrow = ybuf + ((part * NS) * (C::M / 64) + blk) * 64 + pcol;
+        // this thread's y column: steps part * NS .. + NS of each chunk
+        const long long ystep = H * C::P;
+        YT *yg = reinterpret_cast<YT *>(prm.y) +
+                 (((long long)b * prm.L + (long long)c0 * C::Q + part * NS) * H + (hrow < H ? hrow : 0)) * C::P + rp;
+        const bool live = hrow < H;
         uint32_t xprev[NS / 2];
         bool wide_prev = false;
         for (int c = 0; c <= nch; ++c) {
@@ -1386,18 +1380,19 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 float acc[NS];
                 tmem_ld16(tr, *reinterpret_cast<float(*)[16]>(acc));
                 tmem_ld_wait();
-                // the previous chunk's y tile has left shared memory
-                if (cp > 0 && !warp_wait(&yfree_bar, (uint32_t)((cp - 1) & 1), &abort_sh)) break;
+                // straight to global memory: a warp writes one contiguous
+                // run of 32 p per step
+                YT *yc = yg + (long long)cp * C::Q * ystep;
+                if (live)
 #pragma unroll
-                for (int j = 0; j < NS; j += 4) {
-                    const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
-                    const uint32_t w0 = xprev[j / 2], w1 = xprev[j / 2 + 1];
-                    store_y<YT>(yrow + j * YS, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
-                    store_y<YT>(yrow + (j + 1) * YS, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
-                    store_y<YT>(yrow + (j + 2) * YS, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
-                    store_y<YT>(yrow + (j + 3) * YS, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
-                }
-                fence_async_smem();
+                    for (int j = 0; j < NS; j += 4) {
+                        const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
+                        const uint32_t w0 = xprev[j / 2], w1 = xprev[j / 2 + 1];
+                        store_y<YT>(yc + j * ystep, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
+                        store_y<YT>(yc + (j + 1) * ystep, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
+                        store_y<YT>(yc + (j + 2) * ystep, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
+                        store_y<YT>(yc + (j + 3) * ystep, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
+                    }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -1405,7 +1400,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     mbar_arrive(&rfree_bar[r]);
                     mbar_arrive(&vempty_bar[v]);
                     if (wide_prev) mbar_arrive(&empty_bar[s]);
-                    mbar_arrive(&yfull_bar);
                 }
             }
 #pragma unroll
@@ -1416,8 +1410,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // let this CTA's own copies and MMAs land (they normally have) before
     // TMEM is freed and the CTA exits
     if (warp == 0 && lane == 0)
-        for (int s = 0; s < ST; ++s)
+        for (int s = 0; s < ST; ++s) {
             if (nload[s] > 0) mbar_wait(&full_bar[s], (uint32_t)((nload[s] - 1) & 1), kDrainNs);
+            if (npack[s] > 0) mbar_wait(&pfull_bar[s], (uint32_t)((npack[s] - 1) & 1), kDrainNs);
+        }
     if (warp == 1 && lane == 0) {
         mma_commit(&drain_bar);
         mbar_wait(&drain_bar, 0, kDrainNs);
@@ -1474,23 +1470,6 @@ bool make_x_map(CUtensorMap *m, const void *base, uint64_t P, uint64_t H, uint64
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 5-D map of y [b][L][H][P] (fp32 or bf16) viewed as (64, P/64, H, L, b) for
-// TMA stores, box (64, P/64, HB, Q, 1): one chunk of the CTA's heads per
-// store, [Q][HB][P/64][64] in shared memory without swizzle.
-bool make_y_map(CUtensorMap *m, const void *base, bool f32, uint64_t P, uint64_t H, uint64_t L, uint64_t b,
-                uint32_t HB, uint32_t Q) {
-    auto enc = get_encode();
-    if (!enc) return false;
-    const uint64_t es = f32 ? 4 : 2;
-    cuuint64_t dims[5] = {64, P / 64, H, L, b};
-    cuuint64_t strides[4] = {64 * es, P * es, P * H * es, P * H * L * es};
-    cuuint32_t box[5] = {64, (cuuint32_t)(P / 64), HB, Q, 1};
-    cuuint32_t el[5] = {1, 1, 1, 1, 1};
-    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base),
-               dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D map of dt [b][L][H] (bf16), box (8 heads, 4 Q steps, 1); needs the row
@@ -1609,22 +1588,20 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pac
 template <class C>
 cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, dim3 grid, const char *name,
                         cudaStream_t s) {
-    CUtensorMap mx, my, mdt = {};
+    CUtensorMap mx, mdt = {};
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
     const bool f32 = ydtype == SSD_DTYPE_F32;
-    if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q) ||
-        !make_y_map(&my, prm.y, f32, d.P, d.H, d.L, d.b, C::HB, C::Q))
-        return cudaErrorInvalidValue;
+    if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q)) return cudaErrorInvalidValue;
     static int attr_f = 0, attr_b = 0;
     cudaError_t e;
     if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, my, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mdt, prm);
     } else {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, my, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mdt, prm);
     }
     timing_mark(s, name);
     return e;
