@@ -958,8 +958,8 @@ __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) {
 // ===========================================================================
 // Chunk scan with the scaled state carried in TMEM (every segment).
 //   warp 0     : TMA loads of x and the chunk pack (C B^T, B, C)
-//   warp 1     : tcgen05.mma issue, per chunk  R = A CB^T;  Ss += A B (once
-//                the state warps are done with Ss);  R += SB C^T
+//   warp 1     : tcgen05.mma issue, per chunk  Ss += A B (once the state
+//                warps are done with Ss);  R = A CB^T;  R += SB C^T
 //   warp 2     : dt, cumulative decay, rho, the A factors and output
 //                factors (a ring of vector sets)
 //   warps 4-7  : state: Ss rescale when rho moves, and its bf16 copy SB
@@ -1180,8 +1180,25 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 const uint32_t ta = tmem + C::COL_A + a * C::Q, tr = tmem + C::COL_R + a * C::Q;
                 const uint32_t tsb = tmem + C::COL_SB + a * (C::N / 2);
                 if (!wait_bounded(&pfull_bar[s], fill_parity(it, ST), &abort_sh)) break;
+                TRACE(20, it);
                 if (!wait_bounded(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
+                TRACE(21, it);
+                // Ss += A^T B first: the state chain (state warps -> these
+                // MMAs -> state warps) is the longest loop of the pipeline, so
+                // it waits for no other MMA; once the state warps have read
+                // (and rescaled) Ss and written SB
+                if (!wait_bounded(&rt_bar, (uint32_t)(it & 1), &abort_sh)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 8, desc_add(db, ks * 2048), id_state, true);
+#pragma unroll
+                for (int ks = 0; ks < C::Q / 16; ++ks)
+                    mma_bf16_ta(tmem + C::COL_S, ta + C::Q / 2 + ks * 8, desc_add(db, ks * 2048), id_state, true);
+                mma_commit(&sdone_bar);
+                TRACE(3, it);
                 if (it >= NB && !wait_bounded(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
+                TRACE(22, it);
                 tc_fence_after();
                 const bool wide = vec(it % NV)[C::V_FLAG + 1] != 0.f;  // (the A builders saw this slot filled)
                 // R = A CB^T (hi, then lo)
@@ -1193,20 +1210,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                     for (int ks = 0; ks < C::Q / 16; ++ks)
                         mma_bf16_ta(tr, ta + C::Q / 2 + ks * 8, desc_add(dcb, ks * 32), id_intra, true);
                 }
-                TRACE(2, it);
-                // Ss += A^T B: once the state warps have read (and rescaled) Ss
-                // and written SB
-                if (!wait_bounded(&rt_bar, (uint32_t)(it & 1), &abort_sh)) break;
-                tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 8, desc_add(db, ks * 2048), id_state, true);
-#pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + C::Q / 2 + ks * 8, desc_add(db, ks * 2048), id_state, true);
-                mma_commit(&sdone_bar);
                 mma_commit(&afree_bar[a]);
-                TRACE(3, it);
+                TRACE(2, it);
                 // R += SB C^T
 #pragma unroll
                 for (int ks = 0; ks < C::N / 16; ++ks)
