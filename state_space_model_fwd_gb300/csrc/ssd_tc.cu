@@ -622,6 +622,7 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
 //                 (batch, head block), the pass across segments
 // ===========================================================================
 constexpr int kSegThreads = 640;
+constexpr int kSegABWarps = (kSegThreads - 128) / 32;  // warps 4..19
 
 template <class C>
 __global__ void __launch_bounds__(kSegThreads, 1)
@@ -667,14 +668,14 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], 2);  // the MMAs' commit and the operand builders
+            mbar_init(&empty_bar[i], 1 + kSegABWarps);  // the MMAs' commit and each operand-builder warp
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(&vfull_bar[i], 1);
-            mbar_init(&vempty_bar[i], 1);
+            mbar_init(&vempty_bar[i], kSegABWarps);
         }
         for (int i = 0; i < NA; ++i) {
-            mbar_init(&afull_bar[i], 1);
+            mbar_init(&afull_bar[i], kSegABWarps);
             mbar_init(&afree_bar[i], 1);
         }
         mbar_init(&done_bar, 1);
@@ -787,21 +788,22 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
         const uint32_t pcol = (uint32_t)(rp % 64);
         const int blk = rh * C::PB + rp / 64;
+        // every warp waits and arrives on its own (no group-wide barrier per chunk)
         for (int it = 0; it < nch; ++it) {
             const int s = it % ST, v = it % NV, a = it % NA;
-            if (!group_wait(&full_bar[s], fill_parity(it, ST), &abort_sh, &slot[0], 1, gtid, NAB)) break;
+            if (!warp_wait(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
             if (gtid == 0) TRACE(19, it);
-            if (!group_wait(&vfull_bar[v], fill_parity(it, NV), &abort_sh, &slot[1], 1, gtid, NAB)) break;
-            if (it >= NA && !group_wait(&afree_bar[a], free_parity(it, NA), &abort_sh, &slot[2], 1, gtid, NAB)) break;
+            if (!warp_wait(&vfull_bar[v], fill_parity(it, NV), &abort_sh)) break;
+            if (it >= NA && !warp_wait(&afree_bar[a], free_parity(it, NA), &abort_sh)) break;
             if (gtid == 0) TRACE(17, it);
             tc_fence_after();
             build_a<C, C::Q / 4>(stage_x(s), blk, pcol, vec(v) + C::V_AL + rh * C::Q + part * (C::Q / 4), part,
                                  tmem + lane_off + COL_A + a * C::Q);
             tmem_st_wait();
             tc_fence_before();
-            named_bar_sync(1, NAB);
-            if (gtid == 0) {
-                TRACE(15, it);
+            __syncwarp();
+            if (lane == 0) {
+                if (gtid == 0) TRACE(15, it);
                 mbar_arrive(&afull_bar[a]);
                 mbar_arrive(&empty_bar[s]);
                 mbar_arrive(&vempty_bar[v]);
