@@ -123,7 +123,7 @@ struct Cfg {
 
     // segment-state kernel: TMA stages of (x, B) and the vector ring
     static constexpr int SEG_STAGE = X_BYTES + BC_BYTES;
-    static constexpr int seg_smem(int st) { return st * SEG_STAGE + VEC_RING + DT_RING + 1024; }
+    static constexpr int seg_smem(int st) { return st * SEG_STAGE + VEC_RING + HB * DT_RING + 1024; }
     static constexpr int SEG_ST = seg_smem(4) <= kSmemLimit ? 4 : (seg_smem(3) <= kSmemLimit ? 3 : 2);
     static constexpr int SMEM_SEG = seg_smem(SEG_ST);
     static constexpr int SEG_NA = N + 3 * Q <= 512 ? 3 : 2;  // A buffers of the segment-state kernel
@@ -393,6 +393,39 @@ __device__ __forceinline__ void chunk_cums(const TcParams &prm, int b, int h0, i
     }
 }
 
+// In-chunk cumulative decay of one head hh of the block for this lane's
+// steps (or the caller's dA_cumsum); T = the chunk total.
+template <class C>
+__device__ __forceinline__ void head_cums(const TcParams &prm, int b, int h0, int hh, int c, const ChunkDt<C> &dt,
+                                          float a, float (&cum)[C::Q / 32], float &T) {
+    constexpr int QPL = C::Q / 32;
+    const int lane = threadIdx.x & 31;
+    const long long h = h0 + hh;
+    if (prm.cum_in) {
+        const float *src = prm.cum_in + (((long long)b * prm.H + (h < prm.H ? h : 0)) * prm.nc + c) * C::Q;
+#pragma unroll
+        for (int j = 0; j < QPL; ++j) cum[j] = h < prm.H ? __ldg(src + QPL * lane + j) : 0.f;
+        T = h < prm.H ? __ldg(src + C::Q - 1) : 0.f;
+        return;
+    }
+    float run = 0.f;
+#pragma unroll
+    for (int j = 0; j < QPL; ++j) {
+        run += dt.d[hh][j] * a;
+        cum[j] = run;
+    }
+    float tot = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, tot, off);
+        if (lane >= off) tot += o;
+    }
+    const float excl = tot - run;
+#pragma unroll
+    for (int j = 0; j < QPL; ++j) cum[j] += excl;
+    T = __shfl_sync(0xffffffffu, tot, 31);
+}
+
 // Decay rate A of each head of the block (0 past H), loaded once per CTA.
 template <class C>
 __device__ __forceinline__ void load_decay(const TcParams &prm, int h0, float (&Ah)[C::HB]) {
@@ -633,7 +666,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE);
     uint8_t *dt_ring = smem + ST * C::SEG_STAGE + C::VEC_RING;
-    __shared__ uint64_t dt_bar[2];
+    __shared__ uint64_t dt_bar[2 * C::HB];  // a dt ring per vector warp
     TRACE_DECL;
     constexpr int NA = C::SEG_NA;
     __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], afull_bar[NA], afree_bar[NA];
@@ -671,7 +704,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             mbar_init(&empty_bar[i], 1 + kSegABWarps);  // the MMAs' commit and each operand-builder warp
         }
         for (int i = 0; i < NV; ++i) {
-            mbar_init(&vfull_bar[i], 1);
+            mbar_init(&vfull_bar[i], C::HB);  // one vector warp per head
             mbar_init(&vempty_bar[i], kSegABWarps);
         }
         for (int i = 0; i < NA; ++i) {
@@ -680,7 +713,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         }
         mbar_init(&done_bar, 1);
         mbar_init(&drain_bar, 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&dt_bar[i], 1);
+        for (int i = 0; i < 2 * C::HB; ++i) mbar_init(&dt_bar[i], 1);
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
@@ -706,54 +739,41 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 ++nload[s];
                 TRACE(18, it);
             }
-    } else if (warp == 2) {
-        // ---------------- segment weights ----------------
+    } else if (warp == 2 || (warp == 3 && C::HB > 1)) {
+        // ---------------- segment weights, one warp per head ----------------
         //   w_s = exp(after + T - cum_s) dt_s, after = decay of the later chunks
         constexpr int QPL = C::Q / 32;
-        float after[C::HB];
-#pragma unroll
-        for (int hh = 0; hh < C::HB; ++hh) after[hh] = 0.f;
-        DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
+        const int hv = warp - 2;
+        float after = 0.f;
+        DtFeed<C> feed{dt_ring + hv * C::DT_RING, dt_bar + 2 * hv, &mdt, b, h0, nch, 0};
         feed.start(prm, chunk_of);
-        float Ah[C::HB];
-        load_decay<C>(prm, h0, Ah);
+        const float a = (h0 + hv < H && prm.A) ? prm.A[h0 + hv] : 0.f;
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV, c = chunk_of(it);
             ChunkDt<C> dt;
             if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
-            float cum[C::HB][QPL], T[C::HB];
-            chunk_cums<C>(prm, b, h0, c, dt, Ah, cum, T);
-            float w[C::HB][QPL];
+            float cum[QPL], T;
+            head_cums<C>(prm, b, h0, hv, c, dt, a, cum, T);
+            float w[QPL];
 #pragma unroll
-            for (int hh = 0; hh < C::HB; ++hh) {
-#pragma unroll
-                for (int j = 0; j < QPL; ++j) w[hh][j] = __expf(after[hh] + T[hh] - cum[hh][j]) * dt.d[hh][j];
-                after[hh] += T[hh];
-            }
+            for (int j = 0; j < QPL; ++j) w[j] = __expf(after + T - cum[j]) * dt.d[hv][j];
+            after += T;
             if (it >= NV) {
                 int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], free_parity(it, NV), &abort_sh) ? 1 : 0) : 0;
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             }
             float *vv = vec(v);
 #pragma unroll
-            for (int hh = 0; hh < C::HB; ++hh)
-#pragma unroll
-                for (int j = 0; j < QPL; ++j) vv[C::V_AL + hh * C::Q + QPL * lane + j] = w[hh][j];
+            for (int j = 0; j < QPL; ++j) vv[C::V_AL + hv * C::Q + QPL * lane + j] = w[j];
             __syncwarp();
             if (lane == 0) {
-                TRACE(14, it);
+                if (hv == 0) TRACE(14, it);
                 mbar_arrive(&vfull_bar[v]);
             }
         }
         feed.drain();
         // total dt*A of the segment, for the pass across segments
-        if (lane < C::HB && h0 + lane < H && prm.seg_tot) {
-            float t = after[0];
-#pragma unroll
-            for (int hh = 1; hh < C::HB; ++hh)
-                if (lane == hh) t = after[hh];
-            prm.seg_tot[((long long)b * H + h0 + lane) * prm.nseg + seg] = t;
-        }
+        if (lane == 0 && h0 + hv < H && prm.seg_tot) prm.seg_tot[((long long)b * H + h0 + hv) * prm.nseg + seg] = after;
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
