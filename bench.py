@@ -5,7 +5,7 @@
 One step = one ssd_fwd call (the whole chunked forward: cumulative decay,
 chunk states, state passing, chunk outputs) over one batch of the Mamba-2
 130M-shaped layer workload: batch 4, L 2048, H 24, P 64, N 128, G 1, Q 64,
-bf16 inputs, fp32 state / accumulation / y.  Inputs are seeded synthetic
+bf16 inputs and y, fp32 state and accumulation.  Inputs are seeded synthetic
 tensors (ssd_inputs.py), resident in HBM before timing starts; L2 (129 MB,
 larger than this workload's 58 MB) is flushed by a 512 MB write between
 timed steps, outside the timed events.
@@ -38,6 +38,7 @@ WORKLOAD = "mamba2_130m"
 FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+Y_BYTES = 2  # y in bf16, the input dtype (fp32 state and accumulation)
 
 
 # ---------------------------------------------------------------------------
@@ -47,7 +48,7 @@ def elem_bytes(dtype):
     return 4 if dtype == "f32" else 2
 
 
-def compulsory_bytes(cfg, y_bytes=4):
+def compulsory_bytes(cfg, y_bytes=Y_BYTES):
     """Reads of x, dt, B, C, A, D (+ init) and writes of y and final state."""
     b, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
     e = elem_bytes(cfg.dtype)
@@ -280,9 +281,10 @@ def main():
     cfg_rank = cfg.replace(seed=cfg.seed + 7919 * rank)
     inp = si.make_inputs(cfg_rank)
     t = inp.to_torch(dev)
-    y = torch.empty(t["x"].shape, device=dev, dtype=torch.float32)
+    y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
     fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), device=dev, dtype=torch.float32)
-    ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], cfg.chunk_size))),
+    ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], cfg.chunk_size,
+                                                                       torch.bfloat16))),
                      device=dev, dtype=torch.uint8)
     flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream(dev)
@@ -333,7 +335,7 @@ def main():
     dom = int(np.argmax(launch_ms))
 
     peaks = load_peaks()
-    cbytes = compulsory_bytes(cfg, 4)
+    cbytes = compulsory_bytes(cfg)
     dom_name = kernel_names[dom] if dom < len(kernel_names) else f"launch{dom}"
     dom_bytes = KERNEL_BYTES(cfg, dom_name)
     achieved = dom_bytes / (launch_ms[dom] * 1e-3) / 1e9
@@ -384,7 +386,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": cfg.name, "batch": cfg.batch, "seqlen": cfg.seqlen, "nheads": cfg.nheads,
                        "headdim": cfg.headdim, "dstate": cfg.dstate, "ngroups": cfg.ngroups,
-                       "chunk_size": cfg.chunk_size, "state_dtype": "f32", "y_dtype": "f32",
+                       "chunk_size": cfg.chunk_size, "state_dtype": "f32", "y_dtype": "bf16",
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "l2": "flushed between timed steps (512 MB write, outside the step events)"},
             "clocks": clocks,
@@ -414,11 +416,12 @@ def main():
 
 def tc_plan(cfg, target_ctas=148):
     """Segment plan of the fused tensor-core path (mirrors the library):
-    CTAs own 128/P heads; segments of consecutive chunks fill ~148 CTAs."""
+    CTAs own 128/P heads; segments of consecutive 64-step tiles (a 128-step
+    chunk is two of them) fill ~148 CTAs."""
     hb = 128 // cfg.headdim
     nhb = -(-cfg.nheads // hb)
     units = cfg.batch * nhb
-    nc = cfg.seqlen // cfg.chunk_size
+    nc = cfg.seqlen // 64
     nseg = max(1, min(nc, target_ctas // units))
     cps = -(-nc // nseg)
     nseg = -(-nc // cps)
@@ -435,23 +438,26 @@ def KERNEL_BYTES(cfg, name):
     bc = b * L * G * N * e
     st = b * nc * H * P * N * 4
     cum = b * H * L * 4
-    y = b * L * H * P * 4
+    y = b * L * H * P * Y_BYTES
     init = b * H * P * N * 4 if cfg.has_init else 0
     fin = b * H * P * N * 4
-    nseg, cps, _ = tc_plan(cfg)
+    nseg, cps, nt = tc_plan(cfg)
     seg_states = b * (nseg - 1) * H * P * N * 4
-    covered = min(nc, (nseg - 1) * cps) / nc  # share of the sequence the segment-state kernel reads
-    cbm = b * nc * G * Q * Q * 2  # masked C B^T of every (chunk, group), bf16
+    covered = min(nt, (nseg - 1) * cps) / nt  # share of the sequence the segment-state kernel reads
+    # chunk packs: masked C B^T (bf16, 64-step tiles) with the tile's B and C
+    pack = b * nt * G * 64 * 64 * 2 + 2 * bc
     return {
         "chunk_cumsum": dt + cum,
         "chunk_state_simt": x + dt + bc + cum + st,
         "state_passing": st + cum + init + st + fin,
         "chunk_scan_simt": x + dt + 2 * bc + cum + st + y,
-        # fused tensor-core path: C B^T, segment states (with the pass across
-        # segments: one read and one write of every segment state), chunk scan
-        "cb_mask_tc": 2 * bc + cbm,
+        # fused tensor-core path: chunk packs (read B, C; write the packs),
+        # segment states (with the pass across segments: every segment state
+        # written, read back and rewritten in place), chunk scan (reads every
+        # pack once per (batch, chunk, group) as its B, C and C B^T input)
+        "cb_mask_tc": 2 * bc + pack,
         "seg_state_tc": covered * (x + dt + bc) + 3 * seg_states + (init if nseg > 1 else 0),
-        "chunk_scan_tc": x + dt + 2 * bc + cbm + seg_states + init + y + fin,
+        "chunk_scan_tc": x + dt + pack + seg_states + init + y + fin,
     }.get(name, compulsory_bytes(cfg))
 
 
@@ -464,9 +470,10 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
         cfg = si.CONFIGS[name]
         inp = si.make_inputs(cfg)
         t = inp.to_torch(dev)
-        y = torch.empty(t["x"].shape, device=dev, dtype=torch.float32)
+        y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
         fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), device=dev, dtype=torch.float32)
-        ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], cfg.chunk_size))),
+        ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], cfg.chunk_size,
+                                                                           torch.bfloat16))),
                          device=dev, dtype=torch.uint8)
 
         def run():
@@ -474,7 +481,7 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
                         y=y, final_state=fin, workspace=ws)
 
         ms = time_device(run, flush, steps)
-        cb = compulsory_bytes(cfg, 4)
+        cb = compulsory_bytes(cfg)
         rec = {"tokens_per_s": cfg.tokens / (ms * 1e-3), "ms": ms,
                "frac_hbm": cb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                "tflops": chunked_flops(cfg) / (ms * 1e-3) / 1e12}

@@ -1723,9 +1723,23 @@ bool shape_ok(const Dims &d) {
            d.H < (1 << 30) && d.b < 65536 && d.nc < 65536 && d.G < 65536 && d.b * d.nc * d.G < (1ll << 31);
 }
 
+// The fused forward's output does not depend on the chunk length beyond
+// rounding (chunked and unchunked sums agree exactly in exact arithmetic),
+// so a 128-step chunk runs as two 64-step tiles: the tile configurations
+// hold a 64-step chunk's operands in TMEM and shared memory.
+Dims fwd_tiles(const Dims &d) {
+    Dims t = d;
+    if (d.Q == 128) {
+        t.Q = 64;
+        t.nc = d.nc * 2;
+    }
+    return t;
+}
+
 }  // namespace
 
-bool tc_fwd_supported(const Dims &d, ssd_dtype_t dtype) {
+bool tc_fwd_supported(const Dims &dq, ssd_dtype_t dtype) {
+    const Dims d = fwd_tiles(dq);
     if (dtype != SSD_DTYPE_BF16) return false;
     if (d.L == 0 || d.b == 0) return false;
     bool ok = false;
@@ -1736,15 +1750,17 @@ bool tc_fwd_supported(const Dims &d, ssd_dtype_t dtype) {
     return ok;
 }
 
-size_t tc_fwd_workspace(const Dims &d) {
+size_t tc_fwd_workspace(const Dims &dq) {
+    const Dims d = fwd_tiles(dq);
     size_t bytes = 0;
     dispatch(d, [&](auto c) { bytes = workspace_for<decltype(c)>(d); });
     return bytes;
 }
 
-cudaError_t tc_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B,
+cudaError_t tc_fwd(const Dims &dq, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B,
                    const void *C, const float *D, const float *init, void *y, float *fin, void *ws,
                    cudaStream_t s) {
+    const Dims d = fwd_tiles(dq);
     cudaError_t e = cudaErrorNotSupported;
     dispatch(d, [&](auto c) { e = run_fwd<decltype(c)>(d, ydtype, x, dt, A, B, C, D, init, y, fin, ws, s); });
     return e;
