@@ -96,8 +96,8 @@ struct Cfg {
     // image the MMAs read
     static constexpr int PACK_BYTES = CBM_BYTES + 2 * BC_BYTES;
     // vector set of one chunk (floats): per head [Q] arrays dt, cum, a-factor,
-    // epilogue factor; then per head the state rescale factor, the factor of
-    // the bf16 state copy, rho after the chunk; then two block flags
+    // epilogue factor; then per head the state rescale factor (applied twice),
+    // the factor of the bf16 state copy, rho after the chunk; then two block flags
     // (some head rescales, some head takes the wide path)
     static constexpr int V_DT = 0, V_CUM = HB * Q, V_AL = 2 * HB * Q, V_EF = 3 * HB * Q;
     static constexpr int V_F = 4 * HB * Q, V_SBF = V_F + HB, V_RHON = V_SBF + HB, V_FLAG = V_RHON + HB;
@@ -1125,9 +1125,16 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             for (int hh = 0; hh < C::HB; ++hh) {
                 const float lo = unkey(klo[hh]), hi = unkey(khi[hh]);
                 // rho stays while every exponent rho - cum_s stays within kLambda;
-                // else it moves to the middle of the chunk's range; a range wider
-                // than 2 kLambda centres the state at the chunk's end and leaves
-                // the intra-chunk term to the direct path
+                // else it moves to the lowest reference the chunk allows,
+                // hi - kLambda (rho then grows by the decay of each later chunk,
+                // so the lowest start keeps it longest before the next move);
+                // a range wider than 2 kLambda centres the state at the chunk's
+                // end and leaves the intra-chunk term to the direct path.
+                // The rescale exp(rc - rho) may fall below the fp32 range (rho
+                // up to kLambda, rc down to -kLambda) while the rescaled state
+                // does not: the state warps apply it as two factors
+                // f = exp((rc - rho) / 2).  sbf < 0: the bf16 copy is the
+                // rescaled state; else the old state times sbf.
                 float rc = rho[hh];
                 f[hh] = 1.f;
                 sbf[hh] = 1.f;
@@ -1135,13 +1142,15 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 if (rho[hh] - lo > kLambda || hi - rho[hh] > kLambda) {
                     rescale = true;
                     if (hi - lo <= 2.f * kLambda) {
-                        rc = 0.5f * (lo + hi);
-                        f[hh] = __expf(rc - rho[hh]);
-                        sbf[hh] = f[hh];
+                        rc = hi - kLambda;
+                        f[hh] = __expf(0.5f * (rc - rho[hh]));
+                        sbf[hh] = -1.f;
                     } else {
+                        // (after a decay of more than 2 kLambda the old state is
+                        // below fp32 resolution: f may flush to zero)
                         hw = true;
                         rc = T[hh];
-                        f[hh] = __expf(T[hh] - rho[hh]);
+                        f[hh] = __expf(0.5f * (T[hh] - rho[hh]));
                         sbf[hh] = __expf(-rho[hh]);
                     }
                 }
@@ -1286,7 +1295,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             if (gtid == 0) TRACE(7, it);
             tc_fence_after();
             const float *vv = vec(v);
-            const float f = vv[C::V_F + rh], sbf = vv[C::V_SBF + rh];
+            const float f = vv[C::V_F + rh], sbf = vv[C::V_SBF + rh];  // (f applied twice)
             const bool rescale = vv[C::V_FLAG] != 0.f;
             rho_end = vv[C::V_RHON + rh];
 #pragma unroll 1
@@ -1296,29 +1305,37 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 tmem_ld16(tmem + lane_off + C::COL_S + n0 + 16, v1);
                 tmem_ld_wait();
                 uint32_t w[16];
-                if (sbf == 1.f) {  // (uniform per warp: one head per warp)
+                // (sbf and f are uniform per warp: one head per warp)
+                if (sbf == 1.f) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         w[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
                         w[8 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
                     }
-                } else {
+                } else if (sbf > 0.f) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         w[j] = pack_bf16x2(v0[2 * j] * sbf, v0[2 * j + 1] * sbf);
                         w[8 + j] = pack_bf16x2(v1[2 * j] * sbf, v1[2 * j + 1] * sbf);
                     }
                 }
-                tmem_st16u(tmem + lane_off + C::COL_SB + sb * (C::N / 2) + n0 / 2, w);
                 if (rescale) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        v0[j] *= f;
-                        v1[j] *= f;
+                        v0[j] = (v0[j] * f) * f;
+                        v1[j] = (v1[j] * f) * f;
                     }
                     tmem_st16(tmem + lane_off + C::COL_S + n0, v0);
                     tmem_st16(tmem + lane_off + C::COL_S + n0 + 16, v1);
                 }
+                if (sbf < 0.f) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        w[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
+                        w[8 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
+                    }
+                }
+                tmem_st16u(tmem + lane_off + C::COL_SB + sb * (C::N / 2) + n0 / 2, w);
             }
             tmem_st_wait();
             tc_fence_before();

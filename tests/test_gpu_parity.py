@@ -143,6 +143,33 @@ def test_ssd_fwd_decay_regimes(ranges):
     check(to_np(y2), y_ref, TOL["bf16"], "decay regimes staged y")
 
 
+@pytest.mark.parametrize("ranges", [
+    # decays of 40..125 per chunk: every chunk (or every other) moves the
+    # state scale, by factors near the bottom of the fp32 range
+    (100.0, 115.0, 120.0, 125.0, 60.0, 90.0, 40.0, 80.0),
+])
+def test_ssd_fwd_carried_state_strong_decay(ranges):
+    """The state carried into a chunk, where it is most of the output: D = 0
+    and only the first 4 steps of every chunk compared.  A rescale that loses
+    the carried state (a factor flushed to zero) leaves errors of the size of
+    these outputs themselves, which the RMS of the whole output would hide.
+    The bound is relative to the largest of them: their values are heavy
+    tailed (some 20x their RMS), and the bf16 copy of the state used for the
+    inter-chunk term carries a 2^-9 relative rounding per entry."""
+    cfg = si.SSDConfig("tc_carry", 1, 1280, 8, 64, 128, 1, 64, "bf16", True, 92)
+    inp = decay_regime_inputs(cfg, ranges)
+    inp.D = np.zeros_like(inp.D)
+    t = gpu_inputs(inp)
+    y, fin = ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"], chunk_size=64)
+    y_ref, fin_ref = oracle_full(inp)
+    nc = cfg.seqlen // 64
+    head = lambda a: np.asarray(a).reshape(cfg.batch, nc, 64, cfg.nheads, cfg.headdim)[:, 1:, :4]
+    got, want = head(to_np(y)), head(y_ref)
+    e = float(np.max(np.abs(got - want)) / np.max(np.abs(want)))
+    assert e <= TOL["bf16"], f"carried state, first steps of each chunk: max|err| = {e:.3e} x max|y|"
+    check(to_np(fin), fin_ref, TOL["bf16"], "carried state final")
+
+
 @pytest.mark.parametrize("name", ["bf16_p64_n128", "bf16_p128_n256_q128", "tc_p64_n128_seg", "bf16_p128_n256_q64"])
 def test_ssd_fwd_bf16_output(name):
     cfg = SMALL[name]
