@@ -94,9 +94,11 @@ SSD_API int ssd_abi_version(void);
 
 /*
  * Bytes of device workspace ssd_fwd needs for `shape` (0 for an invalid
- * shape).  The workspace holds the per-segment states of the two-pass
- * chunk scan; it needs no initialisation and may be reused by later calls
- * on the same stream.
+ * shape).  The workspace holds a status word and ready flags, the per-chunk
+ * operand packs (masked C B^T with the chunk's B and C, bf16) and the
+ * per-segment states of the two-pass chunk scan; it needs no initialisation
+ * (every call clears what it reads) and may be reused by later calls on the
+ * same stream.
  */
 SSD_API size_t ssd_fwd_workspace_size(const ssd_shape_t *shape);
 
@@ -104,9 +106,12 @@ SSD_API size_t ssd_fwd_workspace_size(const ssd_shape_t *shape);
  * Fused SSD forward: y and final_state from x, dt, A, B, C, D, init_state.
  * The whole chunked algorithm -- cumulative decay, chunk states, the pass of
  * states between chunks, chunk outputs -- runs on the GPU with the state and
- * the intra-chunk score matrix kept on-chip; only per-segment states touch
- * the workspace.  `workspace` must hold ssd_fwd_workspace_size(shape) bytes
- * (SSD_ERR_WORKSPACE otherwise).  D, init_state, final_state may be NULL.
+ * the intra-chunk score matrix kept on-chip; only per-segment states and the
+ * per-chunk operand packs touch the workspace.  `workspace` must hold
+ * ssd_fwd_workspace_size(shape) bytes (SSD_ERR_WORKSPACE otherwise).  D,
+ * init_state, final_state may be NULL.  The result does not depend on
+ * chunk_size beyond rounding (a chunked sum is exact in any blocking): on the
+ * tensor-core path a chunk of 128 steps runs as two 64-step tiles.
  */
 SSD_API ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void *dt,
                      const float *A, const void *B, const void *C,
