@@ -181,6 +181,30 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+# Multi-rank host logic (replicas: every rank its own batch, no data-path
+# collective).  Plain functions so that they run under gloo on CPU as well.
+def rank_config(cfg, rank):
+    """Each rank draws its own batch: the same shapes, a seed offset by rank."""
+    return cfg.replace(seed=cfg.seed + 7919 * rank)
+
+
+def max_over_ranks(x, world, device=None):
+    """Largest value over the ranks (the slowest rank's time); x on one rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank, world, ms):
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def run_reference(args):
     """The fp64 CPU oracle timed on this host's cores: each step runs the
     recurrence over a bounded sample of heads of the workload, scaled to
@@ -278,7 +302,7 @@ def main():
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
 
     cfg = si.CONFIGS[args.workload]
-    cfg_rank = cfg.replace(seed=cfg.seed + 7919 * rank)
+    cfg_rank = rank_config(cfg, rank)
     inp = si.make_inputs(cfg_rank)
     t = inp.to_torch(dev)
     y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
@@ -314,11 +338,7 @@ def main():
         barrier()
         wall = time.perf_counter() - wall0
     step_ms = [s.elapsed_time(e) for s, e in evs]
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        tm = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     launches_per_step = None
 
     # per-launch device times (separate pass, events between the launches)
@@ -340,7 +360,7 @@ def main():
     dom_bytes = KERNEL_BYTES(cfg, dom_name)
     achieved = dom_bytes / (launch_ms[dom] * 1e-3) / 1e9
     tokens = cfg.tokens
-    value = world * tokens / (ms * 1e-3)
+    value = job_tokens_per_s(tokens, world, ms)
 
     # end-to-end through the C ABI with host buffers: H2D inputs, call, D2H outputs
     h = inp.to_torch("cpu", pin_memory=True)
@@ -367,11 +387,7 @@ def main():
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        tm = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tm, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tm.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     sweep = {}
     if not args.no_sweep and rank == 0:
@@ -401,7 +417,7 @@ def main():
                             "achieved_gbs": cbytes / (ms * 1e-3) / 1e9,
                             "frac_hbm": cbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                             "achieved_tflops": chunked_flops(cfg) / (ms * 1e-3) / 1e12},
-            "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "wall_s_timed_region": wall,
             "sm_count": nsm,
