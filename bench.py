@@ -362,32 +362,17 @@ def main():
     tokens = cfg.tokens
     value = job_tokens_per_s(tokens, world, ms)
 
-    # end-to-end through the C ABI with host buffers: H2D inputs, call, D2H outputs
+    # end-to-end through the C ABI with host buffers: every step copies its
+    # inputs in from pinned host memory, calls ssd_fwd, and reads y and the
+    # final state back.  Serial: one stream.  Pipelined: double buffers on
+    # three streams, so step i+1's copies in and step i-1's copies out overlap
+    # step i's kernels (the copy engines and the SMs work side by side).
     h = inp.to_torch("cpu", pin_memory=True)
-    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
-    dbufs = {k: torch.empty_like(v, device=dev) for k, v in h.items() if v is not None}
     h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
-    d2h = y_h.numel() * y_h.element_size() + fin_h.numel() * fin_h.element_size()
-
-    def e2e_step():
-        for k, v in dbufs.items():
-            v.copy_(h[k], non_blocking=True)
-        ssd.ssd_fwd(dbufs["x"], dbufs["dt"], dbufs["A"], dbufs["B"], dbufs["C"], dbufs["D"],
-                    dbufs.get("init_state"), cfg.chunk_size, y=y, final_state=fin, workspace=ws)
-        y_h.copy_(y, non_blocking=True)
-        fin_h.copy_(fin, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
+    d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
+    e2e_serial_ms = max_over_ranks(e2e_serial(ssd, dev, h, y, fin, ws, cfg, args.steps), world, dev)
+    e2e_ms = max_over_ranks(e2e_pipelined(ssd, dev, h, y, fin, ws, cfg, args.steps), world, dev)
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     sweep = {}
     if not args.no_sweep and rank == 0:
@@ -418,7 +403,9 @@ def main():
                             "frac_hbm": cbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                             "achieved_tflops": chunked_flops(cfg) / (ms * 1e-3) / 1e12},
             "e2e": {"value": job_tokens_per_s(tokens, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "mode": "pipelined (double-buffered, 3 streams)",
+                    "serial_ms_per_step": e2e_serial_ms,
+                    "serial_value": job_tokens_per_s(tokens, world, e2e_serial_ms)},
             "wall_s_timed_region": wall,
             "sm_count": nsm,
             "sweep": sweep,
@@ -428,6 +415,84 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def e2e_serial(ssd, dev, h, y, fin, ws, cfg, steps):
+    """ms per step of copy in -> ssd_fwd -> copy out on one stream."""
+    import torch
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    d = {k: torch.empty_like(v, device=dev) for k, v in h.items() if v is not None}
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for k, v in d.items():
+            v.copy_(h[k], non_blocking=True)
+        ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d.get("init_state"), cfg.chunk_size,
+                    y=y, final_state=fin, workspace=ws)
+        y_h.copy_(y, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
+
+
+def e2e_pipelined(ssd, dev, h, y, fin, ws, cfg, steps):
+    """ms per step with two buffer sets: inputs of step i copied in on one
+    stream while step i-1 computes on a second and step i-2's outputs go out
+    on a third.  Every step still copies all its inputs in and its outputs
+    out; the timed region runs from the first copy in to the last copy out."""
+    import torch
+    s_in, s_c, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ins = [{k: torch.empty_like(v, device=dev) for k, v in h.items() if v is not None} for _ in range(2)]
+    ys = [y, torch.empty_like(y)]
+    fins = [fin, torch.empty_like(fin)]
+    y_h = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
+    fin_h = [torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True) for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_c = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        for i in range(n):
+            j = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_c[j])    # step i-2 no longer reads input set j
+            with torch.cuda.stream(s_in):
+                for k, v in ins[j].items():
+                    v.copy_(h[k], non_blocking=True)
+                ev_in[j].record(s_in)
+            s_c.wait_event(ev_in[j])
+            if i >= 2:
+                s_c.wait_event(ev_out[j])   # step i-2's outputs have been read back
+            with torch.cuda.stream(s_c):
+                d = ins[j]
+                ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d.get("init_state"), cfg.chunk_size,
+                            y=ys[j], final_state=fins[j], workspace=ws)
+                ev_c[j].record(s_c)
+            s_out.wait_event(ev_c[j])
+            with torch.cuda.stream(s_out):
+                y_h[j].copy_(ys[j], non_blocking=True)
+                fin_h[j].copy_(fins[j], non_blocking=True)
+                ev_out[j].record(s_out)
+
+    run(3)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    run(steps)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / steps
 
 
 def tc_plan(cfg, target_ctas=148):
