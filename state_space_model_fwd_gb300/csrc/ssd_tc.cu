@@ -60,16 +60,14 @@ struct TcParams {
     const float *A, *D, *init;
     void *y;
     float *fin;
-    float *seg_state;   // [b, nseg, H, P, N]: segment-local states, then (in place) states entering segments 1..
+    float *seg_state;   // [b, nseg, H, P, N]: segment-local states (each segment from a zero state)
     float *seg_tot;     // [b, H, nseg]  total dt*A of each segment (may be null)
     const float *cum_in;    // [b, H, nc, Q] given in-chunk cumulative decay (null: computed from dt, A)
     const float *entering;  // [b, nseg, H, P, N] state entering each segment (null: init / seg_state)
     unsigned *status;   // bit 0: a wait gave up (may be null)
-    unsigned *counters; // [b, nhb] finished segment CTAs (seg_state_kernel, with seg_pass)
     long long b, L, H, G;
     int hpg, nc, nseg, cps;  // cps: chunks per segment
     int nhb;
-    int seg_pass;
     int dt_tma;  // dt has a TMA map (H % 8 == 0): the vector warps take it from a TMA ring
     // [b, nc, G] set to 1 by the C B^T kernel once a matrix is in memory;
     // the chunk scan's TMA producer polls the flag of a chunk before loading
@@ -674,7 +672,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
     __shared__ volatile int slot[8];
-    __shared__ int last_sh;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = blockIdx.z, hblk = blockIdx.x, b = blockIdx.y;
@@ -832,7 +829,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         // segment state: TMEM lane r = row (head, p); each group of four
         // warps a quarter of the columns
         const long long hrow = h0 + rh;
-        bool stored = false;
         if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 1, gtid, NAB)) {
             tc_fence_after();
             float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + hrow) * C::P + rp) * C::N;
@@ -845,67 +841,6 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; j += 4)
                         __stcg(reinterpret_cast<float4 *>(dst + n0 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
-                }
-            }
-            stored = true;
-        }
-        // pass across segments, in place, by the last of the (nseg - 1) CTAs
-        // of this (batch, head block): slot k becomes the state entering
-        // segment k + 1 = exp(T_k) (state entering k) + local_k
-        if (prm.seg_pass && stored) {
-            __threadfence();
-            named_bar_sync(1, NAB);
-            if (gtid == 0) {
-                const unsigned done = atomicAdd(&prm.counters[(long long)b * prm.nhb + hblk], 1u);
-                last_sh = done == (unsigned)(prm.nseg - 2) ? 1 : 0;
-            }
-            named_bar_sync(1, NAB);
-            if (last_sh) {
-                __threadfence();
-                // 4 elements (float4) per thread at a time, two segments'
-                // loads issued before any of their results is used
-                constexpr int ROW4 = C::N / 4, E = C::M * ROW4;
-                const long long sstride = H * C::P * C::N;
-                float *base = prm.seg_state + (long long)b * prm.nseg * sstride;
-                for (int e0 = 0; e0 < E; e0 += 4 * NAB) {
-                    long long off[4];
-                    long long hh4[4];
-                    float4 acc[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int e = e0 + i * NAB + gtid;
-                        const int r = e / ROW4, n4 = e % ROW4;
-                        hh4[i] = e < E ? h0 + r / C::P : H;
-                        off[i] = (hh4[i] * C::P + r % C::P) * C::N + 4 * n4;
-                        acc[i] = (prm.init && hh4[i] < H)
-                                     ? __ldg(reinterpret_cast<const float4 *>(prm.init + b * sstride + off[i]))
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    for (int k0 = 0; k0 < prm.nseg - 1; k0 += 2) {
-                        float4 loc[2][4];
-                        float ex[2][4];
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const bool ok = k0 + kk < prm.nseg - 1 && hh4[i] < H;
-                                loc[kk][i] = ok ? __ldcg(reinterpret_cast<const float4 *>(base + (k0 + kk) * sstride + off[i]))
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                                ex[kk][i] = ok ? __ldcg(prm.seg_tot + ((long long)b * H + hh4[i]) * prm.nseg + k0 + kk) : 0.f;
-                            }
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                if (!(k0 + kk < prm.nseg - 1 && hh4[i] < H)) continue;
-                                const float x = expf(ex[kk][i]);
-                                acc[i].x = fmaf(x, acc[i].x, loc[kk][i].x);
-                                acc[i].y = fmaf(x, acc[i].y, loc[kk][i].y);
-                                acc[i].z = fmaf(x, acc[i].z, loc[kk][i].z);
-                                acc[i].w = fmaf(x, acc[i].w, loc[kk][i].w);
-                                __stcg(reinterpret_cast<float4 *>(base + (k0 + kk) * sstride + off[i]), acc[i]);
-                            }
-                    }
                 }
             }
         }
@@ -1007,7 +942,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // builders need only x, the MMAs only the pack
     __shared__ uint64_t full_bar[4], pfull_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV];
     __shared__ uint64_t afull_bar[NB], afree_bar[NB], rfull_bar[NB], rfree_bar[NB], sbfree_bar[NB];
-    __shared__ uint64_t rt_bar, sdone_bar, drain_bar;
+    __shared__ uint64_t rt_bar, sdone_bar, drain_bar, sinit_bar;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
     __shared__ volatile int slot[12];
@@ -1049,6 +984,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             mbar_init(&sbfree_bar[i], 1);
         }
         mbar_init(&rt_bar, 1);
+        mbar_init(&sinit_bar, kComputeWarps);  // the entering state is in Ss
         mbar_init(&sdone_bar, 1);
         mbar_init(&drain_bar, 1);
         for (int i = 0; i < 2; ++i) mbar_init(&dt_bar[i], 1);
@@ -1259,32 +1195,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const int gtid = tid - 128;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const long long hrow = h0 + rh;
-        // state entering the segment (rho = 0: Ss = S_in)
-        if (prm.dep_seg && seg > 0) griddep_wait();
-        {
-            const float *src = nullptr;
-            if (prm.entering)
-                src = prm.entering + ((((long long)b * prm.nseg + seg) * H + hrow) * C::P + rp) * C::N;
-            else if (seg > 0)
-                src = prm.seg_state + ((((long long)b * prm.nseg + (seg - 1)) * H + hrow) * C::P + rp) * C::N;
-            else if (prm.init)
-                src = prm.init + (((long long)b * H + hrow) * C::P + rp) * C::N;
-            if (hrow >= H) src = nullptr;
-#pragma unroll 1
-            for (int n0 = 0; n0 < C::N; n0 += 16) {
-                float v[16];
-#pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    const float4 a = src ? __ldcg(reinterpret_cast<const float4 *>(src + n0 + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    v[j] = a.x;
-                    v[j + 1] = a.y;
-                    v[j + 2] = a.z;
-                    v[j + 3] = a.w;
-                }
-                tmem_st16(tmem + lane_off + C::COL_S + n0, v);
-            }
-            tmem_st_wait();
+        // the compute warps write the state entering the segment into Ss
+        if (!group_wait(&sinit_bar, 0, &abort_sh, &slot[3], 1, gtid, 128)) {
+            // (abort: fall through; every wait below gives up at once)
         }
+        tc_fence_after();
         if (gtid == 0) TRACE(13, 1);
         float rho_end = 0.f;
         for (int it = 0; it < nch; ++it) {
@@ -1348,7 +1263,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         // final state after the segment's last chunk: S = exp(-rho) Ss
         if (seg == prm.nseg - 1 && prm.fin) {  // (a uniform test: group_wait handles an abort)
-            if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[3], 1, gtid, 128)) {
+            if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[9], 1, gtid, 128)) {
                 tc_fence_after();
                 const float sc = __expf(-rho_end);
                 float *dst = prm.fin + (((long long)b * H + hrow) * C::P + rp) * C::N;
@@ -1381,6 +1296,91 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         YT *yg = reinterpret_cast<YT *>(prm.y) +
                  (((long long)b * prm.L + (long long)c0 * C::Q + part * NS) * H + (hrow < H ? hrow : 0)) * C::P + rp;
         const bool live = hrow < H;
+        // The state entering the segment (rho = 0: Ss = S_in), this warp's
+        // quarter of the columns.  After segment 0 it is the pass across the
+        // earlier segments' local states L_j (each from a zero state) and
+        // totals T_j:
+        //   S_in = e^{T_0 + .. + T_{k-1}} init + sum_j e^{T_{j+1} + .. + T_{k-1}} L_j
+        {
+            if (prm.dep_seg && seg > 0) griddep_wait();
+            const bool live = hrow < H;
+            const float *src = nullptr;  // a ready state (given, or init for segment 0)
+            const float *ini = nullptr;  // init, weighted, in the pass
+            const long long rowoff = (((long long)b * H + (live ? hrow : 0)) * C::P + rp) * C::N;
+            if (prm.entering)
+                src = prm.entering + ((((long long)b * prm.nseg + seg) * H + (live ? hrow : 0)) * C::P + rp) * C::N;
+            else if (seg == 0)
+                src = prm.init ? prm.init + rowoff : nullptr;
+            else if (prm.init)
+                ini = prm.init + rowoff;
+            const bool pass = !prm.entering && seg > 0;
+            const long long sstride = H * C::P * C::N;
+            const float *loc =
+                pass ? prm.seg_state + ((((long long)b * prm.nseg) * H + (live ? hrow : 0)) * C::P + rp) * C::N : nullptr;
+            const float *tot = pass ? prm.seg_tot + ((long long)b * H + (live ? hrow : 0)) * prm.nseg : nullptr;
+            float ttot = 0.f;  // T_0 + .. + T_{k-1}
+            if (pass && live)
+                for (int j = 0; j < seg; ++j) ttot += __ldcg(tot + j);
+            constexpr int NCOL = C::N / 4;  // this warp's columns
+#pragma unroll 1
+            for (int n0 = part * NCOL; n0 < (part + 1) * NCOL; n0 += 16) {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                if (live && src) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(src + n0 + j));
+                        v[j] = a4.x;
+                        v[j + 1] = a4.y;
+                        v[j + 2] = a4.z;
+                        v[j + 3] = a4.w;
+                    }
+                }
+                if (live && pass) {
+                    if (ini) {
+                        const float wi = __expf(ttot);
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 a4 = __ldg(reinterpret_cast<const float4 *>(ini + n0 + j));
+                            v[j] = wi * a4.x;
+                            v[j + 1] = wi * a4.y;
+                            v[j + 2] = wi * a4.z;
+                            v[j + 3] = wi * a4.w;
+                        }
+                    }
+                    // two segments' loads in flight before either is used
+                    float pre = 0.f;  // T_0 + .. + T_j
+                    for (int k = 0; k < seg; k += 2) {
+                        const bool two = k + 1 < seg;
+                        float4 l0[4], l1[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            l0[j] = __ldcg(reinterpret_cast<const float4 *>(loc + k * sstride + n0 + 4 * j));
+                            l1[j] = two ? __ldcg(reinterpret_cast<const float4 *>(loc + (k + 1) * sstride + n0 + 4 * j))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        const float t0 = __ldcg(tot + k), t1 = two ? __ldcg(tot + k + 1) : 0.f;
+                        pre += t0;
+                        const float w0 = __expf(ttot - pre);
+                        pre += t1;
+                        const float w1 = two ? __expf(ttot - pre) : 0.f;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            v[4 * j] = fmaf(w1, l1[j].x, fmaf(w0, l0[j].x, v[4 * j]));
+                            v[4 * j + 1] = fmaf(w1, l1[j].y, fmaf(w0, l0[j].y, v[4 * j + 1]));
+                            v[4 * j + 2] = fmaf(w1, l1[j].z, fmaf(w0, l0[j].z, v[4 * j + 2]));
+                            v[4 * j + 3] = fmaf(w1, l1[j].w, fmaf(w0, l0[j].w, v[4 * j + 3]));
+                        }
+                    }
+                }
+                tmem_st16(tmem + lane_off + C::COL_S + n0, v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sinit_bar);
+        }
         uint32_t xprev[NS / 2];
         bool wide_prev = false;
         for (int c = 0; c <= nch; ++c) {
@@ -1555,20 +1555,15 @@ size_t pack_bytes(const Dims &d) {
     return align256((size_t)C::PACK_BYTES * d.b * d.nc * d.G);
 }
 
-// Workspace: header (status word, segment counters, chunk-pack ready flags)
-// | chunk packs | segment states | segment totals.  The header is cleared on
-// the stream by every call.
+// Workspace: header (status word, chunk-pack ready flags) | chunk packs |
+// segment states | segment totals.  The header is cleared on the stream by
+// every call.
 size_t flag_bytes(const Dims &d) { return align256(sizeof(unsigned) * d.b * d.nc * d.G); }
 
-// header: status word | segment counters [b, nhb] | C B^T ready flags [b, nc, G]
-template <class C>
-size_t counter_bytes(const Dims &d) {
-    return align256(sizeof(unsigned) * d.b * ((d.H + C::HB - 1) / C::HB));
-}
-
+// header: status word | C B^T ready flags [b, nc, G]
 template <class C>
 size_t header_bytes(const Dims &d) {
-    return 256 + counter_bytes<C>(d) + flag_bytes(d);
+    return 256 + flag_bytes(d);
 }
 
 #ifdef SSD_TRACE
@@ -1694,8 +1689,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     char *w = static_cast<char *>(ws);
     const size_t hdr = header_bytes<C>(d);
     prm.status = reinterpret_cast<unsigned *>(w);
-    prm.counters = reinterpret_cast<unsigned *>(w + 256);
-    prm.cb_ready = reinterpret_cast<unsigned *>(w + 256 + counter_bytes<C>(d));
+    prm.cb_ready = reinterpret_cast<unsigned *>(w + 256);
     uint8_t *pack = reinterpret_cast<uint8_t *>(w + hdr);
     prm.pack = pack;
     const size_t seg_off = hdr + pack_bytes<C>(d);
@@ -1706,7 +1700,6 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     prm.nhb = p.nhb;
     prm.nseg = p.nseg;
     prm.cps = p.cps;
-    prm.seg_pass = 1;
 #ifdef SSD_TRACE
     prm.trace = reinterpret_cast<long long *>(w + workspace_for<C>(d) - kTraceBytes);
 #endif
