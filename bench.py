@@ -523,7 +523,10 @@ def KERNEL_BYTES(cfg, name):
     init = b * H * P * N * 4 if cfg.has_init else 0
     fin = b * H * P * N * 4
     nseg, cps, nt = tc_plan(cfg)
-    seg_states = b * (nseg - 1) * H * P * N * 4
+    one_seg = b * H * P * N * 4  # one segment state of every (batch, head)
+    seg_states = (nseg - 1) * one_seg
+    # segment k's entering state combines the k earlier segments' local states
+    seg_reads = one_seg * nseg * (nseg - 1) // 2
     covered = min(nt, (nseg - 1) * cps) / nt  # share of the sequence the segment-state kernel reads
     # chunk packs: masked C B^T (bf16, 64-step tiles) with the tile's B and C
     pack = b * nt * G * 64 * 64 * 2 + 2 * bc
@@ -533,12 +536,13 @@ def KERNEL_BYTES(cfg, name):
         "state_passing": st + cum + init + st + fin,
         "chunk_scan_simt": x + dt + 2 * bc + cum + st + y,
         # fused tensor-core path: chunk packs (read B, C; write the packs),
-        # segment states (with the pass across segments: every segment state
-        # written, read back and rewritten in place), chunk scan (reads every
-        # pack once per (batch, chunk, group) as its B, C and C B^T input)
+        # segment-local states (written once), chunk scan (reads every pack
+        # once per (batch, chunk, group) as its B, C and C B^T input, and the
+        # earlier segments' local states and the initial state for the state
+        # entering each segment)
         "cb_mask_tc": 2 * bc + pack,
-        "seg_state_tc": covered * (x + dt + bc) + 3 * seg_states + (init if nseg > 1 else 0),
-        "chunk_scan_tc": x + dt + pack + seg_states + init + y + fin,
+        "seg_state_tc": covered * (x + dt + bc) + seg_states,
+        "chunk_scan_tc": x + dt + pack + seg_reads + nseg * init + y + fin,
     }.get(name, compulsory_bytes(cfg))
 
 
