@@ -21,17 +21,19 @@
 // CB = C B^T masked to s <= t does not depend on the head: it is computed
 // once per chunk and group (cb_mask_kernel) and read by every head block
 // that shares the group, as the B operand of the intra-chunk contraction.
-// rho moves only when an exponent would leave [-kLambda, kLambda] (Ss is
-// then rescaled in TMEM); a chunk whose own decay range exceeds 2 kLambda
-// takes a direct per-entry path for its intra-chunk term.
+// rho moves (to a per-chunk reference rc, with a_s and y_t taken relative to
+// rc) only when an exponent would leave [-kLambda, kLambda]; Ss is then
+// rescaled in TMEM.  A chunk whose own decay range exceeds 2 kLambda takes a
+// direct per-entry path for its intra-chunk term.
 //
 // The fused forward is three launches:
 //   cb_mask_kernel     CB of every (chunk, group), bf16
 //   seg_state_kernel   the local state of each segment (a run of consecutive
-//                      chunks) but the last, one long-K contraction per
-//                      segment; the last CTA of each (batch, head block)
-//                      passes the states across the segments
-//   chunk_scan_kernel  every segment: the scaled state chain and the outputs
+//                      chunks, from a zero state) but the last, one long-K
+//                      contraction per segment, and its total decay
+//   chunk_scan_kernel  every segment: the state entering it (the pass across
+//                      the earlier segments' local states), then the scaled
+//                      state chain and the outputs
 //
 // Tiles: a CTA owns HB heads of one group with HB * P = 128, so every
 // state-shaped contraction has M = 128 rows (head, p) and TMEM lane r holds
@@ -643,14 +645,14 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
 }
 
 // ===========================================================================
-// Segment-local states (segments 0 .. nseg-2):
+// Segment-local states (segments 0 .. nseg-2, each from a zero state):
 //   S_seg = sum_t exp(sum_{k>t, k in segment} dt_k A) dt_t x_t^T B_t
 //   warp 0      : TMA loads of the x and B tiles
 //   warp 1      : tcgen05.mma S += A^T B, A read from TMEM
-//   warp 2      : dt and the segment weights (a ring of vector sets)
-//   warps 4-11  : the A operand (weights x x, bf16 hi + lo) into TMEM, two
-//                 buffers; then the state to HBM and, in the last CTA of a
-//                 (batch, head block), the pass across segments
+//   warps 2, 3  : dt and the segment weights of one head each (a ring of
+//                 vector sets), and the segment's total decay
+//   warps 4-19  : the A operand (weights x x, bf16 hi + lo) into TMEM, three
+//                 buffers; then the state to HBM
 // ===========================================================================
 constexpr int kSegThreads = 640;
 constexpr int kSegABWarps = (kSegThreads - 128) / 32;  // warps 4..19
@@ -919,11 +921,13 @@ __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) {
 //                warps are done with Ss);  R = A CB^T;  R += SB C^T
 //   warp 2     : dt, cumulative decay, rho, the A factors and output
 //                factors (a ring of vector sets)
-//   warps 4-7  : state: Ss rescale when rho moves, and its bf16 copy SB
-//                (the A operand of the inter-chunk term)
-//   warps 8-23 : compute, a quarter of the steps each: chunk c's A operand
-//                into TMEM from the staged x (kept in registers), then
-//                chunk c - 1's output y = factor R + D x to global memory
+//   warps 4-7  : state: Ss rescale when the reference moves, and its bf16
+//                copy SB (the A operand of the inter-chunk term)
+//   warps 8-23 : compute, a quarter of the steps each: first the state
+//                entering the segment into Ss (a quarter of the columns
+//                each); then per chunk c the A operand into TMEM from the
+//                staged x (kept in registers), and chunk c - 1's output
+//                y = factor R + D x to global memory
 // ===========================================================================
 constexpr int kScanThreads = 768;
 constexpr int kComputeWarps = 16;  // warps 8..23
