@@ -94,6 +94,17 @@ def load_peaks():
 # ---------------------------------------------------------------------------
 # clocks sampler (nvidia-smi during the timed region)
 # ---------------------------------------------------------------------------
+def smi_gpu_id(local_rank):
+    """nvidia-smi's id of this rank's GPU: CUDA numbers the visible devices
+    from 0, nvidia-smi names the physical ones (index or UUID), so a
+    CUDA_VISIBLE_DEVICES list maps one onto the other."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    if 0 <= local_rank < len(ids):
+        return ids[local_rank]
+    return str(local_rank)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -327,7 +338,7 @@ def main():
         step()
     barrier()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(smi_gpu_id(local_rank)) as clk:
         barrier()
         wall0 = time.perf_counter()
         for s, e in evs:

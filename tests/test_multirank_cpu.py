@@ -53,3 +53,12 @@ def test_two_ranks_gloo():
 def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.job_tokens_per_s(1000, 1, 1.0) == pytest.approx(1e6)
+
+
+def test_clock_sampler_names_the_physical_gpu(monkeypatch):
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
+    assert bench.smi_gpu_id(0) == "0" and bench.smi_gpu_id(3) == "3"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "4,6")
+    assert bench.smi_gpu_id(0) == "4" and bench.smi_gpu_id(1) == "6"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-abc, GPU-def")
+    assert bench.smi_gpu_id(1) == "GPU-def"
