@@ -128,3 +128,26 @@ def test_python_binding_refuses_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(ImportError):
         ssd.load_library(str(tmp_path / "libssd.so"))
+
+
+def _a256(v):
+    return (v + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("name", ["mamba2_130m", "mamba2_2p7b", "long_16k", "wide_head", "wide_head_q128"])
+def test_workspace_layout_of_the_tensor_core_path(lib, name):
+    """ssd_fwd's workspace on the bf16 tensor-core path: a header (status word,
+    one ready flag per chunk pack), the chunk packs (masked C B^T of a 64-step
+    tile and the tile's B and C, bf16), and, when the sequence is cut into
+    segments, the segment states (fp32) and the segment totals."""
+    import ssd_inputs as si
+    import bench
+    cfg = si.CONFIGS[name]
+    s = ssd.ssd_shape_t(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups,
+                        cfg.chunk_size, 1, 1)
+    b, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
+    nseg, _, nt = bench.tc_plan(cfg)
+    want = 256 + _a256(4 * b * nt * G) + _a256(b * nt * G * (64 * 64 * 2 + 2 * 64 * N * 2))
+    if nseg > 1:
+        want += _a256(4 * b * nseg * H * P * N) + _a256(4 * b * nseg * H)
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(s)) == want
