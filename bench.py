@@ -263,13 +263,11 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(cfg, inp, budget_s=20.0):
-    """Oracle time on this host for a bounded sample of heads, scaled."""
+def oracle_sample_time(cfg, f, budget_s):
+    """Seconds the oracle takes over the whole workload, from a sample of
+    heads grown (x4) while it fits the budget, scaled by the heads."""
     import oracle
-    oracle.build()
-    f = inp.as_f64()
     nh = 1
-    t_one = None
     while True:
         g_of = [h * cfg.ngroups // cfg.nheads for h in range(nh)]
         t0 = time.perf_counter()
@@ -280,10 +278,27 @@ def cpu_baseline(cfg, inp, budget_s=20.0):
         if t_one * 4 > budget_s or nh == cfg.nheads:
             break
         nh = min(cfg.nheads, nh * 4)
-    t_full = t_one * cfg.nheads / nh
-    return {"value": cfg.tokens / t_full, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+    return t_one * cfg.nheads / nh, nh, t_one
+
+
+def cpu_baseline(cfg, inp, budget_s=12.0):
+    """Oracle time on this host for a bounded sample of heads, scaled: on
+    every core (OpenMP over batch, head, channel) and on one core."""
+    import oracle
+    oracle.build()
+    f = inp.as_f64()
+    cores = oracle.num_threads()
+    t_full, nh, t_one = oracle_sample_time(cfg, f, budget_s)
+    oracle.set_num_threads(1)
+    try:
+        t1_full, nh1, t1_one = oracle_sample_time(cfg, f, budget_s / 2)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": cfg.tokens / t_full, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"fp64 recurrence over {nh} of {cfg.nheads} heads (all batches, all {cfg.seqlen} steps), "
-                      f"{t_one:.2f} s, scaled by {cfg.nheads}/{nh}"}
+                      f"{t_one:.2f} s, scaled by {cfg.nheads}/{nh}",
+            "one_core": {"value": cfg.tokens / t1_full, "unit": "tokens/s", "cores": 1,
+                         "sample": f"{nh1} of {cfg.nheads} heads, {t1_one:.2f} s, scaled by {cfg.nheads}/{nh1}"}}
 
 
 def main():
@@ -368,8 +383,12 @@ def main():
     peaks = load_peaks()
     cbytes = compulsory_bytes(cfg)
     dom_name = kernel_names[dom] if dom < len(kernel_names) else f"launch{dom}"
+    # achieved: the operation's compulsory bytes (reads of x, dt, B, C, A, D,
+    # init; writes of y, final state) over the dominant kernel's time; the
+    # bytes the kernel itself moves (its own intermediates included) are
+    # reported beside it
+    achieved = cbytes / (launch_ms[dom] * 1e-3) / 1e9
     dom_bytes = KERNEL_BYTES(cfg, dom_name)
-    achieved = dom_bytes / (launch_ms[dom] * 1e-3) / 1e9
     tokens = cfg.tokens
     value = job_tokens_per_s(tokens, world, ms)
 
@@ -387,7 +406,9 @@ def main():
 
     sweep = {}
     if not args.no_sweep and rank == 0:
-        sweep = run_sweep(ssd, dev, flush, peaks)
+        with ClockSampler(smi_gpu_id(local_rank)) as clk_sweep:
+            sweep = run_sweep(ssd, dev, flush, peaks)
+        sweep["clocks"] = clk_sweep.summary()
 
     if rank == 0:
         clocks = clk.summary()
@@ -408,7 +429,10 @@ def main():
                           for i, v in enumerate(launch_ms)},
             "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "algorithmic_bytes": dom_bytes, "peak_source": peaks["source"]},
+                         "algorithmic_bytes": cbytes, "kernel_ms": launch_ms[dom],
+                         "kernel_bytes": dom_bytes,
+                         "kernel_bytes_frac": dom_bytes / (launch_ms[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         "peak_source": peaks["source"]},
             "op_roofline": {"compulsory_bytes": cbytes, "flops": chunked_flops(cfg),
                             "achieved_gbs": cbytes / (ms * 1e-3) / 1e9,
                             "frac_hbm": cbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -506,10 +530,11 @@ def e2e_pipelined(ssd, dev, h, y, fin, ws, cfg, steps):
     return e0.elapsed_time(e1) / steps
 
 
-def tc_plan(cfg, target_ctas=148):
+def tc_plan(cfg, target_ctas=152):
     """Segment plan of the fused tensor-core path (mirrors the library):
     CTAs own 128/P heads; segments of consecutive 64-step tiles (a 128-step
-    chunk is two of them) fill ~148 CTAs."""
+    chunk is two of them) fill about one CTA per SM (target_ctas = the SM
+    count)."""
     hb = 128 // cfg.headdim
     nhb = -(-cfg.nheads // hb)
     units = cfg.batch * nhb
@@ -578,20 +603,75 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
 
         ms = time_device(run, flush, steps)
         cb = compulsory_bytes(cfg)
+        kernels = kernel_times(ssd, run, flush, steps)
+        dom = max(kernels, key=kernels.get)
         rec = {"tokens_per_s": cfg.tokens / (ms * 1e-3), "ms": ms,
                "frac_hbm": cb / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-               "tflops": chunked_flops(cfg) / (ms * 1e-3) / 1e12}
+               "tflops": chunked_flops(cfg) / (ms * 1e-3) / 1e12,
+               "launch_ms": {k: round(v, 5) for k, v in kernels.items()},
+               "dominant_kernel": dom,
+               "dominant_kernel_frac_hbm": cb / (kernels[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         if name == "long_16k":
             def scan():
                 ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
                                        y=y, final_state=fin)
             sms = time_device(scan, flush, 3)
+            scan_flops = 5.0 * cfg.tokens * cfg.nheads * cfg.headdim * cfg.dstate
+            ffma = ffma_peak_tflops(dev)
             rec["selective_scan_ms"] = sms
+            rec["selective_scan_roofline"] = {
+                "bound": "alu", "achieved": scan_flops / (sms * 1e-3) / 1e12, "peak": ffma, "unit": "TFLOP/s",
+                "frac": scan_flops / (sms * 1e-3) / 1e12 / ffma,
+                "flops": scan_flops, "flops_model": "5 fp32 flops per (token, head, p, n): decay, input, output",
+                "peak_source": "measured: cuBLAS SGEMM 8192^3 with TF32 off (FFMA), best of 5"}
             rec["chunked_vs_sequential_speedup"] = sms / ms
         out[name] = rec
         del t, y, fin, ws
         torch.cuda.empty_cache()
     return out
+
+
+def kernel_times(ssd, fn, flush, steps):
+    """Mean device time of each kernel launch of one call (library launch
+    timing: events between the launches)."""
+    import torch
+    ssd.launch_timing(True)
+    runs = []
+    for _ in range(max(3, steps)):
+        flush.zero_()
+        fn()
+        runs.append(ssd.launch_times_ms())
+    ssd.launch_timing(False)
+    torch.cuda.synchronize()
+    names = [n for n, _ in runs[-1]]
+    return {n: statistics.mean(r[i][1] for r in runs) for i, n in enumerate(names)}
+
+
+def ffma_peak_tflops(dev):
+    """FP32 FFMA throughput of this GPU, measured: cuBLAS SGEMM with TF32
+    disabled runs on the FFMA pipes; best of 5 timed 8192^3 products."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(2):
+            torch.matmul(a, b, out=c)
+        best = None
+        for _ in range(5):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            torch.matmul(a, b, out=c)
+            e.record()
+            e.synchronize()
+            ms = s.elapsed_time(e)
+            best = ms if best is None else min(best, ms)
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
 
 
 def time_device(fn, flush, steps):

@@ -40,7 +40,10 @@
  * Execution: calls are asynchronous on `stream` (0 = legacy default stream).
  * Errors: argument errors are detected on the host and returned before
  * anything is enqueued (SSD_ERR_INVALID_ARG / SSD_ERR_UNSUPPORTED);
- * a failed launch returns SSD_ERR_CUDA.  No entry point synchronises.
+ * a failed launch returns SSD_ERR_CUDA.  Failures the kernels detect while
+ * they run (a bounded wait that gave up) cannot be returned by the call that
+ * enqueued them: they are latched in a per-device status word that
+ * ssd_get_device_status() reads.  No entry point but that one synchronises.
  * Supported on the GPU: chunk_size 64 or 128, L % chunk_size == 0,
  * H % G == 0, P in {16, 32, 64, 128}, N in {16, 32, 64, 128, 256}.
  * Outputs are bitwise reproducible run to run: no floating-point atomics.
@@ -68,7 +71,8 @@ typedef enum {
     SSD_ERR_UNSUPPORTED = 2,   /* valid shape this build does not run */
     SSD_ERR_CUDA = 3,          /* a CUDA launch or query failed */
     SSD_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
-    SSD_ERR_SCRATCH_LIMIT = 5  /* ssd_fwd_noalloc: shape needs more than its static scratch */
+    SSD_ERR_SCRATCH_LIMIT = 5, /* ssd_fwd_noalloc: shape needs more than its static scratch */
+    SSD_ERR_TIMEOUT = 6        /* a kernel's bounded wait gave up (read by ssd_get_device_status) */
 } ssd_status_t;
 
 typedef enum { SSD_DTYPE_F32 = 0, SSD_DTYPE_BF16 = 1 } ssd_dtype_t;
@@ -93,12 +97,30 @@ SSD_API const char *ssd_status_string(ssd_status_t status);
 SSD_API int ssd_abi_version(void);
 
 /*
- * Bytes of device workspace ssd_fwd needs for `shape` (0 for an invalid
- * shape).  The workspace holds a status word and ready flags, the per-chunk
- * operand packs (masked C B^T with the chunk's B and C, bf16) and the
- * per-segment states of the two-pass chunk scan; it needs no initialisation
- * (every call clears what it reads) and may be reused by later calls on the
- * same stream.
+ * Device-detected failures.  Every wait inside the tensor-core kernels is
+ * bounded in time; a wait that gives up (a producer that never arrives)
+ * makes its CTA drain its own copies and MMAs, free its tensor memory and
+ * exit, and latches SSD_ERR_TIMEOUT in a status word of the current device
+ * that every call of this library shares.  The outputs of the call that
+ * timed out are then incomplete.
+ * ssd_get_device_status(stream) waits for `stream` (cudaStreamSynchronize),
+ * reads the word and clears it: SSD_OK when no wait of any call on this
+ * device has given up since the previous read, SSD_ERR_TIMEOUT otherwise,
+ * SSD_ERR_CUDA when the stream or the read failed.  The word is sticky
+ * across calls and streams (like the CUDA runtime's sticky errors): to pin a
+ * failure on one call, read it before and after that call.
+ */
+SSD_API ssd_status_t ssd_get_device_status(cudaStream_t stream);
+
+/*
+ * Bytes of device workspace ssd_fwd needs for `shape` on the current
+ * device (0 for an invalid shape).  The workspace holds the ready flags and
+ * per-chunk operand packs (masked C B^T with the chunk's B and C, bf16) and
+ * the per-segment states of the two-pass chunk scan; how the sequence is cut
+ * into segments depends on the device's SM count, so query the size with the
+ * device current that will run the call.  It needs no initialisation (every
+ * call clears what it reads) and may be reused by later calls on the same
+ * stream.
  */
 SSD_API size_t ssd_fwd_workspace_size(const ssd_shape_t *shape);
 
@@ -132,11 +154,13 @@ SSD_API ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void
  * until the process exits).  Shapes whose ssd_fwd_workspace_size() exceeds
  * it return SSD_ERR_SCRATCH_LIMIT before anything is enqueued.  The call
  * itself allocates nothing: no cudaMalloc, no cudaFree.
- * The first call on each device looks up the buffer's device address
+ * The first call on each device (and the first after that device's context
+ * was destroyed and created again) looks up the buffer's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  Every call shares the one buffer: calls whose
  * GPU work overlaps (different streams, or several host threads) race on
- * it, so serialise them.  Inputs, outputs and errors as for ssd_fwd.
+ * it, so serialise them.  Inputs, outputs and errors as for ssd_fwd; a wait
+ * that gave up inside its kernels is read with ssd_get_device_status.
  */
 #define SSD_NOALLOC_SCRATCH_BYTES (16u << 20)
 SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, const void *dt,
@@ -188,7 +212,37 @@ SSD_API ssd_status_t ssd_state_passing(const ssd_shape_t *shape, const float *st
 SSD_API ssd_status_t ssd_chunk_scan(const ssd_shape_t *shape, const void *x,
                             const void *dt, const void *B, const void *C,
                             const float *dA_cumsum, const float *states_in,
-                            const float *D, void *y, cudaStream_t stream);
+                            const float *D, void *y, void *workspace,
+                            size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Bytes of device workspace ssd_chunk_scan needs for `shape` (0 for an
+ * invalid shape, and 0 where the call needs none; workspace may then be
+ * NULL).  On the bf16 tensor-core path it holds the per-chunk operand packs
+ * (masked C B^T with the chunk's B and C) and their ready flags; it needs no
+ * initialisation and may be reused by later calls on the same stream.
+ */
+SSD_API size_t ssd_chunk_scan_workspace_size(const ssd_shape_t *shape);
+
+/*
+ * Self-test of the failure path (the pages have no counterpart): enqueues
+ * the tensor-core chunk-scan stage kernel of ssd_chunk_scan alone, with its
+ * operand packs marked "not yet published" and no kernel that publishes
+ * them, so the wait of every CTA for its first pack runs out after
+ * `wait_ns` nanoseconds of wall time (clamped to [1e5, 1e9]).  Each CTA
+ * gives up before it loads any x tile or operand pack or issues any MMA,
+ * lets the loads it did issue (its dt boxes) land, frees its tensor memory
+ * and exits; SSD_ERR_TIMEOUT is latched for ssd_get_device_status.
+ * Arguments as for ssd_chunk_scan; y is left unwritten.  Returns
+ * SSD_ERR_UNSUPPORTED for shapes off the tensor-core path.  Nothing here
+ * faults, traps or hangs the GPU: the test of the bounded waits.
+ */
+SSD_API ssd_status_t ssd_selftest_scan_timeout(const ssd_shape_t *shape, const void *x,
+                                               const void *dt, const void *B, const void *C,
+                                               const float *dA_cumsum, const float *states_in,
+                                               const float *D, void *y, void *workspace,
+                                               size_t workspace_bytes, uint64_t wait_ns,
+                                               cudaStream_t stream);
 
 /*
  * The same recurrence as ssd_fwd, evaluated as a plain sequential scan over

@@ -23,13 +23,15 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libssd.so")
 
 SSD_OK = 0
+SSD_ERR_TIMEOUT = 6
 SSD_DTYPE_F32 = 0
 SSD_DTYPE_BF16 = 1
 
 EXPORTED = ("ssd_status_string", "ssd_abi_version", "ssd_fwd_workspace_size", "ssd_fwd",
             "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
             "selective_scan_fwd", "ssd_launch_timing_enable", "ssd_launch_timing_read",
-            "ssd_launch_timing_name", "ssd_fwd_noalloc")
+            "ssd_launch_timing_name", "ssd_fwd_noalloc", "ssd_chunk_scan_workspace_size",
+            "ssd_get_device_status", "ssd_selftest_scan_timeout")
 
 
 class ssd_shape_t(ctypes.Structure):
@@ -69,7 +71,11 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_chunk_cumsum.argtypes = [shp, vp, vp, vp, vp]
         lib.ssd_chunk_state.argtypes = [shp, vp, vp, vp, vp, vp, vp]
         lib.ssd_state_passing.argtypes = [shp, vp, vp, vp, vp, vp, vp]
-        lib.ssd_chunk_scan.argtypes = [shp] + [vp] * 8 + [vp]
+        lib.ssd_chunk_scan.argtypes = [shp] + [vp] * 9 + [sz, vp]
+        lib.ssd_chunk_scan_workspace_size.argtypes = [shp]
+        lib.ssd_chunk_scan_workspace_size.restype = sz
+        lib.ssd_selftest_scan_timeout.argtypes = [shp] + [vp] * 9 + [sz, ctypes.c_uint64, vp]
+        lib.ssd_get_device_status.argtypes = [vp]
         lib.selective_scan_fwd.argtypes = [shp] + [vp] * 9 + [vp]
         lib.ssd_launch_timing_enable.argtypes = [i32]
         lib.ssd_launch_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i32]
@@ -77,7 +83,9 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_launch_timing_name.restype = ctypes.c_char_p
         lib.ssd_fwd_noalloc.argtypes = [shp] + [vp] * 10
         lib.ssd_fwd_noalloc.restype = i32
-        for name in EXPORTED[3:-2]:
+        for name in ("ssd_fwd", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
+                     "selective_scan_fwd", "ssd_launch_timing_enable", "ssd_launch_timing_read",
+                     "ssd_fwd_noalloc", "ssd_get_device_status", "ssd_selftest_scan_timeout"):
             getattr(lib, name).restype = i32
         if path == LIB_PATH:
             _lib = lib
@@ -91,6 +99,19 @@ def status_string(status: int) -> str:
 def _check(fn: str, status: int):
     if status != SSD_OK:
         raise SSDError(fn, status, status_string(status))
+
+
+def get_device_status(stream=None) -> int:
+    """Wait for the stream, then read and clear the current device's status
+    word: SSD_OK, or SSD_ERR_TIMEOUT when a bounded wait inside any of this
+    library's kernels gave up since the previous read (the outputs of that
+    call are incomplete)."""
+    return int(load_library().ssd_get_device_status(_stream(stream)))
+
+
+def check_device_status(stream=None) -> None:
+    """get_device_status(), raising SSDError unless it is SSD_OK."""
+    _check("ssd_get_device_status", get_device_status(stream))
 
 
 def _ptr(t):
@@ -251,7 +272,7 @@ def ssd_state_passing(states, dA_cumsum, init_state=None, *, out=None, final_sta
 
 
 def ssd_chunk_scan(x, dt, B, C, dA_cumsum, states_in, D=None, *, out=None, y_dtype=torch.float32,
-                   stream=None):
+                   workspace=None, stream=None):
     lib = load_library()
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
@@ -270,10 +291,30 @@ def ssd_chunk_scan(x, dt, B, C, dA_cumsum, states_in, D=None, *, out=None, y_dty
         out = torch.empty(x.shape, device=x.device, dtype=y_dtype)
     _need(out, "y", y_dtype, x.shape)
     shape = make_shape(x, B, Q, y_dtype)
+    ws_bytes = int(lib.ssd_chunk_scan_workspace_size(ctypes.byref(shape)))
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, device=x.device, dtype=torch.uint8)
     _check("ssd_chunk_scan", lib.ssd_chunk_scan(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(B), _ptr(C),
                                                 _ptr(dA_cumsum), _ptr(states_in), _ptr(D), _ptr(out),
+                                                _ptr(workspace), 0 if workspace is None else workspace.numel(),
                                                 _stream(stream)))
     return out
+
+
+def selftest_scan_timeout(x, dt, B, C, dA_cumsum, states_in, D=None, *, out, wait_ns=2_000_000,
+                          stream=None) -> int:
+    """Failure-path self-test: the chunk-scan stage kernel alone with no
+    operand pack ever published, so its bounded wait gives up after
+    ``wait_ns``; returns the status of the enqueue (read the device status
+    with get_device_status afterwards)."""
+    lib = load_library()
+    Q = dA_cumsum.shape[-1]
+    shape = make_shape(x, B, Q, out.dtype)
+    ws_bytes = int(lib.ssd_chunk_scan_workspace_size(ctypes.byref(shape)))
+    workspace = torch.empty(max(ws_bytes, 16), device=x.device, dtype=torch.uint8)
+    return int(lib.ssd_selftest_scan_timeout(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(B), _ptr(C),
+                                             _ptr(dA_cumsum), _ptr(states_in), _ptr(D), _ptr(out),
+                                             _ptr(workspace), workspace.numel(), int(wait_ns), _stream(stream)))
 
 
 def selective_scan_fwd(x, dt, A, B, C, D=None, init_state=None, *, y=None, final_state=None,
@@ -311,6 +352,6 @@ def launch_times_ms() -> list:
     return [((lib.ssd_launch_timing_name(i) or b"?").decode(), float(buf[i])) for i in range(min(n, 16))]
 
 
-__all__ = ["ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
+__all__ = ["get_device_status", "check_device_status", "selftest_scan_timeout", "ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
            "ssd_state_passing", "ssd_chunk_scan", "selective_scan_fwd", "ssd_shape_t", "SSDError",
            "load_library", "status_string", "EXPORTED", "LIB_PATH"]

@@ -2,6 +2,7 @@
 // on the host, then kernel launches on the caller's stream.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -67,6 +68,74 @@ ssd_status_t from_cuda(cudaError_t e) {
 }
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------
+// Library-owned device words and buffers (file-scope __device__ symbols).
+// Host code holds only a host-side stand-in for such a symbol; the device
+// address comes from cudaGetSymbolAddress with the device current, looked up
+// once per (device, context): a context destroyed and created again
+// (cudaDeviceReset) maps the module anew at another address.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+CUcontext current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            (void)cudaGetLastError();
+            return (PFN_cuCtxGetCurrent_v4000) nullptr;
+        }
+        return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }();
+    CUcontext ctx = nullptr;
+    if (fn && fn(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    return ctx;
+}
+
+struct SymbolCache {
+    std::mutex m;
+    CUcontext ctx[kMaxDevices] = {};
+    void *ptr[kMaxDevices] = {};
+};
+
+template <typename Sym>
+cudaError_t symbol_address(const Sym &sym, SymbolCache &cache, void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(cache.m);
+    const CUcontext ctx = current_context();
+    if (!cache.ptr[dev] || !ctx || ctx != cache.ctx[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, sym);  // (makes the device's context current if none was)
+        if (e != cudaSuccess) return e;
+        cache.ptr[dev] = p;
+        cache.ctx[dev] = current_context();
+    }
+    *out = cache.ptr[dev];
+    return cudaSuccess;
+}
+
+// The device status word every kernel of this library latches failures into
+// (bit 0: a bounded wait gave up), and the word ssd_get_device_status
+// exchanges it into.
+static __device__ unsigned g_device_status;
+static __device__ unsigned g_device_status_read;
+SymbolCache g_status_cache, g_status_read_cache;
+
+cudaError_t device_status_word(unsigned **out) {
+    void *p = nullptr;
+    const cudaError_t e = symbol_address(g_device_status, g_status_cache, &p);
+    *out = static_cast<unsigned *>(p);
+    return e;
+}
+
+// Atomically take the status word (so no bit latched by a kernel on another
+// stream between a read and a clear is lost).
+__global__ void take_status_kernel(unsigned *word, unsigned *out) { *out = atomicExch(word, 0u); }
 
 // Workspace of the unfused (four-launch) path: cumsum, chunk states,
 // states entering chunks.
@@ -174,11 +243,12 @@ const char *ssd_status_string(ssd_status_t st) {
         case SSD_ERR_WORKSPACE: return "SSD_ERR_WORKSPACE: workspace missing or too small";
         case SSD_ERR_SCRATCH_LIMIT:
             return "SSD_ERR_SCRATCH_LIMIT: shape needs more scratch than ssd_fwd_noalloc's static buffer holds";
+        case SSD_ERR_TIMEOUT: return "SSD_ERR_TIMEOUT: a bounded wait inside a kernel gave up (outputs incomplete)";
     }
     return "SSD_ERR_UNKNOWN";
 }
 
-int ssd_abi_version(void) { return (1 << 16) | 0; }
+int ssd_abi_version(void) { return (2 << 16) | 0; }
 
 size_t ssd_fwd_workspace_size(const ssd_shape_t *shape) {
     Dims d;
@@ -202,9 +272,13 @@ ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void *dt, co
     const bool tc = ssd::tc_fwd_supported(d, shape->dtype);
     const size_t need = tc ? ssd::tc_fwd_workspace(d) : staged_workspace(d);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace))) return SSD_ERR_WORKSPACE;
-    if (tc)
+    if (tc) {
+        unsigned *status = nullptr;
+        const cudaError_t e = device_status_word(&status);
+        if (e != cudaSuccess) return from_cuda(e);
         return from_cuda(
-            ssd::tc_fwd(d, shape->ydtype, x, dt, A, B, C, D, init_state, y, final_state, workspace, stream));
+            ssd::tc_fwd(d, shape->ydtype, x, dt, A, B, C, D, init_state, y, final_state, workspace, status, stream));
+    }
     if (shape->dtype == SSD_DTYPE_F32)
         return fwd_staged<float, float>(d, x, dt, A, B, C, D, init_state, y, final_state, workspace, stream);
     if (shape->ydtype == SSD_DTYPE_F32)
@@ -231,8 +305,12 @@ ssd_status_t ssd_chunk_state(const ssd_shape_t *shape, const void *x, const void
     if (st != SSD_OK) return st;
     if (d.b == 0 || d.L == 0) return SSD_OK;
     if (!ptrs_ok({x, dt, B, dA_cumsum, states}, {})) return SSD_ERR_INVALID_ARG;
-    if (ssd::tc_stage_supported(d, shape->dtype))
-        return from_cuda(ssd::tc_chunk_state(d, x, dt, B, dA_cumsum, states, stream));
+    if (ssd::tc_stage_supported(d, shape->dtype)) {
+        unsigned *status = nullptr;
+        const cudaError_t e = device_status_word(&status);
+        if (e != cudaSuccess) return from_cuda(e);
+        return from_cuda(ssd::tc_chunk_state(d, x, dt, B, dA_cumsum, states, status, stream));
+    }
     if (shape->dtype == SSD_DTYPE_F32)
         return from_cuda(ssd::launch_chunk_state_simt<float>(d, static_cast<const float *>(x),
                                                              static_cast<const float *>(dt),
@@ -258,16 +336,36 @@ ssd_status_t ssd_state_passing(const ssd_shape_t *shape, const float *states, co
     return from_cuda(ssd::launch_state_passing(d, states, dA_cumsum, init_state, states_in, final_state, stream));
 }
 
-ssd_status_t ssd_chunk_scan(const ssd_shape_t *shape, const void *x, const void *dt, const void *B, const void *C,
-                            const float *dA_cumsum, const float *states_in, const float *D, void *y,
-                            cudaStream_t stream) {
+size_t ssd_chunk_scan_workspace_size(const ssd_shape_t *shape) {
+    Dims d;
+    if (check_shape(shape, true, &d) != SSD_OK) return 0;
+    if (ssd::tc_stage_supported(d, shape->dtype)) return ssd::tc_chunk_scan_workspace(d);
+    return 0;
+}
+
+}  // extern "C"
+
+namespace {
+// The chunk-scan stage, or (selftest_ns > 0) its failure-path self-test.
+ssd_status_t chunk_scan_call(const ssd_shape_t *shape, const void *x, const void *dt, const void *B, const void *C,
+                             const float *dA_cumsum, const float *states_in, const float *D, void *y,
+                             void *workspace, size_t workspace_bytes, uint64_t selftest_ns, cudaStream_t stream) {
     Dims d;
     ssd_status_t st = check_shape(shape, true, &d);
     if (st != SSD_OK) return st;
+    const bool tc = ssd::tc_stage_supported(d, shape->dtype);
+    if (selftest_ns > 0 && !tc) return SSD_ERR_UNSUPPORTED;
     if (d.b == 0 || d.L == 0) return SSD_OK;
     if (!ptrs_ok({x, dt, B, C, dA_cumsum, states_in, y}, {D})) return SSD_ERR_INVALID_ARG;
-    if (ssd::tc_stage_supported(d, shape->dtype))
-        return from_cuda(ssd::tc_chunk_scan(d, shape->ydtype, x, dt, B, C, dA_cumsum, states_in, D, y, stream));
+    if (tc) {
+        const size_t need = ssd::tc_chunk_scan_workspace(d);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return SSD_ERR_WORKSPACE;
+        unsigned *status = nullptr;
+        const cudaError_t e = device_status_word(&status);
+        if (e != cudaSuccess) return from_cuda(e);
+        return from_cuda(ssd::tc_chunk_scan(d, shape->ydtype, x, dt, B, C, dA_cumsum, states_in, D, y, workspace,
+                                            status, selftest_ns, stream));
+    }
     if (shape->dtype == SSD_DTYPE_F32)
         return from_cuda(ssd::launch_chunk_scan_simt<float, float>(
             d, static_cast<const float *>(x), static_cast<const float *>(dt), static_cast<const float *>(B),
@@ -279,6 +377,43 @@ ssd_status_t ssd_chunk_scan(const ssd_shape_t *shape, const void *x, const void 
                                                                   static_cast<float *>(y), stream));
     return from_cuda(ssd::launch_chunk_scan_simt<bf16, bf16>(d, xb, dtb, Bb, Cb, dA_cumsum, states_in, D,
                                                              static_cast<bf16 *>(y), stream));
+}
+}  // namespace
+
+extern "C" {
+
+ssd_status_t ssd_chunk_scan(const ssd_shape_t *shape, const void *x, const void *dt, const void *B, const void *C,
+                            const float *dA_cumsum, const float *states_in, const float *D, void *y,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return chunk_scan_call(shape, x, dt, B, C, dA_cumsum, states_in, D, y, workspace, workspace_bytes, 0, stream);
+}
+
+ssd_status_t ssd_selftest_scan_timeout(const ssd_shape_t *shape, const void *x, const void *dt, const void *B,
+                                       const void *C, const float *dA_cumsum, const float *states_in,
+                                       const float *D, void *y, void *workspace, size_t workspace_bytes,
+                                       uint64_t wait_ns, cudaStream_t stream) {
+    if (wait_ns < 100000ull) wait_ns = 100000ull;
+    if (wait_ns > 1000000000ull) wait_ns = 1000000000ull;
+    return chunk_scan_call(shape, x, dt, B, C, dA_cumsum, states_in, D, y, workspace, workspace_bytes, wait_ns,
+                           stream);
+}
+
+ssd_status_t ssd_get_device_status(cudaStream_t stream) {
+    unsigned *word = nullptr, *taken = nullptr;
+    cudaError_t e = device_status_word(&word);
+    if (e == cudaSuccess) {
+        void *p = nullptr;
+        e = symbol_address(g_device_status_read, g_status_read_cache, &p);
+        taken = static_cast<unsigned *>(p);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    take_status_kernel<<<1, 1, 0, stream>>>(word, taken);
+    e = cudaGetLastError();
+    unsigned v = 0;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&v, taken, sizeof(v), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    return (v & 1u) ? SSD_ERR_TIMEOUT : SSD_OK;
 }
 
 ssd_status_t selective_scan_fwd(const ssd_shape_t *shape, const void *x, const void *dt, const float *A,
@@ -316,27 +451,12 @@ namespace {
 // The scratch every ssd_fwd_noalloc call uses; one copy per device.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SSD_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+SymbolCache g_scratch_cache;
 
-// Device address of the static scratch on the current device, looked up
-// once per device (host code only sees a host-side stand-in for the symbol).
-cudaError_t noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
-    return cudaSuccess;
-}
+// Device address of the static scratch on the current device (host code only
+// sees a host-side stand-in for the symbol), looked up once per device and
+// context.
+cudaError_t noalloc_scratch(void **out) { return symbol_address(g_noalloc_scratch, g_scratch_cache, out); }
 
 }  // namespace
 
@@ -359,10 +479,15 @@ extern "C" ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x,
     cudaError_t e = noalloc_scratch(&scratch);
     if (e != cudaSuccess) return from_cuda(e);
     // the kernels write every scratch word they later read, except the
-    // status word, which the fused path clears on the stream before use
-    if (tc)
+    // chunk-pack ready flags, which the fused path clears on the stream
+    // before use
+    if (tc) {
+        unsigned *status = nullptr;
+        e = device_status_word(&status);
+        if (e != cudaSuccess) return from_cuda(e);
         return from_cuda(
-            ssd::tc_fwd(d, shape->ydtype, x, dt, A, B, C, D, init_state, y, final_state, scratch, stream));
+            ssd::tc_fwd(d, shape->ydtype, x, dt, A, B, C, D, init_state, y, final_state, scratch, status, stream));
+    }
     if (shape->dtype == SSD_DTYPE_F32)
         return fwd_staged<float, float>(d, x, dt, A, B, C, D, init_state, y, final_state, scratch, stream);
     if (shape->ydtype == SSD_DTYPE_F32)

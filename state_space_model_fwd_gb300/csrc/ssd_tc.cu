@@ -49,7 +49,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTargetCtas = 148;        // about one CTA per SM of a GB300 (152 SMs)
 constexpr int kSmemLimit = 226 * 1024;  // dynamic bytes; leaves room for the static mbarriers
 constexpr uint64_t kWaitNs = 100000000ull;    // a wait gives up after 0.1 s
 constexpr uint64_t kDrainNs = 20000000ull;    // the exit drain gives up after 0.02 s
@@ -66,7 +65,12 @@ struct TcParams {
     float *seg_tot;     // [b, H, nseg]  total dt*A of each segment (may be null)
     const float *cum_in;    // [b, H, nc, Q] given in-chunk cumulative decay (null: computed from dt, A)
     const float *entering;  // [b, nseg, H, P, N] state entering each segment (null: init / seg_state)
-    unsigned *status;   // bit 0: a wait gave up (may be null)
+    unsigned *status;   // the device status word: bit 0 = a wait gave up (may be null)
+    // limit of the wait for a chunk pack's ready flag (the self-test of the
+    // failure path shortens it), and whether the producer waits for that
+    // flag before it issues any load of the chunk
+    unsigned long long flag_wait_ns;
+    int flag_first;
     long long b, L, H, G;
     int hpg, nc, nseg, cps;  // cps: chunks per segment
     int nhb;
@@ -224,11 +228,11 @@ __device__ __forceinline__ bool group_wait(uint64_t *bar, uint32_t parity, volat
 // Poll a flag in global memory (set by another grid) until it is non-zero,
 // with the same bound as wait_bounded; then order the acquire before this
 // thread's TMA reads.
-__device__ __forceinline__ bool wait_flag(const unsigned *flag, volatile int *abort_flag) {
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, volatile int *abort_flag, uint64_t limit_ns) {
     if (ld_acquire_gpu(flag) == 0) {
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_gpu(flag) == 0) {
-            if (*abort_flag || globaltimer_ns() - t0 > kWaitNs) {
+            if (*abort_flag || globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 return false;
             }
@@ -1020,10 +1024,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
                 // two operations per chunk: the x box, then the chunk pack
                 // once the C B^T kernel has published it
+                if (prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                 mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES);
                 tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, (c0 + it) * C::Q, b);
                 ++nload[s];
-                if (!wait_flag(prm.cb_ready + plane, &abort_sh)) break;
+                if (!prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                 mbar_arrive_expect_tx(&pfull_bar[s], C::PACK_BYTES);
                 bulk_load(stage_cb(s), prm.pack + plane * C::PACK_BYTES, C::PACK_BYTES, &pfull_bar[s]);
                 ++npack[s];
@@ -1538,12 +1543,25 @@ struct Plan {
     int nseg, cps, nhb;
 };
 
+// SM count of the current device (one chunk-scan CTA fits per SM); the
+// GB300's 152 when no device can be queried (a workspace size asked for on
+// a host without a GPU).
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    return n;
+}
+
 template <class C>
 Plan plan_for(const Dims &d) {
     Plan p;
     p.nhb = (int)((d.H + C::HB - 1) / C::HB);
     const long long units = d.b * p.nhb;
-    int nseg = (int)(kTargetCtas / units);
+    int nseg = (int)(sm_count() / units);
     if (nseg < 1) nseg = 1;
     if (nseg > d.nc) nseg = (int)d.nc;
     p.cps = (int)((d.nc + nseg - 1) / nseg);
@@ -1559,15 +1577,14 @@ size_t pack_bytes(const Dims &d) {
     return align256((size_t)C::PACK_BYTES * d.b * d.nc * d.G);
 }
 
-// Workspace: header (status word, chunk-pack ready flags) | chunk packs |
-// segment states | segment totals.  The header is cleared on the stream by
-// every call.
+// Workspace: chunk-pack ready flags [b, nc, G] | chunk packs | segment
+// states | segment totals.  The flags are cleared on the stream by every
+// call.
 size_t flag_bytes(const Dims &d) { return align256(sizeof(unsigned) * d.b * d.nc * d.G); }
 
-// header: status word | C B^T ready flags [b, nc, G]
 template <class C>
 size_t header_bytes(const Dims &d) {
-    return 256 + flag_bytes(d);
+    return flag_bytes(d);
 }
 
 #ifdef SSD_TRACE
@@ -1666,9 +1683,11 @@ cudaError_t launch_seg_state(const Dims &d, TcParams prm, const void *x, const v
     return e;
 }
 
-TcParams base_params(const Dims &d, const void *dt) {
+TcParams base_params(const Dims &d, const void *dt, unsigned *status) {
     TcParams prm{};
     prm.dt = static_cast<const bf16 *>(dt);
+    prm.status = status;
+    prm.flag_wait_ns = kWaitNs;
     prm.b = d.b;
     prm.L = d.L;
     prm.H = d.H;
@@ -1681,9 +1700,9 @@ TcParams base_params(const Dims &d, const void *dt) {
 template <class C>
 cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B,
                     const void *Cm, const float *D, const float *init, void *y, float *fin, void *ws,
-                    cudaStream_t s) {
+                    unsigned *status, cudaStream_t s) {
     const Plan p = plan_for<C>(d);
-    TcParams prm = base_params(d, dt);
+    TcParams prm = base_params(d, dt, status);
     prm.x = static_cast<const bf16 *>(x);
     prm.A = A;
     prm.D = D;
@@ -1692,8 +1711,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     prm.fin = fin;
     char *w = static_cast<char *>(ws);
     const size_t hdr = header_bytes<C>(d);
-    prm.status = reinterpret_cast<unsigned *>(w);
-    prm.cb_ready = reinterpret_cast<unsigned *>(w + 256);
+    prm.cb_ready = reinterpret_cast<unsigned *>(w);
     uint8_t *pack = reinterpret_cast<uint8_t *>(w + hdr);
     prm.pack = pack;
     const size_t seg_off = hdr + pack_bytes<C>(d);
@@ -1773,10 +1791,10 @@ size_t tc_fwd_workspace(const Dims &dq) {
 
 cudaError_t tc_fwd(const Dims &dq, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B,
                    const void *C, const float *D, const float *init, void *y, float *fin, void *ws,
-                   cudaStream_t s) {
+                   unsigned *status, cudaStream_t s) {
     const Dims d = fwd_tiles(dq);
     cudaError_t e = cudaErrorNotSupported;
-    dispatch(d, [&](auto c) { e = run_fwd<decltype(c)>(d, ydtype, x, dt, A, B, C, D, init, y, fin, ws, s); });
+    dispatch(d, [&](auto c) { e = run_fwd<decltype(c)>(d, ydtype, x, dt, A, B, C, D, init, y, fin, ws, status, s); });
     return e;
 }
 
@@ -1794,8 +1812,8 @@ namespace {
 
 template <class C>
 cudaError_t run_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
-                            float *states, cudaStream_t s) {
-    TcParams prm = base_params(d, dt);
+                            float *states, unsigned *status, cudaStream_t s) {
+    TcParams prm = base_params(d, dt, status);
     prm.cum_in = cum;
     prm.seg_state = states;  // [b, nc, H, P, N]: one segment per chunk
     prm.nseg = (int)d.nc;
@@ -1806,13 +1824,21 @@ cudaError_t run_chunk_state(const Dims &d, const void *x, const void *dt, const 
                                false, s);
 }
 
-// The CB matrices of a stage call live in stream-ordered scratch
-// (cudaMallocAsync / cudaFreeAsync on the caller's stream).
+// The chunk packs of a stage call and their ready flags live in the
+// caller's workspace: flags [b, nc, G] | packs.  With `selftest_ns` > 0 the
+// C B^T kernel is not launched, so no pack is ever published and the scan's
+// wait for its first pack runs out after that many nanoseconds (the test of
+// the bounded waits; the producer waits before it issues any load).
+template <class C>
+size_t scan_stage_workspace(const Dims &d) {
+    return flag_bytes(d) + pack_bytes<C>(d);
+}
+
 template <class C>
 cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
                            const void *Cm, const float *cum, const float *states_in, const float *D, void *y,
-                           cudaStream_t s) {
-    TcParams prm = base_params(d, dt);
+                           void *ws, unsigned *status, uint64_t selftest_ns, cudaStream_t s) {
+    TcParams prm = base_params(d, dt, status);
     prm.cum_in = cum;
     prm.entering = states_in;  // [b, nc, H, P, N]: the state entering each chunk
     prm.x = static_cast<const bf16 *>(x);
@@ -1821,36 +1847,45 @@ cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, con
     prm.nseg = (int)d.nc;
     prm.cps = 1;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
-    char *scratch = nullptr;  // ready flags | C B^T matrices
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&scratch), flag_bytes(d) + pack_bytes<C>(d), s);
-    if (e != cudaSuccess) return e;
-    prm.cb_ready = reinterpret_cast<unsigned *>(scratch);
-    uint8_t *pack = reinterpret_cast<uint8_t *>(scratch + flag_bytes(d));
+    char *w = static_cast<char *>(ws);
+    prm.cb_ready = reinterpret_cast<unsigned *>(w);
+    uint8_t *pack = reinterpret_cast<uint8_t *>(w + flag_bytes(d));
     prm.pack = pack;
-    e = cudaMemsetAsync(scratch, 0, flag_bytes(d), s);
+    if (selftest_ns > 0) {
+        prm.flag_wait_ns = selftest_ns;
+        prm.flag_first = 1;
+    }
+    cudaError_t e = cudaMemsetAsync(w, 0, flag_bytes(d), s);
     timing_begin(s);
-    if (e == cudaSuccess) e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, nullptr, s);
+    if (e == cudaSuccess && selftest_ns == 0) e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, status, s);
     if (e == cudaSuccess)
         e = launch_scan<C>(d, prm, ydtype, x, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc),
                            "chunk_scan_stage_tc", s);
-    const cudaError_t e2 = cudaFreeAsync(scratch, s);
-    return e != cudaSuccess ? e : e2;
+    return e;
 }
 
 }  // namespace
 
 cudaError_t tc_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
-                           float *states, cudaStream_t s) {
+                           float *states, unsigned *status, cudaStream_t s) {
     cudaError_t e = cudaErrorNotSupported;
-    dispatch(d, [&](auto c) { e = run_chunk_state<decltype(c)>(d, x, dt, B, cum, states, s); });
+    dispatch(d, [&](auto c) { e = run_chunk_state<decltype(c)>(d, x, dt, B, cum, states, status, s); });
     return e;
+}
+
+size_t tc_chunk_scan_workspace(const Dims &d) {
+    size_t bytes = 0;
+    dispatch(d, [&](auto c) { bytes = scan_stage_workspace<decltype(c)>(d); });
+    return bytes;
 }
 
 cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
                           const void *C, const float *cum, const float *states_in, const float *D, void *y,
-                          cudaStream_t s) {
+                          void *ws, unsigned *status, uint64_t selftest_ns, cudaStream_t s) {
     cudaError_t e = cudaErrorNotSupported;
-    dispatch(d, [&](auto c) { e = run_chunk_scan<decltype(c)>(d, ydtype, x, dt, B, C, cum, states_in, D, y, s); });
+    dispatch(d, [&](auto c) {
+        e = run_chunk_scan<decltype(c)>(d, ydtype, x, dt, B, C, cum, states_in, D, y, ws, status, selftest_ns, s);
+    });
     return e;
 }
 

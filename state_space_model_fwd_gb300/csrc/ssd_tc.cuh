@@ -10,14 +10,20 @@ namespace ssd {
 bool tc_fwd_supported(const Dims &d, ssd_dtype_t dtype);
 // Workspace bytes the fused path needs.
 size_t tc_fwd_workspace(const Dims &d);
+// `status`: the device status word (bit 0 set when a bounded wait gives up).
 cudaError_t tc_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B, const void *C,
-                   const float *D, const float *init, void *y, float *fin, void *ws, cudaStream_t s);
+                   const float *D, const float *init, void *y, float *fin, void *ws, unsigned *status, cudaStream_t s);
 
 // True when the tcgen05 chunk-state / chunk-scan stage kernels handle this shape.
 bool tc_stage_supported(const Dims &d, ssd_dtype_t dtype);
 cudaError_t tc_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
-                           float *states, cudaStream_t s);
+                           float *states, unsigned *status, cudaStream_t s);
+// Workspace of the tensor-core chunk-scan stage (chunk packs and their flags).
+size_t tc_chunk_scan_workspace(const Dims &d);
+// selftest_ns > 0: launch the scan alone with no pack ever published, so its
+// bounded wait gives up after that many nanoseconds (failure-path test).
 cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B, const void *C,
-                          const float *cum, const float *states_in, const float *D, void *y, cudaStream_t s);
+                          const float *cum, const float *states_in, const float *D, void *y, void *ws,
+                          unsigned *status, uint64_t selftest_ns, cudaStream_t s);
 
 }  // namespace ssd

@@ -268,6 +268,41 @@ def pin_snapshots(rec):
         _close(f2, f, what="final with snapshots")
 
 
+# ---------------------------------------------------------------------------
+# (p11) in-chunk cumulative decay, entry by entry: for steps j <= i of chunk c
+#   exp(cum[b,h,c,i] - cum[b,h,c,j]) = prod_{k=j+1..i} exp(dt_k A_h)
+#   exp(cum[b,h,c,i])                = prod_{k=0..i}   exp(dt_k A_h)
+# with k counted from the chunk's first step c*Q: the decay factors of the
+# recurrence multiplied one step at a time (no running sum), so a permuted,
+# mis-strided, exclusive or shifted layout inside a chunk fails here even
+# when it keeps the chunk totals.
+# ---------------------------------------------------------------------------
+def pin_chunk_cumsum(fn):
+    r = _rng(31)
+    b, L, H = 2, 48, 3
+    dt = 0.3 * np.exp(r.uniform(np.log(0.05), np.log(2.0), (b, L, H)))
+    A = -np.exp(r.uniform(0.0, np.log(16.0), H))
+    for Q in (1, 4, 16, 48):
+        cum = np.asarray(fn(dt, A, Q))
+        nc = L // Q
+        assert cum.shape == (b, H, nc, Q), cum.shape
+        for bi in range(b):
+            for h in range(H):
+                for c in range(nc):
+                    dec = [np.exp(dt[bi, c * Q + k, h] * A[h]) for k in range(Q)]
+                    for i in range(Q):
+                        prod = 1.0
+                        for k in range(i + 1):
+                            prod *= dec[k]
+                        _close(np.exp(cum[bi, h, c, i]), prod, rtol=1e-12, what=f"exp(cum) Q={Q} i={i}")
+                        for j in range(i + 1):
+                            pj = 1.0
+                            for k in range(j + 1, i + 1):
+                                pj *= dec[k]
+                            _close(np.exp(cum[bi, h, c, i] - cum[bi, h, c, j]), pj, rtol=1e-12,
+                                   what=f"exp(cum_i - cum_j) Q={Q} i={i} j={j}")
+
+
 ALL_PINS = [pin_quadratic, pin_closed_form, pin_impulse, pin_chunked,
             pin_split_resume, pin_linearity, pin_dt_zero,
             pin_linear_attention, pin_groups, pin_snapshots]

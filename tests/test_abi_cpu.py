@@ -13,7 +13,7 @@ from state_space_model_fwd_gb300 import _build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "ssd.h")
 
-OK, INVALID, UNSUPPORTED, CUDA_ERR, WORKSPACE = 0, 1, 2, 3, 4
+OK, INVALID, UNSUPPORTED, CUDA_ERR, WORKSPACE, SCRATCH, TIMEOUT = 0, 1, 2, 3, 4, 5, 6
 
 
 @pytest.fixture(scope="module")
@@ -38,11 +38,12 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(5):
+    for code in range(7):
         s = ssd.status_string(code)
         assert s.startswith("SSD_"), s
+    assert "TIMEOUT" in ssd.status_string(TIMEOUT)
     assert ssd.status_string(99) == "SSD_ERR_UNKNOWN"
-    assert lib.ssd_abi_version() >> 16 == 1
+    assert lib.ssd_abi_version() >> 16 == 2
 
 
 def shape(**kw):
@@ -110,7 +111,19 @@ def test_stage_entry_points_validate(lib):
     assert lib.ssd_chunk_cumsum(ctypes.byref(s), None, FAKE, FAKE, None) == INVALID
     assert lib.ssd_chunk_state(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, None, None) == INVALID
     assert lib.ssd_state_passing(ctypes.byref(s), None, FAKE, None, FAKE, None, None) == INVALID
-    assert lib.ssd_chunk_scan(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None) == INVALID
+    assert lib.ssd_chunk_scan(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 1 << 40,
+                              None) == INVALID
+    # the tensor-core stage needs its workspace (chunk packs and ready flags)
+    s = shape(dtype=1)
+    need = lib.ssd_chunk_scan_workspace_size(ctypes.byref(s))
+    assert need > 0
+    assert lib.ssd_chunk_scan(ctypes.byref(s), *([FAKE] * 8), None, 0, None) == WORKSPACE
+    assert lib.ssd_chunk_scan(ctypes.byref(s), *([FAKE] * 8), FAKE, need - 1, None) == WORKSPACE
+    # the FFMA stage (fp32 inputs) needs none
+    assert lib.ssd_chunk_scan_workspace_size(ctypes.byref(shape(dtype=0))) == 0
+    # the failure-path self-test exists only on the tensor-core path
+    assert lib.ssd_selftest_scan_timeout(ctypes.byref(shape(dtype=0)), *([FAKE] * 8), FAKE, 1 << 40, 10 ** 6,
+                                         None) == UNSUPPORTED
     assert lib.selective_scan_fwd(ctypes.byref(s), FAKE, FAKE, FAKE, None, FAKE, None, None, FAKE, None,
                                   None) == INVALID
     # the sequential scan has no chunk restriction, but still checks groups
@@ -136,18 +149,19 @@ def _a256(v):
 
 @pytest.mark.parametrize("name", ["mamba2_130m", "mamba2_2p7b", "long_16k", "wide_head", "wide_head_q128"])
 def test_workspace_layout_of_the_tensor_core_path(lib, name):
-    """ssd_fwd's workspace on the bf16 tensor-core path: a header (status word,
-    one ready flag per chunk pack), the chunk packs (masked C B^T of a 64-step
-    tile and the tile's B and C, bf16), and, when the sequence is cut into
-    segments, the segment states (fp32) and the segment totals."""
+    """ssd_fwd's workspace on the bf16 tensor-core path: one ready flag per
+    chunk pack, the chunk packs (masked C B^T of a 64-step tile and the tile's
+    B and C, bf16), and, when the sequence is cut into segments, the segment
+    states (fp32) and the segment totals.  With no GPU to query, the segment
+    plan assumes the GB300's 152 SMs."""
     import ssd_inputs as si
     import bench
     cfg = si.CONFIGS[name]
     s = ssd.ssd_shape_t(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups,
                         cfg.chunk_size, 1, 1)
     b, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
-    nseg, _, nt = bench.tc_plan(cfg)
-    want = 256 + _a256(4 * b * nt * G) + _a256(b * nt * G * (64 * 64 * 2 + 2 * 64 * N * 2))
+    nseg, _, nt = bench.tc_plan(cfg, 152)
+    want = _a256(4 * b * nt * G) + _a256(b * nt * G * (64 * 64 * 2 + 2 * 64 * N * 2))
     if nseg > 1:
         want += _a256(4 * b * nseg * H * P * N) + _a256(4 * b * nseg * H)
     assert lib.ssd_fwd_workspace_size(ctypes.byref(s)) == want

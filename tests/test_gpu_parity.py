@@ -4,12 +4,18 @@ Tolerances (max |err| over the compared outputs, divided by the oracle
 output's RMS, separately for y and final_state):
   fp32 inputs:  1e-4
   bf16 inputs (fp32 state and accumulation, fp32 y): 1e-2
-  bf16 y: 1e-2 plus the bf16 output rounding of the oracle value (half an
-  ulp, 2^-9 |y| relative), which a bf16 store adds on top of the arithmetic.
-Full-size workloads compare every output of sampled (batch, head) pairs with
-the oracle run on those heads alone (heads are independent), and the whole
-output against the four-stage decomposed path.
+  bf16 y: element by element, |err| <= 1e-2 x RMS + half a bf16 ulp of the
+  value: the bf16 store rounds the fp32 result by up to half an ulp (2^-9 of
+  the value at the bottom of a binade), which no implementation avoids; the
+  arithmetic is held to 1e-2 x RMS beyond it.
+Full-size workloads compare every output of every (batch, head) with the
+oracle, with y in fp32 and in bf16 (the dtype the benchmark times).
+Measured errors are printed, and appended as JSON lines to the file named by
+SSD_PARITY_LOG when that is set.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -38,11 +44,34 @@ def check(got, want, tol, what):
     return e
 
 
-def bf16_half_ulp_rel(want):
-    """bf16 output rounding bound relative to the RMS: half an ulp of each
-    oracle value (|v| * 2^-8 is an upper bound of half an ulp)."""
-    rms = np.sqrt(np.mean(np.asarray(want, np.float64) ** 2))
-    return float(np.max(np.abs(want)) * 2.0 ** -8 / max(rms, 1e-30))
+def bf16_half_ulp(v):
+    """Half a bf16 ulp of each value: |v| in [2^(e-1), 2^e) has an ulp of
+    2^(e-8) (8 significant bits)."""
+    _, e = np.frexp(np.asarray(v, np.float64))
+    return np.ldexp(1.0, e - 9)
+
+
+def check_bf16_y(got, want, tol, what):
+    """bf16 output: |err| <= tol x RMS + half an ulp of the value (of the
+    larger of the two, in case the rounding crossed a power of two).
+    Returns (max|err| / RMS, max (|err| - half ulp) / RMS)."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape
+    assert np.all(np.isfinite(got)), "non-finite output"
+    rms = max(float(np.sqrt(np.mean(want ** 2))), 1e-30)
+    err = np.abs(got - want)
+    beyond = float(np.max(err - bf16_half_ulp(np.maximum(np.abs(got), np.abs(want))))) / rms
+    assert beyond <= tol, f"{what}: max(|err| - half ulp) = {beyond:.3e} x RMS > {tol:.1e}"
+    return float(np.max(err)) / rms, beyond
+
+
+def log_parity(record):
+    print(json.dumps(record))
+    path = os.environ.get("SSD_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(record) + "\n")
 
 
 def to_np(t):
@@ -152,10 +181,12 @@ def test_ssd_fwd_carried_state_strong_decay(ranges):
     """The state carried into a chunk, where it is most of the output: D = 0
     and only the first 4 steps of every chunk compared.  A rescale that loses
     the carried state (a factor flushed to zero) leaves errors of the size of
-    these outputs themselves, which the RMS of the whole output would hide.
-    The bound is relative to the largest of them: their values are heavy
-    tailed (some 20x their RMS), and the bf16 copy of the state used for the
-    inter-chunk term carries a 2^-9 relative rounding per entry."""
+    these outputs themselves.  Bounds: max|err| over these steps <= 1e-2 x
+    the RMS of the whole output (the stated tolerance's normalisation), and
+    <= 1e-2 x the largest of them; the error relative to their own RMS is
+    printed (these values are heavy tailed, some 20x their RMS, and the bf16
+    copy of the state in the inter-chunk term rounds each entry by up to
+    2^-9 of its size)."""
     cfg = si.SSDConfig("tc_carry", 1, 1280, 8, 64, 128, 1, 64, "bf16", True, 92)
     inp = decay_regime_inputs(cfg, ranges)
     inp.D = np.zeros_like(inp.D)
@@ -165,9 +196,15 @@ def test_ssd_fwd_carried_state_strong_decay(ranges):
     nc = cfg.seqlen // 64
     head = lambda a: np.asarray(a).reshape(cfg.batch, nc, 64, cfg.nheads, cfg.headdim)[:, 1:, :4]
     got, want = head(to_np(y)), head(y_ref)
-    e = float(np.max(np.abs(got - want)) / np.max(np.abs(want)))
-    assert e <= TOL["bf16"], f"carried state, first steps of each chunk: max|err| = {e:.3e} x max|y|"
-    check(to_np(fin), fin_ref, TOL["bf16"], "carried state final")
+    err = float(np.max(np.abs(got - want)))
+    e_max = err / float(np.max(np.abs(want)))
+    e_rms_all = err / float(np.sqrt(np.mean(y_ref ** 2)))
+    e_rms_sub = err / float(np.sqrt(np.mean(want ** 2)))
+    ef = check(to_np(fin), fin_ref, TOL["bf16"], "carried state final")
+    log_parity({"test": "carried_state", "err_over_rms_of_y": e_rms_all, "err_over_max_of_subset": e_max,
+                "err_over_rms_of_subset": e_rms_sub, "final_err_over_rms": ef})
+    assert e_rms_all <= TOL["bf16"], f"carried state: max|err| = {e_rms_all:.3e} x RMS(y)"
+    assert e_max <= TOL["bf16"], f"carried state, first steps of each chunk: max|err| = {e_max:.3e} x max|y|"
 
 
 @pytest.mark.parametrize("name", ["bf16_p64_n128", "bf16_p128_n256_q128", "tc_p64_n128_seg", "bf16_p128_n256_q64"])
@@ -179,7 +216,7 @@ def test_ssd_fwd_bf16_output(name):
                          chunk_size=cfg.chunk_size, y_dtype=torch.bfloat16)
     assert y.dtype == torch.bfloat16
     y_ref, fin_ref = oracle_full(inp)
-    check(to_np(y), y_ref, TOL["bf16"] + bf16_half_ulp_rel(y_ref), f"{name} bf16 y")
+    check_bf16_y(to_np(y), y_ref, TOL["bf16"], f"{name} bf16 y")
     check(to_np(fin), fin_ref, TOL["bf16"], f"{name} final")
 
 
@@ -237,9 +274,10 @@ def test_stage_chain_matches_fused(name):
     st = ssd.ssd_chunk_state(t["x"], t["dt"], t["B"], cum)
     sin, fin = ssd.ssd_state_passing(st, cum, t["init_state"])
     y_ref, fin_ref = oracle_full(inp)
-    for y_dtype, tol in ((torch.float32, TOL["bf16"]), (torch.bfloat16, TOL["bf16"] + bf16_half_ulp_rel(y_ref))):
-        y = ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum, sin, t["D"], y_dtype=y_dtype)
-        check(to_np(y), y_ref, tol, f"{name} staged y ({y_dtype})")
+    y = ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum, sin, t["D"], y_dtype=torch.float32)
+    check(to_np(y), y_ref, TOL["bf16"], f"{name} staged y (fp32)")
+    y = ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum, sin, t["D"], y_dtype=torch.bfloat16)
+    check_bf16_y(to_np(y), y_ref, TOL["bf16"], f"{name} staged y (bf16)")
     check(to_np(fin), fin_ref, TOL["bf16"], f"{name} staged final")
 
 
@@ -300,30 +338,40 @@ def test_bitwise_deterministic(name):
 FULL = ["mamba2_130m", "mamba2_2p7b", "long_16k", "wide_head", "wide_head_q128"]
 
 
-def sample_pairs(cfg):
-    b, H = cfg.batch, cfg.nheads
-    return sorted({(0, 0), (b - 1, H - 1), (0, H // 2), (b - 1, 1), (b // 2, H // 3)})
-
-
 @pytest.mark.parametrize("name", FULL)
 def test_ssd_fwd_full_size(name):
-    """Full-size workload, same launch configuration the benchmark times:
-    sampled heads against the oracle, every output against the four-stage
-    decomposed path."""
+    """Full-size workload in the launch configuration the benchmark times:
+    every output of every (batch, head) against the fp64 oracle, with y in
+    fp32 and in bf16 (the benchmark's output dtype); the final state of both
+    calls identical."""
+    cfg = si.CONFIGS[name]
+    inp = si.make_inputs(cfg)
+    t = gpu_inputs(inp)
+    args = (t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"])
+    y32, fin = ssd.ssd_fwd(*args, chunk_size=cfg.chunk_size)
+    y16, fin16 = ssd.ssd_fwd(*args, chunk_size=cfg.chunk_size, y_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert torch.equal(fin, fin16), "final state depends on the output dtype"
+    y32, y16, fin = to_np(y32), to_np(y16), to_np(fin)
+    del args, t
+    torch.cuda.empty_cache()
+    y_ref, fin_ref = oracle_full(inp)
+    e32 = check(y32, y_ref, TOL["bf16"], f"{name} y (fp32, every head)")
+    e16, beyond = check_bf16_y(y16, y_ref, TOL["bf16"], f"{name} y (bf16, every head)")
+    ef = check(fin, fin_ref, TOL["bf16"], f"{name} final (every head)")
+    log_parity({"test": "full_size", "workload": name, "y_f32_err_over_rms": e32, "y_bf16_err_over_rms": e16,
+                "y_bf16_err_beyond_half_ulp_over_rms": beyond, "final_err_over_rms": ef})
+
+
+@pytest.mark.parametrize("name", FULL[:3])
+def test_ssd_fwd_full_size_matches_stages(name):
+    """The fused path against the four stage entry points chained (each its
+    own kernels), whole output, at full size."""
     cfg = si.CONFIGS[name]
     inp = si.make_inputs(cfg)
     t = gpu_inputs(inp)
     y, fin = ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
                          chunk_size=cfg.chunk_size)
-    torch.cuda.synchronize()
-    refs = oracle_heads(inp, sample_pairs(cfg))
-    ys = np.concatenate([refs[k][0] for k in sorted(refs)])
-    fs = np.concatenate([refs[k][1] for k in sorted(refs)])
-    yg = np.concatenate([to_np(y[b, :, h]) for b, h in sorted(refs)])
-    fg = np.concatenate([to_np(fin[b, h]) for b, h in sorted(refs)])
-    check(yg, ys, TOL["bf16"], f"{name} y (sampled heads)")
-    check(fg, fs, TOL["bf16"], f"{name} final (sampled heads)")
-    # whole output against the decomposed stages
     Q = cfg.chunk_size
     cum = ssd.ssd_chunk_cumsum(t["dt"], t["A"], Q)
     st = ssd.ssd_chunk_state(t["x"], t["dt"], t["B"], cum)
@@ -344,8 +392,8 @@ def test_selective_scan_long_sequence():
     t = gpu_inputs(inp)
     y, fin = ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"])
     torch.cuda.synchronize()
-    pairs = [(0, 0), (0, 47), (0, 20)]
-    refs = oracle_heads(inp, pairs)
-    ys = np.concatenate([refs[k][0] for k in pairs])
-    yg = np.concatenate([to_np(y[b, :, h]) for b, h in pairs])
-    check(yg, ys, TOL["bf16"], "long_16k sequential scan y (sampled heads)")
+    y_ref, fin_ref = oracle_full(inp)
+    ey = check(to_np(y), y_ref, TOL["bf16"], "long_16k sequential scan y (every head)")
+    ef = check(to_np(fin), fin_ref, TOL["bf16"], "long_16k sequential scan final (every head)")
+    log_parity({"test": "selective_scan_full_size", "workload": "long_16k", "y_f32_err_over_rms": ey,
+                "final_err_over_rms": ef})

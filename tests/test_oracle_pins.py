@@ -11,6 +11,41 @@ def test_pin(pin):
     pin(oracle.ssd_recurrence)
 
 
+def test_chunk_cumsum_entries():
+    """oracle.chunk_cumsum, every interior entry, against products of the
+    per-step decay factors (pin p11)."""
+    pins.pin_chunk_cumsum(oracle.chunk_cumsum)
+
+
+def _cumsum_layout(dt, A, Q, order):
+    dt = np.asarray(dt, np.float64)
+    b, L, H = dt.shape
+    dA = (dt * A[None, None, :]).reshape(b, L // Q, Q, H)
+    return order(dA).transpose(0, 3, 1, 2).copy()
+
+
+CUMSUM_MUTANTS = {
+    # reversed inside the chunk: the chunk totals (last entries) are unchanged
+    "reversed_in_chunk": lambda dt, A, Q: _cumsum_layout(
+        dt, A, Q, lambda d: np.cumsum(d[:, :, ::-1, :], axis=2)),
+    # exclusive running sum
+    "exclusive": lambda dt, A, Q: _cumsum_layout(
+        dt, A, Q, lambda d: np.cumsum(d, axis=2) - d),
+    # steps and heads strided the wrong way round inside a chunk
+    "head_shifted": lambda dt, A, Q: _cumsum_layout(
+        dt, np.roll(A, 1), Q, lambda d: np.cumsum(d, axis=2)),
+    # one step late: the decay of step q taken from step q - 1
+    "step_shifted": lambda dt, A, Q: _cumsum_layout(
+        np.roll(dt, 1, axis=1), A, Q, lambda d: np.cumsum(d, axis=2)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CUMSUM_MUTANTS))
+def test_cumsum_pin_catches_mutant(name):
+    with pytest.raises(AssertionError):
+        pins.pin_chunk_cumsum(CUMSUM_MUTANTS[name])
+
+
 @pytest.mark.parametrize("Q", [1, 4, 16, 32])
 def test_stage_definitions_match_chunked_algorithm(Q):
     """The per-stage oracle intermediates (cumulative decay, chunk-local
