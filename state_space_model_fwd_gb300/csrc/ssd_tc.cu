@@ -1645,9 +1645,11 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pac
     return e;
 }
 
+// pdl: the scan may start while the kernel before it on the stream (the
+// C B^T kernel, which publishes its packs through ready flags) still runs.
 template <class C>
 cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, dim3 grid, const char *name,
-                        cudaStream_t s) {
+                        bool pdl, cudaStream_t s) {
     CUtensorMap mx, mdt = {};
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
     const bool f32 = ydtype == SSD_DTYPE_F32;
@@ -1657,11 +1659,11 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, prm);
     } else {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, true, mx, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, prm);
     }
     timing_mark(s, name);
     return e;
@@ -1737,7 +1739,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     }
     // segments in the slowest grid dimension: the first segment's CTAs, which
     // need nothing from the segment-state kernel, are scheduled first
-    return launch_scan<C>(d, prm, ydtype, x, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", s);
+    return launch_scan<C>(d, prm, ydtype, x, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", true, s);
 }
 
 // Dispatch over the compiled tile configurations.
@@ -1860,7 +1862,7 @@ cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, con
     if (e == cudaSuccess && selftest_ns == 0) e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, status, s);
     if (e == cudaSuccess)
         e = launch_scan<C>(d, prm, ydtype, x, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc),
-                           "chunk_scan_stage_tc", s);
+                           "chunk_scan_stage_tc", selftest_ns == 0, s);
     return e;
 }
 
