@@ -44,8 +44,12 @@
  * they run (a bounded wait that gave up) cannot be returned by the call that
  * enqueued them: they are latched in a per-device status word that
  * ssd_get_device_status() reads.  No entry point but that one synchronises.
- * Supported on the GPU: chunk_size 64 or 128, L % chunk_size == 0,
- * H % G == 0, P in {16, 32, 64, 128}, N in {16, 32, 64, 128, 256}.
+ * Supported on the GPU: chunk_size 64 or 128, any L (nc = ceil(L / Q): a
+ * partial last chunk is processed as if padded with dt = 0 steps, which
+ * neither decay nor feed the state, and nothing is written for them; the
+ * stage layouts below then hold nc chunks, the missing dA_cumsum entries
+ * repeating the chunk's last value), H % G == 0, P in {16, 32, 64, 128},
+ * N in {16, 32, 64, 128, 256}.
  * Outputs are bitwise reproducible run to run: no floating-point atomics.
  */
 #ifndef SSD_H_
@@ -169,6 +173,31 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, co
                                      float *final_state, cudaStream_t stream);
 
 /*
+ * Packed variable-length batch: nseq independent sequences stored back to
+ * back along L (x [1, Ltot, H, P], dt [1, Ltot, H], B, C [1, Ltot, G, N], y
+ * [1, Ltot, H, P]; shape->batch must be 1 and shape->seqlen = Ltot).
+ * Sequence s covers steps cu_seqlens[s] .. cu_seqlens[s+1] - 1 (a HOST array
+ * of nseq + 1 offsets, 0 first and Ltot last, non-decreasing); its state
+ * starts from init_states[s] (NULL: zero) and ends in final_states[s] (NULL:
+ * not written), both [nseq, H, P, N] fp32.  No state crosses a sequence
+ * boundary.  Each sequence runs the fused forward of ssd_fwd on its own steps,
+ * one after another on `stream`, sharing `workspace`, which must hold
+ * ssd_fwd_varlen_workspace_size(shape, cu_seqlens, nseq) bytes (0 for
+ * invalid arguments).  Every sequence's start must keep the pointers it
+ * derives 16-byte aligned (cu_seqlens[s] * H * sizeof(dtype) a multiple of
+ * 16, e.g. H a multiple of 8 for bf16): SSD_ERR_INVALID_ARG otherwise.
+ * (The pages are silent on batches of unequal lengths; this packs them the
+ * way the chunk split of "Mamba-2 in NVIDIA cuTile", section "Why Mamba-2 is
+ * a useful kernel example", extends to.)
+ */
+SSD_API size_t ssd_fwd_varlen_workspace_size(const ssd_shape_t *shape, const int64_t *cu_seqlens, int64_t nseq);
+SSD_API ssd_status_t ssd_fwd_varlen(const ssd_shape_t *shape, const int64_t *cu_seqlens, int64_t nseq,
+                                    const void *x, const void *dt, const float *A, const void *B,
+                                    const void *C, const float *D, const float *init_states, void *y,
+                                    float *final_states, void *workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
+
+/*
  * Stage 1: dA_cumsum[b,h,c,q] = sum_{k<=q} dt[b, c*Q+k, h] * A[h].
  * ("Mamba-2 in NVIDIA cuTile", section "Why Mamba-2 is a useful kernel
  * example": the kernel that prepares the cumulative decay values.)
@@ -256,6 +285,24 @@ SSD_API ssd_status_t selective_scan_fwd(const ssd_shape_t *shape, const void *x,
                                 const void *C, const float *D,
                                 const float *init_state, void *y,
                                 float *final_state, cudaStream_t stream);
+
+/*
+ * Recurrent (decode) step: one new token per sequence advances the state in
+ * place and gives that token's output -- the recurrence itself for a single
+ * step, O(P N) work per head with a state of constant size (the inference
+ * mode of the da_be19 thread, post 5/6):
+ *   state[b,h] <- exp(dt[b,h] A[h]) state[b,h] + dt[b,h] x[b,h] B[b,g(h)]^T
+ *   y[b,h]      = state[b,h] C[b,g(h)] + D[h] x[b,h]
+ * Layouts: x [b, H, P], dt [b, H], B, C [b, G, N] (T = shape->dtype), A, D [H]
+ * fp32 (D may be NULL), state [b, H, P, N] fp32 (read and written), y
+ * [b, H, P] (shape->ydtype).  shape->seqlen and chunk_size are ignored (one
+ * step).  Running a sequence token by token through this call gives the
+ * same result as ssd_fwd over the whole sequence (up to rounding); a state
+ * left by ssd_fwd (final_state) continues directly.
+ */
+SSD_API ssd_status_t ssd_decode_step(const ssd_shape_t *shape, const void *x, const void *dt,
+                                     const float *A, const void *B, const void *C, const float *D,
+                                     float *state, void *y, cudaStream_t stream);
 
 /*
  * Launch timing (instrumentation; the pages have no counterpart).  While

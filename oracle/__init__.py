@@ -134,20 +134,31 @@ def ssd_recurrence(x, dt, A, B, C, D=None, init_state=None, snap_every=None, lib
     return y, final
 
 
+def _pad_steps(a, Lp):
+    """a [b, L, ...] padded with zero steps to length Lp along axis 1."""
+    if a.shape[1] == Lp:
+        return a
+    pad = [(0, 0)] * a.ndim
+    pad[1] = (0, Lp - a.shape[1])
+    return np.pad(a, pad)
+
+
 def chunk_cumsum(dt, A, chunk_size):
-    """Inclusive running sum of dt*A inside each chunk: [b, H, nc, Q].
+    """Inclusive running sum of dt*A inside each chunk: [b, H, nc, Q],
+    nc = ceil(L / Q).
 
     ("Mamba-2 in NVIDIA cuTile", section "Why Mamba-2 is a useful kernel
     example": the first kernel prepares the cumulative decay values.)
-    Requires L % Q == 0 (the GPU layout has no ragged chunk).
+    A partial last chunk (L % Q != 0) holds its missing steps as dt = 0
+    steps: the running sum stays at its last value.
     """
     dt = _f64(dt)
     A = _f64(A)
     b, L, H = dt.shape
     Q = int(chunk_size)
-    assert L % Q == 0
-    dA = dt * A[None, None, :]                               # [b, L, H]
-    dA = dA.reshape(b, L // Q, Q, H)
+    nc = -(-L // Q)
+    dA = _pad_steps(dt * A[None, None, :], nc * Q)          # [b, nc*Q, H]
+    dA = dA.reshape(b, nc, Q, H)
     return np.cumsum(dA, axis=2).transpose(0, 3, 1, 2).copy()  # [b, H, nc, Q]
 
 
@@ -156,14 +167,15 @@ def chunk_states(x, dt, A, B, chunk_size):
 
     Each chunk is run through the recurrence as an independent sequence, so
     the value is by definition sum_q exp(sum_{k>q} dt_k A) dt_q x_q B_q^T over
-    the chunk.  Requires L % Q == 0.
+    the chunk.  A partial last chunk (L % Q != 0) is run over its own steps
+    (as dt = 0 steps, the missing ones neither decay nor feed the state).
     """
     x, dt, B = _f64(x), _f64(dt), _f64(B)
     b, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     Q = int(chunk_size)
-    assert L % Q == 0
-    nc = L // Q
+    nc = -(-L // Q)
+    x, dt, B = (_pad_steps(a, nc * Q) for a in (x, dt, B))
     zeros_c = np.zeros((b * nc, Q, G, N))
     _, fin = ssd_recurrence(x.reshape(b * nc, Q, H, P), dt.reshape(b * nc, Q, H),
                             A, B.reshape(b * nc, Q, G, N), zeros_c)

@@ -31,7 +31,8 @@ EXPORTED = ("ssd_status_string", "ssd_abi_version", "ssd_fwd_workspace_size", "s
             "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
             "selective_scan_fwd", "ssd_launch_timing_enable", "ssd_launch_timing_read",
             "ssd_launch_timing_name", "ssd_fwd_noalloc", "ssd_chunk_scan_workspace_size",
-            "ssd_get_device_status", "ssd_selftest_scan_timeout")
+            "ssd_get_device_status", "ssd_selftest_scan_timeout", "ssd_decode_step",
+            "ssd_fwd_varlen_workspace_size", "ssd_fwd_varlen")
 
 
 class ssd_shape_t(ctypes.Structure):
@@ -76,6 +77,11 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_chunk_scan_workspace_size.restype = sz
         lib.ssd_selftest_scan_timeout.argtypes = [shp] + [vp] * 9 + [sz, ctypes.c_uint64, vp]
         lib.ssd_get_device_status.argtypes = [vp]
+        lib.ssd_decode_step.argtypes = [shp] + [vp] * 9
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.ssd_fwd_varlen_workspace_size.argtypes = [shp, i64p, ctypes.c_int64]
+        lib.ssd_fwd_varlen_workspace_size.restype = sz
+        lib.ssd_fwd_varlen.argtypes = [shp, i64p, ctypes.c_int64] + [vp] * 10 + [sz, vp]
         lib.selective_scan_fwd.argtypes = [shp] + [vp] * 9 + [vp]
         lib.ssd_launch_timing_enable.argtypes = [i32]
         lib.ssd_launch_timing_read.argtypes = [ctypes.POINTER(ctypes.c_float), i32]
@@ -85,7 +91,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_fwd_noalloc.restype = i32
         for name in ("ssd_fwd", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
                      "selective_scan_fwd", "ssd_launch_timing_enable", "ssd_launch_timing_read",
-                     "ssd_fwd_noalloc", "ssd_get_device_status", "ssd_selftest_scan_timeout"):
+                     "ssd_fwd_noalloc", "ssd_get_device_status", "ssd_selftest_scan_timeout", "ssd_decode_step",
+                     "ssd_fwd_varlen"):
             getattr(lib, name).restype = i32
         if path == LIB_PATH:
             _lib = lib
@@ -220,7 +227,7 @@ def ssd_chunk_cumsum(dt, A, chunk_size, *, out=None, stream=None):
     _need(dt, "dt")
     _need(A, "A", torch.float32, (H,))
     Q = int(chunk_size)
-    nc = L // Q if Q > 0 else 0
+    nc = -(-L // Q) if Q > 0 else 0
     if out is None:
         out = torch.empty((b, H, nc, Q), device=dt.device, dtype=torch.float32)
     _need(out, "dA_cumsum", torch.float32, (b, H, nc, Q))
@@ -337,6 +344,63 @@ def selective_scan_fwd(x, dt, A, B, C, D=None, init_state=None, *, y=None, final
     return y, final_state
 
 
+def ssd_fwd_varlen(x, dt, A, B, C, D=None, init_states=None, cu_seqlens=None, chunk_size=64, *, y=None,
+                   final_states=None, return_final_states=True, y_dtype=torch.float32, workspace=None, stream=None):
+    """Packed variable-length batch: x [1, Ltot, H, P] etc. hold nseq
+    sequences back to back; ``cu_seqlens`` (a host sequence of nseq + 1
+    offsets) marks them.  Returns ``(y, final_states [nseq, H, P, N])``."""
+    lib = load_library()
+    b, L, H, P, G, N = _check_inputs(x, dt, A, B, C, D, None)
+    cu = [int(v) for v in (cu_seqlens.tolist() if isinstance(cu_seqlens, torch.Tensor) else cu_seqlens)]
+    nseq = len(cu) - 1
+    _need(init_states, "init_states", torch.float32, (nseq, H, P, N))
+    if y is not None:
+        y_dtype = y.dtype
+    shape = make_shape(x, B, chunk_size, y_dtype)
+    if y is None:
+        y = torch.empty(x.shape, device=x.device, dtype=y_dtype)
+    _need(y, "y", y_dtype, x.shape)
+    if final_states is None and return_final_states:
+        final_states = torch.empty((nseq, H, P, N), device=x.device, dtype=torch.float32)
+    _need(final_states, "final_states", torch.float32, (nseq, H, P, N))
+    cu_arr = (ctypes.c_int64 * len(cu))(*cu)
+    ws_bytes = int(lib.ssd_fwd_varlen_workspace_size(ctypes.byref(shape), cu_arr, nseq))
+    if workspace is None or workspace.numel() < ws_bytes:
+        workspace = torch.empty(max(ws_bytes, 16), device=x.device, dtype=torch.uint8)
+    _check("ssd_fwd_varlen", lib.ssd_fwd_varlen(ctypes.byref(shape), cu_arr, nseq, _ptr(x), _ptr(dt), _ptr(A),
+                                                _ptr(B), _ptr(C), _ptr(D), _ptr(init_states), _ptr(y),
+                                                _ptr(final_states), _ptr(workspace), workspace.numel(),
+                                                _stream(stream)))
+    return y, final_states
+
+
+def ssd_decode_step(x, dt, A, B, C, D=None, *, state, y=None, y_dtype=torch.float32, stream=None):
+    """One recurrent step: ``state`` [b, H, P, N] fp32 is advanced in place by
+    the token x [b, H, P], dt [b, H], B, C [b, G, N]; returns y [b, H, P]."""
+    lib = load_library()
+    if x.dim() != 3 or B.dim() != 3:
+        raise ValueError("x must be [b, H, P] and B, C [b, G, N]")
+    b, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    _need(x, "x")
+    _need(dt, "dt", x.dtype, (b, H))
+    _need(A, "A", torch.float32, (H,))
+    _need(B, "B", x.dtype, (b, G, N))
+    _need(C, "C", x.dtype, (b, G, N))
+    _need(D, "D", torch.float32, (H,))
+    _need(state, "state", torch.float32, (b, H, P, N))
+    if y is not None:
+        y_dtype = y.dtype
+    if y is None:
+        y = torch.empty((b, H, P), device=x.device, dtype=y_dtype)
+    _need(y, "y", y_dtype, (b, H, P))
+    yc = SSD_DTYPE_F32 if y_dtype == torch.float32 else _dtype_code(torch.empty(0, dtype=y_dtype))
+    shape = ssd_shape_t(b, 1, H, P, N, G, 0, _dtype_code(x), yc)
+    _check("ssd_decode_step", lib.ssd_decode_step(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                                  _ptr(C), _ptr(D), _ptr(state), _ptr(y), _stream(stream)))
+    return y
+
+
 def launch_timing(enable: bool) -> None:
     """Turn per-launch CUDA-event timing inside the library on or off."""
     _check("ssd_launch_timing_enable", load_library().ssd_launch_timing_enable(1 if enable else 0))
@@ -352,6 +416,6 @@ def launch_times_ms() -> list:
     return [((lib.ssd_launch_timing_name(i) or b"?").decode(), float(buf[i])) for i in range(min(n, 16))]
 
 
-__all__ = ["get_device_status", "check_device_status", "selftest_scan_timeout", "ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
+__all__ = ["ssd_fwd_varlen", "ssd_decode_step", "get_device_status", "check_device_status", "selftest_scan_timeout", "ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
            "ssd_state_passing", "ssd_chunk_scan", "selective_scan_fwd", "ssd_shape_t", "SSDError",
            "load_library", "status_string", "EXPORTED", "LIB_PATH"]

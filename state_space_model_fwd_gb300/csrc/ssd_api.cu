@@ -22,7 +22,8 @@ bool pow2_in(int64_t v, int64_t lo, int64_t hi) {
 }
 
 // Shape checks shared by every entry point.  `need_chunks` adds the chunked
-// algorithm's restrictions (Q in {64, 128}, L % Q == 0).
+// algorithm's restriction Q in {64, 128}; the last chunk may be partial
+// (nc = ceil(L / Q)).
 ssd_status_t check_shape(const ssd_shape_t *s, bool need_chunks, Dims *d) {
     if (!s) return SSD_ERR_INVALID_ARG;
     if (s->batch < 0 || s->seqlen < 0 || s->nheads <= 0 || s->headdim <= 0 || s->dstate <= 0 ||
@@ -35,7 +36,6 @@ ssd_status_t check_shape(const ssd_shape_t *s, bool need_chunks, Dims *d) {
     if (need_chunks) {
         if (s->chunk_size <= 0) return SSD_ERR_INVALID_ARG;
         if (s->chunk_size != 64 && s->chunk_size != 128) return SSD_ERR_UNSUPPORTED;
-        if (s->seqlen % s->chunk_size != 0) return SSD_ERR_UNSUPPORTED;
     }
     // every index is formed in int64; keep each grid dimension in range
     if (s->batch > 65535 || s->nheads > 65535) return SSD_ERR_UNSUPPORTED;
@@ -46,7 +46,7 @@ ssd_status_t check_shape(const ssd_shape_t *s, bool need_chunks, Dims *d) {
     d->N = s->dstate;
     d->G = s->ngroups;
     d->Q = need_chunks ? s->chunk_size : 64;
-    d->nc = need_chunks ? s->seqlen / s->chunk_size : 0;
+    d->nc = need_chunks ? (s->seqlen + s->chunk_size - 1) / s->chunk_size : 0;
     d->hpg = (int)(s->nheads / s->ngroups);
     return SSD_OK;
 }
@@ -137,10 +137,12 @@ cudaError_t device_status_word(unsigned **out) {
 // stream between a read and a clear is lost).
 __global__ void take_status_kernel(unsigned *word, unsigned *out) { *out = atomicExch(word, 0u); }
 
-// Workspace of the unfused (four-launch) path: cumsum, chunk states,
+// Workspace of the unfused (four-launch) path: cumsum [b, H, nc, Q] (nc Q
+// >= L: a partial last chunk takes a whole chunk's entries), chunk states,
 // states entering chunks.
+size_t staged_cum_bytes(const Dims &d) { return align256(sizeof(float) * d.b * d.H * d.nc * d.Q); }
 size_t staged_workspace(const Dims &d) {
-    return align256(sizeof(float) * d.b * d.H * d.L) + 2 * align256(sizeof(float) * d.b * d.nc * d.H * d.P * d.N);
+    return staged_cum_bytes(d) + 2 * align256(sizeof(float) * d.b * d.nc * d.H * d.P * d.N);
 }
 
 template <typename T, typename TY>
@@ -149,10 +151,9 @@ ssd_status_t fwd_staged(const Dims &d, const void *x, const void *dt, const floa
                         cudaStream_t s) {
     char *w = static_cast<char *>(ws);
     float *cum = reinterpret_cast<float *>(w);
-    float *states = reinterpret_cast<float *>(w + align256(sizeof(float) * d.b * d.H * d.L));
-    float *states_in =
-        reinterpret_cast<float *>(w + align256(sizeof(float) * d.b * d.H * d.L) +
-                                  align256(sizeof(float) * d.b * d.nc * d.H * d.P * d.N));
+    float *states = reinterpret_cast<float *>(w + staged_cum_bytes(d));
+    float *states_in = reinterpret_cast<float *>(w + staged_cum_bytes(d) +
+                                                 align256(sizeof(float) * d.b * d.nc * d.H * d.P * d.N));
     const T *xt = static_cast<const T *>(x), *dtt = static_cast<const T *>(dt);
     const T *Bt = static_cast<const T *>(B), *Ct = static_cast<const T *>(C);
     ssd::timing_begin(s);
@@ -286,6 +287,75 @@ ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void *dt, co
     return fwd_staged<bf16, bf16>(d, x, dt, A, B, C, D, init_state, y, final_state, workspace, stream);
 }
 
+}  // extern "C"
+
+namespace {
+// Validates a packed variable-length batch; on success the sub-shape of
+// every sequence is `one` with its seqlen replaced.
+ssd_status_t check_varlen(const ssd_shape_t *shape, const int64_t *cu, int64_t nseq, ssd_shape_t *one) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, true, &d);
+    if (st != SSD_OK) return st;
+    if (shape->batch != 1 || nseq < 0 || (nseq > 0 && !cu)) return SSD_ERR_INVALID_ARG;
+    if (nseq > 0 && (cu[0] != 0 || cu[nseq] != shape->seqlen)) return SSD_ERR_INVALID_ARG;
+    for (int64_t s = 0; s < nseq; ++s)
+        if (cu[s + 1] < cu[s]) return SSD_ERR_INVALID_ARG;
+    *one = *shape;
+    return SSD_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t ssd_fwd_varlen_workspace_size(const ssd_shape_t *shape, const int64_t *cu_seqlens, int64_t nseq) {
+    ssd_shape_t one;
+    if (check_varlen(shape, cu_seqlens, nseq, &one) != SSD_OK) return 0;
+    size_t need = 0;
+    for (int64_t s = 0; s < nseq; ++s) {
+        one.seqlen = cu_seqlens[s + 1] - cu_seqlens[s];
+        if (one.seqlen == 0) continue;
+        const size_t w = ssd_fwd_workspace_size(&one);
+        if (w > need) need = w;
+    }
+    return need;
+}
+
+ssd_status_t ssd_fwd_varlen(const ssd_shape_t *shape, const int64_t *cu_seqlens, int64_t nseq, const void *x,
+                            const void *dt, const float *A, const void *B, const void *C, const float *D,
+                            const float *init_states, void *y, float *final_states, void *workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+    ssd_shape_t one;
+    ssd_status_t st = check_varlen(shape, cu_seqlens, nseq, &one);
+    if (st != SSD_OK) return st;
+    if (nseq == 0) return SSD_OK;
+    if (!ptrs_ok({x, dt, A, B, C, y}, {D, init_states, final_states})) return SSD_ERR_INVALID_ARG;
+    const size_t e = shape->dtype == SSD_DTYPE_F32 ? 4 : 2;
+    const size_t ye = shape->ydtype == SSD_DTYPE_F32 ? 4 : 2;
+    const int64_t H = shape->nheads, P = shape->headdim, N = shape->dstate, G = shape->ngroups;
+    // every sequence's pointers are checked before anything is enqueued
+    for (int64_t s = 0; s < nseq; ++s) {
+        const int64_t t0 = cu_seqlens[s];
+        if (cu_seqlens[s + 1] == t0) continue;
+        const char *px = static_cast<const char *>(x) + t0 * H * P * e;
+        const char *pdt = static_cast<const char *>(dt) + t0 * H * e;
+        const char *pb = static_cast<const char *>(B) + t0 * G * N * e;
+        const char *py = static_cast<const char *>(y) + t0 * H * P * ye;
+        if (!ptrs_ok({px, pdt, pb, py}, {})) return SSD_ERR_INVALID_ARG;
+    }
+    if (ssd_fwd_varlen_workspace_size(shape, cu_seqlens, nseq) > workspace_bytes) return SSD_ERR_WORKSPACE;
+    for (int64_t s = 0; s < nseq; ++s) {
+        const int64_t t0 = cu_seqlens[s];
+        one.seqlen = cu_seqlens[s + 1] - t0;
+        const float *ini = init_states ? init_states + s * H * P * N : nullptr;
+        float *fin = final_states ? final_states + s * H * P * N : nullptr;
+        st = ssd_fwd(&one, static_cast<const char *>(x) + t0 * H * P * e, static_cast<const char *>(dt) + t0 * H * e,
+                     A, static_cast<const char *>(B) + t0 * G * N * e, static_cast<const char *>(C) + t0 * G * N * e,
+                     D, ini, static_cast<char *>(y) + t0 * H * P * ye, fin, workspace, workspace_bytes, stream);
+        if (st != SSD_OK) return st;
+    }
+    return SSD_OK;
+}
+
 ssd_status_t ssd_chunk_cumsum(const ssd_shape_t *shape, const void *dt, const float *A, float *dA_cumsum,
                               cudaStream_t stream) {
     Dims d;
@@ -414,6 +484,27 @@ ssd_status_t ssd_get_device_status(cudaStream_t stream) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return from_cuda(e);
     return (v & 1u) ? SSD_ERR_TIMEOUT : SSD_OK;
+}
+
+ssd_status_t ssd_decode_step(const ssd_shape_t *shape, const void *x, const void *dt, const float *A, const void *B,
+                             const void *C, const float *D, float *state, void *y, cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, false, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0) return SSD_OK;
+    if (!ptrs_ok({x, dt, A, B, C, state, y}, {D})) return SSD_ERR_INVALID_ARG;
+    ssd::timing_begin(stream);
+    if (shape->dtype == SSD_DTYPE_F32)
+        return from_cuda(ssd::launch_decode_step<float, float>(
+            d, static_cast<const float *>(x), static_cast<const float *>(dt), A, static_cast<const float *>(B),
+            static_cast<const float *>(C), D, state, static_cast<float *>(y), stream));
+    const bf16 *xb = static_cast<const bf16 *>(x), *dtb = static_cast<const bf16 *>(dt);
+    const bf16 *Bb = static_cast<const bf16 *>(B), *Cb = static_cast<const bf16 *>(C);
+    if (shape->ydtype == SSD_DTYPE_F32)
+        return from_cuda(
+            ssd::launch_decode_step<bf16, float>(d, xb, dtb, A, Bb, Cb, D, state, static_cast<float *>(y), stream));
+    return from_cuda(
+        ssd::launch_decode_step<bf16, bf16>(d, xb, dtb, A, Bb, Cb, D, state, static_cast<bf16 *>(y), stream));
 }
 
 ssd_status_t selective_scan_fwd(const ssd_shape_t *shape, const void *x, const void *dt, const float *A,

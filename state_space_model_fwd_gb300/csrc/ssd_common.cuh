@@ -54,4 +54,9 @@ cudaError_t launch_selective_scan(const Dims &d, const T *x, const T *dt, const 
                                   const T *C, const float *D, const float *init, TY *y, float *final_state,
                                   cudaStream_t s);
 
+// Recurrent step (ssd_decode.cu).
+template <typename T, typename TY>
+cudaError_t launch_decode_step(const Dims &d, const T *x, const T *dt, const float *A, const T *B, const T *C,
+                               const float *D, float *state, TY *y, cudaStream_t s);
+
 }  // namespace ssd

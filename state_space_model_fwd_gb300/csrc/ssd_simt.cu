@@ -34,8 +34,10 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(Dims d, const T *__re
     float run = 0.f;
 #pragma unroll
     for (int i = 0; i < QPL; ++i) {
+        // steps past L (a partial last chunk) count as dt = 0: the cumulative
+        // decay stays at its last value
         const int64_t t = c * d.Q + lane * QPL + i;
-        run += to_f32(dt[(b * d.L + t) * d.H + h]) * a;
+        if (t < d.L) run += to_f32(dt[(b * d.L + t) * d.H + h]) * a;
         v[i] = run;
     }
     float tot = run;
@@ -112,7 +114,7 @@ __global__ void __launch_bounds__(256) chunk_state_simt_kernel(Dims d, const T *
     const int tid = threadIdx.x;
     const float *cc = cum + ((b * d.H + h) * d.nc + c) * d.Q;
     for (int q = tid; q < d.Q; q += blockDim.x)
-        w_s[q] = expf(cc[d.Q - 1] - cc[q]) * to_f32(dt[(b * d.L + c * d.Q + q) * d.H + h]);
+        w_s[q] = c * d.Q + q < d.L ? expf(cc[d.Q - 1] - cc[q]) * to_f32(dt[(b * d.L + c * d.Q + q) * d.H + h]) : 0.f;
     __syncthreads();
     const int tr = tid >> 4, tcol = tid & 15;
     for (int64_t p0 = 0; p0 < d.P; p0 += kTile)
@@ -122,10 +124,11 @@ __global__ void __launch_bounds__(256) chunk_state_simt_kernel(Dims d, const T *
                 for (int i = tid; i < kTile * kTile; i += blockDim.x) {
                     const int q = i / kTile, k = i % kTile;
                     const int64_t t = c * d.Q + q0 + q;
-                    As[q * kLd + k] = (p0 + k < d.P)
+                    const bool in = t < d.L;
+                    As[q * kLd + k] = (in && p0 + k < d.P)
                                           ? w_s[q0 + q] * to_f32(x[((b * d.L + t) * d.H + h) * d.P + p0 + k])
                                           : 0.f;
-                    Bs[q * kLd + k] = (n0 + k < d.N) ? to_f32(B[((b * d.L + t) * d.G + g) * d.N + n0 + k]) : 0.f;
+                    Bs[q * kLd + k] = (in && n0 + k < d.N) ? to_f32(B[((b * d.L + t) * d.G + g) * d.N + n0 + k]) : 0.f;
                 }
                 __syncthreads();
                 mma_tile(As, kLd, Bs, kLd, kTile, tr * 4, tcol * 4, acc);
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(Dims d, const T *_
     const float *cc = cum + ((b * d.H + h) * d.nc + c) * d.Q;
     for (int q = tid; q < Q; q += blockDim.x) {
         cum_s[q] = cc[q];
-        dt_s[q] = to_f32(dt[(b * d.L + t_base + q) * d.H + h]);
+        dt_s[q] = t_base + q < d.L ? to_f32(dt[(b * d.L + t_base + q) * d.H + h]) : 0.f;
     }
     const int nt = Q / kTile;
     // masked score matrix, tile by tile
@@ -193,8 +196,11 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(Dims d, const T *_
                 for (int i = tid; i < kTile * kTile; i += blockDim.x) {
                     const int r = i / kTile, k = i % kTile;
                     const bool ok = n0 + k < d.N;
-                    As[k * kLd + r] = ok ? to_f32(C[((b * d.L + t_base + ti * kTile + r) * d.G + g) * d.N + n0 + k]) : 0.f;
-                    Bs[k * kLd + r] = ok ? to_f32(B[((b * d.L + t_base + si * kTile + r) * d.G + g) * d.N + n0 + k]) : 0.f;
+                    const bool tin = t_base + ti * kTile + r < d.L, sin_ = t_base + si * kTile + r < d.L;
+                    As[k * kLd + r] =
+                        ok && tin ? to_f32(C[((b * d.L + t_base + ti * kTile + r) * d.G + g) * d.N + n0 + k]) : 0.f;
+                    Bs[k * kLd + r] =
+                        ok && sin_ ? to_f32(B[((b * d.L + t_base + si * kTile + r) * d.G + g) * d.N + n0 + k]) : 0.f;
                 }
                 __syncthreads();
                 mma_tile(As, kLd, Bs, kLd, kTile, tr * 4, tcol * 4, acc);
@@ -216,7 +222,7 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(Dims d, const T *_
                 __syncthreads();
                 for (int i = tid; i < kTile * kTile; i += blockDim.x) {
                     const int s = i / kTile, k = i % kTile;
-                    Bs[s * kLd + k] = (p0 + k < d.P)
+                    Bs[s * kLd + k] = (p0 + k < d.P && t_base + si * kTile + s < d.L)
                                           ? to_f32(x[((b * d.L + t_base + si * kTile + s) * d.H + h) * d.P + p0 + k])
                                           : 0.f;
                 }
@@ -229,8 +235,9 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(Dims d, const T *_
                     const int r = i / kTile, k = i % kTile;
                     const bool ok = n0 + k < d.N;
                     const int t = ti * kTile + r;
-                    As[k * kLd + r] =
-                        ok ? to_f32(C[((b * d.L + t_base + t) * d.G + g) * d.N + n0 + k]) * __expf(cum_s[t]) : 0.f;
+                    As[k * kLd + r] = ok && t_base + t < d.L
+                                          ? to_f32(C[((b * d.L + t_base + t) * d.G + g) * d.N + n0 + k]) * __expf(cum_s[t])
+                                          : 0.f;
                     Bs[k * kLd + r] = (ok && p0 + r < d.P) ? hin[(p0 + r) * d.N + n0 + k] : 0.f;
                 }
                 __syncthreads();
@@ -239,6 +246,7 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(Dims d, const T *_
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int64_t t = t_base + ti * kTile + tr * 4 + i;
+                if (t >= d.L) continue;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int64_t p = p0 + tcol * 4 + j;

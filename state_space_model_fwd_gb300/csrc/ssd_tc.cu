@@ -268,7 +268,9 @@ __device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int
         for (int j = 0; j < ChunkDt<C>::QPL; ++j) {
             const long long h = h0 + hh;
             const long long t = (long long)c * C::Q + ChunkDt<C>::QPL * lane + j;
-            o.d[hh][j] = h < prm.H ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + t) * prm.H + h)) : 0.f;
+            // (steps past L in a partial last chunk: dt = 0, as the TMA path's fill)
+            o.d[hh][j] = h < prm.H && t < prm.L ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + t) * prm.H + h))
+                                                : 0.f;
         }
 }
 
@@ -1434,9 +1436,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 tmem_ld16(tr, *reinterpret_cast<float(*)[16]>(acc));
                 tmem_ld_wait();
                 // straight to global memory: a warp writes one contiguous
-                // run of 32 p per step
+                // run of 32 p per step; a partial last chunk stops at L
                 YT *yc = yg + (long long)cp * C::Q * ystep;
-                if (live)
+                const long long tleft = prm.L - ((long long)(c0 + cp) * C::Q + part * NS);
+                if (live && tleft < NS) {
+#pragma unroll 1
+                    for (int j = 0; j < tleft; ++j) {
+                        const uint32_t w = xprev[j / 2];
+                        const float xv = __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+                        store_y<YT>(yc + j * ystep, fmaf(dh, xv, ef[j] * acc[j]));
+                    }
+                } else if (live)
 #pragma unroll
                     for (int j = 0; j < NS; j += 4) {
                         const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
@@ -1765,7 +1775,7 @@ Dims fwd_tiles(const Dims &d) {
     Dims t = d;
     if (d.Q == 128) {
         t.Q = 64;
-        t.nc = d.nc * 2;
+        t.nc = (d.L + 63) / 64;
     }
     return t;
 }

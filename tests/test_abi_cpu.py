@@ -64,7 +64,6 @@ def fwd(lib, s, ptrs=None, ws=FAKE, ws_bytes=1 << 40):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(nheads=6, ngroups=4), INVALID),        # H % G != 0
-    (dict(seqlen=250), UNSUPPORTED),              # ragged last chunk
     (dict(chunk_size=32), UNSUPPORTED),
     (dict(chunk_size=0), INVALID),
     (dict(headdim=48), UNSUPPORTED),
@@ -97,7 +96,10 @@ def test_workspace_checks(lib):
     assert need > 0
     assert fwd(lib, s, ws=None) == WORKSPACE
     assert fwd(lib, s, ws_bytes=need - 1) == WORKSPACE
-    assert lib.ssd_fwd_workspace_size(ctypes.byref(shape(seqlen=250))) == 0
+    # a partial last chunk is supported: its workspace covers ceil(L / Q) chunks
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(shape(seqlen=250))) == lib.ssd_fwd_workspace_size(
+        ctypes.byref(shape(seqlen=256)))
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(shape(chunk_size=32))) == 0
 
 
 def test_empty_batch_is_a_no_op(lib):
@@ -105,7 +107,7 @@ def test_empty_batch_is_a_no_op(lib):
 
 
 def test_stage_entry_points_validate(lib):
-    s = shape(seqlen=100)
+    s = shape(chunk_size=96)
     assert lib.ssd_chunk_cumsum(ctypes.byref(s), FAKE, FAKE, FAKE, None) == UNSUPPORTED
     s = shape()
     assert lib.ssd_chunk_cumsum(ctypes.byref(s), None, FAKE, FAKE, None) == INVALID
@@ -165,3 +167,32 @@ def test_workspace_layout_of_the_tensor_core_path(lib, name):
     if nseg > 1:
         want += _a256(4 * b * nseg * H * P * N) + _a256(4 * b * nseg * H)
     assert lib.ssd_fwd_workspace_size(ctypes.byref(s)) == want
+
+
+def test_decode_step_validates(lib):
+    s = shape(seqlen=1)
+    p = [FAKE] * 8
+    assert lib.ssd_decode_step(ctypes.byref(shape(nheads=6, ngroups=4)), *p, None) == INVALID
+    for i in (0, 1, 2, 3, 4, 6, 7):                  # x, dt, A, B, C, state, y required; D optional
+        q = list(p)
+        q[i] = None
+        assert lib.ssd_decode_step(ctypes.byref(s), *q, None) == INVALID, i
+    assert lib.ssd_decode_step(ctypes.byref(shape(batch=0)), *([None] * 8), None) == OK
+
+
+def test_varlen_validates(lib):
+    i64 = ctypes.c_int64
+    s = shape(batch=1, seqlen=300)
+    good = (i64 * 4)(0, 100, 164, 300)
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), good, 3) == lib.ssd_fwd_workspace_size(
+        ctypes.byref(shape(batch=1, seqlen=136)))
+    for bad in ((0, 100, 90, 300), (1, 100, 164, 300), (0, 100, 164, 299)):
+        arr = (i64 * 4)(*bad)
+        assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), arr, 3) == 0
+        assert lib.ssd_fwd_varlen(ctypes.byref(s), arr, 3, *([FAKE] * 10), 1 << 40, None) == INVALID
+    assert lib.ssd_fwd_varlen(ctypes.byref(shape(batch=2, seqlen=300)), good, 3, *([FAKE] * 10), 1 << 40,
+                              None) == INVALID
+    # a sequence start that leaves dt misaligned (H = 4 bf16: 8 bytes a step)
+    odd = (i64 * 3)(0, 3, 300)
+    assert lib.ssd_fwd_varlen(ctypes.byref(s), odd, 2, *([FAKE] * 10), 1 << 40, None) == INVALID
+    assert lib.ssd_fwd_varlen(ctypes.byref(s), good, 3, *([FAKE] * 10), 16, None) == WORKSPACE

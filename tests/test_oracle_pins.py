@@ -46,14 +46,16 @@ def test_cumsum_pin_catches_mutant(name):
         pins.pin_chunk_cumsum(CUMSUM_MUTANTS[name])
 
 
-@pytest.mark.parametrize("Q", [1, 4, 16, 32])
-def test_stage_definitions_match_chunked_algorithm(Q):
+@pytest.mark.parametrize("L,Q", [(64, 1), (64, 4), (64, 16), (64, 32), (60, 16), (61, 25)])
+def test_stage_definitions_match_chunked_algorithm(L, Q):
     """The per-stage oracle intermediates (cumulative decay, chunk-local
     states, states entering each chunk) equal the stage values of the chunked
-    algorithm written out independently in oracle_pins.chunked_form."""
-    x, dt, A, B, C, D, s0 = pins.small_problem(21, b=2, L=64, H=4, P=3, N=5, G=2)
+    algorithm written out independently in oracle_pins.chunked_form, a
+    partial last chunk included (its missing cumsum entries repeat the last
+    one: dt = 0 steps)."""
+    x, dt, A, B, C, D, s0 = pins.small_problem(21, b=2, L=L, H=4, P=3, N=5, G=2)
     _, fin, cums, locs, ins = pins.chunked_form(x, dt, A, B, C, D, s0, Q)
-    nc = 64 // Q
+    nc = -(-L // Q)
     cum = oracle.chunk_cumsum(dt, A, Q)
     st = oracle.chunk_states(x, dt, A, B, Q)
     sin, f2 = oracle.states_entering(x, dt, A, B, C, Q, s0)
@@ -61,7 +63,9 @@ def test_stage_definitions_match_chunked_algorithm(Q):
     for b in range(2):
         for h in range(4):
             for c in range(nc):
-                pins._close(cum[b, h, c], cums[b, h, c], what="cumsum")
+                n = len(cums[b, h, c])
+                pins._close(cum[b, h, c, :n], cums[b, h, c], what="cumsum")
+                assert np.all(cum[b, h, c, n:] == cum[b, h, c, n - 1])
                 pins._close(st[b, c, h], locs[b, h, c], what="chunk state")
                 pins._close(sin[b, c, h], ins[b, h, c], what="state entering chunk")
     pins._close(f2, fin, what="final")
