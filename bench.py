@@ -628,7 +628,70 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
         out[name] = rec
         del t, y, fin, ws
         torch.cuda.empty_cache()
+    out["crossover"] = crossover_sweep(ssd, dev, flush, steps)
+    out["decode"] = decode_sweep(ssd, dev, flush, peaks, steps)
     return out
+
+
+def crossover_sweep(ssd, dev, flush, steps):
+    """Chunked (ssd_fwd) against the quadratic dual form (ssd_fwd_quadratic)
+    on the 130M-shaped layer at short lengths: ms of each, per length."""
+    import torch
+    rows = []
+    for L in (64, 128, 256, 512, 1024):
+        cfg = si.CONFIGS[WORKLOAD].replace(seqlen=L)
+        t = si.make_inputs(cfg).to_torch(dev)
+        y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
+        fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), device=dev, dtype=torch.float32)
+        ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], 64, torch.bfloat16))),
+                         device=dev, dtype=torch.uint8)
+        args = (t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"])
+        chunked = time_graph(lambda: ssd.ssd_fwd(*args, 64, y=y, final_state=fin, workspace=ws), flush, steps)
+        quad = time_graph(lambda: ssd.ssd_fwd_quadratic(*args, y=y, final_state=fin), flush, steps)
+        rows.append({"seqlen": L, "tokens": cfg.tokens, "chunked_ms": chunked, "quadratic_ms": quad,
+                     "faster": "quadratic" if quad < chunked else "chunked"})
+    return {"workload": "130M-shaped layer (b=4, H=24, P=64, N=128, G=1), bf16 y",
+            "timing": "CUDA graph of one call, replayed after an L2 flush; device events around the replay",
+            "rows": rows}
+
+
+def time_graph(fn, flush, steps):
+    """Device time of fn captured in a CUDA graph (no host launch work inside
+    the timed region), L2 flushed before every replay."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return time_device(g.replay, flush, steps)
+
+
+def decode_sweep(ssd, dev, flush, peaks, steps):
+    """One recurrent step of the 2.7B-shaped layer for a batch of 64
+    sequences: the state (fp32) read and written once, bound by HBM."""
+    import torch
+    b, H, P, N, G = 64, 80, 64, 128, 1
+    gen = torch.Generator(device=dev).manual_seed(5)
+    x = torch.randn(b, H, P, device=dev, generator=gen).to(torch.bfloat16)
+    dt = (0.05 * torch.rand(b, H, device=dev, generator=gen)).to(torch.bfloat16)
+    A = -torch.rand(H, device=dev, generator=gen) * 4 - 1
+    B = (torch.randn(b, G, N, device=dev, generator=gen) / N ** 0.5).to(torch.bfloat16)
+    C = (torch.randn(b, G, N, device=dev, generator=gen) / N ** 0.5).to(torch.bfloat16)
+    D = torch.randn(H, device=dev, generator=gen)
+    state = 0.1 * torch.randn(b, H, P, N, device=dev, generator=gen)
+    y = torch.empty(b, H, P, device=dev, dtype=torch.bfloat16)
+    ms = time_device(lambda: ssd.ssd_decode_step(x, dt, A, B, C, D, state=state, y=y), flush, steps)
+    nbytes = 2 * state.numel() * 4 + x.numel() * 2 + y.numel() * 2 + dt.numel() * 2 + 2 * B.numel() * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"2.7B-shaped layer, one token for {b} sequences (b={b}, H={H}, P={P}, N={N})",
+            "ms": ms, "tokens_per_s": b / (ms * 1e-3), "bytes": nbytes, "achieved_gbs": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"]}
 
 
 def kernel_times(ssd, fn, flush, steps):

@@ -287,6 +287,25 @@ SSD_API ssd_status_t selective_scan_fwd(const ssd_shape_t *shape, const void *x,
                                 float *final_state, cudaStream_t stream);
 
 /*
+ * Quadratic (dual) form for short sequences: the same y and final_state as
+ * ssd_fwd, computed without chunks as
+ *   y     = (L o C B^T) (dt o x) + (exp(cum) o C) init^T + D x,
+ *   L_ts  = exp(cum_t - cum_s) for s <= t (0 above), cum = running sum of dt A,
+ *   final = sum_s exp(cum_{L-1} - cum_s) dt_s x_s^T B_s + exp(cum_{L-1}) init
+ * (the attention-like form that can beat the chunked algorithm on short
+ * sequences: the da_be19 thread, post 5/6).  Work grows with L^2, so it is
+ * offered for L <= 1024 only: bf16 inputs, P in {64, 128}, N in {64, 128},
+ * heads per group a multiple of 128 / P; SSD_ERR_UNSUPPORTED otherwise.
+ * shape->chunk_size is ignored.  No workspace.  D, init_state and
+ * final_state may be NULL.  A bounded wait that gives up is latched for
+ * ssd_get_device_status.
+ */
+SSD_API ssd_status_t ssd_fwd_quadratic(const ssd_shape_t *shape, const void *x, const void *dt,
+                                       const float *A, const void *B, const void *C, const float *D,
+                                       const float *init_state, void *y, float *final_state,
+                                       cudaStream_t stream);
+
+/*
  * Recurrent (decode) step: one new token per sequence advances the state in
  * place and gives that token's output -- the recurrence itself for a single
  * step, O(P N) work per head with a state of constant size (the inference

@@ -32,7 +32,7 @@ EXPORTED = ("ssd_status_string", "ssd_abi_version", "ssd_fwd_workspace_size", "s
             "selective_scan_fwd", "ssd_launch_timing_enable", "ssd_launch_timing_read",
             "ssd_launch_timing_name", "ssd_fwd_noalloc", "ssd_chunk_scan_workspace_size",
             "ssd_get_device_status", "ssd_selftest_scan_timeout", "ssd_decode_step",
-            "ssd_fwd_varlen_workspace_size", "ssd_fwd_varlen")
+            "ssd_fwd_varlen_workspace_size", "ssd_fwd_varlen", "ssd_fwd_quadratic")
 
 
 class ssd_shape_t(ctypes.Structure):
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH):
         lib.ssd_selftest_scan_timeout.argtypes = [shp] + [vp] * 9 + [sz, ctypes.c_uint64, vp]
         lib.ssd_get_device_status.argtypes = [vp]
         lib.ssd_decode_step.argtypes = [shp] + [vp] * 9
+        lib.ssd_fwd_quadratic.argtypes = [shp] + [vp] * 10
         i64p = ctypes.POINTER(ctypes.c_int64)
         lib.ssd_fwd_varlen_workspace_size.argtypes = [shp, i64p, ctypes.c_int64]
         lib.ssd_fwd_varlen_workspace_size.restype = sz
@@ -92,7 +93,7 @@ def load_library(path: str = LIB_PATH):
         for name in ("ssd_fwd", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
                      "selective_scan_fwd", "ssd_launch_timing_enable", "ssd_launch_timing_read",
                      "ssd_fwd_noalloc", "ssd_get_device_status", "ssd_selftest_scan_timeout", "ssd_decode_step",
-                     "ssd_fwd_varlen"):
+                     "ssd_fwd_varlen", "ssd_fwd_quadratic"):
             getattr(lib, name).restype = i32
         if path == LIB_PATH:
             _lib = lib
@@ -374,6 +375,27 @@ def ssd_fwd_varlen(x, dt, A, B, C, D=None, init_states=None, cu_seqlens=None, ch
     return y, final_states
 
 
+def ssd_fwd_quadratic(x, dt, A, B, C, D=None, init_state=None, *, y=None, final_state=None,
+                      return_final_state=True, y_dtype=torch.float32, stream=None):
+    """The quadratic (dual) form, y = (L o C B^T)(dt o x) + ..., for short
+    sequences (L <= 1024).  Returns ``(y, final_state)``."""
+    lib = load_library()
+    b, L, H, P, G, N = _check_inputs(x, dt, A, B, C, D, init_state)
+    if y is not None:
+        y_dtype = y.dtype
+    shape = make_shape(x, B, 0, y_dtype)
+    if y is None:
+        y = torch.empty(x.shape, device=x.device, dtype=y_dtype)
+    _need(y, "y", y_dtype, x.shape)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((b, H, P, N), device=x.device, dtype=torch.float32)
+    _need(final_state, "final_state", torch.float32, (b, H, P, N))
+    _check("ssd_fwd_quadratic", lib.ssd_fwd_quadratic(ctypes.byref(shape), _ptr(x), _ptr(dt), _ptr(A), _ptr(B),
+                                                      _ptr(C), _ptr(D), _ptr(init_state), _ptr(y),
+                                                      _ptr(final_state), _stream(stream)))
+    return y, final_state
+
+
 def ssd_decode_step(x, dt, A, B, C, D=None, *, state, y=None, y_dtype=torch.float32, stream=None):
     """One recurrent step: ``state`` [b, H, P, N] fp32 is advanced in place by
     the token x [b, H, P], dt [b, H], B, C [b, G, N]; returns y [b, H, P]."""
@@ -416,6 +438,6 @@ def launch_times_ms() -> list:
     return [((lib.ssd_launch_timing_name(i) or b"?").decode(), float(buf[i])) for i in range(min(n, 16))]
 
 
-__all__ = ["ssd_fwd_varlen", "ssd_decode_step", "get_device_status", "check_device_status", "selftest_scan_timeout", "ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
+__all__ = ["ssd_fwd_quadratic", "ssd_fwd_varlen", "ssd_decode_step", "get_device_status", "check_device_status", "selftest_scan_timeout", "ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
            "ssd_state_passing", "ssd_chunk_scan", "selective_scan_fwd", "ssd_shape_t", "SSDError",
            "load_library", "status_string", "EXPORTED", "LIB_PATH"]

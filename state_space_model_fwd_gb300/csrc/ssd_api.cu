@@ -486,6 +486,27 @@ ssd_status_t ssd_get_device_status(cudaStream_t stream) {
     return (v & 1u) ? SSD_ERR_TIMEOUT : SSD_OK;
 }
 
+ssd_status_t ssd_fwd_quadratic(const ssd_shape_t *shape, const void *x, const void *dt, const float *A, const void *B,
+                               const void *C, const float *D, const float *init_state, void *y, float *final_state,
+                               cudaStream_t stream) {
+    Dims d;
+    ssd_status_t st = check_shape(shape, false, &d);
+    if (st != SSD_OK) return st;
+    if (d.b == 0) return SSD_OK;
+    if (d.L == 0) {
+        if (!ptrs_ok({A}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+        return empty_sequence(d, init_state, final_state, stream);
+    }
+    if (!ssd::quad_supported(d, shape->dtype)) return SSD_ERR_UNSUPPORTED;
+    if (!ptrs_ok({x, dt, A, B, C, y}, {D, init_state, final_state})) return SSD_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    const cudaError_t e = device_status_word(&status);
+    if (e != cudaSuccess) return from_cuda(e);
+    ssd::timing_begin(stream);
+    return from_cuda(
+        ssd::quad_fwd(d, shape->ydtype, x, dt, A, B, C, D, init_state, y, final_state, status, stream));
+}
+
 ssd_status_t ssd_decode_step(const ssd_shape_t *shape, const void *x, const void *dt, const float *A, const void *B,
                              const void *C, const float *D, float *state, void *y, cudaStream_t stream) {
     Dims d;

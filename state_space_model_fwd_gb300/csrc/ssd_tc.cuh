@@ -26,4 +26,10 @@ cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, cons
                           const float *cum, const float *states_in, const float *D, void *y, void *ws,
                           unsigned *status, uint64_t selftest_ns, cudaStream_t s);
 
+// Quadratic (dual) form for short sequences (ssd_quad.cu).
+bool quad_supported(const Dims &d, ssd_dtype_t dtype);
+cudaError_t quad_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B,
+                     const void *C, const float *D, const float *init, void *y, float *fin, unsigned *status,
+                     cudaStream_t s);
+
 }  // namespace ssd
