@@ -259,89 +259,206 @@ __global__ void __launch_bounds__(256) chunk_scan_simt_kernel(Dims d, const T *_
 }
 
 // ---------------------------------------------------------------------------
-// Sequential selective scan on FFMA.  CTA = 4 warps = 16 head channels of
-// one (b, h); inside a warp lane = (p_sub in 0..3, n_part in 0..7), each lane
-// carries NPL = N/8 state entries of one channel across all t.  Inputs are
-// staged TT steps at a time in shared memory.
+// Sequential selective scan on FFMA.  A lane owns 8 consecutive state
+// entries n of two channels p (so every B, C value it reads serves two state
+// rows); LPP = N / 8 lanes share a channel pair, a warp holds 32 / LPP pairs,
+// a CTA (2 warps) consecutive channels of one (b, h).  Inputs are staged TT
+// steps at a time in shared memory: B and C as fp32 with the 8 entries of a
+// lane in two 16-byte halves placed so that the lanes' loads are contiguous
+// (no bank conflicts), the decay exp(dt A) and the input dt x per step.  The
+// loads of the next block are in flight (in registers) while a block is
+// computed.  Per step a lane updates its 16 entries (h = a h + u B) and forms
+// its part of y_t for each channel (two independent multiply-add chains);
+// the LPP parts of y are summed once per block by a reduce-scatter across
+// the lanes of the pair (each exchange halves the values a lane holds), which
+// leaves every lane with TT / LPP finished outputs per channel.
 // ---------------------------------------------------------------------------
-template <typename T, typename TY, int NPL>
-__global__ void __launch_bounds__(128) selective_scan_kernel(Dims d, const T *__restrict__ x,
-                                                             const T *__restrict__ dt,
-                                                             const float *__restrict__ A,
-                                                             const T *__restrict__ B,
-                                                             const T *__restrict__ C,
-                                                             const float *__restrict__ D,
-                                                             const float *__restrict__ init,
-                                                             TY *__restrict__ y,
-                                                             float *__restrict__ fin) {
-    constexpr int TT = 16;
-    constexpr int NMAX = NPL * 8;
-    __shared__ __align__(16) float Bs[TT][NMAX];
-    __shared__ __align__(16) float Cs[TT][NMAX];
-    __shared__ float xs[TT][16];
-    __shared__ float us[TT][16];
-    __shared__ float as[TT];
-    __shared__ float ys[TT][16];
+constexpr int kScanWarps = 2;
+
+// One exchange per offset O = LPP/2 .. 1 on the first KC values of v (all
+// indices compile-time, so the values stay in registers).
+template <int O, int KC, int TT>
+__device__ __forceinline__ void reduce_scatter(float (&v)[TT], int lane) {
+    if constexpr (O >= 1) {
+        const bool up = (lane & O) != 0;
+#pragma unroll
+        for (int i = 0; i < KC / 2; ++i) {
+            const float send = up ? v[i] : v[i + KC / 2];
+            const float keep = up ? v[i + KC / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+        }
+        reduce_scatter<O / 2, KC / 2, TT>(v, lane);
+    }
+}
+
+template <typename T, typename TY, int LPP>
+__global__ void __launch_bounds__(32 * kScanWarps) selective_scan_kernel(
+    Dims d, const T *__restrict__ x, const T *__restrict__ dt, const float *__restrict__ A,
+    const T *__restrict__ B, const T *__restrict__ C, const float *__restrict__ D,
+    const float *__restrict__ init, TY *__restrict__ y, float *__restrict__ fin) {
+    constexpr int NPL = 8, PPW = 32 / LPP, CPC = 2 * kScanWarps * PPW, N = 8 * LPP;
+    constexpr int TT = LPP > 16 ? LPP : 16;  // steps per staged block
+    constexpr int K = TT / LPP;              // finished outputs per lane, channel and block
+    constexpr int NT = 32 * kScanWarps;
+    extern __shared__ __align__(16) float sm[];
+    float *Bs = sm;                 // [TT][2 halves][LPP][4]
+    float *Cs = Bs + TT * N;        // same
+    float *as = Cs + TT * N;        // [TT]
+    float *us = as + TT;            // [TT][CPC]  dt x
+    float *xs = us + TT * CPC;      // [TT][CPC]  x
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ps = lane >> 3, nq = lane & 7;
-    const int pl = warp * 4 + ps;  // channel within the CTA
     const int64_t h = blockIdx.y, b = blockIdx.z;
     const int64_t g = h / d.hpg;
-    const int64_t p = (int64_t)blockIdx.x * 16 + pl;
+    const int c0 = 2 * (warp * PPW + lane / LPP);  // this lane's channels c0, c0 + 1 within the CTA
+    const int np = lane % LPP;                     // state entries 8 np .. 8 np + 7
+    const int64_t p0 = (int64_t)blockIdx.x * CPC;
+    const bool live0 = p0 + c0 < d.P, live1 = p0 + c0 + 1 < d.P;
     const float ah = A[h];
     const float dh = D ? D[h] : 0.f;
-    float st[NPL];
+    float s0[NPL], s1[NPL];
 #pragma unroll
-    for (int k = 0; k < NPL; ++k)
-        st[k] = (init && p < d.P) ? init[((b * d.H + h) * d.P + p) * d.N + nq * NPL + k] : 0.f;
+    for (int k = 0; k < NPL; ++k) {
+        s0[k] = (init && live0) ? init[((b * d.H + h) * d.P + p0 + c0) * N + NPL * np + k] : 0.f;
+        s1[k] = (init && live1) ? init[((b * d.H + h) * d.P + p0 + c0 + 1) * N + NPL * np + k] : 0.f;
+    }
 
-    for (int64_t t0 = 0; t0 < d.L; t0 += TT) {
-        __syncthreads();
-        for (int i = tid; i < TT * NMAX; i += blockDim.x) {
-            const int tt = i / NMAX, n = i % NMAX;
+    // staging: B and C rows as 16-byte vectors, x and dt as scalars
+    constexpr int VW = 16 / (int)sizeof(T);                 // elements per vector
+    constexpr int NVEC = (TT * N / VW + NT - 1) / NT;
+    constexpr int NX = (TT * CPC + NT - 1) / NT;
+    uint4 bq[NVEC], cq[NVEC];
+    float xq[NX], dq = 0.f;
+    auto fetch = [&](int64_t t0) {
+#pragma unroll
+        for (int k = 0; k < NVEC; ++k) {
+            const int v = tid + k * NT;
+            const int tt = (v * VW) / N, n = (v * VW) % N;
             const int64_t t = t0 + tt;
-            const bool ok = t < d.L;
-            Bs[tt][n] = ok ? to_f32(B[((b * d.L + t) * d.G + g) * d.N + n]) : 0.f;
-            Cs[tt][n] = ok ? to_f32(C[((b * d.L + t) * d.G + g) * d.N + n]) : 0.f;
+            const bool ok = v * VW < TT * N && t < d.L;
+            bq[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(B + ((b * d.L + t) * d.G + g) * N + n)) : make_uint4(0, 0, 0, 0);
+            cq[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(C + ((b * d.L + t) * d.G + g) * N + n)) : make_uint4(0, 0, 0, 0);
         }
-        for (int i = tid; i < TT * 16; i += blockDim.x) {
-            const int tt = i / 16, pp = i % 16;
-            const int64_t t = t0 + tt, pg = (int64_t)blockIdx.x * 16 + pp;
-            const bool ok = t < d.L && pg < d.P;
-            const float dtv = t < d.L ? to_f32(dt[(b * d.L + t) * d.H + h]) : 0.f;
-            const float xv = ok ? to_f32(x[((b * d.L + t) * d.H + h) * d.P + pg]) : 0.f;
-            xs[tt][pp] = xv;
-            us[tt][pp] = dtv * xv;
-            if (pp == 0) as[tt] = expf(dtv * ah);
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int i = tid + k * NT;
+            const int tt = i / CPC, cc = i % CPC;
+            const int64_t t = t0 + tt, pc = p0 + cc;
+            xq[k] = (i < TT * CPC && t < d.L && pc < d.P) ? to_f32(x[((b * d.L + t) * d.H + h) * d.P + pc]) : 0.f;
+        }
+        if (tid < TT) dq = t0 + tid < d.L ? to_f32(dt[(b * d.L + t0 + tid) * d.H + h]) : 0.f;
+    };
+    // element n of a staged row lives at ((n % 8) / 4 * LPP + n / 8) * 4 + n % 4
+    auto stage_row_part = [&](const uint4 &q, float *row, int n) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        float f[8];
+        if constexpr (sizeof(T) == 4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f[e] = __uint_as_float(w[e]);
+            *reinterpret_cast<float4 *>(row + ((n % 8) / 4 * LPP + n / 8) * 4) = make_float4(f[0], f[1], f[2], f[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = __uint_as_float(w[e] << 16);
+                f[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+            *reinterpret_cast<float4 *>(row + (n / 8) * 4) = make_float4(f[0], f[1], f[2], f[3]);
+            *reinterpret_cast<float4 *>(row + (LPP + n / 8) * 4) = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    };
+    fetch(0);
+    for (int64_t t0 = 0; t0 < d.L; t0 += TT) {
+        __syncthreads();  // the previous block's steps are done with the stage
+#pragma unroll
+        for (int k = 0; k < NVEC; ++k) {
+            const int v = tid + k * NT;
+            if (v * VW < TT * N) {
+                const int tt = (v * VW) / N, n = (v * VW) % N;
+                stage_row_part(bq[k], Bs + tt * N, n);
+                stage_row_part(cq[k], Cs + tt * N, n);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NX; ++k) {
+            const int i = tid + k * NT;
+            if (i < TT * CPC) xs[i] = xq[k];
+        }
+        if (tid < TT) {
+            as[tid] = expf(dq * ah);
+            for (int cc = 0; cc < CPC; ++cc) us[tid * CPC + cc] = dq;
         }
         __syncthreads();
-#pragma unroll 2
+        for (int i = tid; i < TT * CPC; i += NT) us[i] *= xs[i];
+        if (t0 + TT < d.L) fetch(t0 + TT);
+        __syncthreads();
+        float part0[TT], part1[TT];
+#pragma unroll
         for (int tt = 0; tt < TT; ++tt) {
-            const float a = as[tt], u = us[tt][pl];
-            const float *Bt = &Bs[tt][nq * NPL];
-            const float *Ct = &Cs[tt][nq * NPL];
-            float acc = 0.f;
+            const float a = as[tt], u0 = us[tt * CPC + c0], u1 = us[tt * CPC + c0 + 1];
+            const float4 b0 = *reinterpret_cast<const float4 *>(Bs + tt * N + np * 4);
+            const float4 b1 = *reinterpret_cast<const float4 *>(Bs + tt * N + (LPP + np) * 4);
+            const float4 q0 = *reinterpret_cast<const float4 *>(Cs + tt * N + np * 4);
+            const float4 q1 = *reinterpret_cast<const float4 *>(Cs + tt * N + (LPP + np) * 4);
+            const float bv[NPL] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float cv[NPL] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
             for (int k = 0; k < NPL; ++k) {
-                st[k] = fmaf(a, st[k], u * Bt[k]);
-                acc = fmaf(Ct[k], st[k], acc);
+                s0[k] = fmaf(a, s0[k], u0 * bv[k]);
+                s1[k] = fmaf(a, s1[k], u1 * bv[k]);
             }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-            if (nq == 0) ys[tt][pl] = acc + dh * xs[tt][pl];
-        }
-        __syncthreads();
-        for (int i = tid; i < TT * 16; i += blockDim.x) {
-            const int tt = i / 16, pp = i % 16;
-            const int64_t t = t0 + tt, pg = (int64_t)blockIdx.x * 16 + pp;
-            if (t < d.L && pg < d.P) y[((b * d.L + t) * d.H + h) * d.P + pg] = from_f32<TY>(ys[tt][pp]);
-        }
-    }
-    if (fin && p < d.P) {
+            float e0 = cv[0] * s0[0], e1 = cv[1] * s0[1], f0 = cv[0] * s1[0], f1 = cv[1] * s1[1];
 #pragma unroll
-        for (int k = 0; k < NPL; ++k) fin[((b * d.H + h) * d.P + p) * d.N + nq * NPL + k] = st[k];
+            for (int k = 2; k < NPL; k += 2) {
+                e0 = fmaf(cv[k], s0[k], e0);
+                e1 = fmaf(cv[k + 1], s0[k + 1], e1);
+                f0 = fmaf(cv[k], s1[k], f0);
+                f1 = fmaf(cv[k + 1], s1[k + 1], f1);
+            }
+            part0[tt] = e0 + e1;
+            part1[tt] = f0 + f1;
+        }
+        reduce_scatter<LPP / 2, TT, TT>(part0, lane);
+        reduce_scatter<LPP / 2, TT, TT>(part1, lane);
+        // part*[i] is y of step t0 + np K + i (before the skip term)
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const int tt = np * K + i;
+            const int64_t t = t0 + tt;
+            if (t < d.L) {
+                const int64_t row = ((b * d.L + t) * d.H + h) * d.P + p0 + c0;
+                if (live0) y[row] = from_f32<TY>(part0[i] + dh * xs[tt * CPC + c0]);
+                if (live1) y[row + 1] = from_f32<TY>(part1[i] + dh * xs[tt * CPC + c0 + 1]);
+            }
+        }
     }
+    if (fin) {
+        if (live0) {
+            float4 *dst = reinterpret_cast<float4 *>(fin + ((b * d.H + h) * d.P + p0 + c0) * N + NPL * np);
+            dst[0] = make_float4(s0[0], s0[1], s0[2], s0[3]);
+            dst[1] = make_float4(s0[4], s0[5], s0[6], s0[7]);
+        }
+        if (live1) {
+            float4 *dst = reinterpret_cast<float4 *>(fin + ((b * d.H + h) * d.P + p0 + c0 + 1) * N + NPL * np);
+            dst[0] = make_float4(s1[0], s1[1], s1[2], s1[3]);
+            dst[1] = make_float4(s1[4], s1[5], s1[6], s1[7]);
+        }
+    }
+}
+
+template <typename T, typename TY, int LPP>
+cudaError_t launch_scan_lpp(const Dims &d, const T *x, const T *dt, const float *A, const T *B, const T *C,
+                            const float *D, const float *init, TY *y, float *final_state, cudaStream_t s) {
+    constexpr int CPC = 2 * kScanWarps * (32 / LPP), N = 8 * LPP, TT = LPP > 16 ? LPP : 16;
+    const size_t smem = sizeof(float) * (2 * TT * N + TT + 2 * TT * CPC);
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(selective_scan_kernel<T, TY, LPP>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid((unsigned)((d.P + CPC - 1) / CPC), (unsigned)d.H, (unsigned)d.b);
+    selective_scan_kernel<T, TY, LPP><<<grid, 32 * kScanWarps, smem, s>>>(d, x, dt, A, B, C, D, init, y, final_state);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -398,16 +515,14 @@ cudaError_t launch_chunk_scan_simt(const Dims &d, const T *x, const T *dt, const
 template <typename T, typename TY>
 cudaError_t launch_selective_scan(const Dims &d, const T *x, const T *dt, const float *A, const T *B, const T *C,
                                   const float *D, const float *init, TY *y, float *final_state, cudaStream_t s) {
-    dim3 grid((unsigned)((d.P + 15) / 16), (unsigned)d.H, (unsigned)d.b);
     switch (d.N) {
-        case 16: selective_scan_kernel<T, TY, 2><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
-        case 32: selective_scan_kernel<T, TY, 4><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
-        case 64: selective_scan_kernel<T, TY, 8><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
-        case 128: selective_scan_kernel<T, TY, 16><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
-        case 256: selective_scan_kernel<T, TY, 32><<<grid, 128, 0, s>>>(d, x, dt, A, B, C, D, init, y, final_state); break;
+        case 16: return launch_scan_lpp<T, TY, 2>(d, x, dt, A, B, C, D, init, y, final_state, s);
+        case 32: return launch_scan_lpp<T, TY, 4>(d, x, dt, A, B, C, D, init, y, final_state, s);
+        case 64: return launch_scan_lpp<T, TY, 8>(d, x, dt, A, B, C, D, init, y, final_state, s);
+        case 128: return launch_scan_lpp<T, TY, 16>(d, x, dt, A, B, C, D, init, y, final_state, s);
+        case 256: return launch_scan_lpp<T, TY, 32>(d, x, dt, A, B, C, D, init, y, final_state, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 template cudaError_t launch_chunk_cumsum<float>(const Dims &, const float *, const float *, float *, cudaStream_t);
