@@ -628,9 +628,49 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
         out[name] = rec
         del t, y, fin, ws
         torch.cuda.empty_cache()
+    out["stages"] = stage_sweep(ssd, dev, flush, peaks, steps)
     out["crossover"] = crossover_sweep(ssd, dev, flush, steps)
     out["decode"] = decode_sweep(ssd, dev, flush, peaks, steps)
     return out
+
+
+def stage_sweep(ssd, dev, flush, peaks, steps):
+    """The four stage entry points on the 2.7B-shaped layer, each timed per
+    launch: the bandwidth-bound ones (chunk cumsum, state passing) against the
+    HBM peak with the bytes each must move."""
+    import torch
+    cfg = si.CONFIGS["mamba2_2p7b"]
+    t = si.make_inputs(cfg).to_torch(dev)
+    b, L, H, P, N, Q = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.chunk_size
+    nc = -(-L // Q)
+    cum = torch.empty(b, H, nc, Q, device=dev)
+    st = torch.empty(b, nc, H, P, N, device=dev)
+    sin = torch.empty_like(st)
+    fin = torch.empty(b, H, P, N, device=dev)
+    y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
+    calls = {
+        "chunk_cumsum": lambda: ssd.ssd_chunk_cumsum(t["dt"], t["A"], Q, out=cum),
+        "chunk_state": lambda: ssd.ssd_chunk_state(t["x"], t["dt"], t["B"], cum, out=st),
+        "state_passing": lambda: ssd.ssd_state_passing(st, cum, t["init_state"], out=sin, final_state=fin),
+        "chunk_scan": lambda: ssd.ssd_chunk_scan(t["x"], t["dt"], t["B"], t["C"], cum, sin, t["D"], out=y),
+    }
+    nbytes = {
+        "chunk_cumsum": b * L * H * 2 + b * H * nc * Q * 4,
+        "state_passing": 2 * st.numel() * 4 + b * H * nc * 4 + 2 * fin.numel() * 4,
+    }
+    rec = {"workload": "2.7B-shaped layer (b=2, L=4096, H=80, P=64, N=128, Q=64)"}
+    for name, fn in calls.items():
+        fn()
+        kernels = kernel_times(ssd, fn, flush, steps)
+        ms = sum(kernels.values())
+        r = {"ms": ms, "launch_ms": {k: round(v, 5) for k, v in kernels.items()}}
+        if name in nbytes:
+            gbs = nbytes[name] / (ms * 1e-3) / 1e9
+            r.update({"bytes": nbytes[name], "achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]})
+        rec[name] = r
+    del st, sin
+    torch.cuda.empty_cache()
+    return rec
 
 
 def crossover_sweep(ssd, dev, flush, steps):

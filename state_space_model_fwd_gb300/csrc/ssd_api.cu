@@ -363,9 +363,13 @@ ssd_status_t ssd_chunk_cumsum(const ssd_shape_t *shape, const void *dt, const fl
     if (st != SSD_OK) return st;
     if (d.b == 0 || d.L == 0) return SSD_OK;
     if (!ptrs_ok({dt, A, dA_cumsum}, {})) return SSD_ERR_INVALID_ARG;
-    if (shape->dtype == SSD_DTYPE_F32)
-        return from_cuda(ssd::launch_chunk_cumsum<float>(d, static_cast<const float *>(dt), A, dA_cumsum, stream));
-    return from_cuda(ssd::launch_chunk_cumsum<bf16>(d, static_cast<const bf16 *>(dt), A, dA_cumsum, stream));
+    ssd::timing_begin(stream);
+    const cudaError_t e =
+        shape->dtype == SSD_DTYPE_F32
+            ? ssd::launch_chunk_cumsum<float>(d, static_cast<const float *>(dt), A, dA_cumsum, stream)
+            : ssd::launch_chunk_cumsum<bf16>(d, static_cast<const bf16 *>(dt), A, dA_cumsum, stream);
+    ssd::timing_mark(stream, "chunk_cumsum");
+    return from_cuda(e);
 }
 
 ssd_status_t ssd_chunk_state(const ssd_shape_t *shape, const void *x, const void *dt, const void *B,
@@ -403,7 +407,10 @@ ssd_status_t ssd_state_passing(const ssd_shape_t *shape, const float *states, co
         return empty_sequence(d, init_state, final_state, stream);
     }
     if (!ptrs_ok({states, dA_cumsum}, {init_state, states_in, final_state})) return SSD_ERR_INVALID_ARG;
-    return from_cuda(ssd::launch_state_passing(d, states, dA_cumsum, init_state, states_in, final_state, stream));
+    ssd::timing_begin(stream);
+    const cudaError_t e = ssd::launch_state_passing(d, states, dA_cumsum, init_state, states_in, final_state, stream);
+    ssd::timing_mark(stream, "state_passing");
+    return from_cuda(e);
 }
 
 size_t ssd_chunk_scan_workspace_size(const ssd_shape_t *shape) {

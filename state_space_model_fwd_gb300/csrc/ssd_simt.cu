@@ -17,39 +17,71 @@ constexpr int kTile = 64;         // SIMT GEMM tile edge
 constexpr int kLd = kTile + 4;    // padded smem row
 
 // ---------------------------------------------------------------------------
-// Stage 1: cum[b,h,c,q] = sum_{k<=q} dt[b,cQ+k,h] * A[h].  One warp per
-// (b, h, c); lane l owns QPL consecutive positions, a warp shuffle scan
-// joins the lane totals.
+// Stage 1: cum[b,h,c,q] = sum_{k<=q} dt[b,cQ+k,h] * A[h].  One CTA per
+// (chunk, batch, block of heads): the chunk's dt rows [Q][H] are one
+// contiguous run of memory (read with 16-byte loads when the row allows it)
+// staged in shared memory; warp w scans head columns w, w + 8, .. (lane l
+// owns QPL consecutive steps, a warp shuffle joins the lane totals) and
+// writes each head's Q cumulative values as one contiguous run (16-byte
+// stores).  Steps past L (a partial last chunk) count as dt = 0.
 // ---------------------------------------------------------------------------
+constexpr int kCumHeads = 64;  // heads per CTA
+
 template <typename T, int QPL>
 __global__ void __launch_bounds__(256) chunk_cumsum_kernel(Dims d, const T *__restrict__ dt,
                                                            const float *__restrict__ A,
                                                            float *__restrict__ cum) {
-    const int lane = threadIdx.x & 31;
-    const int64_t h = (int64_t)blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    constexpr int Q = 32 * QPL;
+    __shared__ float tile[Q][kCumHeads + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t c = blockIdx.x, b = blockIdx.z;
-    if (h >= d.H) return;  // warp-uniform
-    const float a = A[h];
-    float v[QPL];
-    float run = 0.f;
+    const int64_t h0 = (int64_t)blockIdx.y * kCumHeads;
+    const int nh = (int)(d.H - h0 < kCumHeads ? d.H - h0 : kCumHeads);
+    const int64_t t0 = c * Q;
+    const int nt = (int)(d.L - t0 < Q ? d.L - t0 : Q);  // steps of this chunk inside L
+    const T *src = dt + (b * d.L + t0) * d.H + h0;
+    constexpr int VW = 16 / (int)sizeof(T);
+    // 16-byte loads when every row of the block starts 16-byte aligned
+    const bool vec = (d.H % VW == 0) && (h0 % VW == 0) && (nh % VW == 0) &&
+                     ((reinterpret_cast<uintptr_t>(dt) & 15u) == 0);
+    if (vec) {
+        const int per_row = nh / VW;
+        for (int i = tid; i < nt * per_row; i += blockDim.x) {
+            const int tt = i / per_row, v = i % per_row;
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(src + tt * d.H) + v);
+            const T *e = reinterpret_cast<const T *>(&q);
 #pragma unroll
-    for (int i = 0; i < QPL; ++i) {
-        // steps past L (a partial last chunk) count as dt = 0: the cumulative
-        // decay stays at its last value
-        const int64_t t = c * d.Q + lane * QPL + i;
-        if (t < d.L) run += to_f32(dt[(b * d.L + t) * d.H + h]) * a;
-        v[i] = run;
+            for (int k = 0; k < VW; ++k) tile[tt][v * VW + k] = to_f32(e[k]);
+        }
+    } else {
+        for (int i = tid; i < nt * nh; i += blockDim.x) {
+            const int tt = i / nh, hh = i % nh;
+            tile[tt][hh] = to_f32(src[tt * d.H + hh]);
+        }
     }
-    float tot = run;
+    for (int i = nt * kCumHeads + tid; i < Q * kCumHeads; i += blockDim.x) tile[i / kCumHeads][i % kCumHeads] = 0.f;
+    __syncthreads();
+    for (int hh = warp; hh < nh; hh += 8) {
+        const float a = A[h0 + hh];
+        float v[QPL];
+        float run = 0.f;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, tot, off);
-        if (lane >= off) tot += o;
+        for (int i = 0; i < QPL; ++i) {
+            run += tile[lane * QPL + i][hh] * a;
+            v[i] = run;
+        }
+        float tot = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(0xffffffffu, tot, off);
+            if (lane >= off) tot += o;
+        }
+        const float excl = tot - run;
+        float *out = cum + ((b * d.H + h0 + hh) * d.nc + c) * Q + lane * QPL;
+#pragma unroll
+        for (int i = 0; i < QPL; i += 2)
+            *reinterpret_cast<float2 *>(out + i) = make_float2(v[i] + excl, v[i + 1] + excl);
     }
-    const float excl = tot - run;
-    float *out = cum + ((b * d.H + h) * d.nc + c) * d.Q + lane * QPL;
-#pragma unroll
-    for (int i = 0; i < QPL; ++i) out[i] = v[i] + excl;
 }
 
 // ---------------------------------------------------------------------------
@@ -465,7 +497,7 @@ cudaError_t launch_scan_lpp(const Dims &d, const T *x, const T *dt, const float 
 
 template <typename T>
 cudaError_t launch_chunk_cumsum(const Dims &d, const T *dt, const float *A, float *cum, cudaStream_t s) {
-    dim3 grid((unsigned)d.nc, (unsigned)((d.H + 7) / 8), (unsigned)d.b);
+    dim3 grid((unsigned)d.nc, (unsigned)((d.H + kCumHeads - 1) / kCumHeads), (unsigned)d.b);
     if (d.Q == 64)
         chunk_cumsum_kernel<T, 2><<<grid, 256, 0, s>>>(d, dt, A, cum);
     else
