@@ -115,7 +115,10 @@ struct Cfg {
     // tile of one chunk ([half][M/64 blocks][Q/2 steps][64], fp32 or bf16)
     // that the TMA stores to HBM
     static constexpr int SCAN_STAGE = X_BYTES + PACK_BYTES;
-    static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + DT_RING + 1024; }
+    // y staging: one [Q/4 steps][32 p] tile per compute warp (fp32, the
+    // larger case), the source of the warp's TMA store of its outputs
+    static constexpr int YSTAGE = 16 * (Q / 4) * 32 * 4;
+    static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + DT_RING + YSTAGE + 1024; }
     static constexpr int SCAN_ST = scan_smem(4) <= kSmemLimit ? 4 : (scan_smem(3) <= kSmemLimit ? 3 : 2);
     static constexpr int SMEM_SCAN = scan_smem(SCAN_ST);
     static constexpr bool SCAN_FITS = SMEM_SCAN <= kSmemLimit;
@@ -907,19 +910,6 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
     tmem_st_wait();
 }
 
-template <typename T>
-__device__ __forceinline__ void store_y(T *p, float v);
-// streaming (evict-first) stores: y is written once and not read back
-template <>
-__device__ __forceinline__ void store_y<float>(float *p, float v) {
-    asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-template <>
-__device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) {
-    const unsigned short u = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-    asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(u) : "memory");
-}
-
 // ===========================================================================
 // Chunk scan with the scaled state carried in TMEM (every segment).
 //   warp 0     : TMA loads of x and the chunk pack (C B^T, B, C)
@@ -933,19 +923,22 @@ __device__ __forceinline__ void store_y<bf16>(bf16 *p, float v) {
 //                entering the segment into Ss (a quarter of the columns
 //                each); then per chunk c the A operand into TMEM from the
 //                staged x (kept in registers), and chunk c - 1's output
-//                y = factor R + D x to global memory
+//                y = factor R + D x, staged per warp in shared memory and
+//                written with one TMA store per warp
 // ===========================================================================
 constexpr int kScanThreads = 768;
 constexpr int kComputeWarps = 16;  // warps 8..23
 
 template <class C, typename YT>
 __global__ void __launch_bounds__(kScanThreads, 1)
-    chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mdt, TcParams prm) {
+    chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mdt,
+                      const __grid_constant__ CUtensorMap my, TcParams prm) {
     constexpr int ST = C::SCAN_ST, NV = C::NV, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SCAN_STAGE);
     uint8_t *dt_ring = smem + ST * C::SCAN_STAGE + C::VEC_RING;
+    uint8_t *ystage = dt_ring + C::DT_RING;
     __shared__ uint64_t dt_bar[2];
     TRACE_DECL;
     // a stage's x tile and chunk pack land on separate barriers: the A
@@ -1143,8 +1136,9 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         feed.drain();
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+        // ---------------- MMA issuer: the whole warp runs the loop (its
+        // descriptors stay warp-uniform), one elected lane issues ----------------
+        {
             const uint32_t id_intra = idesc_bf16(C::M, C::Q, false, false);
             const uint32_t id_state = idesc_bf16(C::M, C::N, false, true);
             const uint32_t id_inter = idesc_bf16(C::M, C::Q, false, false);
@@ -1157,16 +1151,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 const uint64_t dc = sdesc(smem_u32(stage_c(s)), 16, 1024);
                 const uint32_t ta = tmem + C::COL_A + a * C::Q, tr = tmem + C::COL_R + a * C::Q;
                 const uint32_t tsb = tmem + C::COL_SB + a * (C::N / 2);
-                if (!wait_bounded(&pfull_bar[s], fill_parity(it, ST), &abort_sh)) break;
+                if (!warp_wait(&pfull_bar[s], fill_parity(it, ST), &abort_sh)) break;
                 TRACE(20, it);
-                if (!wait_bounded(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
+                if (!warp_wait(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
                 TRACE(21, it);
                 // Ss += A^T B first: the state chain (state warps -> these
                 // MMAs -> state warps) is the longest loop of the pipeline, so
                 // it waits for no other MMA; once the state warps have read
                 // (and rescaled) Ss and written SB
-                if (!wait_bounded(&rt_bar, (uint32_t)(it & 1), &abort_sh)) break;
+                if (!warp_wait(&rt_bar, (uint32_t)(it & 1), &abort_sh)) break;
                 tc_fence_after();
+                if (elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
                     mma_bf16_ta(tmem + C::COL_S, ta + ks * 8, desc_add(db, ks * 2048), id_state, true);
@@ -1174,11 +1169,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 for (int ks = 0; ks < C::Q / 16; ++ks)
                     mma_bf16_ta(tmem + C::COL_S, ta + C::Q / 2 + ks * 8, desc_add(db, ks * 2048), id_state, true);
                 mma_commit(&sdone_bar);
-                TRACE(3, it);
-                if (it >= NB && !wait_bounded(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
+                }
+                __syncwarp();
+                if (it >= NB && !warp_wait(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
                 TRACE(22, it);
                 tc_fence_after();
                 const bool wide = vec(it % NV)[C::V_FLAG + 1] != 0.f;  // (the A builders saw this slot filled)
+                if (elect_one()) {
                 // R = A CB^T (hi, then lo)
                 if (!wide) {
 #pragma unroll
@@ -1198,7 +1195,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 mma_commit(&rfull_bar[a]);
                 mma_commit(&sbfree_bar[a]);
                 mma_commit(&empty_bar[s]);
-                TRACE(4, it);
+                }
+                __syncwarp();
             }
         }
     } else if (warp >= 4 && warp < 8) {
@@ -1302,11 +1300,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const int blk = rh * C::PB + rp / 64;
         const long long hrow = h0 + rh;
         const float dh = (prm.D && hrow < H) ? prm.D[hrow] : 0.f;
-        // this thread's y column: steps part * NS .. + NS of each chunk
-        const long long ystep = H * C::P;
-        YT *yg = reinterpret_cast<YT *>(prm.y) +
-                 (((long long)b * prm.L + (long long)c0 * C::Q + part * NS) * H + (hrow < H ? hrow : 0)) * C::P + rp;
-        const bool live = hrow < H;
         // The state entering the segment (rho = 0: Ss = S_in), this warp's
         // quarter of the columns.  After segment 0 it is the pass across the
         // earlier segments' local states L_j (each from a zero state) and
@@ -1437,25 +1430,27 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 tmem_ld_wait();
                 // straight to global memory: a warp writes one contiguous
                 // run of 32 p per step; a partial last chunk stops at L
-                YT *yc = yg + (long long)cp * C::Q * ystep;
-                const long long tleft = prm.L - ((long long)(c0 + cp) * C::Q + part * NS);
-                if (live && tleft < NS) {
-#pragma unroll 1
-                    for (int j = 0; j < tleft; ++j) {
-                        const uint32_t w = xprev[j / 2];
-                        const float xv = __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
-                        store_y<YT>(yc + j * ystep, fmaf(dh, xv, ef[j] * acc[j]));
-                    }
-                } else if (live)
+                // into the warp's [NS steps][32 p] staging tile (row j: the 32
+                // consecutive p of step j), then one TMA store of the tile;
+                // the store clips steps past L and heads past H
+                YT *yt = reinterpret_cast<YT *>(ystage) + (warp - 8) * (NS * 32);
+                if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the tile
+                __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < NS; j += 4) {
-                        const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
-                        const uint32_t w0 = xprev[j / 2], w1 = xprev[j / 2 + 1];
-                        store_y<YT>(yc + j * ystep, fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
-                        store_y<YT>(yc + (j + 1) * ystep, fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
-                        store_y<YT>(yc + (j + 2) * ystep, fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
-                        store_y<YT>(yc + (j + 3) * ystep, fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
-                    }
+                for (int j = 0; j < NS; j += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4 *>(ef + j);
+                    const uint32_t w0 = xprev[j / 2], w1 = xprev[j / 2 + 1];
+                    yt[(j + 0) * 32 + lane] = from_f32<YT>(fmaf(dh, __uint_as_float(w0 << 16), e4.x * acc[j]));
+                    yt[(j + 1) * 32 + lane] = from_f32<YT>(fmaf(dh, __uint_as_float(w0 & 0xFFFF0000u), e4.y * acc[j + 1]));
+                    yt[(j + 2) * 32 + lane] = from_f32<YT>(fmaf(dh, __uint_as_float(w1 << 16), e4.z * acc[j + 2]));
+                    yt[(j + 3) * 32 + lane] = from_f32<YT>(fmaf(dh, __uint_as_float(w1 & 0xFFFF0000u), e4.w * acc[j + 3]));
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&my, yt, (q4 * 32) % C::P, (int)(h0 + (q4 * 32) / C::P), (c0 + cp) * C::Q + part * NS, b);
+                    bulk_commit_group();
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -1470,6 +1465,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             wide_prev = wide;
         }
     }
+    // the compute warps' y stores complete before the CTA exits
+    if (warp >= 8 && lane == 0) bulk_wait_all();
     // let this CTA's own copies and MMAs land (they normally have) before
     // TMEM is freed and the CTA exits
     if (warp == 0 && lane == 0)
@@ -1535,6 +1532,21 @@ bool make_x_map(CUtensorMap *m, const void *base, uint64_t P, uint64_t H, uint64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map of y [b][L][H][P] (fp32 or bf16) as (P, H, L, b), box (32 p, 1
+// head, Q/4 steps, 1), no swizzle: a compute warp's [Q/4][32] output tile.
+// Stores clip at L and H.
+bool make_y_map(CUtensorMap *m, void *base, bool f32, uint64_t P, uint64_t H, uint64_t L, uint64_t b, uint32_t Q) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    const uint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[4] = {P, H, L, b};
+    cuuint64_t strides[3] = {P * es, P * H * es, P * H * L * es};
+    cuuint32_t box[4] = {32, 1, Q / 4, 1};
+    cuuint32_t el[4] = {1, 1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides,
+               box, el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 // 3-D map of dt [b][L][H] (bf16), box (8 heads, 4 Q steps, 1); needs the row
 // stride H * 2 bytes to be a multiple of 16 (H % 8 == 0).
 bool make_dt_map(CUtensorMap *m, const void *base, uint64_t H, uint64_t L, uint64_t b, uint32_t Q) {
@@ -1660,20 +1672,21 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pac
 template <class C>
 cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, dim3 grid, const char *name,
                         bool pdl, cudaStream_t s) {
-    CUtensorMap mx, mdt = {};
+    CUtensorMap mx, mdt = {}, my;
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
     const bool f32 = ydtype == SSD_DTYPE_F32;
     if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q)) return cudaErrorInvalidValue;
+    if (!make_y_map(&my, prm.y, f32, d.P, d.H, d.L, d.b, C::Q)) return cudaErrorInvalidValue;
     static int attr_f = 0, attr_b = 0;
     cudaError_t e;
     if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
     } else {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
     }
     timing_mark(s, name);
     return e;
