@@ -784,20 +784,26 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         if (lane == 0 && h0 + hv < H && prm.seg_tot) prm.seg_tot[((long long)b * H + h0 + hv) * prm.nseg + seg] = after;
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(C::M, C::N, false, true);
-            for (int it = 0; it < nch; ++it) {
-                const int s = it % ST, a = it % NA;
-                if (!wait_bounded(&afull_bar[a], fill_parity(it, NA), &abort_sh)) break;
-                if (!wait_bounded(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
-                tc_fence_after();
-                // one descriptor per operand tile, advanced by constants (the
-                // single issuing thread must not spend cycles per MMA)
-                const uint32_t ta = tmem + COL_A + a * C::Q;
-                const uint64_t db = sdesc(smem_u32(stage_b(s)), C::Q * 128, 1024);
+        // (the whole warp runs the loop, so its descriptors stay
+        // warp-uniform; one elected lane issues)
+        const uint32_t idesc = idesc_bf16(C::M, C::N, false, true);
+        for (int it = 0; it < nch; ++it) {
+            const int s = it % ST, a = it % NA;
+            if (!warp_wait(&afull_bar[a], fill_parity(it, NA), &abort_sh)) break;
+            if (!warp_wait(&full_bar[s], fill_parity(it, ST), &abort_sh)) break;
+            tc_fence_after();
+            const uint32_t ta = tmem + COL_A + a * C::Q;
+            const uint64_t db = sdesc(smem_u32(stage_b(s)), C::Q * 128, 1024);
+            if (elect_one()) {
+                if (it == 0) {
 #pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem, ta + ks * 8, desc_add(db, ks * 2048), idesc, (it | ks) != 0);
+                    for (int ks = 0; ks < C::Q / 16; ++ks)
+                        mma_bf16_ta(tmem, ta + ks * 8, desc_add(db, ks * 2048), idesc, ks != 0);
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < C::Q / 16; ++ks)
+                        mma_bf16_ta(tmem, ta + ks * 8, desc_add(db, ks * 2048), idesc, true);
+                }
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
                     mma_bf16_ta(tmem, ta + C::Q / 2 + ks * 8, desc_add(db, ks * 2048), idesc, true);
@@ -805,8 +811,10 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 mma_commit(&afree_bar[a]);
                 TRACE(16, it);
             }
-            mma_commit(&done_bar);  // completes once every MMA above has
+            __syncwarp();
         }
+        if (elect_one()) mma_commit(&done_bar);  // completes once every MMA above has
+        __syncwarp();
     } else if (warp >= 4) {
         // ---------------- A operand builders: thread = row (head, p), a quarter of the steps ----------------
         constexpr int NAB = kSegThreads - 128;
@@ -1213,9 +1221,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         float rho_end = 0.f;
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV, sb = it % NB;
-            if (!group_wait(&vfull_bar[v], fill_parity(it, NV), &abort_sh, &slot[0], 1, gtid, 128)) break;
-            if (it > 0 && !group_wait(&sdone_bar, (uint32_t)((it - 1) & 1), &abort_sh, &slot[1], 1, gtid, 128)) break;
-            if (it >= NB && !group_wait(&sbfree_bar[sb], free_parity(it, NB), &abort_sh, &slot[2], 1, gtid, 128)) break;
+            // one thread waits for every phase this chunk needs (the vector
+            // set, the previous state MMAs, the SB buffer), then one named
+            // barrier hands the outcome to the four warps, which always leave
+            // the loop together
+            if (gtid == 0)
+                slot[0] = (wait_bounded(&vfull_bar[v], fill_parity(it, NV), &abort_sh) &&
+                           (it == 0 || wait_bounded(&sdone_bar, (uint32_t)((it - 1) & 1), &abort_sh)) &&
+                           (it < NB || wait_bounded(&sbfree_bar[sb], free_parity(it, NB), &abort_sh)))
+                              ? 1
+                              : 0;
+            named_bar_sync(1, 128);
+            if (!slot[0]) break;
             if (gtid == 0) TRACE(7, it);
             tc_fence_after();
             const float *vv = vec(v);
