@@ -61,26 +61,40 @@ __global__ void __launch_bounds__(256) chunk_cumsum_kernel(Dims d, const T *__re
     }
     for (int i = nt * kCumHeads + tid; i < Q * kCumHeads; i += blockDim.x) tile[i / kCumHeads][i % kCumHeads] = 0.f;
     __syncthreads();
-    for (int hh = warp; hh < nh; hh += 8) {
-        const float a = A[h0 + hh];
-        float v[QPL];
-        float run = 0.f;
+    // each warp scans kCumHeads / 8 heads with their shuffle chains
+    // interleaved (independent dependency chains, one latency for all)
+    constexpr int KH = kCumHeads / 8;
+    float v[KH][QPL], run[KH], tot[KH];
+#pragma unroll
+    for (int k = 0; k < KH; ++k) {
+        const int hh = warp + 8 * k;
+        const bool live = hh < nh;  // (warp-uniform)
+        const float a = live ? __ldg(A + h0 + hh) : 0.f;
+        run[k] = 0.f;
 #pragma unroll
         for (int i = 0; i < QPL; ++i) {
-            run += tile[lane * QPL + i][hh] * a;
-            v[i] = run;
+            run[k] += tile[lane * QPL + i][live ? hh : 0] * a;
+            v[k][i] = run[k];
         }
-        float tot = run;
+        tot[k] = run[k];
+    }
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(0xffffffffu, tot, off);
-            if (lane >= off) tot += o;
+    for (int off = 1; off < 32; off <<= 1) {
+#pragma unroll
+        for (int k = 0; k < KH; ++k) {
+            const float o = __shfl_up_sync(0xffffffffu, tot[k], off);
+            if (lane >= off) tot[k] += o;
         }
-        const float excl = tot - run;
+    }
+#pragma unroll
+    for (int k = 0; k < KH; ++k) {
+        const int hh = warp + 8 * k;
+        if (hh >= nh) break;  // (warp-uniform; heads ascend with k)
+        const float excl = tot[k] - run[k];
         float *out = cum + ((b * d.H + h0 + hh) * d.nc + c) * Q + lane * QPL;
 #pragma unroll
         for (int i = 0; i < QPL; i += 2)
-            *reinterpret_cast<float2 *>(out + i) = make_float2(v[i] + excl, v[i + 1] + excl);
+            *reinterpret_cast<float2 *>(out + i) = make_float2(v[k][i] + excl, v[k][i + 1] + excl);
     }
 }
 
