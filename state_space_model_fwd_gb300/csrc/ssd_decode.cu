@@ -32,7 +32,7 @@ __device__ __forceinline__ float4 load4<bf16>(const bf16 *p) {
                        __uint_as_float(u.y & 0xFFFF0000u));
 }
 
-constexpr int kRows = 4;  // state rows per warp (P is a multiple of 16)
+constexpr int kRows = 8;  // state rows per warp (P is a multiple of 16)
 
 template <typename T, typename TY>
 __global__ void __launch_bounds__(256) decode_step_kernel(Dims d, const T *__restrict__ x, const T *__restrict__ dt,
