@@ -127,6 +127,12 @@ struct Cfg {
     static constexpr int NB = tmem_cols(2) <= 512 ? 2 : 1;
     static constexpr int COL_S = 0, COL_SB = N, COL_A = N + NB * N / 2, COL_R = COL_A + NB * Q;
     static constexpr bool TMEM_FITS = tmem_cols(NB) <= 512;
+    // state warp groups of the scan: with N = 256 the state pass (a TMEM
+    // round trip per 32 columns) is long enough that a second group of four
+    // warps, each group half of the columns, shortens the per-chunk loop;
+    // at N <= 128 the smaller register budget of the larger CTA costs more
+    static constexpr int SG = N >= 256 ? 2 : 1;
+    static constexpr int SCAN_THREADS = 768 + 128 * (SG - 1);
 
     // segment-state kernel: TMA stages of (x, B) and the vector ring
     static constexpr int SEG_STAGE = X_BYTES + BC_BYTES;
@@ -509,7 +515,11 @@ __device__ __forceinline__ void load_x_part(const uint8_t *xs, int blk, uint32_t
     }
 }
 
-// The A operand part of build_a from x values already in registers.
+// The A operand part of build_a from x values already in registers, for the
+// chunk scan, whose A buffer interleaves the parts per K step: K step k
+// (steps 16 k .. 16 k + 15) holds its hi words in columns 16 k .. 16 k + 7
+// and its lo words in the next 8, so each warp writes its part with one
+// 16-column store (fewer tensor-memory operations on the compute chain).
 template <class C, int NS>
 __device__ __forceinline__ void build_a_regs(const uint32_t (&xk)[NS / 2], const float *f, int part,
                                              uint32_t tmem_a) {
@@ -527,13 +537,14 @@ __device__ __forceinline__ void build_a_regs(const uint32_t (&xk)[NS / 2], const
         lo[j] = pack_bf16x2(a0 - __uint_as_float(h0 << 16), a1 - __uint_as_float(h0 & 0xFFFF0000u));
         lo[j + 1] = pack_bf16x2(a2 - __uint_as_float(h1 << 16), a3 - __uint_as_float(h1 & 0xFFFF0000u));
     }
-    if constexpr (NS == 32) {
-        tmem_st16u(tmem_a + part * 16, hi);
-        tmem_st16u(tmem_a + C::Q / 2 + part * 16, lo);
-    } else {
-        tmem_st8u(tmem_a + part * 8, hi);
-        tmem_st8u(tmem_a + C::Q / 2 + part * 8, lo);
+    static_assert(NS == 16, "one K step per part");
+    uint32_t hl[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        hl[j] = hi[j];
+        hl[8 + j] = lo[j];
     }
+    tmem_st16u(tmem_a + part * 16, hl);  // K step `part`: hi in 8 columns, lo in the next 8
 }
 
 // Every lane of the warp waits for the phase (bounded); uniform result.
@@ -926,7 +937,8 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
 //   warp 2     : dt, cumulative decay, rho, the A factors and output
 //                factors (a ring of vector sets)
 //   warps 4-7  : state: Ss rescale when the reference moves, and its bf16
-//                copy SB (the A operand of the inter-chunk term)
+//                copy SB (the A operand of the inter-chunk term); with
+//                C::SG = 2 warps 24-27 take the second half of the columns
 //   warps 8-23 : compute, a quarter of the steps each: first the state
 //                entering the segment into Ss (a quarter of the columns
 //                each); then per chunk c the A operand into TMEM from the
@@ -934,11 +946,10 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
 //                y = factor R + D x, staged per warp in shared memory and
 //                written with one TMA store per warp
 // ===========================================================================
-constexpr int kScanThreads = 768;
 constexpr int kComputeWarps = 16;  // warps 8..23
 
 template <class C, typename YT>
-__global__ void __launch_bounds__(kScanThreads, 1)
+__global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mdt,
                       const __grid_constant__ CUtensorMap my, TcParams prm) {
     constexpr int ST = C::SCAN_ST, NV = C::NV, NB = C::NB;
@@ -1172,10 +1183,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 if (elect_one()) {
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 8, desc_add(db, ks * 2048), id_state, true);
+                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 16, desc_add(db, ks * 2048), id_state, true);
 #pragma unroll
                 for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + C::Q / 2 + ks * 8, desc_add(db, ks * 2048), id_state, true);
+                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 16 + 8, desc_add(db, ks * 2048), id_state, true);
                 mma_commit(&sdone_bar);
                 }
                 __syncwarp();
@@ -1188,10 +1199,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 if (!wide) {
 #pragma unroll
                     for (int ks = 0; ks < C::Q / 16; ++ks)
-                        mma_bf16_ta(tr, ta + ks * 8, desc_add(dcb, ks * 32), id_intra, ks > 0);
+                        mma_bf16_ta(tr, ta + ks * 16, desc_add(dcb, ks * 32), id_intra, ks > 0);
 #pragma unroll
                     for (int ks = 0; ks < C::Q / 16; ++ks)
-                        mma_bf16_ta(tr, ta + C::Q / 2 + ks * 8, desc_add(dcb, ks * 32), id_intra, true);
+                        mma_bf16_ta(tr, ta + ks * 16 + 8, desc_add(dcb, ks * 32), id_intra, true);
                 }
                 mma_commit(&afree_bar[a]);
                 TRACE(2, it);
@@ -1207,13 +1218,17 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 __syncwarp();
             }
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------- state: rescale and bf16 copy ----------------
-        const int gtid = tid - 128;
+    } else if ((warp >= 4 && warp < 8) || warp >= 24) {
+        // ---------------- state: rescale and bf16 copy (C::SG groups of four
+        // warps, each a 1 / SG share of the columns) ----------------
+        constexpr int NT = 128 * C::SG;  // threads of the state groups
+        constexpr int NCOL = C::N / C::SG;
+        const int half = warp >= 24 ? 1 : 0;
+        const int gtid = half ? tid - 768 + 128 : tid - 128;
         const int row = q4 * 32 + lane, rh = row / C::P, rp = row % C::P;
         const long long hrow = h0 + rh;
         // the compute warps write the state entering the segment into Ss
-        if (!group_wait(&sinit_bar, 0, &abort_sh, &slot[3], 1, gtid, 128)) {
+        if (!group_wait(&sinit_bar, 0, &abort_sh, &slot[3], 1, gtid, NT)) {
             // (abort: fall through; every wait below gives up at once)
         }
         tc_fence_after();
@@ -1223,7 +1238,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             const int v = it % NV, sb = it % NB;
             // one thread waits for every phase this chunk needs (the vector
             // set, the previous state MMAs, the SB buffer), then one named
-            // barrier hands the outcome to the four warps, which always leave
+            // barrier hands the outcome to the state warps, which always leave
             // the loop together
             if (gtid == 0)
                 slot[0] = (wait_bounded(&vfull_bar[v], fill_parity(it, NV), &abort_sh) &&
@@ -1231,7 +1246,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                            (it < NB || wait_bounded(&sbfree_bar[sb], free_parity(it, NB), &abort_sh)))
                               ? 1
                               : 0;
-            named_bar_sync(1, 128);
+            named_bar_sync(1, NT);
             if (!slot[0]) break;
             if (gtid == 0) TRACE(7, it);
             tc_fence_after();
@@ -1240,47 +1255,33 @@ __global__ void __launch_bounds__(kScanThreads, 1)
             const bool rescale = vv[C::V_FLAG] != 0.f;
             rho_end = vv[C::V_RHON + rh];
 #pragma unroll 1
-            for (int n0 = 0; n0 < C::N; n0 += 32) {
-                float v0[16], v1[16];
-                tmem_ld16(tmem + lane_off + C::COL_S + n0, v0);
-                tmem_ld16(tmem + lane_off + C::COL_S + n0 + 16, v1);
+            for (int n0 = half * NCOL; n0 < (half + 1) * NCOL; n0 += 32) {
+                float v[32];
+                tmem_ld32(tmem + lane_off + C::COL_S + n0, v);
                 tmem_ld_wait();
                 uint32_t w[16];
                 // (sbf and f are uniform per warp: one head per warp)
                 if (sbf == 1.f) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        w[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
-                        w[8 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
-                    }
+                    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                 } else if (sbf > 0.f) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        w[j] = pack_bf16x2(v0[2 * j] * sbf, v0[2 * j + 1] * sbf);
-                        w[8 + j] = pack_bf16x2(v1[2 * j] * sbf, v1[2 * j + 1] * sbf);
-                    }
+                    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j] * sbf, v[2 * j + 1] * sbf);
                 }
                 if (rescale) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        v0[j] = (v0[j] * f) * f;
-                        v1[j] = (v1[j] * f) * f;
-                    }
-                    tmem_st16(tmem + lane_off + C::COL_S + n0, v0);
-                    tmem_st16(tmem + lane_off + C::COL_S + n0 + 16, v1);
+                    for (int j = 0; j < 32; ++j) v[j] = (v[j] * f) * f;
+                    tmem_st32(tmem + lane_off + C::COL_S + n0, v);
                 }
                 if (sbf < 0.f) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        w[j] = pack_bf16x2(v0[2 * j], v0[2 * j + 1]);
-                        w[8 + j] = pack_bf16x2(v1[2 * j], v1[2 * j + 1]);
-                    }
+                    for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                 }
                 tmem_st16u(tmem + lane_off + C::COL_SB + sb * (C::N / 2) + n0 / 2, w);
             }
             tmem_st_wait();
             tc_fence_before();
-            named_bar_sync(1, 128);
+            named_bar_sync(1, NT);
             if (gtid == 0) {
                 TRACE(8, it);
                 mbar_arrive(&rt_bar);
@@ -1289,12 +1290,12 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
         // final state after the segment's last chunk: S = exp(-rho) Ss
         if (seg == prm.nseg - 1 && prm.fin) {  // (a uniform test: group_wait handles an abort)
-            if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[9], 1, gtid, 128)) {
+            if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[9], 1, gtid, NT)) {
                 tc_fence_after();
                 const float sc = __expf(-rho_end);
                 float *dst = prm.fin + (((long long)b * H + hrow) * C::P + rp) * C::N;
 #pragma unroll 1
-                for (int n0 = 0; n0 < C::N; n0 += 16) {
+                for (int n0 = half * NCOL; n0 < (half + 1) * NCOL; n0 += 16) {
                     float v[16];
                     tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
                     tmem_ld_wait();
@@ -1306,7 +1307,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
                 }
             }
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 8 && warp < 24) {
         // ---------------- compute warps: thread = row (head, p), a quarter of the Q steps ----------------
         // Chunk c: the A operand from the staged x (kept in registers), then
         // the output of chunk c - 1:  y = factor R + D x.
@@ -1483,7 +1484,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
     }
     // the compute warps' y stores complete before the CTA exits
-    if (warp >= 8 && lane == 0) bulk_wait_all();
+    if (warp >= 8 && warp < 24 && lane == 0) bulk_wait_all();
     // let this CTA's own copies and MMAs land (they normally have) before
     // TMEM is freed and the CTA exits
     if (warp == 0 && lane == 0)
@@ -1699,11 +1700,11 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
+        e = launch_k(chunk_scan_kernel<C, float>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
     } else {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16>, grid, kScanThreads, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
     }
     timing_mark(s, name);
     return e;
