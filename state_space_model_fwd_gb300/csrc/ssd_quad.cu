@@ -19,6 +19,10 @@
 // plus, once, R_h = C_i init_h^T (init split into bf16 hi + lo), and
 // y = Y + exp(cum_t) R + D x.  The CTA of the last tile also forms the final
 // state: Fin += (w o x_j)^T B_j, the A operand (bf16 hi + lo) in TMEM.
+// Each head's masked scores are computed once, both bf16 parts written (the
+// lo part into the init tiles' region, free once R is complete), and the
+// MMAs of the two parts issued together.  The y and final-state tiles leave
+// through shared memory so that the global stores are coalesced.
 // Everything is single-buffered and phase by phase; every wait is bounded.
 #include <cudaTypedefs.h>
 
@@ -31,7 +35,7 @@ namespace {
 using namespace tc;
 
 constexpr int kQT = 128;             // steps per tile
-constexpr int kQuadThreads = 256;    // 8 warps: two per TMEM lane quarter
+constexpr int kQuadThreads = 512;    // 16 warps: four per TMEM lane quarter
 constexpr int kQuadMaxL = 1024;
 constexpr uint64_t kQWaitNs = 100000000ull;
 
@@ -109,7 +113,7 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
     __shared__ uint64_t tma_bar, mma_bar;
     __shared__ uint32_t tmem_sh;
     __shared__ volatile int ok_sh;
-    __shared__ float part_sh[Q::HB][8];
+    __shared__ float part_sh[Q::HB][kQuadThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int i = blockIdx.x, hb = blockIdx.y, b = blockIdx.z;
@@ -119,7 +123,7 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
     const int t0 = i * kQT;
     const bool do_fin = prm.fin && i == prm.nt - 1;
     const int steps = (do_fin ? prm.nt : i + 1) * kQT;  // steps whose decay this CTA needs
-    const int q4 = warp & 3, half = warp >> 2;
+    const int q4 = warp & 3, cq = warp >> 2;            // lane quarter; quarter of the columns
     const int r = q4 * 32 + lane;                        // TMEM lane of this thread
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
 
@@ -145,14 +149,14 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
                 tma_load_5d(xs + (hh * (Q::P / 64) + pb) * Q::XB, &mx, &mma_bar, 0, pb, h0 + hh, 0, b);
     }
     // ---- dt and the running sum of dt*A over the steps this CTA needs
-    // (steps past L: dt = 0), per head: thread k takes steps 4k .. 4k + 3
+    // (steps past L: dt = 0), per head: thread k takes steps 2k, 2k + 1
     for (int hh = 0; hh < Q::HB; ++hh) {
         const long long h = h0 + hh;
         const float a = prm.A[h];
-        float v[4], run = 0.f;
+        float v[2], run = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const long long s = 4 * tid + k;
+        for (int k = 0; k < 2; ++k) {
+            const long long s = 2 * tid + k;
             const float d = (s < L && s < steps) ? __bfloat162float(prm.dt[((long long)b * L + s) * H + h]) : 0.f;
             dts[hh * kQuadMaxL + s] = d;
             run += d * a;
@@ -170,25 +174,20 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
         for (int w = 0; w < warp; ++w) pre += part_sh[hh][w];
         const float excl = pre + tot - run;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) cum[hh * kQuadMaxL + 4 * tid + k] = v[k] + excl;
+        for (int k = 0; k < 2; ++k) cum[hh * kQuadMaxL + 2 * tid + k] = v[k] + excl;
         __syncthreads();
     }
-    // ---- the initial states as bf16 hi + lo, K-major: row (head, p), n
+    // ---- the initial states as bf16 hi + lo, K-major: row (head, p), n; the
+    // block's rows are consecutive in global memory, so consecutive threads
+    // take consecutive 8-float pieces (coalesced loads)
     if (prm.init) {
-        const int rr = tid & 127, nh = tid >> 7;  // two threads per row, half of n each
-        const int rh = rr / Q::P, rp = rr % Q::P;
-        const float *src = prm.init + (((long long)b * H + h0 + rh) * Q::P + rp) * Q::N;
+        const float *src = prm.init + ((long long)b * H + h0) * Q::P * Q::N;
 #pragma unroll 1
-        for (int n8 = nh * (Q::N / 2); n8 < (nh + 1) * (Q::N / 2); n8 += 8) {
-            float v[8];
-#pragma unroll
-            for (int k = 0; k < 8; k += 4) {
-                const float4 a4 = __ldg(reinterpret_cast<const float4 *>(src + n8 + k));
-                v[k] = a4.x;
-                v[k + 1] = a4.y;
-                v[k + 2] = a4.z;
-                v[k + 3] = a4.w;
-            }
+        for (int idx = tid; idx < 128 * (Q::N / 8); idx += kQuadThreads) {
+            const int rr = idx / (Q::N / 8), n8 = (idx % (Q::N / 8)) * 8;
+            const float4 a0 = __ldg(reinterpret_cast<const float4 *>(src + (long long)rr * Q::N + n8));
+            const float4 a1 = __ldg(reinterpret_cast<const float4 *>(src + (long long)rr * Q::N + n8 + 4));
+            const float v[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
             uint4 hi, lo;
             uint32_t *hp = &hi.x, *lp = &lo.x;
 #pragma unroll
@@ -209,7 +208,11 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
     const uint32_t tmem = tmem_sh;
     uint32_t tph = 0, mph = 0;  // barrier phases (thread 0)
     const uint64_t dC = sdesc(smem_u32(cs), 16, 1024), dB = sdesc(smem_u32(bs), 16, 1024);
-    const uint64_t dBmn = sdesc(smem_u32(bs), kQT * 128, 1024), dM = sdesc(smem_u32(ms), 16, 1024);
+    // the masked scores' hi part goes to ms, the lo part to ms2: the region of
+    // the init tiles, whose MMAs (R) completed with the first score MMAs
+    uint8_t *ms2 = ihi;
+    const uint64_t dBmn = sdesc(smem_u32(bs), kQT * 128, 1024), dM = sdesc(smem_u32(ms), 16, 1024),
+                   dM2 = sdesc(smem_u32(ms2), 16, 1024);
     bool ok = true;
 
     QMARK(2);
@@ -269,47 +272,50 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
         tc_fence_after();
         for (int hh = 0; ok && hh < Q::HB; ++hh) {
             // M_h[t, s] = S[t, s] exp(cum_t - cum_s) dt_s for s <= t < L; this
-            // thread: row t = t0 + r, columns s = 64 half .. + 63 (one 64-wide
-            // block of the K-major score tile).  M is rounded to bf16 hi + lo
-            // (together about 2^-17 relative): part 0 writes hi, part 1 the
-            // low part, each followed by its MMAs into Y.
+            // thread: row t = t0 + r, columns s = 32 cq .. + 31 of the K-major
+            // score tile (64-wide block cq / 2).  M is rounded to bf16 hi + lo
+            // (together about 2^-17 relative), computed once: hi into ms, lo
+            // into ms2, then the MMAs of both parts into Y.
             const float *ch = cum + hh * kQuadMaxL, *dh = dts + hh * kQuadMaxL;
             const long long t = t0 + r;
             const float ct = ch[t0 + r];
-            uint8_t *mrow = ms + half * (kQT * 128);
-            for (int part = 0; part < 2; ++part) {
+            const int blk = cq >> 1, cb = (cq & 1) * 32;
+            uint8_t *mhi = ms + blk * (kQT * 128), *mlo = ms2 + blk * (kQT * 128);
 #pragma unroll 1
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + lane_off + Q::T_S + half * 64 + c0, v);
-                    tmem_ld_wait();
-                    uint32_t w[8];
+            for (int c0 = cb; c0 < cb + 32; c0 += 16) {
+                float v[16];
+                tmem_ld16(tmem + lane_off + Q::T_S + blk * 64 + c0, v);
+                tmem_ld_wait();
+                uint32_t wh[8], wl[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        float m2[2];
+                for (int k = 0; k < 8; ++k) {
+                    float m2[2];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int sl = half * 64 + c0 + 2 * k + e;
-                            const long long s = (long long)j * kQT + sl;
-                            m2[e] = (s <= t && t < L) ? v[2 * k + e] * __expf(ct - ch[s]) * dh[s] : 0.f;
-                        }
-                        const uint32_t hw = pack_bf16x2(m2[0], m2[1]);
-                        w[k] = part == 0 ? hw
-                                         : pack_bf16x2(m2[0] - __uint_as_float(hw << 16),
-                                                       m2[1] - __uint_as_float(hw & 0xFFFF0000u));
+                    for (int e = 0; e < 2; ++e) {
+                        const int sl = blk * 64 + c0 + 2 * k + e;
+                        const long long s = (long long)j * kQT + sl;
+                        m2[e] = (s <= t && t < L) ? v[2 * k + e] * __expf(ct - ch[s]) * dh[s] : 0.f;
                     }
-                    *reinterpret_cast<uint4 *>(mrow + swz128((uint32_t)r, (uint32_t)c0)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4 *>(mrow + swz128((uint32_t)r, (uint32_t)(c0 + 8))) =
-                        make_uint4(w[4], w[5], w[6], w[7]);
+                    const uint32_t hw = pack_bf16x2(m2[0], m2[1]);
+                    wh[k] = hw;
+                    wl[k] = pack_bf16x2(m2[0] - __uint_as_float(hw << 16), m2[1] - __uint_as_float(hw & 0xFFFF0000u));
                 }
-                fence_async_smem();
-                tc_fence_before();
-                __syncthreads();
-                QMARK(6 + 8 * j + 2 * hh + part);
-                if (tid == 0) {
-                    tc_fence_after();
-                    const uint32_t id = idesc_bf16(128, 64, false, true);
+                *reinterpret_cast<uint4 *>(mhi + swz128((uint32_t)r, (uint32_t)c0)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                *reinterpret_cast<uint4 *>(mhi + swz128((uint32_t)r, (uint32_t)(c0 + 8))) =
+                    make_uint4(wh[4], wh[5], wh[6], wh[7]);
+                *reinterpret_cast<uint4 *>(mlo + swz128((uint32_t)r, (uint32_t)c0)) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                *reinterpret_cast<uint4 *>(mlo + swz128((uint32_t)r, (uint32_t)(c0 + 8))) =
+                    make_uint4(wl[4], wl[5], wl[6], wl[7]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            QMARK(6 + 8 * j + 2 * hh);
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, false, true);
+                for (int part = 0; part < 2; ++part) {
+                    const uint64_t dm = part == 0 ? dM : dM2;
                     for (int pb = 0; pb < Q::P / 64; ++pb) {
                         const uint64_t dx = sdesc(smem_u32(xs + (hh * (Q::P / 64) + pb) * Q::XB), kQT * 128, 1024);
                         const uint32_t ty = tmem + Q::T_Y + hh * Q::P + pb * 64;
@@ -317,62 +323,80 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
                         for (int ks = 0; ks < kQT / 16; ++ks) {
                             const uint32_t adv = (ks / 4) * (kQT * 128) + (ks % 4) * 32;
                             if (j == 0 && part == 0)
-                                mma_bf16(ty, desc_add(dM, adv), desc_add(dx, ks * 2048), id, ks > 0);
+                                mma_bf16(ty, desc_add(dm, adv), desc_add(dx, ks * 2048), id, ks > 0);
                             else
-                                mma_bf16(ty, desc_add(dM, adv), desc_add(dx, ks * 2048), id, true);
+                                mma_bf16(ty, desc_add(dm, adv), desc_add(dx, ks * 2048), id, true);
                         }
                     }
-                    mma_commit(&mma_bar);
                 }
-                // (the scores tile is rewritten for the next part or head, and
-                // S, B and x for the next tile, only once these MMAs have read
-                // them)
-                if (!(ok = cta_wait(&mma_bar, mph, &ok_sh))) break;
-                tc_fence_after();
+                mma_commit(&mma_bar);
             }
+            // (both score tiles are rewritten for the next head, and S, B and
+            // x for the next tile, only once these MMAs have read them)
+            if (!(ok = cta_wait(&mma_bar, mph, &ok_sh))) break;
+            tc_fence_after();
         }
     }
 
     QMARK(40);
-    // ---- y = Y + exp(cum_t) R + D x for this thread's row and 64 columns
+    // ---- y = Y + exp(cum_t) R + D x for this thread's row and 32 of the
+    // HB * P = 128 columns; the tile leaves through shared memory (rows padded
+    // by 16 bytes: conflict-free 16-byte writes from the row-per-lane layout)
+    // so that the global stores are coalesced: a row of the tile is HB P
+    // consecutive outputs of y (the block's heads are adjacent)
     if (ok) {
         const long long t = t0 + r;
-        const int col0 = half * 64;                    // of the HB * P = 128 columns
+        const int col0 = cq * 32;                      // of the HB * P = 128 columns
         const int rh = col0 / Q::P, pc = col0 % Q::P;  // head, first p
         const long long h = h0 + rh;
         const float et = __expf(cum[rh * kQuadMaxL + t0 + r]);
         const float dd = prm.D ? prm.D[h] : 0.f;
         const uint8_t *xrow = xs + (rh * (Q::P / 64) + pc / 64) * Q::XB;  // x of the diagonal tile (j = i)
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 16) {
+        float o[32];
+#pragma unroll
+        for (int c0 = 0; c0 < 32; c0 += 16) {
             float yv[16], rv[16];
             tmem_ld16(tmem + lane_off + Q::T_Y + col0 + c0, yv);
             if (prm.init) tmem_ld16(tmem + lane_off + Q::T_R + col0 + c0, rv);
             tmem_ld_wait();
-            if (t < L) {
-                const uint4 x0 = *reinterpret_cast<const uint4 *>(xrow + swz128((uint32_t)r, (uint32_t)c0));
-                const uint4 x1 = *reinterpret_cast<const uint4 *>(xrow + swz128((uint32_t)r, (uint32_t)(c0 + 8)));
-                const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                float o[16];
+            const uint32_t xc = (uint32_t)(pc % 64 + c0);  // column in the 64-wide x block
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(xrow + swz128((uint32_t)r, xc));
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(xrow + swz128((uint32_t)r, xc + 8));
+            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float xv = __uint_as_float((k & 1) ? (xw[k / 2] & 0xFFFF0000u) : (xw[k / 2] << 16));
-                    o[k] = yv[k] + (prm.init ? et * rv[k] : 0.f) + dd * xv;
-                }
-                YT *dst = reinterpret_cast<YT *>(prm.y) + (((long long)b * L + t) * H + h) * Q::P + pc + c0;
+            for (int k = 0; k < 16; ++k) {
+                const float xv = __uint_as_float((k & 1) ? (xw[k / 2] & 0xFFFF0000u) : (xw[k / 2] << 16));
+                o[c0 + k] = yv[k] + (prm.init ? et * rv[k] : 0.f) + dd * xv;
+            }
+        }
+        constexpr int ROWB = 128 * (int)sizeof(YT) + 16;  // staging row: the tile row + 16 bytes
+        constexpr int CPR = 128 * (int)sizeof(YT) / 16;   // 16-byte pieces per row
+        uint8_t *stg = ms;                                 // (ms and the init tiles: free once Y is complete)
+        YT *ybase = reinterpret_cast<YT *>(prm.y) + ((long long)b * L * H + h0) * Q::P;
+        for (int h2 = 0; h2 < 2; ++h2) {
+            if ((r >> 6) == h2) {
+                uint8_t *dst = stg + (r & 63) * ROWB + col0 * (int)sizeof(YT);
                 if constexpr (sizeof(YT) == 4) {
 #pragma unroll
-                    for (int k = 0; k < 16; k += 4)
-                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + k) =
-                            make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+                    for (int k = 0; k < 32; k += 4)
+                        *reinterpret_cast<float4 *>(dst + 4 * k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
                 } else {
-                    uint32_t pk[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(o[2 * k], o[2 * k + 1]);
-                    *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    for (int k = 0; k < 32; k += 8)
+                        *reinterpret_cast<uint4 *>(dst + 2 * k) =
+                            make_uint4(pack_bf16x2(o[k], o[k + 1]), pack_bf16x2(o[k + 2], o[k + 3]),
+                                       pack_bf16x2(o[k + 4], o[k + 5]), pack_bf16x2(o[k + 6], o[k + 7]));
                 }
             }
+            __syncthreads();
+            for (int idx = tid; idx < 64 * CPR; idx += kQuadThreads) {
+                const int row = idx / CPR, pcs = idx % CPR;
+                const long long tt = t0 + 64 * h2 + row;
+                if (tt < L)
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(ybase + tt * H * Q::P) + 16 * pcs) =
+                        *reinterpret_cast<const uint4 *>(stg + row * ROWB + 16 * pcs);
+            }
+            __syncthreads();
         }
     }
 
@@ -397,19 +421,19 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
                         tma_load_5d(xs + (hh * (Q::P / 64) + pb) * Q::XB, &mx, &tma_bar, 0, pb, h0 + hh, j * kQT, b);
             }
             if (jj > 0 && !(ok = cta_wait(&tma_bar, tph, &ok_sh))) break;
-            // A operand (w o x)^T: row (head, p), steps s = 64 half .. + 63,
+            // A operand (w o x)^T: row (head, p), steps s = 32 cq .. + 31,
             // hi at column s / 2, lo 64 columns further
             const uint8_t *xb = xs + (rh * (Q::P / 64) + rp / 64) * Q::XB;
             const uint32_t pc = (uint32_t)(rp % 64);
             uint32_t hi[16], lo[16];
-#pragma unroll 1
-            for (int k0 = 0; k0 < 32; k0 += 16) {
+            {
+                constexpr int k0 = 0;
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
                     float a2[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int sl = half * 64 + 2 * (k0 + k) + e;
+                        const int sl = cq * 32 + 2 * (k0 + k) + e;
                         const long long s = (long long)j * kQT + sl;
                         const float xv =
                             __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(xb + swz128((uint32_t)sl, pc))
@@ -419,8 +443,8 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
                     hi[k] = pack_bf16x2(a2[0], a2[1]);
                     lo[k] = pack_bf16x2(a2[0] - __uint_as_float(hi[k] << 16), a2[1] - __uint_as_float(hi[k] & 0xFFFF0000u));
                 }
-                tmem_st16u(tmem + lane_off + Q::T_S + half * 32 + k0, hi);
-                tmem_st16u(tmem + lane_off + Q::T_S + 64 + half * 32 + k0, lo);
+                tmem_st16u(tmem + lane_off + Q::T_S + cq * 16, hi);
+                tmem_st16u(tmem + lane_off + Q::T_S + 64 + cq * 16, lo);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -444,27 +468,35 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
             tc_fence_after();
         }
         if (ok) {
-            const float el = __expf(clast);
-            const long long h = h0 + rh;
-            float *dst = prm.fin + (((long long)b * H + h) * Q::P + rp) * Q::N;
-            const float *ini = prm.init ? prm.init + (((long long)b * H + h) * Q::P + rp) * Q::N : nullptr;
+            // the tile [128 rows (head, p)][N] leaves through shared memory
+            // (rows padded by 16 bytes), then coalesced: the block's rows of
+            // the final state are consecutive in global memory
+            constexpr int ROWF = Q::N * 4 + 16;
+            uint8_t *stg = smem + Q::OFF_C;  // (C, B and x are free once the last MMAs completed)
 #pragma unroll 1
-            for (int n0 = half * (Q::N / 2); n0 < (half + 1) * (Q::N / 2); n0 += 16) {
+            for (int n0 = cq * (Q::N / 4); n0 < (cq + 1) * (Q::N / 4); n0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + lane_off + Q::T_F + n0, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 16; k += 4) {
-                    float4 o = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-                    if (ini) {
-                        const float4 a4 = __ldg(reinterpret_cast<const float4 *>(ini + n0 + k));
-                        o.x = fmaf(el, a4.x, o.x);
-                        o.y = fmaf(el, a4.y, o.y);
-                        o.z = fmaf(el, a4.z, o.z);
-                        o.w = fmaf(el, a4.w, o.w);
-                    }
-                    *reinterpret_cast<float4 *>(dst + n0 + k) = o;
+                for (int k = 0; k < 16; k += 4)
+                    *reinterpret_cast<float4 *>(stg + r * ROWF + 4 * (n0 + k)) =
+                        make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+            }
+            __syncthreads();
+            const long long base = ((long long)b * H + h0) * Q::P * Q::N;
+            for (int idx = tid; idx < 128 * (Q::N / 4); idx += kQuadThreads) {
+                const int row = idx / (Q::N / 4), c4 = idx % (Q::N / 4);
+                float4 o = *reinterpret_cast<const float4 *>(stg + row * ROWF + 16 * c4);
+                if (prm.init) {
+                    const float el = __expf(cum[(row / Q::P) * kQuadMaxL + L - 1]);
+                    const float4 a4 = __ldg(reinterpret_cast<const float4 *>(prm.init + base) + idx);
+                    o.x = fmaf(el, a4.x, o.x);
+                    o.y = fmaf(el, a4.y, o.y);
+                    o.z = fmaf(el, a4.z, o.z);
+                    o.w = fmaf(el, a4.w, o.w);
                 }
+                reinterpret_cast<float4 *>(prm.fin + base)[idx] = o;
             }
         }
     }
