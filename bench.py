@@ -311,10 +311,14 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=4)
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["stages", "sequential", "crossover", "decode"],
+                    help="run one part of the sweep alone and print its JSON (for profiling that part)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return run_reference(args)
+    if args.only:
+        return run_only(args)
 
     import torch
     import state_space_model_fwd_gb300 as ssd
@@ -612,19 +616,8 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
                "dominant_kernel": dom,
                "dominant_kernel_frac_hbm": cb / (kernels[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         if name == "long_16k":
-            def scan():
-                ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
-                                       y=y, final_state=fin)
-            sms = time_device(scan, flush, 3)
-            scan_flops = 5.0 * cfg.tokens * cfg.nheads * cfg.headdim * cfg.dstate
-            ffma = ffma_peak_tflops(dev)
-            rec["selective_scan_ms"] = sms
-            rec["selective_scan_roofline"] = {
-                "bound": "alu", "achieved": scan_flops / (sms * 1e-3) / 1e12, "peak": ffma, "unit": "TFLOP/s",
-                "frac": scan_flops / (sms * 1e-3) / 1e12 / ffma,
-                "flops": scan_flops, "flops_model": "5 fp32 flops per (token, head, p, n): decay, input, output",
-                "peak_source": "measured: cuBLAS SGEMM 8192^3 with TF32 off (FFMA), best of 5"}
-            rec["chunked_vs_sequential_speedup"] = sms / ms
+            rec.update(sequential_scan(ssd, dev, flush, t, y, fin, cfg))
+            rec["chunked_vs_sequential_speedup"] = rec["selective_scan_ms"] / ms
         out[name] = rec
         del t, y, fin, ws
         torch.cuda.empty_cache()
@@ -632,6 +625,49 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
     out["crossover"] = crossover_sweep(ssd, dev, flush, steps)
     out["decode"] = decode_sweep(ssd, dev, flush, peaks, steps)
     return out
+
+
+def sequential_scan(ssd, dev, flush, t, y, fin, cfg, steps=3):
+    """selective_scan_fwd on resident inputs, against the measured FFMA peak."""
+    def scan():
+        ssd.selective_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["init_state"],
+                               y=y, final_state=fin)
+    sms = time_device(scan, flush, steps)
+    scan_flops = 5.0 * cfg.tokens * cfg.nheads * cfg.headdim * cfg.dstate
+    ffma = ffma_peak_tflops(dev)
+    return {"selective_scan_ms": sms,
+            "selective_scan_roofline": {
+                "bound": "alu", "achieved": scan_flops / (sms * 1e-3) / 1e12, "peak": ffma, "unit": "TFLOP/s",
+                "frac": scan_flops / (sms * 1e-3) / 1e12 / ffma,
+                "flops": scan_flops, "flops_model": "5 fp32 flops per (token, head, p, n): decay, input, output",
+                "peak_source": "measured: cuBLAS SGEMM 8192^3 with TF32 off (FFMA), best of 5"}}
+
+
+def run_only(args):
+    """One part of the sweep on its own (stage entry points on the 2.7B-shaped
+    layer, the sequential scan on the 16K-token one, the chunked-vs-quadratic
+    crossover, or the decode step), printed as one JSON line; its kernels are
+    the only ones launched, which is what a profiler capture of them wants."""
+    import torch
+    import state_space_model_fwd_gb300 as ssd
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    peaks = load_peaks()
+    steps = max(1, args.steps)
+    if args.only == "stages":
+        out = stage_sweep(ssd, dev, flush, peaks, steps)
+    elif args.only == "sequential":
+        cfg = si.CONFIGS["long_16k"]
+        t = si.make_inputs(cfg).to_torch(dev)
+        y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
+        fin = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), device=dev, dtype=torch.float32)
+        out = {"workload": cfg.name, **sequential_scan(ssd, dev, flush, t, y, fin, cfg, steps)}
+    elif args.only == "crossover":
+        out = crossover_sweep(ssd, dev, flush, steps)
+    else:
+        out = decode_sweep(ssd, dev, flush, peaks, steps)
+    print(json.dumps({"only": args.only, **out}), flush=True)
 
 
 def stage_sweep(ssd, dev, flush, peaks, steps):

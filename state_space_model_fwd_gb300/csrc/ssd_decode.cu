@@ -13,7 +13,9 @@
 // the loads of all of them before any arithmetic (kRows 16-byte loads in
 // flight per lane), shares the head's scalars and its B and C rows between
 // them, and sums each row of y with interleaved shuffle reductions.  Lane l
-// owns the float4 runs j = l and j = l + 32 of n (N <= 256).
+// owns the float4 runs j = l + 32 jj of n, jj < NJ (NJ = 1 for N <= 128, 2 up
+// to N = 256: a kernel per case, so the N <= 128 one holds half the state
+// registers and fits more warps per SM).
 #include "ssd_common.cuh"
 
 namespace ssd {
@@ -34,7 +36,7 @@ __device__ __forceinline__ float4 load4<bf16>(const bf16 *p) {
 
 constexpr int kRows = 8;  // state rows per warp (P is a multiple of 16)
 
-template <typename T, typename TY>
+template <typename T, typename TY, int NJ>
 __global__ void __launch_bounds__(256) decode_step_kernel(Dims d, const T *__restrict__ x, const T *__restrict__ dt,
                                                           const float *__restrict__ A, const T *__restrict__ B,
                                                           const T *__restrict__ C, const float *__restrict__ D,
@@ -44,10 +46,10 @@ __global__ void __launch_bounds__(256) decode_step_kernel(Dims d, const T *__res
     if (row0 >= d.b * d.H * d.P) return;  // warp-uniform; P % kRows == 0, so all kRows rows exist
     const int64_t n4 = d.N / 4;
     float4 *s4 = reinterpret_cast<float4 *>(state + row0 * d.N);
-    bool has[2];
-    float4 s[kRows][2];
+    bool has[NJ];
+    float4 s[kRows][NJ];
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
+    for (int jj = 0; jj < NJ; ++jj) {
         has[jj] = lane + 32 * jj < n4;
 #pragma unroll
         for (int r = 0; r < kRows; ++r)
@@ -67,7 +69,7 @@ __global__ void __launch_bounds__(256) decode_step_kernel(Dims d, const T *__res
         acc[r] = 0.f;
     }
 #pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
+    for (int jj = 0; jj < NJ; ++jj) {
         if (!has[jj]) continue;
         const int64_t j = lane + 32 * jj;
         const float4 bb = load4<T>(Bt + 4 * j), cc = load4<T>(Ct + 4 * j);
@@ -109,7 +111,10 @@ cudaError_t launch_decode_step(const Dims &d, const T *x, const T *dt, const flo
     constexpr int kWarps = 8;
     const int64_t blocks = (rows / kRows + kWarps - 1) / kWarps;
     if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    decode_step_kernel<T, TY><<<(unsigned)blocks, kWarps * 32, 0, s>>>(d, x, dt, A, B, C, D, state, y);
+    if (d.N <= 128)
+        decode_step_kernel<T, TY, 1><<<(unsigned)blocks, kWarps * 32, 0, s>>>(d, x, dt, A, B, C, D, state, y);
+    else
+        decode_step_kernel<T, TY, 2><<<(unsigned)blocks, kWarps * 32, 0, s>>>(d, x, dt, A, B, C, D, state, y);
     timing_mark(s, "decode_step");
     return cudaGetLastError();
 }
