@@ -133,6 +133,13 @@ struct Cfg {
     // at N <= 128 the smaller register budget of the larger CTA costs more
     static constexpr int SG = N >= 256 ? 2 : 1;
     static constexpr int SCAN_THREADS = 768 + 128 * (SG - 1);
+    // registers per thread: at launch (the kernel's allocation), and after
+    // setmaxnreg for warps 0-3 (producer, MMA, vectors: few live values) and
+    // the compute warps; the split adds up to the launch allocation exactly
+    static constexpr int REG_LAUNCH = SG == 1 ? 80 : 72;
+    static constexpr int REG_LO = SG == 1 ? 48 : 40, REG_HI = SG == 1 ? 88 : 80;
+    static_assert(128 * REG_LO + 128 * SG * REG_LAUNCH + 512 * REG_HI == SCAN_THREADS * REG_LAUNCH,
+                  "register split of the chunk scan");
 
     // segment-state kernel: TMA stages of (x, B) and the vector ring
     static constexpr int SEG_STAGE = X_BYTES + BC_BYTES;
@@ -939,6 +946,8 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
 //   warps 4-7  : state: Ss rescale when the reference moves, and its bf16
 //                copy SB (the A operand of the inter-chunk term); with
 //                C::SG = 2 warps 24-27 take the second half of the columns
+//   (warps 0-3 give registers back with setmaxnreg, the compute warps take
+//   them: C::REG_LO / C::REG_HI per thread)
 //   warps 8-23 : compute, a quarter of the steps each: first the state
 //                entering the segment into Ss (a quarter of the columns
 //                each); then per chunk c the A operand into TMEM from the
@@ -1029,193 +1038,197 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     const int q4 = warp & 3;                  // TMEM lane quarter of this warp
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0)
-            for (int it = 0; it < nch; ++it) {
-                const int s = it % ST;
-                if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
-                const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
-                // two operations per chunk: the x box, then the chunk pack
-                // once the C B^T kernel has published it
-                if (prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
-                mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES);
-                tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, (c0 + it) * C::Q, b);
-                ++nload[s];
-                if (!prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
-                mbar_arrive_expect_tx(&pfull_bar[s], C::PACK_BYTES);
-                bulk_load(stage_cb(s), prm.pack + plane * C::PACK_BYTES, C::PACK_BYTES, &pfull_bar[s]);
-                ++npack[s];
-                TRACE(0, it);
-            }
-    } else if (warp == 2) {
-        // ---------------- per-chunk vectors (run up to NV chunks ahead) ----------------
-        constexpr int QPL = C::Q / 32;
-        float rho[C::HB];
-#pragma unroll
-        for (int hh = 0; hh < C::HB; ++hh) rho[hh] = 0.f;
-        auto chunk_of = [&](int it) { return c0 + it; };
-        DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
-        feed.start(prm, chunk_of);
-        float Ah[C::HB];
-        load_decay<C>(prm, h0, Ah);
-        for (int it = 0; it < nch; ++it) {
-            const int v = it % NV;
-            ChunkDt<C> dt;
-            if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
-            float cum[C::HB][QPL], T[C::HB];
-            chunk_cums<C>(prm, b, h0, c0 + it, dt, Ah, cum, T);
-            // range [lo, hi] of the cumulative decay over the chunk and its start (0)
-            int klo[C::HB], khi[C::HB];
-#pragma unroll
-            for (int hh = 0; hh < C::HB; ++hh) {
-                float lo = 0.f, hi = 0.f;
-#pragma unroll
-                for (int j = 0; j < QPL; ++j) {
-                    lo = fminf(lo, cum[hh][j]);
-                    hi = fmaxf(hi, cum[hh][j]);
+    if (warp < 4) {
+        // (the whole warpgroup gives registers back at one program point)
+        reg_dec<C::REG_LO>();
+        if (warp == 0) {
+            // ---------------- TMA producer ----------------
+            if (lane == 0)
+                for (int it = 0; it < nch; ++it) {
+                    const int s = it % ST;
+                    if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
+                    const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
+                    // two operations per chunk: the x box, then the chunk pack
+                    // once the C B^T kernel has published it
+                    if (prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
+                    mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES);
+                    tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, (c0 + it) * C::Q, b);
+                    ++nload[s];
+                    if (!prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
+                    mbar_arrive_expect_tx(&pfull_bar[s], C::PACK_BYTES);
+                    bulk_load(stage_cb(s), prm.pack + plane * C::PACK_BYTES, C::PACK_BYTES, &pfull_bar[s]);
+                    ++npack[s];
+                    TRACE(0, it);
                 }
-                klo[hh] = __reduce_min_sync(0xffffffffu, fkey(lo));
-                khi[hh] = __reduce_max_sync(0xffffffffu, fkey(hi));
-            }
-            bool rescale = false, wide = false;
-            float al[C::HB][QPL], ef[C::HB][QPL], f[C::HB], sbf[C::HB], rn[C::HB];
+        } else if (warp == 2) {
+            // ---------------- per-chunk vectors (run up to NV chunks ahead) ----------------
+            constexpr int QPL = C::Q / 32;
+            float rho[C::HB];
 #pragma unroll
-            for (int hh = 0; hh < C::HB; ++hh) {
-                const float lo = unkey(klo[hh]), hi = unkey(khi[hh]);
-                // rho stays while every exponent rho - cum_s stays within kLambda;
-                // else it moves to the lowest reference the chunk allows,
-                // hi - kLambda (rho then grows by the decay of each later chunk,
-                // so the lowest start keeps it longest before the next move);
-                // a range wider than 2 kLambda centres the state at the chunk's
-                // end and leaves the intra-chunk term to the direct path.
-                // The rescale exp(rc - rho) may fall below the fp32 range (rho
-                // up to kLambda, rc down to -kLambda) while the rescaled state
-                // does not: the state warps apply it as two factors
-                // f = exp((rc - rho) / 2).  sbf < 0: the bf16 copy is the
-                // rescaled state; else the old state times sbf.
-                float rc = rho[hh];
-                f[hh] = 1.f;
-                sbf[hh] = 1.f;
-                bool hw = false;
-                if (rho[hh] - lo > kLambda || hi - rho[hh] > kLambda) {
-                    rescale = true;
-                    if (hi - lo <= 2.f * kLambda) {
-                        rc = hi - kLambda;
-                        f[hh] = __expf(0.5f * (rc - rho[hh]));
-                        sbf[hh] = -1.f;
-                    } else {
-                        // (after a decay of more than 2 kLambda the old state is
-                        // below fp32 resolution: f may flush to zero)
-                        hw = true;
-                        rc = T[hh];
-                        f[hh] = __expf(0.5f * (T[hh] - rho[hh]));
-                        sbf[hh] = __expf(-rho[hh]);
+            for (int hh = 0; hh < C::HB; ++hh) rho[hh] = 0.f;
+            auto chunk_of = [&](int it) { return c0 + it; };
+            DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
+            feed.start(prm, chunk_of);
+            float Ah[C::HB];
+            load_decay<C>(prm, h0, Ah);
+            for (int it = 0; it < nch; ++it) {
+                const int v = it % NV;
+                ChunkDt<C> dt;
+                if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
+                float cum[C::HB][QPL], T[C::HB];
+                chunk_cums<C>(prm, b, h0, c0 + it, dt, Ah, cum, T);
+                // range [lo, hi] of the cumulative decay over the chunk and its start (0)
+                int klo[C::HB], khi[C::HB];
+#pragma unroll
+                for (int hh = 0; hh < C::HB; ++hh) {
+                    float lo = 0.f, hi = 0.f;
+#pragma unroll
+                    for (int j = 0; j < QPL; ++j) {
+                        lo = fminf(lo, cum[hh][j]);
+                        hi = fmaxf(hi, cum[hh][j]);
+                    }
+                    klo[hh] = __reduce_min_sync(0xffffffffu, fkey(lo));
+                    khi[hh] = __reduce_max_sync(0xffffffffu, fkey(hi));
+                }
+                bool rescale = false, wide = false;
+                float al[C::HB][QPL], ef[C::HB][QPL], f[C::HB], sbf[C::HB], rn[C::HB];
+#pragma unroll
+                for (int hh = 0; hh < C::HB; ++hh) {
+                    const float lo = unkey(klo[hh]), hi = unkey(khi[hh]);
+                    // rho stays while every exponent rho - cum_s stays within kLambda;
+                    // else it moves to the lowest reference the chunk allows,
+                    // hi - kLambda (rho then grows by the decay of each later chunk,
+                    // so the lowest start keeps it longest before the next move);
+                    // a range wider than 2 kLambda centres the state at the chunk's
+                    // end and leaves the intra-chunk term to the direct path.
+                    // The rescale exp(rc - rho) may fall below the fp32 range (rho
+                    // up to kLambda, rc down to -kLambda) while the rescaled state
+                    // does not: the state warps apply it as two factors
+                    // f = exp((rc - rho) / 2).  sbf < 0: the bf16 copy is the
+                    // rescaled state; else the old state times sbf.
+                    float rc = rho[hh];
+                    f[hh] = 1.f;
+                    sbf[hh] = 1.f;
+                    bool hw = false;
+                    if (rho[hh] - lo > kLambda || hi - rho[hh] > kLambda) {
+                        rescale = true;
+                        if (hi - lo <= 2.f * kLambda) {
+                            rc = hi - kLambda;
+                            f[hh] = __expf(0.5f * (rc - rho[hh]));
+                            sbf[hh] = -1.f;
+                        } else {
+                            // (after a decay of more than 2 kLambda the old state is
+                            // below fp32 resolution: f may flush to zero)
+                            hw = true;
+                            rc = T[hh];
+                            f[hh] = __expf(0.5f * (T[hh] - rho[hh]));
+                            sbf[hh] = __expf(-rho[hh]);
+                        }
+                    }
+                    wide |= hw;
+#pragma unroll
+                    for (int j = 0; j < QPL; ++j) {
+                        al[hh][j] = __expf(rc - cum[hh][j]) * dt.d[hh][j];
+                        ef[hh][j] = __expf(hw ? cum[hh][j] : cum[hh][j] - rc);
+                    }
+                    rn[hh] = rc - T[hh];
+                    rho[hh] = rn[hh];
+                }
+                if (it >= NV) {
+                    int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], free_parity(it, NV), &abort_sh) ? 1 : 0) : 0;
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                }
+                float *vv = vec(v);
+#pragma unroll
+                for (int hh = 0; hh < C::HB; ++hh) {
+#pragma unroll
+                    for (int j = 0; j < QPL; ++j) {
+                        const int q = hh * C::Q + QPL * lane + j;
+                        vv[C::V_DT + q] = dt.d[hh][j];
+                        vv[C::V_CUM + q] = cum[hh][j];
+                        vv[C::V_AL + q] = al[hh][j];
+                        vv[C::V_EF + q] = ef[hh][j];
+                    }
+                    if (lane == 0) {
+                        vv[C::V_F + hh] = f[hh];
+                        vv[C::V_SBF + hh] = sbf[hh];
+                        vv[C::V_RHON + hh] = rn[hh];
                     }
                 }
-                wide |= hw;
-#pragma unroll
-                for (int j = 0; j < QPL; ++j) {
-                    al[hh][j] = __expf(rc - cum[hh][j]) * dt.d[hh][j];
-                    ef[hh][j] = __expf(hw ? cum[hh][j] : cum[hh][j] - rc);
-                }
-                rn[hh] = rc - T[hh];
-                rho[hh] = rn[hh];
-            }
-            if (it >= NV) {
-                int ok = lane == 0 ? (wait_bounded(&vempty_bar[v], free_parity(it, NV), &abort_sh) ? 1 : 0) : 0;
-                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            }
-            float *vv = vec(v);
-#pragma unroll
-            for (int hh = 0; hh < C::HB; ++hh) {
-#pragma unroll
-                for (int j = 0; j < QPL; ++j) {
-                    const int q = hh * C::Q + QPL * lane + j;
-                    vv[C::V_DT + q] = dt.d[hh][j];
-                    vv[C::V_CUM + q] = cum[hh][j];
-                    vv[C::V_AL + q] = al[hh][j];
-                    vv[C::V_EF + q] = ef[hh][j];
-                }
                 if (lane == 0) {
-                    vv[C::V_F + hh] = f[hh];
-                    vv[C::V_SBF + hh] = sbf[hh];
-                    vv[C::V_RHON + hh] = rn[hh];
-                }
-            }
-            if (lane == 0) {
-                vv[C::V_FLAG] = rescale ? 1.f : 0.f;
-                vv[C::V_FLAG + 1] = wide ? 1.f : 0.f;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                TRACE(1, it);
-                mbar_arrive(&vfull_bar[v]);
-            }
-        }
-        feed.drain();
-    } else if (warp == 1) {
-        // ---------------- MMA issuer: the whole warp runs the loop (its
-        // descriptors stay warp-uniform), one elected lane issues ----------------
-        {
-            const uint32_t id_intra = idesc_bf16(C::M, C::Q, false, false);
-            const uint32_t id_state = idesc_bf16(C::M, C::N, false, true);
-            const uint32_t id_inter = idesc_bf16(C::M, C::Q, false, false);
-            for (int it = 0; it < nch; ++it) {
-                const int s = it % ST, a = it % NB;
-                // one descriptor per operand tile, advanced by constants (the
-                // single issuing thread must not spend cycles per MMA)
-                const uint64_t dcb = sdesc(smem_u32(stage_cb(s)), 16, 1024);
-                const uint64_t db = sdesc(smem_u32(stage_b(s)), C::Q * 128, 1024);
-                const uint64_t dc = sdesc(smem_u32(stage_c(s)), 16, 1024);
-                const uint32_t ta = tmem + C::COL_A + a * C::Q, tr = tmem + C::COL_R + a * C::Q;
-                const uint32_t tsb = tmem + C::COL_SB + a * (C::N / 2);
-                if (!warp_wait(&pfull_bar[s], fill_parity(it, ST), &abort_sh)) break;
-                TRACE(20, it);
-                if (!warp_wait(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
-                TRACE(21, it);
-                // Ss += A^T B first: the state chain (state warps -> these
-                // MMAs -> state warps) is the longest loop of the pipeline, so
-                // it waits for no other MMA; once the state warps have read
-                // (and rescaled) Ss and written SB
-                if (!warp_wait(&rt_bar, (uint32_t)(it & 1), &abort_sh)) break;
-                tc_fence_after();
-                if (elect_one()) {
-#pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 16, desc_add(db, ks * 2048), id_state, true);
-#pragma unroll
-                for (int ks = 0; ks < C::Q / 16; ++ks)
-                    mma_bf16_ta(tmem + C::COL_S, ta + ks * 16 + 8, desc_add(db, ks * 2048), id_state, true);
-                mma_commit(&sdone_bar);
+                    vv[C::V_FLAG] = rescale ? 1.f : 0.f;
+                    vv[C::V_FLAG + 1] = wide ? 1.f : 0.f;
                 }
                 __syncwarp();
-                if (it >= NB && !warp_wait(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
-                TRACE(22, it);
-                tc_fence_after();
-                const bool wide = vec(it % NV)[C::V_FLAG + 1] != 0.f;  // (the A builders saw this slot filled)
-                if (elect_one()) {
-                // R = A CB^T (hi, then lo)
-                if (!wide) {
+                if (lane == 0) {
+                    TRACE(1, it);
+                    mbar_arrive(&vfull_bar[v]);
+                }
+            }
+            feed.drain();
+        } else if (warp == 1) {
+            // ---------------- MMA issuer: the whole warp runs the loop (its
+            // descriptors stay warp-uniform), one elected lane issues ----------------
+            {
+                const uint32_t id_intra = idesc_bf16(C::M, C::Q, false, false);
+                const uint32_t id_state = idesc_bf16(C::M, C::N, false, true);
+                const uint32_t id_inter = idesc_bf16(C::M, C::Q, false, false);
+                for (int it = 0; it < nch; ++it) {
+                    const int s = it % ST, a = it % NB;
+                    // one descriptor per operand tile, advanced by constants (the
+                    // single issuing thread must not spend cycles per MMA)
+                    const uint64_t dcb = sdesc(smem_u32(stage_cb(s)), 16, 1024);
+                    const uint64_t db = sdesc(smem_u32(stage_b(s)), C::Q * 128, 1024);
+                    const uint64_t dc = sdesc(smem_u32(stage_c(s)), 16, 1024);
+                    const uint32_t ta = tmem + C::COL_A + a * C::Q, tr = tmem + C::COL_R + a * C::Q;
+                    const uint32_t tsb = tmem + C::COL_SB + a * (C::N / 2);
+                    if (!warp_wait(&pfull_bar[s], fill_parity(it, ST), &abort_sh)) break;
+                    TRACE(20, it);
+                    if (!warp_wait(&afull_bar[a], fill_parity(it, NB), &abort_sh)) break;
+                    TRACE(21, it);
+                    // Ss += A^T B first: the state chain (state warps -> these
+                    // MMAs -> state warps) is the longest loop of the pipeline, so
+                    // it waits for no other MMA; once the state warps have read
+                    // (and rescaled) Ss and written SB
+                    if (!warp_wait(&rt_bar, (uint32_t)(it & 1), &abort_sh)) break;
+                    tc_fence_after();
+                    if (elect_one()) {
 #pragma unroll
                     for (int ks = 0; ks < C::Q / 16; ++ks)
-                        mma_bf16_ta(tr, ta + ks * 16, desc_add(dcb, ks * 32), id_intra, ks > 0);
+                        mma_bf16_ta(tmem + C::COL_S, ta + ks * 16, desc_add(db, ks * 2048), id_state, true);
 #pragma unroll
                     for (int ks = 0; ks < C::Q / 16; ++ks)
-                        mma_bf16_ta(tr, ta + ks * 16 + 8, desc_add(dcb, ks * 32), id_intra, true);
-                }
-                mma_commit(&afree_bar[a]);
-                TRACE(2, it);
-                // R += SB C^T
+                        mma_bf16_ta(tmem + C::COL_S, ta + ks * 16 + 8, desc_add(db, ks * 2048), id_state, true);
+                    mma_commit(&sdone_bar);
+                    }
+                    __syncwarp();
+                    if (it >= NB && !warp_wait(&rfree_bar[a], free_parity(it, NB), &abort_sh)) break;
+                    TRACE(22, it);
+                    tc_fence_after();
+                    const bool wide = vec(it % NV)[C::V_FLAG + 1] != 0.f;  // (the A builders saw this slot filled)
+                    if (elect_one()) {
+                    // R = A CB^T (hi, then lo)
+                    if (!wide) {
 #pragma unroll
-                for (int ks = 0; ks < C::N / 16; ++ks)
-                    mma_bf16_ta(tr, tsb + ks * 8, desc_add(dc, (ks / 4) * (C::Q * 128) + (ks % 4) * 32), id_inter,
-                                !wide || ks > 0);
-                mma_commit(&rfull_bar[a]);
-                mma_commit(&sbfree_bar[a]);
-                mma_commit(&empty_bar[s]);
+                        for (int ks = 0; ks < C::Q / 16; ++ks)
+                            mma_bf16_ta(tr, ta + ks * 16, desc_add(dcb, ks * 32), id_intra, ks > 0);
+#pragma unroll
+                        for (int ks = 0; ks < C::Q / 16; ++ks)
+                            mma_bf16_ta(tr, ta + ks * 16 + 8, desc_add(dcb, ks * 32), id_intra, true);
+                    }
+                    mma_commit(&afree_bar[a]);
+                    TRACE(2, it);
+                    // R += SB C^T
+#pragma unroll
+                    for (int ks = 0; ks < C::N / 16; ++ks)
+                        mma_bf16_ta(tr, tsb + ks * 8, desc_add(dc, (ks / 4) * (C::Q * 128) + (ks % 4) * 32), id_inter,
+                                    !wide || ks > 0);
+                    mma_commit(&rfull_bar[a]);
+                    mma_commit(&sbfree_bar[a]);
+                    mma_commit(&empty_bar[s]);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
         }
     } else if ((warp >= 4 && warp < 8) || warp >= 24) {
@@ -1309,6 +1322,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
         }
     } else if (warp >= 8 && warp < 24) {
         // ---------------- compute warps: thread = row (head, p), a quarter of the Q steps ----------------
+        reg_inc<C::REG_HI>();
         // Chunk c: the A operand from the staged x (kept in registers), then
         // the output of chunk c - 1:  y = factor R + D x.
         const int part = (warp - 8) >> 2;
@@ -1696,6 +1710,16 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q)) return cudaErrorInvalidValue;
     if (!make_y_map(&my, prm.y, f32, d.P, d.H, d.L, d.b, C::Q)) return cudaErrorInvalidValue;
     static int attr_f = 0, attr_b = 0;
+    // the warps' register split assumes the kernel's launch allocation: a
+    // build that allocates otherwise must not run (an increase that cannot
+    // be met would wait forever)
+    {
+        cudaFuncAttributes fa;
+        cudaError_t e = f32 ? cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, float>)
+                            : cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, bf16>);
+        if (e != cudaSuccess) return e;
+        if ((fa.numRegs + 7) / 8 * 8 != C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
+    }
     cudaError_t e;
     if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
