@@ -63,7 +63,8 @@ struct TcParams {
     float *fin;
     float *seg_state;   // [b, nseg, H, P, N]: segment-local states (each segment from a zero state)
     float *seg_tot;     // [b, H, nseg]  total dt*A of each segment (may be null)
-    const float *cum_in;    // [b, H, nc, Q] given in-chunk cumulative decay (null: computed from dt, A)
+    const float *cum_in;    // [b, H, nc_cum, cum_q] the caller's in-chunk cumulative decay (null: computed)
+    int cum_q, nc_cum;      // the caller's chunk length (64 or 128: one or two tiles) and chunk count
     const float *entering;  // [b, nseg, H, P, N] state entering each segment (null: init / seg_state)
     unsigned *status;   // the device status word: bit 0 = a wait gave up (may be null)
     // limit of the wait for a chunk pack's ready flag (the self-test of the
@@ -367,6 +368,18 @@ struct DtFeed {
     }
 };
 
+// The caller's dA_cumsum for tile c of head h, relative to the tile's start:
+// a chunk of cum_q = 128 steps is two tiles, and the second tile's values are
+// those of the chunk minus the chunk's value before the tile.
+template <class C>
+__device__ __forceinline__ const float *tile_cum(const TcParams &prm, int b, long long h, int c, float &base) {
+    const int tpc = prm.cum_q / C::Q;  // tiles per caller chunk
+    const int cc = c / tpc, off = (c % tpc) * C::Q;
+    const float *src = prm.cum_in + (((long long)b * prm.H + h) * prm.nc_cum + cc) * prm.cum_q + off;
+    base = off > 0 ? __ldg(src - 1) : 0.f;
+    return src;
+}
+
 // In-chunk cumulative decay of every head for this lane's steps: the scan of
 // dt*A (all heads' shuffle chains interleaved), or the caller's dA_cumsum.
 // T[hh] = the chunk total (cum of the last step).
@@ -380,10 +393,11 @@ __device__ __forceinline__ void chunk_cums(const TcParams &prm, int b, int h0, i
 #pragma unroll
         for (int hh = 0; hh < C::HB; ++hh) {
             const long long h = h0 + hh;
-            const float *src = prm.cum_in + (((long long)b * prm.H + (h < prm.H ? h : 0)) * prm.nc + c) * C::Q;
+            float base;
+            const float *src = tile_cum<C>(prm, b, h < prm.H ? h : 0, c, base);
 #pragma unroll
-            for (int j = 0; j < QPL; ++j) cum[hh][j] = h < prm.H ? __ldg(src + QPL * lane + j) : 0.f;
-            T[hh] = h < prm.H ? __ldg(src + C::Q - 1) : 0.f;
+            for (int j = 0; j < QPL; ++j) cum[hh][j] = h < prm.H ? __ldg(src + QPL * lane + j) - base : 0.f;
+            T[hh] = h < prm.H ? __ldg(src + C::Q - 1) - base : 0.f;
         }
         return;
     }
@@ -424,10 +438,11 @@ __device__ __forceinline__ void head_cums(const TcParams &prm, int b, int h0, in
     const int lane = threadIdx.x & 31;
     const long long h = h0 + hh;
     if (prm.cum_in) {
-        const float *src = prm.cum_in + (((long long)b * prm.H + (h < prm.H ? h : 0)) * prm.nc + c) * C::Q;
+        float base;
+        const float *src = tile_cum<C>(prm, b, h < prm.H ? h : 0, c, base);
 #pragma unroll
-        for (int j = 0; j < QPL; ++j) cum[j] = h < prm.H ? __ldg(src + QPL * lane + j) : 0.f;
-        T = h < prm.H ? __ldg(src + C::Q - 1) : 0.f;
+        for (int j = 0; j < QPL; ++j) cum[j] = h < prm.H ? __ldg(src + QPL * lane + j) - base : 0.f;
+        T = h < prm.H ? __ldg(src + C::Q - 1) - base : 0.f;
         return;
     }
     float run = 0.f;
@@ -1761,6 +1776,8 @@ TcParams base_params(const Dims &d, const void *dt, unsigned *status) {
     prm.G = d.G;
     prm.hpg = d.hpg;
     prm.nc = (int)d.nc;
+    prm.cum_q = (int)d.Q;
+    prm.nc_cum = (int)d.nc;
     return prm;
 }
 
@@ -1865,8 +1882,9 @@ cudaError_t tc_fwd(const Dims &dq, ssd_dtype_t ydtype, const void *x, const void
     return e;
 }
 
-bool tc_stage_supported(const Dims &d, ssd_dtype_t dtype) {
-    if (dtype != SSD_DTYPE_BF16 || d.L == 0 || d.b == 0) return false;
+bool tc_stage_supported(const Dims &dq, ssd_dtype_t dtype) {
+    if (dtype != SSD_DTYPE_BF16 || dq.L == 0 || dq.b == 0) return false;
+    const Dims d = fwd_tiles(dq);
     bool ok = false;
     dispatch(d, [&](auto c) {
         using C = decltype(c);
@@ -1877,18 +1895,22 @@ bool tc_stage_supported(const Dims &d, ssd_dtype_t dtype) {
 
 namespace {
 
+// A stage call's chunks of dq.Q steps run as segments of dq.Q / 64 tiles of
+// 64 steps (d = the tile dimensions).
 template <class C>
-cudaError_t run_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
-                            float *states, unsigned *status, cudaStream_t s) {
+cudaError_t run_chunk_state(const Dims &dq, const Dims &d, const void *x, const void *dt, const void *B,
+                            const float *cum, float *states, unsigned *status, cudaStream_t s) {
     TcParams prm = base_params(d, dt, status);
     prm.cum_in = cum;
+    prm.cum_q = (int)dq.Q;
+    prm.nc_cum = (int)dq.nc;
     prm.seg_state = states;  // [b, nc, H, P, N]: one segment per chunk
-    prm.nseg = (int)d.nc;
-    prm.cps = 1;
+    prm.nseg = (int)dq.nc;
+    prm.cps = (int)(dq.Q / C::Q);
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
     timing_begin(s);
-    return launch_seg_state<C>(d, prm, x, B, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc), "chunk_state_tc",
-                               false, s);
+    return launch_seg_state<C>(d, prm, x, B, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)dq.nc),
+                               "chunk_state_tc", false, s);
 }
 
 // The chunk packs of a stage call and their ready flags live in the
@@ -1902,17 +1924,19 @@ size_t scan_stage_workspace(const Dims &d) {
 }
 
 template <class C>
-cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
-                           const void *Cm, const float *cum, const float *states_in, const float *D, void *y,
-                           void *ws, unsigned *status, uint64_t selftest_ns, cudaStream_t s) {
+cudaError_t run_chunk_scan(const Dims &dq, const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt,
+                           const void *B, const void *Cm, const float *cum, const float *states_in, const float *D,
+                           void *y, void *ws, unsigned *status, uint64_t selftest_ns, cudaStream_t s) {
     TcParams prm = base_params(d, dt, status);
     prm.cum_in = cum;
+    prm.cum_q = (int)dq.Q;
+    prm.nc_cum = (int)dq.nc;
     prm.entering = states_in;  // [b, nc, H, P, N]: the state entering each chunk
     prm.x = static_cast<const bf16 *>(x);
     prm.D = D;
     prm.y = y;
-    prm.nseg = (int)d.nc;
-    prm.cps = 1;
+    prm.nseg = (int)dq.nc;
+    prm.cps = (int)(dq.Q / C::Q);
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
     char *w = static_cast<char *>(ws);
     prm.cb_ready = reinterpret_cast<unsigned *>(w);
@@ -1926,32 +1950,36 @@ cudaError_t run_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, con
     timing_begin(s);
     if (e == cudaSuccess && selftest_ns == 0) e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, status, s);
     if (e == cudaSuccess)
-        e = launch_scan<C>(d, prm, ydtype, x, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)d.nc),
+        e = launch_scan<C>(d, prm, ydtype, x, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)dq.nc),
                            "chunk_scan_stage_tc", selftest_ns == 0, s);
     return e;
 }
 
 }  // namespace
 
-cudaError_t tc_chunk_state(const Dims &d, const void *x, const void *dt, const void *B, const float *cum,
+cudaError_t tc_chunk_state(const Dims &dq, const void *x, const void *dt, const void *B, const float *cum,
                            float *states, unsigned *status, cudaStream_t s) {
+    const Dims d = fwd_tiles(dq);
     cudaError_t e = cudaErrorNotSupported;
-    dispatch(d, [&](auto c) { e = run_chunk_state<decltype(c)>(d, x, dt, B, cum, states, status, s); });
+    dispatch(d, [&](auto c) { e = run_chunk_state<decltype(c)>(dq, d, x, dt, B, cum, states, status, s); });
     return e;
 }
 
-size_t tc_chunk_scan_workspace(const Dims &d) {
+size_t tc_chunk_scan_workspace(const Dims &dq) {
+    const Dims d = fwd_tiles(dq);
     size_t bytes = 0;
     dispatch(d, [&](auto c) { bytes = scan_stage_workspace<decltype(c)>(d); });
     return bytes;
 }
 
-cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
+cudaError_t tc_chunk_scan(const Dims &dq, ssd_dtype_t ydtype, const void *x, const void *dt, const void *B,
                           const void *C, const float *cum, const float *states_in, const float *D, void *y,
                           void *ws, unsigned *status, uint64_t selftest_ns, cudaStream_t s) {
+    const Dims d = fwd_tiles(dq);
     cudaError_t e = cudaErrorNotSupported;
     dispatch(d, [&](auto c) {
-        e = run_chunk_scan<decltype(c)>(d, ydtype, x, dt, B, C, cum, states_in, D, y, ws, status, selftest_ns, s);
+        e = run_chunk_scan<decltype(c)>(dq, d, ydtype, x, dt, B, C, cum, states_in, D, y, ws, status, selftest_ns,
+                                        s);
     });
     return e;
 }

@@ -243,7 +243,8 @@ def test_ssd_fwd_no_optional_inputs():
 
 
 @pytest.mark.parametrize("name", ["tiny_f32", "bf16_p64_n128", "bf16_p128_n256_q128", "bf16_p16_n16",
-                                  "tc_p64_n128_seg", "tc_p64_n128_g2", "bf16_p128_n256_q64", "bf16_p64_n128_h5"])
+                                  "tc_p64_n128_seg", "tc_p64_n128_g2", "bf16_p128_n256_q64", "bf16_p64_n128_h5",
+                                  "tc_p64_n128_q128"])
 def test_stages_against_definitions(name):
     """Each stage entry point against the oracle's definition of its output,
     fed the oracle's own (rounded to fp32) inputs for the stage."""
@@ -272,7 +273,7 @@ def test_stages_against_definitions(name):
     check(to_np(y), y_ref, tol, "chunk scan y")
 
 
-@pytest.mark.parametrize("name", ["tc_p64_n128_seg", "bf16_p128_n256_q64"])
+@pytest.mark.parametrize("name", ["tc_p64_n128_seg", "bf16_p128_n256_q64", "tc_p64_n128_q128"])
 def test_stage_chain_matches_fused(name):
     """cumsum -> chunk_state -> state_passing -> chunk_scan (each on its own
     kernel) against ssd_fwd and the oracle, y in fp32 and in bf16."""

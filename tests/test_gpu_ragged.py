@@ -39,6 +39,8 @@ RAGGED = [
     si.SSDConfig("rg_simt_bf16", 2, 150, 3, 32, 64, 1, 64, "bf16", True, 806),
     si.SSDConfig("rg_f32", 1, 333, 2, 16, 16, 1, 64, "f32", True, 807),
     si.SSDConfig("rg_short", 1, 5, 2, 64, 128, 1, 64, "bf16", True, 808),
+    # Q = 128 chunks run as two 64-step tiles: a last chunk of one partial tile
+    si.SSDConfig("rg_tc_q128_onetile", 1, 936, 4, 64, 128, 1, 128, "bf16", True, 809),
 ]
 
 
@@ -54,7 +56,8 @@ def test_ssd_fwd_ragged(cfg):
     assert rel_err(to_np(fin), fin_ref) <= TOL[cfg.dtype]
 
 
-@pytest.mark.parametrize("cfg", [RAGGED[0], RAGGED[2], RAGGED[5], RAGGED[6]], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [RAGGED[0], RAGGED[1], RAGGED[2], RAGGED[5], RAGGED[6], RAGGED[8]],
+                         ids=lambda c: c.name)
 def test_stages_ragged(cfg):
     """Each stage entry point with a partial last chunk against the oracle's
     stage definitions (its missing cumsum entries repeat the last value)."""
