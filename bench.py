@@ -622,7 +622,8 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
                "tile_steps": FWD_TILE,
                "launch_ms": {k: round(v, 5) for k, v in kernels.items()},
                "dominant_kernel": dom,
-               "dominant_kernel_frac_hbm": cb / (kernels[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+               "dominant_kernel_frac_hbm": cb / (kernels[dom] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+               "dominant_kernel_traffic": recorded_traffic(dom, name)}
         if name == "long_16k":
             rec.update(sequential_scan(ssd, dev, flush, t, y, fin, cfg))
             rec["chunked_vs_sequential_speedup"] = rec["selective_scan_ms"] / ms
