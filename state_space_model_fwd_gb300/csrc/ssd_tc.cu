@@ -1381,7 +1381,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                 if (live && src) {
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
-                        const float4 a4 = __ldcg(reinterpret_cast<const float4 *>(src + n0 + j));
+                        const float4 a4 = __ldg(reinterpret_cast<const float4 *>(src + n0 + j));
                         v[j] = a4.x;
                         v[j + 1] = a4.y;
                         v[j + 2] = a4.z;
@@ -1407,8 +1407,8 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                         float4 l0[4], l1[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            l0[j] = __ldcg(reinterpret_cast<const float4 *>(loc + k * sstride + n0 + 4 * j));
-                            l1[j] = two ? __ldcg(reinterpret_cast<const float4 *>(loc + (k + 1) * sstride + n0 + 4 * j))
+                            l0[j] = __ldg(reinterpret_cast<const float4 *>(loc + k * sstride + n0 + 4 * j));
+                            l1[j] = two ? __ldg(reinterpret_cast<const float4 *>(loc + (k + 1) * sstride + n0 + 4 * j))
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
                         const float t0 = __ldcg(tot + k), t1 = two ? __ldcg(tot + k + 1) : 0.f;
