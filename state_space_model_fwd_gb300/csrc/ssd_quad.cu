@@ -21,8 +21,11 @@
 // state: Fin += (w o x_j)^T B_j, the A operand (bf16 hi + lo) in TMEM.
 // Each head's masked scores are computed once, both bf16 parts written (the
 // lo part into the init tiles' region, free once R is complete), and the
-// MMAs of the two parts issued together.  The y and final-state tiles leave
-// through shared memory so that the global stores are coalesced.
+// MMAs of the two parts issued together.  Score blocks that the mask or the
+// sequence end zero out wholly are written as zeros without reading S, and
+// the MMAs stop at the last K step holding a step before L.  The y and
+// final-state tiles leave through shared memory so that the global stores
+// are coalesced.
 // Everything is single-buffered and phase by phase; every wait is bounded.
 #include <cudaTypedefs.h>
 
@@ -283,10 +286,18 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
             uint8_t *mhi = ms + blk * (kQT * 128), *mlo = ms2 + blk * (kQT * 128);
 #pragma unroll 1
             for (int c0 = cb; c0 < cb + 32; c0 += 16) {
+                uint32_t wh[8], wl[8];
+                // (warp-uniform) every step of the group after every row of the
+                // warp, or every row at or past L: zeros, no scores read
+                const long long s_lo = (long long)j * kQT + blk * 64 + c0;
+                const long long t_lo = t0 + 32 * q4, t_hi = t_lo + 31;
+                if (s_lo > t_hi || t_lo >= L) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) wh[k] = wl[k] = 0u;
+                } else {
                 float v[16];
                 tmem_ld16(tmem + lane_off + Q::T_S + blk * 64 + c0, v);
                 tmem_ld_wait();
-                uint32_t wh[8], wl[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     float m2[2];
@@ -299,6 +310,7 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
                     const uint32_t hw = pack_bf16x2(m2[0], m2[1]);
                     wh[k] = hw;
                     wl[k] = pack_bf16x2(m2[0] - __uint_as_float(hw << 16), m2[1] - __uint_as_float(hw & 0xFFFF0000u));
+                }
                 }
                 *reinterpret_cast<uint4 *>(mhi + swz128((uint32_t)r, (uint32_t)c0)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
                 *reinterpret_cast<uint4 *>(mhi + swz128((uint32_t)r, (uint32_t)(c0 + 8))) =
@@ -314,13 +326,15 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, 64, false, true);
+                // K steps whose 16 columns all lie at or past L hold zeros
+                const long long left = L - (long long)j * kQT;
+                const int nks = left >= kQT ? kQT / 16 : (int)((left + 15) / 16);
                 for (int part = 0; part < 2; ++part) {
                     const uint64_t dm = part == 0 ? dM : dM2;
                     for (int pb = 0; pb < Q::P / 64; ++pb) {
                         const uint64_t dx = sdesc(smem_u32(xs + (hh * (Q::P / 64) + pb) * Q::XB), kQT * 128, 1024);
                         const uint32_t ty = tmem + Q::T_Y + hh * Q::P + pb * 64;
-#pragma unroll
-                        for (int ks = 0; ks < kQT / 16; ++ks) {
+                        for (int ks = 0; ks < nks; ++ks) {
                             const uint32_t adv = (ks / 4) * (kQT * 128) + (ks % 4) * 32;
                             if (j == 0 && part == 0)
                                 mma_bf16(ty, desc_add(dm, adv), desc_add(dx, ks * 2048), id, ks > 0);
@@ -426,7 +440,12 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
             const uint8_t *xb = xs + (rh * (Q::P / 64) + rp / 64) * Q::XB;
             const uint32_t pc = (uint32_t)(rp % 64);
             uint32_t hi[16], lo[16];
-            {
+            if ((long long)j * kQT + cq * 32 >= L) {  // (warp-uniform: steps at or past L)
+#pragma unroll
+                for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
+                tmem_st16u(tmem + lane_off + Q::T_S + cq * 16, hi);
+                tmem_st16u(tmem + lane_off + Q::T_S + 64 + cq * 16, lo);
+            } else {
                 constexpr int k0 = 0;
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
@@ -452,15 +471,15 @@ __global__ void __launch_bounds__(kQuadThreads, 1)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t id = idesc_bf16(128, Q::N, false, true);
-#pragma unroll
-                for (int ks = 0; ks < kQT / 16; ++ks) {
+                const long long left = L - (long long)j * kQT;  // (steps at or past L: zero operand)
+                const int nks = left >= kQT ? kQT / 16 : (int)((left + 15) / 16);
+                for (int ks = 0; ks < nks; ++ks) {
                     if (jj == 0)
                         mma_bf16_ta(tmem + Q::T_F, tmem + Q::T_S + ks * 8, desc_add(dBmn, ks * 2048), id, ks > 0);
                     else
                         mma_bf16_ta(tmem + Q::T_F, tmem + Q::T_S + ks * 8, desc_add(dBmn, ks * 2048), id, true);
                 }
-#pragma unroll
-                for (int ks = 0; ks < kQT / 16; ++ks)
+                for (int ks = 0; ks < nks; ++ks)
                     mma_bf16_ta(tmem + Q::T_F, tmem + Q::T_S + 64 + ks * 8, desc_add(dBmn, ks * 2048), id, true);
                 mma_commit(&mma_bar);
             }
