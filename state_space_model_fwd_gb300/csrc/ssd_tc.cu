@@ -61,7 +61,11 @@ struct TcParams {
     const float *A, *D, *init;
     void *y;
     float *fin;
-    float *seg_state;   // [b, nseg, H, P, N]: segment-local states (each segment from a zero state)
+    // segment-local states (each segment from a zero state): [b, nseg, H, P, N],
+    // or with seg_cl [b, nseg, H, N/4, P, 4] (four columns of one row per 16
+    // bytes, rows innermost: a warp's 32 rows read or write 512 contiguous bytes)
+    float *seg_state;
+    int seg_cl;
     float *seg_tot;     // [b, H, nseg]  total dt*A of each segment (may be null)
     const float *cum_in;    // [b, H, nc_cum, cum_q] the caller's in-chunk cumulative decay (null: computed)
     int cum_q, nc_cum;      // the caller's chunk length (64 or 128: one or two tiles) and chunk count
@@ -119,6 +123,7 @@ struct Cfg {
     // y staging: one [Q/4 steps][32 p] tile per compute warp (fp32, the
     // larger case), the source of the warp's TMA store of its outputs
     static constexpr int YSTAGE = 16 * (Q / 4) * 32 * 4;
+    static_assert(YSTAGE >= 16 * 2048, "the scan prologue's per-warp 2 KB transpose area");
     static constexpr int scan_smem(int st) { return st * SCAN_STAGE + VEC_RING + DT_RING + YSTAGE + 1024; }
     static constexpr int SCAN_ST = scan_smem(4) <= kSmemLimit ? 4 : (scan_smem(3) <= kSmemLimit ? 3 : 2);
     static constexpr int SMEM_SCAN = scan_smem(SCAN_ST);
@@ -789,10 +794,15 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         DtFeed<C> feed{dt_ring + hv * C::DT_RING, dt_bar + 2 * hv, &mdt, b, h0, nch, 0};
         feed.start(prm, chunk_of);
         const float a = (h0 + hv < H && prm.A) ? prm.A[h0 + hv] : 0.f;
+        // dt of the next chunk is read while this one is processed: the
+        // shared-memory reads wait behind the operand builders' traffic
+        ChunkDt<C> dt_next;
+        bool have = nch > 0 && feed.take(prm, 0, chunk_of, &abort_sh, dt_next);
         for (int it = 0; it < nch; ++it) {
+            if (!have) break;
             const int v = it % NV, c = chunk_of(it);
-            ChunkDt<C> dt;
-            if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
+            const ChunkDt<C> dt = dt_next;
+            if (it + 1 < nch) have = feed.take(prm, it + 1, chunk_of, &abort_sh, dt_next);
             float cum[QPL], T;
             head_cums<C>(prm, b, h0, hv, c, dt, a, cum, T);
             float w[QPL];
@@ -883,7 +893,11 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         const long long hrow = h0 + rh;
         if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 1, gtid, NAB)) {
             tc_fence_after();
-            float *dst = prm.seg_state + ((((long long)b * prm.nseg + seg) * H + hrow) * C::P + rp) * C::N;
+            const long long blk0 = (((long long)b * prm.nseg + seg) * H + hrow) * C::P * C::N;
+            // element n of this row: at 4 (n/4) P + n%4 in the column-block
+            // layout, at n in the row layout
+            float *dst = prm.seg_state + blk0 + (prm.seg_cl ? rp * 4 : rp * C::N);
+            const int cstep = prm.seg_cl ? C::P : 1;
 #pragma unroll 1
             for (int n0 = part * (C::N / 4); n0 < (part + 1) * (C::N / 4); n0 += 16) {
                 float v[16];
@@ -892,7 +906,8 @@ __global__ void __launch_bounds__(kSegThreads, 1)
                 if (hrow < H) {
 #pragma unroll
                     for (int j = 0; j < 16; j += 4)
-                        __stcg(reinterpret_cast<float4 *>(dst + n0 + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+                        __stcg(reinterpret_cast<float4 *>(dst + (long long)(n0 + j) * cstep),
+                               make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
                 }
             }
         }
@@ -1354,52 +1369,62 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
         //   S_in = e^{T_0 + .. + T_{k-1}} init + sum_j e^{T_{j+1} + .. + T_{k-1}} L_j
         {
             if (prm.dep_seg && seg > 0) griddep_wait();
+            // (the 32 rows of a warp are 32 consecutive p of one head)
             const bool live = hrow < H;
-            const float *src = nullptr;  // a ready state (given, or init for segment 0)
-            const float *ini = nullptr;  // init, weighted, in the pass
+            const float *dense = nullptr;  // a state in the row layout [.., P, N]: given, init, or init weighted
             const long long rowoff = (((long long)b * H + (live ? hrow : 0)) * C::P + rp) * C::N;
             if (prm.entering)
-                src = prm.entering + ((((long long)b * prm.nseg + seg) * H + (live ? hrow : 0)) * C::P + rp) * C::N;
-            else if (seg == 0)
-                src = prm.init ? prm.init + rowoff : nullptr;
+                dense = prm.entering + ((((long long)b * prm.nseg + seg) * H + (live ? hrow : 0)) * C::P + rp) * C::N;
             else if (prm.init)
-                ini = prm.init + rowoff;
+                dense = prm.init + rowoff;
+            // after segment 0 the local states are in the column-block layout
             const bool pass = !prm.entering && seg > 0;
             const long long sstride = H * C::P * C::N;
             const float *loc =
-                pass ? prm.seg_state + ((((long long)b * prm.nseg) * H + (live ? hrow : 0)) * C::P + rp) * C::N : nullptr;
+                pass ? prm.seg_state + (((long long)b * prm.nseg) * H + (live ? hrow : 0)) * C::P * C::N + rp * 4 : nullptr;
             const float *tot = pass ? prm.seg_tot + ((long long)b * H + (live ? hrow : 0)) * prm.nseg : nullptr;
             float ttot = 0.f;  // T_0 + .. + T_{k-1}
             if (pass && live)
                 for (int j = 0; j < seg; ++j) ttot += __ldcg(tot + j);
+            const float wd = pass ? __expf(ttot) : 1.f;  // weight of the dense state
+            // a row-layout state goes through this warp's 2 KB of the y
+            // staging area (no y tile is staged before every compute warp
+            // has passed here): 16-byte pieces read eight rows per load,
+            // stored with the piece index XOR-ed by bits 1-2 of the row,
+            // read back one row per lane, both without bank conflicts
+            float *scr = reinterpret_cast<float *>(ystage) + (warp - 8) * 512;
+            const float *dense0 = dense ? dense - (long long)lane * C::N : nullptr;  // row of lane 0
             constexpr int NCOL = C::N / 4;  // this warp's columns
 #pragma unroll 1
             for (int n0 = part * NCOL; n0 < (part + 1) * NCOL; n0 += 16) {
                 float v[16];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                if (live && src) {
+                if (live && dense0) {
+                    const int pc = lane & 3;
+                    float4 t4[4];
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const float4 a4 = __ldg(reinterpret_cast<const float4 *>(src + n0 + j));
-                        v[j] = a4.x;
-                        v[j + 1] = a4.y;
-                        v[j + 2] = a4.z;
-                        v[j + 3] = a4.w;
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = (lane >> 2) + 8 * i;
+                        t4[i] = __ldg(reinterpret_cast<const float4 *>(dense0 + (long long)r * C::N + n0 + 4 * pc));
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = (lane >> 2) + 8 * i;
+                        *reinterpret_cast<float4 *>(scr + r * 16 + 4 * (pc ^ ((r >> 1) & 3))) = t4[i];
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(scr + lane * 16 + 4 * (j ^ ((lane >> 1) & 3)));
+                        v[4 * j] = wd * a4.x;
+                        v[4 * j + 1] = wd * a4.y;
+                        v[4 * j + 2] = wd * a4.z;
+                        v[4 * j + 3] = wd * a4.w;
+                    }
+                    __syncwarp();
                 }
                 if (live && pass) {
-                    if (ini) {
-                        const float wi = __expf(ttot);
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 a4 = __ldg(reinterpret_cast<const float4 *>(ini + n0 + j));
-                            v[j] = wi * a4.x;
-                            v[j + 1] = wi * a4.y;
-                            v[j + 2] = wi * a4.z;
-                            v[j + 3] = wi * a4.w;
-                        }
-                    }
                     // two segments' loads in flight before either is used
                     float pre = 0.f;  // T_0 + .. + T_j
                     for (int k = 0; k < seg; k += 2) {
@@ -1407,8 +1432,9 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                         float4 l0[4], l1[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            l0[j] = __ldg(reinterpret_cast<const float4 *>(loc + k * sstride + n0 + 4 * j));
-                            l1[j] = two ? __ldg(reinterpret_cast<const float4 *>(loc + (k + 1) * sstride + n0 + 4 * j))
+                            const long long o = (long long)(n0 / 4 + j) * (C::P * 4);
+                            l0[j] = __ldcg(reinterpret_cast<const float4 *>(loc + k * sstride + o));
+                            l1[j] = two ? __ldcg(reinterpret_cast<const float4 *>(loc + (k + 1) * sstride + o))
                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                         }
                         const float t0 = __ldcg(tot + k), t1 = two ? __ldcg(tot + k + 1) : 0.f;
@@ -1801,6 +1827,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     const size_t seg_off = hdr + pack_bytes<C>(d);
     if (p.nseg > 1) {
         prm.seg_state = reinterpret_cast<float *>(w + seg_off);
+        prm.seg_cl = 1;
         prm.seg_tot = reinterpret_cast<float *>(w + seg_off + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
     }
     prm.nhb = p.nhb;
