@@ -409,8 +409,10 @@ def main():
     # three streams, so step i+1's copies in and step i-1's copies out overlap
     # step i's kernels (the copy engines and the SMs work side by side).
     h = inp.to_torch("cpu", pin_memory=True)
-    h2d = sum(v.numel() * v.element_size() for v in h.values() if v is not None)
-    d2h = y.numel() * y.element_size() + fin.numel() * fin.element_size()
+    # bytes crossing the link per step: the packed buffers (each tensor at a
+    # 256-byte aligned offset, so a few hundred bytes of padding at most)
+    h2d = packed({k: v for k, v in h.items() if v is not None})[0].numel()
+    d2h = packed({"y": y, "fin": fin})[0].numel()
     e2e_serial_ms = max_over_ranks(e2e_serial(ssd, dev, h, y, fin, ws, cfg, args.steps), world, dev)
     e2e_ms = max_over_ranks(e2e_pipelined(ssd, dev, h, y, fin, ws, cfg, args.steps), world, dev)
     barrier()
@@ -463,21 +465,47 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def e2e_serial(ssd, dev, h, y, fin, ws, cfg, steps):
-    """ms per step of copy in -> ssd_fwd -> copy out on one stream."""
+def packed(tensors, dev=None, pin=False):
+    """One contiguous byte buffer holding `tensors` at 256-byte aligned
+    offsets, and views of it with the tensors' dtypes and shapes: a step's
+    inputs (or outputs) then cross the host link as one copy."""
     import torch
-    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
-    d = {k: torch.empty_like(v, device=dev) for k, v in h.items() if v is not None}
+    offs, total = {}, 0
+    for k, v in tensors.items():
+        offs[k] = total
+        total += -(-(v.numel() * v.element_size()) // 256) * 256
+    buf = torch.empty(total, dtype=torch.uint8, device=dev, pin_memory=pin)
+    views = {k: buf[o:o + v.numel() * v.element_size()].view(v.dtype).view(v.shape) for (k, v), o in
+             zip(tensors.items(), offs.values())}
+    return buf, views
+
+
+def e2e_buffers(dev, h, y, fin, nsets):
+    """Pinned host copies of the inputs and outputs, and `nsets` device sets,
+    each packed into one buffer per direction."""
+    src = {k: v for k, v in h.items() if v is not None}
+    h_in, hv = packed(src, pin=True)
+    for k, v in src.items():
+        hv[k].copy_(v)
+    d_in = [packed(src, dev=dev) for _ in range(nsets)]
+    d_out = [packed({"y": y, "fin": fin}, dev=dev) for _ in range(nsets)]
+    h_out = [packed({"y": y, "fin": fin}, pin=True)[0] for _ in range(nsets)]
+    return h_in, d_in, d_out, h_out
+
+
+def e2e_serial(ssd, dev, h, y, fin, ws, cfg, steps):
+    """ms per step of copy in -> ssd_fwd -> copy out on one stream (one
+    packed copy each way)."""
+    import torch
+    h_in, d_in, d_out, h_out = e2e_buffers(dev, h, y, fin, 1)
+    (din, d), (dout, o), hout = d_in[0], d_out[0], h_out[0]
     stream = torch.cuda.current_stream(dev)
 
     def one():
-        for k, v in d.items():
-            v.copy_(h[k], non_blocking=True)
+        din.copy_(h_in, non_blocking=True)
         ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d.get("init_state"), cfg.chunk_size,
-                    y=y, final_state=fin, workspace=ws)
-        y_h.copy_(y, non_blocking=True)
-        fin_h.copy_(fin, non_blocking=True)
+                    y=o["y"], final_state=o["fin"], workspace=ws)
+        hout.copy_(dout, non_blocking=True)
 
     for _ in range(3):
         one()
@@ -495,14 +523,11 @@ def e2e_pipelined(ssd, dev, h, y, fin, ws, cfg, steps):
     """ms per step with two buffer sets: inputs of step i copied in on one
     stream while step i-1 computes on a second and step i-2's outputs go out
     on a third.  Every step still copies all its inputs in and its outputs
-    out; the timed region runs from the first copy in to the last copy out."""
+    out (one packed copy each way); the timed region runs from the first copy
+    in to the last copy out."""
     import torch
     s_in, s_c, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    ins = [{k: torch.empty_like(v, device=dev) for k, v in h.items() if v is not None} for _ in range(2)]
-    ys = [y, torch.empty_like(y)]
-    fins = [fin, torch.empty_like(fin)]
-    y_h = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
-    fin_h = [torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True) for _ in range(2)]
+    h_in, d_in, d_out, h_out = e2e_buffers(dev, h, y, fin, 2)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_c = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
@@ -510,24 +535,22 @@ def e2e_pipelined(ssd, dev, h, y, fin, ws, cfg, steps):
     def run(n):
         for i in range(n):
             j = i % 2
+            (din, d), (dout, o) = d_in[j], d_out[j]
             if i >= 2:
                 s_in.wait_event(ev_c[j])    # step i-2 no longer reads input set j
             with torch.cuda.stream(s_in):
-                for k, v in ins[j].items():
-                    v.copy_(h[k], non_blocking=True)
+                din.copy_(h_in, non_blocking=True)
                 ev_in[j].record(s_in)
             s_c.wait_event(ev_in[j])
             if i >= 2:
                 s_c.wait_event(ev_out[j])   # step i-2's outputs have been read back
             with torch.cuda.stream(s_c):
-                d = ins[j]
                 ssd.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d.get("init_state"), cfg.chunk_size,
-                            y=ys[j], final_state=fins[j], workspace=ws)
+                            y=o["y"], final_state=o["fin"], workspace=ws)
                 ev_c[j].record(s_c)
             s_out.wait_event(ev_c[j])
             with torch.cuda.stream(s_out):
-                y_h[j].copy_(ys[j], non_blocking=True)
-                fin_h[j].copy_(fins[j], non_blocking=True)
+                h_out[j].copy_(dout, non_blocking=True)
                 ev_out[j].record(s_out)
 
     run(3)
