@@ -572,11 +572,19 @@ def tc_plan(cfg, target_ctas=152):
     hb = 128 // cfg.headdim
     nhb = -(-cfg.nheads // hb)
     units = cfg.batch * nhb
-    nc = cfg.seqlen // 64
+    nc = -(-cfg.seqlen // 64)
     nseg = max(1, min(nc, target_ctas // units))
     cps = -(-nc // nseg)
     nseg = -(-nc // cps)
     return nseg, cps, nc
+
+
+def tc_nsub(cfg, target_ctas=152):
+    """Sub-segments of the segment-state pass (mirrors the library): halves
+    with four segments or more, where S and two A buffers fit 256 TMEM
+    columns (N + 128 <= 256) and a segment has two tiles or more."""
+    nseg, cps, _ = tc_plan(cfg, target_ctas)
+    return 2 if nseg >= 4 and cfg.dstate + 128 <= 256 and cps >= 2 else 1
 
 
 def KERNEL_BYTES(cfg, name):
@@ -593,10 +601,11 @@ def KERNEL_BYTES(cfg, name):
     init = b * H * P * N * 4 if cfg.has_init else 0
     fin = b * H * P * N * 4
     nseg, cps, nt = tc_plan(cfg)
+    nsub = tc_nsub(cfg)
     one_seg = b * H * P * N * 4  # one segment state of every (batch, head)
-    seg_states = (nseg - 1) * one_seg
-    # segment k's entering state combines the k earlier segments' local states
-    seg_reads = one_seg * nseg * (nseg - 1) // 2
+    seg_states = (nseg - 1) * nsub * one_seg
+    # segment k's entering state combines the k nsub earlier local states
+    seg_reads = one_seg * nsub * nseg * (nseg - 1) // 2
     covered = min(nt, (nseg - 1) * cps) / nt  # share of the sequence the segment-state kernel reads
     # chunk packs: masked C B^T (bf16, 64-step tiles) with the tile's B and C
     pack = b * nt * G * 64 * 64 * 2 + 2 * bc

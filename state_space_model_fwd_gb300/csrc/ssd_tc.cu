@@ -78,6 +78,10 @@ struct TcParams {
     int flag_first;
     long long b, L, H, G;
     int hpg, nc, nseg, cps;  // cps: chunks per segment
+    // the segment-state pass runs on nsub sub-segments of each segment (of
+    // ceil(cps / nsub) chunks, the last one shorter); seg_state and seg_tot
+    // hold nslot = nseg * nsub slots
+    int nsub, nslot;
     int nhb;
     int dt_tma;  // dt has a TMA map (H % 8 == 0): the vector warps take it from a TMA ring
     // [b, nc, G] set to 1 by the C B^T kernel once a matrix is in memory;
@@ -701,21 +705,36 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
 //   warps 4-19  : the A operand (weights x x, bf16 hi + lo) into TMEM, three
 //                 buffers; then the state to HBM
 // ===========================================================================
-constexpr int kSegThreads = 640;
-constexpr int kSegABWarps = (kSegThreads - 128) / 32;  // warps 4..19
+// NBG groups of four operand-builder warps (each group Q / NBG of the steps):
+// four groups with the deep ring (one CTA per SM), or two groups with two
+// stages and two A buffers in 256 TMEM columns, so that two CTAs share an SM
+template <class C, int NBG>
+struct SegT {
+    static constexpr int THREADS = 128 + 128 * NBG;
+    static constexpr int ABW = 4 * NBG;  // operand-builder warps 4 .. 4 + ABW - 1
+    static constexpr int NS = C::Q / NBG;
+    static constexpr int ST = NBG == 4 ? C::SEG_ST : 2;
+    static constexpr int NA = NBG == 4 ? C::SEG_NA : 2;
+    static constexpr uint32_t TMEM = NBG == 4 ? C::SEG_TMEM : 256;
+    static constexpr int SMEM = C::seg_smem(ST);
+    static constexpr int MIN_CTAS = NBG == 4 ? 1 : 2;
+    static_assert(NBG == 4 || C::N + 2 * C::Q <= 256, "two A buffers and S in 256 columns");
+};
 
-template <class C>
-__global__ void __launch_bounds__(kSegThreads, 1)
+template <class C, int NBG>
+__global__ void __launch_bounds__(SegT<C, NBG>::THREADS, SegT<C, NBG>::MIN_CTAS)
     seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
                      const __grid_constant__ CUtensorMap mdt, TcParams prm) {
-    constexpr int ST = C::SEG_ST, NV = C::NV;
+    using T = SegT<C, NBG>;
+    constexpr int ST = T::ST, NV = C::NV;
+    constexpr int kSegThreads = T::THREADS, kSegABWarps = T::ABW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float *vec_base = reinterpret_cast<float *>(smem + ST * C::SEG_STAGE);
     uint8_t *dt_ring = smem + ST * C::SEG_STAGE + C::VEC_RING;
     __shared__ uint64_t dt_bar[2 * C::HB];  // a dt ring per vector warp
     TRACE_DECL;
-    constexpr int NA = C::SEG_NA;
+    constexpr int NA = T::NA;
     __shared__ uint64_t full_bar[4], empty_bar[4], vfull_bar[NV], vempty_bar[NV], afull_bar[NA], afree_bar[NA];
     __shared__ uint64_t done_bar, drain_bar;
     __shared__ uint32_t tmem_base_sh;
@@ -726,8 +745,11 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     const int seg = blockIdx.z, hblk = blockIdx.x, b = blockIdx.y;
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
-    const int c0 = seg * prm.cps;
-    const int nch = min(prm.nc, c0 + prm.cps) - c0;
+    // sub-segment `seg` of segment seg / nsub
+    const int csub = (prm.cps + prm.nsub - 1) / prm.nsub;
+    const int sbeg = (seg / prm.nsub) * prm.cps;
+    const int c0 = sbeg + (seg % prm.nsub) * csub;
+    const int nch = min(min(prm.nc, sbeg + prm.cps), c0 + csub) - c0;
     const long long H = prm.H;
     // the segment's chunks are taken last to first, so the decay of the
     // chunks after each one (its weights' offset) accumulates as they come
@@ -741,7 +763,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     auto vec = [&](int v) { return vec_base + v * C::VEC_FLOATS; };
 
     if (warp == 1) {
-        tmem_alloc(&tmem_base_sh, C::SEG_TMEM);
+        tmem_alloc(&tmem_base_sh, T::TMEM);
         tmem_relinquish();
     }
     if (tid == 0) {
@@ -824,7 +846,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         }
         feed.drain();
         // total dt*A of the segment, for the pass across segments
-        if (lane == 0 && h0 + hv < H && prm.seg_tot) prm.seg_tot[((long long)b * H + h0 + hv) * prm.nseg + seg] = after;
+        if (lane == 0 && h0 + hv < H && prm.seg_tot) prm.seg_tot[((long long)b * H + h0 + hv) * prm.nslot + seg] = after;
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         // (the whole warp runs the loop, so its descriptors stay
@@ -859,7 +881,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         if (elect_one()) mma_commit(&done_bar);  // completes once every MMA above has
         __syncwarp();
     } else if (warp >= 4) {
-        // ---------------- A operand builders: thread = row (head, p), a quarter of the steps ----------------
+        // ---------------- A operand builders: thread = row (head, p), 1 / NBG of the steps ----------------
         constexpr int NAB = kSegThreads - 128;
         const int gtid = tid - 128;
         const int q4 = warp & 3, part = (warp - 4) >> 2;
@@ -876,8 +898,8 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             if (it >= NA && !warp_wait(&afree_bar[a], free_parity(it, NA), &abort_sh)) break;
             if (gtid == 0) TRACE(17, it);
             tc_fence_after();
-            build_a<C, C::Q / 4>(stage_x(s), blk, pcol, vec(v) + C::V_AL + rh * C::Q + part * (C::Q / 4), part,
-                                 tmem + lane_off + COL_A + a * C::Q);
+            build_a<C, T::NS>(stage_x(s), blk, pcol, vec(v) + C::V_AL + rh * C::Q + part * T::NS, part,
+                              tmem + lane_off + COL_A + a * C::Q);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -889,17 +911,17 @@ __global__ void __launch_bounds__(kSegThreads, 1)
             }
         }
         // segment state: TMEM lane r = row (head, p); each group of four
-        // warps a quarter of the columns
+        // warps 1 / NBG of the columns
         const long long hrow = h0 + rh;
         if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 1, gtid, NAB)) {
             tc_fence_after();
-            const long long blk0 = (((long long)b * prm.nseg + seg) * H + hrow) * C::P * C::N;
+            const long long blk0 = (((long long)b * prm.nslot + seg) * H + hrow) * C::P * C::N;
             // element n of this row: at 4 (n/4) P + n%4 in the column-block
             // layout, at n in the row layout
             float *dst = prm.seg_state + blk0 + (prm.seg_cl ? rp * 4 : rp * C::N);
             const int cstep = prm.seg_cl ? C::P : 1;
 #pragma unroll 1
-            for (int n0 = part * (C::N / 4); n0 < (part + 1) * (C::N / 4); n0 += 16) {
+            for (int n0 = part * (C::N / NBG); n0 < (part + 1) * (C::N / NBG); n0 += 16) {
                 float v[16];
                 tmem_ld16(tmem + lane_off + n0, v);
                 tmem_ld_wait();
@@ -924,7 +946,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
     tc_fence_before();
     __syncthreads();
     TRACE_FLUSH();
-    if (warp == 1) tmem_dealloc(tmem, C::SEG_TMEM);
+    if (warp == 1) tmem_dealloc(tmem, T::TMEM);
     if (abort_sh && tid == 0) flag_timeout(prm.status);
     // complete only after the C B^T grid before this one: a grid that waits
     // for this one then sees those matrices too
@@ -1381,11 +1403,12 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
             const bool pass = !prm.entering && seg > 0;
             const long long sstride = H * C::P * C::N;
             const float *loc =
-                pass ? prm.seg_state + (((long long)b * prm.nseg) * H + (live ? hrow : 0)) * C::P * C::N + rp * 4 : nullptr;
-            const float *tot = pass ? prm.seg_tot + ((long long)b * H + (live ? hrow : 0)) * prm.nseg : nullptr;
+                pass ? prm.seg_state + (((long long)b * prm.nslot) * H + (live ? hrow : 0)) * C::P * C::N + rp * 4 : nullptr;
+            const float *tot = pass ? prm.seg_tot + ((long long)b * H + (live ? hrow : 0)) * prm.nslot : nullptr;
+            const int nprev = seg * prm.nsub;  // local states before this segment (its earlier sub-segments)
             float ttot = 0.f;  // T_0 + .. + T_{k-1}
             if (pass && live)
-                for (int j = 0; j < seg; ++j) ttot += __ldcg(tot + j);
+                for (int j = 0; j < nprev; ++j) ttot += __ldcg(tot + j);
             const float wd = pass ? __expf(ttot) : 1.f;  // weight of the dense state
             // a row-layout state goes through this warp's 2 KB of the y
             // staging area (no y tile is staged before every compute warp
@@ -1427,8 +1450,8 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                 if (live && pass) {
                     // two segments' loads in flight before either is used
                     float pre = 0.f;  // T_0 + .. + T_j
-                    for (int k = 0; k < seg; k += 2) {
-                        const bool two = k + 1 < seg;
+                    for (int k = 0; k < nprev; k += 2) {
+                        const bool two = k + 1 < nprev;
                         float4 l0[4], l1[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -1636,6 +1659,7 @@ bool make_dt_map(CUtensorMap *m, const void *base, uint64_t H, uint64_t L, uint6
 
 struct Plan {
     int nseg, cps, nhb;
+    int nsub;  // sub-segments of the segment-state pass (2: its two-CTAs-per-SM form)
 };
 
 // SM count of the current device (one chunk-scan CTA fits per SM); the
@@ -1661,6 +1685,13 @@ Plan plan_for(const Dims &d) {
     if (nseg > d.nc) nseg = (int)d.nc;
     p.cps = (int)((d.nc + nseg - 1) / nseg);
     p.nseg = (int)((d.nc + p.cps - 1) / p.cps);
+    // With four segments or more the segment-state pass, which the scans of
+    // the later segments wait for, is the longer part of the step: its local
+    // states are then formed on half segments by the two-group kernel, two
+    // CTAs per SM (where S and two A buffers fit 256 TMEM columns and a
+    // segment has two chunks or more).  With fewer segments the halves would
+    // hold the SMs the first segment's scan starts on.
+    p.nsub = (p.nseg >= 4 && C::N + 2 * C::Q <= 256 && p.cps >= 2) ? 2 : 1;
     return p;
 }
 
@@ -1691,7 +1722,8 @@ size_t workspace_for(const Dims &d) {
     const Plan p = plan_for<C>(d);
     size_t bytes = header_bytes<C>(d) + pack_bytes<C>(d);
     if (p.nseg > 1)
-        bytes += align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N) + align256(sizeof(float) * d.b * p.nseg * d.H);
+        bytes += align256(sizeof(float) * d.b * p.nseg * p.nsub * d.H * C::P * C::N) +
+                 align256(sizeof(float) * d.b * p.nseg * p.nsub * d.H);
 #ifdef SSD_TRACE
     bytes += kTraceBytes;
 #endif
@@ -1775,18 +1807,18 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     return e;
 }
 
-template <class C>
+template <class C, int NBG = 4>
 cudaError_t launch_seg_state(const Dims &d, TcParams prm, const void *x, const void *B, dim3 grid,
                              const char *name, bool pdl, cudaStream_t s) {
     CUtensorMap mx, mb, mdt = {};
     if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q) || !make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
-    const int smem = C::SMEM_SEG;
+    const int smem = SegT<C, NBG>::SMEM;
     static int attr = 0;
-    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(seg_state_kernel<C>), smem, attr);
+    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(seg_state_kernel<C, NBG>), smem, attr);
     if (e != cudaSuccess) return e;
-    e = launch_k(seg_state_kernel<C>, grid, kSegThreads, smem, s, pdl, mx, mb, mdt, prm);
+    e = launch_k(seg_state_kernel<C, NBG>, grid, SegT<C, NBG>::THREADS, smem, s, pdl, mx, mb, mdt, prm);
     timing_mark(s, name);
     return e;
 }
@@ -1828,11 +1860,14 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     if (p.nseg > 1) {
         prm.seg_state = reinterpret_cast<float *>(w + seg_off);
         prm.seg_cl = 1;
-        prm.seg_tot = reinterpret_cast<float *>(w + seg_off + align256(sizeof(float) * d.b * p.nseg * d.H * C::P * C::N));
+        prm.seg_tot = reinterpret_cast<float *>(
+            w + seg_off + align256(sizeof(float) * d.b * p.nseg * p.nsub * d.H * C::P * C::N));
     }
     prm.nhb = p.nhb;
     prm.nseg = p.nseg;
     prm.cps = p.cps;
+    prm.nsub = p.nsub;
+    prm.nslot = p.nseg * p.nsub;
 #ifdef SSD_TRACE
     prm.trace = reinterpret_cast<long long *>(w + workspace_for<C>(d) - kTraceBytes);
 #endif
@@ -1842,7 +1877,12 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s);
     if (e != cudaSuccess) return e;
     if (p.nseg > 1) {
-        e = launch_seg_state<C>(d, prm, x, B, dim3(p.nhb, (unsigned)d.b, p.nseg - 1), "seg_state_tc", true, s);
+        const dim3 grid(p.nhb, (unsigned)d.b, (unsigned)((p.nseg - 1) * p.nsub));
+        if constexpr (C::N + 2 * C::Q <= 256)
+            e = p.nsub == 2 ? launch_seg_state<C, 2>(d, prm, x, B, grid, "seg_state_tc", true, s)
+                            : launch_seg_state<C>(d, prm, x, B, grid, "seg_state_tc", true, s);
+        else
+            e = launch_seg_state<C>(d, prm, x, B, grid, "seg_state_tc", true, s);
         if (e != cudaSuccess) return e;
         prm.dep_seg = 1;
     }
@@ -1934,6 +1974,8 @@ cudaError_t run_chunk_state(const Dims &dq, const Dims &d, const void *x, const 
     prm.seg_state = states;  // [b, nc, H, P, N]: one segment per chunk
     prm.nseg = (int)dq.nc;
     prm.cps = (int)(dq.Q / C::Q);
+    prm.nsub = 1;
+    prm.nslot = prm.nseg;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
     timing_begin(s);
     return launch_seg_state<C>(d, prm, x, B, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)dq.nc),
@@ -1964,6 +2006,8 @@ cudaError_t run_chunk_scan(const Dims &dq, const Dims &d, ssd_dtype_t ydtype, co
     prm.y = y;
     prm.nseg = (int)dq.nc;
     prm.cps = (int)(dq.Q / C::Q);
+    prm.nsub = 1;
+    prm.nslot = prm.nseg;
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
     char *w = static_cast<char *>(ws);
     prm.cb_ready = reinterpret_cast<unsigned *>(w);

@@ -163,9 +163,10 @@ def test_workspace_layout_of_the_tensor_core_path(lib, name):
                         cfg.chunk_size, 1, 1)
     b, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
     nseg, _, nt = bench.tc_plan(cfg, 152)
+    nsub = bench.tc_nsub(cfg, 152)
     want = _a256(4 * b * nt * G) + _a256(b * nt * G * (64 * 64 * 2 + 2 * 64 * N * 2))
     if nseg > 1:
-        want += _a256(4 * b * nseg * H * P * N) + _a256(4 * b * nseg * H)
+        want += _a256(4 * b * nseg * nsub * H * P * N) + _a256(4 * b * nseg * nsub * H)
     assert lib.ssd_fwd_workspace_size(ctypes.byref(s)) == want
 
 
