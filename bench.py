@@ -607,21 +607,21 @@ def KERNEL_BYTES(cfg, name):
     # segment k's entering state combines the k nsub earlier local states
     seg_reads = one_seg * nsub * nseg * (nseg - 1) // 2
     covered = min(nt, (nseg - 1) * cps) / nt  # share of the sequence the segment-state kernel reads
-    # chunk packs: masked C B^T (bf16, 64-step tiles) with the tile's B and C
-    pack = b * nt * G * 64 * 64 * 2 + 2 * bc
+    # chunk packs: the masked C B^T of each 64-step tile (bf16)
+    pack = b * nt * G * 64 * 64 * 2
     return {
         "chunk_cumsum": dt + cum,
         "chunk_state_simt": x + dt + bc + cum + st,
         "state_passing": st + cum + init + st + fin,
         "chunk_scan_simt": x + dt + 2 * bc + cum + st + y,
-        # fused tensor-core path: chunk packs (read B, C; write the packs),
-        # segment-local states (written once), chunk scan (reads every pack
-        # once per (batch, chunk, group) as its B, C and C B^T input, and the
-        # earlier segments' local states and the initial state for the state
-        # entering each segment)
+        # fused tensor-core path: chunk packs (read B, C; write the masked
+        # C B^T), segment-local states (written once), chunk scan (reads B, C
+        # and every pack once per (batch, chunk, group), and the earlier
+        # segments' local states and the initial state for the state entering
+        # each segment)
         "cb_mask_tc": 2 * bc + pack,
         "seg_state_tc": covered * (x + dt + bc) + seg_states,
-        "chunk_scan_tc": x + dt + pack + seg_reads + nseg * init + y + fin,
+        "chunk_scan_tc": x + dt + 2 * bc + pack + seg_reads + nseg * init + y + fin,
     }.get(name, compulsory_bytes(cfg))
 
 

@@ -88,7 +88,7 @@ struct TcParams {
     // the chunk scan's TMA producer polls the flag of a chunk before loading
     // its matrix (the C B^T grid is wholly resident or done by then)
     unsigned *cb_ready;
-    const uint8_t *pack;  // [b, nc, G] chunk packs (PACK_BYTES each)
+    const uint8_t *pack;  // [b, nc, G] masked C B^T tiles (CBM_BYTES each)
     // launched with a programmatic dependency on the segment-state kernel:
     // the state warps of segments > 0 wait for it before reading the states
     // entering them
@@ -104,9 +104,9 @@ struct Cfg {
     static constexpr int X_BYTES = M * Q * 2;    // [Q steps][M/64 = 2 blocks (head, 64 p)][64], one TMA box
     static constexpr int BC_BYTES = N * Q * 2;   // [N/64 blocks][Q rows][64]
     static constexpr int CBM_BYTES = Q * Q * 2;  // [Q rows t][Q s]
-    // chunk pack, written by the C B^T kernel and read with one bulk copy:
-    // [CB (K-major, swizzled) | B tile | C tile], each in the shared-memory
-    // image the MMAs read
+    // chunk pack in a scan stage: [CB (K-major, swizzled) | B tile | C tile],
+    // each in the shared-memory image the MMAs read; the C B^T kernel stores
+    // CB alone (one bulk copy of CBM_BYTES), B and C come from the inputs
     static constexpr int PACK_BYTES = CBM_BYTES + 2 * BC_BYTES;
     // vector set of one chunk (floats): per head [Q] arrays dt, cum, a-factor,
     // epilogue factor; then per head the state rescale factor (applied twice),
@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && ok_sh) {
-        bulk_store(pack + plane * C::PACK_BYTES, smem, C::PACK_BYTES);
+        bulk_store(pack + plane * C::CBM_BYTES, smem, C::CBM_BYTES);
         bulk_commit_group();
         bulk_wait_all();
         __threadfence();
@@ -1012,7 +1012,8 @@ constexpr int kComputeWarps = 16;  // warps 8..23
 template <class C, typename YT>
 __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mdt,
-                      const __grid_constant__ CUtensorMap my, TcParams prm) {
+                      const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mb,
+                      const __grid_constant__ CUtensorMap mc, TcParams prm) {
     constexpr int ST = C::SCAN_ST, NV = C::NV, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1074,6 +1075,8 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
         fence_mbar_init();
         abort_sh = 0;
         prefetch_tmap(&mx);
+        prefetch_tmap(&mb);
+        prefetch_tmap(&mc);
         if (prm.dt_tma) prefetch_tmap(&mdt);
     }
     if (tid < 32) ones_sh[tid] = 1.f;
@@ -1100,15 +1103,19 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                     const int s = it % ST;
                     if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
                     const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
-                    // two operations per chunk: the x box, then the chunk pack
-                    // once the C B^T kernel has published it
+                    // the x box, then the pack (C B^T, B, C)
                     if (prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                     mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES);
                     tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, (c0 + it) * C::Q, b);
                     ++nload[s];
+                    // once the C B^T kernel has published the tile's masked C B^T:
+                    // it, and the tile's B and C from the inputs (no copy of a
+                    // stage is issued unless all three are)
                     if (!prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                     mbar_arrive_expect_tx(&pfull_bar[s], C::PACK_BYTES);
-                    bulk_load(stage_cb(s), prm.pack + plane * C::PACK_BYTES, C::PACK_BYTES, &pfull_bar[s]);
+                    bulk_load(stage_cb(s), prm.pack + plane * C::CBM_BYTES, C::CBM_BYTES, &pfull_bar[s]);
+                    tma_load_5d(stage_b(s), &mb, &pfull_bar[s], 0, (c0 + it) * C::Q, 0, g, b);
+                    tma_load_5d(stage_c(s), &mc, &pfull_bar[s], 0, (c0 + it) * C::Q, 0, g, b);
                     ++npack[s];
                     TRACE(0, it);
                 }
@@ -1612,6 +1619,21 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-D map of B [b][L][G][N] viewed as (64, L, N/64, G, b), box (64, Q, N/64,
+// 1, 1): one box per chunk lands as [N/64 blocks][Q steps][64] in shared memory
+// (128-byte swizzle), the layout of N/64 separate (64, Q) boxes.
+bool make_bt_map(CUtensorMap *m, const void *base, uint64_t N, uint64_t G, uint64_t L, uint64_t b, uint32_t Q) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[5] = {64, L, N / 64, G, b};
+    cuuint64_t strides[4] = {G * N * 2, 128, N * 2, L * G * N * 2};
+    cuuint32_t box[5] = {64, Q, (cuuint32_t)(N / 64), 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 5-D map of x [b][L][H][P] viewed as (64, P/64, H, L, b), box (64, P/64, HB,
 // Q, 1): one box per chunk holds the CTA's heads with 256 contiguous bytes
 // per step ([Q][HB][P/64][64] in shared memory, 128-byte swizzle).
@@ -1700,7 +1722,7 @@ size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // chunk packs [b, nc, G] of PACK_BYTES
 template <class C>
 size_t pack_bytes(const Dims &d) {
-    return align256((size_t)C::PACK_BYTES * d.b * d.nc * d.G);
+    return align256((size_t)C::CBM_BYTES * d.b * d.nc * d.G);
 }
 
 // Workspace: chunk-pack ready flags [b, nc, G] | chunk packs | segment
@@ -1775,9 +1797,11 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pac
 // pdl: the scan may start while the kernel before it on the stream (the
 // C B^T kernel, which publishes its packs through ready flags) still runs.
 template <class C>
-cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, dim3 grid, const char *name,
-                        bool pdl, cudaStream_t s) {
-    CUtensorMap mx, mdt = {}, my;
+cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, const void *B, const void *Cm,
+                        dim3 grid, const char *name, bool pdl, cudaStream_t s) {
+    CUtensorMap mx, mdt = {}, my, mb, mc;
+    if (!make_bt_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_bt_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
+        return cudaErrorInvalidValue;
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
     const bool f32 = ydtype == SSD_DTYPE_F32;
     if (!make_x_map(&mx, x, d.P, d.H, d.L, d.b, C::HB, C::Q)) return cudaErrorInvalidValue;
@@ -1797,11 +1821,11 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     if (f32) {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
+        e = launch_k(chunk_scan_kernel<C, float>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
     } else {
         e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
     }
     timing_mark(s, name);
     return e;
@@ -1888,7 +1912,7 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     }
     // segments in the slowest grid dimension: the first segment's CTAs, which
     // need nothing from the segment-state kernel, are scheduled first
-    return launch_scan<C>(d, prm, ydtype, x, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", true, s);
+    return launch_scan<C>(d, prm, ydtype, x, B, Cm, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", true, s);
 }
 
 // Dispatch over the compiled tile configurations.
@@ -2021,7 +2045,7 @@ cudaError_t run_chunk_scan(const Dims &dq, const Dims &d, ssd_dtype_t ydtype, co
     timing_begin(s);
     if (e == cudaSuccess && selftest_ns == 0) e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, status, s);
     if (e == cudaSuccess)
-        e = launch_scan<C>(d, prm, ydtype, x, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)dq.nc),
+        e = launch_scan<C>(d, prm, ydtype, x, B, Cm, dim3((unsigned)prm.nhb, (unsigned)d.b, (unsigned)dq.nc),
                            "chunk_scan_stage_tc", selftest_ns == 0, s);
     return e;
 }

@@ -152,9 +152,9 @@ def _a256(v):
 @pytest.mark.parametrize("name", ["mamba2_130m", "mamba2_2p7b", "long_16k", "wide_head", "wide_head_q128"])
 def test_workspace_layout_of_the_tensor_core_path(lib, name):
     """ssd_fwd's workspace on the bf16 tensor-core path: one ready flag per
-    chunk pack, the chunk packs (masked C B^T of a 64-step tile and the tile's
-    B and C, bf16), and, when the sequence is cut into segments, the segment
-    states (fp32) and the segment totals.  With no GPU to query, the segment
+    chunk pack, the chunk packs (the masked C B^T of a 64-step tile, bf16),
+    and, when the sequence is cut into segments, the segment states (fp32)
+    and the segment totals.  With no GPU to query, the segment
     plan assumes the GB300's 152 SMs."""
     import ssd_inputs as si
     import bench
@@ -164,7 +164,7 @@ def test_workspace_layout_of_the_tensor_core_path(lib, name):
     b, L, H, P, N, G = cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate, cfg.ngroups
     nseg, _, nt = bench.tc_plan(cfg, 152)
     nsub = bench.tc_nsub(cfg, 152)
-    want = _a256(4 * b * nt * G) + _a256(b * nt * G * (64 * 64 * 2 + 2 * 64 * N * 2))
+    want = _a256(4 * b * nt * G) + _a256(b * nt * G * 64 * 64 * 2)
     if nseg > 1:
         want += _a256(4 * b * nseg * nsub * H * P * N) + _a256(4 * b * nseg * nsub * H)
     assert lib.ssd_fwd_workspace_size(ctypes.byref(s)) == want
