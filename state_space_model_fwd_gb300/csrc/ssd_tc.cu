@@ -1366,16 +1366,46 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                 tc_fence_after();
                 const float sc = __expf(-rho_end);
                 float *dst = prm.fin + (((long long)b * H + hrow) * C::P + rp) * C::N;
+                if constexpr (C::SG == 1 && C::DT_RING >= 4 * 2048) {
+                    // coalesced: each 16-column block goes through this warp's
+                    // 2 KB of the dt ring (idle once the last chunk's vector
+                    // set has been taken), the piece index XOR-ed with bits
+                    // 1-2 of the row, then out eight rows per store (the 32
+                    // rows of a warp are consecutive p of one head)
+                    float *scr = reinterpret_cast<float *>(dt_ring) + (warp - 4) * 512;
+                    float *dst0 = dst - (long long)lane * C::N;  // row of lane 0
+                    const int pc = lane & 3;
 #pragma unroll 1
-                for (int n0 = half * NCOL; n0 < (half + 1) * NCOL; n0 += 16) {
-                    float v[16];
-                    tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
-                    tmem_ld_wait();
-                    if (hrow < H)
+                    for (int n0 = 0; n0 < C::N; n0 += 16) {
+                        float v[16];
+                        tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(dst + n0 + j) =
-                                make_float4(v[j] * sc, v[j + 1] * sc, v[j + 2] * sc, v[j + 3] * sc);
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<float4 *>(scr + lane * 16 + 4 * (j ^ ((lane >> 1) & 3))) =
+                                make_float4(v[4 * j] * sc, v[4 * j + 1] * sc, v[4 * j + 2] * sc, v[4 * j + 3] * sc);
+                        __syncwarp();
+                        if (hrow < H)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = (lane >> 2) + 8 * i;
+                                *reinterpret_cast<float4 *>(dst0 + (long long)r * C::N + n0 + 4 * pc) =
+                                    *reinterpret_cast<const float4 *>(scr + r * 16 + 4 * (pc ^ ((r >> 1) & 3)));
+                            }
+                        __syncwarp();
+                    }
+                } else {
+#pragma unroll 1
+                    for (int n0 = half * NCOL; n0 < (half + 1) * NCOL; n0 += 16) {
+                        float v[16];
+                        tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
+                        tmem_ld_wait();
+                        if (hrow < H)
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                *reinterpret_cast<float4 *>(dst + n0 + j) =
+                                    make_float4(v[j] * sc, v[j + 1] * sc, v[j + 2] * sc, v[j + 3] * sc);
+                    }
                 }
             }
         }
