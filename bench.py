@@ -581,10 +581,10 @@ def tc_plan(cfg, target_ctas=152):
 
 def tc_nsub(cfg, target_ctas=152):
     """Sub-segments of the segment-state pass (mirrors the library): halves
-    with four segments or more, where S and two A buffers fit 256 TMEM
-    columns (N + 128 <= 256) and a segment has two tiles or more."""
+    wherever there are segments, S and two A buffers fit 256 TMEM columns
+    (N + 128 <= 256) and a segment has two tiles or more."""
     nseg, cps, _ = tc_plan(cfg, target_ctas)
-    return 2 if nseg >= 4 and cfg.dstate + 128 <= 256 and cps >= 2 else 1
+    return 2 if nseg > 1 and cfg.dstate + 128 <= 256 and cps >= 2 else 1
 
 
 def KERNEL_BYTES(cfg, name):

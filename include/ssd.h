@@ -166,7 +166,7 @@ SSD_API ssd_status_t ssd_fwd(const ssd_shape_t *shape, const void *x, const void
  * it, so serialise them.  Inputs, outputs and errors as for ssd_fwd; a wait
  * that gave up inside its kernels is read with ssd_get_device_status.
  */
-#define SSD_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define SSD_NOALLOC_SCRATCH_BYTES (32u << 20)
 SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, const void *dt,
                                      const float *A, const void *B, const void *C,
                                      const float *D, const float *init_state, void *y,

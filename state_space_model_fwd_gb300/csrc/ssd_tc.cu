@@ -685,6 +685,9 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
+    // the accumulator has been read: give the columns back before the store
+    // (a segment-state CTA on this SM may be waiting for them)
+    if (warp == 0) tmem_dealloc(tmem, 64);
     if (tid == 0 && ok_sh) {
         bulk_store(pack + plane * C::CBM_BYTES, smem, C::CBM_BYTES);
         bulk_commit_group();
@@ -692,7 +695,6 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
         __threadfence();
         if (ready) st_release_gpu(ready + plane, 1u);
     }
-    if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 // ===========================================================================
@@ -717,12 +719,14 @@ struct SegT {
     static constexpr int NA = NBG == 4 ? C::SEG_NA : 2;
     static constexpr uint32_t TMEM = NBG == 4 ? C::SEG_TMEM : 256;
     static constexpr int SMEM = C::seg_smem(ST);
-    static constexpr int MIN_CTAS = NBG == 4 ? 1 : 2;
+    // two CTAs of 384 threads at 72 registers beside a C B^T CTA (128 x 80)
+    // fill the 64 K registers of an SM exactly
+    static constexpr int MAXREG = NBG == 4 ? 64 : 72;
     static_assert(NBG == 4 || C::N + 2 * C::Q <= 256, "two A buffers and S in 256 columns");
 };
 
 template <class C, int NBG>
-__global__ void __launch_bounds__(SegT<C, NBG>::THREADS, SegT<C, NBG>::MIN_CTAS)
+__global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NBG>::MAXREG))
     seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
                      const __grid_constant__ CUtensorMap mdt, TcParams prm) {
     using T = SegT<C, NBG>;
@@ -1737,13 +1741,12 @@ Plan plan_for(const Dims &d) {
     if (nseg > d.nc) nseg = (int)d.nc;
     p.cps = (int)((d.nc + nseg - 1) / nseg);
     p.nseg = (int)((d.nc + p.cps - 1) / p.cps);
-    // With four segments or more the segment-state pass, which the scans of
-    // the later segments wait for, is the longer part of the step: its local
-    // states are then formed on half segments by the two-group kernel, two
-    // CTAs per SM (where S and two A buffers fit 256 TMEM columns and a
-    // segment has two chunks or more).  With fewer segments the halves would
-    // hold the SMs the first segment's scan starts on.
-    p.nsub = (p.nseg >= 4 && C::N + 2 * C::Q <= 256 && p.cps >= 2) ? 2 : 1;
+    // The scans of the later segments wait for the whole segment-state pass:
+    // its local states are formed on half segments by the two-group kernel,
+    // two CTAs per SM, where S and two A buffers fit 256 TMEM columns and a
+    // segment has two chunks or more (its CTAs take every SM, so the first
+    // segment's scan starts once they end, which costs less than it saves).
+    p.nsub = (p.nseg > 1 && C::N + 2 * C::Q <= 256 && p.cps >= 2) ? 2 : 1;
     return p;
 }
 

@@ -24,7 +24,7 @@ SCRATCH_LIMIT_STATUS = 5
 # largest first, so that every later call runs on top of what a larger one
 # left in the shared buffer
 CASES = [
-    # the 2048-token Mamba-2 130M-shaped layer (about 15 MB of scratch)
+    # the 2048-token Mamba-2 130M-shaped layer (about 20 MB of scratch)
     si.CONFIGS["mamba2_130m"],
     # several segments of one chunk each: the scratch holds segment states
     si.SSDConfig("noalloc_segments", 2, 640, 4, 64, 128, 1, 64, "bf16", True, 501),
@@ -62,7 +62,7 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     inputs at this length need ~270 MB of intermediates."""
     lib = ssd.load_library()
     shape = ssd.ssd_shape_t(1, 65536, 8, 64, 128, 1, 64, ssd.SSD_DTYPE_F32, ssd.SSD_DTYPE_F32)
-    assert lib.ssd_fwd_workspace_size(ctypes.byref(shape)) > (16 << 20)
+    assert lib.ssd_fwd_workspace_size(ctypes.byref(shape)) > (32 << 20)
     fake = ctypes.c_void_p(1 << 20)
     st = lib.ssd_fwd_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, None, None, fake, None, None)
     assert st == SCRATCH_LIMIT_STATUS
