@@ -600,94 +600,90 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 
 // ===========================================================================
 // Chunk packs, one CTA per (chunk, group, batch):
-//   CB[t, s] = C_t . B_s for s <= t (0 above the diagonal), bf16, by an
-//   M = Q = 64 tcgen05 contraction over N (rows 16w .. 16w + 15 of the M = 64
-//   accumulator sit in TMEM lanes 32w .. 32w + 15), stored K-major and
-//   swizzled, followed by the chunk's B and C tiles as the TMA delivered
-//   them: pack[(b, c, g)] = [CB | B | C], the shared-memory image the chunk
-//   scan's MMAs read, so that it arrives there with one bulk copy.
+//   CB[t, s] = C_t . B_s for s <= t (0 above the diagonal), bf16, stored
+//   K-major and swizzled (the shared-memory image the chunk scan's MMAs read,
+//   so that it arrives there with one bulk copy): pack[(b, c, g)].  The
+//   64 x 64 x N product runs on the warp-level tensor-core MMA, which needs
+//   no TMEM: these CTAs share SMs with segment-state CTAs whose TMEM
+//   allocations fill the SM's 512 columns.
 // ===========================================================================
 template <class C>
 __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CUtensorMap mb,
                                                       const __grid_constant__ CUtensorMap mc, uint8_t *pack, int nc,
                                                       int G, unsigned *ready, unsigned *status) {
-    static_assert(C::Q == 64, "the M = 64 accumulator layout is assumed");
+    static_assert(C::Q == 64, "four warps of 16 rows");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *cbs = smem, *bs = smem + C::CBM_BYTES, *cs = smem + C::CBM_BYTES + C::BC_BYTES;
-    __shared__ uint64_t full_bar, done_bar;
-    __shared__ uint32_t tmem_base_sh;
+    __shared__ uint64_t full_bar;
     __shared__ int ok_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const long long plane = ((long long)b * nc + c) * G + g;
     griddep_launch();
-    if (warp == 0) {
-        tmem_alloc(&tmem_base_sh, 64);
-        tmem_relinquish();
-    }
     if (tid == 32) {
         mbar_init(&full_bar, 1);
-        mbar_init(&done_bar, 1);
         fence_mbar_init();
     }
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_base_sh;
     if (tid == 32) {
-        int ok = 0;
         mbar_arrive_expect_tx(&full_bar, 2 * C::BC_BYTES);
-#pragma unroll
-        for (int nb = 0; nb < C::N / 64; ++nb) {
-            tma_load_4d(cs + nb * (C::Q * 128), &mc, &full_bar, nb * 64, g, c * C::Q, b);
-            tma_load_4d(bs + nb * (C::Q * 128), &mb, &full_bar, nb * 64, g, c * C::Q, b);
-        }
-        if (mbar_wait(&full_bar, 0, kWaitNs)) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(C::Q, C::Q, false, false);
-            const uint64_t dc = sdesc(smem_u32(cs), 16, 1024), db = sdesc(smem_u32(bs), 16, 1024);
-#pragma unroll
-            for (int ks = 0; ks < C::N / 16; ++ks) {
-                const uint32_t koff = (ks / 4) * (C::Q * 128) + (ks % 4) * 32;
-                mma_bf16(tmem, desc_add(dc, koff), desc_add(db, koff), id, ks > 0);
-            }
-            mma_commit(&done_bar);
-            ok = mbar_wait(&done_bar, 0, kWaitNs) ? 1 : 0;
-        } else {
+        // one box each ([N/64][Q][64], 128-byte swizzle)
+        tma_load_5d(cs, &mc, &full_bar, 0, c * C::Q, 0, g, b);
+        tma_load_5d(bs, &mb, &full_bar, 0, c * C::Q, 0, g, b);
+        const int ok = mbar_wait(&full_bar, 0, kWaitNs) ? 1 : 0;
+        if (!ok) {
             mbar_wait(&full_bar, 0, kDrainNs);
+            flag_timeout(status);
         }
         ok_sh = ok;
-        if (!ok) flag_timeout(status);
     }
     __syncthreads();
-    tc_fence_after();
     if (ok_sh) {
-        // masked CB rows into the pack image: row t, 16-byte chunk k of the
-        // 128-byte row at position k ^ (t % 8)
-        const int t = warp * 16 + (lane & 15);
-        float v[64];
+        // C B^T on the warp tensor cores (a 64 x 64 x N product per tile, too
+        // small to pay for TMEM): warp w owns rows t = 16 w .. 16 w + 15, all
+        // 64 columns s as eight 8-wide tiles.  Element (row r, k) of the
+        // staged C and B tiles sits at (k / 64) Q 128 + r 128 + 16 ((k % 64) / 8
+        // ^ r % 8) + 2 (k % 8).
+        float acc[8][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + k * 16, *reinterpret_cast<float(*)[16]>(v + 16 * k));
-        tmem_ld_wait();
-        if (lane < 16) {
+        for (int j = 0; j < 8; ++j)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                uint4 w;
-                w.x = pack_bf16x2(8 * k + 0 <= t ? v[8 * k + 0] : 0.f, 8 * k + 1 <= t ? v[8 * k + 1] : 0.f);
-                w.y = pack_bf16x2(8 * k + 2 <= t ? v[8 * k + 2] : 0.f, 8 * k + 3 <= t ? v[8 * k + 3] : 0.f);
-                w.z = pack_bf16x2(8 * k + 4 <= t ? v[8 * k + 4] : 0.f, 8 * k + 5 <= t ? v[8 * k + 5] : 0.f);
-                w.w = pack_bf16x2(8 * k + 6 <= t ? v[8 * k + 6] : 0.f, 8 * k + 7 <= t ? v[8 * k + 7] : 0.f);
-                *reinterpret_cast<uint4 *>(cbs + t * 128 + ((k ^ (t & 7)) << 4)) = w;
+            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+        const int ra = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);  // C row this lane addresses
+        const int ka = lane >> 4;                                        // its 8-column half of the k step
+        const int rb = (lane & 7) + 8 * (lane >> 4);                     // B row (within two s tiles)
+        const int kb = (lane >> 3) & 1;
+#pragma unroll 1
+        for (int k0 = 0; k0 < C::N; k0 += 16) {
+            const int blk = (k0 / 64) * (C::Q * 128), kc = (k0 % 64) / 8;
+            uint32_t a[4];
+            ldsm_x4(a, cs + blk + ra * 128 + (((kc + ka) ^ (ra & 7)) << 4));
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                const int r = 8 * j + rb;
+                uint32_t bq[4];
+                ldsm_x4(bq, bs + blk + r * 128 + (((kc + kb) ^ (r & 7)) << 4));
+                mma_16816_bf16(acc[j], a, bq[0], bq[1]);
+                mma_16816_bf16(acc[j + 1], a, bq[2], bq[3]);
+            }
+        }
+        // masked (s <= t) bf16 pairs into the pack image: row t, 16-byte
+        // chunk s / 8 at position (s / 8) ^ (t % 8)
+        const int t0 = 16 * warp + (lane >> 2), q = lane & 3;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int s0 = 8 * j + 2 * q;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int t = t0 + 8 * h;
+                const uint32_t w = pack_bf16x2(s0 <= t ? acc[j][2 * h] : 0.f, s0 + 1 <= t ? acc[j][2 * h + 1] : 0.f);
+                *reinterpret_cast<uint32_t *>(cbs + t * 128 + ((j ^ (t & 7)) << 4) + 4 * q) = w;
             }
         }
         fence_async_smem();
     }
-    tc_fence_before();
     __syncthreads();
-    // the accumulator has been read: give the columns back before the store
-    // (a segment-state CTA on this SM may be waiting for them)
-    if (warp == 0) tmem_dealloc(tmem, 64);
     if (tid == 0 && ok_sh) {
         bulk_store(pack + plane * C::CBM_BYTES, smem, C::CBM_BYTES);
         bulk_commit_group();
@@ -719,8 +715,8 @@ struct SegT {
     static constexpr int NA = NBG == 4 ? C::SEG_NA : 2;
     static constexpr uint32_t TMEM = NBG == 4 ? C::SEG_TMEM : 256;
     static constexpr int SMEM = C::seg_smem(ST);
-    // two CTAs of 384 threads at 72 registers beside a C B^T CTA (128 x 80)
-    // fill the 64 K registers of an SM exactly
+    // two CTAs of 384 threads at 72 registers beside a C B^T CTA (128 x 56)
+    // fit the 64 K registers of an SM
     static constexpr int MAXREG = NBG == 4 ? 64 : 72;
     static_assert(NBG == 4 || C::N + 2 * C::Q <= 256, "two A buffers and S in 256 columns");
 };
@@ -1816,7 +1812,7 @@ template <class C>
 cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pack, unsigned *ready, unsigned *status,
                       cudaStream_t s) {
     CUtensorMap mb, mc;
-    if (!make_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
+    if (!make_bt_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_bt_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
     static int attr = 0;
     cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::SMEM_CB, attr);
