@@ -27,10 +27,11 @@
 // direct per-entry path for its intra-chunk term.
 //
 // The fused forward is three launches:
-//   cb_mask_kernel     CB of every (chunk, group), bf16
+//   cb_mask_kernel     CB of every (chunk, group), bf16 (a warp-level MMA)
 //   seg_state_kernel   the local state of each segment (a run of consecutive
-//                      chunks, from a zero state) but the last, one long-K
-//                      contraction per segment, and its total decay
+//                      chunks, from a zero state) but the last, or of each
+//                      half of it, one long-K contraction per CTA, and its
+//                      total decay
 //   chunk_scan_kernel  every segment: the state entering it (the pass across
 //                      the earlier segments' local states), then the scaled
 //                      state chain and the outputs
@@ -694,14 +695,15 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
 }
 
 // ===========================================================================
-// Segment-local states (segments 0 .. nseg-2, each from a zero state):
+// Segment-local states (segments 0 .. nseg-2, or their nsub sub-segments,
+// each from a zero state):
 //   S_seg = sum_t exp(sum_{k>t, k in segment} dt_k A) dt_t x_t^T B_t
 //   warp 0      : TMA loads of the x and B tiles
 //   warp 1      : tcgen05.mma S += A^T B, A read from TMEM
 //   warps 2, 3  : dt and the segment weights of one head each (a ring of
 //                 vector sets), and the segment's total decay
-//   warps 4-19  : the A operand (weights x x, bf16 hi + lo) into TMEM, three
-//                 buffers; then the state to HBM
+//   warps 4 ..  : the A operand (weights x x, bf16 hi + lo) into TMEM, two
+//                 or three buffers; then the state to HBM
 // ===========================================================================
 // NBG groups of four operand-builder warps (each group Q / NBG of the steps):
 // four groups with the deep ring (one CTA per SM), or two groups with two
@@ -1748,15 +1750,15 @@ Plan plan_for(const Dims &d) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// chunk packs [b, nc, G] of PACK_BYTES
+// chunk packs [b, nc, G] of CBM_BYTES (the masked C B^T of each tile)
 template <class C>
 size_t pack_bytes(const Dims &d) {
     return align256((size_t)C::CBM_BYTES * d.b * d.nc * d.G);
 }
 
-// Workspace: chunk-pack ready flags [b, nc, G] | chunk packs | segment
-// states | segment totals.  The flags are cleared on the stream by every
-// call.
+// Workspace: chunk-pack ready flags [b, nc, G] | chunk packs | local
+// states and totals of the nseg * nsub (sub-)segments.  The flags are
+// cleared on the stream by every call.
 size_t flag_bytes(const Dims &d) { return align256(sizeof(unsigned) * d.b * d.nc * d.G); }
 
 template <class C>
