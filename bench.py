@@ -171,13 +171,23 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # ncu traffic recorded under profiles/ (null when the kernel source changed)
 # ---------------------------------------------------------------------------
+def code_of(text):
+    """The source text without comments, trailing spaces and blank lines: a
+    change to comments alone leaves the recorded profiles valid."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_sha():
+    """Hash of the code of the CUDA sources, the key of the recorded ncu
+    summaries under profiles/."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "state_space_model_fwd_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 
