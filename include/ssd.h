@@ -72,7 +72,7 @@ extern "C" {
 typedef enum {
     SSD_OK = 0,
     SSD_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misaligned pointer */
-    SSD_ERR_UNSUPPORTED = 2,   /* valid shape this build does not run */
+    SSD_ERR_UNSUPPORTED = 2,   /* a valid shape the library has no kernel for */
     SSD_ERR_CUDA = 3,          /* a CUDA launch or query failed */
     SSD_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
     SSD_ERR_SCRATCH_LIMIT = 5, /* ssd_fwd_noalloc: shape needs more than its static scratch */
