@@ -162,8 +162,9 @@ struct Cfg {
     static constexpr uint32_t SEG_TMEM =
         SEG_COLS <= 64 ? 64 : SEG_COLS <= 128 ? 128 : SEG_COLS <= 256 ? 256 : 512;
 
-    // C B^T kernel: the chunk pack
-    static constexpr int SMEM_CB = PACK_BYTES + 1024;
+    // C B^T kernel: the masked C B^T and one or two stages of C and B tiles
+    static constexpr int smem_cb(int nst) { return CBM_BYTES + nst * 2 * BC_BYTES + 1024; }
+    static constexpr int SMEM_CB = smem_cb(1);
 };
 
 // Event trace (SSD_TRACE builds): clock64() of role events of CTA (0, 0, 0),
@@ -600,7 +601,9 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 }
 
 // ===========================================================================
-// Chunk packs, one CTA per (chunk, group, batch):
+// Chunk packs, one per (chunk, group, batch) tile; one CTA per tile, or (where
+// the scan leaves SMs free) one CTA on each such SM walking the tiles in chunk
+// order with the next tile's loads in flight:
 //   CB[t, s] = C_t . B_s for s <= t (0 above the diagonal), bf16, stored
 //   K-major and swizzled (the shared-memory image the chunk scan's MMAs read,
 //   so that it arrives there with one bulk copy): pack[(b, c, g)].  The
@@ -611,36 +614,48 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 template <class C>
 __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CUtensorMap mb,
                                                       const __grid_constant__ CUtensorMap mc, uint8_t *pack, int nc,
-                                                      int G, unsigned *ready, unsigned *status) {
+                                                      int G, int nbatch, int nst, unsigned *ready, unsigned *status) {
     static_assert(C::Q == 64, "four warps of 16 rows");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *cbs = smem, *bs = smem + C::CBM_BYTES, *cs = smem + C::CBM_BYTES + C::BC_BYTES;
-    __shared__ uint64_t full_bar;
+    uint8_t *cbs = smem;
+    // nst stages of [C tile | B tile]
+    auto stage_c = [&](int s) { return smem + C::CBM_BYTES + s * 2 * C::BC_BYTES; };
+    auto stage_b = [&](int s) { return smem + C::CBM_BYTES + s * 2 * C::BC_BYTES + C::BC_BYTES; };
+    __shared__ uint64_t full_bar[2];
     __shared__ int ok_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const long long plane = ((long long)b * nc + c) * G + g;
+    // tiles in chunk-major order (every batch and group of a chunk before the
+    // next chunk), this CTA's every gridDim.x-th
+    const long long per_chunk = (long long)nbatch * G, ntiles = per_chunk * nc;
     griddep_launch();
     if (tid == 32) {
-        mbar_init(&full_bar, 1);
+        for (int s = 0; s < 2; ++s) mbar_init(&full_bar[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 32) {
-        mbar_arrive_expect_tx(&full_bar, 2 * C::BC_BYTES);
+    int nload[2] = {0, 0};  // loads issued per stage (thread 32)
+    auto issue = [&](long long t, int s) {
+        const int c = (int)(t / per_chunk), rem = (int)(t % per_chunk), b = rem / G, g = rem % G;
+        mbar_arrive_expect_tx(&full_bar[s], 2 * C::BC_BYTES);
         // one box each ([N/64][Q][64], 128-byte swizzle)
-        tma_load_5d(cs, &mc, &full_bar, 0, c * C::Q, 0, g, b);
-        tma_load_5d(bs, &mb, &full_bar, 0, c * C::Q, 0, g, b);
-        const int ok = mbar_wait(&full_bar, 0, kWaitNs) ? 1 : 0;
-        if (!ok) {
-            mbar_wait(&full_bar, 0, kDrainNs);
-            flag_timeout(status);
+        tma_load_5d(stage_c(s), &mc, &full_bar[s], 0, c * C::Q, 0, g, b);
+        tma_load_5d(stage_b(s), &mb, &full_bar[s], 0, c * C::Q, 0, g, b);
+        ++nload[s];
+    };
+    if (tid == 32)
+        for (int k = 0; k < nst; ++k)
+            if (blockIdx.x + (long long)k * gridDim.x < ntiles) issue(blockIdx.x + (long long)k * gridDim.x, k);
+    int k = 0;
+    for (long long t = blockIdx.x; t < ntiles; t += gridDim.x, ++k) {
+        const int s = k % nst;
+        if (tid == 32) {
+            const int ok = mbar_wait(&full_bar[s], (uint32_t)((k / nst) & 1), kWaitNs) ? 1 : 0;
+            if (!ok) flag_timeout(status);
+            ok_sh = ok;
         }
-        ok_sh = ok;
-    }
-    __syncthreads();
-    if (ok_sh) {
+        __syncthreads();
+        if (!ok_sh) break;
         // C B^T on the warp tensor cores (a 64 x 64 x N product per tile, too
         // small to pay for TMEM): warp w owns rows t = 16 w .. 16 w + 15, all
         // 64 columns s as eight 8-wide tiles.  Element (row r, k) of the
@@ -648,9 +663,10 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
         // ^ r % 8) + 2 (k % 8).
         float acc[8][4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int jj = 0; jj < 8; ++jj)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+            for (int e = 0; e < 4; ++e) acc[jj][e] = 0.f;
+        const uint8_t *cs = stage_c(s), *bs = stage_b(s);
         const int ra = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);  // C row this lane addresses
         const int ka = lane >> 4;                                        // its 8-column half of the k step
         const int rb = (lane & 7) + 8 * (lane >> 4);                     // B row (within two s tiles)
@@ -661,37 +677,48 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
             uint32_t a[4];
             ldsm_x4(a, cs + blk + ra * 128 + (((kc + ka) ^ (ra & 7)) << 4));
 #pragma unroll
-            for (int j = 0; j < 8; j += 2) {
-                const int r = 8 * j + rb;
+            for (int jj = 0; jj < 8; jj += 2) {
+                const int r = 8 * jj + rb;
                 uint32_t bq[4];
                 ldsm_x4(bq, bs + blk + r * 128 + (((kc + kb) ^ (r & 7)) << 4));
-                mma_16816_bf16(acc[j], a, bq[0], bq[1]);
-                mma_16816_bf16(acc[j + 1], a, bq[2], bq[3]);
+                mma_16816_bf16(acc[jj], a, bq[0], bq[1]);
+                mma_16816_bf16(acc[jj + 1], a, bq[2], bq[3]);
             }
         }
+        // every warp has read the stage: refill it with this CTA's tile nst on
+        __syncthreads();
+        if (tid == 32 && t + (long long)nst * gridDim.x < ntiles) issue(t + (long long)nst * gridDim.x, s);
         // masked (s <= t) bf16 pairs into the pack image: row t, 16-byte
-        // chunk s / 8 at position (s / 8) ^ (t % 8)
+        // chunk s / 8 at position (s / 8) ^ (t % 8) (the previous tile's
+        // store has finished reading it: thread 0 waited for it before the
+        // barriers above)
         const int t0 = 16 * warp + (lane >> 2), q = lane & 3;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int s0 = 8 * j + 2 * q;
+        for (int jj = 0; jj < 8; ++jj) {
+            const int s0 = 8 * jj + 2 * q;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int t = t0 + 8 * h;
-                const uint32_t w = pack_bf16x2(s0 <= t ? acc[j][2 * h] : 0.f, s0 + 1 <= t ? acc[j][2 * h + 1] : 0.f);
-                *reinterpret_cast<uint32_t *>(cbs + t * 128 + ((j ^ (t & 7)) << 4) + 4 * q) = w;
+                const int tr = t0 + 8 * h;
+                const uint32_t w = pack_bf16x2(s0 <= tr ? acc[jj][2 * h] : 0.f, s0 + 1 <= tr ? acc[jj][2 * h + 1] : 0.f);
+                *reinterpret_cast<uint32_t *>(cbs + tr * 128 + ((jj ^ (tr & 7)) << 4) + 4 * q) = w;
             }
         }
         fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            const int c = (int)(t / per_chunk), rem = (int)(t % per_chunk), b = rem / G, g = rem % G;
+            const long long plane = ((long long)b * nc + c) * G + g;
+            bulk_store(pack + plane * C::CBM_BYTES, cbs, C::CBM_BYTES);
+            bulk_commit_group();
+            bulk_wait_all();
+            __threadfence();
+            if (ready) st_release_gpu(ready + plane, 1u);
+        }
     }
-    __syncthreads();
-    if (tid == 0 && ok_sh) {
-        bulk_store(pack + plane * C::CBM_BYTES, smem, C::CBM_BYTES);
-        bulk_commit_group();
-        bulk_wait_all();
-        __threadfence();
-        if (ready) st_release_gpu(ready + plane, 1u);
-    }
+    // (after a wait that gave up) let this CTA's own loads land before it exits
+    if (tid == 32)
+        for (int s = 0; s < nst; ++s)
+            if (nload[s] > 0) mbar_wait(&full_bar[s], (uint32_t)((nload[s] - 1) & 1), kDrainNs);
 }
 
 // ===========================================================================
@@ -1812,15 +1839,21 @@ cudaError_t raise_smem(const void *fn, int bytes, int &done) {
 
 template <class C>
 cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pack, unsigned *ready, unsigned *status,
-                      cudaStream_t s) {
+                      cudaStream_t s, int ncta = 0) {
     CUtensorMap mb, mc;
     if (!make_bt_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_bt_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
+    // ncta > 0: that many CTAs walk the tiles, two stages deep (one CTA per SM
+    // the scan leaves free); otherwise one CTA per tile
+    const long long ntiles = (long long)d.nc * d.b * d.G;
+    const int nst = ncta > 0 && ncta < ntiles ? 2 : 1;
+    const unsigned grid = nst == 2 ? (unsigned)ncta : (unsigned)ntiles;
+    const int smem = C::smem_cb(nst);
     static int attr = 0;
-    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::SMEM_CB, attr);
+    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::smem_cb(2), attr);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)d.nc, (unsigned)d.G, (unsigned)d.b);
-    e = launch_k(cb_mask_kernel<C>, grid, 128, C::SMEM_CB, s, false, mb, mc, pack, (int)d.nc, (int)d.G, ready, status);
+    e = launch_k(cb_mask_kernel<C>, dim3(grid), 128, smem, s, false, mb, mc, pack, (int)d.nc, (int)d.G, (int)d.b, nst,
+                 ready, status);
     timing_mark(s, "cb_mask_tc");
     return e;
 }
@@ -1929,7 +1962,10 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     cudaError_t e = cudaMemsetAsync(w, 0, hdr, s);
     if (e != cudaSuccess) return e;
     timing_begin(s);
-    e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s);
+    // with one segment the scan's CTAs leave SMs free: the C B^T tiles are
+    // walked by one CTA on each of those, and the scan starts at once
+    const long long units = d.b * p.nhb, spare = sm_count() - units;
+    e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, p.nseg == 1 && spare >= 8 ? (int)spare : 0);
     if (e != cudaSuccess) return e;
     if (p.nseg > 1) {
         const dim3 grid(p.nhb, (unsigned)d.b, (unsigned)((p.nseg - 1) * p.nsub));
