@@ -1839,15 +1839,15 @@ cudaError_t raise_smem(const void *fn, int bytes, int &done) {
 
 template <class C>
 cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pack, unsigned *ready, unsigned *status,
-                      cudaStream_t s, int ncta = 0) {
+                      cudaStream_t s, int ncta = 0, int nst_max = 2) {
     CUtensorMap mb, mc;
     if (!make_bt_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_bt_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
     // ncta > 0: that many CTAs walk the tiles, two stages deep (one CTA per SM
     // the scan leaves free); otherwise one CTA per tile
     const long long ntiles = (long long)d.nc * d.b * d.G;
-    const int nst = ncta > 0 && ncta < ntiles ? 2 : 1;
-    const unsigned grid = nst == 2 ? (unsigned)ncta : (unsigned)ntiles;
+    const int nst = ncta > 0 && ncta < ntiles ? nst_max : 1;
+    const unsigned grid = ncta > 0 && ncta < ntiles ? (unsigned)ncta : (unsigned)ntiles;
     const int smem = C::smem_cb(nst);
     static int attr = 0;
     cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::smem_cb(2), attr);
@@ -1965,7 +1965,10 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     // with one segment the scan's CTAs leave SMs free: the C B^T tiles are
     // walked by one CTA on each of those, and the scan starts at once
     const long long units = d.b * p.nhb, spare = sm_count() - units;
-    e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, p.nseg == 1 && spare >= 8 ? (int)spare : 0);
+    // with segments, at most one C B^T CTA per SM (single stage), so that two
+    // segment-state CTAs fit beside it on every SM
+    e = p.nseg == 1 ? launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, spare >= 8 ? (int)spare : 0)
+                    : launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, sm_count(), 1);
     if (e != cudaSuccess) return e;
     if (p.nseg > 1) {
         const dim3 grid(p.nhb, (unsigned)d.b, (unsigned)((p.nseg - 1) * p.nsub));
