@@ -744,7 +744,7 @@ struct SegT {
     static constexpr int NA = NBG == 4 ? C::SEG_NA : 2;
     static constexpr uint32_t TMEM = NBG == 4 ? C::SEG_TMEM : 256;
     static constexpr int SMEM = C::seg_smem(ST);
-    // two CTAs of 384 threads at 72 registers beside a C B^T CTA (128 x 56)
+    // two CTAs of 384 threads at 72 registers beside a C B^T CTA (128 x 72)
     // fit the 64 K registers of an SM
     static constexpr int MAXREG = NBG == 4 ? 64 : 72;
     static_assert(NBG == 4 || C::N + 2 * C::Q <= 256, "two A buffers and S in 256 columns");
