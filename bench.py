@@ -328,7 +328,7 @@ def main():
     ap.add_argument("--ref-heads", type=int, default=4)
     ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["stages", "sequential", "crossover", "decode"],
+    ap.add_argument("--only", choices=["stages", "sequential", "crossover", "decode", "varlen"],
                     help="run one part of the sweep alone and print its JSON (for profiling that part)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -675,6 +675,7 @@ def run_sweep(ssd, dev, flush, peaks, steps=10):
     out["stages"] = stage_sweep(ssd, dev, flush, peaks, steps)
     out["crossover"] = crossover_sweep(ssd, dev, flush, steps)
     out["decode"] = decode_sweep(ssd, dev, flush, peaks, steps)
+    out["varlen"] = varlen_sweep(ssd, dev, flush, peaks, steps)
     return out
 
 
@@ -716,6 +717,8 @@ def run_only(args):
         out = {"workload": cfg.name, **sequential_scan(ssd, dev, flush, t, y, fin, cfg, steps)}
     elif args.only == "crossover":
         out = crossover_sweep(ssd, dev, flush, steps)
+    elif args.only == "varlen":
+        out = varlen_sweep(ssd, dev, flush, peaks, steps)
     else:
         out = decode_sweep(ssd, dev, flush, peaks, steps)
     print(json.dumps({"only": args.only, **out}), flush=True)
@@ -797,6 +800,58 @@ def time_graph(fn, flush, steps):
     with torch.cuda.graph(g):
         fn()
     return time_device(g.replay, flush, steps)
+
+
+VARLEN_MIXES = {
+    # 8192 tokens of the 130M-shaped layer in each, like the b=4, L=2048 batch
+    "ragged4": [3001, 1500, 2600, 1091],
+    "short64": [100, 156] * 32,
+}
+
+
+def varlen_sweep(ssd, dev, flush, peaks, steps):
+    """ssd_fwd_varlen on packed batches of unequal lengths (130M-shaped
+    layer, 8192 tokens, ragged last chunks), beside the equal-length batch
+    of the same tokens: device time of the whole call (a CUDA graph, so the
+    host's per-sequence launches are not in it)."""
+    import torch
+    base = si.CONFIGS[WORKLOAD]
+    H, P, N, G = base.nheads, base.headdim, base.dstate, base.ngroups
+    rows = {}
+    for name, lens in VARLEN_MIXES.items():
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + n)
+        cfg = base.replace(name="varlen_" + name, batch=1, seqlen=cu[-1], has_init=False)
+        t = si.make_inputs(cfg).to_torch(dev)
+        y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
+        fins = torch.empty((len(lens), H, P, N), device=dev, dtype=torch.float32)
+        shape = ssd.make_shape(t["x"], t["B"], base.chunk_size, torch.bfloat16)
+        ws = torch.empty(max(16, ssd.ssd_fwd_varlen_workspace_size(shape, cu)), device=dev, dtype=torch.uint8)
+
+        def run():
+            ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], None, cu, base.chunk_size,
+                               y=y, final_states=fins, workspace=ws)
+
+        ms = time_graph(run, flush, steps)
+        nbytes = (cu[-1] * H * P * 2 + cu[-1] * H * 2 + 2 * cu[-1] * G * N * 2 + 2 * H * 4
+                  + cu[-1] * H * P * 2 + len(lens) * H * P * N * 4)
+        rows[name] = {"nseq": len(lens), "tokens": cu[-1], "min_len": min(lens), "max_len": max(lens),
+                      "ms": ms, "tokens_per_s": cu[-1] / (ms * 1e-3), "bytes": nbytes,
+                      "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        del t, y, fins, ws
+    t = si.make_inputs(base).to_torch(dev)
+    y = torch.empty(t["x"].shape, device=dev, dtype=torch.bfloat16)
+    fin = torch.empty((base.batch, H, P, N), device=dev, dtype=torch.float32)
+    ws = torch.empty(max(16, ssd.ssd_fwd_workspace_size(ssd.make_shape(t["x"], t["B"], base.chunk_size,
+                                                                       torch.bfloat16))),
+                     device=dev, dtype=torch.uint8)
+    eq = time_graph(lambda: ssd.ssd_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], None, base.chunk_size,
+                                        y=y, final_state=fin, workspace=ws), flush, steps)
+    torch.cuda.empty_cache()
+    return {"workload": "130M-shaped layer (H=24, P=64, N=128, G=1), 8192 tokens packed, bf16 y, no initial state",
+            "timing": "CUDA graph of one call, replayed after an L2 flush; device events around the replay",
+            "equal_batch_ms": eq, "rows": rows}
 
 
 def decode_sweep(ssd, dev, flush, peaks, steps):

@@ -180,12 +180,21 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, co
  * of nseq + 1 offsets, 0 first and Ltot last, non-decreasing); its state
  * starts from init_states[s] (NULL: zero) and ends in final_states[s] (NULL:
  * not written), both [nseq, H, P, N] fp32.  No state crosses a sequence
- * boundary.  Each sequence runs the fused forward of ssd_fwd on its own steps,
- * one after another on `stream`, sharing `workspace`, which must hold
- * ssd_fwd_varlen_workspace_size(shape, cu_seqlens, nseq) bytes (0 for
- * invalid arguments).  Every sequence's start must keep the pointers it
- * derives 16-byte aligned (cu_seqlens[s] * H * sizeof(dtype) a multiple of
- * 16, e.g. H a multiple of 8 for bf16): SSD_ERR_INVALID_ARG otherwise.
+ * boundary.  On the tensor-core path (bf16 inputs and a tile shape it
+ * covers) the sequences run in launch sets of up to 1024: one chunk-scan CTA
+ * per (sequence, head block), longest first, with the C B^T pass walking
+ * every sequence's chunks; the longest sequences may instead run the fused
+ * forward of ssd_fwd each (with segments that fill the SMs), whichever a
+ * host-side cost model of the two rates faster.  A sequence's partial last
+ * chunk then reads the next sequence's first steps and gives them dt = 0, so
+ * they add 0 times their values: finite inputs leave no trace across the
+ * boundary (a non-finite x or B there would).  Other inputs run the
+ * fused forward per sequence.  Everything is enqueued on `stream` and shares
+ * `workspace`, which must hold ssd_fwd_varlen_workspace_size(shape,
+ * cu_seqlens, nseq) bytes (0 for invalid arguments).  Every sequence's
+ * start must keep the pointers it derives 16-byte aligned (cu_seqlens[s] *
+ * H * sizeof(dtype) a multiple of 16, e.g. H a multiple of 8 for bf16):
+ * SSD_ERR_INVALID_ARG otherwise.
  * (The pages are silent on batches of unequal lengths; this packs them the
  * way the chunk split of "Mamba-2 in NVIDIA cuTile", section "Why Mamba-2 is
  * a useful kernel example", extends to.)

@@ -345,6 +345,12 @@ def selective_scan_fwd(x, dt, A, B, C, D=None, init_state=None, *, y=None, final
     return y, final_state
 
 
+def ssd_fwd_varlen_workspace_size(shape: ssd_shape_t, cu_seqlens) -> int:
+    cu = [int(v) for v in (cu_seqlens.tolist() if isinstance(cu_seqlens, torch.Tensor) else cu_seqlens)]
+    cu_arr = (ctypes.c_int64 * len(cu))(*cu)
+    return int(load_library().ssd_fwd_varlen_workspace_size(ctypes.byref(shape), cu_arr, len(cu) - 1))
+
+
 def ssd_fwd_varlen(x, dt, A, B, C, D=None, init_states=None, cu_seqlens=None, chunk_size=64, *, y=None,
                    final_states=None, return_final_states=True, y_dtype=torch.float32, workspace=None, stream=None):
     """Packed variable-length batch: x [1, Ltot, H, P] etc. hold nseq
@@ -438,6 +444,6 @@ def launch_times_ms() -> list:
     return [((lib.ssd_launch_timing_name(i) or b"?").decode(), float(buf[i])) for i in range(min(n, 16))]
 
 
-__all__ = ["ssd_fwd_quadratic", "ssd_fwd_varlen", "ssd_decode_step", "get_device_status", "check_device_status", "selftest_scan_timeout", "ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
+__all__ = ["ssd_fwd_quadratic", "ssd_fwd_varlen", "ssd_fwd_varlen_workspace_size", "ssd_decode_step", "get_device_status", "check_device_status", "selftest_scan_timeout", "ssd_fwd_noalloc", "launch_timing", "launch_times_ms", "ssd_fwd", "ssd_fwd_workspace_size", "ssd_chunk_cumsum", "ssd_chunk_state",
            "ssd_state_passing", "ssd_chunk_scan", "selective_scan_fwd", "ssd_shape_t", "SSDError",
            "load_library", "status_string", "EXPORTED", "LIB_PATH"]

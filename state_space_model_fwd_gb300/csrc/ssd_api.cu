@@ -4,7 +4,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "ssd.h"
 #include "ssd_common.cuh"
@@ -182,6 +184,7 @@ ssd_status_t empty_sequence(const Dims &d, const float *init, float *fin, cudaSt
 constexpr int kMaxTimed = 16;
 struct LaunchTimer {
     bool on = false;
+    bool hold = false;  // inside an entry point made of others: their launches append
     int used = 0;
     cudaEvent_t ev[kMaxTimed + 1] = {};
     const char *name[kMaxTimed] = {};
@@ -192,7 +195,7 @@ LaunchTimer g_timer;
 
 namespace ssd {
 void timing_begin(cudaStream_t s) {
-    if (!g_timer.on) return;
+    if (!g_timer.on || (g_timer.hold && g_timer.used > 0)) return;
     g_timer.used = 0;
     if (cudaEventRecord(g_timer.ev[0], s) == cudaSuccess) g_timer.used = 1;
 }
@@ -303,6 +306,48 @@ ssd_status_t check_varlen(const ssd_shape_t *shape, const int64_t *cu, int64_t n
     *one = *shape;
     return SSD_OK;
 }
+
+// How a packed batch runs on the tensor-core path: the `nfwd` longest
+// sequences one fused forward each (their segments fill the SMs), the rest
+// in launch sets of up to kVarlenMaxUnits sequences (a unit per sequence and
+// head block), whichever split the cost model rates fastest.  `order` holds
+// the non-empty sequences, longest first.
+struct VarlenPlan {
+    bool tc = false;
+    std::vector<ssd::VarlenSeq> order;
+    size_t nfwd = 0;
+};
+
+constexpr size_t kMaxSeparate = 64;  // longest sequences considered for a fused forward of their own
+
+VarlenPlan plan_varlen(const ssd_shape_t *shape, const int64_t *cu, int64_t nseq) {
+    VarlenPlan p;
+    Dims d;
+    if (check_shape(shape, true, &d) != SSD_OK || !ssd::tc_varlen_supported(d, shape->dtype)) return p;
+    p.tc = true;
+    for (int64_t s = 0; s < nseq; ++s)
+        if (cu[s + 1] > cu[s]) p.order.push_back({(int)cu[s], (int)(cu[s + 1] - cu[s]), (int)s});
+    std::stable_sort(p.order.begin(), p.order.end(),
+                     [](const ssd::VarlenSeq &a, const ssd::VarlenSeq &b) { return a.len > b.len; });
+    const size_t m = p.order.size();
+    auto sets_cost = [&](size_t from) {
+        double us = 0;
+        for (size_t i = from; i < m; i += ssd::kVarlenMaxUnits)
+            us += ssd::tc_varlen_cost_us(d, p.order.data() + i,
+                                         (int)std::min<size_t>(ssd::kVarlenMaxUnits, m - i));
+        return us;
+    };
+    double best = sets_cost(0), sep = 0;
+    for (size_t k = 1; k <= std::min(m, kMaxSeparate); ++k) {
+        sep += ssd::tc_fwd_cost_us(d, p.order[k - 1].len);
+        const double us = sep + sets_cost(k);
+        if (us < best) {
+            best = us;
+            p.nfwd = k;
+        }
+    }
+    return p;
+}
 }  // namespace
 
 extern "C" {
@@ -311,6 +356,22 @@ size_t ssd_fwd_varlen_workspace_size(const ssd_shape_t *shape, const int64_t *cu
     ssd_shape_t one;
     if (check_varlen(shape, cu_seqlens, nseq, &one) != SSD_OK) return 0;
     size_t need = 0;
+    const VarlenPlan p = plan_varlen(shape, cu_seqlens, nseq);
+    if (p.tc) {
+        Dims d;
+        (void)check_shape(shape, true, &d);
+        for (size_t i = 0; i < p.order.size(); ++i) {
+            if (i < p.nfwd) {
+                one.seqlen = p.order[i].len;
+                need = std::max(need, ssd_fwd_workspace_size(&one));
+            } else {
+                const int n = (int)std::min<size_t>(ssd::kVarlenMaxUnits, p.order.size() - i);
+                need = std::max(need, ssd::tc_varlen_workspace(d, p.order.data() + i, n));
+                i += n - 1;
+            }
+        }
+        return need;
+    }
     for (int64_t s = 0; s < nseq; ++s) {
         one.seqlen = cu_seqlens[s + 1] - cu_seqlens[s];
         if (one.seqlen == 0) continue;
@@ -343,14 +404,51 @@ ssd_status_t ssd_fwd_varlen(const ssd_shape_t *shape, const int64_t *cu_seqlens,
         if (!ptrs_ok({px, pdt, pb, py}, {})) return SSD_ERR_INVALID_ARG;
     }
     if (ssd_fwd_varlen_workspace_size(shape, cu_seqlens, nseq) > workspace_bytes) return SSD_ERR_WORKSPACE;
-    for (int64_t s = 0; s < nseq; ++s) {
+    // one sequence's own fused forward
+    auto own = [&](int64_t s) {
         const int64_t t0 = cu_seqlens[s];
         one.seqlen = cu_seqlens[s + 1] - t0;
         const float *ini = init_states ? init_states + s * H * P * N : nullptr;
         float *fin = final_states ? final_states + s * H * P * N : nullptr;
-        st = ssd_fwd(&one, static_cast<const char *>(x) + t0 * H * P * e, static_cast<const char *>(dt) + t0 * H * e,
-                     A, static_cast<const char *>(B) + t0 * G * N * e, static_cast<const char *>(C) + t0 * G * N * e,
-                     D, ini, static_cast<char *>(y) + t0 * H * P * ye, fin, workspace, workspace_bytes, stream);
+        return ssd_fwd(&one, static_cast<const char *>(x) + t0 * H * P * e,
+                       static_cast<const char *>(dt) + t0 * H * e, A, static_cast<const char *>(B) + t0 * G * N * e,
+                       static_cast<const char *>(C) + t0 * G * N * e, D, ini,
+                       static_cast<char *>(y) + t0 * H * P * ye, fin, workspace, workspace_bytes, stream);
+    };
+    const VarlenPlan p = plan_varlen(shape, cu_seqlens, nseq);
+    if (!p.tc) {
+        for (int64_t s = 0; s < nseq; ++s)
+            if ((st = own(s)) != SSD_OK) return st;
+        return SSD_OK;
+    }
+    Dims d;
+    (void)check_shape(shape, true, &d);
+    // the launch list of this call holds every launch it makes
+    ssd::timing_begin(stream);
+    g_timer.hold = true;
+    struct Release {
+        ~Release() { g_timer.hold = false; }
+    } release;
+    // empty sequences: the final state is the initial one
+    for (int64_t s = 0; s < nseq; ++s)
+        if (cu_seqlens[s + 1] == cu_seqlens[s]) {
+            Dims d1 = d;
+            d1.b = 1;
+            st = empty_sequence(d1, init_states ? init_states + s * H * P * N : nullptr,
+                                final_states ? final_states + s * H * P * N : nullptr, stream);
+            if (st != SSD_OK) return st;
+        }
+    for (size_t i = 0; i < p.nfwd; ++i)
+        if ((st = own(p.order[i].seq)) != SSD_OK) return st;
+    unsigned *status = nullptr;
+    if (p.nfwd < p.order.size()) {
+        const cudaError_t ce = device_status_word(&status);
+        if (ce != cudaSuccess) return from_cuda(ce);
+    }
+    for (size_t i = p.nfwd; i < p.order.size(); i += ssd::kVarlenMaxUnits) {
+        const int n = (int)std::min<size_t>(ssd::kVarlenMaxUnits, p.order.size() - i);
+        st = from_cuda(ssd::tc_fwd_varlen(d, p.order.data() + i, n, shape->ydtype, x, dt, A, B, C, D, init_states,
+                                          y, final_states, workspace, status, stream));
         if (st != SSD_OK) return st;
     }
     return SSD_OK;

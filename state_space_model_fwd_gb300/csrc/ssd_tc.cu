@@ -42,6 +42,8 @@
 // bf16.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "ssd_tc.cuh"
 #include "tc_ptx.cuh"
 
@@ -54,6 +56,14 @@ constexpr int kSmemLimit = 226 * 1024;  // dynamic bytes; leaves room for the st
 constexpr uint64_t kWaitNs = 100000000ull;    // a wait gives up after 0.1 s
 constexpr uint64_t kDrainNs = 20000000ull;    // the exit drain gives up after 0.02 s
 constexpr float kLambda = 64.f;               // |exponent| bound of the scaled operands
+
+// One sequence of a packed batch of unequal lengths (x, dt, B, C, y as one
+// [1, Ltot, ..] tensor): its steps are rows t0 .. t0 + len - 1, its chunk
+// packs and flags start at plane cbase (times G), its states are init /
+// fin [seq].  The chunk scan runs one unit per blockIdx.y.
+struct VlUnit {
+    int t0, len, cbase, seq;
+};
 
 struct TcParams {
     long long *trace;  // optional event trace of CTA (0, 0, 0) (trace builds only)
@@ -94,6 +104,9 @@ struct TcParams {
     // the state warps of segments > 0 wait for it before reading the states
     // entering them
     int dep_seg;
+    // packed sequences (null: the equal-length batch b); one segment each,
+    // blockIdx.y = the unit
+    const VlUnit *vl;
 };
 
 template <int P_, int N_, int Q_>
@@ -286,9 +299,11 @@ struct ChunkDt {
     float d[C::HB][QPL];
 };
 
-// dt of chunk c (plain loads; the caller keeps kDtAhead chunks in flight).
+// dt of chunk c of the sequence whose steps start at row t0 and stop before
+// step slen (plain loads; the caller keeps kDtAhead chunks in flight).
 template <class C>
-__device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int c, ChunkDt<C> &o) {
+__device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int c, int t0, long long slen,
+                                         ChunkDt<C> &o) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int hh = 0; hh < C::HB; ++hh)
@@ -296,9 +311,10 @@ __device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int
         for (int j = 0; j < ChunkDt<C>::QPL; ++j) {
             const long long h = h0 + hh;
             const long long t = (long long)c * C::Q + ChunkDt<C>::QPL * lane + j;
-            // (steps past L in a partial last chunk: dt = 0, as the TMA path's fill)
-            o.d[hh][j] = h < prm.H && t < prm.L ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + t) * prm.H + h))
-                                                : 0.f;
+            // (steps past the sequence in a partial last chunk: dt = 0)
+            o.d[hh][j] = h < prm.H && t < slen
+                             ? __bfloat162float(__ldg(prm.dt + ((long long)b * prm.L + t0 + t) * prm.H + h))
+                             : 0.f;
         }
 }
 
@@ -310,13 +326,19 @@ __device__ __forceinline__ void fetch_dt(const TcParams &prm, int b, int h0, int
 // each chunk's dt is loaded when needed.
 constexpr int kDtGroup = 4;
 
-template <class C>
+// (VL: a packed sequence, with its first row t0 in the map and its length)
+template <class C, bool VL = false>
 struct DtFeed {
     uint8_t *ring;
     uint64_t *bar;  // [2], count 1
     const CUtensorMap *map;
     int b, h0, n;
     int issued;  // boxes issued so far (box i went to slot i % 2)
+    // the sequence's first row in the map and its length: steps at or past
+    // slen (a partial last chunk, which in a packed batch holds the next
+    // sequence's first steps) take dt = 0
+    int t0;
+    long long slen;
     // first chunk of the box of steps 4 gi .. 4 gi + 3 (chunk_of is linear,
     // increasing or decreasing; chunks past the segment are only read along)
     template <class F>
@@ -327,7 +349,8 @@ struct DtFeed {
     __device__ __forceinline__ void issue(int gi, F chunk_of) {
         const int k = gi & 1;
         mbar_arrive_expect_tx(&bar[k], C::DT_BOX);
-        tma_load_3d(ring + k * C::DT_BOX, map, &bar[k], h0 & ~7, box_start(gi, chunk_of) * C::Q, b);
+        tma_load_3d(ring + k * C::DT_BOX, map, &bar[k], h0 & ~7, (VL ? t0 : 0) + box_start(gi, chunk_of) * C::Q,
+                    b);
         ++issued;
     }
     template <class F>
@@ -342,7 +365,7 @@ struct DtFeed {
                                          ChunkDt<C> &o) {
         const int lane = threadIdx.x & 31;
         if (!prm.dt_tma) {
-            fetch_dt<C>(prm, b, h0, chunk_of(it), o);
+            fetch_dt<C>(prm, b, h0, chunk_of(it), VL ? t0 : 0, VL ? slen : prm.L, o);
             return true;
         }
         const int gi = it / kDtGroup, k = gi & 1;
@@ -351,12 +374,13 @@ struct DtFeed {
             if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
         }
         const int row0 = (chunk_of(it) - box_start(gi, chunk_of)) * C::Q;
+        const long long tq = (long long)chunk_of(it) * C::Q + ChunkDt<C>::QPL * lane;  // this lane's first step
         const unsigned short *d16 = reinterpret_cast<const unsigned short *>(ring + k * C::DT_BOX);
 #pragma unroll
         for (int hh = 0; hh < C::HB; ++hh)
 #pragma unroll
             for (int j = 0; j < ChunkDt<C>::QPL; ++j)
-                o.d[hh][j] = h0 + hh < prm.H
+                o.d[hh][j] = h0 + hh < prm.H && (!VL || tq + j < slen)
                                  ? __uint_as_float(
                                        (uint32_t)d16[(row0 + ChunkDt<C>::QPL * lane + j) * 8 + (h0 & 7) + hh] << 16)
                                  : 0.f;
@@ -611,10 +635,58 @@ __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint
 //   no TMEM: these CTAs share SMs with segment-state CTAs whose TMEM
 //   allocations fill the SM's 512 columns.
 // ===========================================================================
-template <class C>
-__global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CUtensorMap mb,
-                                                      const __grid_constant__ CUtensorMap mc, uint8_t *pack, int nc,
-                                                      int G, int nbatch, int nst, unsigned *ready, unsigned *status) {
+// The tiles of the C B^T pass in chunk-major order.  An equal-length batch:
+// tile t = (chunk c, batch b, group g), c slowest.  Packed sequences: chunk
+// level c holds chunk c of every sequence that long (the units are ordered
+// longest first, so these are the first units), vl_off[c] = the chunks
+// before level c (vl_off[nlvl] = all of them), then the group.
+struct CbWalk {
+    int nc, G, nbatch;
+    long long ntiles;
+    const VlUnit *vl;
+    const int *vl_off;
+    int nlvl;
+};
+
+struct CbTile {
+    int row, bq, g;  // first step's row and batch coordinate in the B / C maps, group
+    long long plane;  // pack and flag index
+};
+
+template <class C, bool VL>
+__device__ __forceinline__ CbTile cb_tile(const CbWalk &w, long long t) {
+    CbTile o;
+    if constexpr (!VL) {
+        const long long per_chunk = (long long)w.nbatch * w.G;
+        const int c = (int)(t / per_chunk), rem = (int)(t % per_chunk), b = rem / w.G;
+        o.g = rem % w.G;
+        o.row = c * C::Q;
+        o.bq = b;
+        o.plane = ((long long)b * w.nc + c) * w.G + o.g;
+        return o;
+    }
+    const int k = (int)(t / w.G);
+    o.g = (int)(t % w.G);
+    int lo = 0, hi = w.nlvl - 1;  // the last level whose first chunk is at or before k
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(w.vl_off + mid) <= k) lo = mid;
+        else hi = mid - 1;
+    }
+    const int i = k - __ldg(w.vl_off + lo);
+    const int t0 = __ldg(&w.vl[i].t0), cbase = __ldg(&w.vl[i].cbase);
+    o.row = t0 + lo * C::Q;
+    o.bq = 0;
+    o.plane = ((long long)cbase + lo) * w.G + o.g;
+    return o;
+}
+
+// (at most 72 registers: with segments a C B^T CTA shares its SM with two
+// segment-state CTAs of 384 threads at 72)
+template <class C, bool VL>
+__global__ void __maxnreg__(72) cb_mask_kernel(const __grid_constant__ CUtensorMap mb,
+                                                      const __grid_constant__ CUtensorMap mc, uint8_t *pack,
+                                                      const CbWalk walk, int nst, unsigned *ready, unsigned *status) {
     static_assert(C::Q == 64, "four warps of 16 rows");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -627,7 +699,7 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // tiles in chunk-major order (every batch and group of a chunk before the
     // next chunk), this CTA's every gridDim.x-th
-    const long long per_chunk = (long long)nbatch * G, ntiles = per_chunk * nc;
+    const long long ntiles = walk.ntiles;
     griddep_launch();
     if (tid == 32) {
         for (int s = 0; s < 2; ++s) mbar_init(&full_bar[s], 1);
@@ -636,11 +708,11 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
     __syncthreads();
     int nload[2] = {0, 0};  // loads issued per stage (thread 32)
     auto issue = [&](long long t, int s) {
-        const int c = (int)(t / per_chunk), rem = (int)(t % per_chunk), b = rem / G, g = rem % G;
+        const CbTile tl = cb_tile<C, VL>(walk, t);
         mbar_arrive_expect_tx(&full_bar[s], 2 * C::BC_BYTES);
         // one box each ([N/64][Q][64], 128-byte swizzle)
-        tma_load_5d(stage_c(s), &mc, &full_bar[s], 0, c * C::Q, 0, g, b);
-        tma_load_5d(stage_b(s), &mb, &full_bar[s], 0, c * C::Q, 0, g, b);
+        tma_load_5d(stage_c(s), &mc, &full_bar[s], 0, tl.row, 0, tl.g, tl.bq);
+        tma_load_5d(stage_b(s), &mb, &full_bar[s], 0, tl.row, 0, tl.g, tl.bq);
         ++nload[s];
     };
     if (tid == 32)
@@ -706,8 +778,7 @@ __global__ void __launch_bounds__(128) cb_mask_kernel(const __grid_constant__ CU
         fence_async_smem();
         __syncthreads();
         if (tid == 0) {
-            const int c = (int)(t / per_chunk), rem = (int)(t % per_chunk), b = rem / G, g = rem % G;
-            const long long plane = ((long long)b * nc + c) * G + g;
+            const long long plane = cb_tile<C, VL>(walk, t).plane;
             bulk_store(pack + plane * C::CBM_BYTES, cbs, C::CBM_BYTES);
             bulk_commit_group();
             bulk_wait_all();
@@ -842,7 +913,7 @@ __global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NB
         constexpr int QPL = C::Q / 32;
         const int hv = warp - 2;
         float after = 0.f;
-        DtFeed<C> feed{dt_ring + hv * C::DT_RING, dt_bar + 2 * hv, &mdt, b, h0, nch, 0};
+        DtFeed<C> feed{dt_ring + hv * C::DT_RING, dt_bar + 2 * hv, &mdt, b, h0, nch, 0, 0, prm.L};
         feed.start(prm, chunk_of);
         const float a = (h0 + hv < H && prm.A) ? prm.A[h0 + hv] : 0.f;
         // dt of the next chunk is read while this one is processed: the
@@ -1038,7 +1109,8 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
 // ===========================================================================
 constexpr int kComputeWarps = 16;  // warps 8..23
 
-template <class C, typename YT>
+// VL: the units are packed sequences (prm.vl)
+template <class C, typename YT, bool VL>
 __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mdt,
                       const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mb,
@@ -1065,8 +1137,21 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     const int seg = blockIdx.z, hblk = blockIdx.x, b = blockIdx.y;
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
-    const int c0 = seg * prm.cps;
-    const int nch = min(prm.nc, c0 + prm.cps) - c0;
+    // the unit's sequence: batch coordinate bq of the maps, first row t0,
+    // length slen, first pack plane pbase (per group), state index sidx
+    int bq = b, t0 = 0, sidx = b;
+    long long slen = prm.L, pbase = (long long)b * prm.nc;
+    int c0 = seg * prm.cps, nch = min(prm.nc, c0 + prm.cps) - c0;
+    if constexpr (VL) {
+        const VlUnit u = prm.vl[b];
+        bq = 0;
+        t0 = u.t0;
+        slen = u.len;
+        sidx = u.seq;
+        pbase = u.cbase;
+        c0 = 0;
+        nch = (u.len + C::Q - 1) / C::Q;
+    }
     const long long H = prm.H;
     auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
     auto stage_cb = [&](int s) { return smem + s * C::SCAN_STAGE + C::X_BYTES; };
@@ -1131,11 +1216,11 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                 for (int it = 0; it < nch; ++it) {
                     const int s = it % ST;
                     if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
-                    const long long plane = (((long long)b * prm.nc) + c0 + it) * prm.G + g;
+                    const long long plane = (pbase + c0 + it) * prm.G + g;
                     // the x box, then the pack (C B^T, B, C)
                     if (prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                     mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES);
-                    tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, (c0 + it) * C::Q, b);
+                    tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, t0 + (c0 + it) * C::Q, bq);
                     ++nload[s];
                     // once the C B^T kernel has published the tile's masked C B^T:
                     // it, and the tile's B and C from the inputs (no copy of a
@@ -1143,8 +1228,8 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                     if (!prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                     mbar_arrive_expect_tx(&pfull_bar[s], C::PACK_BYTES);
                     bulk_load(stage_cb(s), prm.pack + plane * C::CBM_BYTES, C::CBM_BYTES, &pfull_bar[s]);
-                    tma_load_5d(stage_b(s), &mb, &pfull_bar[s], 0, (c0 + it) * C::Q, 0, g, b);
-                    tma_load_5d(stage_c(s), &mc, &pfull_bar[s], 0, (c0 + it) * C::Q, 0, g, b);
+                    tma_load_5d(stage_b(s), &mb, &pfull_bar[s], 0, t0 + (c0 + it) * C::Q, 0, g, bq);
+                    tma_load_5d(stage_c(s), &mc, &pfull_bar[s], 0, t0 + (c0 + it) * C::Q, 0, g, bq);
                     ++npack[s];
                     TRACE(0, it);
                 }
@@ -1155,7 +1240,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
 #pragma unroll
             for (int hh = 0; hh < C::HB; ++hh) rho[hh] = 0.f;
             auto chunk_of = [&](int it) { return c0 + it; };
-            DtFeed<C> feed{dt_ring, dt_bar, &mdt, b, h0, nch, 0};
+            DtFeed<C, VL> feed{dt_ring, dt_bar, &mdt, bq, h0, nch, 0, t0, slen};
             feed.start(prm, chunk_of);
             float Ah[C::HB];
             load_decay<C>(prm, h0, Ah);
@@ -1394,7 +1479,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
             if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[9], 1, gtid, NT)) {
                 tc_fence_after();
                 const float sc = __expf(-rho_end);
-                float *dst = prm.fin + (((long long)b * H + hrow) * C::P + rp) * C::N;
+                float *dst = prm.fin + (((long long)sidx * H + hrow) * C::P + rp) * C::N;
                 if constexpr (C::SG == 1 && C::DT_RING >= 4 * 2048) {
                     // coalesced: each 16-column block goes through this warp's
                     // 2 KB of the dt ring (idle once the last chunk's vector
@@ -1460,7 +1545,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
             // (the 32 rows of a warp are 32 consecutive p of one head)
             const bool live = hrow < H;
             const float *dense = nullptr;  // a state in the row layout [.., P, N]: given, init, or init weighted
-            const long long rowoff = (((long long)b * H + (live ? hrow : 0)) * C::P + rp) * C::N;
+            const long long rowoff = (((long long)sidx * H + (live ? hrow : 0)) * C::P + rp) * C::N;
             if (prm.entering)
                 dense = prm.entering + ((((long long)b * prm.nseg + seg) * H + (live ? hrow : 0)) * C::P + rp) * C::N;
             else if (prm.init)
@@ -1609,9 +1694,21 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    tma_store_4d(&my, yt, (q4 * 32) % C::P, (int)(h0 + (q4 * 32) / C::P), (c0 + cp) * C::Q + part * NS, b);
-                    bulk_commit_group();
+                const long long trow = (long long)(c0 + cp) * C::Q + part * NS;  // step of the tile's first row
+                if (!VL || trow + NS <= slen) {
+                    if (lane == 0) {
+                        tma_store_4d(&my, yt, (q4 * 32) % C::P, (int)(h0 + (q4 * 32) / C::P), (int)(t0 + trow), bq);
+                        bulk_commit_group();
+                    }
+                } else if constexpr (VL) {
+                    // a packed sequence's partial last chunk: its rows stop at
+                    // the sequence's end (the next rows belong to the next one)
+                    if (h0 + (q4 * 32) / C::P < H) {
+                        YT *yg = static_cast<YT *>(prm.y) +
+                                 ((t0 + trow) * H + h0 + (q4 * 32) / C::P) * C::P + (q4 * 32) % C::P + lane;
+                        for (int j = 0; j < NS && trow + j < slen; ++j)
+                            yg[(long long)j * H * C::P] = yt[j * 32 + lane];
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1837,30 +1934,35 @@ cudaError_t raise_smem(const void *fn, int bytes, int &done) {
     return e;
 }
 
+// (walk: the packed sequences' tiles; null: the batch's)
 template <class C>
 cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pack, unsigned *ready, unsigned *status,
-                      cudaStream_t s, int ncta = 0, int nst_max = 2) {
+                      cudaStream_t s, int ncta = 0, int nst_max = 2, const CbWalk *walk = nullptr) {
     CUtensorMap mb, mc;
     if (!make_bt_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_bt_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
+    CbWalk w{(int)d.nc, (int)d.G, (int)d.b, (long long)d.nc * d.b * d.G, nullptr, nullptr, 0};
+    if (walk) w = *walk;
     // ncta > 0: that many CTAs walk the tiles, two stages deep (one CTA per SM
     // the scan leaves free); otherwise one CTA per tile
-    const long long ntiles = (long long)d.nc * d.b * d.G;
+    const long long ntiles = w.ntiles;
     const int nst = ncta > 0 && ncta < ntiles ? nst_max : 1;
     const unsigned grid = ncta > 0 && ncta < ntiles ? (unsigned)ncta : (unsigned)ntiles;
     const int smem = C::smem_cb(nst);
     static int attr = 0;
-    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(cb_mask_kernel<C>), C::smem_cb(2), attr);
+    auto kern = walk ? cb_mask_kernel<C, true> : cb_mask_kernel<C, false>;
+    static int attr_vl = 0;
+    cudaError_t e =
+        raise_smem<C>(reinterpret_cast<const void *>(kern), C::smem_cb(2), walk ? attr_vl : attr);
     if (e != cudaSuccess) return e;
-    e = launch_k(cb_mask_kernel<C>, dim3(grid), 128, smem, s, false, mb, mc, pack, (int)d.nc, (int)d.G, (int)d.b, nst,
-                 ready, status);
+    e = launch_k(kern, dim3(grid), 128, smem, s, false, mb, mc, pack, w, nst, ready, status);
     timing_mark(s, "cb_mask_tc");
     return e;
 }
 
 // pdl: the scan may start while the kernel before it on the stream (the
 // C B^T kernel, which publishes its packs through ready flags) still runs.
-template <class C>
+template <class C, bool VL = false>
 cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, const void *B, const void *Cm,
                         dim3 grid, const char *name, bool pdl, cudaStream_t s) {
     CUtensorMap mx, mdt = {}, my, mb, mc;
@@ -1876,20 +1978,20 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     // be met would wait forever)
     {
         cudaFuncAttributes fa;
-        cudaError_t e = f32 ? cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, float>)
-                            : cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, bf16>);
+        cudaError_t e = f32 ? cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, float, VL>)
+                            : cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, bf16, VL>);
         if (e != cudaSuccess) return e;
         if ((fa.numRegs + 7) / 8 * 8 != C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
     }
     cudaError_t e;
     if (f32) {
-        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float>), C::SMEM_SCAN, attr_f);
+        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float, VL>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
+        e = launch_k(chunk_scan_kernel<C, float, VL>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
     } else {
-        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16>), C::SMEM_SCAN, attr_b);
+        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16, VL>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16, VL>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
     }
     timing_mark(s, name);
     return e;
@@ -1985,6 +2087,104 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
     return launch_scan<C>(d, prm, ydtype, x, B, Cm, dim3(p.nhb, (unsigned)d.b, p.nseg), "chunk_scan_tc", true, s);
 }
 
+// ---------------------------------------------------------------------------
+// Packed sequences of unequal lengths in one launch set: a unit per
+// (sequence, head block), the longest sequences' units first.  The unit
+// table reaches the device as a kernel parameter of the setup kernel, which
+// also clears the pack flags (it takes the place of the flag memset).
+// ---------------------------------------------------------------------------
+struct VlArgs {
+    int n, nlvl;  // units; chunk levels (the longest unit's chunks)
+    VlUnit u[kVarlenMaxUnits];
+};
+static_assert(sizeof(VlArgs) <= 32000, "kernel parameter space");
+
+// vl_off[c] = the chunks of levels below c = sum over units of min(nc_i, c).
+template <int Q>
+__global__ void varlen_setup_kernel(const __grid_constant__ VlArgs a, VlUnit *vl, int *vl_off, unsigned *flags,
+                                    long long nflags) {
+    const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x, nthr = (long long)gridDim.x * blockDim.x;
+    for (long long i = tid; i < a.n; i += nthr) vl[i] = a.u[i];
+    for (long long c = tid; c <= a.nlvl; c += nthr) {
+        long long o = 0;
+        for (int i = 0; i < a.n; ++i) o += min((a.u[i].len + Q - 1) / Q, (int)c);
+        vl_off[c] = (int)o;
+    }
+    for (long long i = tid; i < nflags; i += nthr) flags[i] = 0u;
+}
+
+struct VlLayout {
+    size_t flags, pack, table, off, total;
+};
+
+template <class C>
+VlLayout varlen_layout(const Dims &d, int n, long long nchunks, int nlvl) {
+    VlLayout l;
+    const long long nplanes = nchunks * d.G;
+    l.flags = 0;
+    l.pack = align256(sizeof(unsigned) * nplanes);
+    l.table = l.pack + align256((size_t)C::CBM_BYTES * nplanes);
+    l.off = l.table + align256(sizeof(VlUnit) * n);
+    l.total = l.off + align256(sizeof(int) * (nlvl + 1));
+    return l;
+}
+
+// The units of the sequences (t0, len, seq), longest first, with their pack
+// planes; returns the total chunks and sets the level count.
+long long varlen_units(const VarlenSeq *seqs, int n, int Q, VlArgs &a) {
+    a.n = n;
+    a.nlvl = 0;
+    for (int i = 0; i < n; ++i) a.u[i] = VlUnit{seqs[i].t0, seqs[i].len, 0, seqs[i].seq};
+    std::stable_sort(a.u, a.u + n, [](const VlUnit &p, const VlUnit &q) { return p.len > q.len; });
+    long long k = 0;
+    for (int i = 0; i < n; ++i) {
+        const int nc = (a.u[i].len + Q - 1) / Q;
+        a.u[i].cbase = (int)k;
+        k += nc;
+        a.nlvl = std::max(a.nlvl, nc);
+    }
+    return k;
+}
+
+template <class C>
+cudaError_t run_fwd_varlen(const Dims &d, const VlArgs &a, long long nchunks, ssd_dtype_t ydtype, const void *x,
+                           const void *dt, const float *A, const void *B, const void *Cm, const float *D,
+                           const float *init, void *y, float *fin, void *ws, unsigned *status, cudaStream_t s) {
+    const VlLayout l = varlen_layout<C>(d, a.n, nchunks, a.nlvl);
+    char *w = static_cast<char *>(ws);
+    const long long nflags = nchunks * d.G;
+    TcParams prm = base_params(d, dt, status);
+    prm.x = static_cast<const bf16 *>(x);
+    prm.A = A;
+    prm.D = D;
+    prm.init = init;
+    prm.y = y;
+    prm.fin = fin;
+    prm.cb_ready = reinterpret_cast<unsigned *>(w + l.flags);
+    prm.pack = reinterpret_cast<uint8_t *>(w + l.pack);
+    prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
+    prm.nseg = 1;
+    prm.cps = (int)d.nc;
+    prm.nsub = 1;
+    prm.nslot = 1;
+    VlUnit *vl = reinterpret_cast<VlUnit *>(w + l.table);
+    int *vl_off = reinterpret_cast<int *>(w + l.off);
+    prm.vl = vl;
+    const long long work = std::max<long long>(std::max<long long>(nflags, a.nlvl + 1), a.n);
+    const unsigned blocks = (unsigned)std::min<long long>((work + 255) / 256, sm_count());
+    timing_begin(s);
+    varlen_setup_kernel<C::Q><<<blocks, 256, 0, s>>>(a, vl, const_cast<int *>(vl_off), prm.cb_ready, nflags);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    timing_mark(s, "varlen_setup");
+    const CbWalk walk{(int)d.nc, (int)d.G, 1, nflags, vl, vl_off, a.nlvl};
+    const long long units = (long long)a.n * prm.nhb, spare = sm_count() - units;
+    e = launch_cb<C>(d, B, Cm, reinterpret_cast<uint8_t *>(w + l.pack), prm.cb_ready, prm.status, s,
+                     spare >= 8 ? (int)spare : 0, 2, &walk);
+    if (e != cudaSuccess) return e;
+    return launch_scan<C, true>(d, prm, ydtype, x, B, Cm, dim3(prm.nhb, (unsigned)a.n, 1), "chunk_scan_tc", true, s);
+}
+
 // Dispatch over the compiled tile configurations.
 template <class F>
 bool dispatch(const Dims &d, F &&f) {
@@ -2041,6 +2241,72 @@ cudaError_t tc_fwd(const Dims &dq, ssd_dtype_t ydtype, const void *x, const void
     cudaError_t e = cudaErrorNotSupported;
     dispatch(d, [&](auto c) { e = run_fwd<decltype(c)>(d, ydtype, x, dt, A, B, C, D, init, y, fin, ws, status, s); });
     return e;
+}
+
+bool tc_varlen_supported(const Dims &dq, ssd_dtype_t dtype) {
+    if (!tc_fwd_supported(dq, dtype)) return false;
+    const Dims d = fwd_tiles(dq);
+    return d.b == 1 && d.L < (1ll << 30) && (d.L / 64 + kVarlenMaxUnits) * d.G < (1ll << 31);
+}
+
+size_t tc_varlen_workspace(const Dims &dq, const VarlenSeq *seqs, int n) {
+    const Dims d = fwd_tiles(dq);
+    if (n <= 0 || n > kVarlenMaxUnits) return 0;
+    thread_local VlArgs a;
+    const long long k = varlen_units(seqs, n, (int)d.Q, a);
+    size_t bytes = 0;
+    dispatch(d, [&](auto c) { bytes = varlen_layout<decltype(c)>(d, n, k, a.nlvl).total; });
+    return bytes;
+}
+
+cudaError_t tc_fwd_varlen(const Dims &dq, const VarlenSeq *seqs, int n, ssd_dtype_t ydtype, const void *x,
+                          const void *dt, const float *A, const void *B, const void *C, const float *D,
+                          const float *init, void *y, float *fin, void *ws, unsigned *status, cudaStream_t s) {
+    const Dims d = fwd_tiles(dq);
+    if (n <= 0 || n > kVarlenMaxUnits) return cudaErrorInvalidValue;
+    thread_local VlArgs a;  // (the launch copies it into its parameters)
+    const long long k = varlen_units(seqs, n, (int)d.Q, a);
+    cudaError_t e = cudaErrorNotSupported;
+    dispatch(d, [&](auto c) {
+        e = run_fwd_varlen<decltype(c)>(d, a, k, ydtype, x, dt, A, B, C, D, init, y, fin, ws, status, s);
+    });
+    return e;
+}
+
+// The model: a scan CTA takes about kChunkUs per 64-step tile (N = 128;
+// N = 256 about 1.35 times that), one wave of units after another; a launch
+// set adds a fixed cost; a fused forward with segments adds its
+// segment-state pass (about half the scan's time per chunk).
+namespace {
+constexpr double kChunkUs = 2.0, kSetUs = 8.0, kFwdUs = 16.0, kSegFrac = 0.6;
+double chunk_us(const Dims &d) { return d.N > 128 ? 1.35 * kChunkUs : kChunkUs; }
+}  // namespace
+
+double tc_varlen_cost_us(const Dims &dq, const VarlenSeq *seqs, int n) {
+    const Dims d = fwd_tiles(dq);
+    int nhb = 1;
+    dispatch(d, [&](auto c) { nhb = (int)((d.H + decltype(c)::HB - 1) / decltype(c)::HB); });
+    long long maxc = 0, sum = 0;
+    for (int i = 0; i < n; ++i) {
+        const long long nc = (seqs[i].len + d.Q - 1) / d.Q;
+        maxc = std::max(maxc, nc);
+        sum += nc;
+    }
+    const long long sms = sm_count(), waves = (sum * nhb + sms - 1) / sms;
+    return kSetUs + chunk_us(d) * (double)std::max(maxc, waves);
+}
+
+double tc_fwd_cost_us(const Dims &dq, int64_t len) {
+    Dims d = fwd_tiles(dq);
+    d.b = 1;
+    d.L = len;
+    d.nc = (len + d.Q - 1) / d.Q;
+    double us = 0;
+    dispatch(d, [&](auto c) {
+        const Plan p = plan_for<decltype(c)>(d);
+        us = kFwdUs + chunk_us(d) * p.cps * (p.nseg > 1 ? 1.0 + kSegFrac : 1.0);
+    });
+    return us;
 }
 
 bool tc_stage_supported(const Dims &dq, ssd_dtype_t dtype) {

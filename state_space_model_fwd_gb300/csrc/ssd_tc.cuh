@@ -26,6 +26,25 @@ cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, cons
                           const float *cum, const float *states_in, const float *D, void *y, void *ws,
                           unsigned *status, uint64_t selftest_ns, cudaStream_t s);
 
+// Packed sequences of unequal lengths (ssd_fwd_varlen) in one launch set:
+// `d` is the packed batch (b = 1, L = all steps); each sequence is its first
+// row t0 in the packed tensors, its steps len (> 0) and its index seq (its
+// init / fin state).  At most kVarlenMaxUnits sequences per call.
+constexpr int kVarlenMaxUnits = 1024;
+struct VarlenSeq {
+    int t0, len, seq;
+};
+bool tc_varlen_supported(const Dims &d, ssd_dtype_t dtype);
+size_t tc_varlen_workspace(const Dims &d, const VarlenSeq *seqs, int n);
+cudaError_t tc_fwd_varlen(const Dims &d, const VarlenSeq *seqs, int n, ssd_dtype_t ydtype, const void *x,
+                          const void *dt, const float *A, const void *B, const void *C, const float *D,
+                          const float *init, void *y, float *fin, void *ws, unsigned *status, cudaStream_t s);
+// Estimated device time in microseconds of one launch set over the
+// sequences, and of the fused forward of one sequence of `len` steps (the
+// choice between them in ssd_fwd_varlen; a model, not a measurement).
+double tc_varlen_cost_us(const Dims &d, const VarlenSeq *seqs, int n);
+double tc_fwd_cost_us(const Dims &d, int64_t len);
+
 // Quadratic (dual) form for short sequences (ssd_quad.cu).
 bool quad_supported(const Dims &d, ssd_dtype_t dtype);
 cudaError_t quad_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void *dt, const float *A, const void *B,

@@ -181,12 +181,34 @@ def test_decode_step_validates(lib):
     assert lib.ssd_decode_step(ctypes.byref(shape(batch=0)), *([None] * 8), None) == OK
 
 
+CBM = 64 * 64 * 2  # one chunk's masked C B^T (64 x 64 bf16)
+
+
+def test_varlen_plan_splits_off_long_sequences(lib):
+    """One long sequence among short ones runs as a fused forward of its own
+    (its segments fill the SMs), the short ones as one launch set: the
+    workspace is the larger of the two (152 SMs assumed without a GPU)."""
+    i64 = ctypes.c_int64
+    lens = [100, 4096, 37, 64, 1]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    s = shape(batch=1, seqlen=cu[-1], nheads=8)
+    arr = (i64 * len(cu))(*cu)
+    own = lib.ssd_fwd_workspace_size(ctypes.byref(shape(batch=1, seqlen=4096, nheads=8)))
+    chunks = 2 + 1 + 1 + 1
+    rest = 256 + chunks * CBM + 256 + 256
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), arr, len(lens)) == max(own, rest)
+    assert own > rest
+
+
 def test_varlen_validates(lib):
     i64 = ctypes.c_int64
     s = shape(batch=1, seqlen=300)
     good = (i64 * 4)(0, 100, 164, 300)
-    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), good, 3) == lib.ssd_fwd_workspace_size(
-        ctypes.byref(shape(batch=1, seqlen=136)))
+    # three short sequences run as one launch set: flags | packs of their
+    # 2 + 1 + 3 chunks | unit table | chunk-level offsets, each 256-aligned
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), good, 3) == 256 + 6 * CBM + 256 + 256
     for bad in ((0, 100, 90, 300), (1, 100, 164, 300), (0, 100, 164, 299)):
         arr = (i64 * 4)(*bad)
         assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), arr, 3) == 0

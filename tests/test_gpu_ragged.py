@@ -12,6 +12,7 @@ import torch
 import oracle
 import ssd_inputs as si
 import state_space_model_fwd_gb300 as ssd
+from tests.test_gpu_parity import check_bf16_y
 
 pytestmark = pytest.mark.gpu
 
@@ -122,3 +123,64 @@ def test_varlen_packed_batch(dtype, chunk):
         if e > a:
             assert rel_err(to_np(y[:, a:e]), y_ref) <= tol, s
         assert rel_err(to_np(fins[s:s + 1]), fin_ref) <= tol, s
+
+
+# Packed batches that run as one launch set (a chunk-scan unit per sequence
+# and head block, the C B^T pass walking every sequence's chunks), or, for
+# the last, the longest sequence as a fused forward of its own and the rest
+# as one launch set.  (name, H, P, N, G, chunk, lengths, kernels expected;
+# the lengths keep every sequence's dt 16-byte aligned: even starts for H = 4,
+# multiples of 4 for H = 6)
+VARLEN_SETS = [
+    ("short_many", 8, 64, 128, 2, 64, [1, 63, 64, 65, 100, 129, 7, 200, 31, 64] * 4, {"varlen_setup"}),
+    ("short_q128", 8, 64, 128, 2, 128, [300, 1, 128, 129, 77, 256, 40], {"varlen_setup"}),
+    ("wide_head", 4, 128, 256, 2, 64, [70, 6, 130, 64, 2, 190], {"varlen_setup"}),
+    ("h6_plain_dt", 6, 64, 64, 3, 64, [100, 36, 200, 4, 64, 0, 8], {"varlen_setup"}),
+    ("long_and_short", 8, 64, 128, 1, 64, [100, 37] * 5 + [4096] + [64, 1] * 5,
+     {"varlen_setup", "seg_state_tc"}),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN_SETS, ids=[c[0] for c in VARLEN_SETS])
+@pytest.mark.parametrize("ydt", [torch.float32, torch.bfloat16], ids=["y_f32", "y_bf16"])
+def test_varlen_launch_set(case, ydt):
+    """Every sequence of a packed batch against the oracle run on it alone
+    (from its own initial state); y starts as NaN, so a row left unwritten
+    fails; the launch list shows which path ran.  bf16 y: 1e-2 x RMS beyond
+    half a bf16 ulp of each value (the store's rounding)."""
+    name, H, P, N, G, chunk, lens, kernels = case
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    cfg = si.SSDConfig("varlen_" + name, 1, cu[-1], H, P, N, G, chunk, "bf16", False, 811)
+    inp = si.make_inputs(cfg)
+    t = inp.to_torch("cuda")
+    init = 0.1 * torch.randn(len(lens), H, P, N, device="cuda", generator=torch.Generator("cuda").manual_seed(12))
+    y = torch.full(t["x"].shape, float("nan"), device="cuda", dtype=ydt)
+    fins = torch.full((len(lens), H, P, N), float("nan"), device="cuda")
+    ssd.launch_timing(True)
+    try:
+        ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], init, cu, chunk_size=chunk, y=y,
+                           final_states=fins)
+        torch.cuda.synchronize()
+        names = {n for n, _ in ssd.launch_times_ms()}
+    finally:
+        ssd.launch_timing(False)
+    ssd.check_device_status()
+    assert kernels <= names, names
+    if "seg_state_tc" not in kernels:
+        assert "seg_state_tc" not in names, names
+    f = inp.as_f64()
+    ini = init.double().cpu().numpy()
+    tol = TOL["bf16"]
+    errs = []
+    for s, (a, e) in enumerate(zip(cu[:-1], cu[1:])):
+        y_ref, fin_ref = oracle.ssd_recurrence(f["x"][:, a:e], f["dt"][:, a:e], f["A"], f["B"][:, a:e],
+                                               f["C"][:, a:e], f["D"], ini[s:s + 1])
+        if e > a:
+            if ydt == torch.bfloat16:
+                errs.append(check_bf16_y(to_np(y[:, a:e]), y_ref, tol, f"sequence {s}")[1])
+            else:
+                errs.append(rel_err(to_np(y[:, a:e]), y_ref))
+                assert errs[-1] <= tol, (s, errs[-1])
+        assert rel_err(to_np(fins[s:s + 1]), fin_ref) <= tol, s
+    print(f"{name} {ydt}: max err / RMS over {len(lens)} sequences {max(errs):.2e}"
+          + (" (beyond half a bf16 ulp)" if ydt == torch.bfloat16 else ""))
