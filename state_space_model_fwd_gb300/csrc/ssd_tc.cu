@@ -2273,13 +2273,18 @@ cudaError_t tc_fwd_varlen(const Dims &dq, const VarlenSeq *seqs, int n, ssd_dtyp
     return e;
 }
 
-// The model: a scan CTA takes about kChunkUs per 64-step tile (N = 128;
-// N = 256 about 1.35 times that), one wave of units after another; a launch
-// set adds a fixed cost; a fused forward with segments adds its
-// segment-state pass (about half the scan's time per chunk).
+// The model, fitted to GB300 timings of the 130M-shaped heads (one sequence
+// of 128 to 8192 steps; sets of 4 to 256 sequences), within ~12 %:
+//   a launch set: kSetUs + max(the longest unit, ceil(units / SMs) x the
+//     mean unit), a unit (one scan CTA) taking kUnitUs + kSetChunkUs per
+//     64-step tile;
+//   a fused forward: kFwdUs + kFwdChunkUs per tile of a segment +
+//     kPrevUs per local state the last segment's prologue combines.
+// Tile costs scale by 1.35 for N = 256.
 namespace {
-constexpr double kChunkUs = 2.0, kSetUs = 8.0, kFwdUs = 16.0, kSegFrac = 0.6;
-double chunk_us(const Dims &d) { return d.N > 128 ? 1.35 * kChunkUs : kChunkUs; }
+constexpr double kSetUs = 8.0, kUnitUs = 6.5, kSetChunkUs = 1.7;
+constexpr double kFwdUs = 17.6, kFwdChunkUs = 2.1, kPrevUs = 0.75;
+double n_scale(const Dims &d) { return d.N > 128 ? 1.35 : 1.0; }
 }  // namespace
 
 double tc_varlen_cost_us(const Dims &dq, const VarlenSeq *seqs, int n) {
@@ -2292,8 +2297,11 @@ double tc_varlen_cost_us(const Dims &dq, const VarlenSeq *seqs, int n) {
         maxc = std::max(maxc, nc);
         sum += nc;
     }
-    const long long sms = sm_count(), waves = (sum * nhb + sms - 1) / sms;
-    return kSetUs + chunk_us(d) * (double)std::max(maxc, waves);
+    if (n == 0) return 0.0;
+    const double tile = kSetChunkUs * n_scale(d);
+    const long long units = (long long)n * nhb, sms = sm_count(), waves = (units + sms - 1) / sms;
+    const double longest = kUnitUs + tile * (double)maxc, mean = kUnitUs + tile * (double)sum / n;
+    return kSetUs + std::max(longest, (double)waves * mean);
 }
 
 double tc_fwd_cost_us(const Dims &dq, int64_t len) {
@@ -2304,7 +2312,7 @@ double tc_fwd_cost_us(const Dims &dq, int64_t len) {
     double us = 0;
     dispatch(d, [&](auto c) {
         const Plan p = plan_for<decltype(c)>(d);
-        us = kFwdUs + chunk_us(d) * p.cps * (p.nseg > 1 ? 1.0 + kSegFrac : 1.0);
+        us = kFwdUs + kFwdChunkUs * n_scale(d) * p.cps + kPrevUs * (p.nseg - 1) * p.nsub;
     });
     return us;
 }
