@@ -806,6 +806,7 @@ VARLEN_MIXES = {
     # 8192 tokens of the 130M-shaped layer in each, like the b=4, L=2048 batch
     "ragged4": [3001, 1500, 2600, 1091],
     "short64": [100, 156] * 32,
+    "long_and_short": [4096] + [128] * 32,
 }
 
 
@@ -833,11 +834,16 @@ def varlen_sweep(ssd, dev, flush, peaks, steps):
             ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], None, cu, base.chunk_size,
                                y=y, final_states=fins, workspace=ws)
 
+        ssd.launch_timing(True)
+        run()
+        torch.cuda.synchronize()
+        launches = [n for n, _ in ssd.launch_times_ms()]
+        ssd.launch_timing(False)
         ms = time_graph(run, flush, steps)
         nbytes = (cu[-1] * H * P * 2 + cu[-1] * H * 2 + 2 * cu[-1] * G * N * 2 + 2 * H * 4
                   + cu[-1] * H * P * 2 + len(lens) * H * P * N * 4)
         rows[name] = {"nseq": len(lens), "tokens": cu[-1], "min_len": min(lens), "max_len": max(lens),
-                      "ms": ms, "tokens_per_s": cu[-1] / (ms * 1e-3), "bytes": nbytes,
+                      "launches": launches, "ms": ms, "tokens_per_s": cu[-1] / (ms * 1e-3), "bytes": nbytes,
                       "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         del t, y, fins, ws
     t = si.make_inputs(base).to_torch(dev)

@@ -181,11 +181,13 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, co
  * starts from init_states[s] (NULL: zero) and ends in final_states[s] (NULL:
  * not written), both [nseq, H, P, N] fp32.  No state crosses a sequence
  * boundary.  On the tensor-core path (bf16 inputs and a tile shape it
- * covers) the sequences run in launch sets of up to 1024: one chunk-scan CTA
+ * covers) the sequences run in launch sets of up to 960: a chunk-scan CTA
  * per (sequence, head block), longest first, with the C B^T pass walking
- * every sequence's chunks; the longest sequences may instead run the fused
- * forward of ssd_fwd each (with segments that fill the SMs), whichever a
- * host-side cost model of the two rates faster.  A sequence's partial last
+ * every sequence's chunks; when those CTAs leave SMs free, every sequence is
+ * cut into segments of the same chunk count (a segment-state pass forms the
+ * earlier segments' local states, as in ssd_fwd).  The longest sequences
+ * may instead run the fused forward of ssd_fwd each, whichever a host-side
+ * cost model rates faster.  A sequence's partial last
  * chunk then reads the next sequence's first steps and gives them dt = 0, so
  * they add 0 times their values: finite inputs leave no trace across the
  * boundary (a non-finite x or B there would).  Other inputs run the

@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <vector>
 
 #include "ssd_tc.cuh"
 #include "tc_ptx.cuh"
@@ -57,12 +58,17 @@ constexpr uint64_t kWaitNs = 100000000ull;    // a wait gives up after 0.1 s
 constexpr uint64_t kDrainNs = 20000000ull;    // the exit drain gives up after 0.02 s
 constexpr float kLambda = 64.f;               // |exponent| bound of the scaled operands
 
-// One sequence of a packed batch of unequal lengths (x, dt, B, C, y as one
-// [1, Ltot, ..] tensor): its steps are rows t0 .. t0 + len - 1, its chunk
-// packs and flags start at plane cbase (times G), its states are init /
-// fin [seq].  The chunk scan runs one unit per blockIdx.y.
+// A packed batch of sequences of unequal lengths (x, dt, B, C, y as one
+// [1, Ltot, ..] tensor).  A sequence: its steps are rows t0 .. t0 + len - 1,
+// its chunk packs and flags start at plane cbase (times G), its states are
+// init / fin [seq].  A unit of the chunk scan (blockIdx.y) or of the
+// segment-state pass (blockIdx.z) adds its chunks c0 .. c0 + nch - 1 of the
+// sequence; for the scan, slot = the sequence's first local-state slot and
+// nprev = the local states before its segment (0: the first segment); for
+// the segment-state pass, slot = the slot it writes.
 struct VlUnit {
     int t0, len, cbase, seq;
+    int c0, nch, slot, nprev;
 };
 
 struct TcParams {
@@ -104,9 +110,11 @@ struct TcParams {
     // the state warps of segments > 0 wait for it before reading the states
     // entering them
     int dep_seg;
-    // packed sequences (null: the equal-length batch b); one segment each,
-    // blockIdx.y = the unit
+    // packed sequences (null: the equal-length batch b): the scan's units
+    // at vl[vl_scan0 + blockIdx.y], the segment-state pass's at
+    // vl[vl_seg0 + blockIdx.z]
     const VlUnit *vl;
+    int vl_scan0, vl_seg0;
 };
 
 template <int P_, int N_, int Q_>
@@ -614,14 +622,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 template <class C>
 __device__ __forceinline__ void issue_chunk_loads(uint8_t *xs, uint8_t *bs, uint8_t *cs, uint64_t *bar,
                                                   const CUtensorMap *mx, const CUtensorMap *mb,
-                                                  const CUtensorMap *mc, int h0, int g, int c, int b) {
-    tma_load_5d(xs, mx, bar, 0, 0, h0, c * C::Q, b);  // x: [Q][HB][PB][64], 256 contiguous bytes per step
+                                                  const CUtensorMap *mc, int h0, int g, int c, int b, int t0 = 0) {
+    const int row = t0 + c * C::Q;
+    tma_load_5d(xs, mx, bar, 0, 0, h0, row, b);  // x: [Q][HB][PB][64], 256 contiguous bytes per step
 #pragma unroll
-    for (int nb = 0; nb < C::N / 64; ++nb) tma_load_4d(bs + nb * (C::Q * 128), mb, bar, nb * 64, g, c * C::Q, b);
+    for (int nb = 0; nb < C::N / 64; ++nb) tma_load_4d(bs + nb * (C::Q * 128), mb, bar, nb * 64, g, row, b);
     if (cs)
 #pragma unroll
         for (int nb = 0; nb < C::N / 64; ++nb)
-            tma_load_4d(cs + nb * (C::Q * 128), mc, bar, nb * 64, g, c * C::Q, b);
+            tma_load_4d(cs + nb * (C::Q * 128), mc, bar, nb * 64, g, row, b);
 }
 
 // ===========================================================================
@@ -821,7 +830,8 @@ struct SegT {
     static_assert(NBG == 4 || C::N + 2 * C::Q <= 256, "two A buffers and S in 256 columns");
 };
 
-template <class C, int NBG>
+// VL: the units are packed sequences' sub-segments (prm.vl)
+template <class C, int NBG, bool VL>
 __global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NBG>::MAXREG))
     seg_state_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mb,
                      const __grid_constant__ CUtensorMap mdt, TcParams prm) {
@@ -845,11 +855,24 @@ __global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NB
     const int seg = blockIdx.z, hblk = blockIdx.x, b = blockIdx.y;
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
-    // sub-segment `seg` of segment seg / nsub
+    // sub-segment `seg` of segment seg / nsub, written to slot `seg` of batch
+    // entry b; a packed sequence's unit names its chunks and its slot (of
+    // batch entry 0)
     const int csub = (prm.cps + prm.nsub - 1) / prm.nsub;
     const int sbeg = (seg / prm.nsub) * prm.cps;
-    const int c0 = sbeg + (seg % prm.nsub) * csub;
-    const int nch = min(min(prm.nc, sbeg + prm.cps), c0 + csub) - c0;
+    int c0 = sbeg + (seg % prm.nsub) * csub;
+    int nch = min(min(prm.nc, sbeg + prm.cps), c0 + csub) - c0;
+    int bq = b, t0 = 0, sslot = seg;
+    long long slen = prm.L;
+    if constexpr (VL) {
+        const VlUnit u = prm.vl[prm.vl_seg0 + seg];
+        c0 = u.c0;
+        nch = u.nch;
+        bq = 0;
+        t0 = u.t0;
+        slen = u.len;
+        sslot = u.slot;
+    }
     const long long H = prm.H;
     // the segment's chunks are taken last to first, so the decay of the
     // chunks after each one (its weights' offset) accumulates as they come
@@ -903,7 +926,8 @@ __global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NB
                 const int s = it % ST, c = chunk_of(it);
                 if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
                 mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES + C::BC_BYTES);
-                issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c, b);
+                issue_chunk_loads<C>(stage_x(s), stage_b(s), nullptr, &full_bar[s], &mx, &mb, nullptr, h0, g, c, bq,
+                                     t0);
                 ++nload[s];
                 TRACE(18, it);
             }
@@ -913,7 +937,7 @@ __global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NB
         constexpr int QPL = C::Q / 32;
         const int hv = warp - 2;
         float after = 0.f;
-        DtFeed<C> feed{dt_ring + hv * C::DT_RING, dt_bar + 2 * hv, &mdt, b, h0, nch, 0, 0, prm.L};
+        DtFeed<C, VL> feed{dt_ring + hv * C::DT_RING, dt_bar + 2 * hv, &mdt, bq, h0, nch, 0, t0, slen};
         feed.start(prm, chunk_of);
         const float a = (h0 + hv < H && prm.A) ? prm.A[h0 + hv] : 0.f;
         // dt of the next chunk is read while this one is processed: the
@@ -946,7 +970,8 @@ __global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NB
         }
         feed.drain();
         // total dt*A of the segment, for the pass across segments
-        if (lane == 0 && h0 + hv < H && prm.seg_tot) prm.seg_tot[((long long)b * H + h0 + hv) * prm.nslot + seg] = after;
+        if (lane == 0 && h0 + hv < H && prm.seg_tot)
+            prm.seg_tot[((long long)bq * H + h0 + hv) * prm.nslot + sslot] = after;
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         // (the whole warp runs the loop, so its descriptors stay
@@ -1015,7 +1040,7 @@ __global__ void __launch_bounds__(SegT<C, NBG>::THREADS) __maxnreg__((SegT<C, NB
         const long long hrow = h0 + rh;
         if (group_wait(&done_bar, 0, &abort_sh, &slot[3], 1, gtid, NAB)) {
             tc_fence_after();
-            const long long blk0 = (((long long)b * prm.nslot + seg) * H + hrow) * C::P * C::N;
+            const long long blk0 = (((long long)bq * prm.nslot + sslot) * H + hrow) * C::P * C::N;
             // element n of this row: at 4 (n/4) P + n%4 in the column-block
             // layout, at n in the row layout
             float *dst = prm.seg_state + blk0 + (prm.seg_cl ? rp * 4 : rp * C::N);
@@ -1138,19 +1163,28 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     const int h0 = hblk * C::HB;
     const int g = (int)(prm.G == 1 ? 0 : h0 / prm.hpg);
     // the unit's sequence: batch coordinate bq of the maps, first row t0,
-    // length slen, first pack plane pbase (per group), state index sidx
+    // length slen, first pack plane pbase (per group), state index sidx; its
+    // segment: first local-state slot slot0 of the sequence, the local
+    // states before it nprev, whether it follows others (segk > 0) and
+    // whether it ends the sequence
     int bq = b, t0 = 0, sidx = b;
     long long slen = prm.L, pbase = (long long)b * prm.nc;
     int c0 = seg * prm.cps, nch = min(prm.nc, c0 + prm.cps) - c0;
+    int segk = seg, slot0 = 0, nprev = seg * prm.nsub;
+    bool last = seg == prm.nseg - 1;
     if constexpr (VL) {
-        const VlUnit u = prm.vl[b];
+        const VlUnit u = prm.vl[prm.vl_scan0 + b];
         bq = 0;
         t0 = u.t0;
         slen = u.len;
         sidx = u.seq;
         pbase = u.cbase;
-        c0 = 0;
-        nch = (u.len + C::Q - 1) / C::Q;
+        c0 = u.c0;
+        nch = u.nch;
+        segk = u.nprev > 0 ? 1 : 0;
+        slot0 = u.slot;
+        nprev = u.nprev;
+        last = c0 + nch >= (u.len + C::Q - 1) / C::Q;
     }
     const long long H = prm.H;
     auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
@@ -1475,7 +1509,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
             }
         }
         // final state after the segment's last chunk: S = exp(-rho) Ss
-        if (seg == prm.nseg - 1 && prm.fin) {  // (a uniform test: group_wait handles an abort)
+        if (last && prm.fin) {  // (a uniform test: group_wait handles an abort)
             if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[9], 1, gtid, NT)) {
                 tc_fence_after();
                 const float sc = __expf(-rho_end);
@@ -1541,7 +1575,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
         // totals T_j:
         //   S_in = e^{T_0 + .. + T_{k-1}} init + sum_j e^{T_{j+1} + .. + T_{k-1}} L_j
         {
-            if (prm.dep_seg && seg > 0) griddep_wait();
+            if (prm.dep_seg && segk > 0) griddep_wait();
             // (the 32 rows of a warp are 32 consecutive p of one head)
             const bool live = hrow < H;
             const float *dense = nullptr;  // a state in the row layout [.., P, N]: given, init, or init weighted
@@ -1551,12 +1585,15 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
             else if (prm.init)
                 dense = prm.init + rowoff;
             // after segment 0 the local states are in the column-block layout
-            const bool pass = !prm.entering && seg > 0;
+            // (nprev of them before this segment: its earlier sub-segments)
+            const bool pass = !prm.entering && segk > 0;
             const long long sstride = H * C::P * C::N;
             const float *loc =
-                pass ? prm.seg_state + (((long long)b * prm.nslot) * H + (live ? hrow : 0)) * C::P * C::N + rp * 4 : nullptr;
-            const float *tot = pass ? prm.seg_tot + ((long long)b * H + (live ? hrow : 0)) * prm.nslot : nullptr;
-            const int nprev = seg * prm.nsub;  // local states before this segment (its earlier sub-segments)
+                pass ? prm.seg_state + (((long long)bq * prm.nslot + slot0) * H + (live ? hrow : 0)) * C::P * C::N +
+                           rp * 4
+                     : nullptr;
+            const float *tot =
+                pass ? prm.seg_tot + ((long long)bq * H + (live ? hrow : 0)) * prm.nslot + slot0 : nullptr;
             float ttot = 0.f;  // T_0 + .. + T_{k-1}
             if (pass && live)
                 for (int j = 0; j < nprev; ++j) ttot += __ldcg(tot + j);
@@ -1997,7 +2034,7 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     return e;
 }
 
-template <class C, int NBG = 4>
+template <class C, int NBG = 4, bool VL = false>
 cudaError_t launch_seg_state(const Dims &d, TcParams prm, const void *x, const void *B, dim3 grid,
                              const char *name, bool pdl, cudaStream_t s) {
     CUtensorMap mx, mb, mdt = {};
@@ -2006,9 +2043,9 @@ cudaError_t launch_seg_state(const Dims &d, TcParams prm, const void *x, const v
     prm.dt_tma = make_dt_map(&mdt, prm.dt, d.H, d.L, d.b, C::Q) ? 1 : 0;
     const int smem = SegT<C, NBG>::SMEM;
     static int attr = 0;
-    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(seg_state_kernel<C, NBG>), smem, attr);
+    cudaError_t e = raise_smem<C>(reinterpret_cast<const void *>(seg_state_kernel<C, NBG, VL>), smem, attr);
     if (e != cudaSuccess) return e;
-    e = launch_k(seg_state_kernel<C, NBG>, grid, SegT<C, NBG>::THREADS, smem, s, pdl, mx, mb, mdt, prm);
+    e = launch_k(seg_state_kernel<C, NBG, VL>, grid, SegT<C, NBG>::THREADS, smem, s, pdl, mx, mb, mdt, prm);
     timing_mark(s, name);
     return e;
 }
@@ -2088,23 +2125,28 @@ cudaError_t run_fwd(const Dims &d, ssd_dtype_t ydtype, const void *x, const void
 }
 
 // ---------------------------------------------------------------------------
-// Packed sequences of unequal lengths in one launch set: a unit per
-// (sequence, head block), the longest sequences' units first.  The unit
-// table reaches the device as a kernel parameter of the setup kernel, which
-// also clears the pack flags (it takes the place of the flag memset).
+// Packed sequences of unequal lengths in one launch set: the sequences
+// longest first, each cut into segments of cps chunks (one segment each when
+// their units fill the SMs), a scan unit per (segment, head block) and a
+// segment-state unit per sub-segment of every segment but a sequence's last.
+// The table reaches the device as a kernel parameter of the setup kernel,
+// which also clears the pack flags (it takes the place of the flag memset):
+// [0, n) the sequences (the C B^T walk; without segments also the scan's
+// units), then the scan units, then the segment-state units.
 // ---------------------------------------------------------------------------
+constexpr int kVlEntries = kVarlenMaxUnits;
 struct VlArgs {
-    int n, nlvl;  // units; chunk levels (the longest unit's chunks)
-    VlUnit u[kVarlenMaxUnits];
+    int n, nlvl, ntotal;  // sequences; chunk levels (the longest sequence's chunks); entries
+    VlUnit u[kVlEntries];
 };
-static_assert(sizeof(VlArgs) <= 32000, "kernel parameter space");
+static_assert(sizeof(VlArgs) <= 31 * 1024, "kernel parameter space");
 
-// vl_off[c] = the chunks of levels below c = sum over units of min(nc_i, c).
+// vl_off[c] = the chunks of levels below c = sum over sequences of min(nc_i, c).
 template <int Q>
 __global__ void varlen_setup_kernel(const __grid_constant__ VlArgs a, VlUnit *vl, int *vl_off, unsigned *flags,
                                     long long nflags) {
     const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x, nthr = (long long)gridDim.x * blockDim.x;
-    for (long long i = tid; i < a.n; i += nthr) vl[i] = a.u[i];
+    for (long long i = tid; i < a.ntotal; i += nthr) vl[i] = a.u[i];
     for (long long c = tid; c <= a.nlvl; c += nthr) {
         long long o = 0;
         for (int i = 0; i < a.n; ++i) o += min((a.u[i].len + Q - 1) / Q, (int)c);
@@ -2113,46 +2155,122 @@ __global__ void varlen_setup_kernel(const __grid_constant__ VlArgs a, VlUnit *vl
     for (long long i = tid; i < nflags; i += nthr) flags[i] = 0u;
 }
 
-struct VlLayout {
-    size_t flags, pack, table, off, total;
+// The shape of one launch set.
+struct VlPlan {
+    int n = 0, nlvl = 0;
+    long long nchunks = 0;
+    int cps = 0, nsub = 1;  // chunks per segment (the longest sequence's: no segments), sub-segments
+    int nscan = 0, nsegu = 0, maxseg = 1;  // units of the scan and of the segment-state pass; most segments
+    bool segmented() const { return nsegu > 0; }
 };
 
 template <class C>
-VlLayout varlen_layout(const Dims &d, int n, long long nchunks, int nlvl) {
+VlPlan varlen_plan(const VarlenSeq *seqs, int n, int H) {
+    VlPlan p;
+    p.n = n;
+    for (int i = 0; i < n; ++i) {
+        const int nc = (seqs[i].len + C::Q - 1) / C::Q;
+        p.nchunks += nc;
+        p.nlvl = std::max(p.nlvl, nc);
+    }
+    const long long nhb = (H + C::HB - 1) / C::HB, sms = sm_count();
+    auto units = [&](int cps) {
+        long long u = 0;
+        for (int i = 0; i < n; ++i) u += ((seqs[i].len + C::Q - 1) / C::Q + cps - 1) / cps;
+        return u;
+    };
+    // the fewest chunks per segment whose scan units fit the SMs
+    p.cps = p.nlvl;
+    if ((long long)n * nhb < sms) {
+        int lo = 1, hi = p.nlvl;
+        while (lo < hi) {
+            const int mid = (lo + hi) / 2;
+            if (units(mid) * nhb <= sms) hi = mid;
+            else lo = mid + 1;
+        }
+        p.cps = lo;
+    }
+    p.nscan = (int)units(p.cps);
+    if (p.cps < p.nlvl) {
+        p.nsub = (p.cps >= 2 && C::N + 2 * C::Q <= 256) ? 2 : 1;
+        p.nsegu = (int)(p.nscan - n) * p.nsub;
+        p.maxseg = (p.nlvl + p.cps - 1) / p.cps;
+    }
+    return p;
+}
+
+// Entries of the set (the sequences in the given order, longest first).
+template <class C>
+void varlen_entries(const VarlenSeq *seqs, const VlPlan &p, VlArgs &a) {
+    a.n = p.n;
+    a.nlvl = p.nlvl;
+    int k = 0, slot = 0;
+    for (int i = 0; i < p.n; ++i) {
+        const int nc = (seqs[i].len + C::Q - 1) / C::Q;
+        a.u[i] = VlUnit{seqs[i].t0, seqs[i].len, k, seqs[i].seq, 0, nc, 0, 0};
+        k += nc;
+    }
+    a.ntotal = p.n;
+    if (!p.segmented()) return;
+    // scan units: every sequence's first segment, then the second ..., so
+    // that the units that need no segment-state pass are scheduled first
+    std::vector<int> slot0(p.n);
+    for (int i = 0; i < p.n; ++i) {
+        slot0[i] = slot;
+        slot += ((a.u[i].nch + p.cps - 1) / p.cps - 1) * p.nsub;
+    }
+    for (int seg = 0; seg < p.maxseg; ++seg)
+        for (int i = 0; i < p.n; ++i) {
+            const int c0 = seg * p.cps, nc = a.u[i].nch;
+            if (c0 >= nc) continue;
+            VlUnit u = a.u[i];
+            u.c0 = c0;
+            u.nch = std::min(nc, c0 + p.cps) - c0;
+            u.slot = slot0[i];
+            u.nprev = seg * p.nsub;
+            a.u[a.ntotal++] = u;
+        }
+    const int csub = (p.cps + p.nsub - 1) / p.nsub;
+    for (int i = 0; i < p.n; ++i) {
+        const int nseg = (a.u[i].nch + p.cps - 1) / p.cps;
+        for (int seg = 0; seg + 1 < nseg; ++seg)
+            for (int sub = 0; sub < p.nsub; ++sub) {
+                VlUnit u = a.u[i];
+                u.c0 = seg * p.cps + sub * csub;
+                u.nch = std::min(seg * p.cps + p.cps, u.c0 + csub) - u.c0;
+                u.slot = slot0[i] + seg * p.nsub + sub;
+                u.nprev = 0;
+                a.u[a.ntotal++] = u;
+            }
+    }
+}
+
+struct VlLayout {
+    size_t flags, pack, table, off, states, totals, total;
+};
+
+template <class C>
+VlLayout varlen_layout(const Dims &d, const VlPlan &p) {
     VlLayout l;
-    const long long nplanes = nchunks * d.G;
+    const long long nplanes = p.nchunks * d.G;
+    const long long entries = p.n + (p.segmented() ? p.nscan + p.nsegu : 0);
     l.flags = 0;
     l.pack = align256(sizeof(unsigned) * nplanes);
     l.table = l.pack + align256((size_t)C::CBM_BYTES * nplanes);
-    l.off = l.table + align256(sizeof(VlUnit) * n);
-    l.total = l.off + align256(sizeof(int) * (nlvl + 1));
+    l.off = l.table + align256(sizeof(VlUnit) * entries);
+    l.states = l.off + align256(sizeof(int) * (p.nlvl + 1));
+    l.totals = l.states + (p.segmented() ? align256(sizeof(float) * p.nsegu * d.H * C::P * C::N) : 0);
+    l.total = l.totals + (p.segmented() ? align256(sizeof(float) * p.nsegu * d.H) : 0);
     return l;
 }
 
-// The units of the sequences (t0, len, seq), longest first, with their pack
-// planes; returns the total chunks and sets the level count.
-long long varlen_units(const VarlenSeq *seqs, int n, int Q, VlArgs &a) {
-    a.n = n;
-    a.nlvl = 0;
-    for (int i = 0; i < n; ++i) a.u[i] = VlUnit{seqs[i].t0, seqs[i].len, 0, seqs[i].seq};
-    std::stable_sort(a.u, a.u + n, [](const VlUnit &p, const VlUnit &q) { return p.len > q.len; });
-    long long k = 0;
-    for (int i = 0; i < n; ++i) {
-        const int nc = (a.u[i].len + Q - 1) / Q;
-        a.u[i].cbase = (int)k;
-        k += nc;
-        a.nlvl = std::max(a.nlvl, nc);
-    }
-    return k;
-}
-
 template <class C>
-cudaError_t run_fwd_varlen(const Dims &d, const VlArgs &a, long long nchunks, ssd_dtype_t ydtype, const void *x,
+cudaError_t run_fwd_varlen(const Dims &d, const VlPlan &p, const VlArgs &a, ssd_dtype_t ydtype, const void *x,
                            const void *dt, const float *A, const void *B, const void *Cm, const float *D,
                            const float *init, void *y, float *fin, void *ws, unsigned *status, cudaStream_t s) {
-    const VlLayout l = varlen_layout<C>(d, a.n, nchunks, a.nlvl);
+    const VlLayout l = varlen_layout<C>(d, p);
     char *w = static_cast<char *>(ws);
-    const long long nflags = nchunks * d.G;
+    const long long nflags = p.nchunks * d.G;
     TcParams prm = base_params(d, dt, status);
     prm.x = static_cast<const bf16 *>(x);
     prm.A = A;
@@ -2165,24 +2283,49 @@ cudaError_t run_fwd_varlen(const Dims &d, const VlArgs &a, long long nchunks, ss
     prm.nhb = (int)((d.H + C::HB - 1) / C::HB);
     prm.nseg = 1;
     prm.cps = (int)d.nc;
-    prm.nsub = 1;
-    prm.nslot = 1;
+    prm.nsub = p.nsub;
+    prm.nslot = std::max(1, p.nsegu);
     VlUnit *vl = reinterpret_cast<VlUnit *>(w + l.table);
     int *vl_off = reinterpret_cast<int *>(w + l.off);
     prm.vl = vl;
-    const long long work = std::max<long long>(std::max<long long>(nflags, a.nlvl + 1), a.n);
+    prm.vl_scan0 = p.segmented() ? p.n : 0;
+    prm.vl_seg0 = p.n + p.nscan;
+    if (p.segmented()) {
+        prm.seg_state = reinterpret_cast<float *>(w + l.states);
+        prm.seg_cl = 1;
+        prm.seg_tot = reinterpret_cast<float *>(w + l.totals);
+    }
+    const long long work = std::max<long long>(std::max<long long>(nflags, a.nlvl + 1), a.ntotal);
     const unsigned blocks = (unsigned)std::min<long long>((work + 255) / 256, sm_count());
     timing_begin(s);
-    varlen_setup_kernel<C::Q><<<blocks, 256, 0, s>>>(a, vl, const_cast<int *>(vl_off), prm.cb_ready, nflags);
+    varlen_setup_kernel<C::Q><<<blocks, 256, 0, s>>>(a, vl, vl_off, prm.cb_ready, nflags);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     timing_mark(s, "varlen_setup");
     const CbWalk walk{(int)d.nc, (int)d.G, 1, nflags, vl, vl_off, a.nlvl};
-    const long long units = (long long)a.n * prm.nhb, spare = sm_count() - units;
-    e = launch_cb<C>(d, B, Cm, reinterpret_cast<uint8_t *>(w + l.pack), prm.cb_ready, prm.status, s,
-                     spare >= 8 ? (int)spare : 0, 2, &walk);
+    uint8_t *pack = reinterpret_cast<uint8_t *>(w + l.pack);
+    if (!p.segmented()) {
+        // one segment per sequence: the C B^T tiles are walked by one CTA on
+        // each SM the scan leaves free (as for an equal-length batch)
+        const long long units = (long long)p.nscan * prm.nhb, spare = sm_count() - units;
+        e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, spare >= 8 ? (int)spare : 0, 2, &walk);
+        if (e != cudaSuccess) return e;
+        return launch_scan<C, true>(d, prm, ydtype, x, B, Cm, dim3(prm.nhb, (unsigned)p.nscan, 1), "chunk_scan_tc",
+                                    true, s);
+    }
+    // segments: at most one C B^T CTA per SM beside the segment-state CTAs
+    e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, sm_count(), 1, &walk);
     if (e != cudaSuccess) return e;
-    return launch_scan<C, true>(d, prm, ydtype, x, B, Cm, dim3(prm.nhb, (unsigned)a.n, 1), "chunk_scan_tc", true, s);
+    const dim3 sgrid(prm.nhb, 1, (unsigned)p.nsegu);
+    if constexpr (C::N + 2 * C::Q <= 256)
+        e = p.nsub == 2 ? launch_seg_state<C, 2, true>(d, prm, x, B, sgrid, "seg_state_tc", true, s)
+                        : launch_seg_state<C, 4, true>(d, prm, x, B, sgrid, "seg_state_tc", true, s);
+    else
+        e = launch_seg_state<C, 4, true>(d, prm, x, B, sgrid, "seg_state_tc", true, s);
+    if (e != cudaSuccess) return e;
+    prm.dep_seg = 1;
+    return launch_scan<C, true>(d, prm, ydtype, x, B, Cm, dim3(prm.nhb, (unsigned)p.nscan, 1), "chunk_scan_tc", true,
+                                s);
 }
 
 // Dispatch over the compiled tile configurations.
@@ -2249,13 +2392,24 @@ bool tc_varlen_supported(const Dims &dq, ssd_dtype_t dtype) {
     return d.b == 1 && d.L < (1ll << 30) && (d.L / 64 + kVarlenMaxUnits) * d.G < (1ll << 31);
 }
 
+namespace {
+// The sequences sorted longest first (the order of a set's units).
+std::vector<VarlenSeq> longest_first(const VarlenSeq *seqs, int n) {
+    std::vector<VarlenSeq> v(seqs, seqs + n);
+    std::stable_sort(v.begin(), v.end(), [](const VarlenSeq &p, const VarlenSeq &q) { return p.len > q.len; });
+    return v;
+}
+}  // namespace
+
 size_t tc_varlen_workspace(const Dims &dq, const VarlenSeq *seqs, int n) {
     const Dims d = fwd_tiles(dq);
     if (n <= 0 || n > kVarlenMaxUnits) return 0;
-    thread_local VlArgs a;
-    const long long k = varlen_units(seqs, n, (int)d.Q, a);
+    const std::vector<VarlenSeq> v = longest_first(seqs, n);
     size_t bytes = 0;
-    dispatch(d, [&](auto c) { bytes = varlen_layout<decltype(c)>(d, n, k, a.nlvl).total; });
+    dispatch(d, [&](auto c) {
+        using C = decltype(c);
+        bytes = varlen_layout<C>(d, varlen_plan<C>(v.data(), n, (int)d.H)).total;
+    });
     return bytes;
 }
 
@@ -2264,22 +2418,30 @@ cudaError_t tc_fwd_varlen(const Dims &dq, const VarlenSeq *seqs, int n, ssd_dtyp
                           const float *init, void *y, float *fin, void *ws, unsigned *status, cudaStream_t s) {
     const Dims d = fwd_tiles(dq);
     if (n <= 0 || n > kVarlenMaxUnits) return cudaErrorInvalidValue;
+    const std::vector<VarlenSeq> v = longest_first(seqs, n);
     thread_local VlArgs a;  // (the launch copies it into its parameters)
-    const long long k = varlen_units(seqs, n, (int)d.Q, a);
     cudaError_t e = cudaErrorNotSupported;
     dispatch(d, [&](auto c) {
-        e = run_fwd_varlen<decltype(c)>(d, a, k, ydtype, x, dt, A, B, C, D, init, y, fin, ws, status, s);
+        using Cf = decltype(c);
+        const VlPlan p = varlen_plan<Cf>(v.data(), n, (int)d.H);
+        if (p.n + (p.segmented() ? p.nscan + p.nsegu : 0) > kVlEntries) {
+            e = cudaErrorInvalidValue;
+            return;
+        }
+        varlen_entries<Cf>(v.data(), p, a);
+        e = run_fwd_varlen<Cf>(d, p, a, ydtype, x, dt, A, B, C, D, init, y, fin, ws, status, s);
     });
     return e;
 }
 
 // The model, fitted to GB300 timings of the 130M-shaped heads (one sequence
 // of 128 to 8192 steps; sets of 4 to 256 sequences), within ~12 %:
-//   a launch set: kSetUs + max(the longest unit, ceil(units / SMs) x the
-//     mean unit), a unit (one scan CTA) taking kUnitUs + kSetChunkUs per
-//     64-step tile;
+//   a launch set with one segment per sequence: kSetUs + max(the longest
+//     unit, ceil(units / SMs) x the mean unit), a unit (one scan CTA) taking
+//     kUnitUs + kSetChunkUs per 64-step tile;
 //   a fused forward: kFwdUs + kFwdChunkUs per tile of a segment +
-//     kPrevUs per local state the last segment's prologue combines.
+//     kPrevUs per local state the last segment's prologue combines; a
+//     launch set with segments the same plus kSetUs / 4 (its setup kernel).
 // Tile costs scale by 1.35 for N = 256.
 namespace {
 constexpr double kSetUs = 8.0, kUnitUs = 6.5, kSetChunkUs = 1.7;
@@ -2289,19 +2451,23 @@ double n_scale(const Dims &d) { return d.N > 128 ? 1.35 : 1.0; }
 
 double tc_varlen_cost_us(const Dims &dq, const VarlenSeq *seqs, int n) {
     const Dims d = fwd_tiles(dq);
-    int nhb = 1;
-    dispatch(d, [&](auto c) { nhb = (int)((d.H + decltype(c)::HB - 1) / decltype(c)::HB); });
-    long long maxc = 0, sum = 0;
-    for (int i = 0; i < n; ++i) {
-        const long long nc = (seqs[i].len + d.Q - 1) / d.Q;
-        maxc = std::max(maxc, nc);
-        sum += nc;
-    }
     if (n == 0) return 0.0;
-    const double tile = kSetChunkUs * n_scale(d);
-    const long long units = (long long)n * nhb, sms = sm_count(), waves = (units + sms - 1) / sms;
-    const double longest = kUnitUs + tile * (double)maxc, mean = kUnitUs + tile * (double)sum / n;
-    return kSetUs + std::max(longest, (double)waves * mean);
+    const std::vector<VarlenSeq> v = longest_first(seqs, n);
+    double us = 0;
+    dispatch(d, [&](auto c) {
+        using C = decltype(c);
+        const VlPlan p = varlen_plan<C>(v.data(), n, (int)d.H);
+        if (p.segmented()) {
+            us = kSetUs / 4 + kFwdUs + kFwdChunkUs * n_scale(d) * p.cps + kPrevUs * (p.maxseg - 1) * p.nsub;
+            return;
+        }
+        const long long nhb = (d.H + C::HB - 1) / C::HB, sms = sm_count();
+        const long long units = (long long)n * nhb, waves = (units + sms - 1) / sms;
+        const double tile = kSetChunkUs * n_scale(d);
+        const double longest = kUnitUs + tile * p.nlvl, mean = kUnitUs + tile * (double)p.nchunks / n;
+        us = kSetUs + std::max(longest, (double)waves * mean);
+    });
+    return us;
 }
 
 double tc_fwd_cost_us(const Dims &dq, int64_t len) {

@@ -30,7 +30,7 @@ cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, cons
 // `d` is the packed batch (b = 1, L = all steps); each sequence is its first
 // row t0 in the packed tensors, its steps len (> 0) and its index seq (its
 // init / fin state).  At most kVarlenMaxUnits sequences per call.
-constexpr int kVarlenMaxUnits = 1024;
+constexpr int kVarlenMaxUnits = 960;
 struct VarlenSeq {
     int t0, len, seq;
 };

@@ -185,30 +185,37 @@ CBM = 64 * 64 * 2  # one chunk's masked C B^T (64 x 64 bf16)
 
 
 def test_varlen_plan_splits_off_long_sequences(lib):
-    """One long sequence among short ones runs as a fused forward of its own
-    (its segments fill the SMs), the short ones as one launch set: the
-    workspace is the larger of the two (152 SMs assumed without a GPU)."""
+    """One long sequence among many short ones (whose units fill the SMs)
+    runs as a fused forward of its own, its segments filling the SMs, and
+    the short ones as one launch set: the workspace is the larger of the two
+    (152 SMs assumed without a GPU)."""
     i64 = ctypes.c_int64
-    lens = [100, 4096, 37, 64, 1]
+    lens = [100] * 200 + [16384]
     cu = [0]
     for n in lens:
         cu.append(cu[-1] + n)
     s = shape(batch=1, seqlen=cu[-1], nheads=8)
     arr = (i64 * len(cu))(*cu)
-    own = lib.ssd_fwd_workspace_size(ctypes.byref(shape(batch=1, seqlen=4096, nheads=8)))
-    chunks = 2 + 1 + 1 + 1
-    rest = 256 + chunks * CBM + 256 + 256
+    own = lib.ssd_fwd_workspace_size(ctypes.byref(shape(batch=1, seqlen=16384, nheads=8)))
+    # the set: flags | packs of 400 chunks | 200 units of 32 bytes | level offsets
+    rest = 1792 + 400 * CBM + 6400 + 256
+    # all 201 in one set: 656 chunks, 201 units, 257 levels
+    together = 2816 + 656 * CBM + 6656 + 1280
     assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), arr, len(lens)) == max(own, rest)
-    assert own > rest
+    assert own > max(rest, together)
 
 
 def test_varlen_validates(lib):
     i64 = ctypes.c_int64
     s = shape(batch=1, seqlen=300)
     good = (i64 * 4)(0, 100, 164, 300)
-    # three short sequences run as one launch set: flags | packs of their
-    # 2 + 1 + 3 chunks | unit table | chunk-level offsets, each 256-aligned
-    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), good, 3) == 256 + 6 * CBM + 256 + 256
+    # three short sequences (6 units of 2 head blocks, far from filling the
+    # SMs) run as one launch set cut into one-chunk segments: flags | packs of
+    # their 2 + 1 + 3 chunks | 3 sequences + 6 scan units + 3 segment-state
+    # units of 32 bytes | 4 chunk-level offsets | 3 local states (4 heads,
+    # 64 x 128 fp32) | their totals, each 256-aligned
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), good, 3) == (
+        256 + 6 * CBM + 512 + 256 + 3 * 4 * 64 * 128 * 4 + 256)
     for bad in ((0, 100, 90, 300), (1, 100, 164, 300), (0, 100, 164, 299)):
         arr = (i64 * 4)(*bad)
         assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), arr, 3) == 0

@@ -125,19 +125,23 @@ def test_varlen_packed_batch(dtype, chunk):
         assert rel_err(to_np(fins[s:s + 1]), fin_ref) <= tol, s
 
 
-# Packed batches that run as one launch set (a chunk-scan unit per sequence
-# and head block, the C B^T pass walking every sequence's chunks), or, for
-# the last, the longest sequence as a fused forward of its own and the rest
-# as one launch set.  (name, H, P, N, G, chunk, lengths, kernels expected;
-# the lengths keep every sequence's dt 16-byte aligned: even starts for H = 4,
-# multiples of 4 for H = 6)
+# Packed batches and the launches they take: one launch set with one segment
+# per sequence (their units fill the SMs), a set whose sequences are cut into
+# segments (few sequences: a segment-state pass, then the scan), or the
+# longest sequence as a fused forward of its own and the rest as a set.
+# (name, H, P, N, G, chunk, lengths, launch list; the lengths keep every
+# sequence's dt 16-byte aligned: even starts for H = 4, multiples of 4 for
+# H = 6)
+ONE_SET = ["varlen_setup", "cb_mask_tc", "chunk_scan_tc"]
+SEG_SET = ["varlen_setup", "cb_mask_tc", "seg_state_tc", "chunk_scan_tc"]
+OWN_FWD = ["cb_mask_tc", "seg_state_tc", "chunk_scan_tc"]
 VARLEN_SETS = [
-    ("short_many", 8, 64, 128, 2, 64, [1, 63, 64, 65, 100, 129, 7, 200, 31, 64] * 4, {"varlen_setup"}),
-    ("short_q128", 8, 64, 128, 2, 128, [300, 1, 128, 129, 77, 256, 40], {"varlen_setup"}),
-    ("wide_head", 4, 128, 256, 2, 64, [70, 6, 130, 64, 2, 190], {"varlen_setup"}),
-    ("h6_plain_dt", 6, 64, 64, 3, 64, [100, 36, 200, 4, 64, 0, 8], {"varlen_setup"}),
-    ("long_and_short", 8, 64, 128, 1, 64, [100, 37] * 5 + [4096] + [64, 1] * 5,
-     {"varlen_setup", "seg_state_tc"}),
+    ("short_many", 8, 64, 128, 2, 64, [1, 63, 64, 65, 100, 129, 7, 200, 31, 64] * 4, ONE_SET),
+    ("short_q128", 8, 64, 128, 2, 128, [300, 1, 128, 129, 77, 256, 40], SEG_SET),
+    ("wide_head", 4, 128, 256, 2, 64, [70, 6, 130, 64, 2, 190], SEG_SET),
+    ("h6_plain_dt", 6, 64, 64, 3, 64, [100, 36, 200, 4, 64, 0, 8], SEG_SET),
+    ("few_long_halves", 24, 64, 128, 1, 64, [1000, 700, 300, 5], SEG_SET),
+    ("long_and_many", 8, 64, 128, 1, 64, [100, 37] * 100 + [16384], OWN_FWD + ONE_SET),
 ]
 
 
@@ -161,13 +165,11 @@ def test_varlen_launch_set(case, ydt):
         ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], init, cu, chunk_size=chunk, y=y,
                            final_states=fins)
         torch.cuda.synchronize()
-        names = {n for n, _ in ssd.launch_times_ms()}
+        names = [n for n, _ in ssd.launch_times_ms()]
     finally:
         ssd.launch_timing(False)
     ssd.check_device_status()
-    assert kernels <= names, names
-    if "seg_state_tc" not in kernels:
-        assert "seg_state_tc" not in names, names
+    assert names == kernels, names
     f = inp.as_f64()
     ini = init.double().cpu().numpy()
     tol = TOL["bf16"]
