@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <vector>
 
 #include "ssd_tc.cuh"
@@ -2164,14 +2165,46 @@ struct VlPlan {
     bool segmented() const { return nsegu > 0; }
 };
 
+// The cost model of a launch set (microseconds), fitted to GB300 timings of
+// the 130M-shaped heads (one sequence of 128 to 8192 steps; sets of 4 to 256
+// sequences), within ~12 %:
+//   one segment per sequence: kSetUs + max(the longest unit, ceil(units /
+//     SMs) x the mean unit), a unit (one scan CTA) taking kUnitUs +
+//     kSetChunkUs per 64-step tile;
+//   a fused forward: kFwdUs + kFwdChunkUs per tile of a segment + kPrevUs
+//     per local state the last segment's prologue combines; a set with
+//     segments the same plus kSetUs / 4 (its setup kernel), its tiles those
+//     of a segment or, when the units overflow the SMs, 1.15 x the tiles
+//     per SM.
+// Tile costs scale by 1.35 for N = 256.
+constexpr double kSetUs = 8.0, kUnitUs = 6.5, kSetChunkUs = 1.7;
+constexpr double kFwdUs = 17.6, kFwdChunkUs = 2.1, kPrevUs = 0.75;
+double n_scale(long long N) { return N > 128 ? 1.35 : 1.0; }
+
+double set_cost_us(const VlPlan &p, long long nhb, long long N) {
+    const long long sms = sm_count();
+    const double per_sm = (double)p.nchunks * nhb / sms;
+    if (p.segmented())
+        return kSetUs / 4 + kFwdUs + kPrevUs * (p.maxseg - 1) * p.nsub +
+               kFwdChunkUs * n_scale(N) * std::max((double)p.cps, 1.15 * per_sm);
+    const long long waves = ((long long)p.n * nhb + sms - 1) / sms;
+    const double tile = kSetChunkUs * n_scale(N);
+    const double longest = kUnitUs + tile * p.nlvl, mean = kUnitUs + tile * (double)p.nchunks / p.n;
+    return kSetUs + std::max(longest, (double)waves * mean);
+}
+
+// Segments of cps chunks when they shorten the set by the model: the fewest
+// chunks per segment that keep the scan's units within the SMs when the
+// sequences alone leave SMs free, else about 1.25 x the tiles per SM (only
+// the sequences longer than that are cut).
 template <class C>
 VlPlan varlen_plan(const VarlenSeq *seqs, int n, int H) {
-    VlPlan p;
-    p.n = n;
+    VlPlan base;
+    base.n = n;
     for (int i = 0; i < n; ++i) {
         const int nc = (seqs[i].len + C::Q - 1) / C::Q;
-        p.nchunks += nc;
-        p.nlvl = std::max(p.nlvl, nc);
+        base.nchunks += nc;
+        base.nlvl = std::max(base.nlvl, nc);
     }
     const long long nhb = (H + C::HB - 1) / C::HB, sms = sm_count();
     auto units = [&](int cps) {
@@ -2179,24 +2212,36 @@ VlPlan varlen_plan(const VarlenSeq *seqs, int n, int H) {
         for (int i = 0; i < n; ++i) u += ((seqs[i].len + C::Q - 1) / C::Q + cps - 1) / cps;
         return u;
     };
-    // the fewest chunks per segment whose scan units fit the SMs
-    p.cps = p.nlvl;
+    auto make = [&](int cps) {
+        VlPlan p = base;
+        p.cps = cps;
+        p.nscan = (int)units(cps);
+        if (cps < p.nlvl) {
+            p.nsub = (cps >= 2 && C::N + 2 * C::Q <= 256) ? 2 : 1;
+            p.nsegu = (int)(p.nscan - n) * p.nsub;
+            p.maxseg = (p.nlvl + cps - 1) / cps;
+        }
+        return p;
+    };
+    VlPlan best = make(base.nlvl);
+    int cut;
     if ((long long)n * nhb < sms) {
-        int lo = 1, hi = p.nlvl;
+        int lo = 1, hi = base.nlvl;
         while (lo < hi) {
             const int mid = (lo + hi) / 2;
             if (units(mid) * nhb <= sms) hi = mid;
             else lo = mid + 1;
         }
-        p.cps = lo;
+        cut = lo;
+    } else {
+        cut = (int)std::ceil(1.25 * (double)base.nchunks * nhb / sms);
     }
-    p.nscan = (int)units(p.cps);
-    if (p.cps < p.nlvl) {
-        p.nsub = (p.cps >= 2 && C::N + 2 * C::Q <= 256) ? 2 : 1;
-        p.nsegu = (int)(p.nscan - n) * p.nsub;
-        p.maxseg = (p.nlvl + p.cps - 1) / p.cps;
+    if (cut >= 1 && cut < base.nlvl) {
+        const VlPlan q = make(cut);
+        if ((long long)q.n + q.nscan + q.nsegu <= kVlEntries && set_cost_us(q, nhb, C::N) < set_cost_us(best, nhb, C::N))
+            best = q;
     }
-    return p;
+    return best;
 }
 
 // Entries of the set (the sequences in the given order, longest first).
@@ -2424,30 +2469,11 @@ cudaError_t tc_fwd_varlen(const Dims &dq, const VarlenSeq *seqs, int n, ssd_dtyp
     dispatch(d, [&](auto c) {
         using Cf = decltype(c);
         const VlPlan p = varlen_plan<Cf>(v.data(), n, (int)d.H);
-        if (p.n + (p.segmented() ? p.nscan + p.nsegu : 0) > kVlEntries) {
-            e = cudaErrorInvalidValue;
-            return;
-        }
         varlen_entries<Cf>(v.data(), p, a);
         e = run_fwd_varlen<Cf>(d, p, a, ydtype, x, dt, A, B, C, D, init, y, fin, ws, status, s);
     });
     return e;
 }
-
-// The model, fitted to GB300 timings of the 130M-shaped heads (one sequence
-// of 128 to 8192 steps; sets of 4 to 256 sequences), within ~12 %:
-//   a launch set with one segment per sequence: kSetUs + max(the longest
-//     unit, ceil(units / SMs) x the mean unit), a unit (one scan CTA) taking
-//     kUnitUs + kSetChunkUs per 64-step tile;
-//   a fused forward: kFwdUs + kFwdChunkUs per tile of a segment +
-//     kPrevUs per local state the last segment's prologue combines; a
-//     launch set with segments the same plus kSetUs / 4 (its setup kernel).
-// Tile costs scale by 1.35 for N = 256.
-namespace {
-constexpr double kSetUs = 8.0, kUnitUs = 6.5, kSetChunkUs = 1.7;
-constexpr double kFwdUs = 17.6, kFwdChunkUs = 2.1, kPrevUs = 0.75;
-double n_scale(const Dims &d) { return d.N > 128 ? 1.35 : 1.0; }
-}  // namespace
 
 double tc_varlen_cost_us(const Dims &dq, const VarlenSeq *seqs, int n) {
     const Dims d = fwd_tiles(dq);
@@ -2456,16 +2482,7 @@ double tc_varlen_cost_us(const Dims &dq, const VarlenSeq *seqs, int n) {
     double us = 0;
     dispatch(d, [&](auto c) {
         using C = decltype(c);
-        const VlPlan p = varlen_plan<C>(v.data(), n, (int)d.H);
-        if (p.segmented()) {
-            us = kSetUs / 4 + kFwdUs + kFwdChunkUs * n_scale(d) * p.cps + kPrevUs * (p.maxseg - 1) * p.nsub;
-            return;
-        }
-        const long long nhb = (d.H + C::HB - 1) / C::HB, sms = sm_count();
-        const long long units = (long long)n * nhb, waves = (units + sms - 1) / sms;
-        const double tile = kSetChunkUs * n_scale(d);
-        const double longest = kUnitUs + tile * p.nlvl, mean = kUnitUs + tile * (double)p.nchunks / n;
-        us = kSetUs + std::max(longest, (double)waves * mean);
+        us = set_cost_us(varlen_plan<C>(v.data(), n, (int)d.H), (d.H + C::HB - 1) / C::HB, C::N);
     });
     return us;
 }
@@ -2478,7 +2495,7 @@ double tc_fwd_cost_us(const Dims &dq, int64_t len) {
     double us = 0;
     dispatch(d, [&](auto c) {
         const Plan p = plan_for<decltype(c)>(d);
-        us = kFwdUs + kFwdChunkUs * n_scale(d) * p.cps + kPrevUs * (p.nseg - 1) * p.nsub;
+        us = kFwdUs + kFwdChunkUs * n_scale(d.N) * p.cps + kPrevUs * (p.nseg - 1) * p.nsub;
     });
     return us;
 }

@@ -184,24 +184,38 @@ def test_decode_step_validates(lib):
 CBM = 64 * 64 * 2  # one chunk's masked C B^T (64 x 64 bf16)
 
 
-def test_varlen_plan_splits_off_long_sequences(lib):
-    """One long sequence among many short ones (whose units fill the SMs)
-    runs as a fused forward of its own, its segments filling the SMs, and
-    the short ones as one launch set: the workspace is the larger of the two
-    (152 SMs assumed without a GPU)."""
-    i64 = ctypes.c_int64
-    lens = [100] * 200 + [16384]
+def varlen_ws(lib, lens, H):
     cu = [0]
     for n in lens:
         cu.append(cu[-1] + n)
-    s = shape(batch=1, seqlen=cu[-1], nheads=8)
-    arr = (i64 * len(cu))(*cu)
+    arr = (ctypes.c_int64 * len(cu))(*cu)
+    return lib.ssd_fwd_varlen_workspace_size(ctypes.byref(shape(batch=1, seqlen=cu[-1], nheads=H)), arr, len(lens))
+
+
+def test_varlen_plan_cuts_long_sequences_in_a_set(lib):
+    """One long sequence among short ones whose units fill the SMs: the set
+    cuts the sequences longer than ~1.25 x the tiles per SM into segments
+    (here 16384 steps = 256 tiles into 12 segments of 22, the short ones
+    whole) rather than running the long one on its own (152 SMs assumed
+    without a GPU)."""
+    got = varlen_ws(lib, [100] * 200 + [16384], 8)
+    # flags | packs of 656 chunks | 201 sequences + 212 scan units + 22
+    # segment-state units of 32 bytes | 257 level offsets | 22 local states
+    # (8 heads, 64 x 128 fp32) | their totals, each 256-aligned
+    assert got == 2816 + 656 * CBM + 14080 + 1280 + 22 * 8 * 64 * 128 * 4 + 768
+
+
+def test_varlen_plan_splits_off_long_sequences(lib):
+    """Too many short sequences to leave table room for segments: the long
+    one runs as a fused forward of its own (its segments filling the SMs),
+    the short ones as one launch set; the workspace is the larger of the
+    two."""
     own = lib.ssd_fwd_workspace_size(ctypes.byref(shape(batch=1, seqlen=16384, nheads=8)))
-    # the set: flags | packs of 400 chunks | 200 units of 32 bytes | level offsets
-    rest = 1792 + 400 * CBM + 6400 + 256
-    # all 201 in one set: 656 chunks, 201 units, 257 levels
-    together = 2816 + 656 * CBM + 6656 + 1280
-    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), arr, len(lens)) == max(own, rest)
+    # the set of 900 one-tile sequences: flags | packs | 900 units | 2 level offsets
+    rest = 3840 + 900 * CBM + 28928 + 256
+    # all 901 in one set (no segments): 1156 chunks, 901 units, 257 levels
+    together = 4864 + 1156 * CBM + 29184 + 1280
+    assert varlen_ws(lib, [16] * 900 + [16384], 8) == max(own, rest)
     assert own > max(rest, together)
 
 
@@ -209,13 +223,10 @@ def test_varlen_validates(lib):
     i64 = ctypes.c_int64
     s = shape(batch=1, seqlen=300)
     good = (i64 * 4)(0, 100, 164, 300)
-    # three short sequences (6 units of 2 head blocks, far from filling the
-    # SMs) run as one launch set cut into one-chunk segments: flags | packs of
-    # their 2 + 1 + 3 chunks | 3 sequences + 6 scan units + 3 segment-state
-    # units of 32 bytes | 4 chunk-level offsets | 3 local states (4 heads,
-    # 64 x 128 fp32) | their totals, each 256-aligned
-    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), good, 3) == (
-        256 + 6 * CBM + 512 + 256 + 3 * 4 * 64 * 128 * 4 + 256)
+    # three short sequences (at most 3 chunks: segments would not pay) run
+    # as one launch set: flags | packs of their 2 + 1 + 3 chunks | 3 units of
+    # 32 bytes | 4 chunk-level offsets, each 256-aligned
+    assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), good, 3) == 256 + 6 * CBM + 256 + 256
     for bad in ((0, 100, 90, 300), (1, 100, 164, 300), (0, 100, 164, 299)):
         arr = (i64 * 4)(*bad)
         assert lib.ssd_fwd_varlen_workspace_size(ctypes.byref(s), arr, 3) == 0

@@ -127,8 +127,9 @@ def test_varlen_packed_batch(dtype, chunk):
 
 # Packed batches and the launches they take: one launch set with one segment
 # per sequence (their units fill the SMs), a set whose sequences are cut into
-# segments (few sequences: a segment-state pass, then the scan), or the
-# longest sequence as a fused forward of its own and the rest as a set.
+# segments (a segment-state pass, then the scan: few sequences, or one long
+# among many), or the longest sequence as a fused forward of its own and the
+# rest as a set (too many sequences to leave table room for segments).
 # (name, H, P, N, G, chunk, lengths, launch list; the lengths keep every
 # sequence's dt 16-byte aligned: even starts for H = 4, multiples of 4 for
 # H = 6)
@@ -137,11 +138,13 @@ SEG_SET = ["varlen_setup", "cb_mask_tc", "seg_state_tc", "chunk_scan_tc"]
 OWN_FWD = ["cb_mask_tc", "seg_state_tc", "chunk_scan_tc"]
 VARLEN_SETS = [
     ("short_many", 8, 64, 128, 2, 64, [1, 63, 64, 65, 100, 129, 7, 200, 31, 64] * 4, ONE_SET),
-    ("short_q128", 8, 64, 128, 2, 128, [300, 1, 128, 129, 77, 256, 40], SEG_SET),
-    ("wide_head", 4, 128, 256, 2, 64, [70, 6, 130, 64, 2, 190], SEG_SET),
-    ("h6_plain_dt", 6, 64, 64, 3, 64, [100, 36, 200, 4, 64, 0, 8], SEG_SET),
+    ("short_q128", 8, 64, 128, 2, 128, [300, 1, 128, 129, 77, 256, 40], ONE_SET),
+    ("q128_segments", 8, 64, 128, 2, 128, [3000, 1, 1280, 1290, 770, 2560, 400], SEG_SET),
+    ("wide_head", 4, 128, 256, 2, 64, [700, 6, 1300, 64, 2, 1900], SEG_SET),
+    ("h6_plain_dt", 6, 64, 64, 3, 64, [1000, 36, 2000, 4, 640, 0, 8], SEG_SET),
     ("few_long_halves", 24, 64, 128, 1, 64, [1000, 700, 300, 5], SEG_SET),
-    ("long_and_many", 8, 64, 128, 1, 64, [100, 37] * 100 + [16384], OWN_FWD + ONE_SET),
+    ("long_in_set", 8, 64, 128, 1, 64, [100, 37] * 100 + [16384], SEG_SET),
+    ("long_on_its_own", 8, 64, 128, 1, 64, [16] * 900 + [16384], OWN_FWD + ONE_SET),
 ]
 
 
