@@ -2257,8 +2257,11 @@ void varlen_entries(const VarlenSeq *seqs, const VlPlan &p, VlArgs &a) {
     }
     a.ntotal = p.n;
     if (!p.segmented()) return;
-    // scan units: every sequence's first segment, then the second ..., so
-    // that the units that need no segment-state pass are scheduled first
+    // scan units, the longest first (the block scheduler hands out SMs in
+    // unit order): every sequence's full segments, first segments before
+    // later ones, then the shorter last segments; a later segment holds its
+    // SM while the segment-state pass runs, but a long one started last
+    // would end last
     std::vector<int> slot0(p.n);
     for (int i = 0; i < p.n; ++i) {
         slot0[i] = slot;
@@ -2275,6 +2278,7 @@ void varlen_entries(const VarlenSeq *seqs, const VlPlan &p, VlArgs &a) {
             u.nprev = seg * p.nsub;
             a.u[a.ntotal++] = u;
         }
+    std::stable_sort(a.u + p.n, a.u + a.ntotal, [](const VlUnit &x, const VlUnit &y) { return x.nch > y.nch; });
     const int csub = (p.cps + p.nsub - 1) / p.nsub;
     for (int i = 0; i < p.n; ++i) {
         const int nseg = (a.u[i].nch + p.cps - 1) / p.cps;
