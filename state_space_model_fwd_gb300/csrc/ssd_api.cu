@@ -318,7 +318,7 @@ struct VarlenPlan {
     size_t nfwd = 0;
 };
 
-constexpr size_t kMaxSeparate = 64;  // longest sequences considered for a fused forward of their own
+constexpr size_t kMaxSeparate = 8;  // longest sequences considered for a fused forward of their own
 
 VarlenPlan plan_varlen(const ssd_shape_t *shape, const int64_t *cu, int64_t nseq) {
     VarlenPlan p;
@@ -340,6 +340,7 @@ VarlenPlan plan_varlen(const ssd_shape_t *shape, const int64_t *cu, int64_t nseq
     double best = sets_cost(0), sep = 0;
     for (size_t k = 1; k <= std::min(m, kMaxSeparate); ++k) {
         sep += ssd::tc_fwd_cost_us(d, p.order[k - 1].len);
+        if (sep >= best) break;  // (the separate forwards alone already cost more)
         const double us = sep + sets_cost(k);
         if (us < best) {
             best = us;
@@ -348,15 +349,10 @@ VarlenPlan plan_varlen(const ssd_shape_t *shape, const int64_t *cu, int64_t nseq
     }
     return p;
 }
-}  // namespace
-
-extern "C" {
-
-size_t ssd_fwd_varlen_workspace_size(const ssd_shape_t *shape, const int64_t *cu_seqlens, int64_t nseq) {
-    ssd_shape_t one;
-    if (check_varlen(shape, cu_seqlens, nseq, &one) != SSD_OK) return 0;
+// Workspace bytes of a plan: the largest of its fused forwards and sets.
+size_t varlen_workspace(const ssd_shape_t *shape, const int64_t *cu, int64_t nseq, const VarlenPlan &p) {
+    ssd_shape_t one = *shape;
     size_t need = 0;
-    const VarlenPlan p = plan_varlen(shape, cu_seqlens, nseq);
     if (p.tc) {
         Dims d;
         (void)check_shape(shape, true, &d);
@@ -373,12 +369,20 @@ size_t ssd_fwd_varlen_workspace_size(const ssd_shape_t *shape, const int64_t *cu
         return need;
     }
     for (int64_t s = 0; s < nseq; ++s) {
-        one.seqlen = cu_seqlens[s + 1] - cu_seqlens[s];
+        one.seqlen = cu[s + 1] - cu[s];
         if (one.seqlen == 0) continue;
-        const size_t w = ssd_fwd_workspace_size(&one);
-        if (w > need) need = w;
+        need = std::max(need, ssd_fwd_workspace_size(&one));
     }
     return need;
+}
+}  // namespace
+
+extern "C" {
+
+size_t ssd_fwd_varlen_workspace_size(const ssd_shape_t *shape, const int64_t *cu_seqlens, int64_t nseq) {
+    ssd_shape_t one;
+    if (check_varlen(shape, cu_seqlens, nseq, &one) != SSD_OK) return 0;
+    return varlen_workspace(shape, cu_seqlens, nseq, plan_varlen(shape, cu_seqlens, nseq));
 }
 
 ssd_status_t ssd_fwd_varlen(const ssd_shape_t *shape, const int64_t *cu_seqlens, int64_t nseq, const void *x,
@@ -403,7 +407,8 @@ ssd_status_t ssd_fwd_varlen(const ssd_shape_t *shape, const int64_t *cu_seqlens,
         const char *py = static_cast<const char *>(y) + t0 * H * P * ye;
         if (!ptrs_ok({px, pdt, pb, py}, {})) return SSD_ERR_INVALID_ARG;
     }
-    if (ssd_fwd_varlen_workspace_size(shape, cu_seqlens, nseq) > workspace_bytes) return SSD_ERR_WORKSPACE;
+    const VarlenPlan p = plan_varlen(shape, cu_seqlens, nseq);
+    if (varlen_workspace(shape, cu_seqlens, nseq, p) > workspace_bytes) return SSD_ERR_WORKSPACE;
     // one sequence's own fused forward
     auto own = [&](int64_t s) {
         const int64_t t0 = cu_seqlens[s];
@@ -415,7 +420,6 @@ ssd_status_t ssd_fwd_varlen(const ssd_shape_t *shape, const int64_t *cu_seqlens,
                        static_cast<const char *>(C) + t0 * G * N * e, D, ini,
                        static_cast<char *>(y) + t0 * H * P * ye, fin, workspace, workspace_bytes, stream);
     };
-    const VarlenPlan p = plan_varlen(shape, cu_seqlens, nseq);
     if (!p.tc) {
         for (int64_t s = 0; s < nseq; ++s)
             if ((st = own(s)) != SSD_OK) return st;

@@ -2445,7 +2445,8 @@ namespace {
 // The sequences sorted longest first (the order of a set's units).
 std::vector<VarlenSeq> longest_first(const VarlenSeq *seqs, int n) {
     std::vector<VarlenSeq> v(seqs, seqs + n);
-    std::stable_sort(v.begin(), v.end(), [](const VarlenSeq &p, const VarlenSeq &q) { return p.len > q.len; });
+    auto longer = [](const VarlenSeq &p, const VarlenSeq &q) { return p.len > q.len; };
+    if (!std::is_sorted(v.begin(), v.end(), longer)) std::stable_sort(v.begin(), v.end(), longer);
     return v;
 }
 }  // namespace
