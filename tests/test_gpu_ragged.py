@@ -189,3 +189,31 @@ def test_varlen_launch_set(case, ydt):
         assert rel_err(to_np(fins[s:s + 1]), fin_ref) <= tol, s
     print(f"{name} {ydt}: max err / RMS over {len(lens)} sequences {max(errs):.2e}"
           + (" (beyond half a bf16 ulp)" if ydt == torch.bfloat16 else ""))
+
+
+@pytest.mark.parametrize("mix", ["ragged4", "short64", "long_and_short"])
+def test_varlen_bench_mixes(mix):
+    """The packed batches the benchmark times (130M-shaped heads, 8192
+    tokens, bf16 y, no initial state), every sequence against the oracle."""
+    import bench
+    lens = bench.VARLEN_MIXES[mix]
+    base = si.CONFIGS["mamba2_130m"]
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    cfg = base.replace(name="varlen_" + mix, batch=1, seqlen=cu[-1], has_init=False)
+    inp = si.make_inputs(cfg)
+    t = inp.to_torch("cuda")
+    H, P, N = base.nheads, base.headdim, base.dstate
+    y = torch.full(t["x"].shape, float("nan"), device="cuda", dtype=torch.bfloat16)
+    fins = torch.full((len(lens), H, P, N), float("nan"), device="cuda")
+    ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], None, cu, base.chunk_size, y=y,
+                       final_states=fins)
+    torch.cuda.synchronize()
+    ssd.check_device_status()
+    f = inp.as_f64()
+    errs = []
+    for s, (a, e) in enumerate(zip(cu[:-1], cu[1:])):
+        y_ref, fin_ref = oracle.ssd_recurrence(f["x"][:, a:e], f["dt"][:, a:e], f["A"], f["B"][:, a:e],
+                                               f["C"][:, a:e], f["D"], None)
+        errs.append(check_bf16_y(to_np(y[:, a:e]), y_ref, TOL["bf16"], f"sequence {s}")[1])
+        assert rel_err(to_np(fins[s:s + 1]), fin_ref) <= TOL["bf16"], s
+    print(f"{mix}: max err / RMS over {len(lens)} sequences {max(errs):.2e} (beyond half a bf16 ulp)")
