@@ -112,3 +112,29 @@ def test_stage_writes_stay_inside_outputs(cfg):
     for raw, view, what in ((rc, cum, "dA_cumsum"), (rs, st, "states"), (ri, sin, "states_in"),
                             (rf, fin, "final_state"), (ry, y, "chunk-scan y"), (rq, yq, "sequential-scan y")):
         assert_guards(raw, view, f"{cfg.name} {what}")
+
+
+# Packed sequences whose last one ends in a partial chunk (its y rows are
+# written with plain stores that stop at the sequence's end): one launch set
+# with one segment each, one with segments, and one with the long sequence
+# as a fused forward of its own.
+VARLEN_GUARD = [
+    ("one_set", 8, [1, 63, 100, 129, 7, 200] * 8 + [37]),
+    ("segments", 8, [1000, 700, 300, 37]),
+    ("own_forward", 8, [16] * 900 + [16384, 37]),
+]
+
+
+@pytest.mark.parametrize("name,H,lens", VARLEN_GUARD, ids=[c[0] for c in VARLEN_GUARD])
+@pytest.mark.parametrize("y_dtype", [torch.bfloat16, torch.float32])
+def test_varlen_writes_stay_inside_outputs(name, H, lens, y_dtype):
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    cfg = si.SSDConfig("varlen_guard_" + name, 1, cu[-1], H, 64, 128, 1, 64, "bf16", False, 607)
+    t = si.make_inputs(cfg).to_torch("cuda")
+    ry, y = guarded(t["x"].shape, y_dtype)
+    rf, fins = guarded((len(lens), H, 64, 128), torch.float32)
+    ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], None, cu, 64, y=y, final_states=fins)
+    torch.cuda.synchronize()
+    ssd.check_device_status()
+    assert_guards(ry, y, f"{name} y")
+    assert_guards(rf, fins, f"{name} final_states")
