@@ -710,10 +710,18 @@ __global__ void __maxnreg__(72) cb_mask_kernel(const __grid_constant__ CUtensorM
     // tiles in chunk-major order (every batch and group of a chunk before the
     // next chunk), this CTA's every gridDim.x-th
     const long long ntiles = walk.ntiles;
-    griddep_launch();
+    if constexpr (!VL) griddep_launch();
     if (tid == 32) {
         for (int s = 0; s < 2; ++s) mbar_init(&full_bar[s], 1);
         fence_mbar_init();
+        prefetch_tmap(&mb);
+        prefetch_tmap(&mc);
+    }
+    // packed sequences: launched while the setup kernel writes the unit
+    // table and clears the flags; wait for it, then let the next grid go
+    if constexpr (VL) {
+        griddep_wait();
+        griddep_launch();
     }
     __syncthreads();
     int nload[2] = {0, 0};  // loads issued per stage (thread 32)
@@ -1976,6 +1984,8 @@ cudaError_t raise_smem(const void *fn, int bytes, int &done) {
 template <class C>
 cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pack, unsigned *ready, unsigned *status,
                       cudaStream_t s, int ncta = 0, int nst_max = 2, const CbWalk *walk = nullptr) {
+    // (packed sequences: launched with a programmatic dependency on the setup
+    // kernel, which it waits for inside)
     CUtensorMap mb, mc;
     if (!make_bt_map(&mb, B, d.N, d.G, d.L, d.b, C::Q) || !make_bt_map(&mc, Cm, d.N, d.G, d.L, d.b, C::Q))
         return cudaErrorInvalidValue;
@@ -1993,7 +2003,7 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pac
     cudaError_t e =
         raise_smem<C>(reinterpret_cast<const void *>(kern), C::smem_cb(2), walk ? attr_vl : attr);
     if (e != cudaSuccess) return e;
-    e = launch_k(kern, dim3(grid), 128, smem, s, false, mb, mc, pack, w, nst, ready, status);
+    e = launch_k(kern, dim3(grid), 128, smem, s, walk != nullptr, mb, mc, pack, w, nst, ready, status);
     timing_mark(s, "cb_mask_tc");
     return e;
 }
@@ -2146,6 +2156,9 @@ static_assert(sizeof(VlArgs) <= 31 * 1024, "kernel parameter space");
 template <int Q>
 __global__ void varlen_setup_kernel(const __grid_constant__ VlArgs a, VlUnit *vl, int *vl_off, unsigned *flags,
                                     long long nflags) {
+    // the C B^T grid may launch at once: it waits for this grid's completion
+    // before it reads the table or touches a flag
+    griddep_launch();
     const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x, nthr = (long long)gridDim.x * blockDim.x;
     for (long long i = tid; i < a.ntotal; i += nthr) vl[i] = a.u[i];
     for (long long c = tid; c <= a.nlvl; c += nthr) {
