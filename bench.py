@@ -837,7 +837,7 @@ def varlen_sweep(ssd, dev, flush, peaks, steps):
         ssd.launch_timing(True)
         run()
         torch.cuda.synchronize()
-        launches = [n for n, _ in ssd.launch_times_ms()]
+        launches = [[n, round(ms, 5)] for n, ms in ssd.launch_times_ms()]
         ssd.launch_timing(False)
         ms = time_graph(run, flush, steps)
         nbytes = (cu[-1] * H * P * 2 + cu[-1] * H * 2 + 2 * cu[-1] * G * N * 2 + 2 * H * 4

@@ -217,3 +217,37 @@ def test_varlen_bench_mixes(mix):
         errs.append(check_bf16_y(to_np(y[:, a:e]), y_ref, TOL["bf16"], f"sequence {s}")[1])
         assert rel_err(to_np(fins[s:s + 1]), fin_ref) <= TOL["bf16"], s
     print(f"{mix}: max err / RMS over {len(lens)} sequences {max(errs):.2e} (beyond half a bf16 ulp)")
+
+
+def test_varlen_more_sequences_than_one_set():
+    """2000 short sequences of random lengths (some empty): more than one
+    launch set holds (960), so they run as three sets one after another,
+    each sequence against the oracle from its own initial state."""
+    rng = np.random.default_rng(21)
+    lens = [int(v) for v in rng.integers(0, 48, 2000)]
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    H, P, N, G = 8, 64, 128, 2
+    cfg = si.SSDConfig("varlen_many", 1, cu[-1], H, P, N, G, 64, "bf16", False, 813)
+    inp = si.make_inputs(cfg)
+    t = inp.to_torch("cuda")
+    init = 0.1 * torch.randn(len(lens), H, P, N, device="cuda", generator=torch.Generator("cuda").manual_seed(14))
+    y = torch.full(t["x"].shape, float("nan"), device="cuda", dtype=torch.float32)
+    fins = torch.full((len(lens), H, P, N), float("nan"), device="cuda")
+    ssd.launch_timing(True)
+    try:
+        ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], init, cu, 64, y=y, final_states=fins)
+        torch.cuda.synchronize()
+        names = [n for n, _ in ssd.launch_times_ms()]
+    finally:
+        ssd.launch_timing(False)
+    ssd.check_device_status()
+    assert names == ONE_SET * 3, names
+    f = inp.as_f64()
+    ini = init.double().cpu().numpy()
+    ys, fs = to_np(y), to_np(fins)
+    for s, (a, e) in enumerate(zip(cu[:-1], cu[1:])):
+        y_ref, fin_ref = oracle.ssd_recurrence(f["x"][:, a:e], f["dt"][:, a:e], f["A"], f["B"][:, a:e],
+                                               f["C"][:, a:e], f["D"], ini[s:s + 1])
+        if e > a:
+            assert rel_err(ys[:, a:e], y_ref) <= TOL["bf16"], s
+        assert rel_err(fs[s:s + 1], fin_ref) <= TOL["bf16"], s
