@@ -834,12 +834,15 @@ def varlen_sweep(ssd, dev, flush, peaks, steps):
             ssd.ssd_fwd_varlen(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], None, cu, base.chunk_size,
                                y=y, final_states=fins, workspace=ws)
 
+        ms = time_graph(run, flush, steps)
+        # (warm, after an L2 flush; events between the launches, which
+        # include the host's time before the first one)
+        flush.zero_()
         ssd.launch_timing(True)
         run()
         torch.cuda.synchronize()
-        launches = [[n, round(ms, 5)] for n, ms in ssd.launch_times_ms()]
+        launches = [[n, round(t_ms, 5)] for n, t_ms in ssd.launch_times_ms()]
         ssd.launch_timing(False)
-        ms = time_graph(run, flush, steps)
         nbytes = (cu[-1] * H * P * 2 + cu[-1] * H * 2 + 2 * cu[-1] * G * N * 2 + 2 * H * 4
                   + cu[-1] * H * P * 2 + len(lens) * H * P * N * 4)
         rows[name] = {"nseq": len(lens), "tokens": cu[-1], "min_len": min(lens), "max_len": max(lens),
