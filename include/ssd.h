@@ -181,7 +181,7 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, co
  * starts from init_states[s] (NULL: zero) and ends in final_states[s] (NULL:
  * not written), both [nseq, H, P, N] fp32.  No state crosses a sequence
  * boundary.  On the tensor-core path (bf16 inputs and a tile shape it
- * covers) the sequences run in launch sets of up to 960: a chunk-scan CTA
+ * covers) the sequences run in launch sets of up to 800: a chunk-scan CTA
  * per (sequence, head block), longest first, with the C B^T pass walking
  * every sequence's chunks; when those CTAs leave SMs free, every sequence is
  * cut into segments of the same chunk count (a segment-state pass forms the

@@ -332,9 +332,9 @@ VarlenPlan plan_varlen(const ssd_shape_t *shape, const int64_t *cu, int64_t nseq
     const size_t m = p.order.size();
     auto sets_cost = [&](size_t from) {
         double us = 0;
-        for (size_t i = from; i < m; i += ssd::kVarlenMaxUnits)
+        for (size_t i = from; i < m; i += ssd::kVarlenSetSeqs)
             us += ssd::tc_varlen_cost_us(d, p.order.data() + i,
-                                         (int)std::min<size_t>(ssd::kVarlenMaxUnits, m - i));
+                                         (int)std::min<size_t>(ssd::kVarlenSetSeqs, m - i));
         return us;
     };
     double best = sets_cost(0), sep = 0;
@@ -361,7 +361,7 @@ size_t varlen_workspace(const ssd_shape_t *shape, const int64_t *cu, int64_t nse
                 one.seqlen = p.order[i].len;
                 need = std::max(need, ssd_fwd_workspace_size(&one));
             } else {
-                const int n = (int)std::min<size_t>(ssd::kVarlenMaxUnits, p.order.size() - i);
+                const int n = (int)std::min<size_t>(ssd::kVarlenSetSeqs, p.order.size() - i);
                 need = std::max(need, ssd::tc_varlen_workspace(d, p.order.data() + i, n));
                 i += n - 1;
             }
@@ -449,8 +449,8 @@ ssd_status_t ssd_fwd_varlen(const ssd_shape_t *shape, const int64_t *cu_seqlens,
         const cudaError_t ce = device_status_word(&status);
         if (ce != cudaSuccess) return from_cuda(ce);
     }
-    for (size_t i = p.nfwd; i < p.order.size(); i += ssd::kVarlenMaxUnits) {
-        const int n = (int)std::min<size_t>(ssd::kVarlenMaxUnits, p.order.size() - i);
+    for (size_t i = p.nfwd; i < p.order.size(); i += ssd::kVarlenSetSeqs) {
+        const int n = (int)std::min<size_t>(ssd::kVarlenSetSeqs, p.order.size() - i);
         st = from_cuda(ssd::tc_fwd_varlen(d, p.order.data() + i, n, shape->ydtype, x, dt, A, B, C, D, init_states,
                                           y, final_states, workspace, status, stream));
         if (st != SSD_OK) return st;

@@ -71,6 +71,29 @@ struct VlUnit {
     int t0, len, cbase, seq;
     int c0, nch, slot, nprev;
 };
+// A scan unit with seq < 0 runs several whole sequences one after another:
+// sequences t0 .. t0 + len - 1 of the table's sequence section, nch chunks
+// in all; the state is written out and reset at each boundary.
+
+// The chunk a role of the scan is at, walking its unit's chunks in order:
+// its sequence's table entry j and its chunk c within that sequence (the
+// entry's fields are read where needed: two registers per role).
+struct VlCursor {
+    const VlUnit *tab;
+    int j, c;
+    __device__ __forceinline__ int t0() const { return __ldg(&tab[j].t0); }
+    __device__ __forceinline__ int len() const { return __ldg(&tab[j].len); }
+    __device__ __forceinline__ int cbase() const { return __ldg(&tab[j].cbase); }
+    __device__ __forceinline__ int seq() const { return __ldg(&tab[j].seq); }
+    // one chunk on; true when it starts the next sequence
+    template <int Q>
+    __device__ __forceinline__ bool next() {
+        if (++c < (len() + Q - 1) / Q) return false;
+        ++j;
+        c = 0;
+        return true;
+    }
+};
 
 struct TcParams {
     long long *trace;  // optional event trace of CTA (0, 0, 0) (trace builds only)
@@ -1143,8 +1166,9 @@ __device__ __noinline__ void wide_fixup(uint32_t taddr, const float *ef, const u
 // ===========================================================================
 constexpr int kComputeWarps = 16;  // warps 8..23
 
-// VL: the units are packed sequences (prm.vl)
-template <class C, typename YT, bool VL>
+// VL: the units are packed sequences (prm.vl); MULTI: each unit runs several
+// whole sequences one after another (with VL)
+template <class C, typename YT, bool VL, bool MULTI = false>
 __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     chunk_scan_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap mdt,
                       const __grid_constant__ CUtensorMap my, const __grid_constant__ CUtensorMap mb,
@@ -1181,19 +1205,33 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
     int c0 = seg * prm.cps, nch = min(prm.nc, c0 + prm.cps) - c0;
     int segk = seg, slot0 = 0, nprev = seg * prm.nsub;
     bool last = seg == prm.nseg - 1;
+    // (packed sequences: the table entry the unit's chunk walk starts at, and
+    // whether the unit runs several sequences)
+    int vj0 = 0;
+    constexpr bool multi = MULTI;
+    static_assert(VL || !MULTI, "several sequences per unit are packed sequences");
     if constexpr (VL) {
-        const VlUnit u = prm.vl[prm.vl_scan0 + b];
+        VlUnit u = prm.vl[prm.vl_scan0 + b];
+        vj0 = prm.vl_scan0 + b;
+        if constexpr (MULTI) {
+            vj0 = u.t0;
+            nch = u.nch;
+            u = prm.vl[vj0];
+            u.c0 = 0;
+            u.nprev = 0;
+        } else {
+            nch = u.nch;
+        }
         bq = 0;
         t0 = u.t0;
         slen = u.len;
         sidx = u.seq;
         pbase = u.cbase;
         c0 = u.c0;
-        nch = u.nch;
         segk = u.nprev > 0 ? 1 : 0;
         slot0 = u.slot;
         nprev = u.nprev;
-        last = c0 + nch >= (u.len + C::Q - 1) / C::Q;
+        last = multi || c0 + nch >= (u.len + C::Q - 1) / C::Q;
     }
     const long long H = prm.H;
     auto stage_x = [&](int s) { return smem + s * C::SCAN_STAGE; };
@@ -1255,15 +1293,22 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
         reg_dec<C::REG_LO>();
         if (warp == 0) {
             // ---------------- TMA producer ----------------
+            VlCursor cur{prm.vl, vj0, c0};
             if (lane == 0)
                 for (int it = 0; it < nch; ++it) {
                     const int s = it % ST;
                     if (it >= ST && !wait_bounded(&empty_bar[s], free_parity(it, ST), &abort_sh)) break;
-                    const long long plane = (pbase + c0 + it) * prm.G + g;
+                    long long plane = (pbase + c0 + it) * prm.G + g;
+                    int row = t0 + (c0 + it) * C::Q;
+                    if constexpr (MULTI) {
+                        plane = ((long long)cur.cbase() + cur.c) * prm.G + g;
+                        row = cur.t0() + cur.c * C::Q;
+                        if (it + 1 < nch) cur.next<C::Q>();
+                    }
                     // the x box, then the pack (C B^T, B, C)
                     if (prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                     mbar_arrive_expect_tx(&full_bar[s], C::X_BYTES);
-                    tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, t0 + (c0 + it) * C::Q, bq);
+                    tma_load_5d(stage_x(s), &mx, &full_bar[s], 0, 0, h0, row, bq);
                     ++nload[s];
                     // once the C B^T kernel has published the tile's masked C B^T:
                     // it, and the tile's B and C from the inputs (no copy of a
@@ -1271,8 +1316,8 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                     if (!prm.flag_first && !wait_flag(prm.cb_ready + plane, &abort_sh, prm.flag_wait_ns)) break;
                     mbar_arrive_expect_tx(&pfull_bar[s], C::PACK_BYTES);
                     bulk_load(stage_cb(s), prm.pack + plane * C::CBM_BYTES, C::CBM_BYTES, &pfull_bar[s]);
-                    tma_load_5d(stage_b(s), &mb, &pfull_bar[s], 0, t0 + (c0 + it) * C::Q, 0, g, bq);
-                    tma_load_5d(stage_c(s), &mc, &pfull_bar[s], 0, t0 + (c0 + it) * C::Q, 0, g, bq);
+                    tma_load_5d(stage_b(s), &mb, &pfull_bar[s], 0, row, 0, g, bq);
+                    tma_load_5d(stage_c(s), &mc, &pfull_bar[s], 0, row, 0, g, bq);
                     ++npack[s];
                     TRACE(0, it);
                 }
@@ -1284,13 +1329,24 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
             for (int hh = 0; hh < C::HB; ++hh) rho[hh] = 0.f;
             auto chunk_of = [&](int it) { return c0 + it; };
             DtFeed<C, VL> feed{dt_ring, dt_bar, &mdt, bq, h0, nch, 0, t0, slen};
-            feed.start(prm, chunk_of);
+            // (a unit of several sequences takes each chunk's dt with plain
+            // loads: its chunks' rows are not evenly spaced)
+            if (!multi) feed.start(prm, chunk_of);
+            VlCursor cur{prm.vl, vj0, c0};
             float Ah[C::HB];
             load_decay<C>(prm, h0, Ah);
             for (int it = 0; it < nch; ++it) {
                 const int v = it % NV;
                 ChunkDt<C> dt;
-                if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) break;
+                if constexpr (MULTI) {
+                    fetch_dt<C>(prm, 0, h0, cur.c, cur.t0(), cur.len(), dt);
+                    if (cur.c == 0)  // a sequence starts: its state from its initial one, rho = 0
+#pragma unroll
+                        for (int hh = 0; hh < C::HB; ++hh) rho[hh] = 0.f;
+                    if (it + 1 < nch) cur.next<C::Q>();
+                } else if (!feed.take(prm, it, chunk_of, &abort_sh, dt)) {
+                    break;
+                }
                 float cum[C::HB][QPL], T[C::HB];
                 chunk_cums<C>(prm, b, h0, c0 + it, dt, Ah, cum, T);
                 // range [lo, hi] of the cumulative decay over the chunk and its start (0)
@@ -1381,7 +1437,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                     mbar_arrive(&vfull_bar[v]);
                 }
             }
-            feed.drain();
+            if (!multi) feed.drain();
         } else if (warp == 1) {
             // ---------------- MMA issuer: the whole warp runs the loop (its
             // descriptors stay warp-uniform), one elected lane issues ----------------
@@ -1463,6 +1519,55 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
         tc_fence_after();
         if (gtid == 0) TRACE(13, 1);
         float rho_end = 0.f;
+        // the final state S = exp(-rho) Ss of sequence seq_idx (fin [seq, H, P, N])
+        auto write_fin = [&](long long seq_idx, float rho_e) {
+            tc_fence_after();
+            const float sc = __expf(-rho_e);
+            float *dst = prm.fin + (((long long)seq_idx * H + hrow) * C::P + rp) * C::N;
+            if constexpr (C::SG == 1 && C::DT_RING >= 4 * 2048) {
+                // coalesced: each 16-column block goes through this warp's
+                // 2 KB of the dt ring (idle once the last chunk's vector
+                // set has been taken), the piece index XOR-ed with bits
+                // 1-2 of the row, then out eight rows per store (the 32
+                // rows of a warp are consecutive p of one head)
+                float *scr = reinterpret_cast<float *>(dt_ring) + (warp - 4) * 512;
+                float *dst0 = dst - (long long)lane * C::N;  // row of lane 0
+                const int pc = lane & 3;
+#pragma unroll 1
+                for (int n0 = 0; n0 < C::N; n0 += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<float4 *>(scr + lane * 16 + 4 * (j ^ ((lane >> 1) & 3))) =
+                            make_float4(v[4 * j] * sc, v[4 * j + 1] * sc, v[4 * j + 2] * sc, v[4 * j + 3] * sc);
+                    __syncwarp();
+                    if (hrow < H)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = (lane >> 2) + 8 * i;
+                            *reinterpret_cast<float4 *>(dst0 + (long long)r * C::N + n0 + 4 * pc) =
+                                *reinterpret_cast<const float4 *>(scr + r * 16 + 4 * (pc ^ ((r >> 1) & 3)));
+                        }
+                    __syncwarp();
+                }
+            } else {
+#pragma unroll 1
+                for (int n0 = half * NCOL; n0 < (half + 1) * NCOL; n0 += 16) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
+                    tmem_ld_wait();
+                    if (hrow < H)
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(dst + n0 + j) =
+                                make_float4(v[j] * sc, v[j + 1] * sc, v[j + 2] * sc, v[j + 3] * sc);
+                }
+            }
+        };
+        VlCursor cur{prm.vl, vj0, c0};
+        int prev_seq = 0;  // (several sequences: the one the previous chunk ended)
         for (int it = 0; it < nch; ++it) {
             const int v = it % NV, sb = it % NB;
             // one thread waits for every phase this chunk needs (the vector
@@ -1479,6 +1584,33 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
             if (!slot[0]) break;
             if (gtid == 0) TRACE(7, it);
             tc_fence_after();
+            if constexpr (MULTI) {
+                if (it > 0 && cur.c == 0) {
+                    // a sequence ends with the previous chunk (its state MMAs are
+                    // done): its final state out, the next one's initial state
+                    // (or zero) in, before this chunk's state MMAs are released
+                    if (prm.fin) write_fin(prev_seq, rho_end);
+                    const float *ini =
+                        prm.init ? prm.init + (((long long)cur.seq() * H + hrow) * C::P + rp) * C::N : nullptr;
+#pragma unroll 1
+                    for (int n0 = half * NCOL; n0 < (half + 1) * NCOL; n0 += 32) {
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 q = ini && hrow < H ? __ldg(reinterpret_cast<const float4 *>(ini + n0 + j))
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                            v[j] = q.x;
+                            v[j + 1] = q.y;
+                            v[j + 2] = q.z;
+                            v[j + 3] = q.w;
+                        }
+                        tmem_st32(tmem + lane_off + C::COL_S + n0, v);
+                    }
+                    tmem_st_wait();
+                    // (every state thread has written its rows before any reads them back)
+                    named_bar_sync(1, NT);
+                }
+            }
             const float *vv = vec(v);
             const float f = vv[C::V_F + rh], sbf = vv[C::V_SBF + rh];  // (f applied twice)
             const bool rescale = vv[C::V_FLAG] != 0.f;
@@ -1516,54 +1648,18 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                 mbar_arrive(&rt_bar);
                 mbar_arrive(&vempty_bar[v]);
             }
+            if constexpr (MULTI) {
+                if (it + 1 < nch) {
+                    const int seq_now = cur.seq();
+                    if (cur.next<C::Q>()) prev_seq = seq_now;
+                }
+            }
         }
-        // final state after the segment's last chunk: S = exp(-rho) Ss
+        // final state after the segment's last chunk
         if (last && prm.fin) {  // (a uniform test: group_wait handles an abort)
             if (group_wait(&sdone_bar, (uint32_t)((nch - 1) & 1), &abort_sh, &slot[9], 1, gtid, NT)) {
                 tc_fence_after();
-                const float sc = __expf(-rho_end);
-                float *dst = prm.fin + (((long long)sidx * H + hrow) * C::P + rp) * C::N;
-                if constexpr (C::SG == 1 && C::DT_RING >= 4 * 2048) {
-                    // coalesced: each 16-column block goes through this warp's
-                    // 2 KB of the dt ring (idle once the last chunk's vector
-                    // set has been taken), the piece index XOR-ed with bits
-                    // 1-2 of the row, then out eight rows per store (the 32
-                    // rows of a warp are consecutive p of one head)
-                    float *scr = reinterpret_cast<float *>(dt_ring) + (warp - 4) * 512;
-                    float *dst0 = dst - (long long)lane * C::N;  // row of lane 0
-                    const int pc = lane & 3;
-#pragma unroll 1
-                    for (int n0 = 0; n0 < C::N; n0 += 16) {
-                        float v[16];
-                        tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            *reinterpret_cast<float4 *>(scr + lane * 16 + 4 * (j ^ ((lane >> 1) & 3))) =
-                                make_float4(v[4 * j] * sc, v[4 * j + 1] * sc, v[4 * j + 2] * sc, v[4 * j + 3] * sc);
-                        __syncwarp();
-                        if (hrow < H)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const int r = (lane >> 2) + 8 * i;
-                                *reinterpret_cast<float4 *>(dst0 + (long long)r * C::N + n0 + 4 * pc) =
-                                    *reinterpret_cast<const float4 *>(scr + r * 16 + 4 * (pc ^ ((r >> 1) & 3)));
-                            }
-                        __syncwarp();
-                    }
-                } else {
-#pragma unroll 1
-                    for (int n0 = half * NCOL; n0 < (half + 1) * NCOL; n0 += 16) {
-                        float v[16];
-                        tmem_ld16(tmem + lane_off + C::COL_S + n0, v);
-                        tmem_ld_wait();
-                        if (hrow < H)
-#pragma unroll
-                            for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4 *>(dst + n0 + j) =
-                                    make_float4(v[j] * sc, v[j + 1] * sc, v[j + 2] * sc, v[j + 3] * sc);
-                    }
-                }
+                write_fin(multi ? (long long)cur.seq() : (long long)sidx, rho_end);
             }
         }
     } else if (warp >= 8 && warp < 24) {
@@ -1680,6 +1776,7 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
         }
         uint32_t xprev[NS / 2];
         bool wide_prev = false;
+        VlCursor ocur{prm.vl, vj0, c0};  // (packed sequences: the chunk whose output is next)
         for (int c = 0; c <= nch; ++c) {
             uint32_t xcur[NS / 2];
             bool wide = false;
@@ -1740,10 +1837,18 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                 }
                 fence_async_smem();
                 __syncwarp();
-                const long long trow = (long long)(c0 + cp) * C::Q + part * NS;  // step of the tile's first row
-                if (!VL || trow + NS <= slen) {
+                // step of the tile's first row in its sequence, the sequence's
+                // first row and length
+                long long trow = (long long)(c0 + cp) * C::Q + part * NS, yt0 = t0, ylen = slen;
+                if constexpr (MULTI) {
+                    trow = (long long)ocur.c * C::Q + part * NS;
+                    yt0 = ocur.t0();
+                    ylen = ocur.len();
+                    if (cp + 1 < nch) ocur.next<C::Q>();
+                }
+                if (!VL || trow + NS <= ylen) {
                     if (lane == 0) {
-                        tma_store_4d(&my, yt, (q4 * 32) % C::P, (int)(h0 + (q4 * 32) / C::P), (int)(t0 + trow), bq);
+                        tma_store_4d(&my, yt, (q4 * 32) % C::P, (int)(h0 + (q4 * 32) / C::P), (int)(yt0 + trow), bq);
                         bulk_commit_group();
                     }
                 } else if constexpr (VL) {
@@ -1751,8 +1856,8 @@ __global__ void __launch_bounds__(C::SCAN_THREADS, 1)
                     // the sequence's end (the next rows belong to the next one)
                     if (h0 + (q4 * 32) / C::P < H) {
                         YT *yg = static_cast<YT *>(prm.y) +
-                                 ((t0 + trow) * H + h0 + (q4 * 32) / C::P) * C::P + (q4 * 32) % C::P + lane;
-                        for (int j = 0; j < NS && trow + j < slen; ++j)
+                                 ((yt0 + trow) * H + h0 + (q4 * 32) / C::P) * C::P + (q4 * 32) % C::P + lane;
+                        for (int j = 0; j < NS && trow + j < ylen; ++j)
                             yg[(long long)j * H * C::P] = yt[j * 32 + lane];
                     }
                 }
@@ -2010,7 +2115,7 @@ cudaError_t launch_cb(const Dims &d, const void *B, const void *Cm, uint8_t *pac
 
 // pdl: the scan may start while the kernel before it on the stream (the
 // C B^T kernel, which publishes its packs through ready flags) still runs.
-template <class C, bool VL = false>
+template <class C, bool VL = false, bool MULTI = false>
 cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const void *x, const void *B, const void *Cm,
                         dim3 grid, const char *name, bool pdl, cudaStream_t s) {
     CUtensorMap mx, mdt = {}, my, mb, mc;
@@ -2026,20 +2131,20 @@ cudaError_t launch_scan(const Dims &d, TcParams prm, ssd_dtype_t ydtype, const v
     // be met would wait forever)
     {
         cudaFuncAttributes fa;
-        cudaError_t e = f32 ? cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, float, VL>)
-                            : cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, bf16, VL>);
+        cudaError_t e = f32 ? cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, float, VL, MULTI>)
+                            : cudaFuncGetAttributes(&fa, chunk_scan_kernel<C, bf16, VL, MULTI>);
         if (e != cudaSuccess) return e;
         if ((fa.numRegs + 7) / 8 * 8 != C::REG_LAUNCH) return cudaErrorInvalidConfiguration;
     }
     cudaError_t e;
     if (f32) {
-        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float, VL>), C::SMEM_SCAN, attr_f);
+        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, float, VL, MULTI>), C::SMEM_SCAN, attr_f);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, float, VL>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
+        e = launch_k(chunk_scan_kernel<C, float, VL, MULTI>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
     } else {
-        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16, VL>), C::SMEM_SCAN, attr_b);
+        e = raise_smem<C>(reinterpret_cast<const void *>(chunk_scan_kernel<C, bf16, VL, MULTI>), C::SMEM_SCAN, attr_b);
         if (e != cudaSuccess) return e;
-        e = launch_k(chunk_scan_kernel<C, bf16, VL>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
+        e = launch_k(chunk_scan_kernel<C, bf16, VL, MULTI>, grid, C::SCAN_THREADS, C::SMEM_SCAN, s, pdl, mx, mdt, my, mb, mc, prm);
     }
     timing_mark(s, name);
     return e;
@@ -2175,8 +2280,32 @@ struct VlPlan {
     long long nchunks = 0;
     int cps = 0, nsub = 1;  // chunks per segment (the longest sequence's: no segments), sub-segments
     int nscan = 0, nsegu = 0, maxseg = 1;  // units of the scan and of the segment-state pass; most segments
+    // several whole sequences per scan unit: the units' chunk target, the
+    // most chunks and sequences of one unit (0: one sequence per unit)
+    int gchunks = 0, gmaxc = 0, gmaxn = 0;
     bool segmented() const { return nsegu > 0; }
+    bool grouped() const { return gchunks > 0; }
+    long long entries() const { return n + (segmented() ? (long long)nscan + nsegu : grouped() ? nscan : 0); }
 };
+
+// Consecutive sequences (longest first) into units of at most `target`
+// chunks (a longer sequence alone); calls f(first, count, chunks) per unit.
+template <int Q, class F>
+void varlen_groups(const VarlenSeq *seqs, int n, int target, F f) {
+    int i0 = 0, cnt = 0, ch = 0;
+    for (int i = 0; i < n; ++i) {
+        const int nc = (seqs[i].len + Q - 1) / Q;
+        if (cnt > 0 && ch + nc > target) {
+            f(i0, cnt, ch);
+            i0 = i;
+            cnt = 0;
+            ch = 0;
+        }
+        ++cnt;
+        ch += nc;
+    }
+    if (cnt > 0) f(i0, cnt, ch);
+}
 
 // The cost model of a launch set (microseconds), fitted to GB300 timings of
 // the 130M-shaped heads (one sequence of 128 to 8192 steps; sets of 4 to 256
@@ -2188,15 +2317,23 @@ struct VlPlan {
 //     per local state the last segment's prologue combines; a set with
 //     segments the same plus kSetUs / 4 (its setup kernel), its tiles those
 //     of a segment or, when the units overflow the SMs, 1.15 x the tiles
-//     per SM.
+//     per SM;
+//   several sequences per unit: kSetUs + waves x (kUnitUs + kSetChunkUs
+//     per tile of the largest unit + kSeqUs per sequence boundary in the
+//     unit with the most: the state written out and reset, the state chain
+//     stalled meanwhile).
 // Tile costs scale by 1.35 for N = 256.
-constexpr double kSetUs = 8.0, kUnitUs = 6.5, kSetChunkUs = 1.7;
+constexpr double kSetUs = 8.0, kUnitUs = 6.5, kSetChunkUs = 1.7, kSeqUs = 3.5;
 constexpr double kFwdUs = 17.6, kFwdChunkUs = 2.1, kPrevUs = 0.75;
 double n_scale(long long N) { return N > 128 ? 1.35 : 1.0; }
 
 double set_cost_us(const VlPlan &p, long long nhb, long long N) {
     const long long sms = sm_count();
     const double per_sm = (double)p.nchunks * nhb / sms;
+    if (p.grouped()) {
+        const long long waves = ((long long)p.nscan * nhb + sms - 1) / sms;
+        return kSetUs + (double)waves * (kUnitUs + kSetChunkUs * n_scale(N) * p.gmaxc + kSeqUs * (p.gmaxn - 1));
+    }
     if (p.segmented())
         return kSetUs / 4 + kFwdUs + kPrevUs * (p.maxseg - 1) * p.nsub +
                kFwdChunkUs * n_scale(N) * std::max((double)p.cps, 1.15 * per_sm);
@@ -2251,8 +2388,27 @@ VlPlan varlen_plan(const VarlenSeq *seqs, int n, int H) {
     }
     if (cut >= 1 && cut < base.nlvl) {
         const VlPlan q = make(cut);
-        if ((long long)q.n + q.nscan + q.nsegu <= kVlEntries && set_cost_us(q, nhb, C::N) < set_cost_us(best, nhb, C::N))
-            best = q;
+        if (q.entries() <= kVlEntries && set_cost_us(q, nhb, C::N) < set_cost_us(best, nhb, C::N)) best = q;
+    }
+    // several short sequences per unit, the units one wave (their CTAs' fixed
+    // cost paid once per SM rather than once per sequence)
+    if ((long long)n * nhb > sms && n > 1) {
+        int target = std::max<int>(base.nlvl, (int)((base.nchunks * nhb + sms - 1) / sms));
+        for (;; ++target) {
+            VlPlan q = base;
+            q.cps = base.nlvl;
+            q.gchunks = target;
+            varlen_groups<C::Q>(seqs, n, target, [&](int, int cnt, int ch) {
+                ++q.nscan;
+                q.gmaxc = std::max(q.gmaxc, ch);
+                q.gmaxn = std::max(q.gmaxn, cnt);
+            });
+            if ((long long)q.nscan * nhb <= sms || target >= base.nchunks) {
+                if (q.nscan < n && q.entries() <= kVlEntries && set_cost_us(q, nhb, C::N) < set_cost_us(best, nhb, C::N))
+                    best = q;
+                break;
+            }
+        }
     }
     return best;
 }
@@ -2269,6 +2425,12 @@ void varlen_entries(const VarlenSeq *seqs, const VlPlan &p, VlArgs &a) {
         k += nc;
     }
     a.ntotal = p.n;
+    if (p.grouped()) {
+        varlen_groups<C::Q>(seqs, p.n, p.gchunks, [&](int i0, int cnt, int ch) {
+            a.u[a.ntotal++] = VlUnit{i0, cnt, 0, -1, 0, ch, 0, 0};
+        });
+        return;
+    }
     if (!p.segmented()) return;
     // scan units, the longest first (the block scheduler hands out SMs in
     // unit order): every sequence's full segments, first segments before
@@ -2315,7 +2477,7 @@ template <class C>
 VlLayout varlen_layout(const Dims &d, const VlPlan &p) {
     VlLayout l;
     const long long nplanes = p.nchunks * d.G;
-    const long long entries = p.n + (p.segmented() ? p.nscan + p.nsegu : 0);
+    const long long entries = p.entries();
     l.flags = 0;
     l.pack = align256(sizeof(unsigned) * nplanes);
     l.table = l.pack + align256((size_t)C::CBM_BYTES * nplanes);
@@ -2350,7 +2512,7 @@ cudaError_t run_fwd_varlen(const Dims &d, const VlPlan &p, const VlArgs &a, ssd_
     VlUnit *vl = reinterpret_cast<VlUnit *>(w + l.table);
     int *vl_off = reinterpret_cast<int *>(w + l.off);
     prm.vl = vl;
-    prm.vl_scan0 = p.segmented() ? p.n : 0;
+    prm.vl_scan0 = p.segmented() || p.grouped() ? p.n : 0;
     prm.vl_seg0 = p.n + p.nscan;
     if (p.segmented()) {
         prm.seg_state = reinterpret_cast<float *>(w + l.states);
@@ -2368,12 +2530,17 @@ cudaError_t run_fwd_varlen(const Dims &d, const VlPlan &p, const VlArgs &a, ssd_
     uint8_t *pack = reinterpret_cast<uint8_t *>(w + l.pack);
     if (!p.segmented()) {
         // one segment per sequence: the C B^T tiles are walked by one CTA on
-        // each SM the scan leaves free (as for an equal-length batch)
+        // each SM the scan leaves free (as for an equal-length batch); units
+        // of several sequences take their chunks sequence by sequence, out of
+        // the walk's level order, so their tiles are all launched at once
         const long long units = (long long)p.nscan * prm.nhb, spare = sm_count() - units;
-        e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, spare >= 8 ? (int)spare : 0, 2, &walk);
+        e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, spare >= 8 && !p.grouped() ? (int)spare : 0, 2,
+                         &walk);
         if (e != cudaSuccess) return e;
-        return launch_scan<C, true>(d, prm, ydtype, x, B, Cm, dim3(prm.nhb, (unsigned)p.nscan, 1), "chunk_scan_tc",
-                                    true, s);
+        return p.grouped() ? launch_scan<C, true, true>(d, prm, ydtype, x, B, Cm, dim3(prm.nhb, (unsigned)p.nscan, 1),
+                                                        "chunk_scan_tc", true, s)
+                           : launch_scan<C, true>(d, prm, ydtype, x, B, Cm, dim3(prm.nhb, (unsigned)p.nscan, 1),
+                                                  "chunk_scan_tc", true, s);
     }
     // segments: at most one C B^T CTA per SM beside the segment-state CTAs
     e = launch_cb<C>(d, B, Cm, pack, prm.cb_ready, prm.status, s, sm_count(), 1, &walk);

@@ -31,6 +31,9 @@ cudaError_t tc_chunk_scan(const Dims &d, ssd_dtype_t ydtype, const void *x, cons
 // row t0 in the packed tensors, its steps len (> 0) and its index seq (its
 // init / fin state).  At most kVarlenMaxUnits sequences per call.
 constexpr int kVarlenMaxUnits = 960;
+// Sequences per launch set: a set of several sequences per scan unit adds
+// its units (at most one per SM) to the table.
+constexpr int kVarlenSetSeqs = 800;
 struct VarlenSeq {
     int t0, len, seq;
 };

@@ -208,15 +208,27 @@ def test_varlen_plan_cuts_long_sequences_in_a_set(lib):
 def test_varlen_plan_splits_off_long_sequences(lib):
     """Too many short sequences to leave table room for segments: the long
     one runs as a fused forward of its own (its segments filling the SMs),
-    the short ones as one launch set; the workspace is the larger of the
-    two."""
+    the short ones as launch sets of up to 800; the workspace is the
+    largest of those."""
     own = lib.ssd_fwd_workspace_size(ctypes.byref(shape(batch=1, seqlen=16384, nheads=8)))
-    # the set of 900 one-tile sequences: flags | packs | 900 units | 2 level offsets
-    rest = 3840 + 900 * CBM + 28928 + 256
-    # all 901 in one set (no segments): 1156 chunks, 901 units, 257 levels
-    together = 4864 + 1156 * CBM + 29184 + 1280
+    # the first set, 800 one-tile sequences in 37 units of up to 22: flags |
+    # packs | 800 sequences + 37 units of 32 bytes | 2 level offsets
+    rest = 3328 + 800 * CBM + 26880 + 256
+    # all 801 of a first set without segments or groups: 1055 chunks, 801 units, 257 levels
+    together = 4352 + 1055 * CBM + 25856 + 1280
     assert varlen_ws(lib, [16] * 900 + [16384], 8) == max(own, rest)
     assert own > max(rest, together)
+
+
+def test_varlen_plan_groups_short_sequences(lib):
+    """64 sequences of 100 / 156 steps with 24 heads (768 one-sequence units,
+    five waves): the set packs consecutive sequences (longest first) into
+    units of up to 15 chunks, the fewest per unit that keep the units (11 x
+    12 head blocks) within one wave; the table holds the 64 sequences and
+    the 11 units."""
+    got = varlen_ws(lib, [100, 156] * 32, 24)
+    # flags | packs of 160 chunks | 64 + 11 entries of 32 bytes | 4 level offsets
+    assert got == 768 + 160 * CBM + 2560 + 256
 
 
 def test_varlen_validates(lib):

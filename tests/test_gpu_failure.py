@@ -116,10 +116,11 @@ def test_stage_writes_stay_inside_outputs(cfg):
 
 # Packed sequences whose last one ends in a partial chunk (its y rows are
 # written with plain stores that stop at the sequence's end): one launch set
-# with one segment each, one with segments, and one with the long sequence
-# as a fused forward of its own.
+# with one segment each, one with several sequences per scan unit, one with
+# segments, and one with the long sequence as a fused forward of its own.
 VARLEN_GUARD = [
     ("one_set", 8, [1, 63, 100, 129, 7, 200] * 8 + [37]),
+    ("grouped", 24, [100, 156] * 32 + [37]),
     ("segments", 8, [1000, 700, 300, 37]),
     ("own_forward", 8, [16] * 900 + [16384, 37]),
 ]

@@ -126,7 +126,8 @@ def test_varlen_packed_batch(dtype, chunk):
 
 
 # Packed batches and the launches they take: one launch set with one segment
-# per sequence (their units fill the SMs), a set whose sequences are cut into
+# per sequence or several short sequences per scan unit (their units fill
+# the SMs), a set whose sequences are cut into
 # segments (a segment-state pass, then the scan: few sequences, or one long
 # among many), or the longest sequence as a fused forward of its own and the
 # rest as a set (too many sequences to leave table room for segments).
@@ -144,7 +145,7 @@ VARLEN_SETS = [
     ("h6_plain_dt", 6, 64, 64, 3, 64, [1000, 36, 2000, 4, 640, 0, 8], SEG_SET),
     ("few_long_halves", 24, 64, 128, 1, 64, [1000, 700, 300, 5], SEG_SET),
     ("long_in_set", 8, 64, 128, 1, 64, [100, 37] * 100 + [16384], SEG_SET),
-    ("long_on_its_own", 8, 64, 128, 1, 64, [16] * 900 + [16384], OWN_FWD + ONE_SET),
+    ("long_on_its_own", 8, 64, 128, 1, 64, [16] * 900 + [16384], OWN_FWD + ONE_SET * 2),
 ]
 
 
@@ -221,8 +222,9 @@ def test_varlen_bench_mixes(mix):
 
 def test_varlen_more_sequences_than_one_set():
     """2000 short sequences of random lengths (some empty): more than one
-    launch set holds (960), so they run as three sets one after another,
-    each sequence against the oracle from its own initial state."""
+    launch set holds (800), so they run as three sets one after another,
+    each packing several sequences per scan unit; each sequence against the
+    oracle from its own initial state."""
     rng = np.random.default_rng(21)
     lens = [int(v) for v in rng.integers(0, 48, 2000)]
     cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
