@@ -185,7 +185,9 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, co
  * per (sequence, head block), longest first, with the C B^T pass walking
  * every sequence's chunks; when those CTAs leave SMs free, every sequence is
  * cut into segments of the same chunk count (a segment-state pass forms the
- * earlier segments' local states, as in ssd_fwd).  The longest sequences
+ * earlier segments' local states, as in ssd_fwd); when they would take
+ * several waves of CTAs, consecutive short sequences may share a CTA, which
+ * runs them one after another.  The longest sequences
  * may instead run the fused forward of ssd_fwd each, whichever a host-side
  * cost model rates faster.  A sequence's partial last
  * chunk then reads the next sequence's first steps and gives them dt = 0, so
