@@ -187,18 +187,17 @@ SSD_API ssd_status_t ssd_fwd_noalloc(const ssd_shape_t *shape, const void *x, co
  * cut into segments of the same chunk count (a segment-state pass forms the
  * earlier segments' local states, as in ssd_fwd); when they would take
  * several waves of CTAs, consecutive short sequences may share a CTA, which
- * runs them one after another.  The longest sequences
- * may instead run the fused forward of ssd_fwd each, whichever a host-side
- * cost model rates faster.  A sequence's partial last
- * chunk then reads the next sequence's first steps and gives them dt = 0, so
- * they add 0 times their values: finite inputs leave no trace across the
- * boundary (a non-finite x or B there would).  Other inputs run the
- * fused forward per sequence.  Everything is enqueued on `stream` and shares
- * `workspace`, which must hold ssd_fwd_varlen_workspace_size(shape,
- * cu_seqlens, nseq) bytes (0 for invalid arguments).  Every sequence's
- * start must keep the pointers it derives 16-byte aligned (cu_seqlens[s] *
- * H * sizeof(dtype) a multiple of 16, e.g. H a multiple of 8 for bf16):
- * SSD_ERR_INVALID_ARG otherwise.
+ * runs them one after another.  The longest sequences may instead run the
+ * fused forward of ssd_fwd each, whichever a host-side cost model rates
+ * faster.  A sequence's partial last chunk then reads the next sequence's
+ * first steps and gives them dt = 0, so they add 0 times their values:
+ * finite inputs leave no trace across the boundary (a non-finite x or B
+ * there would).  Other inputs run the fused forward per sequence.
+ * Everything is enqueued on `stream` and shares `workspace`, which must hold
+ * ssd_fwd_varlen_workspace_size(shape, cu_seqlens, nseq) bytes (0 for
+ * invalid arguments).  Every sequence's start must keep the pointers it
+ * derives 16-byte aligned (cu_seqlens[s] * H * sizeof(dtype) a multiple of
+ * 16, e.g. H a multiple of 8 for bf16): SSD_ERR_INVALID_ARG otherwise.
  * (The pages are silent on batches of unequal lengths; this packs them the
  * way the chunk split of "Mamba-2 in NVIDIA cuTile", section "Why Mamba-2 is
  * a useful kernel example", extends to.)
