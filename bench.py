@@ -369,6 +369,17 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
+    # per-launch device times (a separate, untimed pass with events between
+    # the launches; run first, its steps also settle the device: in a fresh
+    # process the first tens of steps run slower)
+    ssd.launch_timing(True)
+    per_launch = []
+    for _ in range(max(10, args.steps // 2)):
+        flush.zero_()
+        step()
+        per_launch.append(ssd.launch_times_ms())
+    ssd.launch_timing(False)
+    torch.cuda.synchronize(dev)
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -386,16 +397,6 @@ def main():
         wall = time.perf_counter() - wall0
     step_ms = [s.elapsed_time(e) for s, e in evs]
     ms = max_over_ranks(statistics.mean(step_ms), world, dev)
-    launches_per_step = None
-
-    # per-launch device times (separate pass, events between the launches)
-    ssd.launch_timing(True)
-    per_launch = []
-    for _ in range(max(5, args.steps // 2)):
-        flush.zero_()
-        step()
-        per_launch.append(ssd.launch_times_ms())
-    ssd.launch_timing(False)
     launches_per_step = len(per_launch[-1])
     kernel_names = [name for name, _ in per_launch[-1]]
     launch_ms = [statistics.mean(p[i][1] for p in per_launch) for i in range(launches_per_step)]
